@@ -1,0 +1,195 @@
+/*
+ * kda.h -- C ABI of the KDA (gated delta rule) hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The recurrence, per head, with a fixed-size state S in R^{dk x dv}
+ * ("Noyaux KDA et FlashKDA", section "Le conflit fondamental"):
+ *     S_t = (I - b_t k_t k_t^T) Diag(exp g_t) S_{t-1} + b_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,
+ * where g_t in R^{dk} is a per-channel log-decay acting on the key axis and
+ * floored at g_min = -5 per token and channel ("Noyaux KDA et FlashKDA",
+ * section "Le role de la decroissance bornee").
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller allocates and owns all memory.  Pointers named
+ *    "device" must be device memory of the current CUDA device; the library
+ *    never allocates device memory, except inside caller-provided workspace.
+ *  - Layouts: contiguous, row-major, token-major ("THD"):
+ *        q, k, g [T][H][dk], v, o [T][H][dv], beta [T][H];
+ *    states head-contiguous [.., H, dk, dv] with dv fastest ("Inference :
+ *    cache KV, decodage, quantification": each head's state is one
+ *    self-contained byte stream).
+ *  - Alignment: every tensor pointer must be 16-byte aligned.
+ *  - Streams: every call takes a cudaStream_t passed as void* (NULL = the
+ *    legacy default stream), enqueues its kernels there and returns without
+ *    synchronising.
+ *  - Errors: every call returns an int status.  Host-side validation runs
+ *    before any launch: on failure nothing is enqueued.  KDA_ERR_CUDA means a
+ *    launch failed (cudaGetLastError).  Conditions only visible on the device
+ *    (bad cu_seqlens, out-of-range accepted lengths) set bits in the optional
+ *    device status word `status` (a uint32 the caller zeroes and reads back
+ *    when convenient); the affected work unit is skipped.  No kernel traps.
+ *  - Supported shapes: dk, dv in {64, 128}; H >= 1.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARG (-1)
+#define KDA_ERR_UNSUPPORTED_SHAPE (-2)
+#define KDA_ERR_ALIGNMENT (-3)
+#define KDA_ERR_WORKSPACE (-4)
+#define KDA_ERR_CUDA (-5)
+
+#define KDA_DTYPE_BF16 0
+#define KDA_DTYPE_F32 1
+
+#define KDA_CONV_NONE 0
+#define KDA_CONV_SILU 1
+
+#define KDA_CP_OFF 0
+#define KDA_CP_ON 1
+#define KDA_CP_AUTO (-1)
+
+/* Bits of the device status word. */
+#define KDA_STATUS_BAD_SEQLENS 0x1u      /* cu_seqlens not monotone / out of [0, T] */
+#define KDA_STATUS_BAD_ACCEPTED_LEN 0x2u /* accepted_len[r] outside [0, Wd]        */
+#define KDA_STATUS_SEGMENT_OVERFLOW 0x4u /* segment table larger than planned      */
+
+/* Human-readable name of a return status. Never NULL. */
+const char *kda_status_string(int status);
+
+/* ABI version (major*100 + minor). */
+int kda_version(void);
+
+/*
+ * Chunkwise prefill / training forward ("Noyaux KDA et FlashKDA", section
+ * "FlashKDA : le noyau par blocs": parallel inside a 64-token chunk, serial
+ * between chunks; the floor makes every causal tile a dense product, section
+ * "Le role de la decroissance bornee").
+ *
+ *  q, k, v      device, [T][H][dk] / [T][H][dv], dtype in_dtype (bf16 | f32).
+ *  g            device, f32 [T][H][dk], raw log-decay; floored at g_min on load.
+ *  beta         device, f32 [T][H].
+ *  cu_seqlens   device, int32 [N+1], N sequences packed along T
+ *               (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T).
+ *               Chunks restart at every sequence start.
+ *  initial_state device f32 [N][H][dk][dv] or NULL (zero state).
+ *  final_state  device f32 [N][H][dk][dv] or NULL (not written).
+ *  o            device, [T][H][dv], dtype in_dtype.
+ *  scale        multiplies o (1.0 for the plain rule).
+ *  g_min        decay floor (-5).
+ *  cp_mode      KDA_CP_OFF: one pass per (sequence, head).
+ *               KDA_CP_ON: intra-device context parallelism ("Noyaux KDA et
+ *               FlashKDA", section "Le parallelisme de contexte
+ *               intra-appareil"): segments of segment_len tokens are turned
+ *               into independent affine transitions (M, N), composed in order
+ *               per (sequence, head), then replayed in parallel from their
+ *               exact initial states (4 launches).
+ *               KDA_CP_AUTO: CP when (sequence, head) units are too few to
+ *               fill the GPU and sequences are long.
+ *  segment_len  CP segment length in tokens (multiple of 64), or 0 = automatic.
+ *  workspace    device scratch of at least kda_chunk_fwd_workspace_size(...)
+ *               bytes (may be NULL when that size is 0).  Contents on entry
+ *               are ignored; on exit they are unspecified.
+ *  status       device uint32 status word or NULL.
+ */
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                  const float *beta, const int32_t *cu_seqlens, int N, int T, int H, int dk,
+                  int dv, const float *initial_state, float *final_state, void *o, float scale,
+                  float g_min, int in_dtype, int cp_mode, int segment_len, void *workspace,
+                  size_t workspace_bytes, uint32_t *status, void *stream);
+
+/* Workspace bytes kda_chunk_fwd needs for these arguments (0 when cp_mode
+ * resolves to OFF).  Pure host arithmetic. */
+size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,
+                                    int segment_len);
+
+/* The segment length (tokens) and CP decision kda_chunk_fwd would use:
+ * returns 0 when CP is off, else the segment length. Pure host arithmetic. */
+int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len);
+
+/*
+ * Segment transitions of one sequence ("Noyaux KDA et FlashKDA", section "Le
+ * parallelisme de contexte intra-appareil": the transition of each segment is
+ * evaluated independently of the incoming state).  Exported for tests and
+ * debugging; kda_chunk_fwd's CP path runs the same kernel.
+ * Tokens [0, T) of one sequence are cut into P = ceil(T / segment_len)
+ * segments; per segment p and head h:
+ *     M[p][h] = A_last ... A_first   (A_t = (I - b_t k_t k_t^T) Diag(exp g_t)),
+ *     Nmat[p][h] = state reached from S = 0 over the segment.
+ *  k, v, g, beta  device, as in kda_chunk_fwd (single sequence, length T).
+ *  M              device f32 [P][H][dk][dk];  Nmat device f32 [P][H][dk][dv].
+ */
+int kda_segment_transition(const void *k, const void *v, const float *g, const float *beta,
+                           int T, int H, int dk, int dv, int segment_len, float *M, float *Nmat,
+                           float g_min, int in_dtype, void *stream);
+
+/*
+ * Exact ordered composition of segment transitions, per head ("Dentro de los
+ * esfuerzos de optimizacion de Kimi K3", section 5: group summaries are
+ * scanned in order to give every group its exact initial state):
+ *     S_in[p] = S_{p-1},   S_p = M[p] S_{p-1} + Nmat[p],   S_{-1} = S0 (or 0).
+ *  M      device f32 [P][H][dk][dk];  Nmat device f32 [P][H][dk][dv].
+ *  S0     device f32 [H][dk][dv] or NULL.
+ *  S_in   device f32 [P][H][dk][dv] or NULL (initial state of each segment).
+ *  S_final device f32 [H][dk][dv] or NULL.
+ * Arithmetic is fp32 with fp32 accumulation.
+ */
+int kda_segment_compose(const float *M, const float *Nmat, const float *S0, float *S_in,
+                        float *S_final, int P, int H, int dk, int dv, void *stream);
+
+/*
+ * Fused speculative-decode verify with replay from projected inputs, one KDA
+ * layer, R requests ("Noyaux d'inference", section 1 "Le decodage KDA",
+ * subsections "La solution : rejouer plutot que sauvegarder" and "La fusion").
+ * Per request r the token sequence is: cached rows 0..a-1 (accepted drafts of
+ * the previous window, replayed), new row 0 (bonus token), new rows 1..Wd
+ * (next draft window), a = accepted_len[r].  For each token, in one kernel:
+ * depthwise causal short conv of width W over the pre-conv q|k|v channels
+ * (the W-1 previous rows come from conv_tail, then from earlier tokens),
+ * optional SiLU, L2 norm of q and k over dk (eps_in), gates
+ * g = max(-softplus(g_raw), g_min), b = sigmoid(b_raw), the recurrence, and
+ * for the bonus and draft tokens the per-head RMSNorm of o over dv (eps_out)
+ * times out_norm_w.  The state reached after the bonus token is written back
+ * to `state` (bf16, round to nearest even) and conv_tail receives the W-1
+ * most recent pre-conv rows up to and including the bonus row (bitwise
+ * copies).  Draft tokens never touch HBM state.
+ *
+ *  state        device bf16 [R][H][dk][dv], in/out.
+ *  conv_tail    device bf16 [R][W-1][Cq], in/out, Cq = H*(2*dk+dv), rows oldest
+ *               first; channel order q (H*dk) | k (H*dk) | v (H*dv), head-major.
+ *  conv_w       device f32 [Cq][W]; y_t = sum_j conv_w[c][j] x_{t-(W-1)+j}[c].
+ *  cached_qkv   device bf16 [R][Wd][Cq];  cached_g bf16 [R][Wd][H*dk];
+ *  cached_beta  bf16 [R][Wd][H]  -- the previous window's draft rows.
+ *  accepted_len device int32 [R], valid range [0, Wd]; a request outside it
+ *               is skipped (state, tail and o untouched) and
+ *               KDA_STATUS_BAD_ACCEPTED_LEN is set.
+ *  new_qkv      device bf16 [R][Wd+1][Cq];  new_g bf16 [R][Wd+1][H*dk];
+ *  new_beta     bf16 [R][Wd+1][H]  -- row 0 bonus, rows 1..Wd drafts.
+ *  out_norm_w   device f32 [dv].
+ *  o            device bf16 [R][Wd+1][H][dv]: rows for bonus + drafts.
+ *  Limits: W in [1, 4] and Wd in [0, 7], so that the a + 1 + Wd <= 2*Wd + 1
+ *  tokens of a request fit one 16-token tile on chip.
+ * The caller swaps the cached and new buffers between steps (new rows 1..Wd
+ * become the next cached rows); the kernel copies no projection.
+ */
+int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w,
+                             const void *cached_qkv, const void *cached_g,
+                             const void *cached_beta, const int32_t *accepted_len,
+                             const void *new_qkv, const void *new_g, const void *new_beta,
+                             const float *out_norm_w, void *o, int R, int H, int dk, int dv,
+                             int W, int Wd, float scale, float g_min, float eps_in,
+                             float eps_out, int conv_act, uint32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,1 +1,180 @@
-"""KDA (gated delta rule) hot path for GB300 -- Python binding placeholder."""
+"""KDA (Kimi Delta Attention) recurrence hot path for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/kda.h`` (``libkda.so``, built
+in-tree by ``kda_gated_delta_02_gb300.build``).  Every function marshals
+torch tensors into pointers and sizes, passes the current CUDA stream and
+checks the returned status; all arithmetic runs in the library's kernels.
+There is no CPU fallback: without the compiled library or a CUDA device the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_plan", "segment_transition",
+           "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
+           "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
+           "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libkda.so")
+_lock = threading.Lock()
+_lib = None
+
+CP_OFF, CP_ON, CP_AUTO = 0, 1, -1
+CONV_NONE, CONV_SILU = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
+STATUS_BAD_SEQLENS, STATUS_BAD_ACCEPTED_LEN, STATUS_SEGMENT_OVERFLOW = 1, 2, 4
+
+
+class KDAError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise KDAError(f"{_LIB_PATH} is missing: run `python -m kda_gated_delta_02_gb300.build` "
+                           "(the KDA path has no CPU fallback)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_version.restype = I
+        lib.kda_chunk_fwd.restype = I
+        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, I, I, P, S, P, P]
+        lib.kda_chunk_fwd_workspace_size.restype = S
+        lib.kda_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_chunk_fwd_plan.restype = I
+        lib.kda_chunk_fwd_plan.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_segment_transition.restype = I
+        lib.kda_segment_transition.argtypes = [P, P, P, P, I, I, I, I, I, P, P, F, I, P]
+        lib.kda_segment_compose.restype = I
+        lib.kda_segment_compose.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.kda_decode_verify_replay.restype = I
+        lib.kda_decode_verify_replay.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                                 F, F, F, F, I, P, P]
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = load_library().kda_status_string(rc).decode()
+        raise KDAError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise KDAError("KDA calls take CUDA tensors")
+    if not t.is_contiguous():
+        raise KDAError("KDA calls take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _in_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise KDAError(f"unsupported input dtype {t.dtype}")
+
+
+def chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
+    return int(load_library().kda_chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len))
+
+
+def chunk_fwd_plan(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
+    return int(load_library().kda_chunk_fwd_plan(N, T, H, dk, dv, cp_mode, segment_len))
+
+
+def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,
+              g_min=-5.0, cp_mode=CP_AUTO, segment_len=0, out=None, final_state=None,
+              workspace=None, status=None, stream=None):
+    """Chunkwise KDA prefill.  q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H];
+    cu_seqlens int32 [N+1]; initial_state f32 [N,H,dk,dv] or None.
+    Returns (o [T,H,dv] in q's dtype, final_state f32 [N,H,dk,dv] or None)."""
+    lib = load_library()
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                           _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
+                           _in_dtype(q), int(cp_mode), int(segment_len),
+                           _ptr(workspace) if ws_bytes else None,
+                           ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0),
+                           _ptr(status), _stream(stream))
+    _check(rc, "kda_chunk_fwd")
+    return out, final_state
+
+
+def segment_transition(k, v, g, beta, segment_len, g_min=-5.0, stream=None):
+    """Transitions (M [P,H,dk,dk], N [P,H,dk,dv]) of fixed-length segments of one sequence."""
+    lib = load_library()
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    P = (T + segment_len - 1) // segment_len
+    M = torch.empty((P, H, dk, dk), dtype=torch.float32, device=k.device)
+    Nm = torch.empty((P, H, dk, dv), dtype=torch.float32, device=k.device)
+    rc = lib.kda_segment_transition(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), T, H, dk, dv, int(segment_len),
+                                    _ptr(M), _ptr(Nm), float(g_min), _in_dtype(k), _stream(stream))
+    _check(rc, "kda_segment_transition")
+    return M, Nm
+
+
+def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
+    """Ordered composition: returns (S_in [P,H,dk,dv] or None, S_final [H,dk,dv])."""
+    lib = load_library()
+    P, H, dk, dv = Nm.shape
+    S_in = torch.empty_like(Nm) if want_segment_states else None
+    Sf = torch.empty((H, dk, dv), dtype=torch.float32, device=Nm.device)
+    rc = lib.kda_segment_compose(_ptr(M), _ptr(Nm), _ptr(S0), _ptr(S_in), _ptr(Sf), P, H, dk, dv,
+                                 _stream(stream))
+    _check(rc, "kda_segment_compose")
+    return S_in, Sf
+
+
+def decode_verify_replay(state, conv_tail, conv_w, cached_qkv, cached_g, cached_beta, accepted_len,
+                         new_qkv, new_g, new_beta, out_norm_w, scale=1.0, g_min=-5.0, eps_in=1e-6,
+                         eps_out=1e-6, conv_act=CONV_SILU, out=None, status=None, stream=None):
+    """Fused verify with replay.  Updates state and conv_tail in place; returns
+    o [R, Wd+1, H, dv] (bf16): rows for the bonus token and the next drafts."""
+    lib = load_library()
+    R, H, dk, dv = state.shape
+    W = conv_w.shape[1]
+    Wd = new_qkv.shape[1] - 1
+    if out is None:
+        out = torch.empty((R, Wd + 1, H, dv), dtype=torch.bfloat16, device=state.device)
+    rc = lib.kda_decode_verify_replay(_ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv),
+                                      _ptr(cached_g), _ptr(cached_beta), _ptr(accepted_len), _ptr(new_qkv),
+                                      _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w), _ptr(out), R, H, dk, dv,
+                                      W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
+                                      int(conv_act), _ptr(status), _stream(stream))
+    _check(rc, "kda_decode_verify_replay")
+    return out

@@ -1,0 +1,247 @@
+// api.cu -- the C ABI declared in include/kda.h: argument validation, the
+// context-parallel plan, workspace carving and kernel launches.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+constexpr int kChunk = 64;
+
+inline bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool dim_ok(int d) { return d == 64 || d == 128; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int sm_count() {
+    static int cached = 0;
+    if (cached > 0) return cached;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+        cached = n;
+    } else {
+        cudaGetLastError();
+        n = 152;  // GB300
+    }
+    return n;
+}
+
+// value-tile width of the prefill kernel
+int prefill_dvt(int dk, int dv, bool transition) {
+    const char *env = getenv("KDA_PREFILL_DVT");
+    int want = env ? atoi(env) : 128;
+    if (want != 64 && want != 128) want = 128;
+    int dvt = (dv % want == 0) ? want : 64;
+    if (transition && (dk % dvt != 0)) dvt = 64;
+    return dvt;
+}
+
+struct CpLayout {
+    int seg_len = 0;
+    int P_max = 0;
+    size_t off_count = 0, off_table = 0, off_first = 0, off_M = 0, off_N = 0, off_Sin = 0, total = 0;
+};
+
+CpLayout cp_layout(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
+    CpLayout L;
+    if (cp_mode == KDA_CP_OFF || N <= 0 || H <= 0) return L;
+    if (cp_mode == KDA_CP_AUTO) {
+        const int sms = sm_count();
+        const long units = (long)N * H;
+        const long avg = T / (N > 0 ? N : 1);
+        if (!(units * 2 <= sms && avg >= 16 * kChunk)) return L;
+    }
+    int seg = segment_len;
+    if (seg <= 0) {
+        const int sms = sm_count();
+        long target = (2L * sms + (long)N * H - 1) / ((long)N * H);  // segments per sequence
+        if (target < 1) target = 1;
+        long per = (T / (N > 0 ? N : 1) + target - 1) / target;
+        seg = (int)(((per + kChunk - 1) / kChunk) * kChunk);
+        if (seg < 16 * kChunk) seg = 16 * kChunk;
+    }
+    L.seg_len = seg;
+    L.P_max = T / seg + N;
+    size_t o = 0;
+    L.off_count = o;
+    o = align256(o + 16);
+    L.off_table = o;
+    o = align256(o + (size_t)L.P_max * 16);
+    L.off_first = o;
+    o = align256(o + (size_t)(N + 1) * 4);
+    L.off_M = o;
+    o = align256(o + (size_t)L.P_max * H * dk * dk * 4);
+    L.off_N = o;
+    o = align256(o + (size_t)L.P_max * H * dk * dv * 4);
+    L.off_Sin = o;
+    o = align256(o + (size_t)L.P_max * H * dk * dv * 4);
+    L.total = o;
+    return L;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA launch error";
+        default: return "unknown status";
+    }
+}
+
+int kda_version(void) { return 100; }
+
+size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
+    return cp_layout(N, T, H, dk, dv, cp_mode, segment_len).total;
+}
+
+int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
+    return cp_layout(N, T, H, dk, dv, cp_mode, segment_len).seg_len;
+}
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                  const float *initial_state, float *final_state, void *o, float scale, float g_min,
+                  int in_dtype, int cp_mode, int segment_len, void *workspace, size_t workspace_bytes,
+                  uint32_t *status, void *stream) {
+    if (N < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (cp_mode < -1 || cp_mode > 1) return KDA_ERR_INVALID_ARG;
+    if (segment_len < 0 || (segment_len % kChunk) != 0) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) || !aligned16(workspace))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)T * H * (dk > dv ? dk : dv) >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf = in_dtype == KDA_DTYPE_BF16;
+
+    kda::ChunkArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = o;
+    a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.scale = scale; a.g_min = g_min;
+    a.status = status;
+
+    CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
+    if (L.seg_len == 0) {
+        a.mode = kda::MODE_SEQ;
+        a.cu_seqlens = cu_seqlens;
+        a.S_init = initial_state;
+        a.S_final = final_state;
+        return cuda_status(kda::launch_chunk(a, N, prefill_dvt(dk, dv, false), bf, st));
+    }
+    if (!workspace || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *count = reinterpret_cast<int32_t *>(ws + L.off_count);
+    int32_t *table = reinterpret_cast<int32_t *>(ws + L.off_table);
+    int32_t *first = reinterpret_cast<int32_t *>(ws + L.off_first);
+    float *M = reinterpret_cast<float *>(ws + L.off_M);
+    float *Nm = reinterpret_cast<float *>(ws + L.off_N);
+    float *Sin = reinterpret_cast<float *>(ws + L.off_Sin);
+
+    cudaError_t e = kda::launch_segment_table(cu_seqlens, N, T, L.seg_len, L.P_max, table, first, count,
+                                              status, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    // pass 1: transitions of every segment, independent of the incoming state
+    a.mode = kda::MODE_TRANSITION;
+    a.seg_table = table;
+    a.seg_count = count;
+    a.M_out = M;
+    a.N_out = Nm;
+    e = kda::launch_chunk(a, L.P_max, prefill_dvt(dk, dv, true), bf, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    // pass 2: ordered scan per (sequence, head)
+    kda::ComposeArgs c = {};
+    c.M = M; c.Nm = Nm; c.S0 = initial_state; c.S_in = Sin; c.S_final = nullptr;
+    c.first = first; c.P = 0; c.chains = N; c.H = H; c.dk = dk; c.dv = dv;
+    e = kda::launch_compose(c, st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    // pass 3: replay every segment from its exact initial state
+    a.mode = kda::MODE_REPLAY;
+    a.S_in = Sin;
+    a.S_final = final_state;
+    a.M_out = a.N_out = nullptr;
+    return cuda_status(kda::launch_chunk(a, L.P_max, prefill_dvt(dk, dv, false), bf, st));
+}
+
+int kda_segment_transition(const void *k, const void *v, const float *g, const float *beta, int T, int H,
+                           int dk, int dv, int segment_len, float *M, float *Nmat, float g_min,
+                           int in_dtype, void *stream) {
+    if (T < 0 || H < 1 || segment_len <= 0 || (segment_len % kChunk) != 0) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!k || !v || !g || !beta || !M || !Nmat)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(M) ||
+        !aligned16(Nmat))
+        return KDA_ERR_ALIGNMENT;
+    if (T == 0) return KDA_OK;
+    kda::ChunkArgs a = {};
+    a.q = nullptr; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = nullptr;
+    a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.scale = 1.f; a.g_min = g_min;
+    a.mode = kda::MODE_TRANSITION;
+    a.seg_table = nullptr;
+    a.seg_len = segment_len;
+    a.M_out = M;
+    a.N_out = Nmat;
+    const int P = (T + segment_len - 1) / segment_len;
+    return cuda_status(kda::launch_chunk(a, P, prefill_dvt(dk, dv, true), in_dtype == KDA_DTYPE_BF16,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int kda_segment_compose(const float *M, const float *Nmat, const float *S0, float *S_in, float *S_final,
+                        int P, int H, int dk, int dv, void *stream) {
+    if (P < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (P > 0 && (!M || !Nmat)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(M) || !aligned16(Nmat) || !aligned16(S0) || !aligned16(S_in) || !aligned16(S_final))
+        return KDA_ERR_ALIGNMENT;
+    kda::ComposeArgs c = {};
+    c.M = M; c.Nm = Nmat; c.S0 = S0; c.S_in = S_in; c.S_final = S_final;
+    c.first = nullptr; c.P = P; c.chains = 1; c.H = H; c.dk = dk; c.dv = dv;
+    return cuda_status(kda::launch_compose(c, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w, const void *cached_qkv,
+                             const void *cached_g, const void *cached_beta, const int32_t *accepted_len,
+                             const void *new_qkv, const void *new_g, const void *new_beta,
+                             const float *out_norm_w, void *o, int R, int H, int dk, int dv, int W, int Wd,
+                             float scale, float g_min, float eps_in, float eps_out, int conv_act,
+                             uint32_t *status, void *stream) {
+    if (R < 0 || H < 1 || W < 1 || W > 4 || Wd < 0 || Wd > 7) return KDA_ERR_INVALID_ARG;
+    if (conv_act != KDA_CONV_NONE && conv_act != KDA_CONV_SILU) return KDA_ERR_INVALID_ARG;
+    if (!(dk == dv && dim_ok(dk))) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (R > 0 && (!state || !conv_w || !accepted_len || !new_qkv || !new_g || !new_beta || !out_norm_w ||
+                  !o || (W > 1 && !conv_tail) || (Wd > 0 && (!cached_qkv || !cached_g || !cached_beta))))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state) || !aligned16(conv_tail) || !aligned16(conv_w) || !aligned16(cached_qkv) ||
+        !aligned16(cached_g) || !aligned16(new_qkv) || !aligned16(new_g) || !aligned16(o) ||
+        !aligned16(out_norm_w))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)R * H >= ((size_t)1 << 31)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    kda::VerifyArgs a = {};
+    a.state = state; a.tail = conv_tail; a.conv_w = conv_w;
+    a.cached_qkv = cached_qkv; a.cached_g = cached_g; a.cached_b = cached_beta;
+    a.accepted = accepted_len;
+    a.new_qkv = new_qkv; a.new_g = new_g; a.new_b = new_beta;
+    a.out_w = out_norm_w; a.o = o;
+    a.R = R; a.H = H; a.dk = dk; a.dv = dv; a.W = W; a.Wd = Wd;
+    a.scale = scale; a.g_min = g_min; a.eps_in = eps_in; a.eps_out = eps_out; a.conv_act = conv_act;
+    a.status = status;
+    return cuda_status(kda::launch_verify(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// kda_internal.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+enum ChunkMode : int {
+    MODE_SEQ = 0,         // one unit per (sequence, head, dv tile)
+    MODE_TRANSITION = 1,  // one unit per (segment, head, tile of [M | N])
+    MODE_REPLAY = 2,      // one unit per (segment, head, dv tile), seeded from S_in
+};
+
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    void *o;                    // [T][H][dv] (SEQ / REPLAY)
+    int T, H, dk, dv;
+    float scale, g_min;
+    int mode;
+    const int32_t *cu_seqlens;  // SEQ: [N+1]
+    const int32_t *seg_table;   // TRANSITION / REPLAY: [P_max][4]
+    const int32_t *seg_count;   // device scalar
+    int seg_len;                // fixed segment length when seg_table is null
+    const float *S_init;        // SEQ: initial_state [N][H][dk][dv] or null
+    const float *S_in;          // REPLAY: [P][H][dk][dv]
+    float *S_final;             // SEQ / REPLAY: final_state [N][H][dk][dv] or null
+    float *M_out, *N_out;       // TRANSITION: [P][H][dk][dk], [P][H][dk][dv]
+    uint32_t *status;
+};
+
+cudaError_t launch_chunk(const ChunkArgs &a, int units, int dvt, bool in_bf16, cudaStream_t st);
+
+cudaError_t launch_segment_table(const int32_t *cu_seqlens, int N, int T, int seg_len, int P_max,
+                                 int32_t *table, int32_t *seq_first, int32_t *seg_count,
+                                 uint32_t *status, cudaStream_t st);
+
+// Ordered composition over chains.  Chain c covers segments
+// [first[c], first[c+1]) when `first` is given, else [c*P, (c+1)*P); per head.
+struct ComposeArgs {
+    const float *M, *Nm;
+    const float *S0;      // [chains][H][dk][dv] or null
+    float *S_in;          // [P_total][H][dk][dv] or null
+    float *S_final;       // [chains][H][dk][dv] or null
+    const int32_t *first; // [chains+1] device or null
+    int P;                // segments per chain when first == null
+    int chains, H, dk, dv;
+};
+cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t st);
+
+struct VerifyArgs {
+    void *state, *tail;
+    const float *conv_w;
+    const void *cached_qkv, *cached_g, *cached_b;
+    const int32_t *accepted;
+    const void *new_qkv, *new_g, *new_b;
+    const float *out_w;
+    void *o;
+    int R, H, dk, dv, W, Wd;
+    float scale, g_min, eps_in, eps_out;
+    int conv_act;
+    uint32_t *status;
+};
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t st);
+
+}  // namespace kda

@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads and exports every entry point of include/kda.h.
+
+No compute call is made here (no GPU needed): only symbol lookups and the pure
+host arithmetic entry points.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kda_gated_delta_02_gb300 import build
+    build.build()
+    return ctypes.CDLL(build.LIB)
+
+
+def test_header_declares_the_three_calls():
+    fns = header_functions()
+    for name in ("kda_chunk_fwd", "kda_segment_compose", "kda_decode_verify_replay"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} declared in include/kda.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    lib.kda_status_string.restype = ctypes.c_char_p
+    assert lib.kda_status_string(0) == b"ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert lib.kda_status_string(code) not in (b"ok", b"unknown status")
+    assert lib.kda_status_string(12345) == b"unknown status"
+    assert lib.kda_version() >= 100
+
+
+def test_cp_plan_and_workspace_arithmetic(lib):
+    lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    # CP off: no workspace
+    assert lib.kda_chunk_fwd_workspace_size(1, 32768, 96, 128, 128, 0, 0) == 0
+    assert lib.kda_chunk_fwd_plan(1, 32768, 96, 128, 128, 0, 0) == 0
+    # many heads: auto keeps one pass per (sequence, head)
+    assert lib.kda_chunk_fwd_plan(1, 32768, 96, 128, 128, -1, 0) == 0
+    # few heads, long sequence: auto turns CP on with a 64-multiple segment
+    seg = lib.kda_chunk_fwd_plan(1, 1 << 20, 12, 128, 128, -1, 0)
+    assert seg > 0 and seg % 64 == 0
+    # explicit segment length: M, N and S_in for T/seg + N segments at least
+    ws = lib.kda_chunk_fwd_workspace_size(1, 1 << 20, 12, 128, 128, 1, 32768)
+    P = (1 << 20) // 32768 + 1
+    assert ws >= 3 * P * 12 * 128 * 128 * 4
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    f = lib.kda_chunk_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, P] + [ctypes.c_int] * 5 + [P, P, P, ctypes.c_float, ctypes.c_float] + \
+        [ctypes.c_int] * 3 + [P, ctypes.c_size_t, P, P]
+    buf = ctypes.create_string_buffer(64)
+    aligned = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    misaligned = ctypes.c_void_p(aligned.value + 4)
+    # unsupported head size
+    assert f(aligned, aligned, aligned, aligned, aligned, aligned, 1, 64, 2, 96, 128, None, None, aligned,
+             1.0, -5.0, 0, 0, 0, None, 0, None, None) == -2
+    # no cu_seqlens
+    assert f(aligned, aligned, aligned, aligned, aligned, None, 1, 64, 2, 128, 128, None, None, aligned,
+             1.0, -5.0, 0, 0, 0, None, 0, None, None) == -1
+    # misaligned q
+    assert f(misaligned, aligned, aligned, aligned, aligned, aligned, 1, 64, 2, 128, 128, None, None, aligned,
+             1.0, -5.0, 0, 0, 0, None, 0, None, None) == -3
+    # CP on without workspace
+    assert f(aligned, aligned, aligned, aligned, aligned, aligned, 1, 1 << 16, 2, 128, 128, None, None, aligned,
+             1.0, -5.0, 0, 1, 4096, None, 0, None, None) == -4
+    # segment length not a multiple of 64
+    assert f(aligned, aligned, aligned, aligned, aligned, aligned, 1, 1 << 16, 2, 128, 128, None, None, aligned,
+             1.0, -5.0, 0, 1, 100, None, 0, None, None) == -1
+    v = lib.kda_decode_verify_replay
+    v.restype = ctypes.c_int
+    v.argtypes = [P] * 12 + [ctypes.c_int] * 6 + [ctypes.c_float] * 4 + [ctypes.c_int, P, P]
+    args = [aligned] * 12
+    # draft window above 7 does not fit the 16-token tile
+    assert v(*args, 4, 2, 128, 128, 4, 8, 1.0, -5.0, 1e-6, 1e-6, 1, None, None) == -1
+    # dk != dv is not supported by the verify kernel
+    assert v(*args, 4, 2, 128, 64, 4, 7, 1.0, -5.0, 1e-6, 1e-6, 1, None, None) == -2
+    # conv width above 4
+    assert v(*args, 4, 2, 128, 128, 5, 7, 1.0, -5.0, 1e-6, 1e-6, 1, None, None) == -1
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    import kda_gated_delta_02_gb300 as kda
+    x = torch.zeros(64, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(kda.KDAError):
+        kda.chunk_fwd(x, x, x, x.float(), torch.zeros(64, 2), torch.tensor([0, 64], dtype=torch.int32))

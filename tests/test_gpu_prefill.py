@@ -1,0 +1,229 @@
+"""GPU parity of kda_chunk_fwd / kda_segment_transition / kda_segment_compose
+against the fp64 oracle, on the same seeded inputs, through the C ABI.
+
+Bars: outputs 2e-2 and final states 1e-2 normwise relative error per head
+(max|gpu - oracle| / max|oracle|); device status word and untouched buffers
+are compared exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import OUT_TOL, STATE_TOL, normwise_err, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from kda_gated_delta_02_gb300 import build
+    build.build()
+    import kda_gated_delta_02_gb300 as k
+    k.load_library()
+    return k
+
+
+def make_inputs(T_list, H, dk, dv, dtype=torch.bfloat16, seed=0, s0=False, g_fill=None, device="cuda"):
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    T = int(sum(T_list))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(T_list)]), dtype=torch.int32)
+    q = torch.randn(T, H, dk, generator=gen)
+    k = torch.randn(T, H, dk, generator=gen)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(T, H, dv, generator=gen)
+    g = torch.clamp_min(-torch.nn.functional.softplus(torch.randn(T, H, dk, generator=gen)), -5.0)
+    if g_fill is not None:
+        g = g_fill(g)
+    beta = torch.sigmoid(torch.randn(T, H, generator=gen))
+    S0 = 0.02 * torch.randn(len(T_list), H, dk, dv, generator=gen) if s0 else None
+    to = lambda x: None if x is None else x.to(device)
+    return dict(q=to(q.to(dtype)), k=to(k.to(dtype)), v=to(v.to(dtype)), g=to(g.float()), beta=to(beta),
+                cu_seqlens=to(cu), S0=to(S0))
+
+
+def run_and_compare(kda, oracle, inp, scale=1.0, cp_mode=0, segment_len=0, head_mask=None,
+                    out_tol=OUT_TOL, state_tol=STATE_TOL):
+    o, Sf = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
+                          initial_state=inp["S0"], scale=scale, cp_mode=cp_mode, segment_len=segment_len)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.prefill(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["g"]),
+                                  to64(inp["beta"]), inp["cu_seqlens"].cpu().numpy(),
+                                  S0=None if inp["S0"] is None else to64(inp["S0"]), scale=scale,
+                                  head_mask=head_mask)
+    heads = np.arange(o.shape[1]) if head_mask is None else np.nonzero(np.asarray(head_mask))[0]
+    e_o = normwise_err(to64(o)[:, heads], o_ref[:, heads], head_axis=1)
+    e_s = normwise_err(to64(Sf)[:, heads], S_ref[:, heads], head_axis=1)
+    assert e_o <= out_tol, f"output error {e_o:.3e}"
+    assert e_s <= state_tol, f"final-state error {e_s:.3e}"
+    return o, Sf, e_o, e_s
+
+
+def test_tiny_fp32_config(kda, oracle):
+    """1 sequence, T=256, H=4, dk=dv=64, fp32 in/out, zero initial state, seed 0."""
+    from kda_gated_delta_02_gb300 import synth
+    inp = synth.make_prefill(synth.TINY, device="cuda")
+    assert inp["q"].dtype == torch.float32 and inp["S0"] is None
+    run_and_compare(kda, oracle, inp)
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 64), (64, 128)])
+def test_ragged_single_sequence_with_state(kda, oracle, dk, dv):
+    inp = make_inputs([3 * 64 + 17], 3, dk, dv, s0=True, seed=dk + dv)
+    run_and_compare(kda, oracle, inp, scale=0.5)
+
+
+def test_varlen_edge_lengths(kda, oracle):
+    """Empty, length-1, exact-chunk and ragged sequences packed together."""
+    inp = make_inputs([1, 63, 64, 65, 0, 200, 130], 2, 128, 128, s0=True, seed=7)
+    o, Sf, _, _ = run_and_compare(kda, oracle, inp)
+    # the empty sequence returns its initial state unchanged (bitwise)
+    assert torch.equal(Sf[4], inp["S0"][4])
+
+
+def test_fp32_inputs_dk128(kda, oracle):
+    inp = make_inputs([150], 2, 128, 128, dtype=torch.float32, s0=True, seed=9)
+    run_and_compare(kda, oracle, inp)
+
+
+def test_floor_stress(kda, oracle):
+    """g = -5 on whole chunks (the tightest factor range) and values far below
+    the floor, which the kernel must clamp."""
+    def fill(g):
+        g = g.clone()
+        g[:128] = -5.0
+        g[128:160, :, ::3] = -40.0
+        return g
+    inp = make_inputs([300], 2, 128, 128, s0=True, seed=11, g_fill=fill)
+    run_and_compare(kda, oracle, inp)
+
+
+def test_no_decay_no_floor_activity(kda, oracle):
+    """g = 0 (no decay) keeps every factor at 1."""
+    inp = make_inputs([200], 2, 128, 128, s0=True, seed=12, g_fill=lambda g: torch.zeros_like(g))
+    run_and_compare(kda, oracle, inp)
+
+
+def test_dependency_inverse_example_through_kernel(kda, oracle):
+    """Three tokens whose intra-chunk corrections are those of the worked
+    example (A21 = A32 = 1/4, A31 = 1/8 with b = 1/2, g = 0): the chunk kernel
+    must reproduce the token-by-token result."""
+    dk = dv = 64
+    T, H = 3, 1
+    k = torch.zeros(T, H, dk)
+    # unit keys with k2.k1 = 1/2, k3.k2 = 1/2, k3.k1 = 1/4  -> b * dot = 1/4, 1/4, 1/8
+    k[0, 0, 0] = 1.0
+    k[1, 0, 0], k[1, 0, 1] = 0.5, (0.75) ** 0.5
+    c1 = 0.25
+    c2 = (0.5 - 0.5 * c1) / (0.75 ** 0.5)
+    k[2, 0, 0], k[2, 0, 1], k[2, 0, 2] = c1, c2, (1 - c1 ** 2 - c2 ** 2) ** 0.5
+    q = torch.randn(T, H, dk, generator=torch.Generator().manual_seed(3))
+    v = torch.randn(T, H, dv, generator=torch.Generator().manual_seed(4))
+    inp = dict(q=q.cuda(), k=k.cuda(), v=v.cuda(), g=torch.zeros(T, H, dk).cuda(),
+               beta=torch.full((T, H), 0.5).cuda(), cu_seqlens=torch.tensor([0, T], dtype=torch.int32).cuda(),
+               S0=None)
+    run_and_compare(kda, oracle, inp, out_tol=5e-3, state_tol=5e-3)
+
+
+def test_bad_cu_seqlens_sets_status(kda):
+    inp = make_inputs([64, 64], 1, 128, 128, seed=13)
+    cu = torch.tensor([0, 100, 64], dtype=torch.int32, device="cuda")  # not monotone
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((128, 1, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu, out=o, cp_mode=0, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kda.STATUS_BAD_SEQLENS
+    assert torch.all(o[100:] == 7.0)  # the rejected unit wrote nothing
+
+
+# ------------------------------------------------------------------ context parallelism
+def test_cp_single_sequence_matches_oracle(kda, oracle):
+    inp = make_inputs([5000], 2, 128, 128, s0=True, seed=20)
+    o_cp, S_cp, _, _ = run_and_compare(kda, oracle, inp, cp_mode=1, segment_len=1024)
+    o_seq, S_seq = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
+                                 initial_state=inp["S0"], cp_mode=0)
+    torch.cuda.synchronize()
+    assert normwise_err(to64(o_cp), to64(o_seq), 1) <= OUT_TOL
+
+
+def test_cp_varlen_with_empty_sequence(kda, oracle):
+    inp = make_inputs([3000, 0, 1500, 64], 2, 128, 128, s0=True, seed=21)
+    _, Sf, _, _ = run_and_compare(kda, oracle, inp, cp_mode=1, segment_len=1024)
+    assert torch.equal(Sf[1], inp["S0"][1])
+
+
+def test_cp_dk64(kda, oracle):
+    inp = make_inputs([2100], 2, 64, 64, s0=True, seed=22)
+    run_and_compare(kda, oracle, inp, cp_mode=1, segment_len=512)
+
+
+def test_segment_transition_matches_oracle(kda, oracle):
+    inp = make_inputs([2500], 2, 128, 128, seed=23)
+    L = 1024
+    M, N = kda.segment_transition(inp["k"], inp["v"], inp["g"], inp["beta"], L)
+    torch.cuda.synchronize()
+    for p in range(M.shape[0]):
+        a, b = p * L, min(2500, (p + 1) * L)
+        Mr, Nr = oracle.segment_transition(to64(inp["k"][a:b]), to64(inp["v"][a:b]), to64(inp["g"][a:b]),
+                                           to64(inp["beta"][a:b]))
+        assert normwise_err(to64(M[p]), Mr, 0) <= STATE_TOL
+        assert normwise_err(to64(N[p]), Nr, 0) <= STATE_TOL
+
+
+def test_segment_compose_matches_oracle(kda, oracle):
+    gen = torch.Generator().manual_seed(24)
+    P, H, dk, dv = 5, 3, 128, 128
+    M = 0.1 * torch.randn(P, H, dk, dk, generator=gen)
+    N = torch.randn(P, H, dk, dv, generator=gen)
+    S0 = torch.randn(H, dk, dv, generator=gen)
+    S_in, Sf = kda.segment_compose(M.cuda(), N.cuda(), S0.cuda())
+    torch.cuda.synchronize()
+    S_in_r, Sf_r = oracle.segment_compose(M.double().numpy(), N.double().numpy(), S0.double().numpy())
+    assert normwise_err(to64(S_in), S_in_r, 1) <= 1e-5
+    assert normwise_err(to64(Sf), Sf_r, 0) <= 1e-5
+
+
+def test_segment_compose_worked_example(kda):
+    """Per element, (S/2 + 2) then (S/2 + 1) composes to S/4 + 2, exactly."""
+    P, H, d = 2, 1, 64
+    M = torch.zeros(P, H, d, d)
+    M[:, 0] = 0.5 * torch.eye(d)
+    N = torch.stack([torch.full((H, d, d), 2.0), torch.full((H, d, d), 1.0)])
+    S0 = torch.randn(H, d, d, generator=torch.Generator().manual_seed(25))
+    S_in, Sf = kda.segment_compose(M.cuda(), N.cuda(), S0.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(Sf.cpu(), 0.25 * S0 + 2.0)
+    assert torch.equal(S_in[0].cpu(), S0) and torch.equal(S_in[1].cpu(), 0.5 * S0 + 2.0)
+
+
+# ------------------------------------------------------------------ full-size workloads
+def test_full_prefill_32k_h96(kda, oracle):
+    """B=1, T=32768, H=96, dk=dv=128, bf16 q/k/v, fp32 g/beta, fp32 final state."""
+    from kda_gated_delta_02_gb300 import synth
+    inp = synth.make_prefill(synth.PREFILL_32K, device="cuda")
+    run_and_compare(kda, oracle, inp, cp_mode=-1)
+
+
+def test_full_varlen_prefix_continuation(kda, oracle):
+    """16 packed sequences, lengths U[1K, 8K], stored fp32 initial states; every
+    8th head compared (the oracle's cost grows with heads, not with sampling)."""
+    from kda_gated_delta_02_gb300 import synth
+    inp = synth.make_prefill(synth.VARLEN, device="cuda")
+    mask = np.zeros(96, dtype=np.uint8)
+    mask[::8] = 1
+    run_and_compare(kda, oracle, inp, cp_mode=-1, head_mask=mask)
+
+
+def test_full_ultra_long_context_parallel(kda, oracle):
+    """T = 1,048,576, H = 12 with the automatic context-parallel schedule (the
+    benchmark's launch configuration); heads 0 and 7 compared at every token."""
+    from kda_gated_delta_02_gb300 import synth
+    w = synth.ULTRA_LONG
+    assert kda.chunk_fwd_plan(1, w.T, w.H, w.dk, w.dv, kda.CP_AUTO) > 0
+    inp = synth.make_prefill(w, device="cuda")
+    mask = np.zeros(w.H, dtype=np.uint8)
+    mask[[0, 7]] = 1
+    run_and_compare(kda, oracle, inp, cp_mode=-1, head_mask=mask)
