@@ -1,0 +1,400 @@
+"""Benchmark of the KDA hot path on GB300.
+
+One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
+32K-token, 96-head, d=128 bf16 workload, inputs resident in HBM, one
+kda_chunk_fwd launch per step.  Extra keys measured in the same run:
+  "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
+  "cp":     1M-token, 12-head prefill with the context-parallel schedule
+  "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches".
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+repository) on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): independent replicas, one per rank (the recurrence needs
+no exchange step when heads and sequences are the work units); time = max over
+ranks, value = all ranks' tokens / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import platform
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tok/s @H96 d128 (% TC peak); spec-verify state GB/s (% HBM)"
+BYTES_PER_TOKHEAD = 1540        # q,k,v bf16 768 + g fp32 512 + beta 4 + o bf16 256 (dk=dv=128)
+FLOPS_PER_TOKHEAD_ALGO = 139264  # 3*C*dk + 2*C*dv + 6*dk*dv, C=64, causal halves only
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x, ws):
+    """Max over ranks (identity at world size 1)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cuda_time(fn, steps, stream):
+    """Mean ms per call, CUDA events on `stream`, synchronised on both sides."""
+    import torch
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        fn()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def cpu_baseline_sample(nthreads=0):
+    """The oracle as it stands on a bounded sample of the prefill workload:
+    all 96 heads of the first 4096 tokens of the 32K sequence."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from kda_gated_delta_02_gb300 import synth
+    oracle.build()
+    Ts = 4096
+    w = synth.PREFILL_32K
+    inp = synth.make_prefill(w, device="cpu", T_override=Ts)
+    to = lambda t: t.double().numpy()
+    args = [to(inp[k]) for k in ("q", "k", "v", "g", "beta")]
+    cu = np.array([0, Ts], dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.prefill(*args, cu, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return {"value": Ts / dt, "unit": "tok/s", "cores": oracle.max_threads() if nthreads <= 0 else nthreads,
+            "kind": "oracle", "seconds": dt,
+            "sample": f"first {Ts} tokens x all {w.H} heads of the T=32768 H=96 d=128 prefill (fp64, OpenMP over heads)",
+            "cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count()}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    steps = max(1, args.steps)
+    res = None
+    total_t, total_tok = 0.0, 0
+    for _ in range(max(0, args.warmup)):
+        pass  # the oracle has no warm-up state; warm-up steps are skipped
+    for _ in range(steps):
+        res = cpu_baseline_sample()
+        total_t += res["seconds"]
+        total_tok += res["value"] * res["seconds"]
+    value = total_tok / total_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "prefill T=32768 H=96 dk=dv=128 (bounded sample: first 4096 tokens)",
+                       "sample_tokens": 4096},
+            "cpu_baseline": {"kind": "oracle", "cores": res["cores"], "sample": res["sample"], "value": value,
+                             "unit": "tok/s"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_profile(args):
+    """Plain launches of one kernel family on a chosen size (for ncu captures)."""
+    import torch
+    torch.cuda.set_device(0)
+    from kda_gated_delta_02_gb300 import build as kbuild
+    kbuild.build()
+    import kda_gated_delta_02_gb300 as kda
+    from kda_gated_delta_02_gb300 import synth
+    n = max(1, args.warmup) + max(1, args.steps)
+    if args.profile in ("prefill", "cp"):
+        w = synth.PREFILL_32K if args.profile == "prefill" else synth.ULTRA_LONG
+        inp = synth.make_prefill(w, device="cuda", T_override=args.T or None)
+        for _ in range(n):
+            kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
+                          cp_mode=kda.CP_AUTO if args.profile == "cp" else kda.CP_OFF)
+    else:
+        d = synth.make_decode(synth.VERIFY, device="cuda", R_override=args.R or None)
+        for _ in range(n):
+            kda.decode_verify_replay(d["state"], d["tail"], d["conv_w"], d["cached_qkv"], d["cached_g"],
+                                     d["cached_b"], d["accepted"], d["new_qkv"], d["new_g"], d["new_b"],
+                                     d["out_w"])
+    torch.cuda.synchronize()
+    print(f"profile {args.profile}: {n} launches ok")
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma list of prefill,verify,cp (default: all)")
+    ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "cp"],
+                    help="launch only this kernel family (warmup + steps launches, no JSON) for ncu")
+    ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp")
+    ap.add_argument("--R", type=int, default=0, help="request count override for --profile verify")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.profile:
+        return run_profile(args)
+
+    import torch
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from kda_gated_delta_02_gb300 import build as kbuild
+    kbuild.build()
+    import kda_gated_delta_02_gb300 as kda
+    from kda_gated_delta_02_gb300 import synth
+    kda.load_library()
+    peaks = load_peaks()
+    only = set(args.only.split(",")) if args.only else {"prefill", "verify", "cp"}
+    K, Wm = max(1, args.steps), max(3, args.warmup)
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    # ------------------------------------------------------------ prefill (headline)
+    w = synth.PREFILL_32K
+    inp = synth.make_prefill(w, device="cuda")
+    T, H = inp["q"].shape[:2]
+    o = torch.empty_like(inp["v"])
+    Sf = torch.empty((1, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+
+    def prefill_step():
+        kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], out=o,
+                      final_state=Sf, cp_mode=kda.CP_AUTO)
+
+    for _ in range(Wm):
+        prefill_step()
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(ws)
+    ms = cuda_time(prefill_step, K, stream)
+    barrier(ws)
+    clocks = sampler.stop()
+    ms = reduce_max(ms, ws)
+    tok_s = ws * T / (ms * 1e-3)
+    algo_bytes = T * H * BYTES_PER_TOKHEAD + H * w.dk * w.dv * 4
+    achieved_gbs = algo_bytes / (ms * 1e-3) / 1e9
+    algo_flops = T * H * FLOPS_PER_TOKHEAD_ALGO
+    tflops = algo_flops / (ms * 1e-3) / 1e12
+    launches = K  # one kda_chunk_fwd launch per step (CP resolves off at 96 heads)
+    out["prefill"] = {"ms": ms, "tok_s": tok_s}
+
+    # e2e: host buffers through the same C-ABI call, copies inside the timed region
+    host = {k: v.to("cpu").pin_memory() for k, v in inp.items() if v is not None}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    Sf_host = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    dev = {k: torch.empty_like(v) for k, v in inp.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size() + Sf_host.numel() * Sf_host.element_size()
+
+    def e2e_step():
+        for k_, v_ in host.items():
+            dev[k_].copy_(v_, non_blocking=True)
+        kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["cu_seqlens"], out=o,
+                      final_state=Sf, cp_mode=kda.CP_AUTO)
+        o_host.copy_(o, non_blocking=True)
+        Sf_host.copy_(Sf, non_blocking=True)
+
+    e2e_step()
+    Ke = max(3, K // 4)
+    ms_e2e = reduce_max(cuda_time(e2e_step, Ke, stream), ws)
+    del host, dev, o_host, Sf_host
+    del inp, o
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ verify-replay
+    if "verify" in only:
+        vw = synth.VERIFY
+        d = synth.make_decode(vw, device="cuda")
+        st, tl = d["state"].clone(), d["tail"].clone()
+        ov = torch.empty((vw.R, vw.Wd + 1, vw.H, vw.dv), dtype=torch.bfloat16, device="cuda")
+
+        def verify_step():
+            kda.decode_verify_replay(st, tl, d["conv_w"], d["cached_qkv"], d["cached_g"], d["cached_b"],
+                                     d["accepted"], d["new_qkv"], d["new_g"], d["new_b"], d["out_w"], out=ov)
+
+        for _ in range(Wm):
+            verify_step()
+        vms = reduce_max(cuda_time(verify_step, K, stream), ws)
+        state_bytes = 2 * st.numel() * st.element_size()  # read + write
+        acc = d["accepted"].to(torch.int64)
+        row = 3 * vw.H * vw.dk * 2 + vw.H * vw.dk * 2 + vw.H * 2  # pre-conv qkv + g + beta per token row
+        proj_bytes = int((acc.sum().item() + vw.R * (vw.Wd + 1)) * row)
+        tail_bytes = 2 * tl.numel() * tl.element_size()
+        o_bytes = ov.numel() * ov.element_size()
+        total_bytes = state_bytes + proj_bytes + tail_bytes + o_bytes
+        out["verify"] = {"workload": vw.name, "ms": vms, "state_gbs": ws * state_bytes / (vms * 1e-3) / 1e9,
+                         "total_gbs": ws * total_bytes / (vms * 1e-3) / 1e9,
+                         "frac_hbm": (total_bytes / (vms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+                         "bytes_per_launch": total_bytes, "state_bytes_per_launch": state_bytes,
+                         "requests_per_s": ws * vw.R / (vms * 1e-3)}
+        launches += K
+        del d, st, tl, ov
+        torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ ultra-long, context parallel
+    if "cp" in only:
+        cw = synth.ULTRA_LONG
+        ci = synth.make_prefill(cw, device="cuda")
+        Tc, Hc = ci["q"].shape[:2]
+        oc = torch.empty_like(ci["v"])
+        Sc = torch.empty((1, Hc, cw.dk, cw.dv), dtype=torch.float32, device="cuda")
+        seg = kda.chunk_fwd_plan(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO)
+        wsb = kda.chunk_fwd_workspace_size(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO)
+        wbuf = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+
+        def cp_step(mode=kda.CP_AUTO):
+            kda.chunk_fwd(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], ci["cu_seqlens"], out=oc,
+                          final_state=Sc, cp_mode=mode, workspace=wbuf)
+
+        for _ in range(3):
+            cp_step()
+        Kc = max(3, K // 4)
+        cms = reduce_max(cuda_time(cp_step, Kc, stream), ws)
+        cms_off = reduce_max(cuda_time(lambda: cp_step(kda.CP_OFF), 1, stream), ws)
+        minimal = Tc * Hc * BYTES_PER_TOKHEAD
+        out["cp"] = {"workload": cw.name, "segment_len": seg, "ms": cms, "tok_s": ws * Tc / (cms * 1e-3),
+                     "ms_cp_off": cms_off, "speedup_vs_off": cms_off / cms,
+                     "frac_hbm_min_bytes": (minimal / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"]}
+        launches += 4 * Kc
+        del ci, oc, wbuf
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample()
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded torch generator, shapes of the pages' workloads)",
+            "config": {"workload": w.name, "T": T, "H": H, "dk": w.dk, "dv": w.dv, "chunk": 64,
+                       "global_batch": 1, "seq_len": T, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs (4.8 GB) larger than L2 (129 MB); no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": peaks["source"], "kernel": "kda_chunk_kernel<128,128,bf16>",
+                         "algorithmic_bytes_per_launch": algo_bytes,
+                         "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],
+                         "tensor_frac": tflops / peaks["bf16_tflops"]},
+            "e2e": {"value": ws * T / (ms_e2e * 1e-3), "unit": "tok/s", "ms": ms_e2e,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clocks, "gpu_launches": launches,
+        }
+        line.update({k: v for k, v in out.items() if k != "prefill"})
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

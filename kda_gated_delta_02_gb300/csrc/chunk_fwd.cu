@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
         vcol0 = m_part ? 0 : colbase - DK;
     }
     const bool has_v = !m_part;
+    const bool need_q = p.mode != MODE_TRANSITION;  // transitions produce no output
     const int dv = p.dv;
 
     // ---------------------------------------------------------------- state init
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
                 int r = idx / QCH, c = idx % QCH;
                 bool ok = r < Lc;
                 size_t row = ok ? ((size_t)(tc + r) * H + h) : 0;
-                cp_async16(&sQ[r * LDB + c * 8], qg + row * DK + c * 8, ok);
+                if (need_q) cp_async16(&sQ[r * LDB + c * 8], qg + row * DK + c * 8, ok);
                 cp_async16(&sK[r * LDB + c * 8], kg + row * DK + c * 8, ok);
             }
             constexpr int VCH = DVT / 8;
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
                 if (r < Lc) {
                     size_t row = (size_t)(tc + r) * H + h;
-                    a = *reinterpret_cast<const float4 *>(qg + row * DK + c * 4);
+                    if (need_q) a = *reinterpret_cast<const float4 *>(qg + row * DK + c * 4);
                     b = *reinterpret_cast<const float4 *>(kg + row * DK + c * 4);
                 }
                 uint2 pa = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
             const int isB = (warp >> 1) & 1;   // 0: A (keys), 1: B (queries)
             const int hf = warp & 1;           // half of the column tiles
             const __nv_bfloat16 *lsrc = isB ? sQ : sK;
+            if (isB && !need_q) goto ab_done;
             float acc[4][4];
 #pragma unroll
             for (int a = 0; a < 4; ++a)
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
                 }
             }
         }
+    ab_done:
         __syncthreads();
 
         // ------------------------------------------------------------ inverse (diagonal blocks)
@@ -508,6 +511,7 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
             uint32_t af[4];
+            if (rb < 4 && !need_q) break;
             if (rb < 4) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {

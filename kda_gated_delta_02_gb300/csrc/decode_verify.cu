@@ -34,25 +34,42 @@ struct VerifySmem {
     static constexpr int CH3 = 3 * D;
     static constexpr int LDR = CH3 + 8;
     static constexpr int MAXROWS = 3 + VT;
+    static constexpr int TILE = VT * LDS * 2;  // one [16][D] bf16 plane
     static constexpr int off_s = 0;
-    static constexpr int off_u1 = off_s + D * LDS * 2;  // raw rows + raw g | QX KX KR
-    static constexpr int raw_bytes = MAXROWS * LDR * 2 + VT * LDS * 2;
-    static constexpr int ops_bytes = 3 * VT * LDS * 2;
+    static constexpr int off_u1 = off_s + D * LDS * 2;  // raw rows + raw g | QX KX KR (hi, lo)
+    static constexpr int raw_bytes = MAXROWS * LDR * 2 + TILE;
+    static constexpr int ops_bytes = 6 * TILE;
     static constexpr int u1_bytes = raw_bytes > ops_bytes ? raw_bytes : ops_bytes;
-    static constexpr int off_kt = off_u1 + ((u1_bytes + 127) / 128) * 128;
-    static constexpr int off_v = off_kt + VT * LDS * 2;
-    static constexpr int off_w = off_v + VT * LDS * 2;
-    static constexpr int off_u = off_w + VT * LDS * 2;
-    static constexpr int off_af = off_u + VT * LDS * 2;      // fp32 [16][20]
+    static constexpr int off_kt = off_u1 + ((u1_bytes + 127) / 128) * 128;  // K~ hi, lo
+    static constexpr int off_v = off_kt + 2 * TILE;                          // V hi, lo
+    static constexpr int off_w = off_v + 2 * TILE;
+    static constexpr int off_u = off_w + TILE;                               // U hi, lo
+    static constexpr int off_af = off_u + 2 * TILE;          // fp32 [16][20]
     static constexpr int off_tf = off_af + VT * 20 * 4;      // fp32 [16][20]
-    static constexpr int off_bm = off_tf + VT * 20 * 4;      // bf16 [16][24]
-    static constexpr int off_beta = off_bm + VT * 24 * 2;    // fp32 [16]
+    static constexpr int off_bm = off_tf + VT * 20 * 4;      // bf16 [16][24] hi, lo
+    static constexpr int off_beta = off_bm + 2 * VT * 24 * 2; // fp32 [16]
     static constexpr int off_rq = off_beta + VT * 4;         // fp32 [16]
     static constexpr int off_rk = off_rq + VT * 4;           // fp32 [16]
     static constexpr int off_xa = off_rk + VT * 4;           // fp32 [D]
     static constexpr int off_part = off_xa + D * 4;          // fp32 [2][D/32][32]
     static constexpr int bytes = off_part + 2 * (D / 32) * 32 * 4;
 };
+
+// x = hi + lo with both halves bf16: products of split operands recover ~16
+// mantissa bits (hi*hi + hi*lo + lo*hi), used where bf16 rounding of a
+// derived operand would dominate the error.
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint32_t &lo) {
+    __nv_bfloat16 ha, la, hb, lb;
+    split_bf16(a, ha, la);
+    split_bf16(b, hb, lb);
+    __nv_bfloat162 h2(ha, hb), l2(la, lb);
+    hi = *reinterpret_cast<uint32_t *>(&h2);
+    lo = *reinterpret_cast<uint32_t *>(&l2);
+}
 
 template <int D>
 __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
@@ -62,9 +79,10 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
     __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_s);
     __nv_bfloat16 *sRaw = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_u1);
     __nv_bfloat16 *sGr = sRaw + L::MAXROWS * LDR;
-    __nv_bfloat16 *sQX = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_u1);
-    __nv_bfloat16 *sKX = sQX + VT * LDS;
-    __nv_bfloat16 *sKR = sKX + VT * LDS;
+    constexpr int PL = VT * LDS;  // elements in one [16][D] plane
+    __nv_bfloat16 *sQX = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_u1);  // hi; lo at +PL
+    __nv_bfloat16 *sKX = sQX + 2 * PL;
+    __nv_bfloat16 *sKR = sKX + 2 * PL;
     __nv_bfloat16 *sKT = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_kt);
     __nv_bfloat16 *sVv = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_v);
     __nv_bfloat16 *sW = reinterpret_cast<__nv_bfloat16 *>(smem + L::off_w);
@@ -238,11 +256,12 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
             float qh = xq[t] * sRq[t], kh = xk[t] * sRk[t];
             float rx = 1.f / xd[t];
             bool live = t < ntok;
-            sQX[t * LDS + c] = __float2bfloat16_rn(live ? qh * xd[t] : 0.f);
-            sKX[t * LDS + c] = __float2bfloat16_rn(live ? kh * xd[t] : 0.f);
-            sKR[t * LDS + c] = __float2bfloat16_rn(live ? kh * rx : 0.f);
-            sKT[t * LDS + c] = __float2bfloat16_rn((t <= a) ? kh * (xa * rx) : 0.f);
-            sVv[t * LDS + c] = __float2bfloat16_rn(live ? xv[t] : 0.f);
+            const int e = t * LDS + c;
+            split_bf16(live ? qh * xd[t] : 0.f, sQX[e], sQX[PL + e]);
+            split_bf16(live ? kh * xd[t] : 0.f, sKX[e], sKX[PL + e]);
+            split_bf16(live ? kh * rx : 0.f, sKR[e], sKR[PL + e]);
+            split_bf16((t <= a) ? kh * (xa * rx) : 0.f, sKT[e], sKT[PL + e]);
+            split_bf16(live ? xv[t] : 0.f, sVv[e], sVv[PL + e]);
         }
     }
     __syncthreads();
@@ -250,17 +269,23 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
     // ---------------------------------------------------------------- A, B (warps 0, 1)
     if (warp < 2) {
         const bool isB = warp == 1;
+        const __nv_bfloat16 *lft = isB ? sQX : sKX;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            uint32_t af[4];
-            ld_a_rowmajor(af, isB ? sQX : sKX, LDS, 0, 16 * kk, lane);
+            uint32_t ah[4], al[4];
+            ld_a_rowmajor(ah, lft, LDS, 0, 16 * kk, lane);
+            ld_a_rowmajor(al, lft + PL, LDS, 0, 16 * kk, lane);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                int s = 8 * nt + gq;
-                uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sKR[s * LDS + 16 * kk + 2 * q4]);
-                uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sKR[s * LDS + 16 * kk + 2 * q4 + 8]);
-                mma_bf16(acc[nt], af, b0, b1);
+                int e0 = (8 * nt + gq) * LDS + 16 * kk + 2 * q4;
+                uint32_t bh0 = *reinterpret_cast<const uint32_t *>(&sKR[e0]);
+                uint32_t bh1 = *reinterpret_cast<const uint32_t *>(&sKR[e0 + 8]);
+                uint32_t bl0 = *reinterpret_cast<const uint32_t *>(&sKR[PL + e0]);
+                uint32_t bl1 = *reinterpret_cast<const uint32_t *>(&sKR[PL + e0 + 8]);
+                mma_bf16(acc[nt], ah, bh0, bh1);
+                mma_bf16(acc[nt], ah, bl0, bl1);
+                mma_bf16(acc[nt], al, bh0, bh1);
             }
         }
 #pragma unroll
@@ -274,8 +299,10 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
                     sAf[t * 20 + s] = (s < t) ? bt * v0 : 0.f;
                     sAf[t * 20 + s + 1] = (s + 1 < t) ? bt * v1 : 0.f;
                 } else {
-                    *reinterpret_cast<uint32_t *>(&sBm[t * 24 + s]) =
-                        pack_bf16((s <= t) ? v0 : 0.f, (s + 1 <= t) ? v1 : 0.f);
+                    uint32_t hi, lo;
+                    split_pack((s <= t) ? v0 : 0.f, (s + 1 <= t) ? v1 : 0.f, hi, lo);
+                    *reinterpret_cast<uint32_t *>(&sBm[t * 24 + s]) = hi;
+                    *reinterpret_cast<uint32_t *>(&sBm[VT * 24 + t * 24 + s]) = lo;
                 }
             }
     }
@@ -298,12 +325,12 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
     }
     __syncthreads();
 
-    // A fragment of T diag(beta), shared by W and U~
-    uint32_t atb[4];
+    // A fragments of T diag(beta) (hi, lo), shared by W and U~
+    uint32_t atb[4], atl[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         int t = gq + 8 * (e & 1), s = 2 * q4 + 8 * (e >> 1);
-        atb[e] = pack_bf16(sTf[t * 20 + s] * sBeta[s], sTf[t * 20 + s + 1] * sBeta[s + 1]);
+        split_pack(sTf[t * 20 + s] * sBeta[s], sTf[t * 20 + s + 1] * sBeta[s + 1], atb[e], atl[e]);
     }
     const int cw0 = 32 * warp;  // this warp's 32 columns
     // W = T diag(b) (K . x), columns [cw0, cw0 + 32) of dk
@@ -319,6 +346,8 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
             ld_b_kmajor_rows(bf, sKX, LDS, 0, cw0 + 16 * np, lane);
             mma_bf16(acc[2 * np], atb, bf[0], bf[1]);
             mma_bf16(acc[2 * np + 1], atb, bf[2], bf[3]);
+            mma_bf16(acc[2 * np], atl, bf[0], bf[1]);
+            mma_bf16(acc[2 * np + 1], atl, bf[2], bf[3]);
         }
 #pragma unroll
         for (int x = 0; x < 4; ++x)
@@ -359,28 +388,43 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
 #pragma unroll
     for (int np = 0; np < 2; ++np) {
         uint32_t bf[4];
+        uint32_t bl[4];
         ld_b_kmajor_rows(bf, sVv, LDS, 0, cw0 + 16 * np, lane);
+        ld_b_kmajor_rows(bl, sVv + PL, LDS, 0, cw0 + 16 * np, lane);
         mma_bf16(aw[2 * np], atb, bf[0], bf[1]);
         mma_bf16(aw[2 * np + 1], atb, bf[2], bf[3]);
+        mma_bf16(aw[2 * np], atb, bl[0], bl[1]);
+        mma_bf16(aw[2 * np + 1], atb, bl[2], bl[3]);
+        mma_bf16(aw[2 * np], atl, bf[0], bf[1]);
+        mma_bf16(aw[2 * np + 1], atl, bf[2], bf[3]);
     }
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             int t = gq + 8 * hh, col = cw0 + 8 * x + 2 * q4;
-            *reinterpret_cast<uint32_t *>(&sU[t * LDS + col]) = pack_bf16(aw[x][2 * hh], aw[x][2 * hh + 1]);
+            uint32_t hi, lo;
+            split_pack(aw[x][2 * hh], aw[x][2 * hh + 1], hi, lo);
+            *reinterpret_cast<uint32_t *>(&sU[t * LDS + col]) = hi;
+            *reinterpret_cast<uint32_t *>(&sU[PL + t * LDS + col]) = lo;
         }
     __syncwarp();
     // O = scale (Q x S0 + B U)
     {
-        uint32_t fb[4];
+        uint32_t fb[4], fbl[4];
         ld_a_rowmajor(fb, sBm, 24, 0, 0, lane);
+        ld_a_rowmajor(fbl, sBm + VT * 24, 24, 0, 0, lane);
 #pragma unroll
         for (int np = 0; np < 2; ++np) {
-            uint32_t bf[4];
+            uint32_t bf[4], bl[4];
             ld_b_kmajor_rows(bf, sU, LDS, 0, cw0 + 16 * np, lane);
+            ld_b_kmajor_rows(bl, sU + PL, LDS, 0, cw0 + 16 * np, lane);
             mma_bf16(aq[2 * np], fb, bf[0], bf[1]);
             mma_bf16(aq[2 * np + 1], fb, bf[2], bf[3]);
+            mma_bf16(aq[2 * np], fb, bl[0], bl[1]);
+            mma_bf16(aq[2 * np + 1], fb, bl[2], bl[3]);
+            mma_bf16(aq[2 * np], fbl, bf[0], bf[1]);
+            mma_bf16(aq[2 * np + 1], fbl, bf[2], bf[3]);
         }
     }
     float ss[2] = {0.f, 0.f};
@@ -438,14 +482,20 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
                 acc[x][2 * hh] = xa * s0.x;
                 acc[x][2 * hh + 1] = xa * s0.y;
             }
-        uint32_t ak[4];
+        uint32_t ak[4], akl[4];
         ld_a_transposed(ak, sKT, LDS, 16 * mb, 0, lane);
+        ld_a_transposed(akl, sKT + PL, LDS, 16 * mb, 0, lane);
 #pragma unroll
         for (int np = 0; np < 2; ++np) {
-            uint32_t bf[4];
+            uint32_t bf[4], bl[4];
             ld_b_kmajor_rows(bf, sU, LDS, 0, cw0 + 16 * np, lane);
+            ld_b_kmajor_rows(bl, sU + PL, LDS, 0, cw0 + 16 * np, lane);
             mma_bf16(acc[2 * np], ak, bf[0], bf[1]);
             mma_bf16(acc[2 * np + 1], ak, bf[2], bf[3]);
+            mma_bf16(acc[2 * np], ak, bl[0], bl[1]);
+            mma_bf16(acc[2 * np + 1], ak, bl[2], bl[3]);
+            mma_bf16(acc[2 * np], akl, bf[0], bf[1]);
+            mma_bf16(acc[2 * np + 1], akl, bf[2], bf[3]);
         }
 #pragma unroll
         for (int x = 0; x < 4; ++x)
