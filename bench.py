@@ -46,6 +46,21 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def kernel_traffic(kernel_key, T):
+    """DRAM bytes per launch of `kernel_key` from the committed ncu summary,
+    scaled to T tokens, or None when the kernel source changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel_key]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
+                return None
+        return rec["traffic_bytes_captured"] * T / rec["captured_T"]
+    except Exception:
+        return None
+
+
 def dist_info():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -377,7 +392,8 @@ def main(argv=None):
                        "global_batch": 1, "seq_len": T, "parallelism": f"replicas x{ws}",
                        "l2": "inputs (4.8 GB) larger than L2 (129 MB); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": kernel_traffic("kda_chunk_kernel<128,128,bf16>", T),
                          "peak_source": peaks["source"], "kernel": "kda_chunk_kernel<128,128,bf16>",
                          "algorithmic_bytes_per_launch": algo_bytes,
                          "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],

@@ -125,7 +125,7 @@ def test_dependency_inverse_example_through_kernel(kda, oracle):
     inp = dict(q=q.cuda(), k=k.cuda(), v=v.cuda(), g=torch.zeros(T, H, dk).cuda(),
                beta=torch.full((T, H), 0.5).cuda(), cu_seqlens=torch.tensor([0, T], dtype=torch.int32).cuda(),
                S0=None)
-    run_and_compare(kda, oracle, inp, out_tol=5e-3, state_tol=5e-3)
+    run_and_compare(kda, oracle, inp)
 
 
 def test_bad_cu_seqlens_sets_status(kda):
@@ -187,7 +187,9 @@ def test_segment_compose_matches_oracle(kda, oracle):
 
 
 def test_segment_compose_worked_example(kda):
-    """Per element, (S/2 + 2) then (S/2 + 1) composes to S/4 + 2, exactly."""
+    """Per element, (S/2 + 2) then (S/2 + 1) composes to S/4 + 2.  In fp32 each
+    step rounds once (one fused multiply-add), so the GPU must equal the two
+    sequential fp32 steps bit for bit and the closed form within one rounding."""
     P, H, d = 2, 1, 64
     M = torch.zeros(P, H, d, d)
     M[:, 0] = 0.5 * torch.eye(d)
@@ -195,8 +197,11 @@ def test_segment_compose_worked_example(kda):
     S0 = torch.randn(H, d, d, generator=torch.Generator().manual_seed(25))
     S_in, Sf = kda.segment_compose(M.cuda(), N.cuda(), S0.cuda())
     torch.cuda.synchronize()
-    assert torch.equal(Sf.cpu(), 0.25 * S0 + 2.0)
-    assert torch.equal(S_in[0].cpu(), S0) and torch.equal(S_in[1].cpu(), 0.5 * S0 + 2.0)
+    s1 = 0.5 * S0 + 2.0          # exact halving, one rounding
+    s2 = 0.5 * s1 + 1.0
+    assert torch.equal(S_in[0].cpu(), S0) and torch.equal(S_in[1].cpu(), s1)
+    assert torch.equal(Sf.cpu(), s2)
+    torch.testing.assert_close(Sf.cpu().double(), 0.25 * S0.double() + 2.0, rtol=0, atol=2.5e-7)
 
 
 # ------------------------------------------------------------------ full-size workloads
