@@ -46,6 +46,7 @@ extern "C" {
 #define KDA_ERR_ALIGNMENT (-3)
 #define KDA_ERR_WORKSPACE (-4)
 #define KDA_ERR_CUDA (-5)
+#define KDA_ERR_SCRATCH_LIMIT (-6)
 
 #define KDA_DTYPE_BF16 0
 #define KDA_DTYPE_F32 1
@@ -187,6 +188,36 @@ int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w,
                              const float *out_norm_w, void *o, int R, int H, int dk, int dv,
                              int W, int Wd, float scale, float g_min, float eps_in,
                              float eps_out, int conv_act, uint32_t *status, void *stream);
+
+/*
+ * Context-parallel prefill that allocates nothing.  (The pages have no
+ * counterpart: this is an interface for callers of this library.)
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace: for example a
+ * serving loop whose host forbids device allocation after start-up, or a
+ * plugin whose host owns every device buffer.  This entry point runs exactly
+ * kda_chunk_fwd with cp_mode = KDA_CP_ON, but takes its scratch (segment
+ * table, per-segment transitions M and N, per-segment initial states) from
+ * one fixed device array inside the library, KDA_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) on every GPU that loads the library, held until the process exits.
+ * The caller still passes all inputs and outputs, with kda_chunk_fwd's
+ * meaning, layout and rules.
+ *
+ * Limit: kda_chunk_fwd_workspace_size(N, T, H, dk, dv, KDA_CP_ON, segment_len)
+ * must not exceed KDA_NOALLOC_SCRATCH_BYTES (about 3 * segments * H * dk * dv
+ * * 4 bytes); larger requests return KDA_ERR_SCRATCH_LIMIT before any launch.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and it keeps the last call's
+ * contents (nothing in it needs clearing): calls that overlap on the GPU, on
+ * any streams, race on it and must be serialised by the caller.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int kda_chunk_fwd_cp_noalloc(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const int32_t *cu_seqlens, int N, int T, int H,
+                             int dk, int dv, const float *initial_state, float *final_state,
+                             void *o, float scale, float g_min, int in_dtype, int segment_len,
+                             uint32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

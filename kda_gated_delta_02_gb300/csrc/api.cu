@@ -98,6 +98,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
         case KDA_ERR_WORKSPACE: return "workspace missing or too small";
         case KDA_ERR_CUDA: return "CUDA launch error";
+        case KDA_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation entry point";
         default: return "unknown status";
     }
 }
