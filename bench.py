@@ -270,6 +270,9 @@ def main(argv=None):
     out = {}
 
     # ------------------------------------------------------------ prefill (headline)
+    # dk = dv = 128 bf16 runs the tcgen05 / tensor-memory kernel (one launch per step)
+    prefill_kernel = ("kda_chunk_kernel<128,128,bf16>" if os.environ.get("KDA_PREFILL_TC", "1") == "0"
+                      else "kda_chunk_tc_kernel")
     w = synth.PREFILL_32K
     inp = synth.make_prefill(w, device="cuda")
     T, H = inp["q"].shape[:2]
@@ -393,8 +396,8 @@ def main(argv=None):
                        "l2": "inputs (4.8 GB) larger than L2 (129 MB); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": kernel_traffic("kda_chunk_kernel<128,128,bf16>", T),
-                         "peak_source": peaks["source"], "kernel": "kda_chunk_kernel<128,128,bf16>",
+                         "traffic": kernel_traffic(prefill_kernel, T),
+                         "peak_source": peaks["source"], "kernel": prefill_kernel,
                          "algorithmic_bytes_per_launch": algo_bytes,
                          "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],
                          "tensor_frac": tflops / peaks["bf16_tflops"]},

@@ -62,6 +62,7 @@ extern "C" {
 #define KDA_STATUS_BAD_SEQLENS 0x1u      /* cu_seqlens not monotone / out of [0, T] */
 #define KDA_STATUS_BAD_ACCEPTED_LEN 0x2u /* accepted_len[r] outside [0, Wd]        */
 #define KDA_STATUS_SEGMENT_OVERFLOW 0x4u /* segment table larger than planned      */
+#define KDA_STATUS_TIMEOUT 0x8u          /* a bounded on-chip wait gave up; unit left unfinished */
 
 /* Human-readable name of a return status. Never NULL. */
 const char *kda_status_string(int status);

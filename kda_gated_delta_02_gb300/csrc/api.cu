@@ -86,6 +86,16 @@ CpLayout cp_layout(int N, int T, int H, int dk, int dv, int cp_mode, int segment
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Chunk-kernel dispatch by shape: the tcgen05 / tensor-memory kernel for
+// dk = dv = 128 with bf16 inputs, the warp-level kernel otherwise.
+// KDA_PREFILL_TC=0 selects the warp-level kernel everywhere (comparisons).
+cudaError_t run_chunk(const kda::ChunkArgs &a, int units, bool bf, cudaStream_t st) {
+    const char *env = getenv("KDA_PREFILL_TC");
+    const bool tc_ok = !(env && env[0] == '0');
+    if (tc_ok && kda::chunk_tc_supported(a, bf)) return kda::launch_chunk_tc(a, units, st);
+    return kda::launch_chunk(a, units, prefill_dvt(a.dk, a.dv, a.mode == kda::MODE_TRANSITION), bf, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -143,7 +153,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
         a.cu_seqlens = cu_seqlens;
         a.S_init = initial_state;
         a.S_final = final_state;
-        return cuda_status(kda::launch_chunk(a, N, prefill_dvt(dk, dv, false), bf, st));
+        return cuda_status(run_chunk(a, N, bf, st));
     }
     if (!workspace || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -163,7 +173,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
     a.seg_count = count;
     a.M_out = M;
     a.N_out = Nm;
-    e = kda::launch_chunk(a, L.P_max, prefill_dvt(dk, dv, true), bf, st);
+    e = run_chunk(a, L.P_max, bf, st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     // pass 2: ordered scan per (sequence, head)
     kda::ComposeArgs c = {};
@@ -176,7 +186,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
     a.S_in = Sin;
     a.S_final = final_state;
     a.M_out = a.N_out = nullptr;
-    return cuda_status(kda::launch_chunk(a, L.P_max, prefill_dvt(dk, dv, false), bf, st));
+    return cuda_status(run_chunk(a, L.P_max, bf, st));
 }
 
 int kda_segment_transition(const void *k, const void *v, const float *g, const float *beta, int T, int H,
@@ -199,8 +209,7 @@ int kda_segment_transition(const void *k, const void *v, const float *g, const f
     a.M_out = M;
     a.N_out = Nmat;
     const int P = (T + segment_len - 1) / segment_len;
-    return cuda_status(kda::launch_chunk(a, P, prefill_dvt(dk, dv, true), in_dtype == KDA_DTYPE_BF16,
-                                         static_cast<cudaStream_t>(stream)));
+    return cuda_status(run_chunk(a, P, in_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
 int kda_segment_compose(const float *M, const float *Nmat, const float *S0, float *S_in, float *S_final,

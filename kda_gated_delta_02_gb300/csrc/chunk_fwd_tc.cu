@@ -1,0 +1,712 @@
+// chunk_fwd_tc.cu -- chunkwise KDA prefill on the sm_103a tensor cores
+// (tcgen05.mma, accumulators in tensor memory), dk = dv = 128, bf16 inputs.
+//
+// One CTA (16 warps) walks one (segment, head) unit, 64 tokens per chunk
+// ("Noyaux KDA et FlashKDA", section "FlashKDA : le noyau par blocs").  The
+// fp32 state S^T (dv rows x dk) stays in registers for the whole walk: thread
+// (lane quadrant q, column group g) owns row 32q + lane, columns 32g .. 32g+31,
+// which is exactly the tensor-memory tile it reads back.  Every product of the
+// chunk runs as a tcgen05 MMA with M = 128 on operands staged in shared memory
+// in the 128-byte swizzled layouts; transposed forms put dv (or dk) on M:
+//   A/B tiles  D[s][t']  = R_i[s] . L[t']   (per 16-row block i, N = 16 keys + 16 queries)
+//   W^T        D[i][t]   = (K e^gamma)^T  (T diag b)^T
+//   U~^T       D[j][t]   = V^T (T diag b)^T,      then  -= S^T W^T   ->  U^T
+//   O^T        D[j][t]   = S^T Q~^T + U^T B^T
+//   S update   S^T <- Diag-cols(e^{gamma_63}) S^T + U^T K~
+// with R_i[s] = k_s y_s c_{i,j(s)} (1/delta_i on the diagonal block) and
+// L[t] = k_t x_t or q_t x_t: the per-16-token-block anchoring that the
+// g >= -5 floor makes overflow-free ("Noyaux KDA et FlashKDA", "Le role de la
+// decroissance bornee"); x, y are running products of e^{g} inside a block.
+// The dependency inverse T = (I + A)^{-1} is fp32 throughout ("Dentro de los
+// esfuerzos de optimizacion de Kimi K3", "Nota tecnica: Precision del KDA").
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace tc {
+
+constexpr int D = 128;  // dk = dv
+constexpr int CH = 64;
+constexpr int NT = 512;
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_Q = 0;         // raw q bf16 [64][128]
+constexpr uint32_t OFF_K = 16384;     // raw k bf16 [64][128]
+constexpr uint32_t OFF_G = 32768;     // raw g f32 [64][128]
+constexpr uint32_t OFF_V = 65536;     // V, MN-major (s x dv): two 64-wide halves of [64 s][128 B]
+constexpr uint32_t OFF_UN = 81920;    // union, 73728 bytes:
+constexpr uint32_t UN_L = 0;          //   L (K-major 128 x 128)         steps 2-3
+// R_i (16(i+1) rows, K-major) at 32768 + 4096 * i(i+1)/2: 32768, 36864, 45056, 57344
+__host__ __device__ constexpr uint32_t un_r(int i) { return 32768u + 4096u * (uint32_t)(i * (i + 1) / 2); }
+constexpr uint32_t UN_AF = 0;         //   A fp32 [64][68]                steps 4-5
+constexpr uint32_t UN_TF = 17408;     //   T fp32 [64][68]
+constexpr uint32_t UN_ST = 0;         //   S^T bf16 (K-major 128 x 128)   steps 7-8
+constexpr uint32_t UN_W = 32768;      //   W (MN-major: 128 k-rows i x 64 t)
+constexpr uint32_t UN_UT = 49152;     //   U^T (K-major 128 x 64)         steps 9-10
+constexpr uint32_t OFF_KG = 155648;   // K e^gamma, MN-major (s x dk)
+constexpr uint32_t OFF_QT = 172032;   // Q e^gamma, K-major 64 x 128
+constexpr uint32_t OFF_KT = 188416;   // K e^{gamma_63 - gamma}, MN-major (s x dk)
+constexpr uint32_t OFF_TB = 204800;   // T diag(b), K-major 64 x 64
+constexpr uint32_t OFF_BM = 212992;   // B, MN-major (64 k-rows s x 64 t)
+constexpr uint32_t OFF_BETA = 221184; // f32 [64]
+constexpr uint32_t OFF_PART = 221440; // f32 [2][4][128] half-block products
+constexpr uint32_t OFF_DEL = 225536;  // f32 [4][128] block decays
+constexpr uint32_t OFF_GAM = 227584;  // f32 [128] chunk decay e^{gamma_63}
+constexpr uint32_t OFF_BAR = 228096;  // 6 mbarriers: 4 MMA groups, q/k/g loads, v loads
+constexpr uint32_t OFF_TMEM = 228144; // tensor-memory base address
+constexpr uint32_t SMEM_BYTES = 228160 + 1024;  // + alignment slack
+constexpr int LDF = 68;               // fp32 [64][68] row stride
+
+// tensor-memory columns
+constexpr uint32_t TM_AB = 0, TM_W = 128, TM_U = 192, TM_O = 256, TM_S = 320;
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+
+__device__ __forceinline__ void st_bf16x2(unsigned char *base, uint32_t off, float a, float b) {
+    *reinterpret_cast<uint32_t *>(base + off) = pack_bf16(a, b);
+}
+
+// Tensor maps of the chunk loads: q, k, g as plain [64 tokens][128] boxes,
+// v as two 64-wide halves with the 128-byte swizzle (the MN-major operand
+// layout of the U~ product, atoms ordered [half][k group]).
+struct TcParams {
+    ChunkArgs a;
+    CUtensorMap tq, tk, tg, tv;
+};
+
+__global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams P) {
+    const ChunkArgs &p = P.a;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned base for the swizzled operand tiles; an offset from the
+    // __shared__ array (not an integer round trip) keeps accesses in the
+    // shared state space
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
+    float *sPart = reinterpret_cast<float *>(sm + OFF_PART);
+    float *sDel = reinterpret_cast<float *>(sm + OFF_DEL);
+    float *sGam = reinterpret_cast<float *>(sm + OFF_GAM);
+    const uint32_t bar0 = sb + OFF_BAR;
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
+    const int H = p.H, dv = p.dv;
+
+    // ---------------------------------------------------------------- work unit
+    int n, t0, t1;
+    bool last_seg = true;
+    if (p.mode == MODE_SEQ) {
+        n = unit;
+        t0 = p.cu_seqlens[n];
+        t1 = p.cu_seqlens[n + 1];
+        if (t0 < 0 || t1 < t0 || t1 > p.T) {
+            if (tid == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
+            return;
+        }
+    } else if (p.seg_table) {
+        if (unit >= *p.seg_count) return;
+        const int4 e = reinterpret_cast<const int4 *>(p.seg_table)[unit];
+        n = e.x;
+        t0 = e.y;
+        t1 = e.z;
+        last_seg = e.w != 0;
+    } else {
+        n = 0;
+        t0 = unit * p.seg_len;
+        t1 = min(p.T, t0 + p.seg_len);
+        last_seg = t1 == p.T;
+    }
+    const bool transition = p.mode == MODE_TRANSITION;
+    const bool m_part = transition && tile == 0;  // augmented columns [0, dk): M
+    const bool has_v = !m_part;
+    const bool need_q = !transition;
+    const int vcol0 = transition ? 0 : tile * D;
+
+    // ---------------------------------------------------------------- setup
+    if (tid == 0) {
+        for (int b = 0; b < 6; ++b) umma::mbar_init(bar0 + 8 * b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 0) umma::tmem_alloc(sb + OFF_TMEM, 512);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *sTmem;
+
+    const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, column group
+    const int jrow = 32 * qd + lane;          // S^T row (value column j) owned
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+
+    float Sreg[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const int i = 32 * cg + c;
+        float v0 = 0.f;
+        if (transition) {
+            v0 = (m_part && i == jrow) ? 1.f : 0.f;
+        } else {
+            const float *src = (p.mode == MODE_SEQ) ? p.S_init : p.S_in;
+            if (src) {
+                size_t sidx = (p.mode == MODE_SEQ) ? (size_t)n : (size_t)unit;
+                v0 = src[((sidx * H + h) * D + i) * (size_t)dv + vcol0 + jrow];
+            }
+        }
+        Sreg[c] = v0;
+    }
+
+    const float g_min = p.g_min;
+
+    const uint32_t bar_qkg = bar0 + 32, bar_v = bar0 + 40;
+    // one thread issues the bulk copies of a chunk; rows past the end of the
+    // tensor are zero-filled by the copy engine, rows past the end of the
+    // segment are zeroed after arrival (fix_tail)
+    auto issue_qkg = [&](int tc) {
+        if (tid == 0) {
+            umma::fence_proxy_async();
+            umma::mbar_expect_tx(bar_qkg, (need_q ? 16384u : 0u) + 16384u + 32768u);
+            if (need_q) umma::tma_load_3d(sb + OFF_Q, &P.tq, 0, h, tc, bar_qkg);
+            umma::tma_load_3d(sb + OFF_K, &P.tk, 0, h, tc, bar_qkg);
+            umma::tma_load_3d(sb + OFF_G, &P.tg, 0, h, tc, bar_qkg);
+        }
+    };
+    // values: consumed up to the W / U~ products (step 6), so they are
+    // prefetched after those, separately from q, k, g (consumed in step 2)
+    auto issue_v = [&](int tc) {
+        if (tid == 0 && has_v) {
+            umma::fence_proxy_async();
+            umma::mbar_expect_tx(bar_v, 16384u);
+            umma::tma_load_3d(sb + OFF_V, &P.tv, vcol0, h, tc, bar_v);
+            umma::tma_load_3d(sb + OFF_V + 8192, &P.tv, vcol0 + 64, h, tc, bar_v);
+        }
+    };
+    auto load_beta = [&](int tc) -> float {
+        const int Lc = min(CH, t1 - tc);
+        return (tid < Lc) ? p.beta[(size_t)(tc + tid) * H + h] : 0.f;
+    };
+    if (!has_v) {  // the M part of a transition walks v = 0
+        for (int idx = tid; idx < 16384 / 16; idx += NT)
+            *reinterpret_cast<uint4 *>(sm + OFF_V + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+        umma::fence_proxy_async();
+    }
+
+    bool timed_out = false;
+    uint32_t phase = 0;
+    float beta_next = 0.f;
+    uint32_t pending = 0;  // bulk copies issued for the chunk after the current one
+    if (t0 < t1) {
+        issue_qkg(t0);
+        issue_v(t0);
+        if (tid < CH) beta_next = load_beta(t0);
+    }
+
+    for (int tc = t0; tc < t1; tc += CH, phase ^= 1u) {
+        const int Lc = min(CH, t1 - tc);
+        if (tid < CH) sBeta[tid] = beta_next;
+        pending = 0;
+        timed_out |= !umma::mbar_wait(bar_qkg, phase, WAIT_LIMIT);
+        if (has_v) timed_out |= !umma::mbar_wait(bar_v, phase, WAIT_LIMIT);
+        if (Lc < CH) {  // last chunk of the segment: rows past its end are not ours
+            for (int idx = tid; idx < (CH - Lc) * 16; idx += NT) {
+                const int r = Lc + (idx >> 4), c = idx & 15;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sm + OFF_Q + r * 256 + c * 16) = z;
+                *reinterpret_cast<uint4 *>(sm + OFF_K + r * 256 + c * 16) = z;
+                *reinterpret_cast<uint4 *>(sm + OFF_G + r * 512 + c * 16) = z;
+                *reinterpret_cast<uint4 *>(sm + OFF_G + r * 512 + 256 + c * 16) = z;
+                // V rows (token r) in both 64-wide halves: 8 chunks of 16 bytes each
+                *reinterpret_cast<uint4 *>(sm + OFF_V + (c >> 3) * 8192 + umma::mnmaj(8 * (c & 7), r, 1)) = z;
+            }
+            umma::fence_proxy_async();
+        }
+        if (__syncthreads_or(timed_out)) break;
+
+        // ------------------------------------------------------------ step 2: decays and operands
+        {
+            const int c2 = tid & 63, i = (tid >> 6) & 3, hf = tid >> 8;
+            const int ch = 2 * c2;
+            const int tb = 16 * i + 8 * hf;
+            float2 e[8], xl[8], yl[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float2 gv = *reinterpret_cast<const float2 *>(sm + OFF_G + (tb + r) * 512 + ch * 4);
+                e[r].x = __expf(fmaxf(gv.x, g_min));
+                e[r].y = __expf(fmaxf(gv.y, g_min));
+            }
+            float2 pr = make_float2(1.f, 1.f);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                pr.x *= e[r].x;
+                pr.y *= e[r].y;
+                xl[r] = pr;
+            }
+            float2 sf = make_float2(1.f, 1.f);
+#pragma unroll
+            for (int r = 7; r >= 0; --r) {
+                yl[r] = sf;
+                sf.x *= e[r].x;
+                sf.y *= e[r].y;
+            }
+            *reinterpret_cast<float2 *>(sPart + (hf * 4 + i) * 128 + ch) = pr;
+            __syncthreads();
+            const float2 p0 = *reinterpret_cast<const float2 *>(sPart + (0 * 4 + i) * 128 + ch);
+            const float2 p1 = *reinterpret_cast<const float2 *>(sPart + (1 * 4 + i) * 128 + ch);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (hf == 0) {
+                    yl[r].x *= p1.x;
+                    yl[r].y *= p1.y;
+                } else {
+                    xl[r].x *= p0.x;
+                    xl[r].y *= p0.y;
+                }
+            }
+            if (hf == 0) *reinterpret_cast<float2 *>(sDel + i * 128 + ch) = make_float2(p0.x * p1.x, p0.y * p1.y);
+            __syncthreads();
+            float2 dl[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) dl[m] = *reinterpret_cast<const float2 *>(sDel + m * 128 + ch);
+            float2 gb = make_float2(1.f, 1.f), cc = make_float2(1.f, 1.f);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (m < i) { gb.x *= dl[m].x; gb.y *= dl[m].y; }
+                if (m > i) { cc.x *= dl[m].x; cc.y *= dl[m].y; }
+            }
+            if (i == 0 && hf == 0) {
+                *reinterpret_cast<float2 *>(sGam + ch) = make_float2(
+                    ((dl[0].x * dl[1].x) * dl[2].x) * dl[3].x, ((dl[0].y * dl[1].y) * dl[2].y) * dl[3].y);
+            }
+            // right-operand factors for row blocks i2 >= i: 1/delta_i (i2 == i), c_{i2,i} otherwise
+            float2 vf[4];
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+                float2 f = make_float2(1.f, 1.f);
+                if (i2 == i) {
+                    f = make_float2(__frcp_rn(dl[i].x), __frcp_rn(dl[i].y));
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m > i && m < i2) { f.x *= dl[m].x; f.y *= dl[m].y; }
+                }
+                vf[i2] = f;
+            }
+            // Every destination row of this thread's token r has (row & 7) == r,
+            // so one swizzled column offset per r serves all operands; row bases
+            // are per-thread constants.
+            unsigned char *un = sm + OFF_UN;
+            const uint32_t c8 = (uint32_t)(ch & 63) >> 3, lo = (uint32_t)(ch & 7) << 1, kb = (uint32_t)ch >> 6;
+            const uint32_t rowL = (uint32_t)(32 * i + 8 * hf) * 128u;  // key rows; query rows +2048
+            const uint32_t rowT = (uint32_t)tb * 128u;                 // token rows
+            unsigned char *pL = un + UN_L + kb * 16384u + rowL;
+            unsigned char *pQT = sm + OFF_QT + kb * 8192u + rowT;
+            const uint32_t atom = ((uint32_t)(2 * i + hf) * 2u + kb) * 1024u;
+            unsigned char *pKG = sm + OFF_KG + atom;
+            unsigned char *pKT = sm + OFF_KT + atom;
+            unsigned char *pR0 = un + un_r(0) + kb * (16u * 1u * 128u) + rowT;
+            unsigned char *pR1 = un + un_r(1) + kb * (16u * 2u * 128u) + rowT;
+            unsigned char *pR2 = un + un_r(2) + kb * (16u * 3u * 128u) + rowT;
+            unsigned char *pR3 = un + un_r(3) + kb * (16u * 4u * 128u) + rowT;
+            const unsigned char *pk = sm + OFF_K + rowT * 2u + ch * 2;  // raw rows are 256 B
+            const unsigned char *pq = sm + OFF_Q + rowT * 2u + ch * 2;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const uint32_t o = (uint32_t)r * 128u + ((c8 ^ (uint32_t)r) << 4) + lo;
+                const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(pk + r * 256));
+                const float2 x = xl[r], y = yl[r];
+                const float2 lk = make_float2(kv.x * x.x, kv.y * x.y);
+                const float2 ky = make_float2(kv.x * y.x, kv.y * y.y);
+                *reinterpret_cast<uint32_t *>(pL + o) = pack_bf16(lk.x, lk.y);
+                if (i <= 0) *reinterpret_cast<uint32_t *>(pR0 + o) = pack_bf16(ky.x * vf[0].x, ky.y * vf[0].y);
+                if (i <= 1) *reinterpret_cast<uint32_t *>(pR1 + o) = pack_bf16(ky.x * vf[1].x, ky.y * vf[1].y);
+                if (i <= 2) *reinterpret_cast<uint32_t *>(pR2 + o) = pack_bf16(ky.x * vf[2].x, ky.y * vf[2].y);
+                *reinterpret_cast<uint32_t *>(pR3 + o) = pack_bf16(ky.x * vf[3].x, ky.y * vf[3].y);
+                *reinterpret_cast<uint32_t *>(pKG + o) = pack_bf16(lk.x * gb.x, lk.y * gb.y);
+                *reinterpret_cast<uint32_t *>(pKT + o) = pack_bf16(ky.x * cc.x, ky.y * cc.y);
+                if (need_q) {
+                    const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(pq + r * 256));
+                    const float2 lq = make_float2(qv.x * x.x, qv.y * x.y);
+                    *reinterpret_cast<uint32_t *>(pL + 2048 + o) = pack_bf16(lq.x, lq.y);
+                    *reinterpret_cast<uint32_t *>(pQT + o) = pack_bf16(lq.x * gb.x, lq.y * gb.y);
+                }
+            }
+        }
+        umma::fence_proxy_async();
+        __syncthreads();
+
+        // ------------------------------------------------------------ step 3: A and B tiles
+        if (tid == 0) {
+            umma::fence_after();
+            constexpr uint32_t id = umma::idesc_bf16(128, 32, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t rows = 16 * (i + 1);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                    const uint64_t a = umma::sdesc(sb + OFF_UN + un_r(i) + kb * rows * 128 + kin, 16, 1024);
+                    const uint64_t b = umma::sdesc(sb + OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin, 16, 1024);
+                    umma::mma(tmem + TM_AB + 32 * i, a, b, id, ks > 0 ? 1u : 0u);
+                }
+            }
+            umma::commit(bar0 + 0);
+        }
+        if (tc + CH < t1) {  // raw q, k, g consumed: prefetch the next chunk's
+            issue_qkg(tc + CH);
+            pending |= 1u;
+        }
+        timed_out |= !umma::mbar_wait(bar0 + 0, phase, WAIT_LIMIT);
+        umma::fence_after();
+
+        // ------------------------------------------------------------ step 4: A (fp32, scaled by b_t) and B (bf16)
+        {
+            float *sAf = reinterpret_cast<float *>(sm + OFF_UN + UN_AF);
+            if (qd < 2) {
+                float v[32];
+                umma::ld32(tq + TM_AB + 32 * cg, v);
+                const int s = jrow;  // key position (0..63)
+                uint32_t bp[8];
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    const int t = 16 * cg + tt;
+                    sAf[t * LDF + s] = (s < t) ? sBeta[t] * v[tt] : 0.f;
+                }
+#pragma unroll
+                for (int tt = 0; tt < 16; tt += 2) {
+                    const int t = 16 * cg + tt;
+                    bp[tt >> 1] = pack_bf16((s <= t) ? v[16 + tt] : 0.f, (s <= t + 1) ? v[17 + tt] : 0.f);
+                }
+                // B as an MN-major operand: element (n = t, k = s), t contiguous
+                *reinterpret_cast<uint4 *>(sm + OFF_BM + umma::mnmaj(16 * cg, s, 1)) =
+                    make_uint4(bp[0], bp[1], bp[2], bp[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_BM + umma::mnmaj(16 * cg + 8, s, 1)) =
+                    make_uint4(bp[4], bp[5], bp[6], bp[7]);
+            }
+        }
+        if (__syncthreads_or(timed_out)) break;
+
+        // ------------------------------------------------------------ step 5: T = (I + A)^{-1}, fp32
+        {
+            const float *sAf = reinterpret_cast<const float *>(sm + OFF_UN + UN_AF);
+            float *sTf = reinterpret_cast<float *>(sm + OFF_UN + UN_TF);
+            // diagonal 16 x 16 blocks, right-looking substitution with one column
+            // per lane in registers: lanes 0-15 of warp w -> block 2w, 16-31 -> 2w+1
+            if (warp < 2) {
+                const int i = 2 * warp + (lane >> 4), c = lane & 15;
+                const float *Ab = sAf + (16 * i) * LDF + 16 * i;
+                float acc[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < 15; ++m) {
+                    const float cm = acc[m];
+#pragma unroll
+                    for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(-Ab[r * LDF + m], cm, acc[r]);
+                }
+                float *Tb = sTf + (16 * i) * LDF + 16 * i;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tb[r * LDF + c] = acc[r];
+            }
+            __syncthreads();
+            // 32 x 32 diagonal halves: T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22
+            {
+                const int hb = tid >> 8, e = tid & 255, r = e >> 4, c = e & 15;
+                const int i = 2 * hb + 1, j = 2 * hb;
+                const float *Ar = sAf + (16 * i + r) * LDF + 16 * j;
+                const float *Tc = sTf + (16 * j) * LDF + 16 * j + c;
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    x0 = fmaf(Ar[m], Tc[m * LDF], x0);
+                    x1 = fmaf(Ar[m + 1], Tc[(m + 1) * LDF], x1);
+                }
+                float *Xp = sTf + (16 * i + r) * LDF + 16 * j + c;
+                *Xp = x0 + x1;
+                // the upper blocks (0,1) and (2,3) of T are zero (read as parts of the
+                // lower-triangular 32 x 32 halves below)
+                sTf[(16 * j + r) * LDF + 16 * i + c] = 0.f;
+                __syncthreads();
+                const float *Ti = sTf + (16 * i + r) * LDF + 16 * i;
+                const float *Xc = sTf + (16 * i) * LDF + 16 * j + c;
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    y0 = fmaf(Ti[m], Xc[m * LDF], y0);
+                    y1 = fmaf(Ti[m + 1], Xc[(m + 1) * LDF], y1);
+                }
+                __syncthreads();
+                *Xp = -(y0 + y1);
+                __syncthreads();
+            }
+            // lower-left 32 x 32: T_21 = -T_22 A_21 T_11 (blocks of 32)
+            {
+                const int r = tid >> 4, c = 2 * (tid & 15);
+                const float *Ar = sAf + (32 + r) * LDF;
+                float2 x0 = make_float2(0.f, 0.f), x1 = x0;
+#pragma unroll 8
+                for (int m = 0; m < 32; m += 2) {
+                    const float2 t0 = *reinterpret_cast<const float2 *>(sTf + m * LDF + c);
+                    const float2 t1 = *reinterpret_cast<const float2 *>(sTf + (m + 1) * LDF + c);
+                    const float a0 = Ar[m], a1 = Ar[m + 1];
+                    x0.x = fmaf(a0, t0.x, x0.x); x0.y = fmaf(a0, t0.y, x0.y);
+                    x1.x = fmaf(a1, t1.x, x1.x); x1.y = fmaf(a1, t1.y, x1.y);
+                }
+                float *Xp = sTf + (32 + r) * LDF + c;
+                *reinterpret_cast<float2 *>(Xp) = make_float2(x0.x + x1.x, x0.y + x1.y);
+                __syncthreads();
+                const float *Tr = sTf + (32 + r) * LDF + 32;
+                float2 y0 = make_float2(0.f, 0.f), y1 = y0;
+#pragma unroll 8
+                for (int m = 0; m < 32; m += 2) {
+                    const float2 u0 = *reinterpret_cast<const float2 *>(sTf + (32 + m) * LDF + c);
+                    const float2 u1 = *reinterpret_cast<const float2 *>(sTf + (33 + m) * LDF + c);
+                    const float b0 = Tr[m], b1 = Tr[m + 1];
+                    y0.x = fmaf(b0, u0.x, y0.x); y0.y = fmaf(b0, u0.y, y0.y);
+                    y1.x = fmaf(b1, u1.x, y1.x); y1.y = fmaf(b1, u1.y, y1.y);
+                }
+                __syncthreads();
+                *reinterpret_cast<float2 *>(Xp) = make_float2(-(y0.x + y1.x), -(y0.y + y1.y));
+                __syncthreads();
+            }
+            // T diag(b) as bf16, zero above the diagonal
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e2 = tid + u * NT;  // pair index over 64 x 32 pairs
+                const int t = e2 >> 5, s = 2 * (e2 & 31);
+                const float a0 = (s <= t) ? sTf[t * LDF + s] * sBeta[s] : 0.f;
+                const float a1 = (s + 1 <= t) ? sTf[t * LDF + s + 1] * sBeta[s + 1] : 0.f;
+                st_bf16x2(sm, OFF_TB + umma::kmaj(t, s, 64), a0, a1);
+            }
+        }
+        umma::fence_proxy_async();
+        __syncthreads();
+
+        // ------------------------------------------------------------ step 6: W^T and U~^T
+        if (tid == 0) {
+            umma::fence_after();
+            constexpr uint32_t id = umma::idesc_bf16(128, 64, 1, 0, 0);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t b = umma::sdesc(sb + OFF_TB + ks * 32, 16, 1024);
+                umma::mma(tmem + TM_W, umma::sdesc(sb + OFF_KG + ks * 4096, 1024, 2048), b, id, ks > 0 ? 1u : 0u);
+                if (has_v)  // V halves are 8 KB apart (LBO), k groups 1 KB apart (SBO)
+                    umma::mma(tmem + TM_U, umma::sdesc(sb + OFF_V + ks * 2048, 8192, 1024), b, id, ks > 0 ? 1u : 0u);
+            }
+            umma::commit(bar0 + 8);
+        }
+        timed_out |= !umma::mbar_wait(bar0 + 8, phase, WAIT_LIMIT);
+        umma::fence_after();
+        if (tc + CH < t1) {  // V and b consumed: prefetch the next chunk's
+            issue_v(tc + CH);
+            pending |= 2u;
+            if (tid < CH) beta_next = load_beta(tc + CH);
+        }
+
+        // ------------------------------------------------------------ step 7: W (bf16) and S^T (bf16) operands
+        {
+            float v[16];
+            umma::ld16(tq + TM_W + 16 * cg, v);
+            const int i = jrow;  // key channel
+            // W as an MN-major operand: element (n = t, k = i), t contiguous
+            *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_W + umma::mnmaj(16 * cg, i, 1)) =
+                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+            *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_W + umma::mnmaj(16 * cg + 8, i, 1)) =
+                make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
+                           pack_bf16(v[14], v[15]));
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(Sreg[c + 0], Sreg[c + 1]);
+                pk.y = pack_bf16(Sreg[c + 2], Sreg[c + 3]);
+                pk.z = pack_bf16(Sreg[c + 4], Sreg[c + 5]);
+                pk.w = pack_bf16(Sreg[c + 6], Sreg[c + 7]);
+                *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_ST + umma::kmaj(jrow, 32 * cg + c, 128)) = pk;
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before();
+        if (__syncthreads_or(timed_out)) break;
+
+        // ------------------------------------------------------------ step 8: S^T Q~^T and U~^T - S^T W^T
+        if (tid == 0) {
+            umma::fence_after();
+            constexpr uint32_t idq = umma::idesc_bf16(128, 64, 0, 0, 0);
+            constexpr uint32_t idw = umma::idesc_bf16(128, 64, 0, 1, 1);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                const uint64_t a = umma::sdesc(sb + OFF_UN + UN_ST + kb * 16384 + kin, 16, 1024);
+                if (need_q)
+                    umma::mma(tmem + TM_O, a, umma::sdesc(sb + OFF_QT + kb * 8192 + kin, 16, 1024), idq,
+                              ks > 0 ? 1u : 0u);
+                umma::mma(tmem + TM_U, a, umma::sdesc(sb + OFF_UN + UN_W + ks * 2048, 1024, 1024), idw,
+                          (has_v || ks > 0) ? 1u : 0u);
+            }
+            umma::commit(bar0 + 16);
+        }
+        timed_out |= !umma::mbar_wait(bar0 + 16, phase, WAIT_LIMIT);
+        umma::fence_after();
+
+        // ------------------------------------------------------------ step 9: U^T (bf16) operand
+        {
+            float v[16];
+            umma::ld16(tq + TM_U + 16 * cg, v);
+#pragma unroll
+            for (int c = 0; c < 16; c += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(v[c + 0], v[c + 1]);
+                pk.y = pack_bf16(v[c + 2], v[c + 3]);
+                pk.z = pack_bf16(v[c + 4], v[c + 5]);
+                pk.w = pack_bf16(v[c + 6], v[c + 7]);
+                *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_UT + umma::kmaj(jrow, 16 * cg + c, 128)) = pk;
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before();
+        if (__syncthreads_or(timed_out)) break;
+
+        // ------------------------------------------------------------ step 10: + U^T B^T, U^T K~
+        if (tid == 0) {
+            umma::fence_after();
+            constexpr uint32_t ido = umma::idesc_bf16(128, 64, 0, 1, 0);
+            constexpr uint32_t ids = umma::idesc_bf16(128, 128, 0, 1, 0);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = umma::sdesc(sb + OFF_UN + UN_UT + ks * 32, 16, 1024);
+                if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc(sb + OFF_BM + ks * 2048, 1024, 1024), ido, 1u);
+                umma::mma(tmem + TM_S, a, umma::sdesc(sb + OFF_KT + ks * 4096, 1024, 2048), ids, ks > 0 ? 1u : 0u);
+            }
+            umma::commit(bar0 + 24);
+        }
+        timed_out |= !umma::mbar_wait(bar0 + 24, phase, WAIT_LIMIT);
+        umma::fence_after();
+
+        // ------------------------------------------------------------ step 11: outputs and state
+        // outputs are staged as a row-major [64][128] bf16 tile in the (now free)
+        // union region, then written with 16-byte stores
+        unsigned char *ostage = sm + OFF_UN;
+        if (need_q) {
+            float v[16];
+            umma::ld16(tq + TM_O + 16 * cg, v);
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt)
+                *reinterpret_cast<__nv_bfloat16 *>(ostage + (16 * cg + tt) * 256 + jrow * 2) =
+                    __float2bfloat16_rn(p.scale * v[tt]);
+        }
+        {
+            float v[32];
+            umma::ld32(tq + TM_S + 32 * cg, v);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
+                Sreg[c + 0] = fmaf(gm.x, Sreg[c + 0], v[c + 0]);
+                Sreg[c + 1] = fmaf(gm.y, Sreg[c + 1], v[c + 1]);
+                Sreg[c + 2] = fmaf(gm.z, Sreg[c + 2], v[c + 2]);
+                Sreg[c + 3] = fmaf(gm.w, Sreg[c + 3], v[c + 3]);
+            }
+        }
+        umma::fence_before();
+        if (__syncthreads_or(timed_out)) break;
+        if (need_q) {
+            __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(p.o);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int idx = tid + u * NT, t = idx >> 4, c = idx & 15;
+                if (t < Lc)
+                    *reinterpret_cast<uint4 *>(og + ((size_t)(tc + t) * H + h) * dv + vcol0 + c * 8) =
+                        *reinterpret_cast<const uint4 *>(ostage + t * 256 + c * 16);
+            }
+        }
+    }
+
+    if (timed_out) {
+        if (tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
+        // let copies already issued for the next chunk land before leaving
+        if (pending & 1u) umma::mbar_wait(bar_qkg, phase ^ 1u, WAIT_LIMIT);
+        if ((pending & 2u) && has_v) umma::mbar_wait(bar_v, phase ^ 1u, WAIT_LIMIT);
+    } else {
+        // ------------------------------------------------------------ state out
+        float *dst = nullptr;
+        size_t ld_dst = (size_t)dv, col0 = (size_t)vcol0;
+        if (p.mode == MODE_SEQ) {
+            if (p.S_final) dst = p.S_final + ((size_t)n * H + h) * D * (size_t)dv;
+        } else if (p.mode == MODE_REPLAY) {
+            if (p.S_final && last_seg) dst = p.S_final + ((size_t)n * H + h) * D * (size_t)dv;
+        } else if (m_part) {
+            dst = p.M_out + ((size_t)unit * H + h) * D * (size_t)D;
+            ld_dst = D;
+            col0 = 0;
+        } else {
+            dst = p.N_out + ((size_t)unit * H + h) * D * (size_t)dv;
+            col0 = 0;
+        }
+        if (dst) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * ld_dst + col0 + jrow] = Sreg[c];
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace tc
+
+bool chunk_tc_supported(const ChunkArgs &a, bool in_bf16) {
+    return in_bf16 && a.dk == 128 && a.dv == 128;
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [T][H][inner] tensor, box of `box_inner` x 1 head x 64 tokens
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int inner, int H, int T,
+              int box_inner, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)inner * esize * H};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, 64u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st) {
+    const int ntiles = (a.mode == MODE_TRANSITION) ? 2 : 1;
+    if (units <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(tc::kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    tc::TcParams P;
+    memset(&P, 0, sizeof(P));
+    P.a = a;
+    const int T = a.T;
+    bool ok = make_map(&P.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, T, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&P.tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, a.H, T, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map(&P.tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.dv, a.H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok && a.q) ok = make_map(&P.tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, T, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return cudaErrorInvalidValue;
+    dim3 grid(units, a.H, ntiles);
+    tc::kda_chunk_tc_kernel<<<grid, tc::NT, tc::SMEM_BYTES, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

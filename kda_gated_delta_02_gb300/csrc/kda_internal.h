@@ -33,6 +33,10 @@ struct ChunkArgs {
 
 cudaError_t launch_chunk(const ChunkArgs &a, int units, int dvt, bool in_bf16, cudaStream_t st);
 
+// tcgen05 / tensor-memory version of the chunk kernel (dk = dv = 128, bf16).
+bool chunk_tc_supported(const ChunkArgs &a, bool in_bf16);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st);
+
 cudaError_t launch_segment_table(const int32_t *cu_seqlens, int N, int T, int seg_len, int P_max,
                                  int32_t *table, int32_t *seq_first, int32_t *seg_count,
                                  uint32_t *status, cudaStream_t st);
