@@ -3,9 +3,9 @@
 //
 // One CTA (16 warps) walks one (segment, head) unit, 64 tokens per chunk
 // ("Noyaux KDA et FlashKDA", section "FlashKDA : le noyau par blocs").  The
-// fp32 state S^T (dv rows x dk) stays in registers for the whole walk: thread
-// (lane quadrant q, column group g) owns row 32q + lane, columns 32g .. 32g+31,
-// which is exactly the tensor-memory tile it reads back.  Every product of the
+// fp32 state S^T (dv rows x dk) stays on chip for the whole walk: thread
+// (lane quadrant q, column group g) owns row 32q + lane, columns 32g .. 32g+31;
+// the state itself lives in tensor memory for the whole walk.  Every product of the
 // chunk runs as a tcgen05 MMA with M = 128 on operands staged in shared memory
 // in the 128-byte swizzled layouts; transposed forms put dv (or dk) on M:
 //   A/B tiles  D[s][t']  = R_i[s] . L[t']   (per 16-row block i, N = 16 keys + 16 queries)
@@ -65,7 +65,9 @@ constexpr uint32_t SMEM_BYTES = 228160 + 1024;  // + alignment slack
 constexpr int LDF = 68;               // fp32 [64][68] row stride
 
 // tensor-memory columns
-constexpr uint32_t TM_AB = 0, TM_W = 128, TM_U = 192, TM_O = 256, TM_S = 320;
+//   S^T (fp32, the state, resident for the whole walk) | A/B tiles, later the
+//   U^T K~ update | W^T | U^T | O^T
+constexpr uint32_t TM_ST = 0, TM_AB = 128, TM_S = 128, TM_W = 256, TM_U = 320, TM_O = 384;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
 __device__ __forceinline__ void st_bf16x2(unsigned char *base, uint32_t off, float a, float b) {
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
     // shared state space
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
+    const uint32_t sb4 = sb >> 4;  // 16-byte units, for matrix descriptors
     float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
     float *sPart = reinterpret_cast<float *>(sm + OFF_PART);
     float *sDel = reinterpret_cast<float *>(sm + OFF_DEL);
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
     const int jrow = 32 * qd + lane;          // S^T row (value column j) owned
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
 
+    {
     float Sreg[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
@@ -159,6 +163,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             }
         }
         Sreg[c] = v0;
+    }
+    umma::st32(tq + TM_ST + 32 * cg, Sreg);
     }
 
     const float g_min = p.g_min;
@@ -299,40 +305,46 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             // Every destination row of this thread's token r has (row & 7) == r,
             // so one swizzled column offset per r serves all operands; row bases
             // are per-thread constants.
-            unsigned char *un = sm + OFF_UN;
             const uint32_t c8 = (uint32_t)(ch & 63) >> 3, lo = (uint32_t)(ch & 7) << 1, kb = (uint32_t)ch >> 6;
             const uint32_t rowL = (uint32_t)(32 * i + 8 * hf) * 128u;  // key rows; query rows +2048
             const uint32_t rowT = (uint32_t)tb * 128u;                 // token rows
-            unsigned char *pL = un + UN_L + kb * 16384u + rowL;
-            unsigned char *pQT = sm + OFF_QT + kb * 8192u + rowT;
+            const uint32_t un = sb + OFF_UN;
+            const uint32_t aL = un + UN_L + kb * 16384u + rowL;
+            const uint32_t aQT = sb + OFF_QT + kb * 8192u + rowT;
             const uint32_t atom = ((uint32_t)(2 * i + hf) * 2u + kb) * 1024u;
-            unsigned char *pKG = sm + OFF_KG + atom;
-            unsigned char *pKT = sm + OFF_KT + atom;
-            unsigned char *pR0 = un + un_r(0) + kb * (16u * 1u * 128u) + rowT;
-            unsigned char *pR1 = un + un_r(1) + kb * (16u * 2u * 128u) + rowT;
-            unsigned char *pR2 = un + un_r(2) + kb * (16u * 3u * 128u) + rowT;
-            unsigned char *pR3 = un + un_r(3) + kb * (16u * 4u * 128u) + rowT;
-            const unsigned char *pk = sm + OFF_K + rowT * 2u + ch * 2;  // raw rows are 256 B
-            const unsigned char *pq = sm + OFF_Q + rowT * 2u + ch * 2;
+            const uint32_t aKG = sb + OFF_KG + atom;
+            const uint32_t aKT = sb + OFF_KT + atom;
+            const uint32_t aR0 = un + un_r(0) + kb * (16u * 1u * 128u) + rowT;
+            const uint32_t aR1 = un + un_r(1) + kb * (16u * 2u * 128u) + rowT;
+            const uint32_t aR2 = un + un_r(2) + kb * (16u * 3u * 128u) + rowT;
+            const uint32_t aR3 = un + un_r(3) + kb * (16u * 4u * 128u) + rowT;
+            const uint32_t ak = sb + OFF_K + rowT * 2u + (uint32_t)ch * 2u;  // raw rows are 256 B
+            const uint32_t aq = sb + OFF_Q + rowT * 2u + (uint32_t)ch * 2u;
+            uint32_t kraw[8], qraw[8];  // loads first: the stores below are ordered asm
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                kraw[r] = lds32(ak + r * 256);
+                qraw[r] = need_q ? lds32(aq + r * 256) : 0u;
+            }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const uint32_t o = (uint32_t)r * 128u + ((c8 ^ (uint32_t)r) << 4) + lo;
-                const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(pk + r * 256));
+                const float2 kv = unpack_bf16(kraw[r]);
                 const float2 x = xl[r], y = yl[r];
                 const float2 lk = make_float2(kv.x * x.x, kv.y * x.y);
                 const float2 ky = make_float2(kv.x * y.x, kv.y * y.y);
-                *reinterpret_cast<uint32_t *>(pL + o) = pack_bf16(lk.x, lk.y);
-                if (i <= 0) *reinterpret_cast<uint32_t *>(pR0 + o) = pack_bf16(ky.x * vf[0].x, ky.y * vf[0].y);
-                if (i <= 1) *reinterpret_cast<uint32_t *>(pR1 + o) = pack_bf16(ky.x * vf[1].x, ky.y * vf[1].y);
-                if (i <= 2) *reinterpret_cast<uint32_t *>(pR2 + o) = pack_bf16(ky.x * vf[2].x, ky.y * vf[2].y);
-                *reinterpret_cast<uint32_t *>(pR3 + o) = pack_bf16(ky.x * vf[3].x, ky.y * vf[3].y);
-                *reinterpret_cast<uint32_t *>(pKG + o) = pack_bf16(lk.x * gb.x, lk.y * gb.y);
-                *reinterpret_cast<uint32_t *>(pKT + o) = pack_bf16(ky.x * cc.x, ky.y * cc.y);
+                sts32(aL + o, pack_bf16(lk.x, lk.y));
+                if (i <= 0) sts32(aR0 + o, pack_bf16(ky.x * vf[0].x, ky.y * vf[0].y));
+                if (i <= 1) sts32(aR1 + o, pack_bf16(ky.x * vf[1].x, ky.y * vf[1].y));
+                if (i <= 2) sts32(aR2 + o, pack_bf16(ky.x * vf[2].x, ky.y * vf[2].y));
+                sts32(aR3 + o, pack_bf16(ky.x * vf[3].x, ky.y * vf[3].y));
+                sts32(aKG + o, pack_bf16(lk.x * gb.x, lk.y * gb.y));
+                sts32(aKT + o, pack_bf16(ky.x * cc.x, ky.y * cc.y));
                 if (need_q) {
-                    const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(pq + r * 256));
+                    const float2 qv = unpack_bf16(qraw[r]);
                     const float2 lq = make_float2(qv.x * x.x, qv.y * x.y);
-                    *reinterpret_cast<uint32_t *>(pL + 2048 + o) = pack_bf16(lq.x, lq.y);
-                    *reinterpret_cast<uint32_t *>(pQT + o) = pack_bf16(lq.x * gb.x, lq.y * gb.y);
+                    sts32(aL + 2048 + o, pack_bf16(lq.x, lq.y));
+                    sts32(aQT + o, pack_bf16(lq.x * gb.x, lq.y * gb.y));
                 }
             }
         }
@@ -346,10 +358,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t rows = 16 * (i + 1);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                    const uint64_t a = umma::sdesc(sb + OFF_UN + un_r(i) + kb * rows * 128 + kin, 16, 1024);
-                    const uint64_t b = umma::sdesc(sb + OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin, 16, 1024);
+                    const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + un_r(i) + kb * rows * 128 + kin) >> 4), 16, 1024);
+                    const uint64_t b = umma::sdesc4(sb4 + ((OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin) >> 4), 16, 1024);
                     umma::mma(tmem + TM_AB + 32 * i, a, b, id, ks > 0 ? 1u : 0u);
                 }
             }
@@ -442,34 +455,42 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 *Xp = -(y0 + y1);
                 __syncthreads();
             }
-            // lower-left 32 x 32: T_21 = -T_22 A_21 T_11 (blocks of 32)
+            // lower-left 32 x 32: T_21 = -T_22 (A_21 T_11), two 32x32x32 fp32
+            // products as tf32 tensor products with hi/lo splits (3 MMAs per step):
+            // warp w < 8 owns the 16 x 8 output tile (rows 16(w>>2), cols 8(w&3))
             {
-                const int r = tid >> 4, c = 2 * (tid & 15);
-                const float *Ar = sAf + (32 + r) * LDF;
-                float2 x0 = make_float2(0.f, 0.f), x1 = x0;
-#pragma unroll 8
-                for (int m = 0; m < 32; m += 2) {
-                    const float2 t0 = *reinterpret_cast<const float2 *>(sTf + m * LDF + c);
-                    const float2 t1 = *reinterpret_cast<const float2 *>(sTf + (m + 1) * LDF + c);
-                    const float a0 = Ar[m], a1 = Ar[m + 1];
-                    x0.x = fmaf(a0, t0.x, x0.x); x0.y = fmaf(a0, t0.y, x0.y);
-                    x1.x = fmaf(a1, t1.x, x1.x); x1.y = fmaf(a1, t1.y, x1.y);
+                const int gq = lane >> 2, q4 = lane & 3;
+                const int mt = (warp >> 2) & 1, nt = warp & 3;
+                auto product = [&](const float *Am, const float *Bm, float (&acc)[4]) {
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+                        split_tf32(Am[(16 * mt + gq) * LDF + 8 * kk + q4], ah[0], al[0]);
+                        split_tf32(Am[(16 * mt + gq + 8) * LDF + 8 * kk + q4], ah[1], al[1]);
+                        split_tf32(Am[(16 * mt + gq) * LDF + 8 * kk + q4 + 4], ah[2], al[2]);
+                        split_tf32(Am[(16 * mt + gq + 8) * LDF + 8 * kk + q4 + 4], ah[3], al[3]);
+                        split_tf32(Bm[(8 * kk + q4) * LDF + 8 * nt + gq], bh0, bl0);
+                        split_tf32(Bm[(8 * kk + q4 + 4) * LDF + 8 * nt + gq], bh1, bl1);
+                        mma_tf32(acc, al, bh0, bh1);
+                        mma_tf32(acc, ah, bl0, bl1);
+                        mma_tf32(acc, ah, bh0, bh1);
+                    }
+                };
+                float acc[4];
+                if (warp < 8) product(sAf + 32 * LDF, sTf, acc);  // X = A_21 T_11
+                float *Xt = sTf + (32 + 16 * mt + gq) * LDF + 8 * nt + 2 * q4;
+                if (warp < 8) {
+                    *reinterpret_cast<float2 *>(Xt) = make_float2(acc[0], acc[1]);
+                    *reinterpret_cast<float2 *>(Xt + 8 * LDF) = make_float2(acc[2], acc[3]);
                 }
-                float *Xp = sTf + (32 + r) * LDF + c;
-                *reinterpret_cast<float2 *>(Xp) = make_float2(x0.x + x1.x, x0.y + x1.y);
                 __syncthreads();
-                const float *Tr = sTf + (32 + r) * LDF + 32;
-                float2 y0 = make_float2(0.f, 0.f), y1 = y0;
-#pragma unroll 8
-                for (int m = 0; m < 32; m += 2) {
-                    const float2 u0 = *reinterpret_cast<const float2 *>(sTf + (32 + m) * LDF + c);
-                    const float2 u1 = *reinterpret_cast<const float2 *>(sTf + (33 + m) * LDF + c);
-                    const float b0 = Tr[m], b1 = Tr[m + 1];
-                    y0.x = fmaf(b0, u0.x, y0.x); y0.y = fmaf(b0, u0.y, y0.y);
-                    y1.x = fmaf(b1, u1.x, y1.x); y1.y = fmaf(b1, u1.y, y1.y);
+                if (warp < 8) product(sTf + 32 * LDF + 32, sTf + 32 * LDF, acc);  // T_22 X
+                __syncthreads();
+                if (warp < 8) {
+                    *reinterpret_cast<float2 *>(Xt) = make_float2(-acc[0], -acc[1]);
+                    *reinterpret_cast<float2 *>(Xt + 8 * LDF) = make_float2(-acc[2], -acc[3]);
                 }
-                __syncthreads();
-                *reinterpret_cast<float2 *>(Xp) = make_float2(-(y0.x + y1.x), -(y0.y + y1.y));
                 __syncthreads();
             }
             // T diag(b) as bf16, zero above the diagonal
@@ -489,11 +510,12 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         if (tid == 0) {
             umma::fence_after();
             constexpr uint32_t id = umma::idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t b = umma::sdesc(sb + OFF_TB + ks * 32, 16, 1024);
-                umma::mma(tmem + TM_W, umma::sdesc(sb + OFF_KG + ks * 4096, 1024, 2048), b, id, ks > 0 ? 1u : 0u);
+                const uint64_t b = umma::sdesc4(sb4 + ((OFF_TB + ks * 32) >> 4), 16, 1024);
+                umma::mma(tmem + TM_W, umma::sdesc4(sb4 + ((OFF_KG + ks * 4096) >> 4), 1024, 2048), b, id, ks > 0 ? 1u : 0u);
                 if (has_v)  // V halves are 8 KB apart (LBO), k groups 1 KB apart (SBO)
-                    umma::mma(tmem + TM_U, umma::sdesc(sb + OFF_V + ks * 2048, 8192, 1024), b, id, ks > 0 ? 1u : 0u);
+                    umma::mma(tmem + TM_U, umma::sdesc4(sb4 + ((OFF_V + ks * 2048) >> 4), 8192, 1024), b, id, ks > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 8);
         }
@@ -516,6 +538,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_W + umma::mnmaj(16 * cg + 8, i, 1)) =
                 make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                            pack_bf16(v[14], v[15]));
+            float Sreg[32];
+            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
 #pragma unroll
             for (int c = 0; c < 32; c += 8) {
                 uint4 pk;
@@ -535,13 +559,14 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             umma::fence_after();
             constexpr uint32_t idq = umma::idesc_bf16(128, 64, 0, 0, 0);
             constexpr uint32_t idw = umma::idesc_bf16(128, 64, 0, 1, 1);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                const uint64_t a = umma::sdesc(sb + OFF_UN + UN_ST + kb * 16384 + kin, 16, 1024);
+                const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_ST + kb * 16384 + kin) >> 4), 16, 1024);
                 if (need_q)
-                    umma::mma(tmem + TM_O, a, umma::sdesc(sb + OFF_QT + kb * 8192 + kin, 16, 1024), idq,
+                    umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_QT + kb * 8192 + kin) >> 4), 16, 1024), idq,
                               ks > 0 ? 1u : 0u);
-                umma::mma(tmem + TM_U, a, umma::sdesc(sb + OFF_UN + UN_W + ks * 2048, 1024, 1024), idw,
+                umma::mma(tmem + TM_U, a, umma::sdesc4(sb4 + ((OFF_UN + UN_W + ks * 2048) >> 4), 1024, 1024), idw,
                           (has_v || ks > 0) ? 1u : 0u);
             }
             umma::commit(bar0 + 16);
@@ -572,10 +597,11 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             umma::fence_after();
             constexpr uint32_t ido = umma::idesc_bf16(128, 64, 0, 1, 0);
             constexpr uint32_t ids = umma::idesc_bf16(128, 128, 0, 1, 0);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = umma::sdesc(sb + OFF_UN + UN_UT + ks * 32, 16, 1024);
-                if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc(sb + OFF_BM + ks * 2048, 1024, 1024), ido, 1u);
-                umma::mma(tmem + TM_S, a, umma::sdesc(sb + OFF_KT + ks * 4096, 1024, 2048), ids, ks > 0 ? 1u : 0u);
+                const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_UT + ks * 32) >> 4), 16, 1024);
+                if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_BM + ks * 2048) >> 4), 1024, 1024), ido, 1u);
+                umma::mma(tmem + TM_S, a, umma::sdesc4(sb4 + ((OFF_KT + ks * 4096) >> 4), 1024, 2048), ids, ks > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 24);
         }
@@ -595,8 +621,9 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                     __float2bfloat16_rn(p.scale * v[tt]);
         }
         {
-            float v[32];
+            float v[32], Sreg[32];
             umma::ld32(tq + TM_S + 32 * cg, v);
+            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
                 const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
@@ -605,6 +632,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 Sreg[c + 2] = fmaf(gm.z, Sreg[c + 2], v[c + 2]);
                 Sreg[c + 3] = fmaf(gm.w, Sreg[c + 3], v[c + 3]);
             }
+            umma::st32(tq + TM_ST + 32 * cg, Sreg);
         }
         umma::fence_before();
         if (__syncthreads_or(timed_out)) break;
@@ -642,6 +670,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             col0 = 0;
         }
         if (dst) {
+            float Sreg[32];
+            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
 #pragma unroll
             for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * ld_dst + col0 + jrow] = Sreg[c];
         }

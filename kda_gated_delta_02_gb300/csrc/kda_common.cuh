@@ -42,6 +42,28 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A(16x8, row) * B(8x8, col) + C in tf32 with fp32 accumulate.
+//   A: a0 (g, q)  a1 (g+8, q)  a2 (g, q+4)  a3 (g+8, q+4);  B: b0 (k q, n g)  b1 (k q+4, n g)
+//   C: as for the bf16 shape.
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// x = hi + lo with hi, lo representable in tf32: products hi*hi + hi*lo + lo*hi
+// keep about 21 mantissa bits (fp32-level accuracy from tf32 tensor products).
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    uint32_t h;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(h) : "f"(x));
+    const float r = x - __uint_as_float(h);
+    uint32_t l;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(l) : "f"(r));
+    hi = h;
+    lo = l;
+}
+
 // Four 8x8 b16 matrices; lane l supplies the row address of matrix l/8, row l%8.
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -93,6 +115,16 @@ __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src, 
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
+
+// 32-bit shared-state-space accesses by address (keeps address math 32-bit)
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void report_status(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
