@@ -683,6 +683,19 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
 
 }  // namespace tc
 
+void *tensor_map_encoder() {
+    static void *fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = ptr;
+    }
+    return fn;
+}
+
 bool chunk_tc_supported(const ChunkArgs &a, bool in_bf16) {
     return in_bf16 && a.dk == 128 && a.dv == 128;
 }
@@ -692,18 +705,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
+EncodeTiledFn encode_fn() { return reinterpret_cast<EncodeTiledFn>(tensor_map_encoder()); }
 
 // [T][H][inner] tensor, box of `box_inner` x 1 head x 64 tokens
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int inner, int H, int T,

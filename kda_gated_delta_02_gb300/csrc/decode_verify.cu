@@ -20,6 +20,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -526,7 +527,12 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, cudaStream_t st) {
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t st) {
     if (a.R <= 0) return cudaSuccess;
-    if (a.dk == 128 && a.dv == 128) return launch_verify_t<128>(a, st);
+    if (a.dk == 128 && a.dv == 128) {
+        // the tensor-memory kernel unless KDA_VERIFY_TC=0 asks for this one
+        const char *env = getenv("KDA_VERIFY_TC");
+        if (!(env && env[0] == '0')) return launch_verify_tc(a, st);
+        return launch_verify_t<128>(a, st);
+    }
     if (a.dk == 64 && a.dv == 64) return launch_verify_t<64>(a, st);
     return cudaErrorInvalidValue;
 }

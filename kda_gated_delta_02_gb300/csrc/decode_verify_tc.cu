@@ -1,0 +1,619 @@
+// decode_verify_tc.cu -- fused speculative-decode verify with replay on the
+// sm_103a tensor cores (tcgen05.mma, accumulators in tensor memory), dk = dv = 128.
+//
+// "Noyaux d'inference", section 1 "Le decodage KDA": only the projected inputs
+// of draft tokens are cached; the accepted prefix is replayed on chip, and one
+// kernel runs short conv -> input norm -> gating -> recurrence -> output norm
+// over the replayed tokens, the bonus token and the next draft window, writing
+// back the state reached after the bonus token.
+//
+// One CTA (8 warps; thread (c, half) = channel c, tokens 8 half .. 8 half + 7)
+// owns one (request, head).  The a + 1 + Wd <= 16 tokens form one tile and the
+// recurrence over it is the chunk (WY) form on that tile, with per-channel
+// running decays x_t = prod_{r<=t} e^{g_r} from the window start:
+//   QX = q^ . x, KX = k^ . x, KR = k^ / x,  K~_s = k^_s . x_a / x_s (s <= a)
+//   A[t,s] = b_t KX_t . KR_s (s < t),  B[t,s] = QX_t . KR_s (s <= t)
+//   T = (I + A)^{-1},  U = T diag(b) (V - KX S0)
+//   O = scale (QX S0 + B U) -> RMSNorm over dv,  S_a = Diag(x_a) S0 + K~^T U
+// (U = T diag(b) V - W S0 with W = T diag(b) KX, regrouped so that the only
+// products with S0 are the two 16-row ones.)  Products run transposed with
+// dv (or dk) on the MMA's M = 128:
+//   batch 1   D[j][QX|KX rows]  = S0^T [QX hi|lo ; KX hi|lo]^T      (N = 64, K = dk)
+//             D[QX|KX rows][s]  = [QX hi|lo ; KX hi|lo] [KR hi|lo]^T (N = 32, K = dk)
+//   batch 2   U^T = P^T (T diag b)^T,   P = V - KX S0                (N = 16, K = 16)
+//   batch 3   S = K~^T U                                             (N = 128, K = 16)
+// and O = QX S0 + B U on the CUDA cores in fp32 while batch 3 runs.
+// Operands derived on chip (QX, KX, KR, K~, P, T diag b, U) are split into
+// bf16 hi + lo parts and multiplied as hi*hi + hi*lo + lo*hi, which keeps
+// about 16 mantissa bits; the state is read once as bf16 (exact as an MMA
+// operand) and written back rounded once (nearest even).  The state tile moves
+// between HBM and shared memory by TMA in the 128-byte swizzled layout, which
+// is also the MN-major operand layout of S0^T.
+#include <cuda.h>  // CUtensorMap
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace vtc {
+
+constexpr int D = 128, VT = 16, NT = 256, HT = 8, NR = HT + 3;
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_S0 = 0;       // state bf16 [dk][dv]: two 64-wide swizzled halves [128][128 B]
+constexpr uint32_t OFF_X = 32768;    // QX hi, QX lo, KX hi, KX lo: K-major 64 rows x dk
+constexpr uint32_t OFF_KR = 49152;   // KR hi, KR lo: K-major 32 rows x dk; also the rows 64..127 that
+                                     // the M = 128 product over X reads past X (discarded)
+constexpr uint32_t OFF_RAW = OFF_X;  // before the operands: pre-conv rows [19][q|k|v][128] bf16
+constexpr uint32_t OFF_GR = OFF_X + 19 * 768;  //   and g rows [16][128] bf16, up to 51456
+constexpr uint32_t OFF_TB = 52224;   // after batch 1: T diag(b), 16 rows t, k = s: hi 0-15, lo 16-31
+constexpr uint32_t OFF_AF = 54272;   //   A fp32 [16][17]
+constexpr uint32_t OFF_BF = 55360;   //   B fp32 [16][16] (masked)
+constexpr uint32_t OFF_P = 57344;    // 128 rows; k 0-31: P^T (hi 0-15, lo 16-31) for batch 2, then
+                                     // K~^T (same split) for batch 3; k 32-63: U^T (hi, lo)
+constexpr uint32_t OFF_BETA = 73728; // fp32 [16]
+constexpr uint32_t OFF_RN = 73792;   // fp32 [32]: 1/||q_t||, 1/||k_t||
+constexpr uint32_t OFF_XA = 73920;   // fp32 [128]: x_a per key channel
+constexpr uint32_t OFF_CAR = 74432;  // fp32 [128]: x_7 per channel (decay carried to tokens 8-15)
+constexpr uint32_t OFF_PART = 74944; // fp32 [8][16] per-warp partial sums (input norms)
+constexpr uint32_t OFF_PART2 = 75456;// fp32 [8][8] per-warp partial sums (output norm)
+constexpr uint32_t OFF_BAR = 75712;  // 5 mbarriers: state tile, MMA batches 1-3, row copies
+constexpr uint32_t OFF_TMEM = 75752; // tensor-memory base address
+constexpr uint32_t SMEM_BYTES = 75760 + 1024;  // + alignment slack; three CTAs fit one SM
+
+// tensor-memory columns (128 allocated)
+constexpr uint32_t TM_Q = 0;    // S0^T QX^T: hi tokens in columns 0-15, lo in 16-31
+constexpr uint32_t TM_K = 32;   // S0^T KX^T: hi 32-47, lo 48-63
+constexpr uint32_t TM_AB = 64;  // X KR^T, lanes 0-63 (32 columns)
+constexpr uint32_t TM_U = 96;   // U^T (16 columns)
+constexpr uint32_t TM_S = 0;    // K~^T U (128 columns, batch 3, after all of the above are read)
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+
+struct VtcParams {
+    VerifyArgs a;
+    CUtensorMap ts;  // state [R*H][dk][dv] bf16, box 64 x 128 x 1, 128-byte swizzle
+};
+
+__device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+__device__ __forceinline__ void split2(float x, uint16_t &hi, uint16_t &lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi = __bfloat16_as_ushort(h);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+// hi / lo parts of 8 consecutive values packed as 4 x bf16x2 each
+__device__ __forceinline__ void split8(const float *x, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint16_t h0, l0, h1, l1;
+        split2(x[2 * i], h0, l0);
+        split2(x[2 * i + 1], h1, l1);
+        hi[i] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lo[i] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+}
+// One row of a K-major 128-byte swizzled tile: 16-byte chunk j (elements
+// 8j .. 8j+7 of the row's first 64) sits at chunk j ^ (row & 7).
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t row_base, int row, int j) {
+    return row_base + (uint32_t)(((j ^ (row & 7)) & 7) << 4);
+}
+// 8 values as the hi chunk j and the lo chunk j + 2 of a swizzled row
+__device__ __forceinline__ void store_split8(uint32_t row_base, int row, int j, const float *x) {
+    uint32_t hi[4], lo[4];
+    split8(x, hi, lo);
+    sts128(chunk_addr(row_base, row, j), hi[0], hi[1], hi[2], hi[3]);
+    sts128(chunk_addr(row_base, row, j + 2), lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Transpose-reduce over the warp: N (32, 16 or 8) values per lane in; entry
+// (lane * N / 32) summed over all 32 lanes comes out in every lane that
+// holds that entry.
+template <int N>
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[N], int lane) {
+#pragma unroll
+    for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = 32 / N / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_constant__ VtcParams P) {
+    const VerifyArgs &p = P.a;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t sb4 = sb >> 4;
+    float *sAf = reinterpret_cast<float *>(sm + OFF_AF);
+    float *sBf = reinterpret_cast<float *>(sm + OFF_BF);
+    float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
+    float *sRN = reinterpret_cast<float *>(sm + OFF_RN);
+    float *sXa = reinterpret_cast<float *>(sm + OFF_XA);
+    float *sCar = reinterpret_cast<float *>(sm + OFF_CAR);
+    float *sPart = reinterpret_cast<float *>(sm + OFF_PART);
+    float *sPart2 = reinterpret_cast<float *>(sm + OFF_PART2);
+    const uint32_t bar0 = sb + OFF_BAR;  // state tile
+    const uint32_t bar_raw = bar0 + 32;  // row copies
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // thread (c, hf): channel c of q, k, v (TMEM lane c), tokens 8 hf .. 8 hf + 7
+    const int c = tid & (D - 1), hf = tid >> 7, t0 = HT * hf;
+    const int H = p.H, W = p.W, Wd = p.Wd;
+    const int unit = blockIdx.x;
+    const int h = unit % H, r = unit / H;
+    const int a = p.accepted[r];
+    if (a < 0 || a > Wd) {
+        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_ACCEPTED_LEN);
+        return;
+    }
+    const int ntok = a + 1 + Wd;  // <= 15 (host-checked Wd <= 7), so a <= 7 lies in the first half
+    const int nrows = (W - 1) + ntok;
+    const size_t HD = (size_t)H * D, Cq = 3 * HD;
+    const size_t chq = (size_t)h * D + c;
+
+    // ---------------------------------------------------------------- setup, loads
+    // The state tile arrives by TMA; the pre-conv q|k|v rows of this head (three
+    // 256-byte pieces per row) and the g rows by 256-byte bulk copies spread
+    // over warp 0, into the operand region (rewritten only after the conv).
+    if (tid == 0) {
+        for (int b = 0; b < 5; ++b) umma::mbar_init(bar0 + 8 * b, b == 1 ? 2u : 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        umma::mbar_expect_tx(bar0, 32768u);
+        umma::tma_load_3d(sb + OFF_S0, &P.ts, 0, 0, unit, bar0);
+        umma::tma_load_3d(sb + OFF_S0 + 16384, &P.ts, 64, 0, unit, bar0);
+        umma::mbar_expect_tx(bar_raw, (uint32_t)nrows * 768u + (uint32_t)ntok * 256u);
+    }
+    __syncthreads();  // the barriers are initialised before any thread polls them
+    if (warp == 0) {
+        const unsigned char *tail = reinterpret_cast<const unsigned char *>(p.tail);
+        const unsigned char *cq = reinterpret_cast<const unsigned char *>(p.cached_qkv);
+        const unsigned char *nq = reinterpret_cast<const unsigned char *>(p.new_qkv);
+        const unsigned char *cgp = reinterpret_cast<const unsigned char *>(p.cached_g);
+        const unsigned char *ngp = reinterpret_cast<const unsigned char *>(p.new_g);
+        const int nrc = 3 * nrows, ncp = nrc + ntok;
+        for (int i = lane; i < ncp; i += 32) {
+            const unsigned char *src;
+            uint32_t dst;
+            if (i < nrc) {
+                const int pr = i / 3, part = i - 3 * pr;
+                const unsigned char *row;
+                if (pr < W - 1) row = tail + ((size_t)r * (W - 1) + pr) * Cq * 2;
+                else if (pr - (W - 1) < a) row = cq + ((size_t)r * Wd + (pr - (W - 1))) * Cq * 2;
+                else row = nq + ((size_t)r * (Wd + 1) + (pr - (W - 1) - a)) * Cq * 2;
+                src = row + ((size_t)part * HD + (size_t)h * D) * 2;
+                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u;
+            } else {
+                const int t = i - nrc;
+                src = ((t < a) ? cgp + ((size_t)r * Wd + t) * HD * 2 : ngp + ((size_t)r * (Wd + 1) + (t - a)) * HD * 2) +
+                      (size_t)h * D * 2;
+                dst = sb + OFF_GR + (uint32_t)t * 256u;
+            }
+            umma::bulk_load(dst, src, 256u, bar_raw);
+        }
+        __syncwarp();
+        umma::tmem_alloc(sb + OFF_TMEM, TMEM_COLS);
+    }
+    float braw = 0.f;
+    if (tid < ntok) {
+        const uint16_t *src = (tid < a) ? reinterpret_cast<const uint16_t *>(p.cached_b) + ((size_t)r * Wd + tid) * H
+                                        : reinterpret_cast<const uint16_t *>(p.new_b) + ((size_t)r * (Wd + 1) + (tid - a)) * H;
+        braw = bf2f(src[h]);
+    }
+    float wq[4], wk[4], wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        wq[j] = (j < W) ? p.conv_w[chq * W + j] : 0.f;
+        wk[j] = (j < W) ? p.conv_w[(HD + chq) * W + j] : 0.f;
+        wv[j] = (j < W) ? p.conv_w[(2 * HD + chq) * W + j] : 0.f;
+    }
+    bool ok = __all_sync(0xffffffffu, umma::mbar_wait(bar_raw, 0, WAIT_LIMIT));
+
+    // pre-conv rows t0 .. t0 + 10 of channel c (row i is token i - (W - 1));
+    // rows past the last token were not copied and are never used
+    uint16_t rq[NR], rk[NR], rv[NR], gr[HT];
+    {
+        const uint32_t rb = sb + OFF_RAW + (uint32_t)t0 * 768u + (uint32_t)c * 2u;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            rq[i] = lds16(rb + i * 768u);
+            rk[i] = lds16(rb + i * 768u + 256u);
+            rv[i] = lds16(rb + i * 768u + 512u);
+        }
+        const uint32_t gb = sb + OFF_GR + (uint32_t)t0 * 256u + (uint32_t)c * 2u;
+#pragma unroll
+        for (int j = 0; j < HT; ++j) gr[j] = lds16(gb + j * 256u);
+    }
+    // conv tail write-back: the W-1 most recent pre-conv rows up to the bonus
+    // token (rows a+1 .. a+W-1 <= 10, all in the first half's registers), this
+    // head's channels, bitwise copies; each thread writes only its own channels
+    if (hf == 0 && ok) {
+        uint16_t *tw = reinterpret_cast<uint16_t *>(p.tail);
+#pragma unroll
+        for (int i = 1; i < NR; ++i) {
+            const int m = i - a - 1;
+            if (m >= 0 && m < W - 1) {
+                uint16_t *row = tw + ((size_t)r * (W - 1) + m) * Cq;
+                row[chq] = rq[i];
+                row[chq + HD] = rk[i];
+                row[chq + 2 * HD] = rv[i];
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- conv, gates
+    const bool silu = p.conv_act == KDA_CONV_SILU;
+    float yq[HT], yk[HT], yv[HT];
+#pragma unroll
+    for (int j = 0; j < HT; ++j) {
+        float sq = 0.f, sk = 0.f, sv = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i < W) {
+                sq = fmaf(wq[i], bf2f(rq[j + i]), sq);
+                sk = fmaf(wk[i], bf2f(rk[j + i]), sk);
+                sv = fmaf(wv[i], bf2f(rv[j + i]), sv);
+            }
+        }
+        if (silu) {  // y / (1 + e^{-y}); the fast quotient is 0 where e^{-y} overflows, the limit
+            sq = __fdividef(sq, 1.f + __expf(-sq));
+            sk = __fdividef(sk, 1.f + __expf(-sk));
+            sv = __fdividef(sv, 1.f + __expf(-sv));
+        }
+        const bool live = t0 + j < ntok;
+        yq[j] = live ? sq : 0.f;
+        yk[j] = live ? sk : 0.f;
+        yv[j] = live ? sv : 0.f;
+    }
+    // decay x_t = prod_{r<=t} e^{max(-softplus(g_r), g_min)}; e^{-softplus(g)}
+    // is 1 / (1 + e^g), and the floor commutes with the exponential.  The
+    // second half's products are completed with x_7 after the next barrier.
+    float xd[HT];
+    {
+        const float emin = __expf(p.g_min);
+        float run = 1.f;
+#pragma unroll
+        for (int j = 0; j < HT; ++j) {
+            if (t0 + j < ntok) run *= fmaxf(__fdividef(1.f, 1.f + __expf(bf2f(gr[j]))), emin);
+            xd[j] = run;
+        }
+        if (hf == 0) {
+            sCar[c] = run;
+            float xa0 = run;
+#pragma unroll
+            for (int j = 0; j < HT; ++j)
+                if (j == a) xa0 = xd[j];
+            sXa[c] = xa0;
+        }
+    }
+    if (tid < VT) sBeta[tid] = (tid < ntok) ? 1.f / (1.f + __expf(-braw)) : 0.f;
+
+    // input norms: per-token sums of squares over the D channels
+    {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < HT; ++j) {
+            v[j] = yq[j] * yq[j];
+            v[HT + j] = yk[j] * yk[j];
+        }
+        const float s = warp_transpose_sum<16>(v, lane);
+        if ((lane & 1) == 0) sPart[warp * 16 + (lane >> 1)] = s;
+    }
+    __syncthreads();
+    if (tid < 32) {  // entry tid = (q|k, token): the four warps of that token's half
+        const int t = tid & 15, e = (tid >> 4) * HT + (t & 7), w0 = 4 * (t >> 3);
+        sRN[tid] = rsqrtf(sPart[w0 * 16 + e] + sPart[(w0 + 1) * 16 + e] + sPart[(w0 + 2) * 16 + e] +
+                          sPart[(w0 + 3) * 16 + e] + p.eps_in);
+    }
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *sTmem;
+    const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lane quadrant
+    const float xa = sXa[c];
+    if (hf) {
+        const float car = sCar[c];
+#pragma unroll
+        for (int j = 0; j < HT; ++j) xd[j] *= car;
+    }
+
+    // ---------------------------------------------------------------- operands
+    float kt[HT];
+    {
+        const uint32_t xcol = sb + OFF_X + (uint32_t)(c >> 6) * 8192u + ((uint32_t)(c & 7) << 1);
+        const uint32_t rcol = sb + OFF_KR + (uint32_t)(c >> 6) * 4096u + ((uint32_t)(c & 7) << 1);
+        const int ch = (c & 63) >> 3;
+#pragma unroll
+        for (int j = 0; j < HT; ++j) {
+            const int t = t0 + j;
+            const float qh = yq[j] * sRN[t], kh = yk[j] * sRN[VT + t];
+            const float rx = __frcp_rn(xd[j]);
+            const uint32_t sw = (uint32_t)((ch ^ (j & 7)) << 4);  // row t = t0 + j has t & 7 == j
+            uint16_t hi, lo;
+            split2(qh * xd[j], hi, lo);
+            sts16(xcol + (uint32_t)t * 128u + sw, hi);
+            sts16(xcol + (uint32_t)(16 + t) * 128u + sw, lo);
+            split2(kh * xd[j], hi, lo);
+            sts16(xcol + (uint32_t)(32 + t) * 128u + sw, hi);
+            sts16(xcol + (uint32_t)(48 + t) * 128u + sw, lo);
+            split2(kh * rx, hi, lo);
+            sts16(rcol + (uint32_t)t * 128u + sw, hi);
+            sts16(rcol + (uint32_t)(16 + t) * 128u + sw, lo);
+            kt[j] = (t <= a) ? kh * (xa * rx) : 0.f;
+        }
+    }
+    umma::fence_proxy_async();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 1
+    // thread 0 issues the products with S0 once its tile has landed; thread 32
+    // issues X KR^T at once (two commits to one barrier of count 2)
+    if (tid == 0) {
+        ok = umma::mbar_wait(bar0, 0, WAIT_LIMIT) && ok;
+        if (ok) {
+            umma::fence_after();
+            constexpr uint32_t idqk = umma::idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t kin = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
+                umma::mma(tmem + TM_Q, umma::sdesc4(sb4 + ((OFF_S0 + kk * 2048) >> 4), 16384, 1024),
+                          umma::sdesc4(sb4 + ((OFF_X + kin) >> 4), 16, 1024), idqk, kk > 0 ? 1u : 0u);
+            }
+            umma::commit(bar0 + 8);
+        }
+    } else if (tid == 32 && ok) {
+        umma::fence_after();
+        constexpr uint32_t idab = umma::idesc_bf16(128, 32, 0, 0, 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t kin = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
+            const uint32_t rin = (uint32_t)(kk >> 2) * 4096u + (uint32_t)(kk & 3) * 32u;
+            umma::mma(tmem + TM_AB, umma::sdesc4(sb4 + ((OFF_X + kin) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((OFF_KR + rin) >> 4), 16, 1024), idab, kk > 0 ? 1u : 0u);
+        }
+        umma::commit(bar0 + 8);
+    }
+    // every thread polls the MMA barrier; `ok` stays uniform within a warp
+    // (the TMEM loads are warp-collective) and across the CTA at each barrier
+    ok = __syncthreads_and(ok) != 0;
+    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 8, 0, WAIT_LIMIT));
+    umma::fence_after();
+
+    // ---------------------------------------------------------------- A, B, T, P
+    float qs[HT];
+    if (ok) {
+        float v0[8], v1[8];
+        umma::ld8(tq + TM_Q + t0, v0);
+        umma::ld8(tq + TM_Q + 16 + t0, v1);
+#pragma unroll
+        for (int j = 0; j < HT; ++j) qs[j] = v0[j] + v1[j];
+        // P = V - KX S0 for value column c, tokens t0 .. t0 + 7
+        umma::ld8(tq + TM_K + t0, v0);
+        umma::ld8(tq + TM_K + 16 + t0, v1);
+        float pv[HT];
+#pragma unroll
+        for (int j = 0; j < HT; ++j) pv[j] = yv[j] - (v0[j] + v1[j]);
+        store_split8(sb + OFF_P + (uint32_t)c * 128u, c, hf, pv);
+    }
+    if (ok && warp < 2) {
+        // lane l holds X row 32*warp + l against KR hi (columns 0-15) and KR lo (16-31);
+        // lanes 0-15 are the hi rows, lanes 16-31 the lo rows of the same tokens
+        float v[32];
+        umma::ld32(tq + TM_AB, v);
+        float lh[VT];
+#pragma unroll
+        for (int s = 0; s < VT; ++s) lh[s] = __shfl_down_sync(0xffffffffu, v[s], 16);
+        if (warp == 0) {
+            if (lane < VT) {  // B[t][s], s <= t, fp32
+                const int t = lane;
+#pragma unroll
+                for (int s = 0; s < VT; s += 4) {
+                    float4 b4;
+                    b4.x = (s + 0 <= t) ? (v[s + 0] + v[VT + s + 0]) + lh[s + 0] : 0.f;
+                    b4.y = (s + 1 <= t) ? (v[s + 1] + v[VT + s + 1]) + lh[s + 1] : 0.f;
+                    b4.z = (s + 2 <= t) ? (v[s + 2] + v[VT + s + 2]) + lh[s + 2] : 0.f;
+                    b4.w = (s + 3 <= t) ? (v[s + 3] + v[VT + s + 3]) + lh[s + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(sBf + t * 16 + s) = b4;
+                }
+            }
+        } else {
+            if (lane < VT) {  // A[t][s] = b_t KX_t . KR_s, s < t
+                const int t = lane;
+                const float bt = sBeta[t];
+#pragma unroll
+                for (int s = 0; s < VT; ++s) sAf[t * 17 + s] = (s < t) ? bt * ((v[s] + v[VT + s]) + lh[s]) : 0.f;
+            }
+            __syncwarp();
+            // T = (I + A)^{-1} by forward substitution, one column per lane;
+            // then column cc of T diag(b) into the operand tile
+            if (lane < VT) {
+                const int cc = lane;
+                float col[VT];
+#pragma unroll
+                for (int rr = 0; rr < VT; ++rr) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < rr; ++m) acc = fmaf(sAf[rr * 17 + m], col[m], acc);
+                    col[rr] = (rr == cc) ? 1.f : ((rr < cc) ? 0.f : -acc);
+                }
+                const float bc = sBeta[cc];
+                const uint32_t cb = sb + OFF_TB + ((uint32_t)(cc & 7) << 1);
+                const int ch = cc >> 3;
+#pragma unroll
+                for (int t = 0; t < VT; ++t) {
+                    uint16_t hi, lo;
+                    split2(col[t] * bc, hi, lo);
+                    sts16(cb + (uint32_t)(t * 128 + ((ch ^ (t & 7)) << 4)), hi);
+                    sts16(cb + (uint32_t)(t * 128 + (((2 + ch) ^ (t & 7)) << 4)), lo);
+                }
+            }
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    ok = __syncthreads_and(ok) != 0;
+
+    // ---------------------------------------------------------------- batch 2: U^T
+    if (tid == 0 && ok) {
+        umma::fence_after();
+        constexpr uint32_t idu = umma::idesc_bf16(128, 16, 0, 0, 0);
+        const uint64_t pdh = umma::sdesc4(sb4 + (OFF_P >> 4), 16, 1024), pdl = umma::sdesc4(sb4 + ((OFF_P + 32) >> 4), 16, 1024);
+        const uint64_t tdh = umma::sdesc4(sb4 + (OFF_TB >> 4), 16, 1024), tdl = umma::sdesc4(sb4 + ((OFF_TB + 32) >> 4), 16, 1024);
+        umma::mma(tmem + TM_U, pdh, tdh, idu, 0u);
+        umma::mma(tmem + TM_U, pdh, tdl, idu, 1u);
+        umma::mma(tmem + TM_U, pdl, tdh, idu, 1u);
+        umma::commit(bar0 + 16);
+    }
+    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 16, 0, WAIT_LIMIT));
+    umma::fence_after();
+    float uu[VT];
+    if (ok) {
+        umma::ld16(tq + TM_U, uu);
+        const uint32_t row = sb + OFF_P + (uint32_t)c * 128u;
+        float uh[HT];  // this half's tokens (a register select, not an indexed array)
+#pragma unroll
+        for (int j = 0; j < HT; ++j) uh[j] = hf ? uu[HT + j] : uu[j];
+        store_split8(row, c, 4 + hf, uh);  // U^T, k = 32 + s
+        store_split8(row, c, hf, kt);      // K~^T over P^T (consumed by batch 2)
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    ok = __syncthreads_and(ok) != 0;
+
+    // ---------------------------------------------------------------- batch 3: state
+    if (tid == 0 && ok) {
+        umma::fence_after();
+        constexpr uint32_t ids = umma::idesc_bf16(128, 128, 0, 0, 0);
+        const uint64_t kdh = umma::sdesc4(sb4 + (OFF_P >> 4), 16, 1024), kdl = umma::sdesc4(sb4 + ((OFF_P + 32) >> 4), 16, 1024);
+        const uint64_t udh = umma::sdesc4(sb4 + ((OFF_P + 64) >> 4), 16, 1024);
+        const uint64_t udl = umma::sdesc4(sb4 + ((OFF_P + 96) >> 4), 16, 1024);
+        umma::mma(tmem + TM_S, kdh, udh, ids, 0u);
+        umma::mma(tmem + TM_S, kdh, udl, ids, 1u);
+        umma::mma(tmem + TM_S, kdl, udh, ids, 1u);
+        umma::commit(bar0 + 24);
+    }
+    // outputs while the state product runs: O = scale (QX S0 + B U) in fp32
+    float o[HT];
+    if (ok) {
+#pragma unroll
+        for (int j = 0; j < HT; ++j) {
+            const float *brow = sBf + (t0 + j) * 16;
+            float acc = qs[j];
+#pragma unroll
+            for (int s = 0; s < VT; s += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(brow + s);
+                acc = fmaf(b4.x, uu[s], acc);
+                acc = fmaf(b4.y, uu[s + 1], acc);
+                acc = fmaf(b4.z, uu[s + 2], acc);
+                acc = fmaf(b4.w, uu[s + 3], acc);
+            }
+            o[j] = p.scale * acc;
+        }
+        float s2[HT];
+#pragma unroll
+        for (int j = 0; j < HT; ++j) s2[j] = o[j] * o[j];
+        const float tot = warp_transpose_sum<8>(s2, lane);
+        if ((lane & 3) == 0) sPart2[warp * 8 + (lane >> 2)] = tot;
+    }
+    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 24, 0, WAIT_LIMIT));
+    umma::fence_after();
+
+    // ---------------------------------------------------------------- state write-back
+    // S_a = Diag(x_a) S0 + K~^T U: row dk = c, value columns 64 hf .. 64 hf + 63,
+    // written in place over S0 in the swizzled layout of the TMA store
+    if (ok) {
+        umma::mbar_wait(bar0, 0, WAIT_LIMIT);  // (completed long ago) orders the TMA-written tile
+        const uint32_t rowb = sb + OFF_S0 + (uint32_t)hf * 16384u + (uint32_t)c * 128u;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            float acc[32];
+            umma::ld32(tq + TM_S + 64 * hf + 32 * q2, acc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t ad = chunk_addr(rowb, c, 4 * q2 + j);
+                const uint4 s0 = lds128(ad);
+                const uint32_t w[4] = {s0.x, s0.y, s0.z, s0.w};
+                uint32_t out[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16(w[e]);
+                    out[e] = pack_bf16(fmaf(xa, f.x, acc[8 * j + 2 * e]), fmaf(xa, f.y, acc[8 * j + 2 * e + 1]));
+                }
+                sts128(ad, out[0], out[1], out[2], out[3]);
+            }
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    ok = __syncthreads_and(ok) != 0;
+    if (tid == 0 && ok) {
+        umma::tma_store_3d(&P.ts, 0, 0, unit, sb + OFF_S0);
+        umma::tma_store_3d(&P.ts, 64, 0, unit, sb + OFF_S0 + 16384);
+        umma::bulk_commit();
+    }
+    if (ok) {
+        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(p.o);
+        const float ow = p.out_w[c];
+        const int w0 = 4 * hf;
+#pragma unroll
+        for (int j = 0; j < HT; ++j) {
+            const int t = t0 + j;
+            if (t >= a && t < ntok) {
+                const float tot = sPart2[w0 * 8 + j] + sPart2[(w0 + 1) * 8 + j] + sPart2[(w0 + 2) * 8 + j] +
+                                  sPart2[(w0 + 3) * 8 + j];
+                const float rs = rsqrtf(tot / D + p.eps_out);
+                og[(((size_t)r * (Wd + 1) + (t - a)) * H + h) * D + c] = __float2bfloat16_rn(o[j] * rs * ow);
+            }
+        }
+    } else if (tid == 0) {
+        report_status(p.status, KDA_STATUS_TIMEOUT);
+        umma::mbar_wait(bar_raw, 0, WAIT_LIMIT);  // let the copies land before leaving (bounded)
+        umma::mbar_wait(bar0, 0, WAIT_LIMIT);
+    }
+    if (warp == 0) umma::tmem_dealloc(tmem, TMEM_COLS);
+    if (tid == 0 && ok) umma::bulk_wait_read();
+}
+
+}  // namespace vtc
+
+cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t st) {
+    typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                      CUtensorMapFloatOOBfill);
+    if (a.R <= 0) return cudaSuccess;
+    EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!fn) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(vtc::kda_verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         vtc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    vtc::VtcParams P;
+    memset(&P, 0, sizeof(P));
+    P.a = a;
+    const size_t units = (size_t)a.R * a.H;
+    cuuint64_t dims[3] = {(cuuint64_t)vtc::D, (cuuint64_t)vtc::D, (cuuint64_t)units};
+    cuuint64_t strides[2] = {(cuuint64_t)vtc::D * 2, (cuuint64_t)vtc::D * vtc::D * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)vtc::D, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (fn(&P.ts, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.state, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    vtc::kda_verify_tc_kernel<<<(unsigned)units, vtc::NT, vtc::SMEM_BYTES, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -36,6 +36,9 @@ cudaError_t launch_chunk(const ChunkArgs &a, int units, int dvt, bool in_bf16, c
 // tcgen05 / tensor-memory version of the chunk kernel (dk = dv = 128, bf16).
 bool chunk_tc_supported(const ChunkArgs &a, bool in_bf16);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st);
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), reached through
+// the runtime's entry-point query; null when the driver does not provide it.
+void *tensor_map_encoder();
 
 cudaError_t launch_segment_table(const int32_t *cu_seqlens, int N, int T, int seg_len, int P_max,
                                  int32_t *table, int32_t *seq_first, int32_t *seg_count,
@@ -68,5 +71,7 @@ struct VerifyArgs {
     uint32_t *status;
 };
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t st);
+// tcgen05 / tensor-memory version of the verify kernel (dk = dv = 128).
+cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t st);
 
 }  // namespace kda

@@ -96,8 +96,19 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols));
 }
 
-// 16 / 32 consecutive fp32 columns of this thread's TMEM lane.  The wait is
+// 8 / 16 / 32 consecutive fp32 columns of this thread's TMEM lane.  The wait is
 // part of the same asm statement, so the outputs are valid when it returns.
+__device__ __forceinline__ void ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
 __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -136,9 +147,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst_saddr, const void *tmap
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(mbar_saddr)
         : "memory");
 }
+// Plain (1-D) bulk copy global -> shared of `bytes` (multiple of 16, both
+// addresses 16-byte aligned); completion counted in bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst_saddr, const void *src, uint32_t bytes, uint32_t mbar_saddr) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst_saddr),
+        "l"(src), "r"(bytes), "r"(mbar_saddr)
+        : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar_saddr, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar_saddr), "r"(bytes) : "memory");
 }
+
+// Bulk tensor copy (TMA) of a 3-D box from shared memory to global memory,
+// tracked as a bulk group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2, uint32_t src_saddr) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src_saddr)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until the source shared memory of this thread's bulk groups has been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
 // Store 32 consecutive fp32 columns of this thread's TMEM lane (waits for completion).
 __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
