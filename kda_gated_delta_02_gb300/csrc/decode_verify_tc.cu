@@ -62,7 +62,7 @@ constexpr uint32_t OFF_XA = 73920;   // fp32 [128]: x_a per key channel
 constexpr uint32_t OFF_CAR = 74432;  // fp32 [128]: x_7 per channel (decay carried to tokens 8-15)
 constexpr uint32_t OFF_PART = 74944; // fp32 [8][16] per-warp partial sums (input norms)
 constexpr uint32_t OFF_PART2 = 75456;// fp32 [8][8] per-warp partial sums (output norm)
-constexpr uint32_t OFF_BAR = 75712;  // 5 mbarriers: state tile, MMA batches 1-3, row copies
+constexpr uint32_t OFF_BAR = 75712;  // 4 mbarriers: state tile, MMA batches 1-3
 constexpr uint32_t OFF_TMEM = 75752; // tensor-memory base address
 constexpr uint32_t SMEM_BYTES = 75760 + 1024;  // + alignment slack; three CTAs fit one SM
 
@@ -146,7 +146,6 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     float *sPart = reinterpret_cast<float *>(sm + OFF_PART);
     float *sPart2 = reinterpret_cast<float *>(sm + OFF_PART2);
     const uint32_t bar0 = sb + OFF_BAR;  // state tile
-    const uint32_t bar_raw = bar0 + 32;  // row copies
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,46 +166,44 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
 
     // ---------------------------------------------------------------- setup, loads
     // The state tile arrives by TMA; the pre-conv q|k|v rows of this head (three
-    // 256-byte pieces per row) and the g rows by 256-byte bulk copies spread
-    // over warp 0, into the operand region (rewritten only after the conv).
+    // 256-byte pieces per row) and the g rows by 16-byte cp.async pieces spread
+    // over all threads, into the operand region (rewritten only after the conv).
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) umma::mbar_init(bar0 + 8 * b, b == 1 ? 2u : 1u);
+        for (int b = 0; b < 4; ++b) umma::mbar_init(bar0 + 8 * b, b == 1 ? 2u : 1u);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         umma::mbar_expect_tx(bar0, 32768u);
         umma::tma_load_3d(sb + OFF_S0, &P.ts, 0, 0, unit, bar0);
         umma::tma_load_3d(sb + OFF_S0 + 16384, &P.ts, 64, 0, unit, bar0);
-        umma::mbar_expect_tx(bar_raw, (uint32_t)nrows * 768u + (uint32_t)ntok * 256u);
     }
-    __syncthreads();  // the barriers are initialised before any thread polls them
-    if (warp == 0) {
+    {
         const unsigned char *tail = reinterpret_cast<const unsigned char *>(p.tail);
         const unsigned char *cq = reinterpret_cast<const unsigned char *>(p.cached_qkv);
         const unsigned char *nq = reinterpret_cast<const unsigned char *>(p.new_qkv);
         const unsigned char *cgp = reinterpret_cast<const unsigned char *>(p.cached_g);
         const unsigned char *ngp = reinterpret_cast<const unsigned char *>(p.new_g);
-        const int nrc = 3 * nrows, ncp = nrc + ntok;
-        for (int i = lane; i < ncp; i += 32) {
+        const int nrc = 48 * nrows, ncp = nrc + 16 * ntok;  // 16 pieces per 256-byte row piece
+        for (int i = tid; i < ncp; i += NT) {
             const unsigned char *src;
             uint32_t dst;
             if (i < nrc) {
-                const int pr = i / 3, part = i - 3 * pr;
+                const int pr = i / 48, rem = i - 48 * pr, part = rem >> 4, q = rem & 15;
                 const unsigned char *row;
                 if (pr < W - 1) row = tail + ((size_t)r * (W - 1) + pr) * Cq * 2;
                 else if (pr - (W - 1) < a) row = cq + ((size_t)r * Wd + (pr - (W - 1))) * Cq * 2;
                 else row = nq + ((size_t)r * (Wd + 1) + (pr - (W - 1) - a)) * Cq * 2;
-                src = row + ((size_t)part * HD + (size_t)h * D) * 2;
-                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u;
+                src = row + ((size_t)part * HD + (size_t)h * D) * 2 + 16 * q;
+                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u + 16u * q;
             } else {
-                const int t = i - nrc;
+                const int t = (i - nrc) >> 4, q = (i - nrc) & 15;
                 src = ((t < a) ? cgp + ((size_t)r * Wd + t) * HD * 2 : ngp + ((size_t)r * (Wd + 1) + (t - a)) * HD * 2) +
-                      (size_t)h * D * 2;
-                dst = sb + OFF_GR + (uint32_t)t * 256u;
+                      (size_t)h * D * 2 + 16 * q;
+                dst = sb + OFF_GR + (uint32_t)t * 256u + 16u * q;
             }
-            umma::bulk_load(dst, src, 256u, bar_raw);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
         }
-        __syncwarp();
-        umma::tmem_alloc(sb + OFF_TMEM, TMEM_COLS);
+        cp_async_commit();
     }
+    if (warp == 0) umma::tmem_alloc(sb + OFF_TMEM, TMEM_COLS);
     float braw = 0.f;
     if (tid < ntok) {
         const uint16_t *src = (tid < a) ? reinterpret_cast<const uint16_t *>(p.cached_b) + ((size_t)r * Wd + tid) * H
@@ -220,7 +217,9 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         wk[j] = (j < W) ? p.conv_w[(HD + chq) * W + j] : 0.f;
         wv[j] = (j < W) ? p.conv_w[(2 * HD + chq) * W + j] : 0.f;
     }
-    bool ok = __all_sync(0xffffffffu, umma::mbar_wait(bar_raw, 0, WAIT_LIMIT));
+    cp_async_wait_all();
+    __syncthreads();  // every thread's row pieces are in (and the barriers initialised)
+    bool ok = true;
 
     // pre-conv rows t0 .. t0 + 10 of channel c (row i is token i - (W - 1));
     // rows past the last token were not copied and are never used
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     // conv tail write-back: the W-1 most recent pre-conv rows up to the bonus
     // token (rows a+1 .. a+W-1 <= 10, all in the first half's registers), this
     // head's channels, bitwise copies; each thread writes only its own channels
-    if (hf == 0 && ok) {
+    if (hf == 0) {
         uint16_t *tw = reinterpret_cast<uint16_t *>(p.tail);
 #pragma unroll
         for (int i = 1; i < NR; ++i) {
@@ -580,8 +579,7 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         }
     } else if (tid == 0) {
         report_status(p.status, KDA_STATUS_TIMEOUT);
-        umma::mbar_wait(bar_raw, 0, WAIT_LIMIT);  // let the copies land before leaving (bounded)
-        umma::mbar_wait(bar0, 0, WAIT_LIMIT);
+        umma::mbar_wait(bar0, 0, WAIT_LIMIT);  // let the state copy land before leaving (bounded)
     }
     if (warp == 0) umma::tmem_dealloc(tmem, TMEM_COLS);
     if (tid == 0 && ok) umma::bulk_wait_read();
