@@ -181,25 +181,30 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         const unsigned char *nq = reinterpret_cast<const unsigned char *>(p.new_qkv);
         const unsigned char *cgp = reinterpret_cast<const unsigned char *>(p.cached_g);
         const unsigned char *ngp = reinterpret_cast<const unsigned char *>(p.new_g);
-        const int nrc = 48 * nrows, ncp = nrc + 16 * ntok;  // 16 pieces per 256-byte row piece
-        for (int i = tid; i < ncp; i += NT) {
+        // per-source row bases of this request and head (row pr of the window is
+        // tail row pr, cached row pr - (W-1), or new row pr - (W-1) - a)
+        const size_t rs = Cq * 2, hoff = (size_t)h * D * 2;
+        const unsigned char *tb = tail + (size_t)r * (W - 1) * rs + hoff;
+        const unsigned char *cb = cq + ((size_t)r * Wd - (W - 1)) * rs + hoff;
+        const unsigned char *nb = nq + ((size_t)r * (Wd + 1) - (W - 1) - a) * rs + hoff;
+        const unsigned char *gcb = cgp + (size_t)r * Wd * HD * 2 + hoff;
+        const unsigned char *gnb = ngp + ((size_t)r * (Wd + 1) - a) * HD * 2 + hoff;
+        const int q = tid & 15;  // 16-byte piece within a 256-byte row piece
+        const int nrc = 3 * nrows, ncp = nrc + ntok;
+        for (int i = tid >> 4; i < ncp; i += NT / 16) {
             const unsigned char *src;
             uint32_t dst;
             if (i < nrc) {
-                const int pr = i / 48, rem = i - 48 * pr, part = rem >> 4, q = rem & 15;
-                const unsigned char *row;
-                if (pr < W - 1) row = tail + ((size_t)r * (W - 1) + pr) * Cq * 2;
-                else if (pr - (W - 1) < a) row = cq + ((size_t)r * Wd + (pr - (W - 1))) * Cq * 2;
-                else row = nq + ((size_t)r * (Wd + 1) + (pr - (W - 1) - a)) * Cq * 2;
-                src = row + ((size_t)part * HD + (size_t)h * D) * 2 + 16 * q;
-                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u + 16u * q;
+                const int pr = i / 3, part = i - 3 * pr;
+                const unsigned char *base = (pr < W - 1) ? tb : ((pr - (W - 1) < a) ? cb : nb);
+                src = base + (size_t)pr * rs + (size_t)part * HD * 2;
+                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u;
             } else {
-                const int t = (i - nrc) >> 4, q = (i - nrc) & 15;
-                src = ((t < a) ? cgp + ((size_t)r * Wd + t) * HD * 2 : ngp + ((size_t)r * (Wd + 1) + (t - a)) * HD * 2) +
-                      (size_t)h * D * 2 + 16 * q;
-                dst = sb + OFF_GR + (uint32_t)t * 256u + 16u * q;
+                const int t = i - nrc;
+                src = ((t < a) ? gcb : gnb) + (size_t)t * HD * 2;
+                dst = sb + OFF_GR + (uint32_t)t * 256u;
             }
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16u * q), "l"(src + 16 * q) : "memory");
         }
         cp_async_commit();
     }
@@ -237,20 +242,13 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         for (int j = 0; j < HT; ++j) gr[j] = lds16(gb + j * 256u);
     }
     // conv tail write-back: the W-1 most recent pre-conv rows up to the bonus
-    // token (rows a+1 .. a+W-1 <= 10, all in the first half's registers), this
-    // head's channels, bitwise copies; each thread writes only its own channels
-    if (hf == 0) {
-        uint16_t *tw = reinterpret_cast<uint16_t *>(p.tail);
-#pragma unroll
-        for (int i = 1; i < NR; ++i) {
-            const int m = i - a - 1;
-            if (m >= 0 && m < W - 1) {
-                uint16_t *row = tw + ((size_t)r * (W - 1) + m) * Cq;
-                row[chq] = rq[i];
-                row[chq + HD] = rk[i];
-                row[chq + 2 * HD] = rv[i];
-            }
-        }
+    // token (window rows a+1 .. a+W-1), this head's q|k|v pieces, bitwise, as
+    // 16-byte copies from the row region; every tail row was read above
+    if (tid < 48 * (W - 1)) {
+        const int m = tid / 48, rem = tid - 48 * m, part = rem >> 4, q = rem & 15;
+        const uint4 v = lds128(sb + OFF_RAW + (uint32_t)(a + 1 + m) * 768u + (uint32_t)part * 256u + 16u * q);
+        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.tail) +
+                                   (((size_t)r * (W - 1) + m) * Cq + (size_t)part * HD + (size_t)h * D) * 2 + 16 * q) = v;
     }
 
     // ---------------------------------------------------------------- conv, gates
@@ -385,10 +383,11 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         }
         umma::commit(bar0 + 8);
     }
-    // every thread polls the MMA barrier; `ok` stays uniform within a warp
-    // (the TMEM loads are warp-collective) and across the CTA at each barrier
+    // thread 0 polls the MMA barrier (both commits); a CTA barrier releases
+    // the rest, so `ok` is uniform across the CTA (the TMEM loads are
+    // warp-collective)
+    if (tid == 0) ok = ok && umma::mbar_wait(bar0 + 8, 0, WAIT_LIMIT);
     ok = __syncthreads_and(ok) != 0;
-    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 8, 0, WAIT_LIMIT));
     umma::fence_after();
 
     // ---------------------------------------------------------------- A, B, T, P
@@ -475,8 +474,9 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         umma::mma(tmem + TM_U, pdh, tdl, idu, 1u);
         umma::mma(tmem + TM_U, pdl, tdh, idu, 1u);
         umma::commit(bar0 + 16);
+        ok = umma::mbar_wait(bar0 + 16, 0, WAIT_LIMIT);
     }
-    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 16, 0, WAIT_LIMIT));
+    ok = __syncthreads_and(ok) != 0;
     umma::fence_after();
     float uu[VT];
     if (ok) {
@@ -527,7 +527,8 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         const float tot = warp_transpose_sum<8>(s2, lane);
         if ((lane & 3) == 0) sPart2[warp * 8 + (lane >> 2)] = tot;
     }
-    ok = __all_sync(0xffffffffu, ok && umma::mbar_wait(bar0 + 24, 0, WAIT_LIMIT));
+    if (tid == 0) ok = ok && umma::mbar_wait(bar0 + 24, 0, WAIT_LIMIT);
+    ok = __syncthreads_and(ok) != 0;
     umma::fence_after();
 
     // ---------------------------------------------------------------- state write-back
