@@ -49,8 +49,8 @@ constexpr uint32_t OFF_S0 = 0;       // state bf16 [dk][dv]: two 64-wide swizzle
 constexpr uint32_t OFF_X = 32768;    // QX hi, QX lo, KX hi, KX lo: K-major 64 rows x dk
 constexpr uint32_t OFF_KR = 49152;   // KR hi, KR lo: K-major 32 rows x dk; also the rows 64..127 that
                                      // the M = 128 product over X reads past X (discarded)
-constexpr uint32_t OFF_RAW = OFF_X;  // before the operands: pre-conv rows [19][q|k|v][128] bf16
-constexpr uint32_t OFF_GR = OFF_X + 19 * 768;  //   and g rows [16][128] bf16, up to 51456
+constexpr uint32_t OFF_RAW = OFF_X;  // before the operands: pre-conv rows [<= 18][q|k|v][128] bf16
+constexpr uint32_t OFF_GR = OFF_X + 18 * 768;  //   and g rows [<= 15][128] bf16, up to 50432
 constexpr uint32_t OFF_TB = 52224;   // after batch 1: T diag(b), 16 rows t, k = s: hi 0-15, lo 16-31
 constexpr uint32_t OFF_AF = 54272;   //   A fp32 [16][17]
 constexpr uint32_t OFF_BF = 55360;   //   B fp32 [16][16] (masked)
@@ -62,7 +62,7 @@ constexpr uint32_t OFF_XA = 73920;   // fp32 [128]: x_a per key channel
 constexpr uint32_t OFF_CAR = 74432;  // fp32 [128]: x_7 per channel (decay carried to tokens 8-15)
 constexpr uint32_t OFF_PART = 74944; // fp32 [8][16] per-warp partial sums (input norms)
 constexpr uint32_t OFF_PART2 = 75456;// fp32 [8][8] per-warp partial sums (output norm)
-constexpr uint32_t OFF_BAR = 75712;  // 4 mbarriers: state tile, MMA batches 1-3
+constexpr uint32_t OFF_BAR = 75712;  // 5 mbarriers: state tile, MMA batches 1-3, rows
 constexpr uint32_t OFF_TMEM = 75752; // tensor-memory base address
 constexpr uint32_t SMEM_BYTES = 75760 + 1024;  // + alignment slack; three CTAs fit one SM
 
@@ -77,7 +77,9 @@ constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
 struct VtcParams {
     VerifyArgs a;
-    CUtensorMap ts;  // state [R*H][dk][dv] bf16, box 64 x 128 x 1, 128-byte swizzle
+    CUtensorMap ts;            // state [R*H][dk][dv] bf16, box 64 x 128 x 1, 128-byte swizzle
+    CUtensorMap tt, tc, tn;    // tail / cached / new q|k|v rows as [rows][3][H][128], box 128 x 1 x 3 x n
+    CUtensorMap tgc, tgn;      // cached / new g rows as [rows][H][128], box 128 x 1 x n
 };
 
 __device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
@@ -165,48 +167,26 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     const size_t chq = (size_t)h * D + c;
 
     // ---------------------------------------------------------------- setup, loads
-    // The state tile arrives by TMA; the pre-conv q|k|v rows of this head (three
-    // 256-byte pieces per row) and the g rows by 16-byte cp.async pieces spread
-    // over all threads, into the operand region (rewritten only after the conv).
+    // One thread starts every copy of the unit: the state tile by TMA, and the
+    // window's pre-conv q|k|v rows of this head and its g rows as whole boxes
+    // (tail rows, all Wd cached rows, the Wd + 1 new rows) into the row region:
+    // window row pr sits at row region pr when pr < W-1+a, else pr + Wd - a
+    // (cached rows a .. Wd-1 are copied but not used).
+    const uint32_t bar_raw = bar0 + 32;
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) umma::mbar_init(bar0 + 8 * b, b == 1 ? 2u : 1u);
+        for (int b = 0; b < 5; ++b) umma::mbar_init(bar0 + 8 * b, b == 1 ? 2u : 1u);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         umma::mbar_expect_tx(bar0, 32768u);
         umma::tma_load_3d(sb + OFF_S0, &P.ts, 0, 0, unit, bar0);
         umma::tma_load_3d(sb + OFF_S0 + 16384, &P.ts, 64, 0, unit, bar0);
-    }
-    {
-        const unsigned char *tail = reinterpret_cast<const unsigned char *>(p.tail);
-        const unsigned char *cq = reinterpret_cast<const unsigned char *>(p.cached_qkv);
-        const unsigned char *nq = reinterpret_cast<const unsigned char *>(p.new_qkv);
-        const unsigned char *cgp = reinterpret_cast<const unsigned char *>(p.cached_g);
-        const unsigned char *ngp = reinterpret_cast<const unsigned char *>(p.new_g);
-        // per-source row bases of this request and head (row pr of the window is
-        // tail row pr, cached row pr - (W-1), or new row pr - (W-1) - a)
-        const size_t rs = Cq * 2, hoff = (size_t)h * D * 2;
-        const unsigned char *tb = tail + (size_t)r * (W - 1) * rs + hoff;
-        const unsigned char *cb = cq + ((size_t)r * Wd - (W - 1)) * rs + hoff;
-        const unsigned char *nb = nq + ((size_t)r * (Wd + 1) - (W - 1) - a) * rs + hoff;
-        const unsigned char *gcb = cgp + (size_t)r * Wd * HD * 2 + hoff;
-        const unsigned char *gnb = ngp + ((size_t)r * (Wd + 1) - a) * HD * 2 + hoff;
-        const int q = tid & 15;  // 16-byte piece within a 256-byte row piece
-        const int nrc = 3 * nrows, ncp = nrc + ntok;
-        for (int i = tid >> 4; i < ncp; i += NT / 16) {
-            const unsigned char *src;
-            uint32_t dst;
-            if (i < nrc) {
-                const int pr = i / 3, part = i - 3 * pr;
-                const unsigned char *base = (pr < W - 1) ? tb : ((pr - (W - 1) < a) ? cb : nb);
-                src = base + (size_t)pr * rs + (size_t)part * HD * 2;
-                dst = sb + OFF_RAW + (uint32_t)pr * 768u + (uint32_t)part * 256u;
-            } else {
-                const int t = i - nrc;
-                src = ((t < a) ? gcb : gnb) + (size_t)t * HD * 2;
-                dst = sb + OFF_GR + (uint32_t)t * 256u;
-            }
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16u * q), "l"(src + 16 * q) : "memory");
+        umma::mbar_expect_tx(bar_raw, (uint32_t)(W - 1 + 2 * Wd + 1) * 768u + (uint32_t)(2 * Wd + 1) * 256u);
+        if (W > 1) umma::tma_load_4d(sb + OFF_RAW, &P.tt, 0, h, 0, r * (W - 1), bar_raw);
+        if (Wd > 0) {
+            umma::tma_load_4d(sb + OFF_RAW + (uint32_t)(W - 1) * 768u, &P.tc, 0, h, 0, r * Wd, bar_raw);
+            umma::tma_load_3d(sb + OFF_GR, &P.tgc, 0, h, r * Wd, bar_raw);
         }
-        cp_async_commit();
+        umma::tma_load_4d(sb + OFF_RAW + (uint32_t)(W - 1 + Wd) * 768u, &P.tn, 0, h, 0, r * (Wd + 1), bar_raw);
+        umma::tma_load_3d(sb + OFF_GR + (uint32_t)Wd * 256u, &P.tgn, 0, h, r * (Wd + 1), bar_raw);
     }
     if (warp == 0) umma::tmem_alloc(sb + OFF_TMEM, TMEM_COLS);
     float braw = 0.f;
@@ -222,31 +202,38 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         wk[j] = (j < W) ? p.conv_w[(HD + chq) * W + j] : 0.f;
         wv[j] = (j < W) ? p.conv_w[(2 * HD + chq) * W + j] : 0.f;
     }
-    cp_async_wait_all();
-    __syncthreads();  // every thread's row pieces are in (and the barriers initialised)
     bool ok = true;
+    if (tid == 0) ok = umma::mbar_wait(bar_raw, 0, WAIT_LIMIT);
+    ok = __syncthreads_and(ok) != 0;  // the rows are in (and the barriers initialised)
 
-    // pre-conv rows t0 .. t0 + 10 of channel c (row i is token i - (W - 1));
+    // pre-conv window rows t0 .. t0 + 10 of channel c (row i is token i - (W - 1));
     // rows past the last token were not copied and are never used
     uint16_t rq[NR], rk[NR], rv[NR], gr[HT];
     {
-        const uint32_t rb = sb + OFF_RAW + (uint32_t)t0 * 768u + (uint32_t)c * 2u;
+        const int split = W - 1 + a, shift = Wd - a;  // new rows sit shift rows further on
+        const uint32_t rb = sb + OFF_RAW + (uint32_t)c * 2u;
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
-            rq[i] = lds16(rb + i * 768u);
-            rk[i] = lds16(rb + i * 768u + 256u);
-            rv[i] = lds16(rb + i * 768u + 512u);
+            const int pr = t0 + i;
+            const uint32_t ad = rb + (uint32_t)(pr + (pr >= split ? shift : 0)) * 768u;
+            rq[i] = lds16(ad);
+            rk[i] = lds16(ad + 256u);
+            rv[i] = lds16(ad + 512u);
         }
-        const uint32_t gb = sb + OFF_GR + (uint32_t)t0 * 256u + (uint32_t)c * 2u;
+        const uint32_t gb = sb + OFF_GR + (uint32_t)c * 2u;
 #pragma unroll
-        for (int j = 0; j < HT; ++j) gr[j] = lds16(gb + j * 256u);
+        for (int j = 0; j < HT; ++j) {
+            const int t = t0 + j;
+            gr[j] = lds16(gb + (uint32_t)(t + (t >= a ? shift : 0)) * 256u);
+        }
     }
     // conv tail write-back: the W-1 most recent pre-conv rows up to the bonus
     // token (window rows a+1 .. a+W-1), this head's q|k|v pieces, bitwise, as
     // 16-byte copies from the row region; every tail row was read above
-    if (tid < 48 * (W - 1)) {
+    if (ok && tid < 48 * (W - 1)) {
         const int m = tid / 48, rem = tid - 48 * m, part = rem >> 4, q = rem & 15;
-        const uint4 v = lds128(sb + OFF_RAW + (uint32_t)(a + 1 + m) * 768u + (uint32_t)part * 256u + 16u * q);
+        const int pr = a + 1 + m, row = pr + (pr >= W - 1 + a ? Wd - a : 0);
+        const uint4 v = lds128(sb + OFF_RAW + (uint32_t)row * 768u + (uint32_t)part * 256u + 16u * q);
         *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.tail) +
                                    (((size_t)r * (W - 1) + m) * Cq + (size_t)part * HD + (size_t)h * D) * 2 + 16 * q) = v;
     }
@@ -580,7 +567,8 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         }
     } else if (tid == 0) {
         report_status(p.status, KDA_STATUS_TIMEOUT);
-        umma::mbar_wait(bar0, 0, WAIT_LIMIT);  // let the state copy land before leaving (bounded)
+        umma::mbar_wait(bar_raw, 0, WAIT_LIMIT);  // let the copies land before leaving (bounded)
+        umma::mbar_wait(bar0, 0, WAIT_LIMIT);
     }
     if (warp == 0) umma::tmem_dealloc(tmem, TMEM_COLS);
     if (tid == 0 && ok) umma::bulk_wait_read();
@@ -611,6 +599,34 @@ cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t st) {
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // q|k|v rows [rows][Cq], Cq = 3 * H * 128, seen as [rows][3][H][128]; g rows [rows][H][128]
+    const cuuint64_t H = (cuuint64_t)a.H, hb = (cuuint64_t)vtc::D * 2;
+    auto rows_map = [&](CUtensorMap *m, const void *base, cuuint64_t rows, cuuint32_t box_rows) {
+        cuuint64_t d[4] = {(cuuint64_t)vtc::D, H, 3, rows};
+        cuuint64_t st[3] = {hb, H * hb, 3 * H * hb};
+        cuuint32_t bx[4] = {(cuuint32_t)vtc::D, 1u, 3u, box_rows};
+        cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    auto g_map = [&](CUtensorMap *m, const void *base, cuuint64_t rows, cuuint32_t box_rows) {
+        cuuint64_t d[3] = {(cuuint64_t)vtc::D, H, rows};
+        cuuint64_t st[2] = {hb, H * hb};
+        cuuint32_t bx[3] = {(cuuint32_t)vtc::D, 1u, box_rows};
+        cuuint32_t es[3] = {1u, 1u, 1u};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    const cuuint64_t R = (cuuint64_t)a.R;
+    bool ok = rows_map(&P.tn, a.new_qkv, R * (a.Wd + 1), (cuuint32_t)(a.Wd + 1)) &&
+              g_map(&P.tgn, a.new_g, R * (a.Wd + 1), (cuuint32_t)(a.Wd + 1));
+    if (ok && a.W > 1) ok = rows_map(&P.tt, a.tail, R * (a.W - 1), (cuuint32_t)(a.W - 1));
+    if (ok && a.Wd > 0)
+        ok = rows_map(&P.tc, a.cached_qkv, R * a.Wd, (cuuint32_t)a.Wd) &&
+             g_map(&P.tgc, a.cached_g, R * a.Wd, (cuuint32_t)a.Wd);
+    if (!ok) return cudaErrorInvalidValue;
     vtc::kda_verify_tc_kernel<<<(unsigned)units, vtc::NT, vtc::SMEM_BYTES, st>>>(P);
     return cudaGetLastError();
 }

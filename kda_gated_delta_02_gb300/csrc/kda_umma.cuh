@@ -155,6 +155,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst_saddr, const void *src, u
         "l"(src), "r"(bytes), "r"(mbar_saddr)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(uint32_t dst_saddr, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t mbar_saddr) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(
+            dst_saddr),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar_saddr)
+        : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar_saddr, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar_saddr), "r"(bytes) : "memory");
 }
