@@ -48,7 +48,8 @@ def load_peaks():
 
 def kernel_traffic(kernel_key, T):
     """DRAM bytes per launch of `kernel_key` from the committed ncu summary,
-    scaled to T tokens, or None when the kernel source changed since."""
+    scaled to T tokens (requests, for the verify kernel), or None when the
+    kernel source changed since."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -56,7 +57,7 @@ def kernel_traffic(kernel_key, T):
         with open(os.path.join(ROOT, rec["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
                 return None
-        return rec["traffic_bytes_captured"] * T / rec["captured_T"]
+        return rec["traffic_bytes_captured"] * T / rec.get("captured_T", rec.get("captured_R"))
     except Exception:
         return None
 
@@ -326,6 +327,8 @@ def main(argv=None):
     # ------------------------------------------------------------ verify-replay
     if "verify" in only:
         vw = synth.VERIFY
+        verify_kernel = ("kda_verify_kernel<128>" if os.environ.get("KDA_VERIFY_TC", "1") == "0"
+                         else "kda_verify_tc_kernel")
         d = synth.make_decode(vw, device="cuda")
         st, tl = d["state"].clone(), d["tail"].clone()
         ov = torch.empty((vw.R, vw.Wd + 1, vw.H, vw.dv), dtype=torch.bfloat16, device="cuda")
@@ -348,6 +351,7 @@ def main(argv=None):
                          "total_gbs": ws * total_bytes / (vms * 1e-3) / 1e9,
                          "frac_hbm": (total_bytes / (vms * 1e-3) / 1e9) / peaks["hbm_gbs"],
                          "bytes_per_launch": total_bytes, "state_bytes_per_launch": state_bytes,
+                         "kernel": verify_kernel, "traffic": kernel_traffic(verify_kernel, vw.R),
                          "requests_per_s": ws * vw.R / (vms * 1e-3)}
         launches += K
         del d, st, tl, ov
