@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) umma::mbar_init(bar0 + 8 * b, 1);
+        for (int b = 0; b < 6; ++b) umma::mbar_init(bar0 + 8 * b, b == 0 ? 4u : 1u);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 0) umma::tmem_alloc(sb + OFF_TMEM, 512);
@@ -352,19 +352,19 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         __syncthreads();
 
         // ------------------------------------------------------------ step 3: A and B tiles
-        if (tid == 0) {
+        // one issuing thread per column block i (lane 0 of warps 0-3), each
+        // committing to the same barrier (arrival count 4)
+        if (lane == 0 && warp < 4) {
             umma::fence_after();
             constexpr uint32_t id = umma::idesc_bf16(128, 32, 0, 0, 0);
+            const int i = warp;
+            const uint32_t rows = 16 * (i + 1);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t rows = 16 * (i + 1);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                    const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + un_r(i) + kb * rows * 128 + kin) >> 4), 16, 1024);
-                    const uint64_t b = umma::sdesc4(sb4 + ((OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin) >> 4), 16, 1024);
-                    umma::mma(tmem + TM_AB + 32 * i, a, b, id, ks > 0 ? 1u : 0u);
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + un_r(i) + kb * rows * 128 + kin) >> 4), 16, 1024);
+                const uint64_t b = umma::sdesc4(sb4 + ((OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin) >> 4), 16, 1024);
+                umma::mma(tmem + TM_AB + 32 * i, a, b, id, ks > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 0);
         }
