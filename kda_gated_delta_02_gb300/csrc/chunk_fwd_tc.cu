@@ -12,7 +12,7 @@
 //   W^T        D[i][t]   = (K e^gamma)^T  (T diag b)^T
 //   U~^T       D[j][t]   = V^T (T diag b)^T,      then  -= S^T W^T   ->  U^T
 //   O^T        D[j][t]   = S^T Q~^T + U^T B^T
-//   S update   S^T <- Diag-cols(e^{gamma_63}) S^T + U^T K~
+//   S update   S^T <- Diag-cols(e^{gamma_63}) S^T (in place), then += U^T K~ by the MMA
 // with R_i[s] = k_s y_s c_{i,j(s)} (1/delta_i on the diagonal block) and
 // L[t] = k_t x_t or q_t x_t: the per-16-token-block anchoring that the
 // g >= -5 floor makes overflow-free ("Noyaux KDA et FlashKDA", "Le role de la
@@ -65,9 +65,9 @@ constexpr uint32_t SMEM_BYTES = 228160 + 1024;  // + alignment slack
 constexpr int LDF = 68;               // fp32 [64][68] row stride
 
 // tensor-memory columns
-//   S^T (fp32, the state, resident for the whole walk) | A/B tiles, later the
-//   U^T K~ update | W^T | U^T | O^T
-constexpr uint32_t TM_ST = 0, TM_AB = 128, TM_S = 128, TM_W = 256, TM_U = 320, TM_O = 384;
+//   S^T (fp32, the state, resident for the whole walk; the U^T K~ update
+//   accumulates onto it) | A/B tiles | W^T | U^T | O^T
+constexpr uint32_t TM_ST = 0, TM_AB = 128, TM_W = 256, TM_U = 320, TM_O = 384;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
 __device__ __forceinline__ void st_bf16x2(unsigned char *base, uint32_t off, float a, float b) {
@@ -538,6 +538,9 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_W + umma::mnmaj(16 * cg + 8, i, 1)) =
                 make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                            pack_bf16(v[14], v[15]));
+            // S^T as the bf16 operand of step 8, and the resident state decayed to the
+            // chunk end in place, Diag-cols(e^{gamma_63}) S^T, onto which step 10
+            // accumulates U^T K~
             float Sreg[32];
             umma::ld32(tq + TM_ST + 32 * cg, Sreg);
 #pragma unroll
@@ -549,6 +552,15 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 pk.w = pack_bf16(Sreg[c + 6], Sreg[c + 7]);
                 *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_ST + umma::kmaj(jrow, 32 * cg + c, 128)) = pk;
             }
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
+                Sreg[c + 0] *= gm.x;
+                Sreg[c + 1] *= gm.y;
+                Sreg[c + 2] *= gm.z;
+                Sreg[c + 3] *= gm.w;
+            }
+            umma::st32(tq + TM_ST + 32 * cg, Sreg);
         }
         umma::fence_proxy_async();
         umma::fence_before();
@@ -601,7 +613,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_UT + ks * 32) >> 4), 16, 1024);
                 if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_BM + ks * 2048) >> 4), 1024, 1024), ido, 1u);
-                umma::mma(tmem + TM_S, a, umma::sdesc4(sb4 + ((OFF_KT + ks * 4096) >> 4), 1024, 2048), ids, ks > 0 ? 1u : 0u);
+                umma::mma(tmem + TM_ST, a, umma::sdesc4(sb4 + ((OFF_KT + ks * 4096) >> 4), 1024, 2048), ids, 1u);
             }
             umma::commit(bar0 + 24);
         }
@@ -619,20 +631,6 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             for (int tt = 0; tt < 16; ++tt)
                 *reinterpret_cast<__nv_bfloat16 *>(ostage + (16 * cg + tt) * 256 + jrow * 2) =
                     __float2bfloat16_rn(p.scale * v[tt]);
-        }
-        {
-            float v[32], Sreg[32];
-            umma::ld32(tq + TM_S + 32 * cg, v);
-            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
-                Sreg[c + 0] = fmaf(gm.x, Sreg[c + 0], v[c + 0]);
-                Sreg[c + 1] = fmaf(gm.y, Sreg[c + 1], v[c + 1]);
-                Sreg[c + 2] = fmaf(gm.z, Sreg[c + 2], v[c + 2]);
-                Sreg[c + 3] = fmaf(gm.w, Sreg[c + 3], v[c + 3]);
-            }
-            umma::st32(tq + TM_ST + 32 * cg, Sreg);
         }
         umma::fence_before();
         if (__syncthreads_or(timed_out)) break;
