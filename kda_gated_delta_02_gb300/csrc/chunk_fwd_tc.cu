@@ -45,9 +45,9 @@ constexpr uint32_t OFF_UN = 81920;    // union, 73728 bytes:
 constexpr uint32_t UN_L = 0;          //   L (K-major 128 x 128)         steps 2-3
 // R_i (16(i+1) rows, K-major) at 32768 + 4096 * i(i+1)/2: 32768, 36864, 45056, 57344
 __host__ __device__ constexpr uint32_t un_r(int i) { return 32768u + 4096u * (uint32_t)(i * (i + 1) / 2); }
-constexpr uint32_t UN_AF = 0;         //   A fp32 [64][68]                steps 4-5
-constexpr uint32_t UN_TF = 17408;     //   T fp32 [64][68]
-constexpr uint32_t UN_ST = 0;         //   S^T bf16 (K-major 128 x 128)   steps 7-8
+constexpr uint32_t UN_AF = 34816;     //   A fp32 [64][68]                steps 4-5
+constexpr uint32_t UN_TF = 52224;     //   T fp32 [64][68]
+constexpr uint32_t UN_ST = 0;         //   S^T bf16 (K-major 128 x 128)   steps 4-8
 constexpr uint32_t UN_W = 32768;      //   W (MN-major: 128 k-rows i x 64 t)
 constexpr uint32_t UN_UT = 49152;     //   U^T (K-major 128 x 64)         steps 9-10
 constexpr uint32_t OFF_KG = 155648;   // K e^gamma, MN-major (s x dk)
@@ -375,7 +375,36 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         timed_out |= !umma::mbar_wait(bar0 + 0, phase, WAIT_LIMIT);
         umma::fence_after();
 
+        // S^T (rows of this thread's TMEM lane, columns 32 cg ..) as the bf16
+        // operand of steps 6 and 8, and the resident state decayed to the chunk
+        // end in place, Diag-cols(e^{gamma_63}) S^T, onto which step 10 accumulates
+        // U^T K~.  Lane quadrants 2-3 do it in step 4, 0-1 in step 5.
+        auto copy_decay_state = [&]() {
+            float Sreg[32];
+            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(Sreg[c + 0], Sreg[c + 1]);
+                pk.y = pack_bf16(Sreg[c + 2], Sreg[c + 3]);
+                pk.z = pack_bf16(Sreg[c + 4], Sreg[c + 5]);
+                pk.w = pack_bf16(Sreg[c + 6], Sreg[c + 7]);
+                *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_ST + umma::kmaj(jrow, 32 * cg + c, 128)) = pk;
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
+                Sreg[c + 0] *= gm.x;
+                Sreg[c + 1] *= gm.y;
+                Sreg[c + 2] *= gm.z;
+                Sreg[c + 3] *= gm.w;
+            }
+            umma::st32(tq + TM_ST + 32 * cg, Sreg);
+            umma::fence_before();
+        };
+
         // ------------------------------------------------------------ step 4: A (fp32, scaled by b_t) and B (bf16)
+        if (qd >= 2) copy_decay_state();
         {
             float *sAf = reinterpret_cast<float *>(sm + OFF_UN + UN_AF);
             if (qd < 2) {
@@ -407,9 +436,10 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             const float *sAf = reinterpret_cast<const float *>(sm + OFF_UN + UN_AF);
             float *sTf = reinterpret_cast<float *>(sm + OFF_UN + UN_TF);
             // diagonal 16 x 16 blocks, right-looking substitution with one column
-            // per lane in registers: lanes 0-15 of warp w -> block 2w, 16-31 -> 2w+1
-            if (warp < 2) {
-                const int i = 2 * warp + (lane >> 4), c = lane & 15;
+            // per lane in registers: lanes 0-15 of warp 2 + w -> block 2w, 16-31 -> 2w+1
+            if (qd < 2) copy_decay_state();
+            if (warp == 2 || warp == 3) {
+                const int i = 2 * (warp - 2) + (lane >> 4), c = lane & 15;
                 const float *Ab = sAf + (16 * i) * LDF + 16 * i;
                 float acc[16];
 #pragma unroll
@@ -518,6 +548,17 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                     umma::mma(tmem + TM_U, umma::sdesc4(sb4 + ((OFF_V + ks * 2048) >> 4), 8192, 1024), b, id, ks > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 8);
+            // S^T Q~^T needs only the state copy and Q~: it runs behind W / U~ and
+            // completes under step 8's commit
+            if (need_q) {
+                constexpr uint32_t idq = umma::idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                    umma::mma(tmem + TM_O, umma::sdesc4(sb4 + ((OFF_UN + UN_ST + kb * 16384 + kin) >> 4), 16, 1024),
+                              umma::sdesc4(sb4 + ((OFF_QT + kb * 8192 + kin) >> 4), 16, 1024), idq, ks > 0 ? 1u : 0u);
+                }
+            }
         }
         timed_out |= !umma::mbar_wait(bar0 + 8, phase, WAIT_LIMIT);
         umma::fence_after();
@@ -527,7 +568,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             if (tid < CH) beta_next = load_beta(tc + CH);
         }
 
-        // ------------------------------------------------------------ step 7: W (bf16) and S^T (bf16) operands
+        // ------------------------------------------------------------ step 7: W (bf16) operand
         {
             float v[16];
             umma::ld16(tq + TM_W + 16 * cg, v);
@@ -538,46 +579,19 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_W + umma::mnmaj(16 * cg + 8, i, 1)) =
                 make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                            pack_bf16(v[14], v[15]));
-            // S^T as the bf16 operand of step 8, and the resident state decayed to the
-            // chunk end in place, Diag-cols(e^{gamma_63}) S^T, onto which step 10
-            // accumulates U^T K~
-            float Sreg[32];
-            umma::ld32(tq + TM_ST + 32 * cg, Sreg);
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-                uint4 pk;
-                pk.x = pack_bf16(Sreg[c + 0], Sreg[c + 1]);
-                pk.y = pack_bf16(Sreg[c + 2], Sreg[c + 3]);
-                pk.z = pack_bf16(Sreg[c + 4], Sreg[c + 5]);
-                pk.w = pack_bf16(Sreg[c + 6], Sreg[c + 7]);
-                *reinterpret_cast<uint4 *>(sm + OFF_UN + UN_ST + umma::kmaj(jrow, 32 * cg + c, 128)) = pk;
-            }
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 gm = *reinterpret_cast<const float4 *>(sGam + 32 * cg + c);
-                Sreg[c + 0] *= gm.x;
-                Sreg[c + 1] *= gm.y;
-                Sreg[c + 2] *= gm.z;
-                Sreg[c + 3] *= gm.w;
-            }
-            umma::st32(tq + TM_ST + 32 * cg, Sreg);
         }
         umma::fence_proxy_async();
         umma::fence_before();
         if (__syncthreads_or(timed_out)) break;
 
-        // ------------------------------------------------------------ step 8: S^T Q~^T and U~^T - S^T W^T
+        // ------------------------------------------------------------ step 8: U~^T - S^T W^T
         if (tid == 0) {
             umma::fence_after();
-            constexpr uint32_t idq = umma::idesc_bf16(128, 64, 0, 0, 0);
             constexpr uint32_t idw = umma::idesc_bf16(128, 64, 0, 1, 1);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
                 const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_ST + kb * 16384 + kin) >> 4), 16, 1024);
-                if (need_q)
-                    umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_QT + kb * 8192 + kin) >> 4), 16, 1024), idq,
-                              ks > 0 ? 1u : 0u);
                 umma::mma(tmem + TM_U, a, umma::sdesc4(sb4 + ((OFF_UN + UN_W + ks * 2048) >> 4), 1024, 1024), idw,
                           (has_v || ks > 0) ? 1u : 0u);
             }
