@@ -4,6 +4,8 @@ One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
 32K-token, 96-head, d=128 bf16 workload, inputs resident in HBM, one
 kda_chunk_fwd launch per step.  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
+  "decode": the same kernel as single-token decode (window 0) on 256 x 96
+  "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
   "cp":     1M-token, 12-head prefill with the context-parallel schedule
   "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches".
 
@@ -240,7 +242,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of prefill,verify,cp (default: all)")
+    ap.add_argument("--only", default="", help="comma list of prefill,verify,decode,varlen,cp (default: all)")
     ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "cp"],
                     help="launch only this kernel family (warmup + steps launches, no JSON) for ncu")
     ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp")
@@ -265,7 +267,7 @@ def main(argv=None):
     from kda_gated_delta_02_gb300 import synth
     kda.load_library()
     peaks = load_peaks()
-    only = set(args.only.split(",")) if args.only else {"prefill", "verify", "cp"}
+    only = set(args.only.split(",")) if args.only else {"prefill", "verify", "decode", "varlen", "cp"}
     K, Wm = max(1, args.steps), max(3, args.warmup)
     stream = torch.cuda.current_stream()
     out = {}
@@ -355,6 +357,54 @@ def main(argv=None):
                          "requests_per_s": ws * vw.R / (vms * 1e-3)}
         launches += K
         del d, st, tl, ov
+        torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ single-token decode (window 0)
+    if "decode" in only:
+        dw = synth.DecodeWorkload("decode R=256 H=96 d=128 W=4 one token (window 0)", 256, 96, 128, 128,
+                                  Wd=0, seed=5)
+        d = synth.make_decode(dw, device="cuda", accepted=[0] * dw.R)
+        st, tl = d["state"].clone(), d["tail"].clone()
+        od = torch.empty((dw.R, 1, dw.H, dw.dv), dtype=torch.bfloat16, device="cuda")
+
+        def decode_step():
+            kda.decode_verify_replay(st, tl, d["conv_w"], d["cached_qkv"], d["cached_g"], d["cached_b"],
+                                     d["accepted"], d["new_qkv"], d["new_g"], d["new_b"], d["out_w"], out=od)
+
+        for _ in range(Wm):
+            decode_step()
+        dms = reduce_max(cuda_time(decode_step, K, stream), ws)
+        state_bytes = 2 * st.numel() * st.element_size()
+        row = 3 * dw.H * dw.dk * 2 + dw.H * dw.dk * 2 + dw.H * 2
+        total_bytes = state_bytes + dw.R * row + 2 * tl.numel() * tl.element_size() + od.numel() * od.element_size()
+        out["decode"] = {"workload": dw.name, "ms": dms, "state_gbs": ws * state_bytes / (dms * 1e-3) / 1e9,
+                         "frac_hbm": (total_bytes / (dms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+                         "bytes_per_launch": total_bytes, "tokens_per_s": ws * dw.R / (dms * 1e-3)}
+        launches += K
+        del d, st, tl, od
+        torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ varlen prefix continuation
+    if "varlen" in only:
+        vl = synth.VARLEN
+        vi = synth.make_prefill(vl, device="cuda")
+        Tv, Hv = vi["q"].shape[:2]
+        ov = torch.empty_like(vi["v"])
+        Sv = torch.empty_like(vi["S0"])
+
+        def varlen_step():
+            kda.chunk_fwd(vi["q"], vi["k"], vi["v"], vi["g"], vi["beta"], vi["cu_seqlens"],
+                          initial_state=vi["S0"], out=ov, final_state=Sv, cp_mode=kda.CP_AUTO)
+
+        for _ in range(3):
+            varlen_step()
+        Kv = max(3, K // 2)
+        vms_ = reduce_max(cuda_time(varlen_step, Kv, stream), ws)
+        vbytes = Tv * Hv * BYTES_PER_TOKHEAD + 2 * vi["S0"].numel() * 4
+        out["varlen"] = {"workload": vl.name, "tokens": Tv, "ms": vms_, "tok_s": ws * Tv / (vms_ * 1e-3),
+                         "frac_hbm": (vbytes / (vms_ * 1e-3) / 1e9) / peaks["hbm_gbs"]}
+        launches += Kv
+        del vi, ov, Sv
         torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ ultra-long, context parallel

@@ -121,3 +121,20 @@ def test_full_verify_r256_h96(kda, oracle):
     got, ref = run_both(kda, oracle, inp)
     assert got[3] == 0
     compare(inp, got, ref)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_single_token_decode_chain(kda, oracle, D):
+    """Non-speculative decode: window 0, accepted 0, one token per request per
+    step; three steps chained through the written-back state and conv tail."""
+    R, H = 8, 3
+    inp = gpu_inputs(R, H, D, accepted=[0] * R, seed=20 + D, Wd=0)
+    assert inp["new_qkv"].shape[1] == 1 and inp["cached_qkv"].shape[1] == 0
+    for step in range(3):
+        got, ref = run_both(kda, oracle, inp)
+        assert got[3] == 0 and ref[3] == 0
+        compare(inp, got, ref)
+        nxt = gpu_inputs(R, H, D, accepted=[0] * R, seed=30 + 10 * step + D, Wd=0)
+        nxt["state"], nxt["tail"] = got[0], got[1]
+        nxt["conv_w"], nxt["out_w"] = inp["conv_w"], inp["out_w"]
+        inp = nxt
