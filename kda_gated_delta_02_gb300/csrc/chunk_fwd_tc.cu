@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 for (int r = 0; r < 16; ++r) Tb[r * LDF + c] = acc[r];
             }
             __syncthreads();
-            // 32 x 32 diagonal halves: T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22
+            // 32 x 32 diagonal halves: T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22.
+            // X = A_10 T_00 goes to the (unused) upper block (0,1) of the A scratch.
             {
                 const int hb = tid >> 8, e = tid & 255, r = e >> 4, c = e & 15;
                 const int i = 2 * hb + 1, j = 2 * hb;
@@ -467,28 +468,30 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                     x0 = fmaf(Ar[m], Tc[m * LDF], x0);
                     x1 = fmaf(Ar[m + 1], Tc[(m + 1) * LDF], x1);
                 }
-                float *Xp = sTf + (16 * i + r) * LDF + 16 * j + c;
-                *Xp = x0 + x1;
+                float *Xs = const_cast<float *>(sAf) + (16 * j) * LDF + 16 * i;  // X[r][c] at row r
+                Xs[r * LDF + c] = x0 + x1;
                 // the upper blocks (0,1) and (2,3) of T are zero (read as parts of the
                 // lower-triangular 32 x 32 halves below)
                 sTf[(16 * j + r) * LDF + 16 * i + c] = 0.f;
                 __syncthreads();
                 const float *Ti = sTf + (16 * i + r) * LDF + 16 * i;
-                const float *Xc = sTf + (16 * i) * LDF + 16 * j + c;
                 float y0 = 0.f, y1 = 0.f;
 #pragma unroll
                 for (int m = 0; m < 16; m += 2) {
-                    y0 = fmaf(Ti[m], Xc[m * LDF], y0);
-                    y1 = fmaf(Ti[m + 1], Xc[(m + 1) * LDF], y1);
+                    y0 = fmaf(Ti[m], Xs[m * LDF + c], y0);
+                    y1 = fmaf(Ti[m + 1], Xs[(m + 1) * LDF + c], y1);
                 }
-                __syncthreads();
-                *Xp = -(y0 + y1);
+                sTf[(16 * i + r) * LDF + 16 * j + c] = -(y0 + y1);
                 __syncthreads();
             }
-            // lower-left 32 x 32: T_21 = -T_22 (A_21 T_11), two 32x32x32 fp32
-            // products as tf32 tensor products with hi/lo splits (3 MMAs per step):
-            // warp w < 8 owns the 16 x 8 output tile (rows 16(w>>2), cols 8(w&3))
-            {
+            // Warps 0-7: lower-left 32 x 32, T_21 = -T_22 (A_21 T_11), two 32x32x32
+            // fp32 products as tf32 tensor products with hi/lo splits (3 MMAs per
+            // step); warp w owns the 16 x 8 tile (rows 16(w>>2), cols 8(w&3)); the
+            // intermediate X goes to the unused upper-right 32 x 32 of the A scratch
+            // and the result straight into T diag(b) as bf16.
+            // Warps 8-15 meanwhile: T diag(b) for the rest (rows 0-31 and the
+            // lower-right 32 x 32), zero above the diagonal.
+            if (warp < 8) {
                 const int gq = lane >> 2, q4 = lane & 3;
                 const int mt = (warp >> 2) & 1, nt = warp & 3;
                 auto product = [&](const float *Am, const float *Bm, float (&acc)[4]) {
@@ -508,29 +511,32 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                     }
                 };
                 float acc[4];
-                if (warp < 8) product(sAf + 32 * LDF, sTf, acc);  // X = A_21 T_11
-                float *Xt = sTf + (32 + 16 * mt + gq) * LDF + 8 * nt + 2 * q4;
-                if (warp < 8) {
-                    *reinterpret_cast<float2 *>(Xt) = make_float2(acc[0], acc[1]);
-                    *reinterpret_cast<float2 *>(Xt + 8 * LDF) = make_float2(acc[2], acc[3]);
+                float *X64 = const_cast<float *>(sAf) + 32;  // rows 0-31, columns 32-63
+                product(sAf + 32 * LDF, sTf, acc);           // X = A_21 T_11
+                float *Xt = X64 + (16 * mt + gq) * LDF + 8 * nt + 2 * q4;
+                *reinterpret_cast<float2 *>(Xt) = make_float2(acc[0], acc[1]);
+                *reinterpret_cast<float2 *>(Xt + 8 * LDF) = make_float2(acc[2], acc[3]);
+                asm volatile("bar.sync 1, 256;\n" ::: "memory");  // warps 0-7 only
+                product(sTf + 32 * LDF + 32, X64, acc);      // T_22 X
+                const int t = 32 + 16 * mt + gq, s0 = 8 * nt + 2 * q4;
+                const float b0 = sBeta[s0], b1 = sBeta[s0 + 1];
+                st_bf16x2(sm, OFF_TB + umma::kmaj(t, s0, 64), -acc[0] * b0, -acc[1] * b1);
+                st_bf16x2(sm, OFF_TB + umma::kmaj(t + 8, s0, 64), -acc[2] * b0, -acc[3] * b1);
+            } else {
+                // 1536 pairs: rows 0-31 x 32 pairs, then rows 32-63 x pairs 16-31
+                for (int e2 = tid - 256; e2 < 1536; e2 += 256) {
+                    int t, s;
+                    if (e2 < 1024) {
+                        t = e2 >> 5;
+                        s = 2 * (e2 & 31);
+                    } else {
+                        t = 32 + ((e2 - 1024) >> 4);
+                        s = 32 + 2 * ((e2 - 1024) & 15);
+                    }
+                    const float a0 = (s <= t) ? sTf[t * LDF + s] * sBeta[s] : 0.f;
+                    const float a1 = (s + 1 <= t) ? sTf[t * LDF + s + 1] * sBeta[s + 1] : 0.f;
+                    st_bf16x2(sm, OFF_TB + umma::kmaj(t, s, 64), a0, a1);
                 }
-                __syncthreads();
-                if (warp < 8) product(sTf + 32 * LDF + 32, sTf + 32 * LDF, acc);  // T_22 X
-                __syncthreads();
-                if (warp < 8) {
-                    *reinterpret_cast<float2 *>(Xt) = make_float2(-acc[0], -acc[1]);
-                    *reinterpret_cast<float2 *>(Xt + 8 * LDF) = make_float2(-acc[2], -acc[3]);
-                }
-                __syncthreads();
-            }
-            // T diag(b) as bf16, zero above the diagonal
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e2 = tid + u * NT;  // pair index over 64 x 32 pairs
-                const int t = e2 >> 5, s = 2 * (e2 & 31);
-                const float a0 = (s <= t) ? sTf[t * LDF + s] * sBeta[s] : 0.f;
-                const float a1 = (s + 1 <= t) ? sTf[t * LDF + s + 1] * sBeta[s + 1] : 0.f;
-                st_bf16x2(sm, OFF_TB + umma::kmaj(t, s, 64), a0, a1);
             }
         }
         umma::fence_proxy_async();
