@@ -8,7 +8,8 @@
 // the state itself lives in tensor memory for the whole walk.  Every product of the
 // chunk runs as a tcgen05 MMA with M = 128 on operands staged in shared memory
 // in the 128-byte swizzled layouts; transposed forms put dv (or dk) on M:
-//   A/B tiles  D[s][t']  = R_i[s] . L[t']   (per 16-row block i, N = 16 keys + 16 queries)
+//   A/B tiles  D[t'][s'] = L[t'] . R[s']    (all 128 L rows x the 160 rows of R_0..R_3;
+//                                            block i uses its L rows against R_i)
 //   W^T        D[i][t]   = (K e^gamma)^T  (T diag b)^T
 //   U~^T       D[j][t]   = V^T (T diag b)^T,      then  -= S^T W^T   ->  U^T
 //   O^T        D[j][t]   = S^T Q~^T + U^T B^T
@@ -43,8 +44,10 @@ constexpr uint32_t OFF_G = 32768;     // raw g f32 [64][128]
 constexpr uint32_t OFF_V = 65536;     // V, MN-major (s x dv): two 64-wide halves of [64 s][128 B]
 constexpr uint32_t OFF_UN = 81920;    // union, 73728 bytes:
 constexpr uint32_t UN_L = 0;          //   L (K-major 128 x 128)         steps 2-3
-// R_i (16(i+1) rows, K-major) at 32768 + 4096 * i(i+1)/2: 32768, 36864, 45056, 57344
-__host__ __device__ constexpr uint32_t un_r(int i) { return 32768u + 4096u * (uint32_t)(i * (i + 1) / 2); }
+constexpr uint32_t UN_R = 32768;      //   R = [R_0; R_1; R_2; R_3] (K-major 160 rows x 128)  steps 2-3
+constexpr uint32_t R_KB = 160 * 128;  //   its K-block stride (two 64-wide K-blocks, 20480 B each)
+// rows of R_i start at row 8 i (i+1): 0, 16, 48, 96 (16 (i+1) rows each)
+__host__ __device__ constexpr uint32_t r_row(int i) { return 8u * (uint32_t)(i * (i + 1)); }
 constexpr uint32_t UN_AF = 34816;     //   A fp32 [64][68]                steps 4-5
 constexpr uint32_t UN_TF = 52224;     //   T fp32 [64][68]
 constexpr uint32_t UN_ST = 0;         //   S^T bf16 (K-major 128 x 128)   steps 4-8
@@ -54,7 +57,7 @@ constexpr uint32_t OFF_KG = 155648;   // K e^gamma, MN-major (s x dk)
 constexpr uint32_t OFF_QT = 172032;   // Q e^gamma, K-major 64 x 128
 constexpr uint32_t OFF_KT = 188416;   // K e^{gamma_63 - gamma}, MN-major (s x dk)
 constexpr uint32_t OFF_TB = 204800;   // T diag(b), K-major 64 x 64
-constexpr uint32_t OFF_BM = 212992;   // B, MN-major (64 k-rows s x 64 t)
+constexpr uint32_t OFF_BM = 212992;   // B, K-major (64 rows t x 64 s)
 constexpr uint32_t OFF_BETA = 221184; // f32 [64]
 constexpr uint32_t OFF_PART = 221440; // f32 [2][4][128] half-block products
 constexpr uint32_t OFF_DEL = 225536;  // f32 [4][128] block decays
@@ -66,8 +69,8 @@ constexpr int LDF = 68;               // fp32 [64][68] row stride
 
 // tensor-memory columns
 //   S^T (fp32, the state, resident for the whole walk; the U^T K~ update
-//   accumulates onto it) | A/B tiles | W^T | U^T | O^T
-constexpr uint32_t TM_ST = 0, TM_AB = 128, TM_W = 256, TM_U = 320, TM_O = 384;
+//   accumulates onto it) | L R^T (160 columns) | W^T | U^T | O^T
+constexpr uint32_t TM_ST = 0, TM_AB = 128, TM_W = 288, TM_U = 352, TM_O = 416;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
 __device__ __forceinline__ void st_bf16x2(unsigned char *base, uint32_t off, float a, float b) {
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) umma::mbar_init(bar0 + 8 * b, b == 0 ? 4u : 1u);
+        for (int b = 0; b < 6; ++b) umma::mbar_init(bar0 + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 0) umma::tmem_alloc(sb + OFF_TMEM, 512);
@@ -314,10 +317,9 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             const uint32_t atom = ((uint32_t)(2 * i + hf) * 2u + kb) * 1024u;
             const uint32_t aKG = sb + OFF_KG + atom;
             const uint32_t aKT = sb + OFF_KT + atom;
-            const uint32_t aR0 = un + un_r(0) + kb * (16u * 1u * 128u) + rowT;
-            const uint32_t aR1 = un + un_r(1) + kb * (16u * 2u * 128u) + rowT;
-            const uint32_t aR2 = un + un_r(2) + kb * (16u * 3u * 128u) + rowT;
-            const uint32_t aR3 = un + un_r(3) + kb * (16u * 4u * 128u) + rowT;
+            const uint32_t aRk = un + UN_R + kb * R_KB + rowT;
+            const uint32_t aR0 = aRk + r_row(0) * 128u, aR1 = aRk + r_row(1) * 128u;
+            const uint32_t aR2 = aRk + r_row(2) * 128u, aR3 = aRk + r_row(3) * 128u;
             const uint32_t ak = sb + OFF_K + rowT * 2u + (uint32_t)ch * 2u;  // raw rows are 256 B
             const uint32_t aq = sb + OFF_Q + rowT * 2u + (uint32_t)ch * 2u;
             uint32_t kraw[8], qraw[8];  // loads first: the stores below are ordered asm
@@ -352,19 +354,18 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         __syncthreads();
 
         // ------------------------------------------------------------ step 3: A and B tiles
-        // one issuing thread per column block i (lane 0 of warps 0-3), each
-        // committing to the same barrier (arrival count 4)
-        if (lane == 0 && warp < 4) {
+        // D[t'][s'] = L[t'] . R[s'] over all 128 L rows and 160 R rows in one
+        // M = 128, N = 160 product: block i reads its 32 L rows (TMEM lane
+        // quadrant i) against its R_i columns; the other pairs are not used
+        if (tid == 0) {
             umma::fence_after();
-            constexpr uint32_t id = umma::idesc_bf16(128, 32, 0, 0, 0);
-            const int i = warp;
-            const uint32_t rows = 16 * (i + 1);
+            constexpr uint32_t id = umma::idesc_bf16(128, 160, 0, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + un_r(i) + kb * rows * 128 + kin) >> 4), 16, 1024);
-                const uint64_t b = umma::sdesc4(sb4 + ((OFF_UN + UN_L + kb * 16384 + 32 * i * 128 + kin) >> 4), 16, 1024);
-                umma::mma(tmem + TM_AB + 32 * i, a, b, id, ks > 0 ? 1u : 0u);
+                const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_L + kb * 16384 + kin) >> 4), 16, 1024);
+                const uint64_t b = umma::sdesc4(sb4 + ((OFF_UN + UN_R + kb * R_KB + kin) >> 4), 16, 1024);
+                umma::mma(tmem + TM_AB, a, b, id, ks > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 0);
         }
@@ -378,7 +379,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         // S^T (rows of this thread's TMEM lane, columns 32 cg ..) as the bf16
         // operand of steps 6 and 8, and the resident state decayed to the chunk
         // end in place, Diag-cols(e^{gamma_63}) S^T, onto which step 10 accumulates
-        // U^T K~.  Lane quadrants 2-3 do it in step 4, 0-1 in step 5.
+        // U^T K~.  Warps 2 and 3 (the diagonal inverse of step 5) do it in step 4,
+        // the others in step 5.
         auto copy_decay_state = [&]() {
             float Sreg[32];
             umma::ld32(tq + TM_ST + 32 * cg, Sreg);
@@ -404,30 +406,41 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         };
 
         // ------------------------------------------------------------ step 4: A (fp32, scaled by b_t) and B (bf16)
-        if (qd >= 2) copy_decay_state();
+        // Lane quadrant i holds block i: lanes 0-15 the key rows t = 16 i + l (A),
+        // 16-31 the query rows (B); warp (i, cg) takes key columns s = 16 cg ..
+        // 16 cg + 15 of R_i when cg <= i, else those entries are zero.
         {
             float *sAf = reinterpret_cast<float *>(sm + OFF_UN + UN_AF);
-            if (qd < 2) {
-                float v[32];
-                umma::ld32(tq + TM_AB + 32 * cg, v);
-                const int s = jrow;  // key position (0..63)
+            const int i = qd, t = 16 * i + (lane & 15), s0 = 16 * cg;
+            const bool is_q = lane >= 16;
+            float v[16];
+            if (cg <= i) umma::ld16(tq + TM_AB + r_row(i) + 16 * cg, v);
+            else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            }
+            if (!is_q) {
+                if (cg <= i) {
+                    const float bt = sBeta[t];
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(sAf + t * LDF + s0 + j) =
+                            make_float4((s0 + j < t) ? bt * v[j] : 0.f, (s0 + j + 1 < t) ? bt * v[j + 1] : 0.f,
+                                        (s0 + j + 2 < t) ? bt * v[j + 2] : 0.f, (s0 + j + 3 < t) ? bt * v[j + 3] : 0.f);
+                }
+            } else {
                 uint32_t bp[8];
 #pragma unroll
-                for (int tt = 0; tt < 16; ++tt) {
-                    const int t = 16 * cg + tt;
-                    sAf[t * LDF + s] = (s < t) ? sBeta[t] * v[tt] : 0.f;
-                }
-#pragma unroll
-                for (int tt = 0; tt < 16; tt += 2) {
-                    const int t = 16 * cg + tt;
-                    bp[tt >> 1] = pack_bf16((s <= t) ? v[16 + tt] : 0.f, (s <= t + 1) ? v[17 + tt] : 0.f);
-                }
-                // B as an MN-major operand: element (n = t, k = s), t contiguous
-                *reinterpret_cast<uint4 *>(sm + OFF_BM + umma::mnmaj(16 * cg, s, 1)) =
+                for (int j = 0; j < 16; j += 2)
+                    bp[j >> 1] = pack_bf16((s0 + j <= t) ? v[j] : 0.f, (s0 + j + 1 <= t) ? v[j + 1] : 0.f);
+                // B as a K-major operand: row t, k = s
+                const uint32_t row = (uint32_t)t * 128u, sw = (uint32_t)(t & 7);
+                *reinterpret_cast<uint4 *>(sm + OFF_BM + row + (((2u * cg) ^ sw) << 4)) =
                     make_uint4(bp[0], bp[1], bp[2], bp[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_BM + umma::mnmaj(16 * cg + 8, s, 1)) =
+                *reinterpret_cast<uint4 *>(sm + OFF_BM + row + (((2u * cg + 1u) ^ sw) << 4)) =
                     make_uint4(bp[4], bp[5], bp[6], bp[7]);
             }
+            if (warp == 2 || warp == 3) copy_decay_state();
         }
         if (__syncthreads_or(timed_out)) break;
 
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             float *sTf = reinterpret_cast<float *>(sm + OFF_UN + UN_TF);
             // diagonal 16 x 16 blocks, right-looking substitution with one column
             // per lane in registers: lanes 0-15 of warp 2 + w -> block 2w, 16-31 -> 2w+1
-            if (qd < 2) copy_decay_state();
+            if (warp != 2 && warp != 3) copy_decay_state();
             if (warp == 2 || warp == 3) {
                 const int i = 2 * (warp - 2) + (lane >> 4), c = lane & 15;
                 const float *Ab = sAf + (16 * i) * LDF + 16 * i;
@@ -627,12 +640,12 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         // ------------------------------------------------------------ step 10: + U^T B^T, U^T K~
         if (tid == 0) {
             umma::fence_after();
-            constexpr uint32_t ido = umma::idesc_bf16(128, 64, 0, 1, 0);
+            constexpr uint32_t ido = umma::idesc_bf16(128, 64, 0, 0, 0);
             constexpr uint32_t ids = umma::idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t a = umma::sdesc4(sb4 + ((OFF_UN + UN_UT + ks * 32) >> 4), 16, 1024);
-                if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_BM + ks * 2048) >> 4), 1024, 1024), ido, 1u);
+                if (need_q) umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((OFF_BM + ks * 32) >> 4), 16, 1024), ido, 1u);
                 umma::mma(tmem + TM_ST, a, umma::sdesc4(sb4 + ((OFF_KT + ks * 4096) >> 4), 1024, 2048), ids, 1u);
             }
             umma::commit(bar0 + 24);
