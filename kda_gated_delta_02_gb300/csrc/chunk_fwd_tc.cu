@@ -379,8 +379,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         // S^T (rows of this thread's TMEM lane, columns 32 cg ..) as the bf16
         // operand of steps 6 and 8, and the resident state decayed to the chunk
         // end in place, Diag-cols(e^{gamma_63}) S^T, onto which step 10 accumulates
-        // U^T K~.  Warps 2 and 3 (the diagonal inverse of step 5) do it in step 4,
-        // the others in step 5.
+        // U^T K~.  Done in step 4 or step 5 (see early_copy).
         auto copy_decay_state = [&]() {
             float Sreg[32];
             umma::ld32(tq + TM_ST + 32 * cg, Sreg);
@@ -404,6 +403,10 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             umma::st32(tq + TM_ST + 32 * cg, Sreg);
             umma::fence_before();
         };
+
+        // half of the warps copy the state in step 4: those without A/B columns
+        // there (cg > lane quadrant) and warps 2, 3 (busy in step 5)
+        const bool early_copy = cg > qd || warp == 2 || warp == 3;
 
         // ------------------------------------------------------------ step 4: A (fp32, scaled by b_t) and B (bf16)
         // Lane quadrant i holds block i: lanes 0-15 the key rows t = 16 i + l (A),
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 *reinterpret_cast<uint4 *>(sm + OFF_BM + row + (((2u * cg + 1u) ^ sw) << 4)) =
                     make_uint4(bp[4], bp[5], bp[6], bp[7]);
             }
-            if (warp == 2 || warp == 3) copy_decay_state();
+            if (early_copy) copy_decay_state();
         }
         if (__syncthreads_or(timed_out)) break;
 
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             float *sTf = reinterpret_cast<float *>(sm + OFF_UN + UN_TF);
             // diagonal 16 x 16 blocks, right-looking substitution with one column
             // per lane in registers: lanes 0-15 of warp 2 + w -> block 2w, 16-31 -> 2w+1
-            if (warp != 2 && warp != 3) copy_decay_state();
+            if (!early_copy) copy_decay_state();
             if (warp == 2 || warp == 3) {
                 const int i = 2 * (warp - 2) + (lane >> 4), c = lane & 15;
                 const float *Ab = sAf + (16 * i) * LDF + 16 * i;

@@ -73,5 +73,7 @@ struct VerifyArgs {
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t st);
 // tcgen05 / tensor-memory version of the verify kernel (dk = dv = 128).
 cudaError_t launch_verify_tc(const VerifyArgs &a, cudaStream_t st);
+// Single-token decode (Wd = 0) on the CUDA cores (dk = dv = 64 or 128).
+cudaError_t launch_decode_token(const VerifyArgs &a, cudaStream_t st);
 
 }  // namespace kda
