@@ -108,6 +108,28 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                   float g_min, int in_dtype, int cp_mode, int segment_len, void *workspace,
                   size_t workspace_bytes, uint32_t *status, void *stream);
 
+/*
+ * kda_chunk_fwd that also emits intermediate states: prefix-cache resume
+ * points ("Dentro de los esfuerzos de optimizacion de Kimi K3", section 5:
+ * states kept at block-aligned positions so that a later request sharing the
+ * prefix continues from them).  Same arguments and results as kda_chunk_fwd,
+ * plus:
+ *  ckpt_every  positive multiple of 64: a checkpoint is the state after token
+ *              ckpt_every * (k + 1) of a sequence (positions counted from the
+ *              sequence start), k = 0 .. ckpt_count - 1.
+ *  ckpt_count  checkpoints kept per sequence; positions past a sequence's end
+ *              are not written (those slots keep their contents).
+ *  ckpt        device f32 [N][ckpt_count][H][dk][dv], or NULL when ckpt_count = 0.
+ * Works with context parallelism on or off (the replay pass writes them).
+ * Invalid ckpt arguments return KDA_ERR_INVALID_ARG before any launch.
+ */
+int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const int32_t *cu_seqlens, int N, int T, int H,
+                       int dk, int dv, const float *initial_state, float *final_state, void *o,
+                       float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
+                       void *workspace, size_t workspace_bytes, int ckpt_every, int ckpt_count,
+                       float *ckpt, uint32_t *status, void *stream);
+
 /* Workspace bytes kda_chunk_fwd needs for these arguments (0 when cp_mode
  * resolves to OFF).  Pure host arithmetic. */
 size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,

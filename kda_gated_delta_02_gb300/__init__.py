@@ -55,6 +55,9 @@ def load_library():
         lib.kda_version.restype = I
         lib.kda_chunk_fwd.restype = I
         lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, I, I, P, S, P, P]
+        lib.kda_chunk_fwd_ckpt.restype = I
+        lib.kda_chunk_fwd_ckpt.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, I, I, P, S,
+                                           I, I, P, P, P]
         lib.kda_chunk_fwd_workspace_size.restype = S
         lib.kda_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.kda_chunk_fwd_plan.restype = I
@@ -109,10 +112,13 @@ def chunk_fwd_plan(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
 
 def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,
               g_min=-5.0, cp_mode=CP_AUTO, segment_len=0, out=None, final_state=None,
-              workspace=None, status=None, stream=None):
+              workspace=None, status=None, stream=None, ckpt_every=0, ckpt=None):
     """Chunkwise KDA prefill.  q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H];
     cu_seqlens int32 [N+1]; initial_state f32 [N,H,dk,dv] or None.
-    Returns (o [T,H,dv] in q's dtype, final_state f32 [N,H,dk,dv] or None)."""
+    Returns (o [T,H,dv] in q's dtype, final_state f32 [N,H,dk,dv] or None).
+    With ckpt_every > 0 (a multiple of 64) also writes the state after every
+    ckpt_every tokens of each sequence into ckpt f32 [N,K,H,dk,dv] (K = its
+    second dimension) through kda_chunk_fwd_ckpt."""
     lib = load_library()
     T, H, dk = k.shape
     dv = v.shape[2]
@@ -124,13 +130,20 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
     ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
-                           _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
-                           _in_dtype(q), int(cp_mode), int(segment_len),
-                           _ptr(workspace) if ws_bytes else None,
-                           ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0),
-                           _ptr(status), _stream(stream))
-    _check(rc, "kda_chunk_fwd")
+    common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+              _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
+              _in_dtype(q), int(cp_mode), int(segment_len),
+              _ptr(workspace) if ws_bytes else None,
+              ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0))
+    if ckpt_every:
+        if ckpt is None or ckpt.dim() != 5 or ckpt.dtype != torch.float32:
+            raise KDAError("ckpt must be an f32 tensor [N, K, H, dk, dv]")
+        rc = lib.kda_chunk_fwd_ckpt(*common, int(ckpt_every), int(ckpt.shape[1]), _ptr(ckpt), _ptr(status),
+                                    _stream(stream))
+        _check(rc, "kda_chunk_fwd_ckpt")
+    else:
+        rc = lib.kda_chunk_fwd(*common, _ptr(status), _stream(stream))
+        _check(rc, "kda_chunk_fwd")
     return out, final_state
 
 

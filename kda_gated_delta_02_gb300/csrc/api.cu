@@ -123,11 +123,12 @@ int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int seg
     return cp_layout(N, T, H, dk, dv, cp_mode, segment_len).seg_len;
 }
 
-int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                  const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
-                  const float *initial_state, float *final_state, void *o, float scale, float g_min,
-                  int in_dtype, int cp_mode, int segment_len, void *workspace, size_t workspace_bytes,
-                  uint32_t *status, void *stream) {
+namespace {
+int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                   const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                   const float *initial_state, float *final_state, void *o, float scale, float g_min,
+                   int in_dtype, int cp_mode, int segment_len, void *workspace, size_t workspace_bytes,
+                   int ckpt_every, int ckpt_count, float *ckpt, uint32_t *status, void *stream) {
     if (N < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
     if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
@@ -146,6 +147,12 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = o;
     a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.scale = scale; a.g_min = g_min;
     a.status = status;
+    a.cu_seqlens = cu_seqlens;
+    if (ckpt_count > 0) {
+        a.ckpt = ckpt;
+        a.ckpt_every = ckpt_every;
+        a.ckpt_count = ckpt_count;
+    }
 
     CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
     if (L.seg_len == 0) {
@@ -173,7 +180,11 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
     a.seg_count = count;
     a.M_out = M;
     a.N_out = Nm;
-    e = run_chunk(a, L.P_max, bf, st);
+    {
+        kda::ChunkArgs at = a;  // transitions emit no checkpoints
+        at.ckpt = nullptr;
+        e = run_chunk(at, L.P_max, bf, st);
+    }
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     // pass 2: ordered scan per (sequence, head)
     kda::ComposeArgs c = {};
@@ -187,6 +198,31 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
     a.S_final = final_state;
     a.M_out = a.N_out = nullptr;
     return cuda_status(run_chunk(a, L.P_max, bf, st));
+}
+
+}  // namespace
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                  const float *initial_state, float *final_state, void *o, float scale, float g_min,
+                  int in_dtype, int cp_mode, int segment_len, void *workspace, size_t workspace_bytes,
+                  uint32_t *status, void *stream) {
+    return chunk_fwd_impl(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, final_state, o, scale,
+                          g_min, in_dtype, cp_mode, segment_len, workspace, workspace_bytes, 0, 0, nullptr,
+                          status, stream);
+}
+
+int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                       const float *initial_state, float *final_state, void *o, float scale, float g_min,
+                       int in_dtype, int cp_mode, int segment_len, void *workspace, size_t workspace_bytes,
+                       int ckpt_every, int ckpt_count, float *ckpt, uint32_t *status, void *stream) {
+    if (ckpt_every <= 0 || (ckpt_every % kChunk) != 0 || ckpt_count < 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_count > 0 && !ckpt) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(ckpt)) return KDA_ERR_ALIGNMENT;
+    return chunk_fwd_impl(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, final_state, o, scale,
+                          g_min, in_dtype, cp_mode, segment_len, workspace, workspace_bytes, ckpt_every,
+                          ckpt_count, ckpt, status, stream);
 }
 
 int kda_segment_transition(const void *k, const void *v, const float *g, const float *beta, int T, int H,

@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
         t1 = min(p.T, t0 + p.seg_len);
         last_seg = t1 == p.T;
     }
+    // start of this unit's sequence (checkpoint positions are relative to it)
+    const int seq0 = (p.mode == MODE_SEQ) ? t0 : ((p.seg_table && p.cu_seqlens) ? p.cu_seqlens[n] : 0);
     // columns: in transition mode the tile walks the augmented state [M | N]
     const int colbase = tile * DVT;
     bool m_part = false;
@@ -627,6 +629,24 @@ __global__ void __launch_bounds__(NTHR, 1) kda_chunk_kernel(ChunkArgs p) {
                 }
             }
             store_state_bf16();
+        }
+        // checkpoint: the state after token (tc + Lc) when that position of the
+        // sequence is a multiple of ckpt_every
+        if (p.ckpt && p.mode != MODE_TRANSITION) {
+            const int rel = tc + Lc - seq0;
+            const int kq = rel / p.ckpt_every - 1;
+            if (rel % p.ckpt_every == 0 && kq < p.ckpt_count) {
+                float *dst = p.ckpt + (((size_t)n * p.ckpt_count + kq) * H + h) * DK * (size_t)dv;
+#pragma unroll
+                for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        int row = 16 * mb + gq + 8 * hh;
+                        int col = cs * CPW + 8 * nt + 2 * q4;
+                        *reinterpret_cast<float2 *>(dst + (size_t)row * dv + vcol0 + col) =
+                            make_float2(sreg[nt][2 * hh], sreg[nt][2 * hh + 1]);
+                    }
+            }
         }
         __syncthreads();
     }

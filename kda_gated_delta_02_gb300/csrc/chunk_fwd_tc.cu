@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         t1 = min(p.T, t0 + p.seg_len);
         last_seg = t1 == p.T;
     }
+    // start of this unit's sequence (checkpoint positions are relative to it)
+    const int seq0 = (p.mode == MODE_SEQ) ? t0 : ((p.seg_table && p.cu_seqlens) ? p.cu_seqlens[n] : 0);
     const bool transition = p.mode == MODE_TRANSITION;
     const bool m_part = transition && tile == 0;  // augmented columns [0, dk): M
     const bool has_v = !m_part;
@@ -655,6 +657,19 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         }
         timed_out |= !umma::mbar_wait(bar0 + 24, phase, WAIT_LIMIT);
         umma::fence_after();
+        // checkpoint: the state after token (tc + Lc) when that position of the
+        // sequence is a multiple of ckpt_every (S^T lane = value column)
+        if (p.ckpt && !transition) {
+            const int rel = tc + Lc - seq0;
+            const int kq = rel / p.ckpt_every - 1;
+            if (rel % p.ckpt_every == 0 && kq < p.ckpt_count) {
+                float *dst = p.ckpt + (((size_t)n * p.ckpt_count + kq) * H + h) * D * (size_t)dv;
+                float Sreg[32];
+                umma::ld32(tq + TM_ST + 32 * cg, Sreg);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * dv + vcol0 + jrow] = Sreg[c];
+            }
+        }
 
         // ------------------------------------------------------------ step 11: outputs and state
         // outputs are staged as a row-major [64][128] bf16 tile in the (now free)

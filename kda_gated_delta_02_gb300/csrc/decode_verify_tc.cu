@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         return;
     }
     const int ntok = a + 1 + Wd;  // <= 15 (host-checked Wd <= 7), so a <= 7 lies in the first half
-    const int nrows = (W - 1) + ntok;
     const size_t HD = (size_t)H * D, Cq = 3 * HD;
     const size_t chq = (size_t)h * D + c;
 

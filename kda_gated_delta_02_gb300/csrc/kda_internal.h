@@ -29,6 +29,11 @@ struct ChunkArgs {
     float *S_final;             // SEQ / REPLAY: final_state [N][H][dk][dv] or null
     float *M_out, *N_out;       // TRANSITION: [P][H][dk][dk], [P][H][dk][dv]
     uint32_t *status;
+    // SEQ / REPLAY: the state every ckpt_every tokens of a sequence (positions
+    // ckpt_every * (k + 1), k < ckpt_count) into ckpt [N][ckpt_count][H][dk][dv];
+    // null for none.  REPLAY reads the sequence starts from cu_seqlens.
+    float *ckpt;
+    int ckpt_every, ckpt_count;
 };
 
 cudaError_t launch_chunk(const ChunkArgs &a, int units, int dvt, bool in_bf16, cudaStream_t st);

@@ -232,3 +232,44 @@ def test_full_ultra_long_context_parallel(kda, oracle):
     mask = np.zeros(w.H, dtype=np.uint8)
     mask[[0, 7]] = 1
     run_and_compare(kda, oracle, inp, cp_mode=-1, head_mask=mask)
+
+
+@pytest.mark.parametrize("cfg", ["bf16_d128", "fp32_d64", "cp_d128"])
+def test_checkpoints_match_oracle_prefixes(kda, oracle, cfg):
+    """kda_chunk_fwd_ckpt: checkpoint k of sequence n is the state after
+    ckpt_every * (k + 1) tokens of n, i.e. the oracle's final state on that
+    prefix; slots past a sequence's end stay untouched."""
+    torch.manual_seed(11)
+    if cfg == "cp_d128":
+        lens, H, d, dt, every, cp, seg = [4096], 2, 128, torch.bfloat16, 768, kda.CP_ON, 1024
+    elif cfg == "fp32_d64":
+        lens, H, d, dt, every, cp, seg = [700, 256, 1100], 3, 64, torch.float32, 256, kda.CP_OFF, 0
+    else:
+        lens, H, d, dt, every, cp, seg = [640, 1000, 1536], 4, 128, torch.bfloat16, 256, kda.CP_OFF, 0
+    T = sum(lens)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    q = torch.nn.functional.normalize(torch.randn(T, H, d), dim=-1).to(dt)
+    k = torch.nn.functional.normalize(torch.randn(T, H, d), dim=-1).to(dt)
+    v = torch.randn(T, H, d).to(dt)
+    g = torch.clamp_min(-torch.nn.functional.softplus(torch.randn(T, H, d)), -5.0)
+    beta = torch.sigmoid(torch.randn(T, H))
+    S0 = 0.02 * torch.randn(len(lens), H, d, d)
+    K = max(lens) // every
+    ck = torch.full((len(lens), K, H, d, d), 7.0, device="cuda")
+    dev = lambda t: t.cuda()
+    kda.chunk_fwd(dev(q), dev(k), dev(v), dev(g), dev(beta), dev(cu), initial_state=dev(S0), cp_mode=cp,
+                  segment_len=seg, ckpt_every=every, ckpt=ck)
+    torch.cuda.synchronize()
+    ck = ck.cpu().double().numpy()
+    for n, L in enumerate(lens):
+        s0 = int(cu[n])
+        for kq in range(K):
+            P = every * (kq + 1)
+            if P > L:
+                assert np.all(ck[n, kq] == 7.0), "a slot past the sequence end was written"
+                continue
+            sl = slice(s0, s0 + P)
+            _, Sf = oracle.prefill(to64(q[sl]), to64(k[sl]), to64(v[sl]), to64(g[sl]), to64(beta[sl]),
+                                   np.array([0, P], dtype=np.int32), S0=to64(S0[n:n + 1]))
+            e = normwise_err(ck[n, kq][None], Sf, head_axis=1)
+            assert e <= STATE_TOL, f"sequence {n} checkpoint {kq}: state error {e:.3e}"
