@@ -20,10 +20,11 @@
 // dv (or dk) on the MMA's M = 128:
 //   batch 1   D[j][QX|KX rows]  = S0^T [QX hi|lo ; KX hi|lo]^T      (N = 64, K = dk)
 //             D[QX|KX rows][s]  = [QX hi|lo ; KX hi|lo] [KR hi|lo]^T (N = 32, K = dk)
-//   batch 2   U^T = P^T (T diag b)^T,   P = V - KX S0                (N = 16, K = 16)
-//   batch 3   S = K~^T U                                             (N = 128, K = 16)
-// and O = QX S0 + B U on the CUDA cores in fp32 while batch 3 runs.
-// Operands derived on chip (QX, KX, KR, K~, P, T diag b, U) are split into
+//   then      U = T diag(b) P, P = V - KX S0, as the fp32 forward substitution
+//             (I + A) U = diag(b) P, one value column per thread (no T formed)
+//   batch 2   S = K~^T U                                             (N = 128, K = 16)
+// and O = QX S0 + B U on the CUDA cores in fp32 while batch 2 runs.
+// Operands derived on chip (QX, KX, KR, K~, U) are split into
 // bf16 hi + lo parts and multiplied as hi*hi + hi*lo + lo*hi, which keeps
 // about 16 mantissa bits; the state is read once as bf16 (exact as an MMA
 // operand) and written back rounded once (nearest even).  The state tile moves
@@ -51,18 +52,18 @@ constexpr uint32_t OFF_KR = 49152;   // KR hi, KR lo: K-major 32 rows x dk; also
                                      // the M = 128 product over X reads past X (discarded)
 constexpr uint32_t OFF_RAW = OFF_X;  // before the operands: pre-conv rows [<= 18][q|k|v][128] bf16
 constexpr uint32_t OFF_GR = OFF_X + 18 * 768;  //   and g rows [<= 15][128] bf16, up to 50432
-constexpr uint32_t OFF_TB = 52224;   // after batch 1: T diag(b), 16 rows t, k = s: hi 0-15, lo 16-31
-constexpr uint32_t OFF_AF = 54272;   //   A fp32 [16][17]
+constexpr uint32_t OFF_PF = OFF_X;           // after batch 1: P = V - KX S0, fp32 [16][128]
+constexpr uint32_t OFF_UF = OFF_X + 8192;    //   U, fp32 [16][128]
+constexpr uint32_t OFF_AF = 54272;   //   A fp32 [16][16] (strictly lower)
 constexpr uint32_t OFF_BF = 55360;   //   B fp32 [16][16] (masked)
-constexpr uint32_t OFF_P = 57344;    // 128 rows; k 0-31: P^T (hi 0-15, lo 16-31) for batch 2, then
-                                     // K~^T (same split) for batch 3; k 32-63: U^T (hi, lo)
+constexpr uint32_t OFF_P = 57344;    // 128 rows; k 0-31: K~^T (hi 0-15, lo 16-31), k 32-63: U^T (hi, lo)
 constexpr uint32_t OFF_BETA = 73728; // fp32 [16]
 constexpr uint32_t OFF_RN = 73792;   // fp32 [32]: 1/||q_t||, 1/||k_t||
 constexpr uint32_t OFF_XA = 73920;   // fp32 [128]: x_a per key channel
 constexpr uint32_t OFF_CAR = 74432;  // fp32 [128]: x_7 per channel (decay carried to tokens 8-15)
 constexpr uint32_t OFF_PART = 74944; // fp32 [8][16] per-warp partial sums (input norms)
 constexpr uint32_t OFF_PART2 = 75456;// fp32 [8][8] per-warp partial sums (output norm)
-constexpr uint32_t OFF_BAR = 75712;  // 5 mbarriers: state tile, MMA batches 1-3, rows
+constexpr uint32_t OFF_BAR = 75712;  // 5 mbarriers: state tile, MMA batch 1, (spare), MMA batch 2, rows
 constexpr uint32_t OFF_TMEM = 75752; // tensor-memory base address
 constexpr uint32_t SMEM_BYTES = 75760 + 1024;  // + alignment slack; three CTAs fit one SM
 
@@ -70,7 +71,6 @@ constexpr uint32_t SMEM_BYTES = 75760 + 1024;  // + alignment slack; three CTAs 
 constexpr uint32_t TM_Q = 0;    // S0^T QX^T: hi tokens in columns 0-15, lo in 16-31
 constexpr uint32_t TM_K = 32;   // S0^T KX^T: hi 32-47, lo 48-63
 constexpr uint32_t TM_AB = 64;  // X KR^T, lanes 0-63 (32 columns)
-constexpr uint32_t TM_U = 96;   // U^T (16 columns)
 constexpr uint32_t TM_S = 0;    // K~^T U (128 columns, batch 3, after all of the above are read)
 constexpr uint32_t TMEM_COLS = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     float *sAf = reinterpret_cast<float *>(sm + OFF_AF);
+    float *sPf = reinterpret_cast<float *>(sm + OFF_PF);
+    float *sUf = reinterpret_cast<float *>(sm + OFF_UF);
     float *sBf = reinterpret_cast<float *>(sm + OFF_BF);
     float *sBeta = reinterpret_cast<float *>(sm + OFF_BETA);
     float *sRN = reinterpret_cast<float *>(sm + OFF_RN);
@@ -384,13 +386,13 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         umma::ld8(tq + TM_Q + 16 + t0, v1);
 #pragma unroll
         for (int j = 0; j < HT; ++j) qs[j] = v0[j] + v1[j];
-        // P = V - KX S0 for value column c, tokens t0 .. t0 + 7
+        // P = V - KX S0 for value column c, tokens t0 .. t0 + 7 (fp32, for the solve)
         umma::ld8(tq + TM_K + t0, v0);
         umma::ld8(tq + TM_K + 16 + t0, v1);
-        float pv[HT];
 #pragma unroll
-        for (int j = 0; j < HT; ++j) pv[j] = yv[j] - (v0[j] + v1[j]);
-        store_split8(sb + OFF_P + (uint32_t)c * 128u, c, hf, pv);
+        for (int j = 0; j < HT; ++j) sPf[(t0 + j) * D + c] = yv[j] - (v0[j] + v1[j]);
+        // K~^T operand (k = s: hi 0-15, lo 16-31), this half's tokens
+        store_split8(sb + OFF_P + (uint32_t)c * 128u, c, hf, kt);
     }
     if (ok && warp < 2) {
         // lane l holds X row 32*warp + l against KR hi (columns 0-15) and KR lo (16-31);
@@ -400,85 +402,61 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         float lh[VT];
 #pragma unroll
         for (int s = 0; s < VT; ++s) lh[s] = __shfl_down_sync(0xffffffffu, v[s], 16);
-        if (warp == 0) {
-            if (lane < VT) {  // B[t][s], s <= t, fp32
-                const int t = lane;
+        if (lane < VT) {
+            const int t = lane;
+            // warp 0: B[t][s], s <= t;  warp 1: A[t][s] = b_t KX_t . KR_s, s < t (fp32)
+            const bool isA = warp == 1;
+            const float bt = isA ? sBeta[t] : 1.f;
+            float *dst = isA ? sAf : sBf;
 #pragma unroll
-                for (int s = 0; s < VT; s += 4) {
-                    float4 b4;
-                    b4.x = (s + 0 <= t) ? (v[s + 0] + v[VT + s + 0]) + lh[s + 0] : 0.f;
-                    b4.y = (s + 1 <= t) ? (v[s + 1] + v[VT + s + 1]) + lh[s + 1] : 0.f;
-                    b4.z = (s + 2 <= t) ? (v[s + 2] + v[VT + s + 2]) + lh[s + 2] : 0.f;
-                    b4.w = (s + 3 <= t) ? (v[s + 3] + v[VT + s + 3]) + lh[s + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(sBf + t * 16 + s) = b4;
-                }
-            }
-        } else {
-            if (lane < VT) {  // A[t][s] = b_t KX_t . KR_s, s < t
-                const int t = lane;
-                const float bt = sBeta[t];
-#pragma unroll
-                for (int s = 0; s < VT; ++s) sAf[t * 17 + s] = (s < t) ? bt * ((v[s] + v[VT + s]) + lh[s]) : 0.f;
-            }
-            __syncwarp();
-            // T = (I + A)^{-1} by forward substitution, one column per lane;
-            // then column cc of T diag(b) into the operand tile
-            if (lane < VT) {
-                const int cc = lane;
-                float col[VT];
-#pragma unroll
-                for (int rr = 0; rr < VT; ++rr) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < rr; ++m) acc = fmaf(sAf[rr * 17 + m], col[m], acc);
-                    col[rr] = (rr == cc) ? 1.f : ((rr < cc) ? 0.f : -acc);
-                }
-                const float bc = sBeta[cc];
-                const uint32_t cb = sb + OFF_TB + ((uint32_t)(cc & 7) << 1);
-                const int ch = cc >> 3;
-#pragma unroll
-                for (int t = 0; t < VT; ++t) {
-                    uint16_t hi, lo;
-                    split2(col[t] * bc, hi, lo);
-                    sts16(cb + (uint32_t)(t * 128 + ((ch ^ (t & 7)) << 4)), hi);
-                    sts16(cb + (uint32_t)(t * 128 + (((2 + ch) ^ (t & 7)) << 4)), lo);
-                }
+            for (int s = 0; s < VT; s += 4) {
+                float4 x4;
+                x4.x = (isA ? (s + 0 < t) : (s + 0 <= t)) ? bt * ((v[s + 0] + v[VT + s + 0]) + lh[s + 0]) : 0.f;
+                x4.y = (isA ? (s + 1 < t) : (s + 1 <= t)) ? bt * ((v[s + 1] + v[VT + s + 1]) + lh[s + 1]) : 0.f;
+                x4.z = (isA ? (s + 2 < t) : (s + 2 <= t)) ? bt * ((v[s + 2] + v[VT + s + 2]) + lh[s + 2]) : 0.f;
+                x4.w = (isA ? (s + 3 < t) : (s + 3 <= t)) ? bt * ((v[s + 3] + v[VT + s + 3]) + lh[s + 3]) : 0.f;
+                *reinterpret_cast<float4 *>(dst + t * 16 + s) = x4;
             }
         }
     }
-    umma::fence_proxy_async();
-    umma::fence_before();
     ok = __syncthreads_and(ok) != 0;
 
-    // ---------------------------------------------------------------- batch 2: U^T
-    if (tid == 0 && ok) {
-        umma::fence_after();
-        constexpr uint32_t idu = umma::idesc_bf16(128, 16, 0, 0, 0);
-        const uint64_t pdh = umma::sdesc4(sb4 + (OFF_P >> 4), 16, 1024), pdl = umma::sdesc4(sb4 + ((OFF_P + 32) >> 4), 16, 1024);
-        const uint64_t tdh = umma::sdesc4(sb4 + (OFF_TB >> 4), 16, 1024), tdl = umma::sdesc4(sb4 + ((OFF_TB + 32) >> 4), 16, 1024);
-        umma::mma(tmem + TM_U, pdh, tdh, idu, 0u);
-        umma::mma(tmem + TM_U, pdh, tdl, idu, 1u);
-        umma::mma(tmem + TM_U, pdl, tdh, idu, 1u);
-        umma::commit(bar0 + 16);
-        ok = umma::mbar_wait(bar0 + 16, 0, WAIT_LIMIT);
+    // ---------------------------------------------------------------- U by forward substitution
+    // (I + A) U = diag(b) P, one value column per thread of the first half, fp32
+    // (the WY form's U = T diag(b) P without forming T)
+    if (ok && hf == 0) {
+        float u[VT];
+#pragma unroll
+        for (int t = 0; t < VT; ++t) {
+            float acc0 = sBeta[t] * sPf[t * D + c], acc1 = 0.f;
+#pragma unroll
+            for (int s4 = 0; s4 < t; s4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(sAf + t * 16 + s4);
+                acc0 = fmaf(-a4.x, u[s4], acc0);
+                if (s4 + 1 < t) acc1 = fmaf(-a4.y, u[s4 + 1], acc1);
+                if (s4 + 2 < t) acc0 = fmaf(-a4.z, u[s4 + 2], acc0);
+                if (s4 + 3 < t) acc1 = fmaf(-a4.w, u[s4 + 3], acc1);
+            }
+            u[t] = acc0 + acc1;
+        }
+#pragma unroll
+        for (int t = 0; t < VT; ++t) sUf[t * D + c] = u[t];
     }
     ok = __syncthreads_and(ok) != 0;
-    umma::fence_after();
     float uu[VT];
     if (ok) {
-        umma::ld16(tq + TM_U, uu);
-        const uint32_t row = sb + OFF_P + (uint32_t)c * 128u;
+#pragma unroll
+        for (int t = 0; t < VT; ++t) uu[t] = sUf[t * D + c];
         float uh[HT];  // this half's tokens (a register select, not an indexed array)
 #pragma unroll
         for (int j = 0; j < HT; ++j) uh[j] = hf ? uu[HT + j] : uu[j];
-        store_split8(row, c, 4 + hf, uh);  // U^T, k = 32 + s
-        store_split8(row, c, hf, kt);      // K~^T over P^T (consumed by batch 2)
+        store_split8(sb + OFF_P + (uint32_t)c * 128u, c, 4 + hf, uh);  // U^T, k = 32 + s
     }
     umma::fence_proxy_async();
     umma::fence_before();
     ok = __syncthreads_and(ok) != 0;
 
-    // ---------------------------------------------------------------- batch 3: state
+    // ---------------------------------------------------------------- batch 2: state
     if (tid == 0 && ok) {
         umma::fence_after();
         constexpr uint32_t ids = umma::idesc_bf16(128, 128, 0, 0, 0);
