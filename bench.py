@@ -4,7 +4,8 @@ One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
 32K-token, 96-head, d=128 bf16 workload, inputs resident in HBM, one
 kda_chunk_fwd launch per step.  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
-  "decode": the same kernel as single-token decode (window 0) on 256 x 96
+  "ckpt":   the headline prefill also emitting the state every 4096 tokens
+  "decode": the same entry point as single-token decode (window 0) on 256 x 96
   "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
   "cp":     1M-token, 12-head prefill with the context-parallel schedule
   "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches".
@@ -209,6 +210,16 @@ def run_reference(args):
     return 0
 
 
+def verify_kernel_name():
+    return "kda_verify_kernel<128>" if os.environ.get("KDA_VERIFY_TC", "1") == "0" else "kda_verify_tc_kernel"
+
+
+def decode_workload(synth):
+    """Single-token decode: 256 requests x 96 heads, d = 128, conv width 4, no draft window."""
+    return synth.DecodeWorkload("decode R=256 H=96 d=128 W=4 one token (window 0)", 256, 96, 128, 128,
+                                Wd=0, seed=5)
+
+
 def run_profile(args):
     """Plain launches of one kernel family on a chosen size (for ncu captures)."""
     import torch
@@ -225,7 +236,10 @@ def run_profile(args):
             kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
                           cp_mode=kda.CP_AUTO if args.profile == "cp" else kda.CP_OFF)
     else:
-        d = synth.make_decode(synth.VERIFY, device="cuda", R_override=args.R or None)
+        dw = synth.VERIFY if args.profile == "verify" else decode_workload(synth)
+        R = args.R or dw.R
+        d = synth.make_decode(dw, device="cuda", R_override=R,
+                              accepted=None if args.profile == "verify" else [0] * R)
         for _ in range(n):
             kda.decode_verify_replay(d["state"], d["tail"], d["conv_w"], d["cached_qkv"], d["cached_g"],
                                      d["cached_b"], d["accepted"], d["new_qkv"], d["new_g"], d["new_b"],
@@ -243,10 +257,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of prefill,verify,decode,varlen,cp (default: all)")
-    ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "cp"],
+    ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "decode", "cp"],
                     help="launch only this kernel family (warmup + steps launches, no JSON) for ncu")
     ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp")
-    ap.add_argument("--R", type=int, default=0, help="request count override for --profile verify")
+    ap.add_argument("--R", type=int, default=0, help="request count override for --profile verify/decode")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
@@ -303,6 +317,23 @@ def main(argv=None):
     launches = K  # one kda_chunk_fwd launch per step (CP resolves off at 96 heads)
     out["prefill"] = {"ms": ms, "tok_s": tok_s}
 
+    # the same launch emitting the state every 4096 tokens (8 checkpoints per head)
+    every = 4096
+    ck = torch.empty((1, T // every, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+
+    def ckpt_step():
+        kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], out=o,
+                      final_state=Sf, cp_mode=kda.CP_AUTO, ckpt_every=every, ckpt=ck)
+
+    for _ in range(2):
+        ckpt_step()
+    ms_ck = reduce_max(cuda_time(ckpt_step, K, stream), ws)
+    out["ckpt"] = {"workload": f"{w.name}, state every {every} tokens", "ms": ms_ck,
+                   "tok_s": ws * T / (ms_ck * 1e-3), "overhead_vs_plain": ms_ck / ms - 1.0,
+                   "checkpoint_bytes_per_launch": ck.numel() * 4}
+    launches += K
+    del ck
+
     # e2e: host buffers through the same C-ABI call, copies inside the timed region
     host = {k: v.to("cpu").pin_memory() for k, v in inp.items() if v is not None}
     o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -329,8 +360,7 @@ def main(argv=None):
     # ------------------------------------------------------------ verify-replay
     if "verify" in only:
         vw = synth.VERIFY
-        verify_kernel = ("kda_verify_kernel<128>" if os.environ.get("KDA_VERIFY_TC", "1") == "0"
-                         else "kda_verify_tc_kernel")
+        verify_kernel = verify_kernel_name()
         d = synth.make_decode(vw, device="cuda")
         st, tl = d["state"].clone(), d["tail"].clone()
         ov = torch.empty((vw.R, vw.Wd + 1, vw.H, vw.dv), dtype=torch.bfloat16, device="cuda")
@@ -361,8 +391,9 @@ def main(argv=None):
 
     # ------------------------------------------------------------ single-token decode (window 0)
     if "decode" in only:
-        dw = synth.DecodeWorkload("decode R=256 H=96 d=128 W=4 one token (window 0)", 256, 96, 128, 128,
-                                  Wd=0, seed=5)
+        dw = decode_workload(synth)
+        decode_kernel = ("kda_decode_token_kernel<128>" if os.environ.get("KDA_DECODE_TOKEN", "1") != "0"
+                         else verify_kernel_name())
         d = synth.make_decode(dw, device="cuda", accepted=[0] * dw.R)
         st, tl = d["state"].clone(), d["tail"].clone()
         od = torch.empty((dw.R, 1, dw.H, dw.dv), dtype=torch.bfloat16, device="cuda")
@@ -379,7 +410,8 @@ def main(argv=None):
         total_bytes = state_bytes + dw.R * row + 2 * tl.numel() * tl.element_size() + od.numel() * od.element_size()
         out["decode"] = {"workload": dw.name, "ms": dms, "state_gbs": ws * state_bytes / (dms * 1e-3) / 1e9,
                          "frac_hbm": (total_bytes / (dms * 1e-3) / 1e9) / peaks["hbm_gbs"],
-                         "bytes_per_launch": total_bytes, "tokens_per_s": ws * dw.R / (dms * 1e-3)}
+                         "bytes_per_launch": total_bytes, "tokens_per_s": ws * dw.R / (dms * 1e-3),
+                         "kernel": decode_kernel, "traffic": kernel_traffic(decode_kernel, dw.R)}
         launches += K
         del d, st, tl, od
         torch.cuda.empty_cache()

@@ -99,7 +99,17 @@ int kda_version(void);
  *  segment_len  CP segment length in tokens (multiple of 64), or 0 = automatic.
  *  workspace    device scratch of at least kda_chunk_fwd_workspace_size(...)
  *               bytes (may be NULL when that size is 0).  Contents on entry
- *               are ignored; on exit they are unspecified.
+ *               are ignored; on exit they are unspecified.  With bf16 inputs
+ *               and dk = dv = 128, a workspace of at least
+ *               kda_chunk_fwd_prep_workspace_size(...) bytes selects the
+ *               two-kernel form: the chunk-local products of every (chunk,
+ *               head) (decays, causal tiles, the dependency inverse, W, the
+ *               decayed q and k) run first, in parallel over all chunks, into
+ *               an operand area of the workspace; then each (sequence or
+ *               segment, head) walks its chunks with only the state products
+ *               left on its serial path.  Same results as the one-kernel form
+ *               (same operations in the same order); a smaller workspace runs
+ *               the one-kernel form.
  *  status       device uint32 status word or NULL.
  */
 int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
@@ -134,6 +144,17 @@ int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v, const float 
  * resolves to OFF).  Pure host arithmetic. */
 size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,
                                     int segment_len);
+
+/* Workspace bytes that select kda_chunk_fwd's two-kernel form (bf16 inputs,
+ * dk = dv = 128): the CP scratch above, then a slot list (8 bytes per 64-token
+ * chunk slot; floor(T / 64) + units slots, units = sequences or segments), two
+ * carry states (2 x 2 x H x 128 x 128 f32) and the operand blobs of up to
+ * 2 GiB of slots (66,048 bytes per chunk and head; longer inputs run in equal
+ * pieces of slots).  Equals kda_chunk_fwd_workspace_size for other shapes.
+ * Pure host arithmetic; this form has no counterpart on the pages beyond the
+ * chunk algebra it reorders. */
+size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,
+                                         int segment_len);
 
 /* The segment length (tokens) and CP decision kda_chunk_fwd would use:
  * returns 0 when CP is off, else the segment length. Pure host arithmetic. */

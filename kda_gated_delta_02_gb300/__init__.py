@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_plan", "segment_transition",
+__all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_prep_workspace_size", "chunk_fwd_plan", "segment_transition",
            "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
            "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
            "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW"]
@@ -60,6 +60,8 @@ def load_library():
                                            I, I, P, P, P]
         lib.kda_chunk_fwd_workspace_size.restype = S
         lib.kda_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_chunk_fwd_prep_workspace_size.restype = S
+        lib.kda_chunk_fwd_prep_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.kda_chunk_fwd_plan.restype = I
         lib.kda_chunk_fwd_plan.argtypes = [I, I, I, I, I, I, I]
         lib.kda_segment_transition.restype = I
@@ -106,19 +108,25 @@ def chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) ->
     return int(load_library().kda_chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len))
 
 
+def chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
+    return int(load_library().kda_chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len))
+
+
 def chunk_fwd_plan(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
     return int(load_library().kda_chunk_fwd_plan(N, T, H, dk, dv, cp_mode, segment_len))
 
 
 def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,
               g_min=-5.0, cp_mode=CP_AUTO, segment_len=0, out=None, final_state=None,
-              workspace=None, status=None, stream=None, ckpt_every=0, ckpt=None):
+              workspace=None, status=None, stream=None, ckpt_every=0, ckpt=None, prep=True):
     """Chunkwise KDA prefill.  q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H];
     cu_seqlens int32 [N+1]; initial_state f32 [N,H,dk,dv] or None.
     Returns (o [T,H,dv] in q's dtype, final_state f32 [N,H,dk,dv] or None).
     With ckpt_every > 0 (a multiple of 64) also writes the state after every
     ckpt_every tokens of each sequence into ckpt f32 [N,K,H,dk,dv] (K = its
-    second dimension) through kda_chunk_fwd_ckpt."""
+    second dimension) through kda_chunk_fwd_ckpt.  With prep (the default) a
+    bf16, dk = dv = 128 call gets the workspace of the two-kernel form; a
+    caller-provided workspace is used as given when it is large enough."""
     lib = load_library()
     T, H, dk = k.shape
     dv = v.shape[2]
@@ -127,7 +135,10 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
         out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+    if prep and q.dtype == torch.bfloat16:
+        ws_bytes = chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+    else:
+        ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,

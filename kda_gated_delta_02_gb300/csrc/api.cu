@@ -86,6 +86,67 @@ CpLayout cp_layout(int N, int T, int H, int dk, int dv, int cp_mode, int segment
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Two-kernel tcgen05 prefill (dk = dv = 128): workspace after the CP scratch =
+// slot list | two carry states [2 tiles][H][128][128] f32 | operand blobs of
+// one piece of slots.  The blob area is capped (KDA_PREP_BUDGET_MB, default
+// 2048 MiB); longer inputs run as several pieces of equal size.
+struct SplitLayout {
+    int nslots = 0, piece = 0;
+    size_t off_list = 0, off_carry = 0, carry_stride = 0, off_blob = 0, total = 0;
+};
+
+SplitLayout split_layout(int units, int T, int H) {
+    SplitLayout S;
+    S.nslots = T / kChunk + units;
+    const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
+    size_t budget_mb = 2048;
+    if (const char *env = getenv("KDA_PREP_BUDGET_MB")) {
+        const long v = atol(env);
+        if (v > 0) budget_mb = (size_t)v;
+    }
+    long piece = (long)((budget_mb << 20) / per_slot);
+    if (piece < 1) piece = 1;
+    if (piece > S.nslots) piece = S.nslots;
+    const long pieces = (S.nslots + piece - 1) / piece;
+    S.piece = (int)((S.nslots + pieces - 1) / pieces);
+    size_t o = 0;
+    S.off_list = o;
+    o = align256(o + (size_t)S.nslots * 8);
+    S.off_carry = o;
+    S.carry_stride = (size_t)2 * H * 128 * 128;  // floats per carry state
+    o = align256(o + 2 * S.carry_stride * 4);
+    S.off_blob = o;
+    o = align256(o + (size_t)S.piece * per_slot);
+    S.total = o;
+    return S;
+}
+
+bool split_enabled() {
+    const char *a = getenv("KDA_PREFILL_SPLIT"), *b = getenv("KDA_PREFILL_TC");
+    return !(a && a[0] == '0') && !(b && b[0] == '0');
+}
+
+// One pass of the two-kernel prefill over `units` units: the chunk list, then
+// per piece the chunk-local kernel and the walk.  With skip_prep the blobs of
+// a single piece are already in place (written by an earlier pass with
+// need_q set).
+cudaError_t run_split(const kda::ChunkArgs &a, int units, unsigned char *ws, const SplitLayout &S, bool need_q,
+                      bool skip_prep, cudaStream_t st) {
+    int2 *list = reinterpret_cast<int2 *>(ws + S.off_list);
+    float *carry = reinterpret_cast<float *>(ws + S.off_carry);
+    unsigned char *blob = ws + S.off_blob;
+    cudaError_t e = cudaSuccess;
+    if (!skip_prep) e = kda::launch_chunk_list(a, units, S.nslots, list, st);
+    for (int s0 = 0, pc = 0; e == cudaSuccess && s0 < S.nslots; s0 += S.piece, ++pc) {
+        const int s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
+        if (!skip_prep) e = kda::launch_chunk_prep(a, list, s0, s1, blob, need_q, st);
+        if (e == cudaSuccess)
+            e = kda::launch_chunk_walk(a, units, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
+                                       carry + (size_t)((pc + 1) & 1) * S.carry_stride, st);
+    }
+    return e;
+}
+
 // Chunk-kernel dispatch by shape: the tcgen05 / tensor-memory kernel for
 // dk = dv = 128 with bf16 inputs, the warp-level kernel otherwise.
 // KDA_PREFILL_TC=0 selects the warp-level kernel everywhere (comparisons).
@@ -117,6 +178,13 @@ int kda_version(void) { return 100; }
 
 size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
     return cp_layout(N, T, H, dk, dv, cp_mode, segment_len).total;
+}
+
+size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
+    const CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
+    if (dk != 128 || dv != 128 || N < 1 || T < 0 || H < 1) return L.total;
+    const int units = L.seg_len ? L.P_max : N;
+    return align256(L.total) + split_layout(units, T, H).total;
 }
 
 int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
@@ -155,15 +223,27 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     }
 
     CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
+    // the two-kernel path when the workspace also holds its area
+    SplitLayout SL;
+    const size_t split_off = align256(L.total);
+    bool split = bf && dk == 128 && dv == 128 && workspace && T > 0 && split_enabled();
+    if (split) {
+        SL = split_layout(L.seg_len ? L.P_max : N, T, H);
+        split = workspace_bytes >= split_off + SL.total;
+    }
+    unsigned char *wsplit = split ? static_cast<unsigned char *>(workspace) + split_off : nullptr;
     if (L.seg_len == 0) {
         a.mode = kda::MODE_SEQ;
         a.cu_seqlens = cu_seqlens;
         a.S_init = initial_state;
         a.S_final = final_state;
+        if (split) return cuda_status(run_split(a, N, wsplit, SL, true, false, st));
         return cuda_status(run_chunk(a, N, bf, st));
     }
     if (!workspace || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
+    // one piece: the blobs written for the transitions (with Q~ and B) serve the replay too
+    const bool one_piece = split && SL.piece >= SL.nslots;
     int32_t *count = reinterpret_cast<int32_t *>(ws + L.off_count);
     int32_t *table = reinterpret_cast<int32_t *>(ws + L.off_table);
     int32_t *first = reinterpret_cast<int32_t *>(ws + L.off_first);
@@ -183,7 +263,7 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     {
         kda::ChunkArgs at = a;  // transitions emit no checkpoints
         at.ckpt = nullptr;
-        e = run_chunk(at, L.P_max, bf, st);
+        e = split ? run_split(at, L.P_max, wsplit, SL, one_piece, false, st) : run_chunk(at, L.P_max, bf, st);
     }
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     // pass 2: ordered scan per (sequence, head)
@@ -197,6 +277,7 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     a.S_in = Sin;
     a.S_final = final_state;
     a.M_out = a.N_out = nullptr;
+    if (split) return cuda_status(run_split(a, L.P_max, wsplit, SL, true, one_piece, st));
     return cuda_status(run_chunk(a, L.P_max, bf, st));
 }
 

@@ -41,6 +41,21 @@ cudaError_t launch_chunk(const ChunkArgs &a, int units, int dvt, bool in_bf16, c
 // tcgen05 / tensor-memory version of the chunk kernel (dk = dv = 128, bf16).
 bool chunk_tc_supported(const ChunkArgs &a, bool in_bf16);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st);
+// The same prefill as two kernels (chunk_split_tc.cu): the chunk-local
+// products of every (chunk, head) in parallel, written as one operand blob of
+// kChunkBlobBytes per (chunk, head), then the state walk over the blobs.
+// Chunk j of unit u (tokens [t0, t1)) is slot floor(t0 / 64) + u + j.
+constexpr unsigned kChunkBlobBytes = 66048;
+// list[slot] = {first token, length} for every chunk of units [0, units), 0 elsewhere
+cudaError_t launch_chunk_list(const ChunkArgs &a, int units, int nslots, int2 *list, cudaStream_t st);
+// blobs of slots [slot0, slot1) into blob[(slot - slot0) * H + h]
+cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
+                              bool need_q, cudaStream_t st);
+// the chunks of every unit that fall in slots [slot0, slot1); a unit cut at
+// slot0 starts from carry_in, one cut at slot1 leaves its state in carry_out
+// ([tiles][H][128][128] fp32 each)
+cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char *blob, int slot0, int slot1,
+                              const float *carry_in, float *carry_out, cudaStream_t st);
 // The driver's tensor-map encoder (cuTensorMapEncodeTiled), reached through
 // the runtime's entry-point query; null when the driver does not provide it.
 void *tensor_map_encoder();
