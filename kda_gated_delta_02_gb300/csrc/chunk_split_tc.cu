@@ -104,10 +104,10 @@ constexpr uint32_t P_TF = 17408;     // T fp32 [64][68]
 constexpr uint32_t P_KG = 73728;     // K e^gamma, MN-major (s x dk)
 constexpr uint32_t P_TB = 90112;     // T diag(b), K-major 64 x 64
 constexpr uint32_t P_BETA = 98304;   // f32 [64]
-constexpr uint32_t P_DEL = 98560;    // f32 [4][128] block decays
-constexpr uint32_t P_BAR = 100608;   // 2 mbarriers: A/B product, W product
-constexpr uint32_t P_TMEM = 100624;  // tensor-memory base address
-constexpr uint32_t P_SMEM = 100640 + 1024;
+constexpr uint32_t P_PART = 98560;   // f32 [2][4][128] half-block products
+constexpr uint32_t P_BAR = 102656;   // 2 mbarriers: A/B product, W product
+constexpr uint32_t P_TMEM = 102672;  // tensor-memory base address
+constexpr uint32_t P_SMEM = 102688 + 1024;
 constexpr int LDF = 68;
 constexpr uint32_t TM1_AB = 0, TM1_W = 160;  // 224 of 256 columns
 
@@ -118,8 +118,9 @@ struct PrepParams {
     int H;
     float g_min;
     const int2 *list;    // slot -> {first token, length}
-    int slot0;           // first slot of this launch (blockIdx.x = slot - slot0)
-    unsigned char *blob; // [(slot - slot0) * H + h][kChunkBlobBytes]
+    int slot0;           // first slot of this launch
+    int nitems;          // (slot1 - slot0) * H items, w = (slot - slot0) * H + h
+    unsigned char *blob; // [w][kChunkBlobBytes]
     int need_q;          // 0: transitions only (no Q~, no B)
     uint32_t *status;
 };
@@ -130,149 +131,184 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y, H = p.H;
-    const int2 cl = p.list[p.slot0 + blockIdx.x];
-    const int tc = cl.x, Lc = cl.y;
-    if (Lc <= 0) return;
-    unsigned char *out = p.blob + ((size_t)blockIdx.x * H + h) * kChunkBlobBytes;
+    const int H = p.H, nitems = p.nitems, G = gridDim.x;
     float *sBeta = reinterpret_cast<float *>(sm + P_BETA);
-    float *sDel = reinterpret_cast<float *>(sm + P_DEL);
+    float *sPart = reinterpret_cast<float *>(sm + P_PART);
     const uint32_t bar_ab = sb + P_BAR, bar_w = sb + P_BAR + 8;
     const bool need_q = p.need_q != 0;
     const float g_min = p.g_min;
 
-    // ---------------------------------------------------------------- loads
-    // thread (channel pair c2, block i): channels 2 c2, 2 c2 + 1 of tokens
-    // 16 i .. 16 i + 15; rows past the chunk end read as zero (g = 0 -> e = 1)
-    const int c2 = tid & 63, i = tid >> 6, ch = 2 * c2;
-    float2 e[16];
-    uint32_t kraw[16], qraw[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const int t = 16 * i + r;
-        const bool ok = t < Lc;
-        const size_t row = ((size_t)(tc + t) * H + h) * D;  // element offset of the token's row
-        e[r] = ok ? __ldg(reinterpret_cast<const float2 *>(p.g + row) + c2) : make_float2(0.f, 0.f);
-        kraw[r] = ok ? __ldg(reinterpret_cast<const unsigned int *>(p.k) + (row >> 1) + c2) : 0u;
-        qraw[r] = (ok && need_q) ? __ldg(reinterpret_cast<const unsigned int *>(p.q) + (row >> 1) + c2) : 0u;
-    }
-    if (tid < CH) sBeta[tid] = (tid < Lc) ? p.beta[(size_t)(tc + tid) * H + h] : 0.f;
     if (tid == 0) {
         umma::mbar_init(bar_ab, 1);
         umma::mbar_init(bar_w, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 0) umma::tmem_alloc(sb + P_TMEM, 256);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<const uint32_t *>(sm + P_TMEM);
+    const int qd = warp & 3;  // TMEM lane quadrant of this warp
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+
+    // Items w = (slot - slot0) * H + h, strided over the resident CTAs.  While
+    // item w runs, the rows of item w + G are prefetched into L2 (its chunk
+    // entry was read one item earlier), so its loads do not wait on DRAM.
+    bool alive = true;
+    uint32_t it = 0;  // items processed (mbarrier parity)
+    int w = blockIdx.x;
+    int2 cl = (w < nitems) ? p.list[p.slot0 + w / H] : make_int2(0, 0);
+    int2 ncl = (w + G < nitems) ? p.list[p.slot0 + (w + G) / H] : make_int2(0, 0);
+    for (; w < nitems; w += G) {
+    const int h = w % H;
+    const int tc = cl.x, Lc = cl.y;
+    int2 nncl = make_int2(0, 0);
+    {
+        const int wn = w + G;
+        if (wn < nitems && ncl.y > 0) {
+            const int hn = wn % H, t = tid & 63, kind = tid >> 6;
+            if (t < ncl.y) {
+                const size_t row = ((size_t)(ncl.x + t) * H + hn) * D;
+                if (kind == 0) {
+                    if (need_q) umma::prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(p.q) + row, 256);
+                } else if (kind == 1) {
+                    umma::prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(p.k) + row, 256);
+                } else if (kind == 2) {
+                    umma::prefetch_l2(p.g + row, 512);
+                } else {
+                    const uintptr_t ba = reinterpret_cast<uintptr_t>(p.beta + (size_t)(ncl.x + t) * H + hn);
+                    umma::prefetch_l2(reinterpret_cast<const void *>(ba & ~(uintptr_t)15), 16);
+                }
+            }
+        }
+        if (w + 2 * G < nitems) nncl = p.list[p.slot0 + (w + 2 * G) / H];
+    }
+    if (Lc > 0) {
+    unsigned char *out = p.blob + ((size_t)w * kChunkBlobBytes);
+
+    // ---------------------------------------------------------------- loads
+    // warp w = half block (block i = w / 2, half hf = w % 2, tokens 8 w .. 8 w + 7),
+    // lane = channel quad (channels 4 lane .. 4 lane + 3); rows past the chunk
+    // end read as zero (g = 0 -> e = 1)
+    const int i = warp >> 1, hf = warp & 1, ch = 4 * lane, tb = 8 * warp;
+    float4 e[8];
+    uint2 kraw[8], qraw[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int t = tb + r;
+        const bool ok = t < Lc;
+        const size_t row = ((size_t)(tc + t) * H + h) * D;  // element offset of the token's row
+        e[r] = ok ? __ldg(reinterpret_cast<const float4 *>(p.g + row) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        kraw[r] = ok ? __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) + row) + lane)
+                     : make_uint2(0u, 0u);
+        qraw[r] = (ok && need_q)
+                      ? __ldg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) + row) + lane)
+                      : make_uint2(0u, 0u);
+    }
+    if (tid < CH) sBeta[tid] = (tid < Lc) ? p.beta[(size_t)(tc + tid) * H + h] : 0.f;
 
     // ---------------------------------------------------------------- decays
     // running products of e^{g} inside each 8-token half block, combined as in
     // the single-kernel version: x_t = prod_{block start <= r <= t}, y_t =
     // prod_{t < r <= block end}, delta_i = block product
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
+    for (int r = 0; r < 8; ++r) {
         e[r].x = __expf(fmaxf(e[r].x, g_min));
         e[r].y = __expf(fmaxf(e[r].y, g_min));
+        e[r].z = __expf(fmaxf(e[r].z, g_min));
+        e[r].w = __expf(fmaxf(e[r].w, g_min));
     }
-    float2 p0 = make_float2(1.f, 1.f), p1 = make_float2(1.f, 1.f);
+    {
+        float4 ph = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        p0.x *= e[r].x;
-        p0.y *= e[r].y;
-        p1.x *= e[8 + r].x;
-        p1.y *= e[8 + r].y;
+        for (int r = 0; r < 8; ++r) {
+            ph.x *= e[r].x;
+            ph.y *= e[r].y;
+            ph.z *= e[r].z;
+            ph.w *= e[r].w;
+        }
+        *reinterpret_cast<float4 *>(sPart + (hf * 4 + i) * 128 + ch) = ph;
     }
-    *reinterpret_cast<float2 *>(sDel + i * 128 + ch) = make_float2(p0.x * p1.x, p0.y * p1.y);
-    umma::fence_before();
     __syncthreads();
-    umma::fence_after();
-    const uint32_t tmem = *reinterpret_cast<const uint32_t *>(sm + P_TMEM);
-    float2 dl[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) dl[m] = *reinterpret_cast<const float2 *>(sDel + m * 128 + ch);
-    float2 gb = make_float2(1.f, 1.f), cc = make_float2(1.f, 1.f);
+    auto mul4 = [](float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); };
+    float4 dl[4], pz;  // block decays; the other half's product for this thread's half
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        if (m < i) { gb.x *= dl[m].x; gb.y *= dl[m].y; }
-        if (m > i) { cc.x *= dl[m].x; cc.y *= dl[m].y; }
+        const float4 a0 = *reinterpret_cast<const float4 *>(sPart + (0 * 4 + m) * 128 + ch);
+        const float4 a1 = *reinterpret_cast<const float4 *>(sPart + (1 * 4 + m) * 128 + ch);
+        dl[m] = mul4(a0, a1);
+        if (m == i) pz = hf ? a0 : a1;
     }
-    if (i == 0) {
-        *reinterpret_cast<float2 *>(out + BL_GAM + ch * 4) = make_float2(
-            ((dl[0].x * dl[1].x) * dl[2].x) * dl[3].x, ((dl[0].y * dl[1].y) * dl[2].y) * dl[3].y);
+    float4 gb = make_float4(1.f, 1.f, 1.f, 1.f), cc = gb;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        if (m < i) gb = mul4(gb, dl[m]);
+        if (m > i) cc = mul4(cc, dl[m]);
     }
+    if (warp == 0)
+        *reinterpret_cast<float4 *>(out + BL_GAM + ch * 4) = mul4(mul4(mul4(dl[0], dl[1]), dl[2]), dl[3]);
     // right-operand factors for row blocks i2 >= i: 1/delta_i (i2 == i), c_{i2,i} otherwise
-    float2 vf[4];
+    float4 vf[4];
 #pragma unroll
     for (int i2 = 0; i2 < 4; ++i2) {
-        float2 f = make_float2(1.f, 1.f);
+        float4 f = make_float4(1.f, 1.f, 1.f, 1.f);
         if (i2 == i) {
-            f = make_float2(__frcp_rn(dl[i].x), __frcp_rn(dl[i].y));
+            f = make_float4(__frcp_rn(dl[i].x), __frcp_rn(dl[i].y), __frcp_rn(dl[i].z), __frcp_rn(dl[i].w));
         } else {
 #pragma unroll
             for (int m = 0; m < 4; ++m)
-                if (m > i && m < i2) { f.x *= dl[m].x; f.y *= dl[m].y; }
+                if (m > i && m < i2) f = mul4(f, dl[m]);
         }
         vf[i2] = f;
     }
 
     // ---------------------------------------------------------------- operands
-    // Every destination row of token r has (row & 7) == (r & 7): one swizzled
-    // column offset per r serves all operands.  L, R and K e^gamma stay in
-    // shared memory (operands here); Q~ and K~ go straight to the blob.
+    // Every destination row of token r has (row & 7) == r: one swizzled column
+    // offset per r serves all operands; each lane stores 8 bytes (4 channels).
+    // L, R and K e^gamma stay in shared memory (operands here); Q~ and K~ go
+    // straight to the blob.  x-side operands in a forward pass, y-side ones in
+    // a backward pass (x_t and y_t are running products in opposite directions).
     {
         const uint32_t c8 = (uint32_t)(ch & 63) >> 3, lo = (uint32_t)(ch & 7) << 1, kb = (uint32_t)ch >> 6;
+        const uint32_t aL = sb + P_L + kb * 16384u + (uint32_t)(32 * i + 8 * hf) * 128u;
+        const uint32_t aRk = sb + P_R + kb * R_KB + (uint32_t)tb * 128u;
+        const uint32_t atom = ((uint32_t)warp * 2u + kb) * 1024u;
+        const uint32_t aKG = sb + P_KG + atom;
+        unsigned char *gKT = out + BL_KT + atom;
+        unsigned char *gQT = out + BL_QT + kb * 8192u + (uint32_t)tb * 128u;
+        auto pk2 = [](float4 v) { return make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w)); };
+        float4 pr = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float2 xl[8], yl[8];
-            float2 pr = make_float2(1.f, 1.f);
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t o = (uint32_t)r * 128u + ((c8 ^ (uint32_t)r) << 4) + lo;
+            pr = mul4(pr, e[r]);
+            const float4 x = hf ? mul4(pr, pz) : pr;
+            const float2 k01 = unpack_bf16(kraw[r].x), k23 = unpack_bf16(kraw[r].y);
+            const float4 lk = mul4(make_float4(k01.x, k01.y, k23.x, k23.y), x);
+            const uint2 lkp = pk2(lk), kgp = pk2(mul4(lk, gb));
+            sts64(aL + o, lkp.x, lkp.y);
+            sts64(aKG + o, kgp.x, kgp.y);
+            const float2 q01 = unpack_bf16(qraw[r].x), q23 = unpack_bf16(qraw[r].y);
+            const float4 lq = mul4(make_float4(q01.x, q01.y, q23.x, q23.y), x);
+            const uint2 lqp = pk2(lq);
+            sts64(aL + 2048u + o, lqp.x, lqp.y);
+            if (need_q) *reinterpret_cast<uint2 *>(gQT + o) = pk2(mul4(lq, gb));
+        }
+        float4 sf = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                pr.x *= e[8 * hh + r].x;
-                pr.y *= e[8 * hh + r].y;
-                xl[r] = pr;
-            }
-            float2 sf = make_float2(1.f, 1.f);
-#pragma unroll
-            for (int r = 7; r >= 0; --r) {
-                yl[r] = sf;
-                sf.x *= e[8 * hh + r].x;
-                sf.y *= e[8 * hh + r].y;
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                if (hh == 0) {
-                    yl[r].x *= p1.x;
-                    yl[r].y *= p1.y;
-                } else {
-                    xl[r].x *= p0.x;
-                    xl[r].y *= p0.y;
-                }
-            }
-            const int tb = 16 * i + 8 * hh;
-            const uint32_t aL = sb + P_L + kb * 16384u + (uint32_t)(32 * i + 8 * hh) * 128u;
-            const uint32_t aRk = sb + P_R + kb * R_KB + (uint32_t)tb * 128u;
-            const uint32_t atom = ((uint32_t)(2 * i + hh) * 2u + kb) * 1024u;
-            const uint32_t aKG = sb + P_KG + atom;
-            unsigned char *gKT = out + BL_KT + atom;
-            unsigned char *gQT = out + BL_QT + kb * 8192u + (uint32_t)tb * 128u;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const uint32_t o = (uint32_t)r * 128u + ((c8 ^ (uint32_t)r) << 4) + lo;
-                const float2 kv = unpack_bf16(kraw[8 * hh + r]);
-                const float2 x = xl[r], y = yl[r];
-                const float2 lk = make_float2(kv.x * x.x, kv.y * x.y);
-                const float2 ky = make_float2(kv.x * y.x, kv.y * y.y);
-                sts32(aL + o, pack_bf16(lk.x, lk.y));
-                if (i <= 0) sts32(aRk + r_row(0) * 128u + o, pack_bf16(ky.x * vf[0].x, ky.y * vf[0].y));
-                if (i <= 1) sts32(aRk + r_row(1) * 128u + o, pack_bf16(ky.x * vf[1].x, ky.y * vf[1].y));
-                if (i <= 2) sts32(aRk + r_row(2) * 128u + o, pack_bf16(ky.x * vf[2].x, ky.y * vf[2].y));
-                sts32(aRk + r_row(3) * 128u + o, pack_bf16(ky.x * vf[3].x, ky.y * vf[3].y));
-                sts32(aKG + o, pack_bf16(lk.x * gb.x, lk.y * gb.y));
-                *reinterpret_cast<uint32_t *>(gKT + o) = pack_bf16(ky.x * cc.x, ky.y * cc.y);
-                const float2 qv = unpack_bf16(qraw[8 * hh + r]);
-                const float2 lq = make_float2(qv.x * x.x, qv.y * x.y);
-                sts32(aL + 2048u + o, pack_bf16(lq.x, lq.y));
-                if (need_q) *reinterpret_cast<uint32_t *>(gQT + o) = pack_bf16(lq.x * gb.x, lq.y * gb.y);
-            }
+        for (int r = 7; r >= 0; --r) {
+            const uint32_t o = (uint32_t)r * 128u + ((c8 ^ (uint32_t)r) << 4) + lo;
+            const float4 y = hf ? sf : mul4(sf, pz);
+            const float2 k01 = unpack_bf16(kraw[r].x), k23 = unpack_bf16(kraw[r].y);
+            const float4 ky = mul4(make_float4(k01.x, k01.y, k23.x, k23.y), y);
+            uint2 v;
+            if (i <= 0) { v = pk2(mul4(ky, vf[0])); sts64(aRk + r_row(0) * 128u + o, v.x, v.y); }
+            if (i <= 1) { v = pk2(mul4(ky, vf[1])); sts64(aRk + r_row(1) * 128u + o, v.x, v.y); }
+            if (i <= 2) { v = pk2(mul4(ky, vf[2])); sts64(aRk + r_row(2) * 128u + o, v.x, v.y); }
+            v = pk2(mul4(ky, vf[3]));
+            sts64(aRk + r_row(3) * 128u + o, v.x, v.y);
+            *reinterpret_cast<uint2 *>(gKT + o) = pk2(mul4(ky, cc));
+            sf = mul4(sf, e[r]);
         }
     }
     umma::fence_proxy_async();
@@ -293,12 +329,10 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
         }
         umma::commit(bar_ab);
     }
-    bool ok = umma::mbar_wait(bar_ab, 0, WAIT_LIMIT);
+    bool ok = umma::mbar_wait(bar_ab, it & 1u, WAIT_LIMIT);
     ok = __syncthreads_and(ok) != 0;
     umma::fence_after();
 
-    const int qd = warp & 3;  // TMEM lane quadrant of this warp
-    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
     if (ok) {
         // A (fp32, scaled by b_t, strictly lower) into shared memory; B (bf16,
         // diagonal included) into the blob.  Lane quadrant i = block i: lanes
@@ -471,7 +505,7 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
             const int idx = tid + u * NT1;
             *reinterpret_cast<uint4 *>(out + BL_TB + idx * 16) = *reinterpret_cast<const uint4 *>(sm + P_TB + idx * 16);
         }
-        ok = umma::mbar_wait(bar_w, 0, WAIT_LIMIT);
+        ok = umma::mbar_wait(bar_w, it & 1u, WAIT_LIMIT);
     }
     ok = __syncthreads_and(ok) != 0;
     umma::fence_after();
@@ -489,11 +523,19 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
                 make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                            pack_bf16(v[14], v[15]));
         }
-    } else if (tid == 0) {
-        report_status(p.status, KDA_STATUS_TIMEOUT);
     }
     umma::fence_before();
     __syncthreads();
+    ++it;
+    if (!ok) {  // uniform: leave with the tensor memory and barriers idle
+        alive = false;
+        break;
+    }
+    }  // Lc > 0
+    cl = ncl;
+    ncl = nncl;
+    }  // items
+    if (!alive && tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
     if (warp == 0) umma::tmem_dealloc(tmem, 256);
 }
 
@@ -855,7 +897,18 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
     P.blob = blob;
     P.need_q = (need_q && a.q) ? 1 : 0;
     P.status = a.status;
-    dim3 grid(slot1 - slot0, a.H);
+    P.nitems = (slot1 - slot0) * a.H;
+    // persistent: two resident CTAs per SM
+    static int sms = 0;
+    if (sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            cudaGetLastError();
+            sms = 152;
+        }
+    }
+    const int grid = P.nitems < 2 * sms ? P.nitems : 2 * sms;
     sp::kda_chunk_prep_kernel<<<grid, sp::NT1, sp::P_SMEM, st>>>(P);
     return cudaGetLastError();
 }

@@ -163,6 +163,10 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst_saddr, const void *tmap
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar_saddr)
         : "memory");
 }
+// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar_saddr, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar_saddr), "r"(bytes) : "memory");
 }
