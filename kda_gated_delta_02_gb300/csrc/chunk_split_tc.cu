@@ -117,15 +117,17 @@ struct PrepParams {
     const float *beta;   // f32 [T][H]
     int H;
     float g_min;
+    CUtensorMap tq, tk, tg, tb;  // q, k, g boxes of 64 tokens x 1 head x 128; beta box of 64 tokens x 4 heads
     const int2 *list;    // slot -> {first token, length}
     int slot0;           // first slot of this launch
     int nitems;          // (slot1 - slot0) * H items, w = (slot - slot0) * H + h
     unsigned char *blob; // [w][kChunkBlobBytes]
     int need_q;          // 0: transitions only (no Q~, no B)
+    int pf_beta;         // tb is encoded (H a multiple of 4)
     uint32_t *status;
 };
 
-__global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_constant__ PrepParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -165,21 +167,12 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
     int2 nncl = make_int2(0, 0);
     {
         const int wn = w + G;
-        if (wn < nitems && ncl.y > 0) {
-            const int hn = wn % H, t = tid & 63, kind = tid >> 6;
-            if (t < ncl.y) {
-                const size_t row = ((size_t)(ncl.x + t) * H + hn) * D;
-                if (kind == 0) {
-                    if (need_q) umma::prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(p.q) + row, 256);
-                } else if (kind == 1) {
-                    umma::prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(p.k) + row, 256);
-                } else if (kind == 2) {
-                    umma::prefetch_l2(p.g + row, 512);
-                } else {
-                    const uintptr_t ba = reinterpret_cast<uintptr_t>(p.beta + (size_t)(ncl.x + t) * H + hn);
-                    umma::prefetch_l2(reinterpret_cast<const void *>(ba & ~(uintptr_t)15), 16);
-                }
-            }
+        if (wn < nitems && ncl.y > 0 && tid == 0) {
+            const int hn = wn % H;
+            if (need_q) umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
+            umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
+            umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
+            if (p.pf_beta) umma::prefetch_tile_2d(&p.tb, hn & ~3, ncl.x);
         }
         if (w + 2 * G < nitems) nncl = p.list[p.slot0 + (w + 2 * G) / H];
     }
@@ -378,19 +371,26 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
     if (ok) {
         float *sAf = reinterpret_cast<float *>(sm + P_AF);
         float *sTf = reinterpret_cast<float *>(sm + P_TF);
-        // diagonal 16 x 16 blocks, right-looking substitution with one column
-        // per lane in registers: lanes 0-15 of warp 2 + w -> block 2w, 16-31 -> 2w+1
+        // diagonal 16 x 16 blocks by substitution with one column per lane in
+        // registers (lanes 0-15 of warp 2 + w -> block 2w, 16-31 -> 2w+1), row by
+        // row: T[r][c] = delta_rc - sum_{m < r} A[r][m] T[m][c], the terms added in
+        // increasing m; the rows of A come in 16-byte loads
         if (warp == 2 || warp == 3) {
             const int bi = 2 * (warp - 2) + (lane >> 4), c = lane & 15;
             const float *Ab = sAf + (16 * bi) * LDF + 16 * bi;
             float acc[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) {
+                float v = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < 15; ++m) {
-                const float cm = acc[m];
-#pragma unroll
-                for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(-Ab[r * LDF + m], cm, acc[r]);
+                for (int m4 = 0; m4 < r; m4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * LDF + m4);
+                    v = fmaf(-a4.x, acc[m4], v);
+                    if (m4 + 1 < r) v = fmaf(-a4.y, acc[m4 + 1], v);
+                    if (m4 + 2 < r) v = fmaf(-a4.z, acc[m4 + 2], v);
+                    if (m4 + 3 < r) v = fmaf(-a4.w, acc[m4 + 3], v);
+                }
+                acc[r] = v;
             }
             float *Tb = sTf + (16 * bi) * LDF + 16 * bi;
 #pragma unroll
@@ -398,36 +398,46 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
         }
         __syncthreads();
         // 32 x 32 diagonal halves: T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22;
-        // X = A_10 T_00 goes to the (unused) upper block (0,1) of the A scratch
+        // X = A_10 T_00 goes to the (unused) upper block (0,1) of the A scratch.
+        // Thread (half hb, row r, column quad cq) of the first 128 forms four
+        // outputs from 16-byte loads (even and odd m summed apart, then added).
         {
-            const int r = tid >> 4, c = tid & 15;
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                const int bi = 2 * hb + 1, bj = 2 * hb;
+            const int hb = (tid >> 6) & 1, r = (tid >> 2) & 15, c0 = 4 * (tid & 3);
+            const int bi = 2 * hb + 1, bj = 2 * hb;
+            auto fma4 = [](float a, float4 b, float4 acc) {
+                return make_float4(fmaf(a, b.x, acc.x), fmaf(a, b.y, acc.y), fmaf(a, b.z, acc.z), fmaf(a, b.w, acc.w));
+            };
+            auto add4 = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+            if (tid < 128) {
                 const float *Ar = sAf + (16 * bi + r) * LDF + 16 * bj;
-                const float *Tc = sTf + (16 * bj) * LDF + 16 * bj + c;
-                float x0 = 0.f, x1 = 0.f;
+                const float *Tc = sTf + (16 * bj) * LDF + 16 * bj + c0;
+                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    x0 = fmaf(Ar[m], Tc[m * LDF], x0);
-                    x1 = fmaf(Ar[m + 1], Tc[(m + 1) * LDF], x1);
+                for (int m4 = 0; m4 < 16; m4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Ar + m4);
+                    x0 = fma4(a4.x, *reinterpret_cast<const float4 *>(Tc + (m4 + 0) * LDF), x0);
+                    x1 = fma4(a4.y, *reinterpret_cast<const float4 *>(Tc + (m4 + 1) * LDF), x1);
+                    x0 = fma4(a4.z, *reinterpret_cast<const float4 *>(Tc + (m4 + 2) * LDF), x0);
+                    x1 = fma4(a4.w, *reinterpret_cast<const float4 *>(Tc + (m4 + 3) * LDF), x1);
                 }
-                sAf[(16 * bj + r) * LDF + 16 * bi + c] = x0 + x1;
-                sTf[(16 * bj + r) * LDF + 16 * bi + c] = 0.f;
+                *reinterpret_cast<float4 *>(sAf + (16 * bj + r) * LDF + 16 * bi + c0) = add4(x0, x1);
+                *reinterpret_cast<float4 *>(sTf + (16 * bj + r) * LDF + 16 * bi + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncthreads();
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                const int bi = 2 * hb + 1, bj = 2 * hb;
+            if (tid < 128) {
                 const float *Ti = sTf + (16 * bi + r) * LDF + 16 * bi;
-                const float *Xs = sAf + (16 * bj) * LDF + 16 * bi;
-                float y0 = 0.f, y1 = 0.f;
+                const float *Xs = sAf + (16 * bj) * LDF + 16 * bi + c0;
+                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    y0 = fmaf(Ti[m], Xs[m * LDF + c], y0);
-                    y1 = fmaf(Ti[m + 1], Xs[(m + 1) * LDF + c], y1);
+                for (int m4 = 0; m4 < 16; m4 += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(Ti + m4);
+                    y0 = fma4(t4.x, *reinterpret_cast<const float4 *>(Xs + (m4 + 0) * LDF), y0);
+                    y1 = fma4(t4.y, *reinterpret_cast<const float4 *>(Xs + (m4 + 1) * LDF), y1);
+                    y0 = fma4(t4.z, *reinterpret_cast<const float4 *>(Xs + (m4 + 2) * LDF), y0);
+                    y1 = fma4(t4.w, *reinterpret_cast<const float4 *>(Xs + (m4 + 3) * LDF), y1);
                 }
-                sTf[(16 * bi + r) * LDF + 16 * bj + c] = -(y0 + y1);
+                const float4 y = add4(y0, y1);
+                *reinterpret_cast<float4 *>(sTf + (16 * bi + r) * LDF + 16 * bj + c0) = make_float4(-y.x, -y.y, -y.z, -y.w);
             }
             __syncthreads();
         }
@@ -468,20 +478,28 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const PrepParams
             *reinterpret_cast<uint32_t *>(sm + P_TB + umma::kmaj(t, s0, 64)) = pack_bf16(-acc[0] * b0, -acc[1] * b1);
             *reinterpret_cast<uint32_t *>(sm + P_TB + umma::kmaj(t + 8, s0, 64)) = pack_bf16(-acc[2] * b0, -acc[3] * b1);
         }
-        // T diag(b) for the rest: rows 0-31 (32 pairs each), rows 32-63 pairs
-        // 16-31; zero above the diagonal
-        for (int e2 = tid; e2 < 1536; e2 += NT1) {
-            int t, s;
-            if (e2 < 1024) {
-                t = e2 >> 5;
-                s = 2 * (e2 & 31);
+        // T diag(b) for the rest, 8 columns per step: rows 0-31 (all 64 columns),
+        // rows 32-63 columns 32-63; zero above the diagonal
+        for (int e2 = tid; e2 < 384; e2 += NT1) {
+            int t, s0;
+            if (e2 < 256) {
+                t = e2 >> 3;
+                s0 = 8 * (e2 & 7);
             } else {
-                t = 32 + ((e2 - 1024) >> 4);
-                s = 32 + 2 * ((e2 - 1024) & 15);
+                t = 32 + ((e2 - 256) >> 2);
+                s0 = 32 + 8 * ((e2 - 256) & 3);
             }
-            const float a0 = (s <= t) ? sTf[t * LDF + s] * sBeta[s] : 0.f;
-            const float a1 = (s + 1 <= t) ? sTf[t * LDF + s + 1] * sBeta[s + 1] : 0.f;
-            *reinterpret_cast<uint32_t *>(sm + P_TB + umma::kmaj(t, s, 64)) = pack_bf16(a0, a1);
+            const float4 ta = *reinterpret_cast<const float4 *>(sTf + t * LDF + s0);
+            const float4 tb4 = *reinterpret_cast<const float4 *>(sTf + t * LDF + s0 + 4);
+            const float4 ba = *reinterpret_cast<const float4 *>(sBeta + s0);
+            const float4 bb = *reinterpret_cast<const float4 *>(sBeta + s0 + 4);
+            const float v[8] = {ta.x * ba.x, ta.y * ba.y, ta.z * ba.z, ta.w * ba.w,
+                                tb4.x * bb.x, tb4.y * bb.y, tb4.z * bb.z, tb4.w * bb.w};
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2)
+                pk[j >> 1] = pack_bf16((s0 + j <= t) ? v[j] : 0.f, (s0 + j + 1 <= t) ? v[j + 1] : 0.f);
+            *reinterpret_cast<uint4 *>(sm + P_TB + umma::kmaj(t, s0, 64)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
     }
     umma::fence_proxy_async();
@@ -864,6 +882,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
 
 }  // namespace sp
 
+
 namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -877,6 +896,31 @@ cudaError_t launch_chunk_list(const ChunkArgs &a, int units, int nslots, int2 *l
     sp::kda_chunk_list_kernel<<<units, 128, 0, st>>>(a, nslots, list);
     return cudaGetLastError();
 }
+
+namespace {
+// [T][H][inner] (or [T][H] with inner = 0) tensor map with a box of box_inner x box_h x 64 tokens
+bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int inner, int H, int T,
+                 int box_inner, int box_h) {
+    EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!fn) return false;
+    const cuuint64_t Tn = (cuuint64_t)(T > 0 ? T : 1);
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (inner > 0) {
+        cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, Tn};
+        cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)inner * esize * H};
+        cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_h, 64u};
+        return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)H, Tn};
+    cuuint64_t strides[1] = {(cuuint64_t)H * esize};
+    cuuint32_t box[2] = {(cuuint32_t)box_h, 64u};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
 
 cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
                               bool need_q, cudaStream_t st) {
@@ -898,6 +942,15 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
     P.need_q = (need_q && a.q) ? 1 : 0;
     P.status = a.status;
     P.nitems = (slot1 - slot0) * a.H;
+    // prefetch boxes (H is a multiple of 4 for the beta box; other H prefetch nothing there)
+    bool ok = encode_rows(&P.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, a.T, 128, 1) &&
+              encode_rows(&P.tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, a.H, a.T, 128, 1) &&
+              encode_rows(&P.tq, P.need_q ? a.q : a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, a.T, 128, 1);
+    if (ok && a.H % 4 == 0) {
+        ok = encode_rows(&P.tb, a.beta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 0, a.H, a.T, 0, 4);
+        P.pf_beta = 1;
+    }
+    if (!ok) return cudaErrorInvalidValue;
     // persistent: two resident CTAs per SM
     static int sms = 0;
     if (sms <= 0) {
