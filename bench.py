@@ -35,6 +35,14 @@ if ROOT not in sys.path:
 METRIC = "KDA prefill tok/s @H96 d128 (% TC peak); spec-verify state GB/s (% HBM)"
 BYTES_PER_TOKHEAD = 1540        # q,k,v bf16 768 + g fp32 512 + beta 4 + o bf16 256 (dk=dv=128)
 FLOPS_PER_TOKHEAD_ALGO = 139264  # 3*C*dk + 2*C*dv + 6*dk*dv, C=64, causal halves only
+BLOB_PER_TOKHEAD = 66048 / 64    # operand blob of a (chunk, head) handed from the chunk-local kernel to the walk
+# bytes per token-head each prefill kernel must move: what it reads and writes at the minimum
+KERNEL_BYTES_PER_TOKHEAD = {
+    "kda_chunk_prep_kernel": 2 * 128 * 2 + 128 * 4 + 4 + BLOB_PER_TOKHEAD,  # q, k, g, beta in; blob out
+    "kda_chunk_walk_kernel": BLOB_PER_TOKHEAD + 128 * 2 + 128 * 2,           # blob, v in; o out
+    "kda_chunk_tc_kernel": BYTES_PER_TOKHEAD,
+    "kda_chunk_kernel": BYTES_PER_TOKHEAD,
+}
 
 
 def load_peaks():
@@ -157,6 +165,17 @@ def cuda_time(fn, steps, stream):
     e.record(stream)
     torch.cuda.synchronize()
     return s.elapsed_time(e) / steps
+
+
+def timed_launches(kda, fn, steps, stream):
+    """cuda_time of `steps` calls with the library's launch timing on: returns
+    (mean ms per call, {kernel family: {"launches", "ms"}} over those calls)."""
+    kda.kernel_timing_start()
+    try:
+        ms = cuda_time(fn, steps, stream)
+    finally:
+        kern = kda.kernel_timing_stop()
+    return ms, kern
 
 
 def cpu_baseline_sample(nthreads=0):
@@ -287,34 +306,50 @@ def main(argv=None):
     out = {}
 
     # ------------------------------------------------------------ prefill (headline)
-    # dk = dv = 128 bf16 runs the tcgen05 / tensor-memory kernel (one launch per step)
-    prefill_kernel = ("kda_chunk_kernel<128,128,bf16>" if os.environ.get("KDA_PREFILL_TC", "1") == "0"
-                      else "kda_chunk_tc_kernel")
+    # dk = dv = 128 bf16 with the workspace of the two-kernel form: per step the
+    # chunk-local kernel and the walk, once per piece of slots
     w = synth.PREFILL_32K
     inp = synth.make_prefill(w, device="cuda")
     T, H = inp["q"].shape[:2]
     o = torch.empty_like(inp["v"])
     Sf = torch.empty((1, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    wsp = torch.empty(max(1, kda.chunk_fwd_prep_workspace_size(1, T, H, w.dk, w.dv, kda.CP_AUTO)),
+                      dtype=torch.uint8, device="cuda")
 
     def prefill_step():
         kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], out=o,
-                      final_state=Sf, cp_mode=kda.CP_AUTO)
+                      final_state=Sf, cp_mode=kda.CP_AUTO, workspace=wsp)
 
     for _ in range(Wm):
         prefill_step()
     sampler = ClockSampler(local)
     sampler.start()
     barrier(ws)
-    ms = cuda_time(prefill_step, K, stream)
+    ms, kern = timed_launches(kda, prefill_step, K, stream)
     barrier(ws)
     clocks = sampler.stop()
     ms = reduce_max(ms, ws)
     tok_s = ws * T / (ms * 1e-3)
-    algo_bytes = T * H * BYTES_PER_TOKHEAD + H * w.dk * w.dv * 4
-    achieved_gbs = algo_bytes / (ms * 1e-3) / 1e9
+    path_bytes = T * H * BYTES_PER_TOKHEAD + H * w.dk * w.dv * 4
+    path_gbs = path_bytes / (ms * 1e-3) / 1e9
     algo_flops = T * H * FLOPS_PER_TOKHEAD_ALGO
     tflops = algo_flops / (ms * 1e-3) / 1e12
-    launches = K  # one kda_chunk_fwd launch per step (CP resolves off at 96 heads)
+    launches = sum(v["launches"] for v in kern.values())
+    # the dominant kernel of the step: its average launch (events on the launching
+    # stream, inside the timed region) against the bytes it must move per launch
+    kernels = {}
+    for name, v in kern.items():
+        per_step = v["launches"] / K
+        lms = v["ms"] / v["launches"]
+        rec = {"launches_per_step": per_step, "ms_per_launch": lms, "share_of_step": v["ms"] / K / ms}
+        if name in KERNEL_BYTES_PER_TOKHEAD:
+            tokens = T / per_step  # tokens one launch covers
+            rec["bytes_per_launch"] = tokens * H * KERNEL_BYTES_PER_TOKHEAD[name]
+            rec["achieved_gbs"] = rec["bytes_per_launch"] / (lms * 1e-3) / 1e9
+            rec["frac_hbm"] = rec["achieved_gbs"] / peaks["hbm_gbs"]
+            rec["traffic"] = kernel_traffic(name, tokens)
+        kernels[name] = rec
+    dom = max((n for n in kernels if n in KERNEL_BYTES_PER_TOKHEAD), key=lambda n: kernels[n]["share_of_step"])
     out["prefill"] = {"ms": ms, "tok_s": tok_s}
 
     # the same launch emitting the state every 4096 tokens (8 checkpoints per head)
@@ -327,11 +362,12 @@ def main(argv=None):
 
     for _ in range(2):
         ckpt_step()
-    ms_ck = reduce_max(cuda_time(ckpt_step, K, stream), ws)
+    ms_ck, kc = timed_launches(kda, ckpt_step, K, stream)
+    ms_ck = reduce_max(ms_ck, ws)
     out["ckpt"] = {"workload": f"{w.name}, state every {every} tokens", "ms": ms_ck,
                    "tok_s": ws * T / (ms_ck * 1e-3), "overhead_vs_plain": ms_ck / ms - 1.0,
                    "checkpoint_bytes_per_launch": ck.numel() * 4}
-    launches += K
+    launches += sum(v["launches"] for v in kc.values())
     del ck
 
     # e2e: host buffers through the same C-ABI call, copies inside the timed region
@@ -346,7 +382,7 @@ def main(argv=None):
         for k_, v_ in host.items():
             dev[k_].copy_(v_, non_blocking=True)
         kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["cu_seqlens"], out=o,
-                      final_state=Sf, cp_mode=kda.CP_AUTO)
+                      final_state=Sf, cp_mode=kda.CP_AUTO, workspace=wsp)
         o_host.copy_(o, non_blocking=True)
         Sf_host.copy_(Sf, non_blocking=True)
 
@@ -354,7 +390,7 @@ def main(argv=None):
     Ke = max(3, K // 4)
     ms_e2e = reduce_max(cuda_time(e2e_step, Ke, stream), ws)
     del host, dev, o_host, Sf_host
-    del inp, o
+    del inp, o, wsp
     torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ verify-replay
@@ -371,7 +407,8 @@ def main(argv=None):
 
         for _ in range(Wm):
             verify_step()
-        vms = reduce_max(cuda_time(verify_step, K, stream), ws)
+        vms, kv = timed_launches(kda, verify_step, K, stream)
+        vms = reduce_max(vms, ws)
         state_bytes = 2 * st.numel() * st.element_size()  # read + write
         acc = d["accepted"].to(torch.int64)
         row = 3 * vw.H * vw.dk * 2 + vw.H * vw.dk * 2 + vw.H * 2  # pre-conv qkv + g + beta per token row
@@ -385,7 +422,7 @@ def main(argv=None):
                          "bytes_per_launch": total_bytes, "state_bytes_per_launch": state_bytes,
                          "kernel": verify_kernel, "traffic": kernel_traffic(verify_kernel, vw.R),
                          "requests_per_s": ws * vw.R / (vms * 1e-3)}
-        launches += K
+        launches += sum(v["launches"] for v in kv.values())
         del d, st, tl, ov
         torch.cuda.empty_cache()
 
@@ -404,7 +441,8 @@ def main(argv=None):
 
         for _ in range(Wm):
             decode_step()
-        dms = reduce_max(cuda_time(decode_step, K, stream), ws)
+        dms, kd = timed_launches(kda, decode_step, K, stream)
+        dms = reduce_max(dms, ws)
         state_bytes = 2 * st.numel() * st.element_size()
         row = 3 * dw.H * dw.dk * 2 + dw.H * dw.dk * 2 + dw.H * 2
         total_bytes = state_bytes + dw.R * row + 2 * tl.numel() * tl.element_size() + od.numel() * od.element_size()
@@ -412,7 +450,7 @@ def main(argv=None):
                          "frac_hbm": (total_bytes / (dms * 1e-3) / 1e9) / peaks["hbm_gbs"],
                          "bytes_per_launch": total_bytes, "tokens_per_s": ws * dw.R / (dms * 1e-3),
                          "kernel": decode_kernel, "traffic": kernel_traffic(decode_kernel, dw.R)}
-        launches += K
+        launches += sum(v["launches"] for v in kd.values())
         del d, st, tl, od
         torch.cuda.empty_cache()
 
@@ -431,11 +469,12 @@ def main(argv=None):
         for _ in range(3):
             varlen_step()
         Kv = max(3, K // 2)
-        vms_ = reduce_max(cuda_time(varlen_step, Kv, stream), ws)
+        vms_, kl = timed_launches(kda, varlen_step, Kv, stream)
+        vms_ = reduce_max(vms_, ws)
         vbytes = Tv * Hv * BYTES_PER_TOKHEAD + 2 * vi["S0"].numel() * 4
         out["varlen"] = {"workload": vl.name, "tokens": Tv, "ms": vms_, "tok_s": ws * Tv / (vms_ * 1e-3),
                          "frac_hbm": (vbytes / (vms_ * 1e-3) / 1e9) / peaks["hbm_gbs"]}
-        launches += Kv
+        launches += sum(v["launches"] for v in kl.values())
         del vi, ov, Sv
         torch.cuda.empty_cache()
 
@@ -447,7 +486,7 @@ def main(argv=None):
         oc = torch.empty_like(ci["v"])
         Sc = torch.empty((1, Hc, cw.dk, cw.dv), dtype=torch.float32, device="cuda")
         seg = kda.chunk_fwd_plan(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO)
-        wsb = kda.chunk_fwd_workspace_size(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO)
+        wsb = kda.chunk_fwd_prep_workspace_size(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO)
         wbuf = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
 
         def cp_step(mode=kda.CP_AUTO):
@@ -457,13 +496,14 @@ def main(argv=None):
         for _ in range(3):
             cp_step()
         Kc = max(3, K // 4)
-        cms = reduce_max(cuda_time(cp_step, Kc, stream), ws)
+        cms, kcp = timed_launches(kda, cp_step, Kc, stream)
+        cms = reduce_max(cms, ws)
         cms_off = reduce_max(cuda_time(lambda: cp_step(kda.CP_OFF), 1, stream), ws)
         minimal = Tc * Hc * BYTES_PER_TOKHEAD
         out["cp"] = {"workload": cw.name, "segment_len": seg, "ms": cms, "tok_s": ws * Tc / (cms * 1e-3),
                      "ms_cp_off": cms_off, "speedup_vs_off": cms_off / cms,
                      "frac_hbm_min_bytes": (minimal / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"]}
-        launches += 4 * Kc
+        launches += sum(v["launches"] for v in kcp.values())
         del ci, oc, wbuf
         torch.cuda.empty_cache()
 
@@ -480,13 +520,16 @@ def main(argv=None):
             "config": {"workload": w.name, "T": T, "H": H, "dk": w.dk, "dv": w.dv, "chunk": 64,
                        "global_batch": 1, "seq_len": T, "parallelism": f"replicas x{ws}",
                        "l2": "inputs (4.8 GB) larger than L2 (129 MB); no flush"},
-            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": kernel_traffic(prefill_kernel, T),
-                         "peak_source": peaks["source"], "kernel": prefill_kernel,
-                         "algorithmic_bytes_per_launch": algo_bytes,
-                         "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],
-                         "tensor_frac": tflops / peaks["bf16_tflops"]},
+            "roofline": {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": kernels[dom]["frac_hbm"], "traffic": kernels[dom]["traffic"],
+                         "peak_source": peaks["source"], "kernel": dom,
+                         "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"],
+                         "ms_per_launch": kernels[dom]["ms_per_launch"]},
+            "path_roofline": {"bound": "hbm", "achieved": path_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": path_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_step": path_bytes,
+                              "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],
+                              "tensor_frac": tflops / peaks["bf16_tflops"]},
+            "kernels": kernels,
             "e2e": {"value": ws * T / (ms_e2e * 1e-3), "unit": "tok/s", "ms": ms_e2e,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clocks, "gpu_launches": launches,

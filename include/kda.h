@@ -64,6 +64,17 @@ extern "C" {
 #define KDA_STATUS_SEGMENT_OVERFLOW 0x4u /* segment table larger than planned      */
 #define KDA_STATUS_TIMEOUT 0x8u          /* a bounded on-chip wait gave up; unit left unfinished */
 
+/* Kernel families, for kda_kernel_timing_stop. */
+#define KDA_KERNEL_CHUNK_LIST 0      /* chunk slot list of the two-kernel prefill */
+#define KDA_KERNEL_CHUNK_PREP 1      /* chunk-local products of the two-kernel prefill */
+#define KDA_KERNEL_CHUNK_WALK 2      /* state walk of the two-kernel prefill */
+#define KDA_KERNEL_CHUNK_TC 3        /* one-kernel tcgen05 prefill */
+#define KDA_KERNEL_CHUNK_MMA 4       /* warp-MMA prefill (d = 64, f32 inputs) */
+#define KDA_KERNEL_SEGMENT_COMPOSE 5 /* CP composition */
+#define KDA_KERNEL_SEGMENT_TABLE 6   /* CP segment table */
+#define KDA_KERNEL_VERIFY 7          /* kda_decode_verify_replay (verify or single-token decode) */
+#define KDA_KERNEL_KINDS 8
+
 /* Human-readable name of a return status. Never NULL. */
 const char *kda_status_string(int status);
 
@@ -262,6 +273,19 @@ int kda_chunk_fwd_cp_noalloc(const void *q, const void *k, const void *v, const 
                              int dk, int dv, const float *initial_state, float *final_state,
                              void *o, float scale, float g_min, int in_dtype, int segment_len,
                              uint32_t *status, void *stream);
+
+/*
+ * Launch timing, for measurement: between kda_kernel_timing_start() and
+ * kda_kernel_timing_stop(), every kernel launch of this library (any thread,
+ * any stream) is bracketed by two CUDA events recorded on its stream.  Stop
+ * waits for those events and writes, per kernel family k < nkinds (the
+ * KDA_KERNEL_* numbers), the launch count launches[k] and the summed device
+ * time total_ms[k]; it returns KDA_ERR_CUDA if an event could not be read.
+ * Start discards anything recorded before.  Host arithmetic and event calls
+ * only; this facility has no counterpart on the pages.
+ */
+int kda_kernel_timing_start(void);
+int kda_kernel_timing_stop(int *launches, float *total_ms, int nkinds);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,8 @@ import torch
 __all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_prep_workspace_size", "chunk_fwd_plan", "segment_transition",
            "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
            "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
-           "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW"]
+           "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW", "KERNEL_FAMILIES", "kernel_timing_start",
+           "kernel_timing_stop"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda.so")
@@ -68,6 +69,10 @@ def load_library():
         lib.kda_segment_transition.argtypes = [P, P, P, P, I, I, I, I, I, P, P, F, I, P]
         lib.kda_segment_compose.restype = I
         lib.kda_segment_compose.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.kda_kernel_timing_start.restype = I
+        lib.kda_kernel_timing_start.argtypes = []
+        lib.kda_kernel_timing_stop.restype = I
+        lib.kda_kernel_timing_stop.argtypes = [P, P, I]
         lib.kda_decode_verify_replay.restype = I
         lib.kda_decode_verify_replay.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
                                                  F, F, F, F, I, P, P]
@@ -182,6 +187,28 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
                                  _stream(stream))
     _check(rc, "kda_segment_compose")
     return S_in, Sf
+
+
+# kernel families of kda_kernel_timing_stop, in KDA_KERNEL_* order
+KERNEL_FAMILIES = ("kda_chunk_list_kernel", "kda_chunk_prep_kernel", "kda_chunk_walk_kernel",
+                   "kda_chunk_tc_kernel", "kda_chunk_kernel", "kda_compose_kernel", "kda_segment_table_kernel",
+                   "kda_decode_verify_replay")
+
+
+def kernel_timing_start():
+    """Record CUDA events around every library launch from now on."""
+    _check(load_library().kda_kernel_timing_start(), "kda_kernel_timing_start")
+
+
+def kernel_timing_stop():
+    """Stop recording; {family: {"launches": n, "ms": summed device time}} for
+    the families that launched (waits for the recorded events)."""
+    n = len(KERNEL_FAMILIES)
+    launches = (ctypes.c_int * n)()
+    total = (ctypes.c_float * n)()
+    _check(load_library().kda_kernel_timing_stop(launches, total, n), "kda_kernel_timing_stop")
+    return {KERNEL_FAMILIES[i]: {"launches": int(launches[i]), "ms": float(total[i])}
+            for i in range(n) if launches[i] > 0}
 
 
 def decode_verify_replay(state, conv_tail, conv_w, cached_qkv, cached_g, cached_beta, accepted_len,

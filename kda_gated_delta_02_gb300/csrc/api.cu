@@ -4,6 +4,10 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <atomic>
+#include <mutex>
+#include <vector>
+
 #include "../../include/kda.h"
 #include "kda_internal.h"
 
@@ -86,6 +90,42 @@ CpLayout cp_layout(int N, int T, int H, int dk, int dv, int cp_mode, int segment
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Opt-in launch timing: a pair of CUDA events on the launching stream around
+// every kernel launch of the library while enabled (kda_kernel_timing_start /
+// kda_kernel_timing_stop).
+struct TimedLaunch {
+    int kind;
+    cudaEvent_t a, b;
+};
+std::atomic<bool> g_timing{false};
+std::mutex g_timing_mu;
+std::vector<TimedLaunch> g_timed;
+
+template <class F>
+cudaError_t timed_launch(int kind, cudaStream_t st, F &&launch) {
+    if (!g_timing.load(std::memory_order_relaxed)) return launch();
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+        if (a) cudaEventDestroy(a);
+        cudaGetLastError();
+        return launch();
+    }
+    cudaEventRecord(a, st);
+    const cudaError_t e = launch();
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    g_timed.push_back({kind, a, b});
+    return e;
+}
+
+void drop_timed() {
+    for (const TimedLaunch &t : g_timed) {
+        cudaEventDestroy(t.a);
+        cudaEventDestroy(t.b);
+    }
+    g_timed.clear();
+}
+
 // Two-kernel tcgen05 prefill (dk = dv = 128): workspace after the CP scratch =
 // slot list | two carry states [2 tiles][H][128][128] f32 | operand blobs of
 // one piece of slots.  The blob area is capped (KDA_PREP_BUDGET_MB, default
@@ -136,13 +176,18 @@ cudaError_t run_split(const kda::ChunkArgs &a, int units, unsigned char *ws, con
     float *carry = reinterpret_cast<float *>(ws + S.off_carry);
     unsigned char *blob = ws + S.off_blob;
     cudaError_t e = cudaSuccess;
-    if (!skip_prep) e = kda::launch_chunk_list(a, units, S.nslots, list, st);
+    if (!skip_prep)
+        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(a, units, S.nslots, list, st); });
     for (int s0 = 0, pc = 0; e == cudaSuccess && s0 < S.nslots; s0 += S.piece, ++pc) {
         const int s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
-        if (!skip_prep) e = kda::launch_chunk_prep(a, list, s0, s1, blob, need_q, st);
+        if (!skip_prep)
+            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st,
+                             [&] { return kda::launch_chunk_prep(a, list, s0, s1, blob, need_q, st); });
         if (e == cudaSuccess)
-            e = kda::launch_chunk_walk(a, units, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
-                                       carry + (size_t)((pc + 1) & 1) * S.carry_stride, st);
+            e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+                return kda::launch_chunk_walk(a, units, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
+                                              carry + (size_t)((pc + 1) & 1) * S.carry_stride, st);
+            });
     }
     return e;
 }
@@ -153,8 +198,11 @@ cudaError_t run_split(const kda::ChunkArgs &a, int units, unsigned char *ws, con
 cudaError_t run_chunk(const kda::ChunkArgs &a, int units, bool bf, cudaStream_t st) {
     const char *env = getenv("KDA_PREFILL_TC");
     const bool tc_ok = !(env && env[0] == '0');
-    if (tc_ok && kda::chunk_tc_supported(a, bf)) return kda::launch_chunk_tc(a, units, st);
-    return kda::launch_chunk(a, units, prefill_dvt(a.dk, a.dv, a.mode == kda::MODE_TRANSITION), bf, st);
+    if (tc_ok && kda::chunk_tc_supported(a, bf))
+        return timed_launch(KDA_KERNEL_CHUNK_TC, st, [&] { return kda::launch_chunk_tc(a, units, st); });
+    return timed_launch(KDA_KERNEL_CHUNK_MMA, st, [&] {
+        return kda::launch_chunk(a, units, prefill_dvt(a.dk, a.dv, a.mode == kda::MODE_TRANSITION), bf, st);
+    });
 }
 
 }  // namespace
@@ -251,8 +299,9 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     float *Nm = reinterpret_cast<float *>(ws + L.off_N);
     float *Sin = reinterpret_cast<float *>(ws + L.off_Sin);
 
-    cudaError_t e = kda::launch_segment_table(cu_seqlens, N, T, L.seg_len, L.P_max, table, first, count,
-                                              status, st);
+    cudaError_t e = timed_launch(KDA_KERNEL_SEGMENT_TABLE, st, [&] {
+        return kda::launch_segment_table(cu_seqlens, N, T, L.seg_len, L.P_max, table, first, count, status, st);
+    });
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     // pass 1: transitions of every segment, independent of the incoming state
     a.mode = kda::MODE_TRANSITION;
@@ -270,7 +319,7 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     kda::ComposeArgs c = {};
     c.M = M; c.Nm = Nm; c.S0 = initial_state; c.S_in = Sin; c.S_final = nullptr;
     c.first = first; c.P = 0; c.chains = N; c.H = H; c.dk = dk; c.dv = dv;
-    e = kda::launch_compose(c, st);
+    e = timed_launch(KDA_KERNEL_SEGMENT_COMPOSE, st, [&] { return kda::launch_compose(c, st); });
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     // pass 3: replay every segment from its exact initial state
     a.mode = kda::MODE_REPLAY;
@@ -368,7 +417,39 @@ int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w, 
     a.R = R; a.H = H; a.dk = dk; a.dv = dv; a.W = W; a.Wd = Wd;
     a.scale = scale; a.g_min = g_min; a.eps_in = eps_in; a.eps_out = eps_out; a.conv_act = conv_act;
     a.status = status;
-    return cuda_status(kda::launch_verify(a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed_launch(KDA_KERNEL_VERIFY, st, [&] { return kda::launch_verify(a, st); }));
+}
+
+int kda_kernel_timing_start(void) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    drop_timed();
+    g_timing.store(true);
+    return KDA_OK;
+}
+
+int kda_kernel_timing_stop(int *launches, float *total_ms, int nkinds) {
+    if (nkinds < 0 || (nkinds > 0 && (!launches || !total_ms))) return KDA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    g_timing.store(false);
+    for (int i = 0; i < nkinds; ++i) {
+        launches[i] = 0;
+        total_ms[i] = 0.f;
+    }
+    int rc = KDA_OK;
+    for (const TimedLaunch &t : g_timed) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(t.b) != cudaSuccess || cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess) {
+            rc = KDA_ERR_CUDA;
+            continue;
+        }
+        if (t.kind >= 0 && t.kind < nkinds) {
+            launches[t.kind] += 1;
+            total_ms[t.kind] += ms;
+        }
+    }
+    drop_timed();
+    return rc;
 }
 
 }  // extern "C"

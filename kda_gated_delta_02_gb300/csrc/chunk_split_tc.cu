@@ -803,15 +803,19 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         umma::fence_after();
         // checkpoint: the state after token (tc + Lc) when that position of the
         // sequence is a multiple of ckpt_every (S^T lane = value column)
-        if (p.ckpt && !transition && !timed_out) {
+        // (the tensor-memory load is warp-collective: it runs whatever this
+        // thread's wait returned; only the stores depend on it)
+        if (p.ckpt && !transition) {
             const int rel = tc + Lc - seq0;
             const int kq = rel / p.ckpt_every - 1;
             if (rel % p.ckpt_every == 0 && kq < p.ckpt_count) {
                 float *dst = p.ckpt + (((size_t)n * p.ckpt_count + kq) * H + h) * D * (size_t)dv;
                 float Sreg[32];
                 umma::ld32(tq + TM_ST + 32 * cg, Sreg);
+                if (!timed_out) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * dv + vcol0 + jrow] = Sreg[c];
+                    for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * dv + vcol0 + jrow] = Sreg[c];
+                }
             }
         }
 
@@ -819,7 +823,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         // staged as a row-major [64][128] bf16 tile over U^T (read by the
         // products that just completed), then written with 16-byte stores
         unsigned char *ostage = sm + W_UT;
-        if (need_q && !timed_out) {
+        if (need_q) {  // staged whatever the wait returned; the barrier below decides
             float v[16];
             umma::ld16(tq + TM_O + 16 * cg, v);
 #pragma unroll

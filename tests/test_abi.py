@@ -103,3 +103,44 @@ def test_binding_fails_loudly_without_cuda_tensors():
     x = torch.zeros(64, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(kda.KDAError):
         kda.chunk_fwd(x, x, x, x.float(), torch.zeros(64, 2), torch.tensor([0, 64], dtype=torch.int32))
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("N,T,H,cp,seg", [(1, 32768, 96, 0, 0), (16, 68775, 96, 0, 0), (1, 1 << 20, 12, 1, 32768),
+                                          (3, 1771, 4, 0, 0)])
+def test_prep_workspace_arithmetic(lib, monkeypatch, N, T, H, cp, seg):
+    """The two-kernel area after the CP scratch: slot list (8 B per slot,
+    floor(T/64) + units slots), two carry states 2 x H x 128 x 128 f32, and the
+    blobs of one piece (66,048 B per chunk-head; pieces of equal size, at most
+    2 GiB of blobs)."""
+    monkeypatch.delenv("KDA_PREP_BUDGET_MB", raising=False)
+    lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_fwd_prep_workspace_size.restype = ctypes.c_size_t
+    base = lib.kda_chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)
+    got = lib.kda_chunk_fwd_prep_workspace_size(N, T, H, 128, 128, cp, seg)
+    plan = lib.kda_chunk_fwd_plan(N, T, H, 128, 128, cp, seg)
+    units = (T // plan + N) if plan else N
+    nslots = T // 64 + units
+    per_slot = H * 66048
+    piece = max(1, min(nslots, (2048 << 20) // per_slot))
+    pieces = -(-nslots // piece)
+    piece = -(-nslots // pieces)
+    area = _align256(nslots * 8) + _align256(2 * 2 * H * 128 * 128 * 4) + _align256(piece * per_slot)
+    assert got == _align256(base) + area
+    # other shapes keep the one-kernel workspace
+    assert lib.kda_chunk_fwd_prep_workspace_size(N, T, H, 64, 64, cp, seg) == \
+        lib.kda_chunk_fwd_workspace_size(N, T, H, 64, 64, cp, seg)
+
+
+def test_kernel_timing_without_launches(lib):
+    """Start / stop with nothing launched: no CUDA call, zero counts."""
+    n = 8
+    launches = (ctypes.c_int * n)(*([7] * n))
+    total = (ctypes.c_float * n)(*([7.0] * n))
+    assert lib.kda_kernel_timing_start() == 0
+    assert lib.kda_kernel_timing_stop(launches, total, n) == 0
+    assert list(launches) == [0] * n and list(total) == [0.0] * n
+    assert lib.kda_kernel_timing_stop(None, None, 2) != 0  # outputs required

@@ -105,3 +105,19 @@ def test_two_kernel_form_reports_bad_seqlens(kda):
     torch.cuda.synchronize()
     assert int(status.item()) & kda.STATUS_BAD_SEQLENS
     assert torch.all(o[100:] == 7.0)
+
+
+def test_kernel_timing_counts_the_launches(kda, monkeypatch):
+    """Launch timing around one two-kernel call: one slot list, and one
+    chunk-local launch and one walk per piece (5 pieces here)."""
+    monkeypatch.setenv("KDA_PREP_BUDGET_MB", "1")
+    x = _inputs([500, 300], 4, seed=3)  # 14 slots; 3 slots of 4 heads per MiB -> pieces of 3 (5 pieces)
+    kda.kernel_timing_start()
+    _run(kda, x, prep=True)
+    kern = kda.kernel_timing_stop()
+    n_pieces = -(-(800 // 64 + 2) // 3)
+    assert kern["kda_chunk_list_kernel"]["launches"] == 1
+    assert kern["kda_chunk_prep_kernel"]["launches"] == n_pieces
+    assert kern["kda_chunk_walk_kernel"]["launches"] == n_pieces
+    assert all(v["ms"] > 0 for v in kern.values())
+    assert kda.kernel_timing_stop() == {}  # nothing recorded after stop
