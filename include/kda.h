@@ -112,7 +112,8 @@ int kda_version(void);
  *               bytes (may be NULL when that size is 0).  Contents on entry
  *               are ignored; on exit they are unspecified.  With bf16 inputs
  *               and dk = dv = 128, a workspace of at least
- *               kda_chunk_fwd_prep_workspace_size(...) bytes selects the
+ *               kda_chunk_fwd_prep_workspace_size(...) bytes (or any size
+ *               with room for one slot, run in pieces) selects the
  *               two-kernel form: the chunk-local products of every (chunk,
  *               head) (decays, causal tiles, the dependency inverse, W, the
  *               decayed q and k) run first, in parallel over all chunks, into
@@ -157,11 +158,14 @@ size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_
                                     int segment_len);
 
 /* Workspace bytes that select kda_chunk_fwd's two-kernel form (bf16 inputs,
- * dk = dv = 128): the CP scratch above, then a slot list (8 bytes per 64-token
- * chunk slot; floor(T / 64) + units slots, units = sequences or segments), two
- * carry states (2 x 2 x H x 128 x 128 f32) and the operand blobs of up to
- * 2 GiB of slots (66,048 bytes per chunk and head; longer inputs run in equal
- * pieces of slots).  Equals kda_chunk_fwd_workspace_size for other shapes.
+ * dk = dv = 128) with all chunk slots in one piece: the CP scratch above, then
+ * a slot list (8 bytes per 64-token chunk slot; floor(T / 64) + units slots,
+ * units = sequences or segments), two carry states (2 x 2 x H x 128 x 128 f32)
+ * and the operand blobs (66,048 bytes per slot and head), the blobs capped at
+ * 16 GiB (KDA_PREP_BUDGET_MB overrides the cap).  kda_chunk_fwd uses whatever
+ * workspace it is given: room for fewer slots runs the slots in equal pieces
+ * (one chunk-local launch and one walk per piece); room for none runs the
+ * one-kernel form.  Equals kda_chunk_fwd_workspace_size for other shapes.
  * Pure host arithmetic; this form has no counterpart on the pages beyond the
  * chunk algebra it reorders. */
 size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,

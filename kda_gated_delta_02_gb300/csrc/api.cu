@@ -128,27 +128,36 @@ void drop_timed() {
 
 // Two-kernel tcgen05 prefill (dk = dv = 128): workspace after the CP scratch =
 // slot list | two carry states [2 tiles][H][128][128] f32 | operand blobs of
-// one piece of slots.  The blob area is capped (KDA_PREP_BUDGET_MB, default
-// 2048 MiB); longer inputs run as several pieces of equal size.
+// one piece of slots.  The piece is as large as the workspace the caller gives
+// allows (pieces of equal size); kda_chunk_fwd_prep_workspace_size asks for
+// all slots in one piece, up to a cap of KDA_PREP_BUDGET_MB (default 16 GiB)
+// of blobs.
 struct SplitLayout {
     int nslots = 0, piece = 0;
     size_t off_list = 0, off_carry = 0, carry_stride = 0, off_blob = 0, total = 0;
 };
 
-SplitLayout split_layout(int units, int T, int H) {
+size_t split_blob_cap() {
+    size_t mb = 16384;
+    if (const char *env = getenv("KDA_PREP_BUDGET_MB")) {
+        const long v = atol(env);
+        if (v > 0) mb = (size_t)v;
+    }
+    return mb << 20;
+}
+
+// Layout for `units` units with `blob_bytes` of room for blobs; piece = 0 when
+// not even one slot fits.
+SplitLayout split_layout(int units, int T, int H, size_t blob_bytes) {
     SplitLayout S;
     S.nslots = T / kChunk + units;
     const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
-    size_t budget_mb = 2048;
-    if (const char *env = getenv("KDA_PREP_BUDGET_MB")) {
-        const long v = atol(env);
-        if (v > 0) budget_mb = (size_t)v;
-    }
-    long piece = (long)((budget_mb << 20) / per_slot);
-    if (piece < 1) piece = 1;
+    long piece = (long)(blob_bytes / per_slot);
     if (piece > S.nslots) piece = S.nslots;
-    const long pieces = (S.nslots + piece - 1) / piece;
-    S.piece = (int)((S.nslots + pieces - 1) / pieces);
+    if (piece >= 1) {
+        const long pieces = (S.nslots + piece - 1) / piece;
+        S.piece = (int)((S.nslots + pieces - 1) / pieces);
+    }
     size_t o = 0;
     S.off_list = o;
     o = align256(o + (size_t)S.nslots * 8);
@@ -159,6 +168,20 @@ SplitLayout split_layout(int units, int T, int H) {
     o = align256(o + (size_t)S.piece * per_slot);
     S.total = o;
     return S;
+}
+
+// The layout kda_chunk_fwd_prep_workspace_size asks for.
+SplitLayout split_layout_wanted(int units, int T, int H) {
+    const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
+    const size_t all = (size_t)(T / kChunk + units) * per_slot, cap = split_blob_cap();
+    return split_layout(units, T, H, all < cap ? all : (cap < per_slot ? per_slot : cap));
+}
+
+// The layout that fits `bytes` of workspace (piece = 0: none fits).
+SplitLayout split_layout_fit(int units, int T, int H, size_t bytes) {
+    const SplitLayout fixed = split_layout(units, T, H, 0);  // list and carries only
+    if (bytes < fixed.total) return fixed;
+    return split_layout(units, T, H, bytes - fixed.total);
 }
 
 bool split_enabled() {
@@ -232,7 +255,7 @@ size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, in
     const CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
     if (dk != 128 || dv != 128 || N < 1 || T < 0 || H < 1) return L.total;
     const int units = L.seg_len ? L.P_max : N;
-    return align256(L.total) + split_layout(units, T, H).total;
+    return align256(L.total) + split_layout_wanted(units, T, H).total;
 }
 
 int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
@@ -276,8 +299,11 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     const size_t split_off = align256(L.total);
     bool split = bf && dk == 128 && dv == 128 && workspace && T > 0 && split_enabled();
     if (split) {
-        SL = split_layout(L.seg_len ? L.P_max : N, T, H);
-        split = workspace_bytes >= split_off + SL.total;
+        split = workspace_bytes > split_off;
+        if (split) {
+            SL = split_layout_fit(L.seg_len ? L.P_max : N, T, H, workspace_bytes - split_off);
+            split = SL.piece >= 1;
+        }
     }
     unsigned char *wsplit = split ? static_cast<unsigned char *>(workspace) + split_off : nullptr;
     if (L.seg_len == 0) {

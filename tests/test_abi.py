@@ -114,8 +114,8 @@ def _align256(x):
 def test_prep_workspace_arithmetic(lib, monkeypatch, N, T, H, cp, seg):
     """The two-kernel area after the CP scratch: slot list (8 B per slot,
     floor(T/64) + units slots), two carry states 2 x H x 128 x 128 f32, and the
-    blobs of one piece (66,048 B per chunk-head; pieces of equal size, at most
-    2 GiB of blobs)."""
+    blobs of all slots (66,048 B per slot and head), capped at 16 GiB of blobs
+    (then pieces of equal size)."""
     monkeypatch.delenv("KDA_PREP_BUDGET_MB", raising=False)
     lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
     lib.kda_chunk_fwd_prep_workspace_size.restype = ctypes.c_size_t
@@ -125,7 +125,7 @@ def test_prep_workspace_arithmetic(lib, monkeypatch, N, T, H, cp, seg):
     units = (T // plan + N) if plan else N
     nslots = T // 64 + units
     per_slot = H * 66048
-    piece = max(1, min(nslots, (2048 << 20) // per_slot))
+    piece = max(1, min(nslots, min(nslots * per_slot, 16384 << 20) // per_slot))
     pieces = -(-nslots // piece)
     piece = -(-nslots // pieces)
     area = _align256(nslots * 8) + _align256(2 * 2 * H * 128 * 128 * 4) + _align256(piece * per_slot)
