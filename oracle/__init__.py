@@ -74,6 +74,8 @@ def _load():
             vargs = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, D, D, I, P, D, D]
             lib.oracle_decode_verify.argtypes = vargs + [I]
             lib.oracle_decode_verify.restype = I
+            lib.oracle_decode_verify_ragged.argtypes = vargs[:13] + [P] + vargs[13:] + [I]
+            lib.oracle_decode_verify_ragged.restype = I
             lib.oracle_decode_stepwise.argtypes = vargs
             lib.oracle_decode_stepwise.restype = I
             _lib = lib
@@ -163,7 +165,8 @@ def chunk_form_head(q, k, v, g, beta, S0=None, C=64, scale=1.0, g_min=-5.0):
 
 
 def _verify_common(fn, stepwise, state, tail, conv_w, cached_qkv, cached_g, cached_b, accepted,
-                   new_qkv, new_g, new_b, out_w, eps_in, eps_out, conv_act, scale, g_min, nthreads):
+                   new_qkv, new_g, new_b, out_w, eps_in, eps_out, conv_act, scale, g_min, nthreads,
+                   draft_len=None):
     state = _f64(state).copy()
     tail = _f64(tail).copy()
     conv_w, cached_qkv, cached_g, cached_b, new_qkv, new_g, new_b, out_w = map(
@@ -180,6 +183,9 @@ def _verify_common(fn, stepwise, state, tail, conv_w, cached_qkv, cached_g, cach
             _ptr(cached_g), _ptr(cached_b), _ptr(acc), _ptr(new_qkv), _ptr(new_g), _ptr(new_b),
             _ptr(out_w), float(eps_in), float(eps_out), int(conv_act), _ptr(o), float(scale),
             float(g_min)]
+    if draft_len is not None:
+        dl = np.ascontiguousarray(np.asarray(draft_len, dtype=np.int32))
+        args.insert(13, _ptr(dl))
     if not stepwise:
         args.append(int(nthreads))
     bad = fn(*args)
@@ -190,11 +196,17 @@ def _verify_common(fn, stepwise, state, tail, conv_w, cached_qkv, cached_g, cach
 
 def decode_verify(state, tail, conv_w, cached_qkv, cached_g, cached_b, accepted, new_qkv, new_g,
                   new_b, out_w, eps_in=1e-6, eps_out=1e-6, conv_act=1, scale=1.0, g_min=-5.0,
-                  nthreads=0):
-    """Replay-based verify.  Returns (state', tail', o [R,Wd+1,H,dv], n_bad)."""
-    return _verify_common(_load().oracle_decode_verify, False, state, tail, conv_w, cached_qkv,
+                  nthreads=0, draft_len=None):
+    """Replay-based verify.  Returns (state', tail', o [R,Wd+1,H,dv], n_bad).
+    draft_len [R] (ragged batches): request r has new rows 0..draft_len[r];
+    its o rows past that stay zero."""
+    if draft_len is None:
+        return _verify_common(_load().oracle_decode_verify, False, state, tail, conv_w, cached_qkv,
+                              cached_g, cached_b, accepted, new_qkv, new_g, new_b, out_w, eps_in,
+                              eps_out, conv_act, scale, g_min, nthreads)
+    return _verify_common(_load().oracle_decode_verify_ragged, False, state, tail, conv_w, cached_qkv,
                           cached_g, cached_b, accepted, new_qkv, new_g, new_b, out_w, eps_in,
-                          eps_out, conv_act, scale, g_min, nthreads)
+                          eps_out, conv_act, scale, g_min, nthreads, draft_len=draft_len)
 
 
 def decode_stepwise(state, tail, conv_w, cached_qkv, cached_g, cached_b, accepted, new_qkv, new_g,

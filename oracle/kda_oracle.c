@@ -340,12 +340,16 @@ int oracle_chunk_form_head(int T, int dk, int dv, int C, const double *q, const 
 /* new_qkv [R][Wd+1][Cq], new_g [R][Wd+1][H*dk], new_b [R][Wd+1][H]            */
 /*                           (row 0 = bonus token, rows 1..Wd = next drafts)   */
 /* accepted [R] in [0, Wd];  out_w [dv];  o [R][Wd+1][H][dv]                  */
+/* draft_len [R] in [0, Wd] or NULL (every request has Wd drafts): request r  */
+/* has new rows 0..draft_len[r] (ragged batches, "Dentro de los esfuerzos de  */
+/* optimizacion de Kimi K3", section 5: irregular batches keep a dynamic      */
+/* path); its o rows past draft_len[r] are not written.                       */
 /* Token order per request: cached rows 0..a-1 (replayed), new row 0 (bonus), */
 /* new rows 1..Wd (drafts).  Per token: conv (+SiLU if conv_act) -> L2 norm   */
 /* of q and k over dk -> g = max(-softplus(g_raw), g_min), b = sigmoid(b_raw) */
 /* -> recurrence step -> for bonus and drafts o = RMSNorm(scale S^T q) * w.   */
-/* Requests with an out-of-range accepted length are skipped entirely (state, */
-/* tail and o untouched) and counted in the return value.                     */
+/* Requests with an out-of-range accepted or draft length are skipped         */
+/* entirely (state, tail and o untouched) and counted in the return value.    */
 /* ------------------------------------------------------------------------- */
 static double softplus(double x) { return (x > 0 ? x : 0.0) + log1p(exp(-fabs(x))); }
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
@@ -439,13 +443,20 @@ static void verify_unit(const struct verify_args *A, int r, int h, int a, int n_
     free(S); free(tmp); free(qv); free(kv); free(vv); free(gv); free(ov);
 }
 
-int oracle_decode_verify(int R, int H, int dk, int dv, int W, int Wd, double *state,
-                         double *tail, const double *conv_w, const double *cached_qkv,
-                         const double *cached_g, const double *cached_b,
-                         const int32_t *accepted, const double *new_qkv, const double *new_g,
-                         const double *new_b, const double *out_w, double eps_in,
-                         double eps_out, int conv_act, double *o, double scale, double g_min,
-                         int nthreads)
+static int request_ok(const int32_t *accepted, const int32_t *draft_len, int Wd, int r)
+{
+    if (accepted[r] < 0 || accepted[r] > Wd) return 0;
+    if (draft_len && (draft_len[r] < 0 || draft_len[r] > Wd)) return 0;
+    return 1;
+}
+
+int oracle_decode_verify_ragged(int R, int H, int dk, int dv, int W, int Wd, double *state,
+                                double *tail, const double *conv_w, const double *cached_qkv,
+                                const double *cached_g, const double *cached_b,
+                                const int32_t *accepted, const int32_t *draft_len,
+                                const double *new_qkv, const double *new_g, const double *new_b,
+                                const double *out_w, double eps_in, double eps_out, int conv_act,
+                                double *o, double scale, double g_min, int nthreads)
 {
     if (R < 0 || H <= 0 || dk <= 0 || dv <= 0 || W < 1 || Wd < 0) return ORACLE_EINVAL;
     struct verify_args A = {R, H, dk, dv, W, Wd, conv_act, eps_in, eps_out, scale, g_min,
@@ -454,7 +465,7 @@ int oracle_decode_verify(int R, int H, int dk, int dv, int W, int Wd, double *st
     int Cq = H * (2 * dk + dv);
     int bad = 0;
     for (int r = 0; r < R; ++r)
-        if (accepted[r] < 0 || accepted[r] > Wd) ++bad;
+        if (!request_ok(accepted, draft_len, Wd, r)) ++bad;
     set_threads(nthreads);
     /* heads read the shared old tail, so the new tails are written after all
        heads of a request are done: copy old tails first */
@@ -464,16 +475,16 @@ int oracle_decode_verify(int R, int H, int dk, int dv, int W, int Wd, double *st
 #pragma omp parallel for schedule(dynamic, 4)
     for (long u = 0; u < units; ++u) {
         int r = (int)(u / H), h = (int)(u % H);
-        int a = accepted[r];
-        if (a < 0 || a > Wd) continue;
+        if (!request_ok(accepted, draft_len, Wd, r)) continue;
+        int a = accepted[r], d = draft_len ? draft_len[r] : Wd;
         double *S = state + ((size_t)r * H + h) * (size_t)dk * dv;
-        verify_unit(&A, r, h, a, a + 1 + Wd, S, old_tail + (size_t)r * (W - 1) * Cq, S, o);
+        verify_unit(&A, r, h, a, a + 1 + d, S, old_tail + (size_t)r * (W - 1) * Cq, S, o);
     }
     /* conv tail write-back: the W-1 most recent pre-conv rows up to and
        including the bonus token, oldest first (a bitwise copy) */
     for (int r = 0; r < R; ++r) {
+        if (!request_ok(accepted, draft_len, Wd, r)) continue;
         int a = accepted[r];
-        if (a < 0 || a > Wd) continue;
         const double *tr = old_tail + (size_t)r * (W - 1) * Cq;
         int last = (W - 1) + a; /* sequence position of the bonus token */
         for (int m = 0; m < W - 1; ++m) {
@@ -483,6 +494,19 @@ int oracle_decode_verify(int R, int H, int dk, int dv, int W, int Wd, double *st
     }
     free(old_tail);
     return bad;
+}
+
+int oracle_decode_verify(int R, int H, int dk, int dv, int W, int Wd, double *state,
+                         double *tail, const double *conv_w, const double *cached_qkv,
+                         const double *cached_g, const double *cached_b,
+                         const int32_t *accepted, const double *new_qkv, const double *new_g,
+                         const double *new_b, const double *out_w, double eps_in,
+                         double eps_out, int conv_act, double *o, double scale, double g_min,
+                         int nthreads)
+{
+    return oracle_decode_verify_ragged(R, H, dk, dv, W, Wd, state, tail, conv_w, cached_qkv,
+                                       cached_g, cached_b, accepted, NULL, new_qkv, new_g, new_b,
+                                       out_w, eps_in, eps_out, conv_act, o, scale, g_min, nthreads);
 }
 
 /* ------------------------------------------------------------------------- */

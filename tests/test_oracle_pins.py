@@ -327,6 +327,53 @@ def test_replay_equals_stepwise_decoding_bitwise(oracle, conv_act):
     np.testing.assert_array_equal(o_v[:, 0], o_s)  # bonus-token output row
 
 
+def test_ragged_windows_pin_the_token_count(oracle):
+    """Ragged verify (a draft count per request, "Dentro de los esfuerzos de
+    optimizacion de Kimi K3" section 5): with no drafts it is one-token-at-a-
+    time decoding of the accepted rows and the bonus (an independent routine),
+    bit for bit; padded draft rows (NaN here) never reach outputs, state or
+    tail; a request's rows match the full window's rows (later drafts cannot
+    change earlier outputs); out-of-range counts skip the request."""
+    rng = np.random.default_rng(35)
+    R, H, dk, dv, Wd = 8, 2, 4, 3, 7
+    inp = decode_inputs(rng, R, H, dk, dv, accepted=list(range(8)))
+    # no drafts == stepwise decoding
+    zero = np.zeros(R, dtype=np.int32)
+    st_r, tl_r, o_r, bad_r = oracle.decode_verify(**inp, draft_len=zero)
+    st_s, tl_s, o_s, bad_s = oracle.decode_stepwise(**inp)
+    assert bad_r == 0 and bad_s == 0
+    np.testing.assert_array_equal(st_r, st_s)
+    np.testing.assert_array_equal(tl_r, tl_s)
+    np.testing.assert_array_equal(o_r[:, 0], o_s)
+    assert np.all(o_r[:, 1:] == 0.0)
+    # random counts, padding poisoned with NaN
+    d = rng.integers(0, Wd + 1, size=R).astype(np.int32)
+    poisoned = {k: v.copy() for k, v in inp.items()}
+    for r in range(R):
+        poisoned["new_qkv"][r, d[r] + 1:] = np.nan
+        poisoned["new_g"][r, d[r] + 1:] = np.nan
+        poisoned["new_b"][r, d[r] + 1:] = np.nan
+    st_p, tl_p, o_p, bad_p = oracle.decode_verify(**poisoned, draft_len=d)
+    st_u, tl_u, o_u, bad_u = oracle.decode_verify(**inp)  # every request with Wd drafts
+    assert bad_p == 0 and bad_u == 0
+    assert np.all(np.isfinite(st_p)) and np.all(np.isfinite(tl_p)) and np.all(np.isfinite(o_p))
+    np.testing.assert_array_equal(st_p, st_u)  # the state is written back after the bonus
+    np.testing.assert_array_equal(tl_p, tl_u)
+    for r in range(R):
+        np.testing.assert_array_equal(o_p[r, :d[r] + 1], o_u[r, :d[r] + 1])
+        assert np.all(o_p[r, d[r] + 1:] == 0.0)
+    # out-of-range counts: request skipped, counted
+    bad_d = d.copy()
+    bad_d[3] = Wd + 1
+    bad_d[5] = -1
+    st_b, tl_b, o_b, nb = oracle.decode_verify(**inp, draft_len=bad_d)
+    assert nb == 2
+    for r in (3, 5):
+        np.testing.assert_array_equal(st_b[r], inp["state"][r])
+        np.testing.assert_array_equal(tl_b[r], inp["tail"][r])
+        assert np.all(o_b[r] == 0.0)
+
+
 def test_conv_identity_and_shift_pin_tail_order(oracle):
     """beta = 0 and g = 0 freeze the state, so each output row reads out
     RMSNorm(S0^T normalize(conv q)).  Identity taps [0,0,0,1] give the token's
