@@ -4,6 +4,7 @@ One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
 32K-token, 96-head, d=128 bf16 workload, inputs resident in HBM, one
 kda_chunk_fwd launch per step.  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
+  "verify_ragged": the same with 3..7 drafts per request (ragged entry point)
   "ckpt":   the headline prefill also emitting the state every 4096 tokens
   "decode": the same entry point as single-token decode (window 0) on 256 x 96
   "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
@@ -424,6 +425,34 @@ def main(argv=None):
                          "requests_per_s": ws * vw.R / (vms * 1e-3)}
         launches += sum(v["launches"] for v in kv.values())
         del d, st, tl, ov
+        torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ ragged verify (drafts 3..7 per request)
+    if "verify" in only:
+        import numpy as np
+        rg = np.random.default_rng(3)
+        rw = synth.DecodeWorkload("verify-replay ragged R=256 H=96 d=128 W=4, window 7, drafts U{3..7}",
+                                  256, 96, 128, 128, Wd=7, seed=4)
+        d = synth.make_decode(rw, device="cuda")
+        dl = torch.as_tensor(rg.integers(3, 8, size=rw.R), dtype=torch.int32, device="cuda")
+        st, tl = d["state"].clone(), d["tail"].clone()
+        ov = torch.empty((rw.R, rw.Wd + 1, rw.H, rw.dv), dtype=torch.bfloat16, device="cuda")
+
+        def ragged_step():
+            kda.decode_verify_replay(st, tl, d["conv_w"], d["cached_qkv"], d["cached_g"], d["cached_b"],
+                                     d["accepted"], d["new_qkv"], d["new_g"], d["new_b"], d["out_w"], out=ov,
+                                     draft_len=dl)
+
+        for _ in range(Wm):
+            ragged_step()
+        rms, kr = timed_launches(kda, ragged_step, K, stream)
+        rms = reduce_max(rms, ws)
+        tokens = int((d["accepted"].to(torch.int64) + 1 + dl.to(torch.int64)).sum().item())
+        out["verify_ragged"] = {"workload": rw.name, "ms": rms, "requests_per_s": ws * rw.R / (rms * 1e-3),
+                                "tokens_replayed_per_launch": tokens,
+                                "state_gbs": ws * 2 * st.numel() * st.element_size() / (rms * 1e-3) / 1e9}
+        launches += sum(v["launches"] for v in kr.values())
+        del d, st, tl, ov, dl
         torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ single-token decode (window 0)

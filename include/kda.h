@@ -63,6 +63,7 @@ extern "C" {
 #define KDA_STATUS_BAD_ACCEPTED_LEN 0x2u /* accepted_len[r] outside [0, Wd]        */
 #define KDA_STATUS_SEGMENT_OVERFLOW 0x4u /* segment table larger than planned      */
 #define KDA_STATUS_TIMEOUT 0x8u          /* a bounded on-chip wait gave up; unit left unfinished */
+#define KDA_STATUS_BAD_DRAFT_LEN 0x10u   /* draft_len[r] outside [0, Wd]                         */
 
 /* Kernel families, for kda_kernel_timing_stop. */
 #define KDA_KERNEL_CHUNK_LIST 0      /* chunk slot list of the two-kernel prefill */
@@ -247,6 +248,32 @@ int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w,
                              const float *out_norm_w, void *o, int R, int H, int dk, int dv,
                              int W, int Wd, float scale, float g_min, float eps_in,
                              float eps_out, int conv_act, uint32_t *status, void *stream);
+
+/*
+ * kda_decode_verify_replay for a ragged batch: request r carries its own
+ * number of drafts draft_len[r] in [0, Wd] ("Dentro de los esfuerzos de
+ * optimizacion de Kimi K3", section 5: uniform batches take a specialised
+ * path, irregular batches keep a dynamic one; the pages' drafts range over
+ * 3-7).  Arrays keep their Wd-sized layouts; request r's verify sequence is
+ * its a_r replayed rows, the bonus and new rows 1..draft_len[r]; new rows past
+ * draft_len[r] are never read into the recurrence (they may hold anything,
+ * NaN included) and its o rows past draft_len[r] are not written.  State and
+ * conv tail are written back after the bonus, as in the uniform call.
+ *  draft_len  device int32 [R]; NULL = every request has Wd drafts (the
+ *             uniform call).  A count outside [0, Wd] sets
+ *             KDA_STATUS_BAD_DRAFT_LEN and skips the request (state, tail and
+ *             o untouched).  With Wd = 0 every count must be 0.
+ * Other arguments, layouts and errors as kda_decode_verify_replay.
+ */
+int kda_decode_verify_replay_ragged(void *state, void *conv_tail, const float *conv_w,
+                                    const void *cached_qkv, const void *cached_g,
+                                    const void *cached_beta, const int32_t *accepted_len,
+                                    const int32_t *draft_len, const void *new_qkv,
+                                    const void *new_g, const void *new_beta,
+                                    const float *out_norm_w, void *o, int R, int H, int dk,
+                                    int dv, int W, int Wd, float scale, float g_min,
+                                    float eps_in, float eps_out, int conv_act,
+                                    uint32_t *status, void *stream);
 
 /*
  * Context-parallel prefill that allocates nothing.  (The pages have no

@@ -18,7 +18,8 @@ import torch
 __all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_prep_workspace_size", "chunk_fwd_plan", "segment_transition",
            "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
            "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
-           "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW", "KERNEL_FAMILIES", "kernel_timing_start",
+           "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW", "STATUS_TIMEOUT", "STATUS_BAD_DRAFT_LEN",
+           "KERNEL_FAMILIES", "kernel_timing_start",
            "kernel_timing_stop"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +31,7 @@ CP_OFF, CP_ON, CP_AUTO = 0, 1, -1
 CONV_NONE, CONV_SILU = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS_BAD_SEQLENS, STATUS_BAD_ACCEPTED_LEN, STATUS_SEGMENT_OVERFLOW = 1, 2, 4
+STATUS_TIMEOUT, STATUS_BAD_DRAFT_LEN = 8, 16
 
 
 class KDAError(RuntimeError):
@@ -73,6 +75,9 @@ def load_library():
         lib.kda_kernel_timing_start.argtypes = []
         lib.kda_kernel_timing_stop.restype = I
         lib.kda_kernel_timing_stop.argtypes = [P, P, I]
+        lib.kda_decode_verify_replay_ragged.restype = I
+        lib.kda_decode_verify_replay_ragged.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                                        F, F, F, F, I, P, P]
         lib.kda_decode_verify_replay.restype = I
         lib.kda_decode_verify_replay.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
                                                  F, F, F, F, I, P, P]
@@ -213,15 +218,26 @@ def kernel_timing_stop():
 
 def decode_verify_replay(state, conv_tail, conv_w, cached_qkv, cached_g, cached_beta, accepted_len,
                          new_qkv, new_g, new_beta, out_norm_w, scale=1.0, g_min=-5.0, eps_in=1e-6,
-                         eps_out=1e-6, conv_act=CONV_SILU, out=None, status=None, stream=None):
+                         eps_out=1e-6, conv_act=CONV_SILU, out=None, status=None, stream=None, draft_len=None):
     """Fused verify with replay.  Updates state and conv_tail in place; returns
-    o [R, Wd+1, H, dv] (bf16): rows for the bonus token and the next drafts."""
+    o [R, Wd+1, H, dv] (bf16): rows for the bonus token and the next drafts.
+    draft_len (int32 [R] on the device) makes the batch ragged: request r has
+    draft_len[r] drafts (kda_decode_verify_replay_ragged); its rows past that
+    are not written."""
     lib = load_library()
     R, H, dk, dv = state.shape
     W = conv_w.shape[1]
     Wd = new_qkv.shape[1] - 1
     if out is None:
         out = torch.empty((R, Wd + 1, H, dv), dtype=torch.bfloat16, device=state.device)
+    if draft_len is not None:
+        rc = lib.kda_decode_verify_replay_ragged(
+            _ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv), _ptr(cached_g), _ptr(cached_beta),
+            _ptr(accepted_len), _ptr(draft_len), _ptr(new_qkv), _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w),
+            _ptr(out), R, H, dk, dv, W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
+            int(conv_act), _ptr(status), _stream(stream))
+        _check(rc, "kda_decode_verify_replay_ragged")
+        return out
     rc = lib.kda_decode_verify_replay(_ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv),
                                       _ptr(cached_g), _ptr(cached_beta), _ptr(accepted_len), _ptr(new_qkv),
                                       _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w), _ptr(out), R, H, dk, dv,

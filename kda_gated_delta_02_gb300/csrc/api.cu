@@ -423,6 +423,18 @@ int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w, 
                              const float *out_norm_w, void *o, int R, int H, int dk, int dv, int W, int Wd,
                              float scale, float g_min, float eps_in, float eps_out, int conv_act,
                              uint32_t *status, void *stream) {
+    return kda_decode_verify_replay_ragged(state, conv_tail, conv_w, cached_qkv, cached_g, cached_beta,
+                                           accepted_len, nullptr, new_qkv, new_g, new_beta, out_norm_w, o, R,
+                                           H, dk, dv, W, Wd, scale, g_min, eps_in, eps_out, conv_act, status,
+                                           stream);
+}
+
+int kda_decode_verify_replay_ragged(void *state, void *conv_tail, const float *conv_w, const void *cached_qkv,
+                                    const void *cached_g, const void *cached_beta, const int32_t *accepted_len,
+                                    const int32_t *draft_len, const void *new_qkv, const void *new_g,
+                                    const void *new_beta, const float *out_norm_w, void *o, int R, int H,
+                                    int dk, int dv, int W, int Wd, float scale, float g_min, float eps_in,
+                                    float eps_out, int conv_act, uint32_t *status, void *stream) {
     if (R < 0 || H < 1 || W < 1 || W > 4 || Wd < 0 || Wd > 7) return KDA_ERR_INVALID_ARG;
     if (conv_act != KDA_CONV_NONE && conv_act != KDA_CONV_SILU) return KDA_ERR_INVALID_ARG;
     if (!(dk == dv && dim_ok(dk))) return KDA_ERR_UNSUPPORTED_SHAPE;
@@ -438,6 +450,7 @@ int kda_decode_verify_replay(void *state, void *conv_tail, const float *conv_w, 
     a.state = state; a.tail = conv_tail; a.conv_w = conv_w;
     a.cached_qkv = cached_qkv; a.cached_g = cached_g; a.cached_b = cached_beta;
     a.accepted = accepted_len;
+    a.draft_len = draft_len;
     a.new_qkv = new_qkv; a.new_g = new_g; a.new_b = new_beta;
     a.out_w = out_norm_w; a.o = o;
     a.R = R; a.H = H; a.dk = dk; a.dv = dv; a.W = W; a.Wd = Wd;

@@ -44,6 +44,10 @@ __global__ void __launch_bounds__(NT, 4) kda_decode_token_kernel(VerifyArgs p) {
         if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_ACCEPTED_LEN);
         return;
     }
+    if (p.draft_len && p.draft_len[r] != 0) {  // and so must the draft count
+        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_DRAFT_LEN);
+        return;
+    }
 
     // ---------------------------------------------------------------- state read (first, to overlap)
     // each thread copies its own 16-byte pieces into shared memory and reads

@@ -107,7 +107,12 @@ __global__ void __launch_bounds__(D) kda_verify_kernel(VerifyArgs p) {
         if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_ACCEPTED_LEN);
         return;
     }
-    const int ntok = a + 1 + Wd;  // <= 16 (host-checked Wd <= 7)
+    const int dr = p.draft_len ? p.draft_len[r] : Wd;  // this request's drafts (ragged batches)
+    if (dr < 0 || dr > Wd) {
+        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_DRAFT_LEN);
+        return;
+    }
+    const int ntok = a + 1 + dr;  // <= 16 (host-checked Wd <= 7)
     const int nrows = (W - 1) + ntok;
     const size_t Cq = (size_t)H * 3 * D;
 

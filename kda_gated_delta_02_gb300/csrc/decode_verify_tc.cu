@@ -163,7 +163,12 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_ACCEPTED_LEN);
         return;
     }
-    const int ntok = a + 1 + Wd;  // <= 15 (host-checked Wd <= 7), so a <= 7 lies in the first half
+    const int dr = p.draft_len ? p.draft_len[r] : Wd;  // this request's drafts (ragged batches)
+    if (dr < 0 || dr > Wd) {
+        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_DRAFT_LEN);
+        return;
+    }
+    const int ntok = a + 1 + dr;  // <= 15 (host-checked Wd <= 7), so a <= 7 lies in the first half
     const size_t HD = (size_t)H * D, Cq = 3 * HD;
     const size_t chq = (size_t)h * D + c;
 

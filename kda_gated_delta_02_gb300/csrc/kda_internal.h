@@ -82,6 +82,7 @@ struct VerifyArgs {
     const float *conv_w;
     const void *cached_qkv, *cached_g, *cached_b;
     const int32_t *accepted;
+    const int32_t *draft_len;  // [R] drafts per request, or null (every request has Wd)
     const void *new_qkv, *new_g, *new_b;
     const float *out_w;
     void *o;
