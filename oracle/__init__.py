@@ -72,6 +72,9 @@ def _load():
             lib.oracle_chunk_form_head.argtypes = [I, I, I, I, P, P, P, P, P, P, P, D, D]
             lib.oracle_chunk_form_head.restype = I
             vargs = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, D, D, I, P, D, D]
+            lib.oracle_kda_backward.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, D, D,
+                                                I]
+            lib.oracle_kda_backward.restype = I
             lib.oracle_decode_verify.argtypes = vargs + [I]
             lib.oracle_decode_verify.restype = I
             lib.oracle_decode_verify_ragged.argtypes = vargs[:13] + [P] + vargs[13:] + [I]
@@ -150,6 +153,30 @@ def unit_lower_inverse(A):
     T = np.zeros((n, n))
     _load().oracle_unit_lower_inverse(n, _ptr(A), _ptr(T))
     return T
+
+
+def backward(q, k, v, g, beta, cu_seqlens, do, S0=None, dS_final=None, scale=1.0, g_min=-5.0, nthreads=0):
+    """Reverse mode of the token recurrence (prefill with erase).  Shapes as
+    prefill; do [T,H,dv]; dS_final [N,H,dk,dv] or None.  Returns float64
+    (dq, dk, dv, dg, dbeta, dS0): dg is w.r.t. the raw g (zero where
+    g < g_min), dS0 w.r.t. the initial state."""
+    q, k, v, g, beta, do = map(_f64, (q, k, v, g, beta, do))
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    S0 = None if S0 is None else _f64(S0).reshape(N, H, dk, dv)
+    dS_final = None if dS_final is None else _f64(dS_final).reshape(N, H, dk, dv)
+    dq, dkk, dg = (np.zeros((T, H, dk)) for _ in range(3))
+    dvv = np.zeros((T, H, dv))
+    db = np.zeros((T, H))
+    dS0 = np.zeros((N, H, dk, dv))
+    rc = _load().oracle_kda_backward(N, T, H, dk, dv, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(S0), _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
+                                     _ptr(db), _ptr(dS0), float(scale), float(g_min), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle backward rejected its arguments")
+    return dq, dkk, dvv, dg, db, dS0
 
 
 def chunk_form_head(q, k, v, g, beta, S0=None, C=64, scale=1.0, g_min=-5.0):

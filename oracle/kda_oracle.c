@@ -155,6 +155,114 @@ int oracle_kda_prefill(int N, int T, int H, int dk, int dv, const int32_t *cu_se
 }
 
 /* ------------------------------------------------------------------------- */
+/* Backward of the prefill (reverse mode of the token recurrence above; the   */
+/* pages name the backward pass as the other use of the chunk kernel,         */
+/* "Noyaux KDA et FlashKDA", section "FlashKDA : le noyau par blocs"), per    */
+/* (sequence, head).  Inputs as oracle_kda_prefill (erase on) plus            */
+/* do_ [T][H][dv] and dS_final [N][H][dk][dv] (or NULL: zero).  Outputs       */
+/* dq, dk_ [T][H][dk], dv_ [T][H][dv], dg [T][H][dk] (gradient w.r.t. the raw */
+/* g: zero where the floor holds, g < g_min), dbeta [T][H], dS0 [N][H][dk][dv] */
+/* (or NULL).  Per token (S before, S' after, D = Diag(e^{max(g, g_min)}),    */
+/* X = D S, p = X^T k, u = beta (v - p), S' = X + k u^T, o = scale S'^T q),   */
+/* with G the gradient w.r.t. S' coming from later tokens:                   */
+/*   G += scale q do^T;  dq = scale S' do;  du = G^T k;  dv = beta du;        */
+/*   dbeta = du . (v - p);  dk = G u - beta X du;  dX = G - beta k du^T;      */
+/*   dg_i = sum_j dX_ij X_ij  (where g_i >= g_min);  G <- D dX.               */
+/* Every forward state of a sequence is kept (small cases only).             */
+/* ------------------------------------------------------------------------- */
+int oracle_kda_backward(int N, int T, int H, int dk, int dv, const int32_t *cu_seqlens,
+                        const double *q, const double *k, const double *v, const double *g,
+                        const double *beta, const double *S0, const double *do_,
+                        const double *dS_final, double *dq, double *dk_, double *dv_, double *dg,
+                        double *dbeta, double *dS0, double scale, double g_min, int nthreads)
+{
+    if (N < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens) return ORACLE_EINVAL;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return ORACLE_EINVAL;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return ORACLE_EINVAL;
+    set_threads(nthreads);
+    const size_t DD = (size_t)dk * dv;
+    long units = (long)N * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long un = 0; un < units; ++un) {
+        int n = (int)(un / H), h = (int)(un % H);
+        int t0 = cu_seqlens[n], L = cu_seqlens[n + 1] - t0;
+        size_t so = ((size_t)n * H + h) * DD;
+        double *Sall = (double *)malloc(sizeof(double) * DD * (size_t)(L + 1));
+        double *G = (double *)malloc(sizeof(double) * DD);
+        double *X = (double *)malloc(sizeof(double) * DD);
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)dv * 4);
+        double *p = tmp, *u = tmp + dv, *du = tmp + 2 * dv;
+        if (S0) memcpy(Sall, S0 + so, sizeof(double) * DD);
+        else memset(Sall, 0, sizeof(double) * DD);
+        for (int t = 0; t < L; ++t) {
+            size_t th = (size_t)(t0 + t) * H + h;
+            memcpy(Sall + DD * (t + 1), Sall + DD * t, sizeof(double) * DD);
+            kda_token(dk, dv, Sall + DD * (t + 1), k + th * dk, v + th * dv, g + th * dk, beta[th], g_min, 1,
+                      tmp + 3 * dv);
+        }
+        if (dS_final) memcpy(G, dS_final + so, sizeof(double) * DD);
+        else memset(G, 0, sizeof(double) * DD);
+        for (int t = L - 1; t >= 0; --t) {
+            size_t th = (size_t)(t0 + t) * H + h;
+            const double *qt = q + th * dk, *kt = k + th * dk, *vt = v + th * dv, *gt = g + th * dk;
+            const double *dot = do_ + th * dv, *Sp = Sall + DD * t, *Sn = Sall + DD * (t + 1);
+            double bt = beta[th];
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] += scale * qt[i] * dot[j];
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j) acc += Sn[(size_t)i * dv + j] * dot[j];
+                dq[th * dk + i] = scale * acc;
+            }
+            for (int i = 0; i < dk; ++i) {
+                double gi = gt[i] < g_min ? g_min : gt[i];
+                double d = exp(gi);
+                for (int j = 0; j < dv; ++j) X[(size_t)i * dv + j] = d * Sp[(size_t)i * dv + j];
+            }
+            for (int j = 0; j < dv; ++j) {
+                double pj = 0.0, dj = 0.0;
+                for (int i = 0; i < dk; ++i) {
+                    pj += X[(size_t)i * dv + j] * kt[i];
+                    dj += G[(size_t)i * dv + j] * kt[i];
+                }
+                p[j] = pj;
+                u[j] = bt * (vt[j] - pj);
+                du[j] = dj;
+            }
+            double db = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                dv_[th * dv + j] = bt * du[j];
+                db += du[j] * (vt[j] - p[j]);
+            }
+            dbeta[th] = db;
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j)
+                    acc += G[(size_t)i * dv + j] * u[j] - bt * X[(size_t)i * dv + j] * du[j];
+                dk_[th * dk + i] = acc;
+            }
+            for (int i = 0; i < dk; ++i) {
+                double gi = gt[i] < g_min ? g_min : gt[i];
+                double d = exp(gi), acc = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    double dx = G[(size_t)i * dv + j] - bt * kt[i] * du[j];
+                    acc += dx * X[(size_t)i * dv + j];
+                    G[(size_t)i * dv + j] = d * dx;
+                }
+                dg[th * dk + i] = (gt[i] < g_min) ? 0.0 : acc;
+            }
+        }
+        if (dS0) memcpy(dS0 + so, G, sizeof(double) * DD);
+        free(Sall);
+        free(G);
+        free(X);
+        free(tmp);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Segment transition over tokens [0, T) of the given arrays, per head:       */
 /*   M = A_T ... A_1,  A_t = (I - b_t k_t k_t^T) Diag(exp g_t)   [H][dk][dk]  */
 /*   N = state reached from S = 0                                 [H][dk][dv] */

@@ -489,3 +489,74 @@ def test_state_traffic_arithmetic():
     from kda_gated_delta_02_gb300 import synth
     assert synth.state_bytes(rows["layers"], rows["heads"], rows["dk"], rows["dv"],
                              rows["bytes_per_elem"]) == rows["state_bytes_all_layers"]
+
+
+# --------------------------------------------------------------------------- backward
+def _fd_case(rng, lens, H=2, dk=3, dv=2, floor_frac=0.25):
+    T = int(sum(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = -np.abs(rng.standard_normal((T, H, dk)))  # above the floor, well away from it
+    below = rng.random((T, H, dk)) < floor_frac
+    g[below] = -5.0 - 0.5 - rng.random(int(below.sum()))  # under the floor by more than the step
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    S0 = 0.3 * rng.standard_normal((len(lens), H, dk, dv))
+    Wo = rng.standard_normal((T, H, dv))
+    Ws = rng.standard_normal((len(lens), H, dk, dv))
+    return dict(q=q, k=k, v=v, g=g, beta=beta, S0=S0, cu=cu), Wo, Ws
+
+
+def test_backward_matches_central_differences(oracle):
+    """The reverse-mode oracle against central differences of the forward
+    oracle's loss <o, Wo> + <S_final, Ws> (h = 1e-6, fp64), for every element of
+    q, k, v, g, beta and S0, on packed sequences (one of length 1) with part of
+    g under the floor (derivative 0 there) and a scale."""
+    rng = np.random.default_rng(90)
+    x, Wo, Ws = _fd_case(rng, [5, 1, 4])
+    scale = 0.7
+
+    def loss(d):
+        o, Sf = oracle.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], S0=d["S0"], scale=scale)
+        return float(np.sum(o * Wo) + np.sum(Sf * Ws))
+
+    dq, dk, dv, dg, db, dS0 = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], Wo,
+                                              S0=x["S0"], dS_final=Ws, scale=scale)
+    grads = dict(q=dq, k=dk, v=dv, g=dg, beta=db, S0=dS0)
+    h = 1e-6
+    for name, gr in grads.items():
+        fd = np.zeros_like(gr)
+        for idx in np.ndindex(gr.shape):
+            xp = {kk: vv.copy() for kk, vv in x.items()}
+            xm = {kk: vv.copy() for kk, vv in x.items()}
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+        err = np.max(np.abs(fd - gr)) / max(1e-3, np.max(np.abs(fd)))
+        assert err < 1e-6, f"d{name}: relative error {err:.2e}"
+    assert np.all(dg[x["g"] < -5.0] == 0.0)  # the floor passes no gradient
+
+
+def test_backward_without_final_state_gradient_and_beta_zero(oracle):
+    """With beta = 0 nothing is written: o_t = scale S_t^T q_t with
+    S_t = D_t..D_1 S0, so dq, dS0 have closed forms and dk = dv = 0."""
+    rng = np.random.default_rng(91)
+    T, H, dk, dv = 4, 1, 3, 2
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    g = -np.abs(rng.standard_normal((T, H, dk)))
+    beta = np.zeros((T, H))
+    S0 = rng.standard_normal((1, H, dk, dv))
+    do = rng.standard_normal((T, H, dv))
+    dq, dkk, dvv, dg, db, dS0 = oracle.backward(q, k, v, g, beta, [0, T], do, S0=S0)
+    np.testing.assert_array_equal(dkk, 0.0)
+    np.testing.assert_array_equal(dvv, 0.0)
+    decay = np.cumprod(np.exp(g[:, 0]), axis=0)  # [T, dk]: prod_{r<=t} e^{g_r}
+    for t in range(T):
+        St = decay[t][:, None] * S0[0, 0]
+        np.testing.assert_allclose(dq[t, 0], St @ do[t, 0], rtol=1e-12, atol=1e-12)
+    want = sum(np.outer(decay[t] * q[t, 0], do[t, 0]) for t in range(T))
+    np.testing.assert_allclose(dS0[0, 0], want, rtol=1e-12, atol=1e-12)
