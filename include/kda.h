@@ -74,7 +74,8 @@ extern "C" {
 #define KDA_KERNEL_SEGMENT_COMPOSE 5 /* CP composition */
 #define KDA_KERNEL_SEGMENT_TABLE 6   /* CP segment table */
 #define KDA_KERNEL_VERIFY 7          /* kda_decode_verify_replay (verify or single-token decode) */
-#define KDA_KERNEL_KINDS 8
+#define KDA_KERNEL_CHUNK_BWD 8       /* kda_chunk_bwd */
+#define KDA_KERNEL_KINDS 9
 
 /* Human-readable name of a return status. Never NULL. */
 const char *kda_status_string(int status);
@@ -175,6 +176,37 @@ size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, in
 /* The segment length (tokens) and CP decision kda_chunk_fwd would use:
  * returns 0 when CP is off, else the segment length. Pure host arithmetic. */
 int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len);
+
+/*
+ * Backward of kda_chunk_fwd (training; "Noyaux KDA et FlashKDA", section
+ * "FlashKDA : le noyau par blocs" names it as the chunk kernel's other use):
+ * the gradients of a loss L with respect to every input, given dL/do and
+ * dL/dS_final.  Reverse mode of the recurrence per token (S before, S' after,
+ * D = Diag(e^{max(g, g_min)}), X = D S, p = X^T k, u = beta (v - p),
+ * S' = X + k u^T, o = scale S'^T q; G = dL/dS'):
+ *     G += scale q do^T;  dq = scale S' do;  du = G^T k;  dv = beta du;
+ *     dbeta = du . (v - p);  dk = G u - beta X du;  dX = G - beta k du^T;
+ *     dg_i = sum_j dX_ij X_ij, 0 where g_i < g_min;  G <- D dX;  dS0 = G at the start.
+ * Computed in fp32 on the CUDA cores, one CTA per (sequence, head); states are
+ * recomputed from chunk-start checkpoints (64 tokens) kept in the workspace.
+ *  q, k, v, g, beta, cu_seqlens, N, T, H, initial_state, scale, g_min,
+ *  in_dtype   as kda_chunk_fwd (dk = dv = 64 or 128; cp off).
+ *  dout       device [T][H][dv], in_dtype: dL/do.
+ *  dS_final   device f32 [N][H][dk][dv] or NULL (zero): dL/dS_final.
+ *  dq, dk, dv device f32 [T][H][d]; dg device f32 [T][H][dk] (w.r.t. the raw
+ *             g); dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
+ *  workspace  device scratch of at least kda_chunk_bwd_workspace_size(...)
+ *             bytes ((floor(T/64) + N) x H chunk checkpoints and N x H x 64
+ *             states, d x d f32 each); KDA_ERR_WORKSPACE when smaller.
+ * Invalid cu_seqlens set KDA_STATUS_BAD_SEQLENS; that sequence is skipped.
+ */
+int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                  const float *initial_state, const void *dout, const float *dS_final, float *dq,
+                  float *dk_, float *dv_, float *dg, float *dbeta, float *dS0, float scale,
+                  float g_min, int in_dtype, void *workspace, size_t workspace_bytes,
+                  uint32_t *status, void *stream);
+size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv);
 
 /*
  * Segment transitions of one sequence ("Noyaux KDA et FlashKDA", section "Le

@@ -19,7 +19,7 @@ __all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_prep_workspace_si
            "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
            "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
            "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW", "STATUS_TIMEOUT", "STATUS_BAD_DRAFT_LEN",
-           "KERNEL_FAMILIES", "kernel_timing_start",
+           "KERNEL_FAMILIES", "chunk_bwd", "kernel_timing_start",
            "kernel_timing_stop"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +71,10 @@ def load_library():
         lib.kda_segment_transition.argtypes = [P, P, P, P, I, I, I, I, I, P, P, F, I, P]
         lib.kda_segment_compose.restype = I
         lib.kda_segment_compose.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.kda_chunk_bwd.restype = I
+        lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, F, F, I, P, S, P, P]
+        lib.kda_chunk_bwd_workspace_size.restype = S
+        lib.kda_chunk_bwd_workspace_size.argtypes = [I, I, I, I, I]
         lib.kda_kernel_timing_start.restype = I
         lib.kda_kernel_timing_start.argtypes = []
         lib.kda_kernel_timing_stop.restype = I
@@ -197,7 +201,36 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
 # kernel families of kda_kernel_timing_stop, in KDA_KERNEL_* order
 KERNEL_FAMILIES = ("kda_chunk_list_kernel", "kda_chunk_prep_kernel", "kda_chunk_walk_kernel",
                    "kda_chunk_tc_kernel", "kda_chunk_kernel", "kda_compose_kernel", "kda_segment_table_kernel",
-                   "kda_decode_verify_replay")
+                   "kda_decode_verify_replay", "kda_chunk_bwd_kernel")
+
+
+def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=None, scale=1.0, g_min=-5.0,
+              workspace=None, status=None, stream=None, want_dS0=True):
+    """Backward of chunk_fwd: returns (dq, dk, dv, dg, dbeta, dS0) in fp32
+    (dS0 None unless want_dS0).  do [T,H,dv] in q's dtype; dS_final f32
+    [N,H,dk,dv] or None."""
+    lib = load_library()
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    f32 = torch.float32
+    dq = torch.empty((T, H, dk), dtype=f32, device=dev)
+    dkk = torch.empty((T, H, dk), dtype=f32, device=dev)
+    dvv = torch.empty((T, H, dv), dtype=f32, device=dev)
+    dg = torch.empty((T, H, dk), dtype=f32, device=dev)
+    db = torch.empty((T, H), dtype=f32, device=dev)
+    dS0 = torch.empty((N, H, dk, dv), dtype=f32, device=dev) if want_dS0 else None
+    need = int(lib.kda_chunk_bwd_workspace_size(N, T, H, dk, dv))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                           _ptr(initial_state), _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
+                           _ptr(db), _ptr(dS0), float(scale), float(g_min), _in_dtype(q), _ptr(workspace),
+                           ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(status),
+                           _stream(stream))
+    _check(rc, "kda_chunk_bwd")
+    return dq, dkk, dvv, dg, db, dS0
 
 
 def kernel_timing_start():

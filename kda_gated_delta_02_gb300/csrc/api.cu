@@ -460,6 +460,42 @@ int kda_decode_verify_replay_ragged(void *state, void *conv_tail, const float *c
     return cuda_status(timed_launch(KDA_KERNEL_VERIFY, st, [&] { return kda::launch_verify(a, st); }));
 }
 
+size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
+    if (N < 1 || T < 0 || H < 1 || dk != dv || !dim_ok(dk)) return 0;
+    const size_t DD = (size_t)dk * dv * 4;
+    return align256((size_t)(T / kChunk + N) * H * DD) + align256((size_t)N * H * kChunk * DD);
+}
+
+int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const float *initial_state,
+                  const void *dout, const float *dS_final, float *dq, float *dk_, float *dv_, float *dg,
+                  float *dbeta, float *dS0, float scale, float g_min, int in_dtype, void *workspace,
+                  size_t workspace_bytes, uint32_t *status, void *stream) {
+    if (N < 1 || T < 0 || H < 1 || !cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (dk != dv || !dim_ok(dk)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dout) ||
+        !aligned16(initial_state) || !aligned16(dS_final) || !aligned16(dS0) || !aligned16(workspace))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)T * H * dk >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = kda_chunk_bwd_workspace_size(N, T, H, dk, dv);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    const size_t DD = (size_t)dk * dv * 4;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    kda::BwdArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.dout = dout; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
+    a.S0 = initial_state; a.dS_final = dS_final;
+    a.dq = dq; a.dk = dk_; a.dv = dv_; a.dg = dg; a.dbeta = dbeta; a.dS0 = dS0;
+    a.ckpt = reinterpret_cast<float *>(ws);
+    a.scratch = reinterpret_cast<float *>(ws + align256((size_t)(T / kChunk + N) * H * DD));
+    a.N = N; a.T = T; a.H = H; a.scale = scale; a.g_min = g_min; a.status = status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,
+                                    [&] { return kda::launch_chunk_bwd(a, dk, in_dtype == KDA_DTYPE_BF16, st); }));
+}
+
 int kda_kernel_timing_start(void) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     drop_timed();

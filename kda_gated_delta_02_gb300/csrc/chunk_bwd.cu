@@ -1,0 +1,322 @@
+// chunk_bwd.cu -- backward of the prefill on the CUDA cores (sm_103a): dq, dk,
+// dv, dg, dbeta and dS0 from the output gradient do and the final-state
+// gradient dS_final.
+//
+// Reverse mode of the token recurrence (the pages name training, which needs
+// this pass, as the other use of the chunk kernel: "Noyaux KDA et FlashKDA",
+// section "FlashKDA : le noyau par blocs").  Per token, with S the state
+// before it, D = Diag(e^{max(g, g_min)}), X = D S, p = X^T k, u = b (v - p),
+// S' = X + k u^T, o = scale S'^T q, and G the gradient w.r.t. S' coming from
+// later tokens:
+//   G += scale q do^T;  dq = scale S' do;  du = G^T k;  dv = b du;
+//   db = du . (v - p);  dk = G u - b X du;  dX = G - b k du^T;
+//   dg_i = sum_j dX_ij X_ij (zero where g_i < g_min);  G <- D dX.
+// The value columns of the state evolve independently (k, g, b are shared by
+// all of them), so a CTA of D/32 groups of D threads walks one (sequence,
+// head): group c owns value columns 32c .. 32c + 31 and its thread i owns key
+// row i of them (32 fp32 of S and 32 of G in registers).  Sums over key rows
+// (p, du) go through a 32-lane transpose-sum and the group's warps; sums over
+// value columns (dq, dk, dg, db) are per-thread partials added across the
+// groups in shared memory, in a fixed order.
+// Pass 1 walks the sequence forward and keeps the state at every chunk start
+// (64 tokens) in a slot-indexed buffer (chunk j of sequence n is slot
+// floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
+// chunk's states from its checkpoint into a per-CTA scratch (u and p per token
+// into shared memory) and runs the backward steps over them.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace bw {
+
+constexpr int CH = 64;
+
+template <bool BF16>
+__device__ __forceinline__ float ld_in(const void *p, size_t idx) {
+    if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[idx]);
+    else return reinterpret_cast<const float *>(p)[idx];
+}
+
+// v[j] summed over the 32 lanes of the warp; lane l returns the sum of column
+// l (five exchange rounds of halves; v is destroyed)
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool hi = (lane & w) != 0;
+#pragma unroll
+        for (int c = 0; c < w; ++c) {
+            const float send = hi ? v[c] : v[c + w];
+            const float keep = hi ? v[c + w] : v[c];
+            v[c] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <int D>
+struct BwdSmem {
+    static constexpr int NG = D / 32;
+    static constexpr int WPG = D / 32;  // warps per group
+    static constexpr size_t off_v = 0;                                  // f32 [CH][D] staged v
+    static constexpr size_t off_do = off_v + (size_t)CH * D * 4;         // f32 [CH][D] staged do
+    static constexpr size_t off_u = off_do + (size_t)CH * D * 4;         // f32 [CH][D] u per token
+    static constexpr size_t off_p = off_u + (size_t)CH * D * 4;          // f32 [CH][D] p per token
+    static constexpr size_t off_red = off_p + (size_t)CH * D * 4;        // f32 [NG][WPG][32]
+    static constexpr size_t off_du = off_red + (size_t)NG * WPG * 32 * 4;  // f32 [D]
+    static constexpr size_t off_row = off_du + (size_t)D * 4;            // f32 [3][NG][D]
+    static constexpr size_t off_db = off_row + (size_t)3 * NG * D * 4;   // f32 [NG]
+    static constexpr size_t bytes = off_db + 64;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdArgs p) {
+    using L = BwdSmem<D>;
+    constexpr int NG = L::NG, WPG = L::WPG;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *sV = reinterpret_cast<float *>(smem + L::off_v);
+    float *sDo = reinterpret_cast<float *>(smem + L::off_do);
+    float *sU = reinterpret_cast<float *>(smem + L::off_u);
+    float *sP = reinterpret_cast<float *>(smem + L::off_p);
+    float *sRed = reinterpret_cast<float *>(smem + L::off_red);
+    float *sDu = reinterpret_cast<float *>(smem + L::off_du);
+    float *sRow = reinterpret_cast<float *>(smem + L::off_row);
+    float *sDb = reinterpret_cast<float *>(smem + L::off_db);
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int gi = tid / D, i = tid % D, wg = i >> 5;  // group, key row, warp in the group
+    const int c0 = 32 * gi;                            // first value column of the group
+    const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+    const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
+    if (t0 < 0 || t1 < t0 || t1 > p.T) {
+        if (tid == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
+        return;
+    }
+    const int Ln = t1 - t0, nch = (Ln + CH - 1) / CH;
+    const size_t DD = (size_t)D * D;
+    const size_t unit = (size_t)n * H + h;
+    const float g_min = p.g_min, scale = p.scale;
+    float *scr = p.scratch + unit * (size_t)CH * DD;  // [CH][D][D]: state before each token of the chunk
+
+    // the staged rows of chunk j (tokens t0 + 64 j ..): v, and do in the backward pass
+    auto stage = [&](int j, bool with_do) {
+        const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
+        for (int idx = tid; idx < lc * D; idx += NG * D) {
+            const int tt = idx / D, c = idx % D;
+            const size_t th = ((size_t)(tb + tt) * H + h) * D + c;
+            sV[tt * D + c] = ld_in<BF16>(p.v, th);
+            if (with_do) sDo[tt * D + c] = ld_in<BF16>(p.dout, th);
+        }
+    };
+    // one forward step of token tb + tt on this thread's slab S (row i, columns
+    // c0 ..); keeps p and u of the token in shared memory
+    auto fwd_step = [&](float (&S)[32], int tb, int tt) {
+        const size_t th = (size_t)(tb + tt) * H + h;
+        const float e = __expf(fmaxf(p.g[th * D + i], g_min));
+        const float ki = ld_in<BF16>(p.k, th * D + i);
+        float pv[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = (e * S[c]) * ki;
+        const float ps = transpose_sum32(pv, lane);
+        sRed[(gi * WPG + wg) * 32 + lane] = ps;
+        group_sync(1 + gi, D);
+        if (wg == 0) {
+            float pj = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPG; ++w) pj += sRed[(gi * WPG + w) * 32 + lane];
+            const float b = p.beta[th];
+            sP[tt * D + c0 + lane] = pj;
+            sU[tt * D + c0 + lane] = b * (sV[tt * D + c0 + lane] - pj);
+        }
+        group_sync(1 + gi, D);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            const float4 u4 = *reinterpret_cast<const float4 *>(sU + tt * D + c0 + c);
+            S[c + 0] = fmaf(ki, u4.x, e * S[c + 0]);
+            S[c + 1] = fmaf(ki, u4.y, e * S[c + 1]);
+            S[c + 2] = fmaf(ki, u4.z, e * S[c + 2]);
+            S[c + 3] = fmaf(ki, u4.w, e * S[c + 3]);
+        }
+    };
+    auto slot_of = [&](int j) { return (size_t)(t0 / CH + n + j); };
+
+    // ---------------------------------------------------------------- pass 1: chunk-start states
+    {
+        float S[32];
+        const float *src = p.S0 ? p.S0 + unit * DD + (size_t)i * D + c0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[c] = v4.x;
+            S[c + 1] = v4.y;
+            S[c + 2] = v4.z;
+            S[c + 3] = v4.w;
+        }
+        for (int j = 0; j < nch; ++j) {
+            float *ck = p.ckpt + (slot_of(j) * H + h) * DD + (size_t)i * D + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4 *>(ck + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+            if (j == nch - 1) break;  // the last chunk's states are recomputed in pass 2
+            stage(j, false);
+            __syncthreads();
+            const int tb = t0 + CH * j;
+            for (int tt = 0; tt < CH; ++tt) fwd_step(S, tb, tt);
+            __syncthreads();
+        }
+    }
+
+    // ---------------------------------------------------------------- pass 2: chunks in reverse
+    float G[32];
+    {
+        const float *src = p.dS_final ? p.dS_final + unit * DD + (size_t)i * D + c0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            G[c] = v4.x;
+            G[c + 1] = v4.y;
+            G[c + 2] = v4.z;
+            G[c + 3] = v4.w;
+        }
+    }
+    for (int j = nch - 1; j >= 0; --j) {
+        const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
+        stage(j, true);
+        __syncthreads();
+        // recompute the chunk's states (the one before each token goes to the scratch)
+        {
+            float S[32];
+            const float *ck = p.ckpt + (slot_of(j) * H + h) * DD + (size_t)i * D + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(ck + c);
+                S[c] = v4.x;
+                S[c + 1] = v4.y;
+                S[c + 2] = v4.z;
+                S[c + 3] = v4.w;
+            }
+            for (int tt = 0; tt < lc; ++tt) {
+                float *dst = scr + (size_t)tt * DD + (size_t)i * D + c0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                fwd_step(S, tb, tt);
+            }
+        }
+        // backward steps, last token first
+        for (int tt = lc - 1; tt >= 0; --tt) {
+            const size_t th = (size_t)(tb + tt) * H + h;
+            const float graw = p.g[th * D + i];
+            const float e = __expf(fmaxf(graw, g_min));
+            const float ki = ld_in<BF16>(p.k, th * D + i), qi = ld_in<BF16>(p.q, th * D + i);
+            const float b = p.beta[th];
+            float Sp[32];
+            {
+                const float *src = scr + (size_t)tt * DD + (size_t)i * D + c0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(src + c);
+                    Sp[c] = v4.x;
+                    Sp[c + 1] = v4.y;
+                    Sp[c + 2] = v4.z;
+                    Sp[c + 3] = v4.w;
+                }
+            }
+            // G += scale q do^T; dq partial = scale S' do over this group's columns
+            float dqp = 0.f, gk[32];
+            const float sq = scale * qi;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float d = sDo[tt * D + c0 + c], u = sU[tt * D + c0 + c];
+                const float st = fmaf(ki, u, e * Sp[c]);  // S' = X + k u^T
+                dqp = fmaf(st, d, dqp);
+                G[c] = fmaf(sq, d, G[c]);
+                gk[c] = G[c] * ki;
+            }
+            const float dus = transpose_sum32(gk, lane);
+            sRed[(gi * WPG + wg) * 32 + lane] = dus;
+            group_sync(1 + gi, D);
+            if (wg == 0) {
+                float du = 0.f;
+#pragma unroll
+                for (int w = 0; w < WPG; ++w) du += sRed[(gi * WPG + w) * 32 + lane];
+                sDu[c0 + lane] = du;
+                p.dv[th * D + c0 + lane] = b * du;
+                float term = du * (sV[tt * D + c0 + lane] - sP[tt * D + c0 + lane]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+                if (lane == 0) sDb[gi] = term;
+            }
+            group_sync(1 + gi, D);
+            float dkp = 0.f, dgp = 0.f;
+            const float bk = b * ki;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float du = sDu[c0 + c], u = sU[tt * D + c0 + c];
+                const float x = e * Sp[c];
+                dkp = fmaf(G[c], u, dkp);
+                dkp = fmaf(-b * x, du, dkp);
+                const float dx = fmaf(-bk, du, G[c]);
+                dgp = fmaf(dx, x, dgp);
+                G[c] = e * dx;
+            }
+            sRow[(0 * NG + gi) * D + i] = scale * dqp;
+            sRow[(1 * NG + gi) * D + i] = dkp;
+            sRow[(2 * NG + gi) * D + i] = dgp;
+            __syncthreads();
+            if (gi == 0) {
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    a0 += sRow[(0 * NG + gg) * D + i];
+                    a1 += sRow[(1 * NG + gg) * D + i];
+                    a2 += sRow[(2 * NG + gg) * D + i];
+                }
+                p.dq[th * D + i] = a0;
+                p.dk[th * D + i] = a1;
+                p.dg[th * D + i] = (graw < g_min) ? 0.f : a2;
+            }
+            if (tid == 0) {
+                float s = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) s += sDb[gg];
+                p.dbeta[th] = s;
+            }
+            __syncthreads();
+        }
+    }
+    if (p.dS0) {
+        float *dst = p.dS0 + unit * DD + (size_t)i * D + c0;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
+    }
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
+    using L = BwdSmem<D>;
+    auto kern = kda_chunk_bwd_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.N, a.H);
+    kern<<<grid, D * D / 32, L::bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace bw
+
+cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st) {
+    if (a.N <= 0) return cudaSuccess;
+    if (d == 128) return bf16 ? bw::launch_t<128, true>(a, st) : bw::launch_t<128, false>(a, st);
+    if (d == 64) return bf16 ? bw::launch_t<64, true>(a, st) : bw::launch_t<64, false>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

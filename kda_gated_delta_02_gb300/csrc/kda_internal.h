@@ -77,6 +77,21 @@ struct ComposeArgs {
 };
 cudaError_t launch_compose(const ComposeArgs &a, cudaStream_t st);
 
+// Backward of the prefill (chunk_bwd.cu), dk = dv = d in {64, 128}.
+struct BwdArgs {
+    const void *q, *k, *v, *dout;  // [T][H][d], bf16 or f32
+    const float *g, *beta;         // [T][H][d], [T][H]
+    const int32_t *cu_seqlens;     // [N+1]
+    const float *S0, *dS_final;    // [N][H][d][d] or null (zero)
+    float *dq, *dk, *dv, *dg, *dbeta, *dS0;  // dS0 may be null
+    float *ckpt;                   // [floor(T/64) + N slots][H][d][d] chunk-start states
+    float *scratch;                // [N][H][64][d][d] states of the chunk being differentiated
+    int N, T, H;
+    float scale, g_min;
+    uint32_t *status;
+};
+cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st);
+
 struct VerifyArgs {
     void *state, *tail;
     const float *conv_w;

@@ -144,3 +144,15 @@ def test_kernel_timing_without_launches(lib):
     assert lib.kda_kernel_timing_stop(launches, total, n) == 0
     assert list(launches) == [0] * n and list(total) == [0.0] * n
     assert lib.kda_kernel_timing_stop(None, None, 2) != 0  # outputs required
+
+
+def test_backward_workspace_arithmetic(lib):
+    """Chunk checkpoints (floor(T/64) + N slots) and 64 states per (sequence,
+    head), d x d fp32 each; 0 for unsupported shapes."""
+    lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+    N, T, H, d = 3, 1000, 4, 128
+    dd = d * d * 4
+    want = _align256((T // 64 + N) * H * dd) + _align256(N * H * 64 * dd)
+    assert lib.kda_chunk_bwd_workspace_size(N, T, H, d, d) == want
+    assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 64) == 0
+    assert lib.kda_chunk_bwd_workspace_size(0, T, H, d, d) == 0
