@@ -5,6 +5,7 @@ One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
 kda_chunk_fwd launch per step.  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
   "verify_ragged": the same with 3..7 drafts per request (ragged entry point)
+  "backward": the backward of the headline prefill (dq, dk, dv, dg, dbeta)
   "ckpt":   the headline prefill also emitting the state every 4096 tokens
   "decode": the same entry point as single-token decode (window 0) on 256 x 96
   "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
@@ -276,7 +277,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of prefill,verify,decode,varlen,cp (default: all)")
+    ap.add_argument("--only", default="", help="comma list of prefill,verify,decode,varlen,cp,backward (default: all)")
     ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "decode", "cp"],
                     help="launch only this kernel family (warmup + steps launches, no JSON) for ncu")
     ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp")
@@ -301,7 +302,7 @@ def main(argv=None):
     from kda_gated_delta_02_gb300 import synth
     kda.load_library()
     peaks = load_peaks()
-    only = set(args.only.split(",")) if args.only else {"prefill", "verify", "decode", "varlen", "cp"}
+    only = set(args.only.split(",")) if args.only else {"prefill", "verify", "decode", "varlen", "cp", "backward"}
     K, Wm = max(1, args.steps), max(3, args.warmup)
     stream = torch.cuda.current_stream()
     out = {}
@@ -425,6 +426,39 @@ def main(argv=None):
                          "requests_per_s": ws * vw.R / (vms * 1e-3)}
         launches += sum(v["launches"] for v in kv.values())
         del d, st, tl, ov
+        torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ backward (training), same workload
+    if "backward" in only:
+        inp = synth.make_prefill(w, device="cuda")
+        dout = torch.randn(inp["v"].shape, dtype=torch.float32, device="cuda").to(inp["v"].dtype)
+        bws = torch.empty(kda.load_library().kda_chunk_bwd_workspace_size(1, T, H, w.dk, w.dv), dtype=torch.uint8,
+                          device="cuda")
+
+        def bwd_step():
+            kda.chunk_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], dout,
+                          workspace=bws)
+
+        bwd_step()
+        Kb = max(2, K // 10)
+        bms, kb = timed_launches(kda, bwd_step, Kb, stream)
+        bms = reduce_max(bms, ws)
+        # per token-head: fp32 flops of two forward passes (pass 1 and the recompute:
+        # 3 d^2 FMA each) and the backward step (8 d^2 FMA); bytes of the recomputed
+        # state written and read back (2 x d^2 x 4) plus the inputs and gradients
+        d2 = w.dk * w.dv
+        flops = T * H * 2.0 * (2 * 3 * d2 + 8 * d2)
+        io = T * H * (4 * 128 * 2 + 128 * 4 + 4 + 3 * 128 * 4 + 128 * 4 + 4)  # q,k,v,do bf16 + g,beta in; dq,dk,dv,dg,dbeta out
+        scratch = T * H * 2.0 * d2 * 4
+        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 flop x max SM clock, TFLOP/s
+        out["backward"] = {"workload": w.name + " backward (dq, dk, dv, dg, dbeta)", "ms": bms,
+                           "tok_s": ws * T / (bms * 1e-3), "fp32_tflops": flops / (bms * 1e-3) / 1e12,
+                           "fp32_peak_tflops": fp32_peak, "frac_alu": flops / (bms * 1e-3) / 1e12 / fp32_peak,
+                           "bytes_gbs": (io + scratch) / (bms * 1e-3) / 1e9,
+                           "frac_hbm": (io + scratch) / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "ratio_to_forward": bms / ms}
+        launches += sum(v["launches"] for v in kb.values())
+        del inp, dout, bws
         torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ ragged verify (drafts 3..7 per request)
