@@ -250,6 +250,14 @@ def run_profile(args):
     import kda_gated_delta_02_gb300 as kda
     from kda_gated_delta_02_gb300 import synth
     n = max(1, args.warmup) + max(1, args.steps)
+    if args.profile == "backward":
+        inp = synth.make_prefill(synth.PREFILL_32K, device="cuda", T_override=args.T or None)
+        dout = torch.randn(inp["v"].shape, dtype=torch.float32, device="cuda").to(inp["v"].dtype)
+        for _ in range(n):
+            kda.chunk_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], dout)
+        torch.cuda.synchronize()
+        print(f"profile {args.profile}: {n} launches ok")
+        return 0
     if args.profile in ("prefill", "cp"):
         w = synth.PREFILL_32K if args.profile == "prefill" else synth.ULTRA_LONG
         inp = synth.make_prefill(w, device="cuda", T_override=args.T or None)
@@ -278,9 +286,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of prefill,verify,decode,varlen,cp,backward (default: all)")
-    ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "decode", "cp"],
+    ap.add_argument("--profile", default="", choices=["", "prefill", "verify", "decode", "cp", "backward"],
                     help="launch only this kernel family (warmup + steps launches, no JSON) for ncu")
-    ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp")
+    ap.add_argument("--T", type=int, default=0, help="token count override for --profile prefill/cp/backward")
     ap.add_argument("--R", type=int, default=0, help="request count override for --profile verify/decode")
     args = ap.parse_args(argv)
     if args.impl == "reference":

@@ -21,8 +21,9 @@
 // Pass 1 walks the sequence forward and keeps the state at every chunk start
 // (64 tokens) in a slot-indexed buffer (chunk j of sequence n is slot
 // floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
-// chunk's states from its checkpoint into a per-CTA scratch (u and p per token
-// into shared memory) and runs the backward steps over them.
+// chunk's states from its checkpoint into a per-CTA scratch (and v - p per
+// token in shared memory) and runs the backward steps over them.  Each chunk's
+// rows of q, k, v, g, b and do are staged in shared memory first.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -65,11 +66,15 @@ template <int D>
 struct BwdSmem {
     static constexpr int NG = D / 32;
     static constexpr int WPG = D / 32;  // warps per group
-    static constexpr size_t off_v = 0;                                  // f32 [CH][D] staged v
-    static constexpr size_t off_do = off_v + (size_t)CH * D * 4;         // f32 [CH][D] staged do
-    static constexpr size_t off_u = off_do + (size_t)CH * D * 4;         // f32 [CH][D] u per token
-    static constexpr size_t off_p = off_u + (size_t)CH * D * 4;          // f32 [CH][D] p per token
-    static constexpr size_t off_red = off_p + (size_t)CH * D * 4;        // f32 [NG][WPG][32]
+    // the chunk's rows, staged once per chunk: v (overwritten by w = v - p as
+    // each token's p is formed; u = b w), do, q, k, g (raw) and b
+    static constexpr size_t off_v = 0;                                   // f32 [CH][D]
+    static constexpr size_t off_do = off_v + (size_t)CH * D * 4;         // f32 [CH][D]
+    static constexpr size_t off_q = off_do + (size_t)CH * D * 4;         // f32 [CH][D]
+    static constexpr size_t off_k = off_q + (size_t)CH * D * 4;          // f32 [CH][D]
+    static constexpr size_t off_g = off_k + (size_t)CH * D * 4;          // f32 [CH][D]
+    static constexpr size_t off_b = off_g + (size_t)CH * D * 4;          // f32 [CH]
+    static constexpr size_t off_red = off_b + (size_t)CH * 4;            // f32 [NG][WPG][32]
     static constexpr size_t off_du = off_red + (size_t)NG * WPG * 32 * 4;  // f32 [D]
     static constexpr size_t off_row = off_du + (size_t)D * 4;            // f32 [3][NG][D]
     static constexpr size_t off_db = off_row + (size_t)3 * NG * D * 4;   // f32 [NG]
@@ -83,8 +88,10 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
     extern __shared__ __align__(16) unsigned char smem[];
     float *sV = reinterpret_cast<float *>(smem + L::off_v);
     float *sDo = reinterpret_cast<float *>(smem + L::off_do);
-    float *sU = reinterpret_cast<float *>(smem + L::off_u);
-    float *sP = reinterpret_cast<float *>(smem + L::off_p);
+    float *sQ = reinterpret_cast<float *>(smem + L::off_q);
+    float *sK = reinterpret_cast<float *>(smem + L::off_k);
+    float *sG = reinterpret_cast<float *>(smem + L::off_g);
+    float *sB = reinterpret_cast<float *>(smem + L::off_b);
     float *sRed = reinterpret_cast<float *>(smem + L::off_red);
     float *sDu = reinterpret_cast<float *>(smem + L::off_du);
     float *sRow = reinterpret_cast<float *>(smem + L::off_row);
@@ -105,22 +112,28 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
     const float g_min = p.g_min, scale = p.scale;
     float *scr = p.scratch + unit * (size_t)CH * DD;  // [CH][D][D]: state before each token of the chunk
 
-    // the staged rows of chunk j (tokens t0 + 64 j ..): v, and do in the backward pass
-    auto stage = [&](int j, bool with_do) {
+    // the rows of chunk j (tokens t0 + 64 j ..) into shared memory; q and do
+    // only for the backward pass
+    auto stage = [&](int j, bool bwd) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
         for (int idx = tid; idx < lc * D; idx += NG * D) {
             const int tt = idx / D, c = idx % D;
             const size_t th = ((size_t)(tb + tt) * H + h) * D + c;
             sV[tt * D + c] = ld_in<BF16>(p.v, th);
-            if (with_do) sDo[tt * D + c] = ld_in<BF16>(p.dout, th);
+            sK[tt * D + c] = ld_in<BF16>(p.k, th);
+            sG[tt * D + c] = p.g[th];
+            if (bwd) {
+                sDo[tt * D + c] = ld_in<BF16>(p.dout, th);
+                sQ[tt * D + c] = ld_in<BF16>(p.q, th);
+            }
         }
+        for (int tt = tid; tt < lc; tt += NG * D) sB[tt] = p.beta[(size_t)(tb + tt) * H + h];
     };
-    // one forward step of token tb + tt on this thread's slab S (row i, columns
-    // c0 ..); keeps p and u of the token in shared memory
-    auto fwd_step = [&](float (&S)[32], int tb, int tt) {
-        const size_t th = (size_t)(tb + tt) * H + h;
-        const float e = __expf(fmaxf(p.g[th * D + i], g_min));
-        const float ki = ld_in<BF16>(p.k, th * D + i);
+    // one forward step of token tt of the staged chunk on this thread's slab S
+    // (row i, columns c0 ..); the token's v row becomes w = v - p (u = b w)
+    auto fwd_step = [&](float (&S)[32], int tt) {
+        const float e = __expf(fmaxf(sG[tt * D + i], g_min));
+        const float ki = sK[tt * D + i], b = sB[tt];
         float pv[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) pv[c] = (e * S[c]) * ki;
@@ -131,18 +144,16 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
             float pj = 0.f;
 #pragma unroll
             for (int w = 0; w < WPG; ++w) pj += sRed[(gi * WPG + w) * 32 + lane];
-            const float b = p.beta[th];
-            sP[tt * D + c0 + lane] = pj;
-            sU[tt * D + c0 + lane] = b * (sV[tt * D + c0 + lane] - pj);
+            sV[tt * D + c0 + lane] -= pj;
         }
         group_sync(1 + gi, D);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-            const float4 u4 = *reinterpret_cast<const float4 *>(sU + tt * D + c0 + c);
-            S[c + 0] = fmaf(ki, u4.x, e * S[c + 0]);
-            S[c + 1] = fmaf(ki, u4.y, e * S[c + 1]);
-            S[c + 2] = fmaf(ki, u4.z, e * S[c + 2]);
-            S[c + 3] = fmaf(ki, u4.w, e * S[c + 3]);
+            const float4 w4 = *reinterpret_cast<const float4 *>(sV + tt * D + c0 + c);
+            S[c + 0] = fmaf(ki, b * w4.x, e * S[c + 0]);
+            S[c + 1] = fmaf(ki, b * w4.y, e * S[c + 1]);
+            S[c + 2] = fmaf(ki, b * w4.z, e * S[c + 2]);
+            S[c + 3] = fmaf(ki, b * w4.w, e * S[c + 3]);
         }
     };
     auto slot_of = [&](int j) { return (size_t)(t0 / CH + n + j); };
@@ -167,8 +178,7 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
             if (j == nch - 1) break;  // the last chunk's states are recomputed in pass 2
             stage(j, false);
             __syncthreads();
-            const int tb = t0 + CH * j;
-            for (int tt = 0; tt < CH; ++tt) fwd_step(S, tb, tt);
+            for (int tt = 0; tt < CH; ++tt) fwd_step(S, tt);
             __syncthreads();
         }
     }
@@ -207,16 +217,22 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)
                     *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
-                fwd_step(S, tb, tt);
+                fwd_step(S, tt);
             }
         }
-        // backward steps, last token first
+        // backward steps, last token first; the state of the token four steps
+        // on is brought into L2 while this one runs
+        constexpr int PF = 4;
+        for (int tt = lc - 1; tt >= lc - PF && tt >= 0; --tt)
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)tt * DD + (size_t)i * D + c0));
         for (int tt = lc - 1; tt >= 0; --tt) {
             const size_t th = (size_t)(tb + tt) * H + h;
-            const float graw = p.g[th * D + i];
+            if (tt >= PF)
+                asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)(tt - PF) * DD + (size_t)i * D + c0));
+            const float graw = sG[tt * D + i];
             const float e = __expf(fmaxf(graw, g_min));
-            const float ki = ld_in<BF16>(p.k, th * D + i), qi = ld_in<BF16>(p.q, th * D + i);
-            const float b = p.beta[th];
+            const float ki = sK[tt * D + i], qi = sQ[tt * D + i];
+            const float b = sB[tt];
             float Sp[32];
             {
                 const float *src = scr + (size_t)tt * DD + (size_t)i * D + c0;
@@ -232,13 +248,20 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
             // G += scale q do^T; dq partial = scale S' do over this group's columns
             float dqp = 0.f, gk[32];
             const float sq = scale * qi;
+            const float *dorow = sDo + tt * D + c0, *wrow = sV + tt * D + c0;  // 16-byte aligned
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float d = sDo[tt * D + c0 + c], u = sU[tt * D + c0 + c];
-                const float st = fmaf(ki, u, e * Sp[c]);  // S' = X + k u^T
-                dqp = fmaf(st, d, dqp);
-                G[c] = fmaf(sq, d, G[c]);
-                gk[c] = G[c] * ki;
+            for (int c4 = 0; c4 < 32; c4 += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(dorow + c4);
+                const float4 w4 = *reinterpret_cast<const float4 *>(wrow + c4);
+                const float dd[4] = {d4.x, d4.y, d4.z, d4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int c = c4 + m;
+                    const float st = fmaf(ki, b * ww[m], e * Sp[c]);  // S' = X + k u^T
+                    dqp = fmaf(st, dd[m], dqp);
+                    G[c] = fmaf(sq, dd[m], G[c]);
+                    gk[c] = G[c] * ki;
+                }
             }
             const float dus = transpose_sum32(gk, lane);
             sRed[(gi * WPG + wg) * 32 + lane] = dus;
@@ -249,7 +272,7 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
                 for (int w = 0; w < WPG; ++w) du += sRed[(gi * WPG + w) * 32 + lane];
                 sDu[c0 + lane] = du;
                 p.dv[th * D + c0 + lane] = b * du;
-                float term = du * (sV[tt * D + c0 + lane] - sP[tt * D + c0 + lane]);
+                float term = du * sV[tt * D + c0 + lane];  // du (v - p)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
                 if (lane == 0) sDb[gi] = term;
@@ -258,14 +281,21 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
             float dkp = 0.f, dgp = 0.f;
             const float bk = b * ki;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float du = sDu[c0 + c], u = sU[tt * D + c0 + c];
-                const float x = e * Sp[c];
-                dkp = fmaf(G[c], u, dkp);
-                dkp = fmaf(-b * x, du, dkp);
-                const float dx = fmaf(-bk, du, G[c]);
-                dgp = fmaf(dx, x, dgp);
-                G[c] = e * dx;
+            for (int c4 = 0; c4 < 32; c4 += 4) {
+                const float4 du4 = *reinterpret_cast<const float4 *>(sDu + c0 + c4);
+                const float4 w4 = *reinterpret_cast<const float4 *>(wrow + c4);
+                const float dus4[4] = {du4.x, du4.y, du4.z, du4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int c = c4 + m;
+                    const float du = dus4[m], u = b * ww[m];
+                    const float x = e * Sp[c];
+                    dkp = fmaf(G[c], u, dkp);
+                    dkp = fmaf(-b * x, du, dkp);
+                    const float dx = fmaf(-bk, du, G[c]);
+                    dgp = fmaf(dx, x, dgp);
+                    G[c] = e * dx;
+                }
             }
             sRow[(0 * NG + gi) * D + i] = scale * dqp;
             sRow[(1 * NG + gi) * D + i] = dkp;
