@@ -178,6 +178,32 @@ size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, in
 int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len);
 
 /*
+ * kda_chunk_fwd (cp off) on host buffers, with the transfers overlapped with
+ * the kernels: q, k, v, g, beta, cu_seqlens, initial_state, final_state and o
+ * are HOST pointers (page-locked for the copies to run asynchronously) with
+ * kda_chunk_fwd's layouts; workspace is device memory of at least
+ * kda_chunk_fwd_host_workspace_size(...) bytes (device copies of inputs and
+ * outputs and the two-kernel area).  With bf16 inputs and dk = dv = 128 the
+ * chunk slots run in `pieces` equal pieces (0: 4): while piece p's chunk-local
+ * kernel and walk run on `stream`, piece p+1's input rows are copied in and
+ * piece p-1's output rows copied out, on two internal streams of the library
+ * ordered by events; other shapes copy in, run kda_chunk_fwd and copy out on
+ * `stream`.  When `stream` completes, o and final_state hold the results.
+ * cu_seqlens must satisfy cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] =
+ * T (checked on the host: KDA_ERR_INVALID_ARG).  A workspace smaller than the
+ * size returns KDA_ERR_WORKSPACE.  Results are those of kda_chunk_fwd with
+ * the same pieces (bit for bit).  The pages have no counterpart: this is an
+ * interface for callers whose inputs live in host memory.
+ */
+int kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const int32_t *cu_seqlens, int N, int T, int H,
+                       int dk, int dv, const float *initial_state, float *final_state, void *o,
+                       float scale, float g_min, int in_dtype, int pieces, void *workspace,
+                       size_t workspace_bytes, uint32_t *status, void *stream);
+size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, int in_dtype,
+                                         int pieces);
+
+/*
  * Backward of kda_chunk_fwd (training; "Noyaux KDA et FlashKDA", section
  * "FlashKDA : le noyau par blocs" names it as the chunk kernel's other use):
  * the gradients of a loss L with respect to every input, given dL/do and

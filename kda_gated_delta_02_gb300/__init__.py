@@ -19,7 +19,7 @@ __all__ = ["chunk_fwd", "chunk_fwd_workspace_size", "chunk_fwd_prep_workspace_si
            "segment_compose", "decode_verify_replay", "KDAError", "load_library", "library_path",
            "CP_OFF", "CP_ON", "CP_AUTO", "CONV_NONE", "CONV_SILU", "STATUS_BAD_SEQLENS",
            "STATUS_BAD_ACCEPTED_LEN", "STATUS_SEGMENT_OVERFLOW", "STATUS_TIMEOUT", "STATUS_BAD_DRAFT_LEN",
-           "KERNEL_FAMILIES", "chunk_bwd", "kernel_timing_start",
+           "KERNEL_FAMILIES", "chunk_bwd", "chunk_fwd_host", "kernel_timing_start",
            "kernel_timing_stop"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +71,10 @@ def load_library():
         lib.kda_segment_transition.argtypes = [P, P, P, P, I, I, I, I, I, P, P, F, I, P]
         lib.kda_segment_compose.restype = I
         lib.kda_segment_compose.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.kda_chunk_fwd_host.restype = I
+        lib.kda_chunk_fwd_host.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, I, P, S, P, P]
+        lib.kda_chunk_fwd_host_workspace_size.restype = S
+        lib.kda_chunk_fwd_host_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.kda_chunk_bwd.restype = I
         lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, F, F, I, P, S, P, P]
         lib.kda_chunk_bwd_workspace_size.restype = S
@@ -100,6 +104,17 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise KDAError("KDA calls take CUDA tensors")
+    if not t.is_contiguous():
+        raise KDAError("KDA calls take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(t):
+    """Host pointer of a contiguous CPU tensor (for the host-buffer entry point)."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise KDAError("kda_chunk_fwd_host takes CPU (host) tensors")
     if not t.is_contiguous():
         raise KDAError("KDA calls take contiguous tensors")
     return ctypes.c_void_p(t.data_ptr())
@@ -202,6 +217,34 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
 KERNEL_FAMILIES = ("kda_chunk_list_kernel", "kda_chunk_prep_kernel", "kda_chunk_walk_kernel",
                    "kda_chunk_tc_kernel", "kda_chunk_kernel", "kda_compose_kernel", "kda_segment_table_kernel",
                    "kda_decode_verify_replay", "kda_chunk_bwd_kernel")
+
+
+def chunk_fwd_host(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,
+                   g_min=-5.0, pieces=4, out=None, final_state=None, workspace=None, status=None, stream=None):
+    """chunk_fwd (cp off) on CPU tensors (pin them for asynchronous copies):
+    the library copies the inputs in and the outputs out by pieces, overlapped
+    with the kernels.  cu_seqlens is a CPU int32 tensor.  Returns CPU tensors
+    (o, final_state); they are complete once `stream` (default: the current
+    one) has completed."""
+    lib = load_library()
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+    dt = _in_dtype(q)
+    need = int(lib.kda_chunk_fwd_host_workspace_size(N, T, H, dk, dv, dt, int(pieces)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    cu = cu_seqlens.to(torch.int32).contiguous()
+    rc = lib.kda_chunk_fwd_host(_hptr(q), _hptr(k), _hptr(v), _hptr(g), _hptr(beta), _hptr(cu), N, T, H, dk, dv,
+                                _hptr(initial_state), _hptr(final_state), _hptr(out), float(scale), float(g_min), dt,
+                                int(pieces), _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                _ptr(status), _stream(stream))
+    _check(rc, "kda_chunk_fwd_host")
+    return out, final_state
 
 
 def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=None, scale=1.0, g_min=-5.0,

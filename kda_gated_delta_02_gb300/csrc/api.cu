@@ -230,6 +230,64 @@ cudaError_t run_chunk(const kda::ChunkArgs &a, int units, bool bf, cudaStream_t 
 
 }  // namespace
 
+namespace {
+// ---------------------------------------------------------------- host-buffer prefill
+// Device workspace of kda_chunk_fwd_host: device copies of the inputs and
+// outputs, then the two-kernel area for one piece of slots.
+struct HostLayout {
+    size_t off_q = 0, off_k = 0, off_v = 0, off_g = 0, off_b = 0, off_cu = 0, off_s0 = 0, off_o = 0, off_sf = 0;
+    size_t off_area = 0, total = 0;
+    bool pipelined = false;
+    SplitLayout S;
+};
+
+HostLayout host_layout(int N, int T, int H, int dk, int dv, int in_dtype, int pieces) {
+    HostLayout L;
+    const size_t es = in_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    size_t o = 0;
+    L.off_q = o; o = align256(o + (size_t)T * H * dk * es);
+    L.off_k = o; o = align256(o + (size_t)T * H * dk * es);
+    L.off_v = o; o = align256(o + (size_t)T * H * dv * es);
+    L.off_g = o; o = align256(o + (size_t)T * H * dk * 4);
+    L.off_b = o; o = align256(o + (size_t)T * H * 4);
+    L.off_cu = o; o = align256(o + (size_t)(N + 1) * 4);
+    L.off_s0 = o; o = align256(o + (size_t)N * H * dk * dv * 4);
+    L.off_o = o; o = align256(o + (size_t)T * H * dv * es);
+    L.off_sf = o; o = align256(o + (size_t)N * H * dk * dv * 4);
+    L.off_area = o;
+    L.pipelined = in_dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && T > 0 && split_enabled();
+    if (L.pipelined) {
+        const int nslots = T / kChunk + N;
+        const int pc = pieces < 1 ? 1 : (pieces > nslots ? nslots : pieces);
+        const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
+        L.S = split_layout(N, T, H, (size_t)((nslots + pc - 1) / pc) * per_slot);
+        o += L.S.total;
+    }
+    L.total = align256(o);
+    return L;
+}
+
+// Per-stream state of the host-buffer prefill: two copy streams per device.
+struct CopyStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+std::mutex g_copy_mu;
+CopyStreams g_copy[64];
+
+int copy_streams(CopyStreams *cs) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_copy_mu);
+    if (!g_copy[dev].in) {
+        if (cudaStreamCreateWithFlags(&g_copy[dev].in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&g_copy[dev].out, cudaStreamNonBlocking) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    *cs = g_copy[dev];
+    return KDA_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char *kda_status_string(int status) {
@@ -494,6 +552,146 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,
                                     [&] { return kda::launch_chunk_bwd(a, dk, in_dtype == KDA_DTYPE_BF16, st); }));
+}
+
+size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, int in_dtype, int pieces) {
+    if (N < 1 || T < 0 || H < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return 0;
+    return host_layout(N, T, H, dk, dv, in_dtype, pieces).total;
+}
+
+int kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const float *initial_state,
+                       float *final_state, void *o, float scale, float g_min, int in_dtype, int pieces,
+                       void *workspace, size_t workspace_bytes, uint32_t *status, void *stream) {
+    if (N < 1 || T < 0 || H < 1 || !cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (in_dtype != KDA_DTYPE_BF16 && in_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return KDA_ERR_INVALID_ARG;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
+    if (pieces < 1) pieces = 4;
+    const HostLayout L = host_layout(N, T, H, dk, dv, in_dtype, pieces);
+    if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t es = in_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const size_t rq = (size_t)H * dk * es, rv = (size_t)H * dv * es, rg = (size_t)H * dk * 4, rb = (size_t)H * 4;
+    const size_t sbytes = (size_t)N * H * dk * dv * 4;
+    void *dq = ws + L.off_q, *dk_ = ws + L.off_k, *dv_ = ws + L.off_v, *dout = ws + L.off_o;
+    float *dg = reinterpret_cast<float *>(ws + L.off_g), *db = reinterpret_cast<float *>(ws + L.off_b);
+    int32_t *dcu = reinterpret_cast<int32_t *>(ws + L.off_cu);
+    float *ds0 = initial_state ? reinterpret_cast<float *>(ws + L.off_s0) : nullptr;
+    float *dsf = final_state ? reinterpret_cast<float *>(ws + L.off_sf) : nullptr;
+    auto rows_in = [&](cudaStream_t s, int lo, int hi) -> cudaError_t {
+        if (hi <= lo) return cudaSuccess;
+        const size_t n = (size_t)(hi - lo);
+        cudaError_t e = cudaMemcpyAsync(static_cast<unsigned char *>(dq) + lo * rq,
+                                        static_cast<const unsigned char *>(q) + lo * rq, n * rq,
+                                        cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<unsigned char *>(dk_) + lo * rq,
+                                static_cast<const unsigned char *>(k) + lo * rq, n * rq, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<unsigned char *>(dv_) + lo * rv,
+                                static_cast<const unsigned char *>(v) + lo * rv, n * rv, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<unsigned char *>(dg) + lo * rg,
+                                reinterpret_cast<const unsigned char *>(g) + lo * rg, n * rg, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<unsigned char *>(db) + lo * rb,
+                                reinterpret_cast<const unsigned char *>(beta) + lo * rb, n * rb,
+                                cudaMemcpyHostToDevice, s);
+        return e;
+    };
+    auto rows_out = [&](cudaStream_t s, int lo, int hi) -> cudaError_t {
+        if (hi <= lo) return cudaSuccess;
+        return cudaMemcpyAsync(static_cast<unsigned char *>(o) + lo * rv,
+                               static_cast<const unsigned char *>(dout) + lo * rv, (size_t)(hi - lo) * rv,
+                               cudaMemcpyDeviceToHost, s);
+    };
+
+    cudaError_t e = cudaSuccess;
+    if (!L.pipelined) {  // copy in, the device call, copy out (all on the caller's stream)
+        e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(N + 1) * 4, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && ds0) e = cudaMemcpyAsync(ds0, initial_state, sbytes, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = rows_in(st, 0, T);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        const int rc = chunk_fwd_impl(dq, dk_, dv_, dg, db, dcu, N, T, H, dk, dv, ds0, dsf, dout, scale, g_min,
+                                      in_dtype, KDA_CP_OFF, 0, ws + L.off_area, L.total - L.off_area, 0, 0, nullptr,
+                                      status, stream);
+        if (rc != KDA_OK) return rc;
+        e = rows_out(st, 0, T);
+        if (e == cudaSuccess && dsf) e = cudaMemcpyAsync(final_state, dsf, sbytes, cudaMemcpyDeviceToHost, st);
+        return cuda_status(e);
+    }
+
+    // pieces of slots and the token range each covers (chunks of unit u are
+    // slots floor(t0/64) + u + j, in token order)
+    const SplitLayout &S = L.S;
+    const int P = (S.nslots + S.piece - 1) / S.piece;
+    std::vector<int> lo(P, T), hi(P, 0);
+    for (int u = 0; u < N; ++u) {
+        const int t0 = cu_seqlens[u], t1 = cu_seqlens[u + 1], base = t0 / kChunk + u;
+        for (int c = t0; c < t1; c += kChunk) {
+            const int pc = (base + (c - t0) / kChunk) / S.piece;
+            lo[pc] = lo[pc] < c ? lo[pc] : c;
+            const int ce = c + kChunk < t1 ? c + kChunk : t1;
+            hi[pc] = hi[pc] > ce ? hi[pc] : ce;
+        }
+    }
+    CopyStreams cs;
+    int rc = copy_streams(&cs);
+    if (rc != KDA_OK) return rc;
+    std::vector<cudaEvent_t> ev(2 * P + 2, nullptr);
+    for (auto &x : ev)
+        if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) {
+            for (auto &y : ev)
+                if (y) cudaEventDestroy(y);
+            return KDA_ERR_CUDA;
+        }
+    cudaEvent_t ev_start = ev[2 * P], ev_done = ev[2 * P + 1];
+    kda::ChunkArgs a = {};
+    a.q = dq; a.k = dk_; a.v = dv_; a.g = dg; a.beta = db; a.o = dout;
+    a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.scale = scale; a.g_min = g_min;
+    a.status = status; a.mode = kda::MODE_SEQ; a.cu_seqlens = dcu; a.S_init = ds0; a.S_final = dsf;
+    unsigned char *area = ws + L.off_area;
+    int2 *list = reinterpret_cast<int2 *>(area + S.off_list);
+    float *carry = reinterpret_cast<float *>(area + S.off_carry);
+    unsigned char *blob = area + S.off_blob;
+    // the copy streams start after earlier work on the caller's stream
+    e = cudaEventRecord(ev_start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_start, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(N + 1) * 4, cudaMemcpyHostToDevice, cs.in);
+    if (e == cudaSuccess && ds0) e = cudaMemcpyAsync(ds0, initial_state, sbytes, cudaMemcpyHostToDevice, cs.in);
+    for (int pc = 0; e == cudaSuccess && pc < P; ++pc) {
+        e = rows_in(cs.in, lo[pc], hi[pc]);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[pc], cs.in);
+    }
+    for (int pc = 0; e == cudaSuccess && pc < P; ++pc) {
+        const int s0 = pc * S.piece, s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
+        e = cudaStreamWaitEvent(st, ev[pc], 0);
+        if (e == cudaSuccess && pc == 0)
+            e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(a, N, S.nslots, list, st); });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st,
+                             [&] { return kda::launch_chunk_prep(a, list, s0, s1, blob, true, st); });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+                return kda::launch_chunk_walk(a, N, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
+                                              carry + (size_t)((pc + 1) & 1) * S.carry_stride, st);
+            });
+        if (e == cudaSuccess) e = cudaEventRecord(ev[P + pc], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev[P + pc], 0);
+        if (e == cudaSuccess) e = rows_out(cs.out, lo[pc], hi[pc]);
+    }
+    if (e == cudaSuccess && dsf) e = cudaMemcpyAsync(final_state, dsf, sbytes, cudaMemcpyDeviceToHost, cs.out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_done, cs.out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_done, 0);
+    for (auto &x : ev) cudaEventDestroy(x);  // released once the work they mark completes
+    return cuda_status(e);
 }
 
 int kda_kernel_timing_start(void) {
