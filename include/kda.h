@@ -222,8 +222,10 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *  dq, dk, dv device f32 [T][H][d]; dg device f32 [T][H][dk] (w.r.t. the raw
  *             g); dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
  *  workspace  device scratch of at least kda_chunk_bwd_workspace_size(...)
- *             bytes ((floor(T/64) + N) x H chunk checkpoints and N x H x 64
- *             states, d x d f32 each); KDA_ERR_WORKSPACE when smaller.
+ *             bytes ((floor(T/64) + N) x H chunk checkpoints and
+ *             min(N x H, 160) x 64 states, d x d f32 each: the kernel runs at
+ *             most 160 persistent CTAs, one scratch slot each);
+ *             KDA_ERR_WORKSPACE when smaller.
  * Invalid cu_seqlens set KDA_STATUS_BAD_SEQLENS; that sequence is skipped.
  */
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,

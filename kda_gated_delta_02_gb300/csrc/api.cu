@@ -521,7 +521,8 @@ int kda_decode_verify_replay_ragged(void *state, void *conv_tail, const float *c
 size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
     if (N < 1 || T < 0 || H < 1 || dk != dv || !dim_ok(dk)) return 0;
     const size_t DD = (size_t)dk * dv * 4;
-    return align256((size_t)(T / kChunk + N) * H * DD) + align256((size_t)N * H * kChunk * DD);
+    const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
+    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD);
 }
 
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,

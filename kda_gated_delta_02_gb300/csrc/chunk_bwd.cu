@@ -18,6 +18,8 @@
 // (p, du) go through a 32-lane transpose-sum and the group's warps; sums over
 // value columns (dq, dk, dg, db) are per-thread partials added across the
 // groups in shared memory, in a fixed order.
+// The CTAs are persistent (at most kBwdMaxCtas, one scratch slot each) and
+// stride over the (sequence, head) units.
 // Pass 1 walks the sequence forward and keeps the state at every chunk start
 // (64 tokens) in a slot-indexed buffer (chunk j of sequence n is slot
 // floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
@@ -100,17 +102,21 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
     const int tid = threadIdx.x, lane = tid & 31;
     const int gi = tid / D, i = tid % D, wg = i >> 5;  // group, key row, warp in the group
     const int c0 = 32 * gi;                            // first value column of the group
-    const int n = blockIdx.x, h = blockIdx.y, H = p.H;
+    const int H = p.H, nunits = p.N * H;
+    const size_t DD = (size_t)D * D;
+    const float g_min = p.g_min, scale = p.scale;
+    // this CTA's scratch slot: [CH][D][D], the state before each token of the chunk
+    float *scr = p.scratch + (size_t)blockIdx.x * CH * DD;
+    // persistent: units (sequence, head) strided over the CTAs
+    for (int un = blockIdx.x; un < nunits; un += gridDim.x) {
+    const int n = un / H, h = un % H;
     const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
     if (t0 < 0 || t1 < t0 || t1 > p.T) {
-        if (tid == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
-        return;
+        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
+        continue;
     }
     const int Ln = t1 - t0, nch = (Ln + CH - 1) / CH;
-    const size_t DD = (size_t)D * D;
-    const size_t unit = (size_t)n * H + h;
-    const float g_min = p.g_min, scale = p.scale;
-    float *scr = p.scratch + unit * (size_t)CH * DD;  // [CH][D][D]: state before each token of the chunk
+    const size_t unit = (size_t)un;
 
     // the rows of chunk j (tokens t0 + 64 j ..) into shared memory; q and do
     // only for the backward pass
@@ -327,6 +333,8 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
     }
+    __syncthreads();  // the next unit stages into the same shared memory
+    }  // units
 }
 
 template <int D, bool BF16>
@@ -335,7 +343,8 @@ static cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
     auto kern = kda_chunk_bwd_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.N, a.H);
+    const long units = (long)a.N * a.H;
+    const int grid = (int)(units < kBwdMaxCtas ? units : kBwdMaxCtas);
     kern<<<grid, D * D / 32, L::bytes, st>>>(a);
     return cudaGetLastError();
 }

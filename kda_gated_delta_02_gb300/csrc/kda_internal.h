@@ -85,11 +85,13 @@ struct BwdArgs {
     const float *S0, *dS_final;    // [N][H][d][d] or null (zero)
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;  // dS0 may be null
     float *ckpt;                   // [floor(T/64) + N slots][H][d][d] chunk-start states
-    float *scratch;                // [N][H][64][d][d] states of the chunk being differentiated
+    float *scratch;                // [min(N H, kBwdMaxCtas)][64][d][d] states of the chunk being differentiated
     int N, T, H;
     float scale, g_min;
     uint32_t *status;
 };
+// the backward runs at most this many persistent CTAs (one per SM; one scratch slot each)
+constexpr int kBwdMaxCtas = 160;
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st);
 
 struct VerifyArgs {

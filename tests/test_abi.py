@@ -154,5 +154,9 @@ def test_backward_workspace_arithmetic(lib):
     dd = d * d * 4
     want = _align256((T // 64 + N) * H * dd) + _align256(N * H * 64 * dd)
     assert lib.kda_chunk_bwd_workspace_size(N, T, H, d, d) == want
+    # many units: the scratch stops growing at 160 slots (persistent CTAs)
+    N2, H2 = 100, 96
+    want2 = _align256((T // 64 + N2) * H2 * dd) + _align256(160 * 64 * dd)
+    assert lib.kda_chunk_bwd_workspace_size(N2, T, H2, d, d) == want2
     assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 64) == 0
     assert lib.kda_chunk_bwd_workspace_size(0, T, H, d, d) == 0

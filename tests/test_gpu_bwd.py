@@ -107,3 +107,12 @@ def test_backward_bad_seqlens_and_workspace(kda):
                                128, 128, None, P(x["do"]), None, *[P(o) for o in outs], None, 1.0, -5.0, 0,
                                P(small), ctypes.c_size_t(1024), None, None)
         kda._check(rc, "kda_chunk_bwd")
+
+
+def test_backward_more_units_than_ctas(kda, oracle):
+    """30 sequences x 8 heads = 240 (sequence, head) units over at most 160
+    persistent CTAs: units share a CTA's scratch in turn."""
+    rng = np.random.default_rng(13)
+    lens = rng.integers(0, 140, size=30).tolist()
+    x = _case(lens, 8, 64, torch.bfloat16, seed=13)
+    _compare(kda, oracle, x, scale=1.0)
