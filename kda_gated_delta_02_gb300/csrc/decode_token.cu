@@ -27,7 +27,7 @@ namespace dtk {
 constexpr int NT = 256, NW = NT / 32;
 
 template <int D>
-__global__ void __launch_bounds__(NT, 4) kda_decode_token_kernel(VerifyArgs p) {
+__global__ void __launch_bounds__(NT, 5) kda_decode_token_kernel(VerifyArgs p) {
     constexpr int CG = D / 8;     // column groups of 8 bf16 (16 bytes)
     constexpr int RG = NT / CG;   // row groups
     constexpr int RPT = D / RG;   // rows per thread
