@@ -2,7 +2,8 @@
 
 One JSON line (rank 0).  Headline `value`: chunkwise-prefill tokens/s on the
 32K-token, 96-head, d=128 bf16 workload, inputs resident in HBM, one
-kda_chunk_fwd launch per step.  Extra keys measured in the same run:
+kda_chunk_fwd call per step (its two-kernel form: chunk slot list, chunk-local
+kernel, state walk).  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
   "verify_ragged": the same with 3..7 drafts per request (ragged entry point)
   "backward": the backward of the headline prefill (dq, dk, dv, dg, dbeta)
@@ -10,7 +11,9 @@ kda_chunk_fwd launch per step.  Extra keys measured in the same run:
   "decode": the same entry point as single-token decode (window 0) on 256 x 96
   "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
   "cp":     1M-token, 12-head prefill with the context-parallel schedule
-  "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches".
+  "roofline" (the step's dominant kernel), "path_roofline", "kernels",
+  "cpu_baseline", "e2e" (host buffers through kda_chunk_fwd_host), "clocks",
+  "gpu_launches".
 
 --impl reference times the fp64 CPU oracle (the reference arm of this
 repository) on a bounded sample of the same workload.
