@@ -213,8 +213,13 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *     G += scale q do^T;  dq = scale S' do;  du = G^T k;  dv = beta du;
  *     dbeta = du . (v - p);  dk = G u - beta X du;  dX = G - beta k du^T;
  *     dg_i = sum_j dX_ij X_ij, 0 where g_i < g_min;  G <- D dX;  dS0 = G at the start.
- * Computed in fp32 on the CUDA cores, one CTA per (sequence, head); states are
- * recomputed from chunk-start checkpoints (64 tokens) kept in the workspace.
+ * Computed in fp32 on the CUDA cores; each (sequence, head) is walked by a
+ * cluster of d/32 CTAs, one per 32 value columns of the state (the columns
+ * evolve independently), whose per-column partial sums of dq, dk, dg and
+ * dbeta are added in a fixed order (results do not depend on scheduling;
+ * KDA_BWD_SPLIT=0 in the environment selects one CTA per (sequence, head),
+ * same bits).  States are recomputed from chunk-start checkpoints (64
+ * tokens) kept in the workspace.
  *  q, k, v, g, beta, cu_seqlens, N, T, H, initial_state, scale, g_min,
  *  in_dtype   as kda_chunk_fwd (dk = dv = 64 or 128; cp off).
  *  dout       device [T][H][dv], in_dtype: dL/do.
@@ -222,9 +227,11 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *  dq, dk, dv device f32 [T][H][d]; dg device f32 [T][H][dk] (w.r.t. the raw
  *             g); dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
  *  workspace  device scratch of at least kda_chunk_bwd_workspace_size(...)
- *             bytes ((floor(T/64) + N) x H chunk checkpoints and
- *             min(N x H, 160) x 64 states, d x d f32 each: the kernel runs at
- *             most 160 persistent CTAs, one scratch slot each);
+ *             bytes: (floor(T/64) + N) x H chunk checkpoints and
+ *             min(N x H, 160) x 64 states, d x d f32 each (at most 160
+ *             (sequence, head) units are in flight, one scratch slot each),
+ *             then min(N x H, 160) x d/32 x 2 buffers of 64 x (3d + 1) f32
+ *             column partials, each part 256-byte aligned;
  *             KDA_ERR_WORKSPACE when smaller.
  * Invalid cu_seqlens set KDA_STATUS_BAD_SEQLENS; that sequence is skipped.
  */

@@ -522,7 +522,8 @@ size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
     if (N < 1 || T < 0 || H < 1 || dk != dv || !dim_ok(dk)) return 0;
     const size_t DD = (size_t)dk * dv * 4;
     const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
-    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD);
+    const size_t parts = slots * (size_t)(dk / 32) * 2 * kda::chunk_bwd_partial_floats(dk) * 4;
+    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD) + align256(parts);
 }
 
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -548,7 +549,10 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     a.S0 = initial_state; a.dS_final = dS_final;
     a.dq = dq; a.dk = dk_; a.dv = dv_; a.dg = dg; a.dbeta = dbeta; a.dS0 = dS0;
     a.ckpt = reinterpret_cast<float *>(ws);
-    a.scratch = reinterpret_cast<float *>(ws + align256((size_t)(T / kChunk + N) * H * DD));
+    const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
+    const size_t off_scr = align256((size_t)(T / kChunk + N) * H * DD);
+    a.scratch = reinterpret_cast<float *>(ws + off_scr);
+    a.partials = reinterpret_cast<float *>(ws + off_scr + align256(slots * kChunk * DD));
     a.N = N; a.T = T; a.H = H; a.scale = scale; a.g_min = g_min; a.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,

@@ -12,23 +12,41 @@
 //   db = du . (v - p);  dk = G u - b X du;  dX = G - b k du^T;
 //   dg_i = sum_j dX_ij X_ij (zero where g_i < g_min);  G <- D dX.
 // The value columns of the state evolve independently (k, g, b are shared by
-// all of them), so a CTA of D/32 groups of D threads walks one (sequence,
-// head): group c owns value columns 32c .. 32c + 31 and its thread i owns key
-// row i of them (32 fp32 of S and 32 of G in registers).  Sums over key rows
-// (p, du) go through a 32-lane transpose-sum and the group's warps; sums over
-// value columns (dq, dk, dg, db) are per-thread partials added across the
-// groups in shared memory, in a fixed order.
-// The CTAs are persistent (at most kBwdMaxCtas, one scratch slot each) and
-// stride over the (sequence, head) units.
+// all of them).  A group of D threads owns 32 value columns: its thread i
+// owns key row i of them (32 fp32 of S and 32 of G in registers, worked as 16
+// pairs by the packed f32x2 instructions).  Sums over key rows (p, du) go
+// through a 32-lane transpose-sum and the group's warps; sums over value
+// columns (dq, dk, dg, db) are per-thread partials added across the groups in
+// group order.
+//
+// Two forms with the same arithmetic in the same order (so the same bits):
+//  * whole (SPLIT = false): a CTA of D/32 groups walks one (sequence, head);
+//    the column sums meet in shared memory token by token;
+//  * split (SPLIT = true): a cluster of D/32 one-group CTAs walks one
+//    (sequence, head), so a unit spreads over D/32 SMs.  Every CTA writes its
+//    column partials of a chunk to a buffer of its own in global memory, a
+//    cluster barrier closes the chunk, and each CTA then adds the partials of
+//    all groups for a share of the chunk's tokens.  Two buffers per CTA
+//    alternate by chunk, so one barrier per chunk suffices: a CTA starts
+//    writing the buffer of chunk c + 2 only after every CTA of the cluster
+//    has arrived at the barrier of chunk c + 1, i.e. finished reading chunk c.
+// CTAs (clusters) are persistent, at most kBwdMaxCtas units at a time (one
+// scratch slot each), and stride over the (sequence, head) units.
 // Pass 1 walks the sequence forward and keeps the state at every chunk start
 // (64 tokens) in a slot-indexed buffer (chunk j of sequence n is slot
 // floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
 // chunk's states from its checkpoint into a per-CTA scratch (and v - p per
-// token in shared memory) and runs the backward steps over them.  Each chunk's
-// rows of q, k, v, g, b and do are staged in shared memory first.
+// token in shared memory) and runs the backward steps over them.  Each
+// chunk's rows of k, g, b and the CTA's value columns of v and do are staged
+// in shared memory first; q is read from global memory one token ahead.
+// The state blocks that go through global memory (chunk-start states and the
+// recomputed per-token states) are stored thread-major: the float4 of value
+// columns c .. c + 3 of every thread lie side by side, so each float4 access
+// of a warp covers 512 contiguous bytes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -39,59 +57,135 @@ namespace bw {
 constexpr int CH = 64;
 
 template <bool BF16>
+struct InType;
+template <>
+struct InType<true> {
+    using T = __nv_bfloat16;
+};
+template <>
+struct InType<false> {
+    using T = float;
+};
+
+template <bool BF16>
 __device__ __forceinline__ float ld_in(const void *p, size_t idx) {
     if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[idx]);
     else return reinterpret_cast<const float *>(p)[idx];
 }
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+// four consecutive elements of shared memory as two pairs
+__device__ __forceinline__ void ld4(const float *p, float2 &a, float2 &b) {
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    a = make_float2(v.x, v.y);
+    b = make_float2(v.z, v.w);
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16 *p, float2 &a, float2 &b) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    a = unpack_bf16(v.x);
+    b = unpack_bf16(v.y);
+}
+__device__ __forceinline__ float2 bc2(float a) { return make_float2(a, a); }
 
 // v[j] summed over the 32 lanes of the warp; lane l returns the sum of column
-// l (five exchange rounds of halves; v is destroyed)
+// l (five exchange rounds of halves, the adds of a round paired; v is
+// destroyed)
 __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
+    for (int w = 16; w >= 2; w >>= 1) {
         const bool hi = (lane & w) != 0;
 #pragma unroll
-        for (int c = 0; c < w; ++c) {
-            const float send = hi ? v[c] : v[c + w];
-            const float keep = hi ? v[c + w] : v[c];
-            v[c] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        for (int c = 0; c < w; c += 2) {
+            const float s0 = hi ? v[c] : v[c + w], s1 = hi ? v[c + 1] : v[c + 1 + w];
+            const float k0 = hi ? v[c + w] : v[c], k1 = hi ? v[c + 1 + w] : v[c + 1];
+            const float r0 = __shfl_xor_sync(0xffffffffu, s0, w), r1 = __shfl_xor_sync(0xffffffffu, s1, w);
+            const float2 sum = __fadd2_rn(make_float2(k0, k1), make_float2(r0, r1));
+            v[c] = sum.x;
+            v[c + 1] = sum.y;
         }
     }
-    return v[0];
+    const bool hi = (lane & 1) != 0;
+    const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
 __device__ __forceinline__ void group_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// all threads of all CTAs of the cluster; global writes before it are visible
+// to the reads after it in every CTA of the cluster
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// the float4 of columns c .. c + 3 (c a multiple of 4) of thread tid's slab in
+// a thread-major state block of nt threads
+__device__ __forceinline__ float4 *slab4(float *blk, int tid, int c, int nt) {
+    return reinterpret_cast<float4 *>(blk) + (size_t)(c >> 2) * nt + tid;
+}
+__device__ __forceinline__ const float4 *slab4(const float *blk, int tid, int c, int nt) {
+    return reinterpret_cast<const float4 *>(blk) + (size_t)(c >> 2) * nt + tid;
+}
+__device__ __forceinline__ void ld_slab(float2 (&S)[16], const float *blk, int tid, int nt) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 v4 = *slab4(blk, tid, c, nt);
+        S[c / 2] = make_float2(v4.x, v4.y);
+        S[c / 2 + 1] = make_float2(v4.z, v4.w);
+    }
+}
+__device__ __forceinline__ void st_slab(float *blk, const float2 (&S)[16], int tid, int nt) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4)
+        *slab4(blk, tid, c, nt) = make_float4(S[c / 2].x, S[c / 2].y, S[c / 2 + 1].x, S[c / 2 + 1].y);
+}
+// 32 consecutive floats of a row of a user [d][d] block (zero when absent)
+__device__ __forceinline__ void ld_row32(float2 (&S)[16], const float *src) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[c / 2] = make_float2(v4.x, v4.y);
+        S[c / 2 + 1] = make_float2(v4.z, v4.w);
+    }
+}
+
+// column partials of one chunk of one CTA: [CH][3][D] (scale dq, dk, dg), then [CH] (db)
 template <int D>
+__host__ __device__ constexpr size_t part_floats() {
+    return (size_t)CH * (3 * D + 1);
+}
+
+template <int D, bool BF16, bool SPLIT>
 struct BwdSmem {
-    static constexpr int NG = D / 32;
-    static constexpr int WPG = D / 32;  // warps per group
-    // the chunk's rows, staged once per chunk: v (overwritten by w = v - p as
-    // each token's p is formed; u = b w), do, q, k, g (raw) and b
-    static constexpr size_t off_v = 0;                                   // f32 [CH][D]
-    static constexpr size_t off_do = off_v + (size_t)CH * D * 4;         // f32 [CH][D]
-    static constexpr size_t off_q = off_do + (size_t)CH * D * 4;         // f32 [CH][D]
-    static constexpr size_t off_k = off_q + (size_t)CH * D * 4;          // f32 [CH][D]
-    static constexpr size_t off_g = off_k + (size_t)CH * D * 4;          // f32 [CH][D]
-    static constexpr size_t off_b = off_g + (size_t)CH * D * 4;          // f32 [CH]
-    static constexpr size_t off_red = off_b + (size_t)CH * 4;            // f32 [NG][WPG][32]
-    static constexpr size_t off_du = off_red + (size_t)NG * WPG * 32 * 4;  // f32 [D]
-    static constexpr size_t off_row = off_du + (size_t)D * 4;            // f32 [3][NG][D]
-    static constexpr size_t off_db = off_row + (size_t)3 * NG * D * 4;   // f32 [NG]
+    using TI = typename InType<BF16>::T;
+    static constexpr int NG = SPLIT ? 1 : D / 32;  // groups of the CTA
+    static constexpr int VW = 32 * NG;             // value columns of the CTA
+    static constexpr int WPG = D / 32;             // warps per group
+    static constexpr size_t off_v = 0;                                         // f32 [CH][VW]: v, then w = v - p
+    static constexpr size_t off_do = off_v + (size_t)CH * VW * 4;              // TI [CH][VW]
+    static constexpr size_t off_k = off_do + (size_t)CH * VW * sizeof(TI);    // TI [CH][D]
+    static constexpr size_t off_g = off_k + (size_t)CH * D * sizeof(TI);      // f32 [CH][D] (raw g)
+    static constexpr size_t off_b = off_g + (size_t)CH * D * 4;                // f32 [CH]
+    static constexpr size_t off_red = off_b + (size_t)CH * 4;                  // f32 [NG][WPG][32]
+    static constexpr size_t off_du = off_red + (size_t)NG * WPG * 32 * 4;      // f32 [VW]
+    static constexpr size_t off_row = off_du + (size_t)VW * 4;                 // f32 [3][NG][D] (whole form)
+    static constexpr size_t off_db = off_row + (SPLIT ? 0 : (size_t)3 * NG * D * 4);  // f32 [NG]
     static constexpr size_t bytes = off_db + 64;
 };
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdArgs p) {
-    using L = BwdSmem<D>;
-    constexpr int NG = L::NG, WPG = L::WPG;
+template <int D, bool BF16, bool SPLIT>
+__global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chunk_bwd_kernel(const BwdArgs p) {
+    using L = BwdSmem<D, BF16, SPLIT>;
+    using TI = typename L::TI;
+    constexpr int NG = L::NG, VW = L::VW, WPG = L::WPG;
+    constexpr int NC = SPLIT ? D / 32 : 1;  // CTAs per unit (the cluster)
+    constexpr int NT = NG * D;              // threads of the CTA
     extern __shared__ __align__(16) unsigned char smem[];
     float *sV = reinterpret_cast<float *>(smem + L::off_v);
-    float *sDo = reinterpret_cast<float *>(smem + L::off_do);
-    float *sQ = reinterpret_cast<float *>(smem + L::off_q);
-    float *sK = reinterpret_cast<float *>(smem + L::off_k);
+    TI *sDo = reinterpret_cast<TI *>(smem + L::off_do);
+    TI *sK = reinterpret_cast<TI *>(smem + L::off_k);
     float *sG = reinterpret_cast<float *>(smem + L::off_g);
     float *sB = reinterpret_cast<float *>(smem + L::off_b);
     float *sRed = reinterpret_cast<float *>(smem + L::off_red);
@@ -100,49 +194,62 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
     float *sDb = reinterpret_cast<float *>(smem + L::off_db);
 
     const int tid = threadIdx.x, lane = tid & 31;
-    const int gi = tid / D, i = tid % D, wg = i >> 5;  // group, key row, warp in the group
-    const int c0 = 32 * gi;                            // first value column of the group
+    const int gi = tid / D, i = tid % D, wg = i >> 5;     // group in the CTA, key row, warp in the group
+    const int rank = SPLIT ? (int)(blockIdx.x % NC) : 0;  // CTA in its cluster (NC consecutive CTAs)
+    const int cl = blockIdx.x / NC, ncl = gridDim.x / NC;
+    const int cbase = 32 * rank;     // first value column of the CTA
+    const int vc = 32 * gi;          // first value column of the thread's group, within the CTA's
+    const int c0 = cbase + vc;       // ... and within the state
     const int H = p.H, nunits = p.N * H;
-    const size_t DD = (size_t)D * D;
+    const size_t DD = (size_t)D * D, BLK = (size_t)32 * NT;  // a unit's state; the CTA's share of it
     const float g_min = p.g_min, scale = p.scale;
-    // this CTA's scratch slot: [CH][D][D], the state before each token of the chunk
-    float *scr = p.scratch + (size_t)blockIdx.x * CH * DD;
-    // persistent: units (sequence, head) strided over the CTAs
-    for (int un = blockIdx.x; un < nunits; un += gridDim.x) {
+    // the CTA's scratch slot: [CH][BLK], its columns of the state before each token of the chunk
+    float *scr = p.scratch + (size_t)blockIdx.x * CH * BLK;
+    // column partials (split form): two buffers per CTA; CTA s of this cluster owns slot cl * NC + s
+    auto part = [&](int s, int buf) { return p.partials + ((size_t)(cl * NC + s) * 2 + buf) * part_floats<D>(); };
+    int pbuf = 0;
+
+    for (int un = cl; un < nunits; un += ncl) {
     const int n = un / H, h = un % H;
     const int t0 = p.cu_seqlens[n], t1 = p.cu_seqlens[n + 1];
-    if (t0 < 0 || t1 < t0 || t1 > p.T) {
-        if (tid == 0 && h == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
+    if (t0 < 0 || t1 < t0 || t1 > p.T) {  // taken by every CTA of the cluster alike
+        if (tid == 0 && h == 0 && rank == 0) report_status(p.status, KDA_STATUS_BAD_SEQLENS);
         continue;
     }
     const int Ln = t1 - t0, nch = (Ln + CH - 1) / CH;
     const size_t unit = (size_t)un;
 
-    // the rows of chunk j (tokens t0 + 64 j ..) into shared memory; q and do
-    // only for the backward pass
+    // the rows of chunk j (tokens t0 + 64 j ..) into shared memory; do only
+    // for the backward pass
     auto stage = [&](int j, bool bwd) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
-        for (int idx = tid; idx < lc * D; idx += NG * D) {
+        for (int idx = tid; idx < lc * D; idx += NT) {
             const int tt = idx / D, c = idx % D;
             const size_t th = ((size_t)(tb + tt) * H + h) * D + c;
-            sV[tt * D + c] = ld_in<BF16>(p.v, th);
-            sK[tt * D + c] = ld_in<BF16>(p.k, th);
+            sK[tt * D + c] = reinterpret_cast<const TI *>(p.k)[th];
             sG[tt * D + c] = p.g[th];
-            if (bwd) {
-                sDo[tt * D + c] = ld_in<BF16>(p.dout, th);
-                sQ[tt * D + c] = ld_in<BF16>(p.q, th);
-            }
         }
-        for (int tt = tid; tt < lc; tt += NG * D) sB[tt] = p.beta[(size_t)(tb + tt) * H + h];
+        for (int idx = tid; idx < lc * VW; idx += NT) {
+            const int tt = idx / VW, c = idx % VW;
+            const size_t th = ((size_t)(tb + tt) * H + h) * D + cbase + c;
+            sV[tt * VW + c] = ld_in<BF16>(p.v, th);
+            if (bwd) sDo[tt * VW + c] = reinterpret_cast<const TI *>(p.dout)[th];
+        }
+        for (int tt = tid; tt < lc; tt += NT) sB[tt] = p.beta[(size_t)(tb + tt) * H + h];
     };
     // one forward step of token tt of the staged chunk on this thread's slab S
     // (row i, columns c0 ..); the token's v row becomes w = v - p (u = b w)
-    auto fwd_step = [&](float (&S)[32], int tt) {
+    auto fwd_step = [&](float2 (&S)[16], int tt) {
         const float e = __expf(fmaxf(sG[tt * D + i], g_min));
-        const float ki = sK[tt * D + i], b = sB[tt];
+        const float ki = to_f(sK[tt * D + i]), b = sB[tt];
+        const float2 e2 = bc2(e), k2 = bc2(ki), b2 = bc2(b);
         float pv[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = (e * S[c]) * ki;
+        for (int c = 0; c < 16; ++c) {
+            const float2 x = __fmul2_rn(__fmul2_rn(e2, S[c]), k2);
+            pv[2 * c] = x.x;
+            pv[2 * c + 1] = x.y;
+        }
         const float ps = transpose_sum32(pv, lane);
         sRed[(gi * WPG + wg) * 32 + lane] = ps;
         group_sync(1 + gi, D);
@@ -150,37 +257,27 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
             float pj = 0.f;
 #pragma unroll
             for (int w = 0; w < WPG; ++w) pj += sRed[(gi * WPG + w) * 32 + lane];
-            sV[tt * D + c0 + lane] -= pj;
+            sV[tt * VW + vc + lane] -= pj;
         }
         group_sync(1 + gi, D);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-            const float4 w4 = *reinterpret_cast<const float4 *>(sV + tt * D + c0 + c);
-            S[c + 0] = fmaf(ki, b * w4.x, e * S[c + 0]);
-            S[c + 1] = fmaf(ki, b * w4.y, e * S[c + 1]);
-            S[c + 2] = fmaf(ki, b * w4.z, e * S[c + 2]);
-            S[c + 3] = fmaf(ki, b * w4.w, e * S[c + 3]);
+            float2 wa, wb;
+            ld4(sV + tt * VW + vc + c, wa, wb);
+            S[c / 2] = __ffma2_rn(k2, __fmul2_rn(b2, wa), __fmul2_rn(e2, S[c / 2]));
+            S[c / 2 + 1] = __ffma2_rn(k2, __fmul2_rn(b2, wb), __fmul2_rn(e2, S[c / 2 + 1]));
         }
     };
     auto slot_of = [&](int j) { return (size_t)(t0 / CH + n + j); };
+    // the CTA's share of the unit's checkpoint block of chunk j
+    auto ckpt_blk = [&](int j) { return p.ckpt + (slot_of(j) * H + h) * DD + (size_t)rank * BLK; };
 
     // ---------------------------------------------------------------- pass 1: chunk-start states
     {
-        float S[32];
-        const float *src = p.S0 ? p.S0 + unit * DD + (size_t)i * D + c0 : nullptr;
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-            const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[c] = v4.x;
-            S[c + 1] = v4.y;
-            S[c + 2] = v4.z;
-            S[c + 3] = v4.w;
-        }
+        float2 S[16];
+        ld_row32(S, p.S0 ? p.S0 + unit * DD + (size_t)i * D + c0 : nullptr);
         for (int j = 0; j < nch; ++j) {
-            float *ck = p.ckpt + (slot_of(j) * H + h) * DD + (size_t)i * D + c0;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-                *reinterpret_cast<float4 *>(ck + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+            st_slab(ckpt_blk(j), S, tid, NT);
             if (j == nch - 1) break;  // the last chunk's states are recomputed in pass 2
             stage(j, false);
             __syncthreads();
@@ -190,83 +287,62 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
     }
 
     // ---------------------------------------------------------------- pass 2: chunks in reverse
-    float G[32];
-    {
-        const float *src = p.dS_final ? p.dS_final + unit * DD + (size_t)i * D + c0 : nullptr;
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-            const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            G[c] = v4.x;
-            G[c + 1] = v4.y;
-            G[c + 2] = v4.z;
-            G[c + 3] = v4.w;
-        }
-    }
+    float2 G[16];
+    ld_row32(G, p.dS_final ? p.dS_final + unit * DD + (size_t)i * D + c0 : nullptr);
     for (int j = nch - 1; j >= 0; --j) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
         stage(j, true);
         __syncthreads();
         // recompute the chunk's states (the one before each token goes to the scratch)
         {
-            float S[32];
-            const float *ck = p.ckpt + (slot_of(j) * H + h) * DD + (size_t)i * D + c0;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(ck + c);
-                S[c] = v4.x;
-                S[c + 1] = v4.y;
-                S[c + 2] = v4.z;
-                S[c + 3] = v4.w;
-            }
+            float2 S[16];
+            ld_slab(S, ckpt_blk(j), tid, NT);
             for (int tt = 0; tt < lc; ++tt) {
-                float *dst = scr + (size_t)tt * DD + (size_t)i * D + c0;
-#pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+                st_slab(scr + (size_t)tt * BLK, S, tid, NT);
                 fwd_step(S, tt);
             }
         }
         // backward steps, last token first; the state of the token four steps
-        // on is brought into L2 while this one runs
+        // on is brought into L2 while this one runs (one 128-byte line of the
+        // block per thread), and q one token ahead into a register
         constexpr int PF = 4;
         for (int tt = lc - 1; tt >= lc - PF && tt >= 0; --tt)
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)tt * DD + (size_t)i * D + c0));
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)tt * BLK + (size_t)tid * 32));
+        float q_next = ld_in<BF16>(p.q, ((size_t)(tb + lc - 1) * H + h) * D + i);
+        float *pw = SPLIT ? part(rank, pbuf) : nullptr;
         for (int tt = lc - 1; tt >= 0; --tt) {
             const size_t th = (size_t)(tb + tt) * H + h;
             if (tt >= PF)
-                asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)(tt - PF) * DD + (size_t)i * D + c0));
+                asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)(tt - PF) * BLK + (size_t)tid * 32));
+            const float qi = q_next;
+            if (tt > 0) q_next = ld_in<BF16>(p.q, (th - H) * D + i);
             const float graw = sG[tt * D + i];
             const float e = __expf(fmaxf(graw, g_min));
-            const float ki = sK[tt * D + i], qi = sQ[tt * D + i];
+            const float ki = to_f(sK[tt * D + i]);
             const float b = sB[tt];
-            float Sp[32];
-            {
-                const float *src = scr + (size_t)tt * DD + (size_t)i * D + c0;
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4 *>(src + c);
-                    Sp[c] = v4.x;
-                    Sp[c + 1] = v4.y;
-                    Sp[c + 2] = v4.z;
-                    Sp[c + 3] = v4.w;
-                }
-            }
+            const float2 e2 = bc2(e), k2 = bc2(ki), b2 = bc2(b);
+            float2 Sp[16];
+            ld_slab(Sp, scr + (size_t)tt * BLK, tid, NT);
             // G += scale q do^T; dq partial = scale S' do over this group's columns
-            float dqp = 0.f, gk[32];
-            const float sq = scale * qi;
-            const float *dorow = sDo + tt * D + c0, *wrow = sV + tt * D + c0;  // 16-byte aligned
+            float2 dq2 = make_float2(0.f, 0.f);
+            float gk[32];
+            const float2 sq2 = bc2(scale * qi);
+            const TI *dorow = sDo + tt * VW + vc;
+            const float *wrow = sV + tt * VW + vc;  // 16-byte aligned
 #pragma unroll
-            for (int c4 = 0; c4 < 32; c4 += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(dorow + c4);
-                const float4 w4 = *reinterpret_cast<const float4 *>(wrow + c4);
-                const float dd[4] = {d4.x, d4.y, d4.z, d4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
+            for (int c = 0; c < 32; c += 4) {
+                float2 d2[2], w2[2];
+                ld4(dorow + c, d2[0], d2[1]);
+                ld4(wrow + c, w2[0], w2[1]);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int c = c4 + m;
-                    const float st = fmaf(ki, b * ww[m], e * Sp[c]);  // S' = X + k u^T
-                    dqp = fmaf(st, dd[m], dqp);
-                    G[c] = fmaf(sq, dd[m], G[c]);
-                    gk[c] = G[c] * ki;
+                for (int m = 0; m < 2; ++m) {
+                    const int cc = c / 2 + m;
+                    const float2 st = __ffma2_rn(k2, __fmul2_rn(b2, w2[m]), __fmul2_rn(e2, Sp[cc]));  // S' = X + k u^T
+                    dq2 = __ffma2_rn(st, d2[m], dq2);
+                    G[cc] = __ffma2_rn(sq2, d2[m], G[cc]);
+                    const float2 x = __fmul2_rn(G[cc], k2);
+                    gk[2 * cc] = x.x;
+                    gk[2 * cc + 1] = x.y;
                 }
             }
             const float dus = transpose_sum32(gk, lane);
@@ -276,85 +352,151 @@ __global__ void __launch_bounds__(D * D / 32, 1) kda_chunk_bwd_kernel(const BwdA
                 float du = 0.f;
 #pragma unroll
                 for (int w = 0; w < WPG; ++w) du += sRed[(gi * WPG + w) * 32 + lane];
-                sDu[c0 + lane] = du;
+                sDu[vc + lane] = du;
                 p.dv[th * D + c0 + lane] = b * du;
-                float term = du * sV[tt * D + c0 + lane];  // du (v - p)
+                float term = du * sV[tt * VW + vc + lane];  // du (v - p)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-                if (lane == 0) sDb[gi] = term;
-            }
-            group_sync(1 + gi, D);
-            float dkp = 0.f, dgp = 0.f;
-            const float bk = b * ki;
-#pragma unroll
-            for (int c4 = 0; c4 < 32; c4 += 4) {
-                const float4 du4 = *reinterpret_cast<const float4 *>(sDu + c0 + c4);
-                const float4 w4 = *reinterpret_cast<const float4 *>(wrow + c4);
-                const float dus4[4] = {du4.x, du4.y, du4.z, du4.w}, ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int c = c4 + m;
-                    const float du = dus4[m], u = b * ww[m];
-                    const float x = e * Sp[c];
-                    dkp = fmaf(G[c], u, dkp);
-                    dkp = fmaf(-b * x, du, dkp);
-                    const float dx = fmaf(-bk, du, G[c]);
-                    dgp = fmaf(dx, x, dgp);
-                    G[c] = e * dx;
+                if (lane == 0) {
+                    if constexpr (SPLIT) pw[(size_t)CH * 3 * D + tt] = term;
+                    else sDb[gi] = term;
                 }
             }
-            sRow[(0 * NG + gi) * D + i] = scale * dqp;
-            sRow[(1 * NG + gi) * D + i] = dkp;
-            sRow[(2 * NG + gi) * D + i] = dgp;
-            __syncthreads();
-            if (gi == 0) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+            group_sync(1 + gi, D);
+            float2 dk2 = make_float2(0.f, 0.f), dg2 = make_float2(0.f, 0.f);
+            const float2 nb2 = bc2(-b), nbk2 = bc2(-(b * ki));
 #pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    a0 += sRow[(0 * NG + gg) * D + i];
-                    a1 += sRow[(1 * NG + gg) * D + i];
-                    a2 += sRow[(2 * NG + gg) * D + i];
+            for (int c = 0; c < 32; c += 4) {
+                float2 du2[2], w2[2];
+                ld4(sDu + vc + c, du2[0], du2[1]);
+                ld4(wrow + c, w2[0], w2[1]);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int cc = c / 2 + m;
+                    const float2 u = __fmul2_rn(b2, w2[m]);
+                    const float2 x = __fmul2_rn(e2, Sp[cc]);
+                    dk2 = __ffma2_rn(G[cc], u, dk2);
+                    dk2 = __ffma2_rn(__fmul2_rn(nb2, x), du2[m], dk2);
+                    const float2 dx = __ffma2_rn(nbk2, du2[m], G[cc]);
+                    dg2 = __ffma2_rn(dx, x, dg2);
+                    G[cc] = __fmul2_rn(e2, dx);
+                }
+            }
+            const float dqp = scale * (dq2.x + dq2.y), dkp = dk2.x + dk2.y, dgp = dg2.x + dg2.y;
+            if constexpr (SPLIT) {
+                float *pr = pw + (size_t)tt * 3 * D;
+                pr[i] = dqp;
+                pr[D + i] = dkp;
+                pr[2 * D + i] = dgp;
+            } else {
+                sRow[(0 * NG + gi) * D + i] = dqp;
+                sRow[(1 * NG + gi) * D + i] = dkp;
+                sRow[(2 * NG + gi) * D + i] = dgp;
+                __syncthreads();
+                if (gi == 0) {
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg) {
+                        a0 += sRow[(0 * NG + gg) * D + i];
+                        a1 += sRow[(1 * NG + gg) * D + i];
+                        a2 += sRow[(2 * NG + gg) * D + i];
+                    }
+                    p.dq[th * D + i] = a0;
+                    p.dk[th * D + i] = a1;
+                    p.dg[th * D + i] = (graw < g_min) ? 0.f : a2;
+                }
+                if (tid == 0) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg) s += sDb[gg];
+                    p.dbeta[th] = s;
+                }
+                __syncthreads();
+            }
+        }
+        if constexpr (SPLIT) {
+            // the chunk's column partials of every CTA of the cluster, added in
+            // group order, for the tokens rank, rank + NC, ... of the chunk
+            cluster_sync();
+            for (int tt = rank; tt < lc; tt += NC) {
+                const size_t th = (size_t)(tb + tt) * H + h;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, sb = 0.f;
+#pragma unroll
+                for (int s = 0; s < NC; ++s) {
+                    const float *pr = part(s, pbuf);
+                    a0 += __ldcg(pr + (size_t)tt * 3 * D + i);
+                    a1 += __ldcg(pr + (size_t)tt * 3 * D + D + i);
+                    a2 += __ldcg(pr + (size_t)tt * 3 * D + 2 * D + i);
+                    if (tid == 0) sb += __ldcg(pr + (size_t)CH * 3 * D + tt);
                 }
                 p.dq[th * D + i] = a0;
                 p.dk[th * D + i] = a1;
-                p.dg[th * D + i] = (graw < g_min) ? 0.f : a2;
+                p.dg[th * D + i] = (sG[tt * D + i] < g_min) ? 0.f : a2;
+                if (tid == 0) p.dbeta[th] = sb;
             }
-            if (tid == 0) {
-                float s = 0.f;
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) s += sDb[gg];
-                p.dbeta[th] = s;
-            }
-            __syncthreads();
+            pbuf ^= 1;
+            __syncthreads();  // sG is restaged next
         }
     }
     if (p.dS0) {
         float *dst = p.dS0 + unit * DD + (size_t)i * D + c0;
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
+        for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4 *>(dst + c) = make_float4(G[c / 2].x, G[c / 2].y, G[c / 2 + 1].x, G[c / 2 + 1].y);
     }
     __syncthreads();  // the next unit stages into the same shared memory
     }  // units
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 static cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
-    using L = BwdSmem<D>;
-    auto kern = kda_chunk_bwd_kernel<D, BF16>;
+    using L = BwdSmem<D, BF16, SPLIT>;
+    auto kern = kda_chunk_bwd_kernel<D, BF16, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
     if (e != cudaSuccess) return e;
     const long units = (long)a.N * a.H;
-    const int grid = (int)(units < kBwdMaxCtas ? units : kBwdMaxCtas);
-    kern<<<grid, D * D / 32, L::bytes, st>>>(a);
-    return cudaGetLastError();
+    int nclusters = (int)(units < kBwdMaxCtas ? units : kBwdMaxCtas);  // units in flight (scratch slots)
+    constexpr int NC = SPLIT ? D / 32 : 1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(SPLIT ? D : D * D / 32);
+    cfg.dynamicSmemBytes = L::bytes;
+    cfg.stream = st;
+    cfg.gridDim = dim3(nclusters * NC);
+    if constexpr (SPLIT) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = NC;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int active = 0;
+        e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (active < 1) return cudaErrorInvalidConfiguration;
+        if (active < nclusters) nclusters = active;  // the clusters stride over the units
+        cfg.gridDim = dim3(nclusters * NC);
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace bw
 
+size_t chunk_bwd_partial_floats(int d) { return d == 128 ? bw::part_floats<128>() : bw::part_floats<64>(); }
+
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st) {
     if (a.N <= 0) return cudaSuccess;
-    if (d == 128) return bf16 ? bw::launch_t<128, true>(a, st) : bw::launch_t<128, false>(a, st);
-    if (d == 64) return bf16 ? bw::launch_t<64, true>(a, st) : bw::launch_t<64, false>(a, st);
+    // the split form unless the caller gave no partial buffers or KDA_BWD_SPLIT=0
+    const char *env = getenv("KDA_BWD_SPLIT");
+    const bool split = a.partials != nullptr && !(env && env[0] == '0');
+    if (d == 128) {
+        if (split) return bf16 ? bw::launch_t<128, true, true>(a, st) : bw::launch_t<128, false, true>(a, st);
+        return bf16 ? bw::launch_t<128, true, false>(a, st) : bw::launch_t<128, false, false>(a, st);
+    }
+    if (d == 64) {
+        if (split) return bf16 ? bw::launch_t<64, true, true>(a, st) : bw::launch_t<64, false, true>(a, st);
+        return bf16 ? bw::launch_t<64, true, false>(a, st) : bw::launch_t<64, false, false>(a, st);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -86,12 +86,17 @@ struct BwdArgs {
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;  // dS0 may be null
     float *ckpt;                   // [floor(T/64) + N slots][H][d][d] chunk-start states
     float *scratch;                // [min(N H, kBwdMaxCtas)][64][d][d] states of the chunk being differentiated
+    float *partials;               // [min(N H, kBwdMaxCtas) d/32][2][chunk_bwd_partial_floats(d)] column
+                                   // partials of the split form (null: the whole form)
     int N, T, H;
     float scale, g_min;
     uint32_t *status;
 };
-// the backward runs at most this many persistent CTAs (one per SM; one scratch slot each)
+// the backward keeps at most this many (sequence, head) units in flight (one
+// scratch slot each; a whole-form CTA or a split-form cluster per unit)
 constexpr int kBwdMaxCtas = 160;
+// floats of one chunk's column partials of one split-form CTA
+size_t chunk_bwd_partial_floats(int d);
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st);
 
 struct VerifyArgs {
