@@ -37,8 +37,12 @@
 // floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
 // chunk's states from its checkpoint into a per-CTA scratch (and v - p per
 // token in shared memory) and runs the backward steps over them.  Each
-// chunk's rows of k, g, b and the CTA's value columns of v and do are staged
-// in shared memory first; q is read from global memory one token ahead.
+// chunk's b and the CTA's value columns of v and do, and its k and g half a
+// chunk (32 tokens) at a time, are copied into shared memory by cp.async
+// batches (one memory latency per batch); q is read from global memory one
+// token ahead, and (split form) the recomputed state of the next token is
+// copied into one of two shared-memory buffers while the current token's step
+// runs.
 // The state blocks that go through global memory (chunk-start states and the
 // recomputed per-token states) are stored thread-major: the float4 of value
 // columns c .. c + 3 of every thread lie side by side, so each float4 access
@@ -55,6 +59,7 @@ namespace kda {
 namespace bw {
 
 constexpr int CH = 64;
+constexpr int HC = 32;  // tokens of k and g staged at a time
 
 template <bool BF16>
 struct InType;
@@ -120,6 +125,17 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// 16-byte global -> shared copies that complete asynchronously (L2 only), the
+// fence that closes a batch and the wait for all of this thread's batches
+__device__ __forceinline__ void cpa16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 // the float4 of columns c .. c + 3 (c a multiple of 4) of thread tid's slab in
 // a thread-major state block of nt threads
 __device__ __forceinline__ float4 *slab4(float *blk, int tid, int c, int nt) {
@@ -135,6 +151,11 @@ __device__ __forceinline__ void ld_slab(float2 (&S)[16], const float *blk, int t
         S[c / 2] = make_float2(v4.x, v4.y);
         S[c / 2 + 1] = make_float2(v4.z, v4.w);
     }
+}
+// thread tid's slab of a thread-major block, global -> shared, asynchronously
+__device__ __forceinline__ void cpa_slab(float *dst, const float *src, int tid, int nt) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) cpa16(slab4(dst, tid, c, nt), slab4(src, tid, c, nt));
 }
 __device__ __forceinline__ void st_slab(float *blk, const float2 (&S)[16], int tid, int nt) {
 #pragma unroll
@@ -163,16 +184,19 @@ struct BwdSmem {
     static constexpr int NG = SPLIT ? 1 : D / 32;  // groups of the CTA
     static constexpr int VW = 32 * NG;             // value columns of the CTA
     static constexpr int WPG = D / 32;             // warps per group
-    static constexpr size_t off_v = 0;                                         // f32 [CH][VW]: v, then w = v - p
-    static constexpr size_t off_do = off_v + (size_t)CH * VW * 4;              // TI [CH][VW]
-    static constexpr size_t off_k = off_do + (size_t)CH * VW * sizeof(TI);    // TI [CH][D]
-    static constexpr size_t off_g = off_k + (size_t)CH * D * sizeof(TI);      // f32 [CH][D] (raw g)
-    static constexpr size_t off_b = off_g + (size_t)CH * D * 4;                // f32 [CH]
+    static constexpr size_t off_v = 0;                                         // f32 [CH][VW]: w = v - p
+    static constexpr size_t off_vr = off_v + (size_t)CH * VW * 4;              // TI [CH][VW]: v
+    static constexpr size_t off_do = off_vr + (size_t)CH * VW * sizeof(TI);   // TI [CH][VW]
+    static constexpr size_t off_k = off_do + (size_t)CH * VW * sizeof(TI);    // TI [HC][D]
+    static constexpr size_t off_g = off_k + (size_t)HC * D * sizeof(TI);      // f32 [HC][D] (raw g)
+    static constexpr size_t off_b = off_g + (size_t)HC * D * 4;                // f32 [CH]
     static constexpr size_t off_red = off_b + (size_t)CH * 4;                  // f32 [NG][WPG][32]
     static constexpr size_t off_du = off_red + (size_t)NG * WPG * 32 * 4;      // f32 [VW]
     static constexpr size_t off_row = off_du + (size_t)VW * 4;                 // f32 [3][NG][D] (whole form)
     static constexpr size_t off_db = off_row + (SPLIT ? 0 : (size_t)3 * NG * D * 4);  // f32 [NG]
-    static constexpr size_t bytes = off_db + 64;
+    static constexpr size_t off_sp = off_db + 64;  // f32 [2][32 D]: next states (split form)
+    static constexpr size_t bytes = off_sp + (SPLIT ? (size_t)2 * 32 * D * 4 : 0);
+    static_assert(bytes <= 227 * 1024, "shared memory of one CTA");
 };
 
 template <int D, bool BF16, bool SPLIT>
@@ -184,6 +208,7 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
     constexpr int NT = NG * D;              // threads of the CTA
     extern __shared__ __align__(16) unsigned char smem[];
     float *sV = reinterpret_cast<float *>(smem + L::off_v);
+    TI *sVr = reinterpret_cast<TI *>(smem + L::off_vr);
     TI *sDo = reinterpret_cast<TI *>(smem + L::off_do);
     TI *sK = reinterpret_cast<TI *>(smem + L::off_k);
     float *sG = reinterpret_cast<float *>(smem + L::off_g);
@@ -192,6 +217,7 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
     float *sDu = reinterpret_cast<float *>(smem + L::off_du);
     float *sRow = reinterpret_cast<float *>(smem + L::off_row);
     float *sDb = reinterpret_cast<float *>(smem + L::off_db);
+    float *sSp = reinterpret_cast<float *>(smem + L::off_sp);
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int gi = tid / D, i = tid % D, wg = i >> 5;     // group in the CTA, key row, warp in the group
@@ -219,29 +245,45 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
     const int Ln = t1 - t0, nch = (Ln + CH - 1) / CH;
     const size_t unit = (size_t)un;
 
-    // the rows of chunk j (tokens t0 + 64 j ..) into shared memory; do only
-    // for the backward pass
+    // k and g rows of tokens 32 hf .. 32 hf + 31 of chunk j into shared memory
+    // (row = token mod 32), as cp.async pieces of 16 bytes
+    auto stage_kg = [&](int j, int hf) {
+        const int tb = t0 + CH * j + HC * hf, lc = min(HC, t1 - tb);
+        constexpr int KP = D * (int)sizeof(TI) / 16, KE = 16 / (int)sizeof(TI), GP = D / 4;
+        for (int idx = tid; idx < lc * KP; idx += NT) {
+            const int tt = idx / KP, c = (idx % KP) * KE;
+            cpa16(sK + tt * D + c, reinterpret_cast<const TI *>(p.k) + ((size_t)(tb + tt) * H + h) * D + c);
+        }
+        for (int idx = tid; idx < lc * GP; idx += NT) {
+            const int tt = idx / GP, c = (idx % GP) * 4;
+            cpa16(sG + tt * D + c, p.g + ((size_t)(tb + tt) * H + h) * D + c);
+        }
+    };
+    // the chunk's b and the CTA's columns of v (and of do for the backward
+    // pass) into shared memory, as cp.async pieces
     auto stage = [&](int j, bool bwd) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
-        for (int idx = tid; idx < lc * D; idx += NT) {
-            const int tt = idx / D, c = idx % D;
-            const size_t th = ((size_t)(tb + tt) * H + h) * D + c;
-            sK[tt * D + c] = reinterpret_cast<const TI *>(p.k)[th];
-            sG[tt * D + c] = p.g[th];
-        }
-        for (int idx = tid; idx < lc * VW; idx += NT) {
-            const int tt = idx / VW, c = idx % VW;
+        constexpr int VP = VW * (int)sizeof(TI) / 16, VE = 16 / (int)sizeof(TI);
+        for (int idx = tid; idx < lc * VP; idx += NT) {
+            const int tt = idx / VP, c = (idx % VP) * VE;
             const size_t th = ((size_t)(tb + tt) * H + h) * D + cbase + c;
-            sV[tt * VW + c] = ld_in<BF16>(p.v, th);
-            if (bwd) sDo[tt * VW + c] = reinterpret_cast<const TI *>(p.dout)[th];
+            cpa16(sVr + tt * VW + c, reinterpret_cast<const TI *>(p.v) + th);
+            if (bwd) cpa16(sDo + tt * VW + c, reinterpret_cast<const TI *>(p.dout) + th);
         }
-        for (int tt = tid; tt < lc; tt += NT) sB[tt] = p.beta[(size_t)(tb + tt) * H + h];
+        for (int tt = tid; tt < lc; tt += NT) cpa4(sB + tt, p.beta + (size_t)(tb + tt) * H + h);
+    };
+    // wait for this thread's copies, then for every thread's
+    auto landed = [&]() {
+        cpa_commit();
+        cpa_wait_all();
+        __syncthreads();
     };
     // one forward step of token tt of the staged chunk on this thread's slab S
     // (row i, columns c0 ..); the token's v row becomes w = v - p (u = b w)
     auto fwd_step = [&](float2 (&S)[16], int tt) {
-        const float e = __expf(fmaxf(sG[tt * D + i], g_min));
-        const float ki = to_f(sK[tt * D + i]), b = sB[tt];
+        const int r = tt & (HC - 1);
+        const float e = __expf(fmaxf(sG[r * D + i], g_min));
+        const float ki = to_f(sK[r * D + i]), b = sB[tt];
         const float2 e2 = bc2(e), k2 = bc2(ki), b2 = bc2(b);
         float pv[32];
 #pragma unroll
@@ -257,7 +299,7 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
             float pj = 0.f;
 #pragma unroll
             for (int w = 0; w < WPG; ++w) pj += sRed[(gi * WPG + w) * 32 + lane];
-            sV[tt * VW + vc + lane] -= pj;
+            sV[tt * VW + vc + lane] = to_f(sVr[tt * VW + vc + lane]) - pj;
         }
         group_sync(1 + gi, D);
 #pragma unroll
@@ -280,9 +322,12 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
             st_slab(ckpt_blk(j), S, tid, NT);
             if (j == nch - 1) break;  // the last chunk's states are recomputed in pass 2
             stage(j, false);
-            __syncthreads();
-            for (int tt = 0; tt < CH; ++tt) fwd_step(S, tt);
-            __syncthreads();
+            for (int hf = 0; hf < CH / HC; ++hf) {
+                stage_kg(j, hf);
+                landed();
+                for (int tt = HC * hf; tt < HC * (hf + 1); ++tt) fwd_step(S, tt);
+                __syncthreads();
+            }
         }
     }
 
@@ -292,37 +337,57 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
     for (int j = nch - 1; j >= 0; --j) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
         stage(j, true);
-        __syncthreads();
-        // recompute the chunk's states (the one before each token goes to the scratch)
+        // recompute the chunk's states (the one before each token goes to the
+        // scratch); k and g of the chunk's last half stay staged
         {
             float2 S[16];
             ld_slab(S, ckpt_blk(j), tid, NT);
-            for (int tt = 0; tt < lc; ++tt) {
-                st_slab(scr + (size_t)tt * BLK, S, tid, NT);
-                fwd_step(S, tt);
+            for (int hf = 0; HC * hf < lc; ++hf) {
+                if (hf) __syncthreads();
+                stage_kg(j, hf);
+                landed();
+                for (int tt = HC * hf; tt < min(lc, HC * (hf + 1)); ++tt) {
+                    st_slab(scr + (size_t)tt * BLK, S, tid, NT);
+                    fwd_step(S, tt);
+                }
             }
         }
-        // backward steps, last token first; the state of the token four steps
-        // on is brought into L2 while this one runs (one 128-byte line of the
-        // block per thread), and q one token ahead into a register
-        constexpr int PF = 4;
-        for (int tt = lc - 1; tt >= lc - PF && tt >= 0; --tt)
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)tt * BLK + (size_t)tid * 32));
+        // backward steps, last token first, with q one token ahead in a register
         float q_next = ld_in<BF16>(p.q, ((size_t)(tb + lc - 1) * H + h) * D + i);
         float *pw = SPLIT ? part(rank, pbuf) : nullptr;
+        // split form: token tt's state goes through buffer tt & 1; a buffer is
+        // refilled one step after the step that read it, whose arithmetic has
+        // consumed the values (so the read is complete)
+        if constexpr (SPLIT) {
+            cpa_slab(sSp + (size_t)((lc - 1) & 1) * BLK, scr + (size_t)(lc - 1) * BLK, tid, NT);
+            cpa_commit();
+        }
         for (int tt = lc - 1; tt >= 0; --tt) {
             const size_t th = (size_t)(tb + tt) * H + h;
-            if (tt >= PF)
-                asm volatile("prefetch.global.L2 [%0];\n" ::"l"(scr + (size_t)(tt - PF) * BLK + (size_t)tid * 32));
+            if (tt == HC - 1 && lc > HC) {  // into the chunk's first half: its k and g
+                __syncthreads();
+                stage_kg(j, 0);
+                landed();
+            }
             const float qi = q_next;
             if (tt > 0) q_next = ld_in<BF16>(p.q, (th - H) * D + i);
-            const float graw = sG[tt * D + i];
+            const int r = tt & (HC - 1);
+            const float graw = sG[r * D + i];
             const float e = __expf(fmaxf(graw, g_min));
-            const float ki = to_f(sK[tt * D + i]);
+            const float ki = to_f(sK[r * D + i]);
             const float b = sB[tt];
             const float2 e2 = bc2(e), k2 = bc2(ki), b2 = bc2(b);
             float2 Sp[16];
-            ld_slab(Sp, scr + (size_t)tt * BLK, tid, NT);
+            if constexpr (SPLIT) {
+                cpa_wait_all();
+                ld_slab(Sp, sSp + (size_t)(tt & 1) * BLK, tid, NT);
+                if (tt > 0) {
+                    cpa_slab(sSp + (size_t)((tt - 1) & 1) * BLK, scr + (size_t)(tt - 1) * BLK, tid, NT);
+                    cpa_commit();
+                }
+            } else {
+                ld_slab(Sp, scr + (size_t)tt * BLK, tid, NT);
+            }
             // G += scale q do^T; dq partial = scale S' do over this group's columns
             float2 dq2 = make_float2(0.f, 0.f);
             float gk[32];
@@ -418,24 +483,41 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
             // the chunk's column partials of every CTA of the cluster, added in
             // group order, for the tokens rank, rank + NC, ... of the chunk
             cluster_sync();
-            for (int tt = rank; tt < lc; tt += NC) {
-                const size_t th = (size_t)(tb + tt) * H + h;
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, sb = 0.f;
+            // four tokens at a time: all their partials are loaded before any sum
+            for (int tq = rank; tq < lc; tq += 4 * NC) {
+                float v[4][NC][3], vb[4][NC];
 #pragma unroll
-                for (int s = 0; s < NC; ++s) {
-                    const float *pr = part(s, pbuf);
-                    a0 += __ldcg(pr + (size_t)tt * 3 * D + i);
-                    a1 += __ldcg(pr + (size_t)tt * 3 * D + D + i);
-                    a2 += __ldcg(pr + (size_t)tt * 3 * D + 2 * D + i);
-                    if (tid == 0) sb += __ldcg(pr + (size_t)CH * 3 * D + tt);
+                for (int u = 0; u < 4; ++u) {
+                    const int tt = tq + u * NC;
+#pragma unroll
+                    for (int s = 0; s < NC; ++s) {
+                        const float *pr = part(s, pbuf);
+                        const bool ok = tt < lc;
+#pragma unroll
+                        for (int x = 0; x < 3; ++x) v[u][s][x] = ok ? __ldcg(pr + (size_t)tt * 3 * D + x * D + i) : 0.f;
+                        vb[u][s] = (ok && tid == 0) ? __ldcg(pr + (size_t)CH * 3 * D + tt) : 0.f;
+                    }
                 }
-                p.dq[th * D + i] = a0;
-                p.dk[th * D + i] = a1;
-                p.dg[th * D + i] = (sG[tt * D + i] < g_min) ? 0.f : a2;
-                if (tid == 0) p.dbeta[th] = sb;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int tt = tq + u * NC;
+                    if (tt >= lc) break;
+                    const size_t th = (size_t)(tb + tt) * H + h;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, sb = 0.f;
+#pragma unroll
+                    for (int s = 0; s < NC; ++s) {
+                        a0 += v[u][s][0];
+                        a1 += v[u][s][1];
+                        a2 += v[u][s][2];
+                        sb += vb[u][s];
+                    }
+                    p.dq[th * D + i] = a0;
+                    p.dk[th * D + i] = a1;
+                    p.dg[th * D + i] = (p.g[th * D + i] < g_min) ? 0.f : a2;
+                    if (tid == 0) p.dbeta[th] = sb;
+                }
             }
             pbuf ^= 1;
-            __syncthreads();  // sG is restaged next
         }
     }
     if (p.dS0) {
