@@ -455,13 +455,14 @@ def main(argv=None):
         Kb = max(2, K // 10)
         bms, kb = timed_launches(kda, bwd_step, Kb, stream)
         bms = reduce_max(bms, ws)
-        # per token-head: fp32 flops of two forward passes (pass 1 and the recompute:
-        # 3 d^2 FMA each) and the backward step (8 d^2 FMA); bytes of the recomputed
-        # state written and read back (2 x d^2 x 4) plus the inputs and gradients
+        # per token-head: fp32 flops of the forward pass (3 d^2 FMA), the recompute
+        # from the stored w = v - p (2 d^2) and the backward step (8 d^2 FMA); bytes
+        # of the recomputed state written and read back (2 x d^2 x 4) and of w
+        # (2 x d x 4) plus the inputs and gradients
         d2 = w.dk * w.dv
-        flops = T * H * 2.0 * (2 * 3 * d2 + 8 * d2)
+        flops = T * H * 2.0 * (3 * d2 + 2 * d2 + 8 * d2)
         io = T * H * (4 * 128 * 2 + 128 * 4 + 4 + 3 * 128 * 4 + 128 * 4 + 4)  # q,k,v,do bf16 + g,beta in; dq,dk,dv,dg,dbeta out
-        scratch = T * H * 2.0 * d2 * 4
+        scratch = T * H * 2.0 * (d2 + w.dv) * 4
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 flop x max SM clock, TFLOP/s
         out["backward"] = {"workload": w.name + " backward (dq, dk, dv, dg, dbeta)", "ms": bms,
                            "tok_s": ws * T / (bms * 1e-3), "fp32_tflops": flops / (bms * 1e-3) / 1e12,

@@ -231,7 +231,9 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *             min(N x H, 160) x 64 states, d x d f32 each (at most 160
  *             (sequence, head) units are in flight, one scratch slot each),
  *             then min(N x H, 160) x d/32 x 2 buffers of 64 x (3d + 1) f32
- *             column partials, each part 256-byte aligned;
+ *             column partials, then T x H x d f32 (w = v - p of every token,
+ *             kept by the forward pass for the recompute), each part
+ *             256-byte aligned;
  *             KDA_ERR_WORKSPACE when smaller.
  * Invalid cu_seqlens set KDA_STATUS_BAD_SEQLENS; that sequence is skipped.
  */

@@ -523,7 +523,8 @@ size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
     const size_t DD = (size_t)dk * dv * 4;
     const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
     const size_t parts = slots * (size_t)(dk / 32) * 2 * kda::chunk_bwd_partial_floats(dk) * 4;
-    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD) + align256(parts);
+    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD) + align256(parts) +
+           align256((size_t)T * H * dk * 4);
 }
 
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -552,7 +553,10 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
     const size_t off_scr = align256((size_t)(T / kChunk + N) * H * DD);
     a.scratch = reinterpret_cast<float *>(ws + off_scr);
-    a.partials = reinterpret_cast<float *>(ws + off_scr + align256(slots * kChunk * DD));
+    const size_t off_par = off_scr + align256(slots * kChunk * DD);
+    a.partials = reinterpret_cast<float *>(ws + off_par);
+    a.wbuf = reinterpret_cast<float *>(
+        ws + off_par + align256(slots * (size_t)(dk / 32) * 2 * kda::chunk_bwd_partial_floats(dk) * 4));
     a.N = N; a.T = T; a.H = H; a.scale = scale; a.g_min = g_min; a.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,

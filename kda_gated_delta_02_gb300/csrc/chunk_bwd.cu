@@ -32,11 +32,13 @@
 //    has arrived at the barrier of chunk c + 1, i.e. finished reading chunk c.
 // CTAs (clusters) are persistent, at most kBwdMaxCtas units at a time (one
 // scratch slot each), and stride over the (sequence, head) units.
-// Pass 1 walks the sequence forward and keeps the state at every chunk start
+// Pass 1 walks the sequence forward, keeps the state at every chunk start
 // (64 tokens) in a slot-indexed buffer (chunk j of sequence n is slot
-// floor(t0 / 64) + n + j); pass 2 takes the chunks in reverse, recomputes the
-// chunk's states from its checkpoint into a per-CTA scratch (and v - p per
-// token in shared memory) and runs the backward steps over them.  Each
+// floor(t0 / 64) + n + j) and w = v - p of every token in a [T][H][d] buffer;
+// pass 2 takes the chunks in reverse, recomputes the chunk's states from its
+// checkpoint and the stored w (S' = D S + k (b w)^T: the same operations as
+// pass 1, so the same bits, without the sum over key rows) into a per-CTA
+// scratch and runs the backward steps over them.  Each
 // chunk's b and the CTA's value columns of v and do, and its k and g half a
 // chunk (32 tokens) at a time, are copied into shared memory by cp.async
 // batches (one memory latency per batch); q is read from global memory one
@@ -259,17 +261,22 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
             cpa16(sG + tt * D + c, p.g + ((size_t)(tb + tt) * H + h) * D + c);
         }
     };
-    // the chunk's b and the CTA's columns of v (and of do for the backward
-    // pass) into shared memory, as cp.async pieces
+    // the chunk's b and the CTA's columns of v (forward pass) or of the
+    // stored w and of do (backward pass) into shared memory, as cp.async pieces
     auto stage = [&](int j, bool bwd) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
-        constexpr int VP = VW * (int)sizeof(TI) / 16, VE = 16 / (int)sizeof(TI);
+        constexpr int VP = VW * (int)sizeof(TI) / 16, VE = 16 / (int)sizeof(TI), WP = VW / 4;
         for (int idx = tid; idx < lc * VP; idx += NT) {
             const int tt = idx / VP, c = (idx % VP) * VE;
             const size_t th = ((size_t)(tb + tt) * H + h) * D + cbase + c;
-            cpa16(sVr + tt * VW + c, reinterpret_cast<const TI *>(p.v) + th);
             if (bwd) cpa16(sDo + tt * VW + c, reinterpret_cast<const TI *>(p.dout) + th);
+            else cpa16(sVr + tt * VW + c, reinterpret_cast<const TI *>(p.v) + th);
         }
+        if (bwd)
+            for (int idx = tid; idx < lc * WP; idx += NT) {
+                const int tt = idx / WP, c = (idx % WP) * 4;
+                cpa16(sV + tt * VW + c, p.wbuf + ((size_t)(tb + tt) * H + h) * D + cbase + c);
+            }
         for (int tt = tid; tt < lc; tt += NT) cpa4(sB + tt, p.beta + (size_t)(tb + tt) * H + h);
     };
     // wait for this thread's copies, then for every thread's
@@ -310,6 +317,20 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
             S[c / 2 + 1] = __ffma2_rn(k2, __fmul2_rn(b2, wb), __fmul2_rn(e2, S[c / 2 + 1]));
         }
     };
+    // the same step with w = v - p already staged (pass 2)
+    auto rec_step = [&](float2 (&S)[16], int tt) {
+        const int r = tt & (HC - 1);
+        const float e = __expf(fmaxf(sG[r * D + i], g_min));
+        const float ki = to_f(sK[r * D + i]), b = sB[tt];
+        const float2 e2 = bc2(e), k2 = bc2(ki), b2 = bc2(b);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            float2 wa, wb;
+            ld4(sV + tt * VW + vc + c, wa, wb);
+            S[c / 2] = __ffma2_rn(k2, __fmul2_rn(b2, wa), __fmul2_rn(e2, S[c / 2]));
+            S[c / 2 + 1] = __ffma2_rn(k2, __fmul2_rn(b2, wb), __fmul2_rn(e2, S[c / 2 + 1]));
+        }
+    };
     auto slot_of = [&](int j) { return (size_t)(t0 / CH + n + j); };
     // the CTA's share of the unit's checkpoint block of chunk j
     auto ckpt_blk = [&](int j) { return p.ckpt + (slot_of(j) * H + h) * DD + (size_t)rank * BLK; };
@@ -319,16 +340,23 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
         float2 S[16];
         ld_row32(S, p.S0 ? p.S0 + unit * DD + (size_t)i * D + c0 : nullptr);
         for (int j = 0; j < nch; ++j) {
+            const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
             st_slab(ckpt_blk(j), S, tid, NT);
-            if (j == nch - 1) break;  // the last chunk's states are recomputed in pass 2
             stage(j, false);
-            for (int hf = 0; hf < CH / HC; ++hf) {
+            for (int hf = 0; HC * hf < lc; ++hf) {
                 stage_kg(j, hf);
                 landed();
-                for (int tt = HC * hf; tt < HC * (hf + 1); ++tt) fwd_step(S, tt);
+                for (int tt = HC * hf; tt < min(lc, HC * (hf + 1)); ++tt) fwd_step(S, tt);
                 __syncthreads();
             }
+            // the chunk's w rows (this CTA's columns) to the w buffer
+            for (int idx = tid; idx < lc * (VW / 4); idx += NT) {
+                const int tt = idx / (VW / 4), c = (idx % (VW / 4)) * 4;
+                *reinterpret_cast<float4 *>(p.wbuf + ((size_t)(tb + tt) * H + h) * D + cbase + c) =
+                    *reinterpret_cast<const float4 *>(sV + tt * VW + c);
+            }
         }
+        __syncthreads();  // sV is restaged next
     }
 
     // ---------------------------------------------------------------- pass 2: chunks in reverse
@@ -337,8 +365,8 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
     for (int j = nch - 1; j >= 0; --j) {
         const int tb = t0 + CH * j, lc = min(CH, t1 - tb);
         stage(j, true);
-        // recompute the chunk's states (the one before each token goes to the
-        // scratch); k and g of the chunk's last half stay staged
+        // recompute the chunk's states from the stored w (the one before each
+        // token goes to the scratch); k and g of the chunk's last half stay staged
         {
             float2 S[16];
             ld_slab(S, ckpt_blk(j), tid, NT);
@@ -348,7 +376,7 @@ __global__ void __launch_bounds__(SPLIT ? D : D * D / 32, SPLIT ? 3 : 1) kda_chu
                 landed();
                 for (int tt = HC * hf; tt < min(lc, HC * (hf + 1)); ++tt) {
                     st_slab(scr + (size_t)tt * BLK, S, tid, NT);
-                    fwd_step(S, tt);
+                    rec_step(S, tt);
                 }
             }
         }

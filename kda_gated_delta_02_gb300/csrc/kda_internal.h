@@ -88,6 +88,7 @@ struct BwdArgs {
     float *scratch;                // [min(N H, kBwdMaxCtas)][64][d][d] states of the chunk being differentiated
     float *partials;               // [min(N H, kBwdMaxCtas) d/32][2][chunk_bwd_partial_floats(d)] column
                                    // partials of the split form (null: the whole form)
+    float *wbuf;                   // [T][H][d] w = v - p of every token (pass 1 -> pass 2)
     int N, T, H;
     float scale, g_min;
     uint32_t *status;

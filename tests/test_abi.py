@@ -148,18 +148,21 @@ def test_kernel_timing_without_launches(lib):
 
 def test_backward_workspace_arithmetic(lib):
     """Chunk checkpoints (floor(T/64) + N slots) and 64 states per (sequence,
-    head) in flight, d x d fp32 each, then two buffers of 64 x (3d + 1) fp32
-    column partials per CTA (d/32 CTAs per unit); 0 for unsupported shapes."""
+    head) in flight, d x d fp32 each, two buffers of 64 x (3d + 1) fp32 column
+    partials per CTA (d/32 CTAs per unit), then w = v - p of every token (T x H
+    x d fp32); 0 for unsupported shapes."""
     lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
     N, T, H = 3, 1000, 4
     for d in (128, 64):
         dd = d * d * 4
         parts = lambda units: units * (d // 32) * 2 * 64 * (3 * d + 1) * 4
-        want = _align256((T // 64 + N) * H * dd) + _align256(N * H * 64 * dd) + _align256(parts(N * H))
+        wb = lambda h: _align256(T * h * d * 4)  # w = v - p of every token
+        want = _align256((T // 64 + N) * H * dd) + _align256(N * H * 64 * dd) + _align256(parts(N * H)) + wb(H)
         assert lib.kda_chunk_bwd_workspace_size(N, T, H, d, d) == want
         # many units: scratch and partials stop growing at 160 units in flight
         N2, H2 = 100, 96
-        want2 = _align256((T // 64 + N2) * H2 * dd) + _align256(160 * 64 * dd) + _align256(parts(160))
+        want2 = (_align256((T // 64 + N2) * H2 * dd) + _align256(160 * 64 * dd) + _align256(parts(160)) +
+                 wb(H2))
         assert lib.kda_chunk_bwd_workspace_size(N2, T, H2, d, d) == want2
     d = 128
     assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 64) == 0
