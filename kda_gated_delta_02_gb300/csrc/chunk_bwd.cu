@@ -583,7 +583,7 @@ static cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
         int active = 0;
         e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
         if (e != cudaSuccess) return e;
-        if (active < 1) return cudaErrorInvalidConfiguration;
+        if (active < 1) return launch_t<D, BF16, false>(a, st);  // no cluster fits: one CTA per unit
         if (active < nclusters) nclusters = active;  // the clusters stride over the units
         cfg.gridDim = dim3(nclusters * NC);
     }
