@@ -147,3 +147,29 @@ def test_whole_form_matches_oracle(kda, oracle, monkeypatch):
     monkeypatch.setenv("KDA_BWD_SPLIT", "0")
     x = _case([300, 64, 0], 2, 128, torch.bfloat16, seed=31)
     _compare(kda, oracle, x, scale=0.9)
+
+
+def test_absent_states_and_no_dS0(kda, oracle):
+    """initial_state and dS_final absent (zero), dS0 not asked for."""
+    x = _case([130, 64], 2, 128, torch.bfloat16, seed=41)
+    got = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], scale=0.8, want_dS0=False)
+    torch.cuda.synchronize()
+    assert got[5] is None
+    ref = oracle.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
+                          x["cu"].cpu().numpy(), to64(x["do"]), scale=0.8)
+    for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got[:5], ref[:5]):
+        e = normwise_err(to64(a), b, head_axis=1)
+        assert e <= BWD_TOL, f"{name}: error {e:.3e}"
+
+
+def test_floor_held_on_whole_chunks(kda, oracle):
+    """g at the floor exactly (-5) on whole chunks passes its gradient; g below
+    it on other chunks passes none."""
+    x = _case([256], 2, 128, torch.bfloat16, seed=43, floor_frac=0.0)
+    g = x["g"].clone()
+    g[0:64] = -5.0
+    g[128:192] = -6.0
+    x["g"] = g
+    got = _compare(kda, oracle, x, scale=1.0)
+    assert torch.all(got[3][128:192] == 0.0)
+    assert torch.count_nonzero(got[3][0:64]) > 0
