@@ -20,6 +20,10 @@ Functions and what they follow (page title, section):
 * ``decode_verify`` / ``decode_stepwise`` -- replay-based verify and the plain
   one-token-at-a-time decoder it must agree with ("Noyaux d'inference",
   section 1, "La solution : rejouer plutot que sauvegarder", "La fusion").
+* ``backward`` -- reverse mode of the token recurrence (training, the chunk
+  kernel's other use: "Noyaux KDA et FlashKDA", "FlashKDA : le noyau par
+  blocs"); the module ``chunk_reverse`` states the same backward in the
+  chunk (WY) form, pinned against it.
 """
 from __future__ import annotations
 

@@ -1,0 +1,160 @@
+"""Reverse mode of the chunk (WY) form, fp64 (test infrastructure only).
+
+Only ``tests/`` may import this module; the CUDA path never does.  It writes
+out, with numpy matrix products and one library inverse per chunk, the
+backward of the chunk form of the prefill -- the algebra a chunked backward
+on the tensor cores runs -- so that such a kernel has a checked statement to
+follow.  It is pinned against the token-level reverse mode
+(``oracle.backward``, itself pinned by finite differences of the forward
+oracle), not against any GPU output.
+
+Chunk form followed ("Dentro de los esfuerzos de optimizacion de Kimi K3",
+"Nota tecnica: Precision del KDA y memoria on-chip"; the backward as the
+chunk kernel's training use: "Noyaux KDA et FlashKDA", "FlashKDA : le noyau
+par blocs").  For a chunk of L tokens entered with state S0, with
+gamma_t = sum_{r<=t} max(g_r, g_min) (per key channel), Gam = e^gamma and
+GamC = Gam of the chunk's last token:
+
+    Kt = K * Gam      Kb = K / Gam      Kh = K * GamC / Gam      Qt = Q * Gam
+    A  = strict_lower(diag(beta) Kt Kb^T)        B = lower(Qt Kb^T)
+    Tm = (I + A)^-1   R = diag(beta) (V - Kt S0)    U = Tm R
+    O  = scale (Qt S0 + B U)                      S_C = diag(GamC) S0 + Kh^T U
+
+(u_t is beta_t (v_t - p_t) of the token recurrence; A_ts carries beta_t.)
+Given dO and dS_C the reverse pass is, step by step in the opposite order:
+
+    dU  = scale B^T dO + Kh dS_C            dB = scale lower(dO U^T)
+    dQt = scale dO S0^T                     dS0 = scale Qt^T dO + diag(GamC) dS_C
+    dKh = U dS_C^T                          dgamma_C += GamC * rowsum(dS_C * S0)
+    dR  = Tm^T dU                           dTm = dU R^T
+    dA  = strict_lower(-Tm^T dTm Tm^T)
+    dV  = diag(beta) dR                     dbeta = rowsum((V - Kt S0) * dR)
+    dKt = -diag(beta) dR S0^T               dS0 -= Kt^T diag(beta) dR
+    dM  = diag(beta) dA  (M = Kt Kb^T)      dbeta += rowsum(dA * M)
+    dKt += dM Kb                            dKb = dM^T Kt
+    dQt += lower(dB) Kb                     dKb += lower(dB)^T Qt
+    dK  = dKt Gam + dKb / Gam + dKh GamC / Gam          dQ = dQt Gam
+    dgamma_t = dKt Kt - dKb Kb - dKh Kh + dQt Qt   (+ sum_t dKh Kh and
+               the dgamma_C term on the chunk's last token)
+    dg'_r = sum_{t >= r} dgamma_t;   dg = dg' where g >= g_min, else 0
+
+and dS0 of a chunk is dS_C of the chunk before it.  In fp64 the factors
+1/Gam stay finite (gamma >= 64 g_min = -320 within a chunk of 64).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _chunk_forward(q, k, v, gp, beta, S0, scale):
+    gam = np.cumsum(gp, axis=0)
+    Gam = np.exp(gam)
+    GamC = Gam[-1]
+    Kt, Kb, Kh, Qt = k * Gam, k / Gam, k * (GamC / Gam), q * Gam
+    L = k.shape[0]
+    M = Kt @ Kb.T
+    A = np.tril(beta[:, None] * M, -1)
+    B = np.tril(Qt @ Kb.T)
+    Tm = np.linalg.inv(np.eye(L) + A)
+    Vres = v - Kt @ S0
+    R = beta[:, None] * Vres
+    U = Tm @ R
+    O = scale * (Qt @ S0 + B @ U)
+    SC = GamC[:, None] * S0 + Kh.T @ U
+    return dict(Gam=Gam, GamC=GamC, Kt=Kt, Kb=Kb, Kh=Kh, Qt=Qt, M=M, B=B, Tm=Tm, Vres=Vres, R=R, U=U,
+                O=O, SC=SC)
+
+
+def _chunk_reverse(f, S0, beta, dO, dSC, scale):
+    Gam, GamC, Kt, Kb, Kh, Qt = f["Gam"], f["GamC"], f["Kt"], f["Kb"], f["Kh"], f["Qt"]
+    M, B, Tm, Vres, R, U = f["M"], f["B"], f["Tm"], f["Vres"], f["R"], f["U"]
+    # O = scale (Qt S0 + B U);  S_C = diag(GamC) S0 + Kh^T U
+    dU = scale * B.T @ dO + Kh @ dSC
+    dB = scale * np.tril(dO @ U.T)
+    dQt = scale * dO @ S0.T
+    dS0 = scale * Qt.T @ dO + GamC[:, None] * dSC
+    dKh = U @ dSC.T
+    dgamC = GamC * np.sum(dSC * S0, axis=1)
+    # U = Tm R;  Tm = (I + A)^-1
+    dR = Tm.T @ dU
+    dTm = dU @ R.T
+    dA = np.tril(-(Tm.T @ dTm @ Tm.T), -1)
+    # R = diag(beta) (V - Kt S0)
+    dV = beta[:, None] * dR
+    dbeta = np.sum(Vres * dR, axis=1)
+    dKt = -(beta[:, None] * dR) @ S0.T
+    dS0 -= Kt.T @ (beta[:, None] * dR)
+    # A = strict_lower(diag(beta) M), M = Kt Kb^T
+    dM = beta[:, None] * dA
+    dbeta += np.sum(dA * M, axis=1)
+    dKt += dM @ Kb
+    dKb = dM.T @ Kt
+    # B = lower(Qt Kb^T)
+    dQt += np.tril(dB) @ Kb
+    dKb += np.tril(dB).T @ Qt
+    # Kt = K Gam, Kb = K / Gam, Kh = K GamC / Gam, Qt = Q Gam (Gam = e^gamma)
+    dK = dKt * Gam + dKb / Gam + dKh * (GamC / Gam)
+    dQ = dQt * Gam
+    dgam = dKt * Kt - dKb * Kb - dKh * Kh + dQt * Qt
+    dgam[-1] += dgamC + np.sum(dKh * Kh, axis=0)
+    # gamma = cumsum(g'): the gradient of g'_r sums those of gamma_t, t >= r
+    dgp = np.cumsum(dgam[::-1], axis=0)[::-1]
+    return dQ, dK, dV, dgp, dbeta, dS0
+
+
+def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0):
+    """One head: q, k, g [T, dk]; v, do [T, dv]; beta [T]; S0, dS_final
+    [dk, dv] or None (zero).  Returns (o, S_final, dq, dk, dv, dg, dbeta,
+    dS0), fp64; dg is with respect to the raw g (zero where g < g_min)."""
+    q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
+    T, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    gp = np.maximum(g, g_min)
+    bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
+    starts, fwd = [], []
+    o = np.zeros((T, dv))
+    for c0, c1 in bounds:
+        starts.append(S)
+        f = _chunk_forward(q[c0:c1], k[c0:c1], v[c0:c1], gp[c0:c1], beta[c0:c1], S, scale)
+        fwd.append(f)
+        o[c0:c1] = f["O"]
+        S = f["SC"]
+    S_final = S
+    dq, dkk, dgp = np.zeros((T, dk)), np.zeros((T, dk)), np.zeros((T, dk))
+    dvv, db = np.zeros((T, dv)), np.zeros(T)
+    dS = np.zeros((dk, dv)) if dS_final is None else np.array(dS_final, dtype=np.float64)
+    for (c0, c1), S_in, f in reversed(list(zip(bounds, starts, fwd))):
+        dQ, dK, dV, dG, dB, dS = _chunk_reverse(f, S_in, beta[c0:c1], do[c0:c1], dS, scale)
+        dq[c0:c1], dkk[c0:c1], dvv[c0:c1], dgp[c0:c1], db[c0:c1] = dQ, dK, dV, dG, dB
+    dg = np.where(g >= g_min, dgp, 0.0)
+    return o, S_final, dq, dkk, dvv, dg, db, dS
+
+
+def chunk_form_backward(q, k, v, g, beta, cu_seqlens, do, S0=None, dS_final=None, C=64, scale=1.0,
+                        g_min=-5.0):
+    """Packed sequences (cu_seqlens [N+1]) and heads: q, k, g [T, H, dk]; v, do
+    [T, H, dv]; beta [T, H]; S0, dS_final [N, H, dk, dv] or None.  Chunks restart
+    at every sequence start.  Returns (o, S_final, dq, dk, dv, dg, dbeta, dS0)."""
+    q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    N = cu.shape[0] - 1
+    o, dq, dkk, dvv, dg = (np.zeros_like(x) for x in (v, q, k, v, g))
+    db = np.zeros((T, H))
+    S_final, dS0 = np.zeros((N, H, dk, dv)), np.zeros((N, H, dk, dv))
+    for n in range(N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        for h in range(H):
+            s0 = None if S0 is None else S0[n, h]
+            dsf = None if dS_final is None else dS_final[n, h]
+            if b == a:
+                S_final[n, h] = 0.0 if s0 is None else s0
+                dS0[n, h] = 0.0 if dsf is None else dsf
+                continue
+            r = chunk_form_backward_head(q[a:b, h], k[a:b, h], v[a:b, h], g[a:b, h], beta[a:b, h],
+                                         do[a:b, h], s0, dsf, C=C, scale=scale, g_min=g_min)
+            o[a:b, h], S_final[n, h] = r[0], r[1]
+            dq[a:b, h], dkk[a:b, h], dvv[a:b, h], dg[a:b, h], db[a:b, h], dS0[n, h] = r[2:]
+    return o, S_final, dq, dkk, dvv, dg, db, dS0

@@ -1,0 +1,89 @@
+"""The chunk (WY) form of the backward (oracle/chunk_reverse.py) against the
+token-level reverse mode of the oracle (itself pinned by central differences
+of the forward oracle), and its forward half against the forward oracle.
+
+CPU only: packed ragged sequences, chunk lengths that split them into many
+chunks (with a partial last chunk), one chunk per sequence, one token per
+chunk (then A = 0 and the chunk form is the token recurrence), part of g
+under the floor and some exactly at it.
+"""
+import numpy as np
+import pytest
+
+from oracle import chunk_reverse
+
+G_MIN = -5.0
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dS0")
+
+
+def _case(rng, lens, H, dk, dv, below=0.1, at=0.05):
+    T = int(sum(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = -np.logaddexp(0.0, rng.standard_normal((T, H, dk)))
+    u = rng.random((T, H, dk))
+    g[u < below] = -5.5 - rng.random(int((u < below).sum()))
+    g[(u >= below) & (u < below + at)] = G_MIN
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    N = len(lens)
+    S0 = 0.05 * rng.standard_normal((N, H, dk, dv))
+    do = rng.standard_normal((T, H, dv))
+    dSf = 0.1 * rng.standard_normal((N, H, dk, dv))
+    return q, k, v, g, beta, cu, S0, do, dSf
+
+
+def _rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+@pytest.mark.parametrize("C,lens", [(16, [37, 0, 64, 5]), (64, [130, 64]), (8, [23]), (1, [9, 4]),
+                                    (256, [100, 0, 3])])
+def test_chunk_reverse_matches_token_reverse(oracle, C, lens):
+    rng = np.random.default_rng(C * 7 + len(lens))
+    H, dk, dv = 2, 8, 6
+    q, k, v, g, beta, cu, S0, do, dSf = _case(rng, lens, H, dk, dv)
+    got = chunk_reverse.chunk_form_backward(q, k, v, g, beta, cu, do, S0=S0, dS_final=dSf, C=C, scale=0.7)
+    ref = oracle.backward(q, k, v, g, beta, cu, do, S0=S0, dS_final=dSf, scale=0.7)
+    for name, a, b in zip(NAMES, got[2:], ref):
+        assert _rel(a, b) <= 1e-10, f"{name}: {_rel(a, b):.2e}"
+    # the floor: no gradient below it, gradient at it
+    assert np.all(got[5][g < G_MIN] == 0.0)
+    o_ref, S_ref = oracle.prefill(q, k, v, g, beta, cu, S0=S0, scale=0.7)
+    assert _rel(got[0], o_ref) <= 1e-11
+    assert _rel(got[1], S_ref) <= 1e-11
+
+
+def test_chunk_reverse_absent_states_d128(oracle):
+    """d = 128, two chunks of 64 and a partial one, no initial state and no
+    final-state gradient."""
+    rng = np.random.default_rng(5)
+    q, k, v, g, beta, cu, _, do, _ = _case(rng, [150], 1, 128, 128)
+    got = chunk_reverse.chunk_form_backward(q, k, v, g, beta, cu, do, C=64)
+    ref = oracle.backward(q, k, v, g, beta, cu, do)
+    for name, a, b in zip(NAMES, got[2:], ref):
+        assert _rel(a, b) <= 1e-10, f"{name}: {_rel(a, b):.2e}"
+
+
+def test_chunk_reverse_gradient_of_a_chunk_boundary_state(oracle):
+    """dS0 of the second chunk is the state gradient the first chunk receives:
+    splitting a sequence's reverse pass at a chunk boundary by hand (second
+    half first, its dS0 fed to the first half as dS_final) gives the same
+    gradients as one pass."""
+    rng = np.random.default_rng(9)
+    q, k, v, g, beta, cu, S0, do, dSf = _case(rng, [48], 1, 8, 8)
+    h = 0
+    full = chunk_reverse.chunk_form_backward_head(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], do[:, h],
+                                                  S0[0, h], dSf[0, h], C=16)
+    _, S1 = oracle.prefill(q[:32], k[:32], v[:32], g[:32], beta[:32], [0, 32], S0=S0)
+    second = chunk_reverse.chunk_form_backward_head(q[32:, h], k[32:, h], v[32:, h], g[32:, h], beta[32:, h],
+                                                    do[32:, h], S1[0, h], dSf[0, h], C=16)
+    first = chunk_reverse.chunk_form_backward_head(q[:32, h], k[:32, h], v[:32, h], g[:32, h], beta[:32, h],
+                                                   do[:32, h], S0[0, h], second[7], C=16)
+    for idx, name in zip(range(2, 7), NAMES[:5]):
+        joined = np.concatenate([first[idx], second[idx]])
+        assert _rel(joined, full[idx]) <= 1e-12, name
+    assert _rel(first[7], full[7]) <= 1e-12
