@@ -133,6 +133,35 @@ def _in_dtype(t):
     raise KDAError(f"unsupported input dtype {t.dtype}")
 
 
+def _expect(t, name, dtype, shape):
+    """The C ABI takes bare pointers, so dtypes and shapes are checked here."""
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise KDAError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise KDAError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state=None, cu_any_int=False):
+    """(T, H, dk, dv, N) of a prefill call whose tensors agree in dtype and shape."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise KDAError("q, k, g must be [T, H, dk] and v [T, H, dv]")
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    _in_dtype(q)
+    _expect(k, "k", q.dtype, (T, H, dk))
+    _expect(v, "v", q.dtype, (T, H, dv))
+    _expect(g, "g", torch.float32, (T, H, dk))
+    _expect(beta, "beta", torch.float32, (T, H))
+    if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 2 or (
+            cu_seqlens.dtype != torch.int32 and not (cu_any_int and not cu_seqlens.dtype.is_floating_point)):
+        raise KDAError("cu_seqlens must be int32 [N + 1] with N >= 1")
+    N = cu_seqlens.shape[0] - 1
+    _expect(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    return T, H, dk, dv, N
+
+
 def chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode=CP_AUTO, segment_len=0) -> int:
     return int(load_library().kda_chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len))
 
@@ -156,10 +185,14 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
     second dimension) through kda_chunk_fwd_ckpt.  With prep (the default) a
     bf16, dk = dv = 128 call gets the workspace of the two-kernel form; a
     caller-provided workspace is used as given when it is large enough."""
+    T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
+    _expect(out, "out", q.dtype, (T, H, dv))
+    _expect(final_state, "final_state", torch.float32, (N, H, dk, dv))
+    if ckpt_every:
+        if ckpt is None or ckpt.dim() != 5:
+            raise KDAError("ckpt must be an f32 tensor [N, K, H, dk, dv]")
+        _expect(ckpt, "ckpt", torch.float32, (N, ckpt.shape[1], H, dk, dv))
     lib = load_library()
-    T, H, dk = k.shape
-    dv = v.shape[2]
-    N = cu_seqlens.shape[0] - 1
     if out is None:
         out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
@@ -176,8 +209,6 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
               _ptr(workspace) if ws_bytes else None,
               ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0))
     if ckpt_every:
-        if ckpt is None or ckpt.dim() != 5 or ckpt.dtype != torch.float32:
-            raise KDAError("ckpt must be an f32 tensor [N, K, H, dk, dv]")
         rc = lib.kda_chunk_fwd_ckpt(*common, int(ckpt_every), int(ckpt.shape[1]), _ptr(ckpt), _ptr(status),
                                     _stream(stream))
         _check(rc, "kda_chunk_fwd_ckpt")
@@ -189,9 +220,17 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
 
 def segment_transition(k, v, g, beta, segment_len, g_min=-5.0, stream=None):
     """Transitions (M [P,H,dk,dk], N [P,H,dk,dv]) of fixed-length segments of one sequence."""
-    lib = load_library()
+    if k.dim() != 3 or v.dim() != 3:
+        raise KDAError("k, g must be [T, H, dk] and v [T, H, dv]")
     T, H, dk = k.shape
     dv = v.shape[2]
+    _in_dtype(k)
+    _expect(v, "v", k.dtype, (T, H, dv))
+    _expect(g, "g", torch.float32, (T, H, dk))
+    _expect(beta, "beta", torch.float32, (T, H))
+    if int(segment_len) < 1:
+        raise KDAError("segment_len must be positive")
+    lib = load_library()
     P = (T + segment_len - 1) // segment_len
     M = torch.empty((P, H, dk, dk), dtype=torch.float32, device=k.device)
     Nm = torch.empty((P, H, dk, dv), dtype=torch.float32, device=k.device)
@@ -203,8 +242,13 @@ def segment_transition(k, v, g, beta, segment_len, g_min=-5.0, stream=None):
 
 def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
     """Ordered composition: returns (S_in [P,H,dk,dv] or None, S_final [H,dk,dv])."""
-    lib = load_library()
+    if Nm.dim() != 4:
+        raise KDAError("Nm must be f32 [P, H, dk, dv]")
     P, H, dk, dv = Nm.shape
+    _expect(Nm, "Nm", torch.float32, (P, H, dk, dv))
+    _expect(M, "M", torch.float32, (P, H, dk, dk))
+    _expect(S0, "S0", torch.float32, (H, dk, dv))
+    lib = load_library()
     S_in = torch.empty_like(Nm) if want_segment_states else None
     Sf = torch.empty((H, dk, dv), dtype=torch.float32, device=Nm.device)
     rc = lib.kda_segment_compose(_ptr(M), _ptr(Nm), _ptr(S0), _ptr(S_in), _ptr(Sf), P, H, dk, dv,
@@ -226,10 +270,10 @@ def chunk_fwd_host(q, k, v, g, beta, cu_seqlens, initial_state=None, output_fina
     with the kernels.  cu_seqlens is a CPU int32 tensor.  Returns CPU tensors
     (o, final_state); they are complete once `stream` (default: the current
     one) has completed."""
+    T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state, cu_any_int=True)
+    _expect(out, "out", q.dtype, (T, H, dv))
+    _expect(final_state, "final_state", torch.float32, (N, H, dk, dv))
     lib = load_library()
-    T, H, dk = k.shape
-    dv = v.shape[2]
-    N = cu_seqlens.shape[0] - 1
     if out is None:
         out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
     if final_state is None and output_final_state:
@@ -252,10 +296,10 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=Non
     """Backward of chunk_fwd: returns (dq, dk, dv, dg, dbeta, dS0) in fp32
     (dS0 None unless want_dS0).  do [T,H,dv] in q's dtype; dS_final f32
     [N,H,dk,dv] or None."""
+    T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
+    _expect(do, "do", q.dtype, (T, H, dv))
+    _expect(dS_final, "dS_final", torch.float32, (N, H, dk, dv))
     lib = load_library()
-    T, H, dk = k.shape
-    dv = v.shape[2]
-    N = cu_seqlens.shape[0] - 1
     dev = q.device
     f32 = torch.float32
     dq = torch.empty((T, H, dk), dtype=f32, device=dev)
@@ -300,10 +344,27 @@ def decode_verify_replay(state, conv_tail, conv_w, cached_qkv, cached_g, cached_
     draft_len (int32 [R] on the device) makes the batch ragged: request r has
     draft_len[r] drafts (kda_decode_verify_replay_ragged); its rows past that
     are not written."""
-    lib = load_library()
+    if state.dim() != 4 or conv_w.dim() != 2 or new_qkv.dim() != 3:
+        raise KDAError("state [R, H, dk, dv], conv_w [Cq, W] and new_qkv [R, Wd + 1, Cq] expected")
     R, H, dk, dv = state.shape
     W = conv_w.shape[1]
     Wd = new_qkv.shape[1] - 1
+    Cq = H * (2 * dk + dv)
+    bf = torch.bfloat16
+    _expect(state, "state", bf, (R, H, dk, dv))
+    _expect(conv_tail, "conv_tail", bf, (R, W - 1, Cq))
+    _expect(conv_w, "conv_w", torch.float32, (Cq, W))
+    _expect(cached_qkv, "cached_qkv", bf, (R, Wd, Cq))
+    _expect(cached_g, "cached_g", bf, (R, Wd, H * dk))
+    _expect(cached_beta, "cached_beta", bf, (R, Wd, H))
+    _expect(accepted_len, "accepted_len", torch.int32, (R,))
+    _expect(new_qkv, "new_qkv", bf, (R, Wd + 1, Cq))
+    _expect(new_g, "new_g", bf, (R, Wd + 1, H * dk))
+    _expect(new_beta, "new_beta", bf, (R, Wd + 1, H))
+    _expect(out_norm_w, "out_norm_w", torch.float32, (dv,))
+    _expect(out, "out", bf, (R, Wd + 1, H, dv))
+    _expect(draft_len, "draft_len", torch.int32, (R,))
+    lib = load_library()
     if out is None:
         out = torch.empty((R, Wd + 1, H, dv), dtype=torch.bfloat16, device=state.device)
     if draft_len is not None:
