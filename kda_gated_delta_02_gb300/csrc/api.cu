@@ -21,17 +21,21 @@ inline bool dim_ok(int d) { return d == 64 || d == 128; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// SM count of the current device (cached per device)
 int sm_count() {
-    static int cached = 0;
-    if (cached > 0) return cached;
+    static std::atomic<int> cached[64];
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
-        cached = n;
-    } else {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
-        n = 152;  // GB300
+        return 152;  // GB300
     }
+    n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -278,10 +282,15 @@ int copy_streams(CopyStreams *cs) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KDA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_copy_mu);
-    if (!g_copy[dev].in) {
-        if (cudaStreamCreateWithFlags(&g_copy[dev].in, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&g_copy[dev].out, cudaStreamNonBlocking) != cudaSuccess)
+    if (!g_copy[dev].in) {  // both streams or neither
+        CopyStreams made;
+        if (cudaStreamCreateWithFlags(&made.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&made.out, cudaStreamNonBlocking) != cudaSuccess) {
+            if (made.in) cudaStreamDestroy(made.in);
+            cudaGetLastError();
             return KDA_ERR_CUDA;
+        }
+        g_copy[dev] = made;
     }
     *cs = g_copy[dev];
     return KDA_OK;
