@@ -131,6 +131,50 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
     return o, S_final, dq, dkk, dvv, dg, db, dS
 
 
+def state_gradient_chain(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0):
+    """The serial part of the chunked backward on its own, one head: the
+    chunk-start states S_in[c] and the state gradients dS_C[c] arriving at the
+    end of each chunk c (chunk order), from
+
+        dS_prev = scale Qt^T dO + diag(GamC) dS_C - Kt^T diag(beta) dR,
+        dR      = Tm^T (scale B^T dO + Kh dS_C).
+
+    Given S_in[c] and dS_C[c], every chunk's token gradients are independent of
+    the other chunks (``chunk_token_gradients``)."""
+    q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
+    T, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    gp = np.maximum(g, g_min)
+    bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
+    S_in, fwd = [], []
+    for c0, c1 in bounds:
+        S_in.append(S)
+        f = _chunk_forward(q[c0:c1], k[c0:c1], v[c0:c1], gp[c0:c1], beta[c0:c1], S, scale)
+        fwd.append(f)
+        S = f["SC"]
+    dS_C = [None] * len(bounds)
+    dS = np.zeros((dk, dv)) if dS_final is None else np.array(dS_final, dtype=np.float64)
+    for c in range(len(bounds) - 1, -1, -1):
+        c0, c1 = bounds[c]
+        f = fwd[c]
+        dS_C[c] = dS
+        dR = f["Tm"].T @ (scale * f["B"].T @ do[c0:c1] + f["Kh"] @ dS)
+        dS = (scale * f["Qt"].T @ do[c0:c1] + f["GamC"][:, None] * dS -
+              f["Kt"].T @ (beta[c0:c1, None] * dR))
+    return bounds, S_in, dS_C, dS
+
+
+def chunk_token_gradients(q, k, v, g, beta, do, S_in, dS_C, scale=1.0, g_min=-5.0):
+    """One chunk's token gradients (dq, dk, dv, dg, dbeta) and its dS0 from the
+    chunk's rows, its start state S_in and the state gradient dS_C at its end."""
+    q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
+    f = _chunk_forward(q, k, v, np.maximum(g, g_min), beta, S_in, scale)
+    dQ, dK, dV, dgp, dB, dS0 = _chunk_reverse(f, S_in, beta, do, dS_C, scale)
+    # dg' of the chunk's tokens is local: gamma restarts at every chunk
+    return dQ, dK, dV, np.where(g >= g_min, dgp, 0.0), dB, dS0
+
+
 def chunk_form_backward(q, k, v, g, beta, cu_seqlens, do, S0=None, dS_final=None, C=64, scale=1.0,
                         g_min=-5.0):
     """Packed sequences (cu_seqlens [N+1]) and heads: q, k, g [T, H, dk]; v, do

@@ -87,3 +87,25 @@ def test_chunk_reverse_gradient_of_a_chunk_boundary_state(oracle):
         joined = np.concatenate([first[idx], second[idx]])
         assert _rel(joined, full[idx]) <= 1e-12, name
     assert _rel(first[7], full[7]) <= 1e-12
+
+
+def test_serial_chain_then_independent_chunks(oracle):
+    """The decomposition a chunked kernel would use: the state-gradient chain
+    alone (serial over chunks), then every chunk's token gradients from its
+    (S_in, dS_C) pair in any order, equal the whole reverse pass."""
+    rng = np.random.default_rng(17)
+    q, k, v, g, beta, cu, S0, do, dSf = _case(rng, [150], 1, 16, 8)
+    h = 0
+    args = (q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], do[:, h])
+    full = chunk_reverse.chunk_form_backward_head(*args, S0=S0[0, h], dS_final=dSf[0, h], C=32, scale=0.9)
+    bounds, S_in, dS_C, dS0 = chunk_reverse.state_gradient_chain(*args, S0=S0[0, h], dS_final=dSf[0, h], C=32,
+                                                                 scale=0.9)
+    assert _rel(dS0, full[7]) <= 1e-12
+    parts = {}
+    for c in reversed(range(len(bounds))):  # any order; reversed to show no hidden carry
+        c0, c1 = bounds[c]
+        parts[c] = chunk_reverse.chunk_token_gradients(q[c0:c1, h], k[c0:c1, h], v[c0:c1, h], g[c0:c1, h],
+                                                       beta[c0:c1, h], do[c0:c1, h], S_in[c], dS_C[c], scale=0.9)
+    for idx, name in enumerate(NAMES[:5]):
+        joined = np.concatenate([parts[c][idx] for c in range(len(bounds))])
+        assert _rel(joined, full[2 + idx]) <= 1e-12, name
