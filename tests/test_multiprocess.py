@@ -65,3 +65,15 @@ def test_reduce_max_is_identity_at_world_size_one():
     import bench
     assert bench.reduce_max(1.25, 1) == 1.25
     bench.barrier(1)
+
+
+def test_both_arms_share_the_headline_config():
+    """The headline line and the reference arm name the same workload; the
+    whole-job parallelism follows the world size."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from kda_gated_delta_02_gb300 import synth
+    c1, c4 = bench.prefill_config(1), bench.prefill_config(4)
+    assert c1["workload"] == synth.PREFILL_32K.name and c1["T"] == 32768 and c1["H"] == 96
+    assert c1["parallelism"] == "replicas x1" and c4["parallelism"] == "replicas x4"
+    assert {k: v for k, v in c1.items() if k != "parallelism"} == {k: v for k, v in c4.items() if k != "parallelism"}
