@@ -134,10 +134,13 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
 def state_gradient_chain(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0):
     """The serial part of the chunked backward on its own, one head: the
     chunk-start states S_in[c] and the state gradients dS_C[c] arriving at the
-    end of each chunk c (chunk order), from
+    end of each chunk c (chunk order).  It is the adjoint of the forward's
+    state walk (U = Tm R = Tm diag(beta) V - W S0, O = scale (Qt S0 + B U),
+    S_C = diag(GamC) S0 + Kh^T U, with W = Tm diag(beta) Kt) and uses the
+    same chunk-local operands:
 
-        dS_prev = scale Qt^T dO + diag(GamC) dS_C - Kt^T diag(beta) dR,
-        dR      = Tm^T (scale B^T dO + Kh dS_C).
+        dU      = scale B^T dO + Kh dS_C
+        dS_prev = scale Qt^T dO + diag(GamC) dS_C - W^T dU
 
     Given S_in[c] and dS_C[c], every chunk's token gradients are independent of
     the other chunks (``chunk_token_gradients``)."""
@@ -159,9 +162,9 @@ def state_gradient_chain(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, sca
         c0, c1 = bounds[c]
         f = fwd[c]
         dS_C[c] = dS
-        dR = f["Tm"].T @ (scale * f["B"].T @ do[c0:c1] + f["Kh"] @ dS)
-        dS = (scale * f["Qt"].T @ do[c0:c1] + f["GamC"][:, None] * dS -
-              f["Kt"].T @ (beta[c0:c1, None] * dR))
+        W = f["Tm"] @ (beta[c0:c1, None] * f["Kt"])
+        dU = scale * f["B"].T @ do[c0:c1] + f["Kh"] @ dS
+        dS = scale * f["Qt"].T @ do[c0:c1] + f["GamC"][:, None] * dS - W.T @ dU
     return bounds, S_in, dS_C, dS
 
 
