@@ -46,52 +46,52 @@ from __future__ import annotations
 import numpy as np
 
 
-def _chunk_forward(q, k, v, gp, beta, S0, scale):
+def _chunk_forward(q, k, v, gp, beta, S0, scale, mm=np.matmul):
     gam = np.cumsum(gp, axis=0)
     Gam = np.exp(gam)
     GamC = Gam[-1]
     Kt, Kb, Kh, Qt = k * Gam, k / Gam, k * (GamC / Gam), q * Gam
     L = k.shape[0]
-    M = Kt @ Kb.T
+    M = mm(Kt, Kb.T)
     A = np.tril(beta[:, None] * M, -1)
-    B = np.tril(Qt @ Kb.T)
+    B = np.tril(mm(Qt, Kb.T))
     Tm = np.linalg.inv(np.eye(L) + A)
-    Vres = v - Kt @ S0
+    Vres = v - mm(Kt, S0)
     R = beta[:, None] * Vres
-    U = Tm @ R
-    O = scale * (Qt @ S0 + B @ U)
-    SC = GamC[:, None] * S0 + Kh.T @ U
+    U = mm(Tm, R)
+    O = scale * (mm(Qt, S0) + mm(B, U))
+    SC = GamC[:, None] * S0 + mm(Kh.T, U)
     return dict(Gam=Gam, GamC=GamC, Kt=Kt, Kb=Kb, Kh=Kh, Qt=Qt, M=M, B=B, Tm=Tm, Vres=Vres, R=R, U=U,
                 O=O, SC=SC)
 
 
-def _chunk_reverse(f, S0, beta, dO, dSC, scale):
+def _chunk_reverse(f, S0, beta, dO, dSC, scale, mm=np.matmul):
     Gam, GamC, Kt, Kb, Kh, Qt = f["Gam"], f["GamC"], f["Kt"], f["Kb"], f["Kh"], f["Qt"]
     M, B, Tm, Vres, R, U = f["M"], f["B"], f["Tm"], f["Vres"], f["R"], f["U"]
     # O = scale (Qt S0 + B U);  S_C = diag(GamC) S0 + Kh^T U
-    dU = scale * B.T @ dO + Kh @ dSC
-    dB = scale * np.tril(dO @ U.T)
-    dQt = scale * dO @ S0.T
-    dS0 = scale * Qt.T @ dO + GamC[:, None] * dSC
-    dKh = U @ dSC.T
+    dU = scale * mm(B.T, dO) + mm(Kh, dSC)
+    dB = scale * np.tril(mm(dO, U.T))
+    dQt = scale * mm(dO, S0.T)
+    dS0 = scale * mm(Qt.T, dO) + GamC[:, None] * dSC
+    dKh = mm(U, dSC.T)
     dgamC = GamC * np.sum(dSC * S0, axis=1)
     # U = Tm R;  Tm = (I + A)^-1
-    dR = Tm.T @ dU
-    dTm = dU @ R.T
-    dA = np.tril(-(Tm.T @ dTm @ Tm.T), -1)
+    dR = mm(Tm.T, dU)
+    dTm = mm(dU, R.T)
+    dA = np.tril(-mm(mm(Tm.T, dTm), Tm.T), -1)
     # R = diag(beta) (V - Kt S0)
     dV = beta[:, None] * dR
     dbeta = np.sum(Vres * dR, axis=1)
-    dKt = -(beta[:, None] * dR) @ S0.T
-    dS0 -= Kt.T @ (beta[:, None] * dR)
+    dKt = -mm(beta[:, None] * dR, S0.T)
+    dS0 -= mm(Kt.T, beta[:, None] * dR)
     # A = strict_lower(diag(beta) M), M = Kt Kb^T
     dM = beta[:, None] * dA
     dbeta += np.sum(dA * M, axis=1)
-    dKt += dM @ Kb
-    dKb = dM.T @ Kt
+    dKt += mm(dM, Kb)
+    dKb = mm(dM.T, Kt)
     # B = lower(Qt Kb^T)
-    dQt += np.tril(dB) @ Kb
-    dKb += np.tril(dB).T @ Qt
+    dQt += mm(np.tril(dB), Kb)
+    dKb += mm(np.tril(dB).T, Qt)
     # Kt = K Gam, Kb = K / Gam, Kh = K GamC / Gam, Qt = Q Gam (Gam = e^gamma)
     dK = dKt * Gam + dKb / Gam + dKh * (GamC / Gam)
     dQ = dQt * Gam
@@ -102,10 +102,13 @@ def _chunk_reverse(f, S0, beta, dO, dSC, scale):
     return dQ, dK, dV, dgp, dbeta, dS0
 
 
-def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0):
+def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0,
+                             mm=np.matmul):
     """One head: q, k, g [T, dk]; v, do [T, dv]; beta [T]; S0, dS_final
     [dk, dv] or None (zero).  Returns (o, S_final, dq, dk, dv, dg, dbeta,
-    dS0), fp64; dg is with respect to the raw g (zero where g < g_min)."""
+    dS0), fp64; dg is with respect to the raw g (zero where g < g_min).
+    `mm` computes every matrix product (a test can round its operands to
+    study a reduced-precision kernel); the inverse stays fp64."""
     q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
     T, dk = k.shape
     dv = v.shape[1]
@@ -116,7 +119,7 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
     o = np.zeros((T, dv))
     for c0, c1 in bounds:
         starts.append(S)
-        f = _chunk_forward(q[c0:c1], k[c0:c1], v[c0:c1], gp[c0:c1], beta[c0:c1], S, scale)
+        f = _chunk_forward(q[c0:c1], k[c0:c1], v[c0:c1], gp[c0:c1], beta[c0:c1], S, scale, mm)
         fwd.append(f)
         o[c0:c1] = f["O"]
         S = f["SC"]
@@ -125,7 +128,7 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
     dvv, db = np.zeros((T, dv)), np.zeros(T)
     dS = np.zeros((dk, dv)) if dS_final is None else np.array(dS_final, dtype=np.float64)
     for (c0, c1), S_in, f in reversed(list(zip(bounds, starts, fwd))):
-        dQ, dK, dV, dG, dB, dS = _chunk_reverse(f, S_in, beta[c0:c1], do[c0:c1], dS, scale)
+        dQ, dK, dV, dG, dB, dS = _chunk_reverse(f, S_in, beta[c0:c1], do[c0:c1], dS, scale, mm)
         dq[c0:c1], dkk[c0:c1], dvv[c0:c1], dgp[c0:c1], db[c0:c1] = dQ, dK, dV, dG, dB
     dg = np.where(g >= g_min, dgp, 0.0)
     return o, S_final, dq, dkk, dvv, dg, db, dS
