@@ -208,3 +208,116 @@ def chunk_form_backward(q, k, v, g, beta, cu_seqlens, do, S0=None, dS_final=None
             o[a:b, h], S_final[n, h] = r[0], r[1]
             dq[a:b, h], dkk[a:b, h], dvv[a:b, h], dg[a:b, h], db[a:b, h], dS0[n, h] = r[2:]
     return o, S_final, dq, dkk, dvv, dg, db, dS0
+
+
+# ---------------------------------------------------------------------------
+# fp32 with block anchoring.  In fp32 the factors 1/Gam overflow inside a
+# chunk of 64 held at the floor (e^{320}).  The forward avoids them by
+# splitting e^{gamma_t - gamma_s} = e^{gamma_t - gamma_a} e^{gamma_a - gamma_s}
+# with the anchor a = the last token of the 16-token block of s: the column
+# factor lies in [e^{-75}, 1] and the row factor in [0, e^{75}] (rows of later
+# blocks are <= 1), both inside fp32.  The same split carries the gradients of
+# M = Kt Kb^T and B = Qt Kb^T, the only products that need 1/Gam:
+#     row part  dK_t += e^{gamma_t - gamma_a} (dM_t,blk  (k_blk e^{gamma_a - gamma_blk}))
+#     col part  dK_s += e^{gamma_a - gamma_s} (dM_rows,s^T (k_rows e^{gamma_rows - gamma_a}))
+# and the log-decay gradient takes k (or q) times the row part minus k times
+# the column part.  Every other factor (e^{gamma}, e^{gamma_C - gamma}) is at
+# most 1 and may only underflow where the true term is below fp32's range.
+
+_BLK = 16
+
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float32)
+
+
+def _anchored_tiles(x_rows, k, gam, L, strict):
+    """Lower(-triangular) products x_rows_t . k_s e^{gamma_t - gamma_s} in fp32,
+    built per 16-token column block with its anchor, and the per-block factors."""
+    P = np.zeros((L, L), dtype=np.float32)
+    blocks = []
+    for j0 in range(0, L, _BLK):
+        j1 = min(j0 + _BLK, L)
+        a = j1 - 1
+        col = np.exp(gam[a] - gam[j0:j1])          # <= 1, >= e^{-75}
+        row = np.exp(gam[j0:] - gam[a])            # <= e^{75}
+        kc = k[j0:j1] * col
+        xr = x_rows[j0:] * row
+        P[j0:, j0:j1] = xr @ kc.T
+        blocks.append((j0, j1, row, col))
+    mask = np.tril(np.ones((L, L), dtype=bool), -1 if strict else 0)
+    return np.where(mask, P, np.float32(0)), blocks
+
+
+def chunk_form_backward_head_f32(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, scale=1.0, g_min=-5.0):
+    """The chunk-form reverse pass in fp32 (numpy float32 products and
+    elementwise work; fp32 inverse), with the block anchoring above.  Same
+    arguments and results as ``chunk_form_backward_head``, as float64 arrays
+    holding fp32 values."""
+    q, k, v, g, beta, do = (_f32(x) for x in (q, k, v, g, beta, do))
+    T, dk = k.shape
+    dv = v.shape[1]
+    scale = np.float32(scale)
+    S = np.zeros((dk, dv), np.float32) if S0 is None else _f32(S0).copy()
+    gp = np.maximum(g, np.float32(g_min))
+    bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
+    starts, fwd = [], []
+    o = np.zeros((T, dv), np.float32)
+    for c0, c1 in bounds:
+        L = c1 - c0
+        kk, qq, vv, bb = k[c0:c1], q[c0:c1], v[c0:c1], beta[c0:c1]
+        gam = np.cumsum(gp[c0:c1], axis=0, dtype=np.float32)
+        Gam = np.exp(gam)
+        GamC = Gam[-1]
+        Kt, Qt, Kh = kk * Gam, qq * Gam, kk * np.exp(gam[-1] - gam)
+        M, blocks = _anchored_tiles(kk, kk, gam, L, strict=True)
+        B, _ = _anchored_tiles(qq, kk, gam, L, strict=False)
+        A = bb[:, None] * M
+        Tm = np.linalg.inv(np.eye(L, dtype=np.float32) + A).astype(np.float32)
+        Vres = vv - Kt @ S
+        R = bb[:, None] * Vres
+        U = Tm @ R
+        o[c0:c1] = scale * (Qt @ S + B @ U)
+        starts.append(S)
+        fwd.append(dict(gam=gam, Gam=Gam, GamC=GamC, Kt=Kt, Qt=Qt, Kh=Kh, M=M, B=B, blocks=blocks, Tm=Tm,
+                        Vres=Vres, R=R, U=U))
+        S = GamC[:, None] * S + Kh.T @ U
+    S_final = S
+    dq, dkk, dgp = (np.zeros((T, dk), np.float32) for _ in range(3))
+    dvv, db = np.zeros((T, dv), np.float32), np.zeros(T, np.float32)
+    dS = np.zeros((dk, dv), np.float32) if dS_final is None else _f32(dS_final).copy()
+    for (c0, c1), S_in, f in reversed(list(zip(bounds, starts, fwd))):
+        kk, qq, bb, dO = k[c0:c1], q[c0:c1], beta[c0:c1], do[c0:c1]
+        Gam, GamC, Kt, Qt, Kh = f["Gam"], f["GamC"], f["Kt"], f["Qt"], f["Kh"]
+        M, B, Tm, Vres, R, U = f["M"], f["B"], f["Tm"], f["Vres"], f["R"], f["U"]
+        dU = scale * (B.T @ dO) + Kh @ dS
+        dB = scale * np.tril(dO @ U.T)
+        dQs = scale * (dO @ S_in.T)                   # through Qt S0
+        dS0 = scale * (Qt.T @ dO) + GamC[:, None] * dS
+        dKh = U @ dS.T
+        dgamC = GamC * np.sum(dS * S_in, axis=1)
+        dR = Tm.T @ dU
+        dTm = dU @ R.T
+        dA = np.tril(-(Tm.T @ dTm @ Tm.T), -1)
+        dvv[c0:c1] = bb[:, None] * dR
+        dbeta = np.sum(Vres * dR, axis=1) + np.sum(dA * M, axis=1)
+        dKs = -(bb[:, None] * dR) @ S_in.T            # through Kt S0
+        dS0 -= Kt.T @ (bb[:, None] * dR)
+        dM = bb[:, None] * dA
+        # M and B through the anchored blocks: row and column parts
+        Krow, Kcol, Qrow = (np.zeros_like(kk) for _ in range(3))
+        for j0, j1, row, col in f["blocks"]:
+            kc = kk[j0:j1] * col
+            Krow[j0:] += row * (dM[j0:, j0:j1] @ kc)
+            Qrow[j0:] += row * (dB[j0:, j0:j1] @ kc)
+            Kcol[j0:j1] += col * (dM[j0:, j0:j1].T @ (kk[j0:] * row) + dB[j0:, j0:j1].T @ (qq[j0:] * row))
+        dkk[c0:c1] = dKs * Gam + Krow + Kcol + dKh * np.exp(f["gam"][-1] - f["gam"])
+        dq[c0:c1] = dQs * Gam + Qrow
+        dgam = dKs * Kt + dQs * Qt - dKh * Kh + kk * Krow + qq * Qrow - kk * Kcol
+        dgam[-1] += dgamC + np.sum(dKh * Kh, axis=0)
+        dgp[c0:c1] = np.cumsum(dgam[::-1], axis=0, dtype=np.float32)[::-1]
+        db[c0:c1] = dbeta
+        dS = dS0
+    dg = np.where(g >= np.float32(g_min), dgp, np.float32(0))
+    out = (o, S_final, dq, dkk, dvv, dg, db, dS)
+    return tuple(np.asarray(x, dtype=np.float64) for x in out)

@@ -137,3 +137,30 @@ def test_bf16_operand_error_budget(oracle):
             for n, a, b in zip(NAMES, got[2:], ref)}
     assert all(e <= 1e-2 for e in errs.values()), errs
     assert max(errs.values()) >= 1e-4, errs  # the rounding is really applied
+
+
+@pytest.mark.parametrize("floor_chunks", [False, True])
+def test_f32_anchored_matches_f64(oracle, floor_chunks):
+    """The fp32 chunk-form reverse pass with 16-token block anchoring against
+    the fp64 reverse mode, d = 128 over 200 tokens (a partial last chunk).  With
+    two chunks held at the floor (gamma down to -320 inside a chunk, where
+    1/e^gamma overflows fp32) everything stays finite and within 2e-5 (fp32
+    rounding; measured about 1e-6)."""
+    rng = np.random.default_rng(29 + floor_chunks)
+    q, k, v, g, beta, cu, S0, do, dSf = _case(rng, [200], 1, 128, 128, below=0.0, at=0.0)
+    if floor_chunks:
+        g[0:64] = G_MIN
+        g[128:192] = G_MIN - 0.5
+        gam = np.cumsum(np.maximum(g[0:64, 0], G_MIN), axis=0).astype(np.float32)
+        with np.errstate(over="ignore", divide="ignore"):
+            assert not np.all(np.isfinite(np.float32(1.0) / np.exp(gam)))  # the naive factor overflows
+    h = 0
+    got = chunk_reverse.chunk_form_backward_head_f32(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], do[:, h],
+                                                     S0[0, h], dSf[0, h], C=64, scale=0.8)
+    ref = chunk_reverse.chunk_form_backward_head(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], do[:, h],
+                                                 S0[0, h], dSf[0, h], C=64, scale=0.8)
+    for name, a, b in zip(("o", "S_final") + NAMES, got, ref):
+        assert np.all(np.isfinite(a)), name
+        assert _rel(a, b) <= 2e-5, f"{name}: {_rel(a, b):.2e}"
+    if floor_chunks:
+        assert np.all(got[5][128:192] == 0.0)  # below the floor: no gradient
