@@ -77,3 +77,25 @@ def test_both_arms_share_the_headline_config():
     assert c1["workload"] == synth.PREFILL_32K.name and c1["T"] == 32768 and c1["H"] == 96
     assert c1["parallelism"] == "replicas x1" and c4["parallelism"] == "replicas x4"
     assert {k: v for k, v in c1.items() if k != "parallelism"} == {k: v for k, v in c4.items() if k != "parallelism"}
+
+
+def test_traffic_of_a_changed_kernel_is_not_reported(tmp_path, monkeypatch):
+    """`traffic` comes from the committed ncu summary only while the kernel's
+    source is the one captured; it scales with the tokens of a launch."""
+    import json
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    root = tmp_path / "r"
+    (root / "profiles").mkdir(parents=True)
+    (root / "k.cu").write_text("kernel source\n")
+    import hashlib
+    sha = hashlib.sha256(b"kernel source\n").hexdigest()[:16]
+    rec = {"k": {"source": "k.cu", "source_sha256_16": sha, "captured_T": 1000, "traffic_bytes_captured": 5e6}}
+    (root / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.kernel_traffic("k", 4000) == 2e7
+    assert bench.kernel_traffic("missing", 4000) is None
+    (root / "k.cu").write_text("kernel source, changed\n")
+    assert bench.kernel_traffic("k", 4000) is None
+    shutil.rmtree(root)
