@@ -164,3 +164,20 @@ def test_f32_anchored_matches_f64(oracle, floor_chunks):
         assert _rel(a, b) <= 2e-5, f"{name}: {_rel(a, b):.2e}"
     if floor_chunks:
         assert np.all(got[5][128:192] == 0.0)  # below the floor: no gradient
+
+
+def test_bf16_rounding_helper_matches_the_pages_example():
+    """The bf16 rounding the error-budget test applies reproduces the pages'
+    example (tests/golden/bf16_rounding_example.txt): 256.5 rounds to 256 in
+    bf16, so the fp32 difference with 256 drops from 0.5 to 0; values bf16
+    holds exactly are kept and ties go to even."""
+    from conftest import read_golden
+    rows = {r[0]: [float(x) for x in r[1:]] for r in read_golden("bf16_rounding_example.txt")}
+    a, b, diff = rows["fp32"]
+    assert np.float32(a) - np.float32(b) == diff
+    ra, rb, rdiff = rows["bf16"]
+    assert _bf16(np.array([a]))[0] == ra and _bf16(np.array([b]))[0] == rb
+    assert np.float32(_bf16(np.array([a]))[0]) - np.float32(_bf16(np.array([b]))[0]) == rdiff
+    # exact values stay; the tie 1 + 2^-8 goes to even (1), 1 + 3 * 2^-8 to 1 + 2^-6
+    assert _bf16(np.array([1.5, -3.25, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8])).tolist() == [1.5, -3.25, 1.0,
+                                                                                         1 + 2.0 ** -6]
