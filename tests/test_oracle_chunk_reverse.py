@@ -181,3 +181,35 @@ def test_bf16_rounding_helper_matches_the_pages_example():
     # exact values stay; the tie 1 + 2^-8 goes to even (1), 1 + 3 * 2^-8 to 1 + 2^-6
     assert _bf16(np.array([1.5, -3.25, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8])).tolist() == [1.5, -3.25, 1.0,
                                                                                          1 + 2.0 ** -6]
+
+
+def test_state_gradient_chain_composes_over_segments(oracle):
+    """The state-gradient chain is affine in the gradient at a segment's end:
+    dS_start = M^T dS_end + r, with M the forward transition of the segment
+    (oracle.segment_transition) and r the chain from dS_end = 0.  Composing
+    (M^T, r) over segments, last to first, gives the chain's value at every
+    segment start, the backward counterpart of the forward's context-parallel
+    composition; each segment can then be reversed on its own."""
+    rng = np.random.default_rng(31)
+    T, seg, C = 192, 64, 32
+    q, k, v, g, beta, cu, S0, do, dSf = _case(rng, [T], 1, 16, 8, below=0.05, at=0.02)
+    h = 0
+    args = lambda a, b: (q[a:b, h], k[a:b, h], v[a:b, h], g[a:b, h], beta[a:b, h], do[a:b, h])
+    _, S_in, dS_C, dS0 = chunk_reverse.state_gradient_chain(*args(0, T), S0=S0[0, h], dS_final=dSf[0, h], C=C,
+                                                            scale=0.6)
+    # the chain's value at each chunk start is dS_C of the chunk before (dS0 at 0)
+    at_start = {0: dS0}
+    for c in range(1, T // C):
+        at_start[c * C] = dS_C[c - 1]
+    bounds = [(a, a + seg) for a in range(0, T, seg)]
+    maps = []
+    for a, b in bounds:
+        M, _ = oracle.segment_transition(k[a:b], v[a:b], g[a:b], beta[a:b])
+        # the segment's own start state (from the forward), then its chain from zero
+        Sa = S_in[a // C]
+        r = chunk_reverse.state_gradient_chain(*args(a, b), S0=Sa, dS_final=None, C=C, scale=0.6)[3]
+        maps.append((M[h], r))
+    dS = dSf[0, h]
+    for (a, b), (M, r) in reversed(list(zip(bounds, maps))):
+        dS = M.T @ dS + r
+        assert _rel(dS, at_start[a]) <= 1e-12, a
