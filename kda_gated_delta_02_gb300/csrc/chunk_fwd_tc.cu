@@ -211,6 +211,15 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
     uint32_t phase = 0;
     float beta_next = 0.f;
     uint32_t pending = 0;  // bulk copies issued for the chunk after the current one
+    // waits of the current chunk that gave up: bits 0-3 the product barriers
+    // bar0 + 8 i, bit 4 the q/k/g copies, bit 5 the v copies
+    uint32_t stuck = 0;
+    auto wait_or_mark = [&](uint32_t bar, uint32_t bit) {
+        if (!umma::mbar_wait(bar, phase, WAIT_LIMIT)) {
+            timed_out = true;
+            stuck |= bit;
+        }
+    };
     if (t0 < t1) {
         issue_qkg(t0);
         issue_v(t0);
@@ -221,8 +230,8 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
         const int Lc = min(CH, t1 - tc);
         if (tid < CH) sBeta[tid] = beta_next;
         pending = 0;
-        timed_out |= !umma::mbar_wait(bar_qkg, phase, WAIT_LIMIT);
-        if (has_v) timed_out |= !umma::mbar_wait(bar_v, phase, WAIT_LIMIT);
+        wait_or_mark(bar_qkg, 16u);
+        if (has_v) wait_or_mark(bar_v, 32u);
         if (Lc < CH) {  // last chunk of the segment: rows past its end are not ours
             for (int idx = tid; idx < (CH - Lc) * 16; idx += NT) {
                 const int r = Lc + (idx >> 4), c = idx & 15;
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             issue_qkg(tc + CH);
             pending |= 1u;
         }
-        timed_out |= !umma::mbar_wait(bar0 + 0, phase, WAIT_LIMIT);
+        wait_or_mark(bar0 + 0, 1u);
         umma::fence_after();
 
         // S^T (rows of this thread's TMEM lane, columns 32 cg ..) as the bf16
@@ -584,7 +593,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
                 }
             }
         }
-        timed_out |= !umma::mbar_wait(bar0 + 8, phase, WAIT_LIMIT);
+        wait_or_mark(bar0 + 8, 2u);
         umma::fence_after();
         if (tc + CH < t1) {  // V and b consumed: prefetch the next chunk's
             issue_v(tc + CH);
@@ -621,7 +630,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             }
             umma::commit(bar0 + 16);
         }
-        timed_out |= !umma::mbar_wait(bar0 + 16, phase, WAIT_LIMIT);
+        wait_or_mark(bar0 + 16, 4u);
         umma::fence_after();
 
         // ------------------------------------------------------------ step 9: U^T (bf16) operand
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
             }
             umma::commit(bar0 + 24);
         }
-        timed_out |= !umma::mbar_wait(bar0 + 24, phase, WAIT_LIMIT);
+        wait_or_mark(bar0 + 24, 8u);
         umma::fence_after();
         // checkpoint: the state after token (tc + Lc) when that position of the
         // sequence is a multiple of ckpt_every (S^T lane = value column)
@@ -699,7 +708,12 @@ __global__ void __launch_bounds__(NT, 1) kda_chunk_tc_kernel(const __grid_consta
 
     if (timed_out) {
         if (tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
-        // let copies already issued for the next chunk land before leaving
+        // let copies still in flight land and products still running finish
+        // before the shared and tensor memory are released
+        for (int i = 0; i < 4; ++i)
+            if (stuck & (1u << i)) umma::mbar_wait(bar0 + 8 * i, phase, WAIT_LIMIT);
+        if (stuck & 16u) umma::mbar_wait(bar_qkg, phase, WAIT_LIMIT);
+        if (stuck & 32u) umma::mbar_wait(bar_v, phase, WAIT_LIMIT);
         if (pending & 1u) umma::mbar_wait(bar_qkg, phase ^ 1u, WAIT_LIMIT);
         if ((pending & 2u) && has_v) umma::mbar_wait(bar_v, phase ^ 1u, WAIT_LIMIT);
     } else {

@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
     }
     bool ok = umma::mbar_wait(bar_ab, it & 1u, WAIT_LIMIT);
     ok = __syncthreads_and(ok) != 0;
+    const bool w_issued = ok;  // the W product is issued exactly when the A/B product landed
+    const uint32_t par = it & 1u;
     umma::fence_after();
 
     if (ok) {
@@ -545,7 +547,9 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
     umma::fence_before();
     __syncthreads();
     ++it;
-    if (!ok) {  // uniform: leave with the tensor memory and barriers idle
+    if (!ok) {  // uniform: leave once the products still in flight are done with tensor memory
+        umma::mbar_wait(bar_ab, par, WAIT_LIMIT);
+        if (w_issued) umma::mbar_wait(bar_w, par, WAIT_LIMIT);
         alive = false;
         break;
     }
@@ -671,8 +675,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
     };
 
     bool timed_out = false;
-    int pend_b = -1;  // buffer with a copy in flight for the chunk after the current one
+    int pend_b = -1;  // buffer with a copy in flight (the next chunk's, or one whose wait gave up)
     uint32_t pend_ph = 0;
+    int pend_m = -1;  // tensor-core products whose completion wait gave up (0: U, 1: O / state)
+    uint32_t pend_mph = 0;
     if (jb < je) {
         issue(jb, 0);
         pend_b = 0;
@@ -684,8 +690,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pm = (uint32_t)it & 1u;
         const int tc = t0 + CH * j, Lc = min(CH, t1 - tc);
         const uint32_t bb = W_BUF + (uint32_t)b * W_BUFSTRIDE;
-        timed_out |= !umma::mbar_wait(bar0 + 8 * b, ph, WAIT_LIMIT);
-        pend_b = -1;
+        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, WAIT_LIMIT);
+        timed_out |= !landed;
+        pend_b = landed ? -1 : b;  // a copy that has not landed is still in flight
+        pend_ph = ph;
         if (j + 1 < je && !timed_out) {
             issue(j + 1, b ^ 1);
             pend_b = b ^ 1;
@@ -761,7 +769,11 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                 }
             }
         }
-        timed_out |= !umma::mbar_wait(bar_u, pm, WAIT_LIMIT);
+        if (!umma::mbar_wait(bar_u, pm, WAIT_LIMIT)) {
+            timed_out = true;
+            pend_m = 0;
+            pend_mph = pm;
+        }
         umma::fence_after();
 
         // ------------------------------------------------------------ U^T (bf16) operand
@@ -799,7 +811,11 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
             }
             umma::commit(bar_o);
         }
-        timed_out |= !umma::mbar_wait(bar_o, pm, WAIT_LIMIT);
+        if (!umma::mbar_wait(bar_o, pm, WAIT_LIMIT)) {
+            timed_out = true;
+            pend_m = 1;
+            pend_mph = pm;
+        }
         umma::fence_after();
         // checkpoint: the state after token (tc + Lc) when that position of the
         // sequence is a multiple of ckpt_every (S^T lane = value column)
@@ -850,8 +866,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
 
     if (timed_out) {
         if (tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
-        // let a copy already issued for the next chunk land before leaving
+        // let a copy still in flight land and products still running finish
+        // before the shared and tensor memory are released
         if (pend_b >= 0) umma::mbar_wait(bar0 + 8 * pend_b, pend_ph, WAIT_LIMIT);
+        if (pend_m >= 0) umma::mbar_wait(pend_m ? bar_o : bar_u, pend_mph, WAIT_LIMIT);
     } else {
         // ------------------------------------------------------------ state out
         float *dst = nullptr;

@@ -351,6 +351,8 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     // ---------------------------------------------------------------- batch 1
     // thread 0 issues the products with S0 once its tile has landed; thread 32
     // issues X KR^T at once (two commits to one barrier of count 2)
+    const bool b1 = ok;  // uniform here: thread 32's part of batch 1 is issued
+    bool b2 = false;     // batch 2 issued (thread 0)
     if (tid == 0) {
         ok = umma::mbar_wait(bar0, 0, WAIT_LIMIT) && ok;
         if (ok) {
@@ -472,6 +474,7 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         umma::mma(tmem + TM_S, kdh, udl, ids, 1u);
         umma::mma(tmem + TM_S, kdl, udh, ids, 1u);
         umma::commit(bar0 + 24);
+        b2 = true;
     }
     // outputs while the state product runs: O = scale (QX S0 + B U) in fp32
     float o[HT];
@@ -551,6 +554,11 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         report_status(p.status, KDA_STATUS_TIMEOUT);
         umma::mbar_wait(bar_raw, 0, WAIT_LIMIT);  // let the copies land before leaving (bounded)
         umma::mbar_wait(bar0, 0, WAIT_LIMIT);
+        // and the products issued finish before tensor memory is freed (when
+        // this thread's own part of batch 1 was never issued the barrier stays
+        // one commit short and the bounded wait outlasts thread 32's product)
+        if (b1) umma::mbar_wait(bar0 + 8, 0, WAIT_LIMIT);
+        if (b2) umma::mbar_wait(bar0 + 24, 0, WAIT_LIMIT);
     }
     if (warp == 0) umma::tmem_dealloc(tmem, TMEM_COLS);
     if (tid == 0 && ok) umma::bulk_wait_read();
