@@ -407,6 +407,53 @@ def test_conv_identity_and_shift_pin_tail_order(oracle):
                     np.testing.assert_allclose(o[r, j, h], ref, rtol=1e-12, atol=1e-12)
 
 
+def test_conv_silu_matches_library_silu(oracle):
+    """The short-conv activation ("Noyaux d'inference" section 1, "La fusion":
+    the pages name the short convolution but no activation; SiLU is the reading
+    adopted, conv_act = 1) against torch.nn.functional.silu, a library routine.
+
+    q branch: identity taps, beta = 0 and g = 0 (the state stays S0 = I),
+    w_o = 1, so every output row is RMSNorm(normalise(silu(q_raw))).
+    k and v branches: random taps over the cached tail, S0 = 0, beta = 1 and
+    g = 0 with no accepted rows, so the state written back after the bonus
+    token is normalise(silu(conv(k))) silu(conv(v))^T -- conv first, then the
+    activation, then the norm."""
+    torch = pytest.importorskip("torch")
+    silu = lambda x: torch.nn.functional.silu(torch.from_numpy(np.asarray(x, dtype=np.float64))).numpy()
+    rng = np.random.default_rng(45)
+    R, H, d, W, Wd = 3, 2, 5, 4, 7
+    Cq = H * 3 * d
+    inp = decode_inputs(rng, R, H, d, d, accepted=[2, 0, 7], state_std=1.0)
+    inp["state"] = np.broadcast_to(np.eye(d), (R, H, d, d)).copy()
+    inp["cached_b"][:] = inp["new_b"][:] = -800.0  # logistic -> 0 exactly
+    inp["cached_g"][:] = inp["new_g"][:] = -800.0  # softplus -> 0 exactly, g = 0
+    inp["out_w"] = np.ones(d)
+    cw = np.tile(np.array([0, 0, 0, 1.0]), (Cq, 1))
+    _, _, o, bad = oracle.decode_verify(**{**inp, "conv_w": cw}, conv_act=1, eps_out=0.0)
+    assert bad == 0
+    for r in range(R):
+        for j in range(Wd + 1):
+            for h in range(H):
+                y = silu(inp["new_qkv"][r, j, h * d:(h + 1) * d])
+                qh = y / np.sqrt(np.sum(y ** 2) + 1e-6)
+                np.testing.assert_allclose(o[r, j, h], qh / np.sqrt(np.mean(qh ** 2)), rtol=1e-12)
+
+    inp = decode_inputs(rng, R, H, d, d, accepted=[0, 0, 0], state_std=1.0)
+    inp["state"][:] = 0.0
+    inp["new_b"][:] = 800.0  # logistic -> 1 exactly
+    inp["new_g"][:] = -800.0
+    st, _, _, bad = oracle.decode_verify(**inp, conv_act=1)
+    assert bad == 0
+    for r in range(R):
+        rows = np.concatenate([inp["tail"][r], inp["new_qkv"][r, :1]], axis=0)  # W rows, oldest first
+        conv = np.einsum("jc,cj->c", rows, inp["conv_w"])
+        for h in range(H):
+            kk = silu(conv[H * d + h * d:H * d + (h + 1) * d])
+            kk = kk / np.sqrt(np.sum(kk ** 2) + 1e-6)
+            vv = silu(conv[2 * H * d + h * d:2 * H * d + (h + 1) * d])
+            np.testing.assert_allclose(st[r, h], np.outer(kk, vv), rtol=1e-12, atol=1e-15)
+
+
 def test_gates_match_library_functions(oracle):
     """The written-back state exposes the gates: with S0 = 0 one bonus token
     gives S = b k v^T (b = logistic(b_raw)); with b = 0, S = Diag(e^g) S0 where
