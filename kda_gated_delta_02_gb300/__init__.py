@@ -9,6 +9,7 @@ calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -125,6 +126,15 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on(stream):
+    """Allocate the tensors a call owns on the stream it launches on.  The
+    caching allocator hands a freed block to the next allocation on the stream
+    that allocated it without waiting for other streams, so a workspace
+    allocated on the current stream but used by kernels on `stream` could be
+    reused by the current stream while those kernels still run."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def _in_dtype(t):
     if t.dtype == torch.bfloat16:
         return DTYPE_BF16
@@ -192,30 +202,31 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
         if ckpt is None or ckpt.dim() != 5:
             raise KDAError("ckpt must be an f32 tensor [N, K, H, dk, dv]")
         _expect(ckpt, "ckpt", torch.float32, (N, ckpt.shape[1], H, dk, dv))
-    lib = load_library()
-    if out is None:
-        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
-    if final_state is None and output_final_state:
-        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    if prep and q.dtype == torch.bfloat16:
-        ws_bytes = chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
-    else:
-        ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
-    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
-              _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
-              _in_dtype(q), int(cp_mode), int(segment_len),
-              _ptr(workspace) if ws_bytes else None,
-              ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0))
-    if ckpt_every:
-        rc = lib.kda_chunk_fwd_ckpt(*common, int(ckpt_every), int(ckpt.shape[1]), _ptr(ckpt), _ptr(status),
-                                    _stream(stream))
-        _check(rc, "kda_chunk_fwd_ckpt")
-    else:
-        rc = lib.kda_chunk_fwd(*common, _ptr(status), _stream(stream))
-        _check(rc, "kda_chunk_fwd")
-    return out, final_state
+    with _on(stream):
+        lib = load_library()
+        if out is None:
+            out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+        if final_state is None and output_final_state:
+            final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+        if prep and q.dtype == torch.bfloat16:
+            ws_bytes = chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+        else:
+            ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+        if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                  _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
+                  _in_dtype(q), int(cp_mode), int(segment_len),
+                  _ptr(workspace) if ws_bytes else None,
+                  ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0))
+        if ckpt_every:
+            rc = lib.kda_chunk_fwd_ckpt(*common, int(ckpt_every), int(ckpt.shape[1]), _ptr(ckpt), _ptr(status),
+                                        _stream(stream))
+            _check(rc, "kda_chunk_fwd_ckpt")
+        else:
+            rc = lib.kda_chunk_fwd(*common, _ptr(status), _stream(stream))
+            _check(rc, "kda_chunk_fwd")
+        return out, final_state
 
 
 def segment_transition(k, v, g, beta, segment_len, g_min=-5.0, stream=None):
@@ -230,14 +241,15 @@ def segment_transition(k, v, g, beta, segment_len, g_min=-5.0, stream=None):
     _expect(beta, "beta", torch.float32, (T, H))
     if int(segment_len) < 1:
         raise KDAError("segment_len must be positive")
-    lib = load_library()
-    P = (T + segment_len - 1) // segment_len
-    M = torch.empty((P, H, dk, dk), dtype=torch.float32, device=k.device)
-    Nm = torch.empty((P, H, dk, dv), dtype=torch.float32, device=k.device)
-    rc = lib.kda_segment_transition(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), T, H, dk, dv, int(segment_len),
-                                    _ptr(M), _ptr(Nm), float(g_min), _in_dtype(k), _stream(stream))
-    _check(rc, "kda_segment_transition")
-    return M, Nm
+    with _on(stream):
+        lib = load_library()
+        P = (T + segment_len - 1) // segment_len
+        M = torch.empty((P, H, dk, dk), dtype=torch.float32, device=k.device)
+        Nm = torch.empty((P, H, dk, dv), dtype=torch.float32, device=k.device)
+        rc = lib.kda_segment_transition(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), T, H, dk, dv, int(segment_len),
+                                        _ptr(M), _ptr(Nm), float(g_min), _in_dtype(k), _stream(stream))
+        _check(rc, "kda_segment_transition")
+        return M, Nm
 
 
 def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
@@ -248,13 +260,14 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
     _expect(Nm, "Nm", torch.float32, (P, H, dk, dv))
     _expect(M, "M", torch.float32, (P, H, dk, dk))
     _expect(S0, "S0", torch.float32, (H, dk, dv))
-    lib = load_library()
-    S_in = torch.empty_like(Nm) if want_segment_states else None
-    Sf = torch.empty((H, dk, dv), dtype=torch.float32, device=Nm.device)
-    rc = lib.kda_segment_compose(_ptr(M), _ptr(Nm), _ptr(S0), _ptr(S_in), _ptr(Sf), P, H, dk, dv,
-                                 _stream(stream))
-    _check(rc, "kda_segment_compose")
-    return S_in, Sf
+    with _on(stream):
+        lib = load_library()
+        S_in = torch.empty_like(Nm) if want_segment_states else None
+        Sf = torch.empty((H, dk, dv), dtype=torch.float32, device=Nm.device)
+        rc = lib.kda_segment_compose(_ptr(M), _ptr(Nm), _ptr(S0), _ptr(S_in), _ptr(Sf), P, H, dk, dv,
+                                     _stream(stream))
+        _check(rc, "kda_segment_compose")
+        return S_in, Sf
 
 
 # kernel families of kda_kernel_timing_stop, in KDA_KERNEL_* order
@@ -273,22 +286,23 @@ def chunk_fwd_host(q, k, v, g, beta, cu_seqlens, initial_state=None, output_fina
     T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state, cu_any_int=True)
     _expect(out, "out", q.dtype, (T, H, dv))
     _expect(final_state, "final_state", torch.float32, (N, H, dk, dv))
-    lib = load_library()
-    if out is None:
-        out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
-    if final_state is None and output_final_state:
-        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
-    dt = _in_dtype(q)
-    need = int(lib.kda_chunk_fwd_host_workspace_size(N, T, H, dk, dv, dt, int(pieces)))
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
-    cu = cu_seqlens.to(torch.int32).contiguous()
-    rc = lib.kda_chunk_fwd_host(_hptr(q), _hptr(k), _hptr(v), _hptr(g), _hptr(beta), _hptr(cu), N, T, H, dk, dv,
-                                _hptr(initial_state), _hptr(final_state), _hptr(out), float(scale), float(g_min), dt,
-                                int(pieces), _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
-                                _ptr(status), _stream(stream))
-    _check(rc, "kda_chunk_fwd_host")
-    return out, final_state
+    with _on(stream):
+        lib = load_library()
+        if out is None:
+            out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
+        if final_state is None and output_final_state:
+            final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+        dt = _in_dtype(q)
+        need = int(lib.kda_chunk_fwd_host_workspace_size(N, T, H, dk, dv, dt, int(pieces)))
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        cu = cu_seqlens.to(torch.int32).contiguous()
+        rc = lib.kda_chunk_fwd_host(_hptr(q), _hptr(k), _hptr(v), _hptr(g), _hptr(beta), _hptr(cu), N, T, H, dk, dv,
+                                    _hptr(initial_state), _hptr(final_state), _hptr(out), float(scale), float(g_min), dt,
+                                    int(pieces), _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                    _ptr(status), _stream(stream))
+        _check(rc, "kda_chunk_fwd_host")
+        return out, final_state
 
 
 def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=None, scale=1.0, g_min=-5.0,
@@ -299,25 +313,26 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=Non
     T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
     _expect(do, "do", q.dtype, (T, H, dv))
     _expect(dS_final, "dS_final", torch.float32, (N, H, dk, dv))
-    lib = load_library()
-    dev = q.device
-    f32 = torch.float32
-    dq = torch.empty((T, H, dk), dtype=f32, device=dev)
-    dkk = torch.empty((T, H, dk), dtype=f32, device=dev)
-    dvv = torch.empty((T, H, dv), dtype=f32, device=dev)
-    dg = torch.empty((T, H, dk), dtype=f32, device=dev)
-    db = torch.empty((T, H), dtype=f32, device=dev)
-    dS0 = torch.empty((N, H, dk, dv), dtype=f32, device=dev) if want_dS0 else None
-    need = int(lib.kda_chunk_bwd_workspace_size(N, T, H, dk, dv))
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
-                           _ptr(initial_state), _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
-                           _ptr(db), _ptr(dS0), float(scale), float(g_min), _in_dtype(q), _ptr(workspace),
-                           ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(status),
-                           _stream(stream))
-    _check(rc, "kda_chunk_bwd")
-    return dq, dkk, dvv, dg, db, dS0
+    with _on(stream):
+        lib = load_library()
+        dev = q.device
+        f32 = torch.float32
+        dq = torch.empty((T, H, dk), dtype=f32, device=dev)
+        dkk = torch.empty((T, H, dk), dtype=f32, device=dev)
+        dvv = torch.empty((T, H, dv), dtype=f32, device=dev)
+        dg = torch.empty((T, H, dk), dtype=f32, device=dev)
+        db = torch.empty((T, H), dtype=f32, device=dev)
+        dS0 = torch.empty((N, H, dk, dv), dtype=f32, device=dev) if want_dS0 else None
+        need = int(lib.kda_chunk_bwd_workspace_size(N, T, H, dk, dv))
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                               _ptr(initial_state), _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
+                               _ptr(db), _ptr(dS0), float(scale), float(g_min), _in_dtype(q), _ptr(workspace),
+                               ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(status),
+                               _stream(stream))
+        _check(rc, "kda_chunk_bwd")
+        return dq, dkk, dvv, dg, db, dS0
 
 
 def kernel_timing_start():
@@ -364,21 +379,22 @@ def decode_verify_replay(state, conv_tail, conv_w, cached_qkv, cached_g, cached_
     _expect(out_norm_w, "out_norm_w", torch.float32, (dv,))
     _expect(out, "out", bf, (R, Wd + 1, H, dv))
     _expect(draft_len, "draft_len", torch.int32, (R,))
-    lib = load_library()
-    if out is None:
-        out = torch.empty((R, Wd + 1, H, dv), dtype=torch.bfloat16, device=state.device)
-    if draft_len is not None:
-        rc = lib.kda_decode_verify_replay_ragged(
-            _ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv), _ptr(cached_g), _ptr(cached_beta),
-            _ptr(accepted_len), _ptr(draft_len), _ptr(new_qkv), _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w),
-            _ptr(out), R, H, dk, dv, W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
-            int(conv_act), _ptr(status), _stream(stream))
-        _check(rc, "kda_decode_verify_replay_ragged")
+    with _on(stream):
+        lib = load_library()
+        if out is None:
+            out = torch.empty((R, Wd + 1, H, dv), dtype=torch.bfloat16, device=state.device)
+        if draft_len is not None:
+            rc = lib.kda_decode_verify_replay_ragged(
+                _ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv), _ptr(cached_g), _ptr(cached_beta),
+                _ptr(accepted_len), _ptr(draft_len), _ptr(new_qkv), _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w),
+                _ptr(out), R, H, dk, dv, W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
+                int(conv_act), _ptr(status), _stream(stream))
+            _check(rc, "kda_decode_verify_replay_ragged")
+            return out
+        rc = lib.kda_decode_verify_replay(_ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv),
+                                          _ptr(cached_g), _ptr(cached_beta), _ptr(accepted_len), _ptr(new_qkv),
+                                          _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w), _ptr(out), R, H, dk, dv,
+                                          W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
+                                          int(conv_act), _ptr(status), _stream(stream))
+        _check(rc, "kda_decode_verify_replay")
         return out
-    rc = lib.kda_decode_verify_replay(_ptr(state), _ptr(conv_tail), _ptr(conv_w), _ptr(cached_qkv),
-                                      _ptr(cached_g), _ptr(cached_beta), _ptr(accepted_len), _ptr(new_qkv),
-                                      _ptr(new_g), _ptr(new_beta), _ptr(out_norm_w), _ptr(out), R, H, dk, dv,
-                                      W, Wd, float(scale), float(g_min), float(eps_in), float(eps_out),
-                                      int(conv_act), _ptr(status), _stream(stream))
-    _check(rc, "kda_decode_verify_replay")
-    return out

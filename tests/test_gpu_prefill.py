@@ -273,3 +273,25 @@ def test_checkpoints_match_oracle_prefixes(kda, oracle, cfg):
                                    np.array([0, P], dtype=np.int32), S0=to64(S0[n:n + 1]))
             e = normwise_err(ck[n, kq][None], Sf, head_axis=1)
             assert e <= STATE_TOL, f"sequence {n} checkpoint {kq}: state error {e:.3e}"
+
+
+def test_side_stream_call_keeps_its_workspace(kda):
+    """A call launched on a side stream allocates its outputs and workspace on
+    that stream: right after it returns, the current stream allocates and
+    overwrites blocks of the workspace's size while the side-stream kernels may
+    still run, and the results still equal those of a call on the current
+    stream, bit for bit."""
+    inp = make_inputs([2048, 1500], 8, 128, 128, s0=True, seed=77)
+    args = (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"])
+    o_ref, S_ref = kda.chunk_fwd(*args, initial_state=inp["S0"])
+    torch.cuda.synchronize()
+    N, T, H = 2, 3548, 8
+    ws = kda.chunk_fwd_prep_workspace_size(N, T, H, 128, 128)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        o, S = kda.chunk_fwd(*args, initial_state=inp["S0"], stream=side)
+        junk = [torch.full((ws,), 0xFF, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        del junk
+        torch.cuda.current_stream().wait_stream(side)
+        assert torch.equal(o, o_ref) and torch.equal(S, S_ref)
