@@ -244,7 +244,7 @@ def run_reference(args):
 
 
 def verify_kernel_name():
-    return "kda_verify_kernel<128>" if os.environ.get("KDA_VERIFY_TC", "1") == "0" else "kda_verify_tc_kernel"
+    return "kda_verify_tc_kernel"
 
 
 def decode_workload(synth):
@@ -372,6 +372,18 @@ def main(argv=None):
             rec["traffic"] = kernel_traffic(name, tokens)
         kernels[name] = rec
     dom = max((n for n in kernels if n in KERNEL_BYTES_PER_TOKHEAD), key=lambda n: kernels[n]["share_of_step"])
+    # the roofline of the dominant kernel counts the path's own 1,540 B per
+    # token-head for the token-heads one launch covers (what the method must
+    # move), not the kernel's own reads and writes of intermediates
+    dom_tokens = T / kernels[dom]["launches_per_step"]
+    dom_algo = dom_tokens * H * BYTES_PER_TOKHEAD
+    dom_gbs = dom_algo / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e9
+    # DRAM bytes per step (ncu, committed captures) against the path's bytes
+    step_traffic = 0.0
+    for name, rec in kernels.items():
+        if name in KERNEL_BYTES_PER_TOKHEAD:
+            step_traffic = None if (step_traffic is None or rec["traffic"] is None) else \
+                step_traffic + rec["traffic"] * rec["launches_per_step"]
     out["prefill"] = {"ms": ms, "tok_s": tok_s}
 
     # the same launch emitting the state every 4096 tokens (8 checkpoints per head)
@@ -470,14 +482,17 @@ def main(argv=None):
         # (2 x d x 4) plus the inputs and gradients
         d2 = w.dk * w.dv
         flops = T * H * 2.0 * (3 * d2 + 2 * d2 + 8 * d2)
-        io = T * H * (4 * 128 * 2 + 128 * 4 + 4 + 3 * 128 * 4 + 128 * 4 + 4)  # q,k,v,do bf16 + g,beta in; dq,dk,dv,dg,dbeta out
-        scratch = T * H * 2.0 * (d2 + w.dv) * 4
+        # algorithmic I/O per token-head: q, k, v, do bf16 + g, beta in; dq, dk, dv, dg, dbeta fp32 out
+        io = T * H * (4 * 128 * 2 + 128 * 4 + 4 + 3 * 128 * 4 + 128 * 4 + 4)
+        scratch = T * H * 2.0 * (d2 + w.dv) * 4  # the kernel's own recomputed states and w, written and read
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 flop x max SM clock, TFLOP/s
         out["backward"] = {"workload": w.name + " backward (dq, dk, dv, dg, dbeta)", "ms": bms,
                            "tok_s": ws * T / (bms * 1e-3), "fp32_tflops": flops / (bms * 1e-3) / 1e12,
                            "fp32_peak_tflops": fp32_peak, "frac_alu": flops / (bms * 1e-3) / 1e12 / fp32_peak,
-                           "bytes_gbs": (io + scratch) / (bms * 1e-3) / 1e9,
-                           "frac_hbm": (io + scratch) / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "algorithmic_bytes_per_step": io,
+                           "frac_hbm": io / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "kernel_own_bytes_gbs": (io + scratch) / (bms * 1e-3) / 1e9,
+                           "kernel_own_frac_hbm": (io + scratch) / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "ratio_to_forward": bms / ms}
         launches += sum(v["launches"] for v in kb.values())
         del inp, dout, bws
@@ -514,8 +529,7 @@ def main(argv=None):
     # ------------------------------------------------------------ single-token decode (window 0)
     if "decode" in only:
         dw = decode_workload(synth)
-        decode_kernel = ("kda_decode_token_kernel<128>" if os.environ.get("KDA_DECODE_TOKEN", "1") != "0"
-                         else verify_kernel_name())
+        decode_kernel = "kda_decode_token_kernel<128>"
         d = synth.make_decode(dw, device="cuda", accepted=[0] * dw.R)
         st, tl = d["state"].clone(), d["tail"].clone()
         od = torch.empty((dw.R, 1, dw.H, dw.dv), dtype=torch.bfloat16, device="cuda")
@@ -603,13 +617,19 @@ def main(argv=None):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded torch generator, shapes of the pages' workloads)",
             "config": prefill_config(ws),
-            "roofline": {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": kernels[dom]["frac_hbm"], "traffic": kernels[dom]["traffic"],
+            "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"], "traffic": kernels[dom]["traffic"],
                          "peak_source": peaks["source"], "kernel": dom,
-                         "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"],
-                         "ms_per_launch": kernels[dom]["ms_per_launch"]},
+                         "algorithmic_bytes_per_launch": dom_algo,
+                         "algorithmic_bytes_per_tokhead": BYTES_PER_TOKHEAD,
+                         "tokheads_per_launch": dom_tokens * H,
+                         "ms_per_launch": kernels[dom]["ms_per_launch"],
+                         "kernel_own_bytes_per_launch": kernels[dom]["bytes_per_launch"],
+                         "kernel_own_frac": kernels[dom]["frac_hbm"]},
             "path_roofline": {"bound": "hbm", "achieved": path_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": path_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_step": path_bytes,
+                              "dram_traffic_per_step": step_traffic,
+                              "traffic_ratio": None if step_traffic is None else step_traffic / path_bytes,
                               "tensor_tflops": tflops, "tensor_peak_tflops": peaks["bf16_tflops"],
                               "tensor_frac": tflops / peaks["bf16_tflops"]},
             "kernels": kernels,

@@ -164,7 +164,7 @@ size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_
  * a slot list (8 bytes per 64-token chunk slot; floor(T / 64) + units slots,
  * units = sequences or segments), two carry states (2 x 2 x H x 128 x 128 f32)
  * and the operand blobs (66,048 bytes per slot and head), the blobs capped at
- * 16 GiB (KDA_PREP_BUDGET_MB overrides the cap).  kda_chunk_fwd uses whatever
+ * 16 GiB.  kda_chunk_fwd uses whatever
  * workspace it is given: room for fewer slots runs the slots in equal pieces
  * (one chunk-local launch and one walk per piece); room for none runs the
  * one-kernel form.  Equals kda_chunk_fwd_workspace_size for other shapes.
@@ -217,8 +217,8 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  * cluster of d/32 CTAs, one per 32 value columns of the state (the columns
  * evolve independently), whose per-column partial sums of dq, dk, dg and
  * dbeta are added in a fixed order (results do not depend on scheduling;
- * KDA_BWD_SPLIT=0 in the environment selects one CTA per (sequence, head),
- * same bits).  States are recomputed from chunk-start checkpoints (64
+ * when no such cluster fits the device, one CTA per (sequence, head) gives
+ * the same bits).  States are recomputed from chunk-start checkpoints (64
  * tokens) kept in the workspace.
  *  q, k, v, g, beta, cu_seqlens, N, T, H, initial_state, scale, g_min,
  *  in_dtype   as kda_chunk_fwd (dk = dv = 64 or 128; cp off).

@@ -194,7 +194,10 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
     ckpt_every tokens of each sequence into ckpt f32 [N,K,H,dk,dv] (K = its
     second dimension) through kda_chunk_fwd_ckpt.  With prep (the default) a
     bf16, dk = dv = 128 call gets the workspace of the two-kernel form; a
-    caller-provided workspace is used as given when it is large enough."""
+    caller-provided workspace is used as given when it holds at least the
+    context-parallel scratch (kda_chunk_fwd_workspace_size): the library runs
+    the two-kernel form in as many pieces as its size requires, or the
+    one-kernel form when it holds no piece."""
     T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
     _expect(out, "out", q.dtype, (T, H, dv))
     _expect(final_state, "final_state", torch.float32, (N, H, dk, dv))
@@ -208,17 +211,17 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_sta
             out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
         if final_state is None and output_final_state:
             final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-        if prep and q.dtype == torch.bfloat16:
-            ws_bytes = chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+        need = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
+        if workspace is not None and workspace.numel() * workspace.element_size() >= max(need, 1):
+            ws_bytes = workspace.numel() * workspace.element_size()
         else:
-            ws_bytes = chunk_fwd_workspace_size(N, T, H, dk, dv, cp_mode, segment_len)
-        if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
-            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+            ws_bytes = chunk_fwd_prep_workspace_size(N, T, H, dk, dv, cp_mode, segment_len) \
+                if (prep and q.dtype == torch.bfloat16) else need
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
         common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
                   _ptr(initial_state), _ptr(final_state), _ptr(out), float(scale), float(g_min),
                   _in_dtype(q), int(cp_mode), int(segment_len),
-                  _ptr(workspace) if ws_bytes else None,
-                  ctypes.c_size_t(workspace.numel() * workspace.element_size() if ws_bytes else 0))
+                  _ptr(workspace) if ws_bytes else None, ctypes.c_size_t(ws_bytes))
         if ckpt_every:
             rc = lib.kda_chunk_fwd_ckpt(*common, int(ckpt_every), int(ckpt.shape[1]), _ptr(ckpt), _ptr(status),
                                         _stream(stream))

@@ -39,12 +39,11 @@ int sm_count() {
     return n;
 }
 
-// value-tile width of the prefill kernel
+// value-tile width of the warp-level prefill kernel: the whole dv, except that
+// a transition (whose augmented state has dk + dv columns) tiles by 64 when
+// dk is 64
 int prefill_dvt(int dk, int dv, bool transition) {
-    const char *env = getenv("KDA_PREFILL_DVT");
-    int want = env ? atoi(env) : 128;
-    if (want != 64 && want != 128) want = 128;
-    int dvt = (dv % want == 0) ? want : 64;
+    int dvt = (dv % 128 == 0) ? 128 : 64;
     if (transition && (dk % dvt != 0)) dvt = 64;
     return dvt;
 }
@@ -134,21 +133,13 @@ void drop_timed() {
 // slot list | two carry states [2 tiles][H][128][128] f32 | operand blobs of
 // one piece of slots.  The piece is as large as the workspace the caller gives
 // allows (pieces of equal size); kda_chunk_fwd_prep_workspace_size asks for
-// all slots in one piece, up to a cap of KDA_PREP_BUDGET_MB (default 16 GiB)
-// of blobs.
+// all slots in one piece, up to a cap of 16 GiB of blobs.
 struct SplitLayout {
     int nslots = 0, piece = 0;
     size_t off_list = 0, off_carry = 0, carry_stride = 0, off_blob = 0, total = 0;
 };
 
-size_t split_blob_cap() {
-    size_t mb = 16384;
-    if (const char *env = getenv("KDA_PREP_BUDGET_MB")) {
-        const long v = atol(env);
-        if (v > 0) mb = (size_t)v;
-    }
-    return mb << 20;
-}
+constexpr size_t kSplitBlobCap = (size_t)16384 << 20;
 
 // Layout for `units` units with `blob_bytes` of room for blobs; piece = 0 when
 // not even one slot fits.
@@ -177,7 +168,7 @@ SplitLayout split_layout(int units, int T, int H, size_t blob_bytes) {
 // The layout kda_chunk_fwd_prep_workspace_size asks for.
 SplitLayout split_layout_wanted(int units, int T, int H) {
     const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
-    const size_t all = (size_t)(T / kChunk + units) * per_slot, cap = split_blob_cap();
+    const size_t all = (size_t)(T / kChunk + units) * per_slot, cap = kSplitBlobCap;
     return split_layout(units, T, H, all < cap ? all : (cap < per_slot ? per_slot : cap));
 }
 
@@ -186,11 +177,6 @@ SplitLayout split_layout_fit(int units, int T, int H, size_t bytes) {
     const SplitLayout fixed = split_layout(units, T, H, 0);  // list and carries only
     if (bytes < fixed.total) return fixed;
     return split_layout(units, T, H, bytes - fixed.total);
-}
-
-bool split_enabled() {
-    const char *a = getenv("KDA_PREFILL_SPLIT"), *b = getenv("KDA_PREFILL_TC");
-    return !(a && a[0] == '0') && !(b && b[0] == '0');
 }
 
 // One pass of the two-kernel prefill over `units` units: the chunk list, then
@@ -221,11 +207,8 @@ cudaError_t run_split(const kda::ChunkArgs &a, int units, unsigned char *ws, con
 
 // Chunk-kernel dispatch by shape: the tcgen05 / tensor-memory kernel for
 // dk = dv = 128 with bf16 inputs, the warp-level kernel otherwise.
-// KDA_PREFILL_TC=0 selects the warp-level kernel everywhere (comparisons).
 cudaError_t run_chunk(const kda::ChunkArgs &a, int units, bool bf, cudaStream_t st) {
-    const char *env = getenv("KDA_PREFILL_TC");
-    const bool tc_ok = !(env && env[0] == '0');
-    if (tc_ok && kda::chunk_tc_supported(a, bf))
+    if (kda::chunk_tc_supported(a, bf))
         return timed_launch(KDA_KERNEL_CHUNK_TC, st, [&] { return kda::launch_chunk_tc(a, units, st); });
     return timed_launch(KDA_KERNEL_CHUNK_MMA, st, [&] {
         return kda::launch_chunk(a, units, prefill_dvt(a.dk, a.dv, a.mode == kda::MODE_TRANSITION), bf, st);
@@ -259,7 +242,7 @@ HostLayout host_layout(int N, int T, int H, int dk, int dv, int in_dtype, int pi
     L.off_o = o; o = align256(o + (size_t)T * H * dv * es);
     L.off_sf = o; o = align256(o + (size_t)N * H * dk * dv * 4);
     L.off_area = o;
-    L.pipelined = in_dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && T > 0 && split_enabled();
+    L.pipelined = in_dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && T > 0;
     if (L.pipelined) {
         const int nslots = T / kChunk + N;
         const int pc = pieces < 1 ? 1 : (pieces > nslots ? nslots : pieces);
@@ -364,7 +347,7 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     // the two-kernel path when the workspace also holds its area
     SplitLayout SL;
     const size_t split_off = align256(L.total);
-    bool split = bf && dk == 128 && dv == 128 && workspace && T > 0 && split_enabled();
+    bool split = bf && dk == 128 && dv == 128 && workspace && T > 0;
     if (split) {
         split = workspace_bytes > split_off;
         if (split) {

@@ -596,9 +596,9 @@ size_t chunk_bwd_partial_floats(int d) { return d == 128 ? bw::part_floats<128>(
 
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st) {
     if (a.N <= 0) return cudaSuccess;
-    // the split form unless the caller gave no partial buffers or KDA_BWD_SPLIT=0
-    const char *env = getenv("KDA_BWD_SPLIT");
-    const bool split = a.partials != nullptr && !(env && env[0] == '0');
+    // the split form unless the caller gave no partial buffers (or, inside
+    // launch_t, no cluster of it fits the device)
+    const bool split = a.partials != nullptr;
     if (d == 128) {
         if (split) return bf16 ? bw::launch_t<128, true, true>(a, st) : bw::launch_t<128, false, true>(a, st);
         return bf16 ? bw::launch_t<128, true, false>(a, st) : bw::launch_t<128, false, false>(a, st);

@@ -51,6 +51,10 @@ extern "C" int kda_chunk_fwd_cp_noalloc(const void *q, const void *k, const void
     // Nothing in the scratch needs to start at zero: the segment-table kernel
     // writes every table entry and count it later reads, the transition kernel
     // writes every M and N tile, and the composition writes every S_in tile.
+    // When the rest of the array holds the two-kernel area, its slot list is
+    // cleared by the launch that fills it, a carried state is written by the
+    // walk of one piece before the next piece reads it, and every operand blob
+    // is written by the chunk-local kernel before the walk of its piece reads it.
     return kda_chunk_fwd(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, final_state, o, scale,
                          g_min, in_dtype, KDA_CP_ON, segment_len, scratch, (size_t)KDA_NOALLOC_SCRATCH_BYTES,
                          status, stream);

@@ -532,17 +532,10 @@ static cudaError_t launch_verify_t(const VerifyArgs &a, cudaStream_t st) {
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t st) {
     if (a.R <= 0) return cudaSuccess;
-    if (a.Wd == 0) {
-        // one token per request: the plain one-step kernel unless KDA_DECODE_TOKEN=0
-        const char *env = getenv("KDA_DECODE_TOKEN");
-        if (!(env && env[0] == '0')) return launch_decode_token(a, st);
-    }
-    if (a.dk == 128 && a.dv == 128) {
-        // the tensor-memory kernel unless KDA_VERIFY_TC=0 asks for this one
-        const char *env = getenv("KDA_VERIFY_TC");
-        if (!(env && env[0] == '0')) return launch_verify_tc(a, st);
-        return launch_verify_t<128>(a, st);
-    }
+    // by shape: one token per request (no draft window) takes the one-step
+    // kernel, d = 128 the tensor-memory kernel, d = 64 the warp-level kernel
+    if (a.Wd == 0) return launch_decode_token(a, st);
+    if (a.dk == 128 && a.dv == 128) return launch_verify_tc(a, st);
     if (a.dk == 64 && a.dv == 64) return launch_verify_t<64>(a, st);
     return cudaErrorInvalidValue;
 }

@@ -111,12 +111,11 @@ def _align256(x):
 
 @pytest.mark.parametrize("N,T,H,cp,seg", [(1, 32768, 96, 0, 0), (16, 68775, 96, 0, 0), (1, 1 << 20, 12, 1, 32768),
                                           (3, 1771, 4, 0, 0)])
-def test_prep_workspace_arithmetic(lib, monkeypatch, N, T, H, cp, seg):
+def test_prep_workspace_arithmetic(lib, N, T, H, cp, seg):
     """The two-kernel area after the CP scratch: slot list (8 B per slot,
     floor(T/64) + units slots), two carry states 2 x H x 128 x 128 f32, and the
     blobs of all slots (66,048 B per slot and head), capped at 16 GiB of blobs
     (then pieces of equal size)."""
-    monkeypatch.delenv("KDA_PREP_BUDGET_MB", raising=False)
     lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
     lib.kda_chunk_fwd_prep_workspace_size.restype = ctypes.c_size_t
     base = lib.kda_chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)

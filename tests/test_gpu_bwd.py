@@ -125,30 +125,6 @@ def _grads(kda, x, scale):
     return got
 
 
-@pytest.mark.parametrize("d,dtype,lens,H", [(128, torch.bfloat16, [200, 0, 65, 1], 3),
-                                            (64, torch.float32, [150, 64, 7], 2),
-                                            (128, torch.float32, [129], 2),
-                                            (64, torch.bfloat16, "many", 8)])
-def test_split_form_equals_whole_form(kda, monkeypatch, d, dtype, lens, H):
-    """The cluster form (one CTA per 32 value columns, partial sums added in
-    group order after each chunk) and the one-CTA-per-unit form give the same
-    bits, including many units over persistent clusters and empty sequences."""
-    if lens == "many":
-        lens = np.random.default_rng(21).integers(0, 200, size=30).tolist()
-    x = _case(lens, H, d, dtype, seed=d + H)
-    split = _grads(kda, x, 0.6)
-    monkeypatch.setenv("KDA_BWD_SPLIT", "0")
-    whole = _grads(kda, x, 0.6)
-    for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta", "dS0"), split, whole):
-        assert torch.equal(a, b), f"{name}: max {float((a - b).abs().max()):.3e}"
-
-
-def test_whole_form_matches_oracle(kda, oracle, monkeypatch):
-    monkeypatch.setenv("KDA_BWD_SPLIT", "0")
-    x = _case([300, 64, 0], 2, 128, torch.bfloat16, seed=31)
-    _compare(kda, oracle, x, scale=0.9)
-
-
 def test_absent_states_and_no_dS0(kda, oracle):
     """initial_state and dS_final absent (zero), dS0 not asked for."""
     x = _case([130, 64], 2, 128, torch.bfloat16, seed=41)

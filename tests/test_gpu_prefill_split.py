@@ -3,8 +3,8 @@ chunk first, then the state walk) against the one-kernel form and the oracle.
 
 Both forms run the same operations in the same order, so their outputs,
 final states and checkpoints must agree bit for bit; the oracle bars of the
-other prefill tests apply to the two-kernel form as well.  A small operand
-budget (KDA_PREP_BUDGET_MB) forces many pieces, so units cross piece
+other prefill tests apply to the two-kernel form as well.  A workspace with
+room for a few slots' operand blobs forces many pieces, so units cross piece
 boundaries (carried states) and empty units fall inside pieces.
 """
 import numpy as np
@@ -42,53 +42,67 @@ def _inputs(lens, H, seed, s0=True, d=128):
     return dict(q=c(q.bfloat16()), k=c(k.bfloat16()), v=c(v.bfloat16()), g=c(g), beta=c(beta), cu=c(cu), S0=c(S0))
 
 
-def _run(kda, x, prep, cp=0, seg=0, scale=1.0, every=0, K=0):
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def piece_workspace(kda, x, slots, cp=0, seg=0):
+    """A workspace with room for the blobs of `slots` chunk slots (all heads):
+    the context-parallel scratch, the slot list, two carry states and the
+    blobs, laid out as the library lays them out."""
+    N, (T, H) = x["cu"].shape[0] - 1, x["q"].shape[:2]
+    plan = kda.chunk_fwd_plan(N, T, H, 128, 128, cp, seg)
+    units = (T // plan + N) if plan else N
+    nbytes = (_align256(kda.chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)) + _align256((T // 64 + units) * 8) +
+              _align256(2 * 2 * H * 128 * 128 * 4) + slots * H * 66048)
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def _run(kda, x, prep, cp=0, seg=0, scale=1.0, every=0, K=0, slots=None):
     ck = None
     if every:
         N, H = x["cu"].shape[0] - 1, x["q"].shape[1]
         ck = torch.full((N, K, H, 128, 128), 7.0, device="cuda")
+    ws = piece_workspace(kda, x, slots, cp, seg) if (prep and slots) else None
     o, Sf = kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"], scale=scale,
-                          cp_mode=cp, segment_len=seg, prep=prep, ckpt_every=every, ckpt=ck)
+                          cp_mode=cp, segment_len=seg, prep=prep, ckpt_every=every, ckpt=ck, workspace=ws)
     torch.cuda.synchronize()
     return o, Sf, ck
 
 
 CASES = {
-    # name: (lengths, H, cp_mode, segment_len, operand budget in MiB or None, checkpoint every, count)
+    # name: (lengths, H, cp_mode, segment_len, slots per piece or None (one piece), checkpoint every, count)
     "varlen_ragged": ([3 * 64 + 17, 0, 1, 64, 700], 3, 0, 0, None, 0, 0),
-    "pieces_varlen": ([1000, 130, 0, 640, 1], 4, 0, 0, 1, 0, 0),
-    "pieces_ckpt": ([640, 1000, 1536], 4, 0, 0, 2, 256, 6),
+    "pieces_varlen": ([1000, 130, 0, 640, 1], 4, 0, 0, 3, 0, 0),
+    "pieces_ckpt": ([640, 1000, 1536], 4, 0, 0, 7, 256, 6),
     "cp_one_piece": ([5000], 2, 1, 1024, None, 0, 0),
-    "cp_pieces": ([3000, 0, 1500, 64], 2, 1, 1024, 1, 0, 0),
+    "cp_pieces": ([3000, 0, 1500, 64], 2, 1, 1024, 7, 0, 0),
     "cp_ckpt": ([4096], 2, 1, 1024, None, 768, 5),
 }
 
 
 @pytest.mark.parametrize("name", list(CASES))
-def test_two_kernel_form_equals_one_kernel_form(kda, monkeypatch, name):
-    lens, H, cp, seg, budget, every, K = CASES[name]
-    if budget is not None:
-        monkeypatch.setenv("KDA_PREP_BUDGET_MB", str(budget))
+def test_two_kernel_form_equals_one_kernel_form(kda, name):
+    lens, H, cp, seg, slots, every, K = CASES[name]
     x = _inputs(lens, H, seed=len(name))
     T = int(sum(lens))
     ws_split = kda.chunk_fwd_prep_workspace_size(len(lens), T, H, 128, 128, cp, seg)
     ws_one = kda.chunk_fwd_workspace_size(len(lens), T, H, 128, 128, cp, seg)
     assert ws_split > ws_one
     o1, S1, c1 = _run(kda, x, prep=False, cp=cp, seg=seg, scale=0.5, every=every, K=K)
-    o2, S2, c2 = _run(kda, x, prep=True, cp=cp, seg=seg, scale=0.5, every=every, K=K)
+    o2, S2, c2 = _run(kda, x, prep=True, cp=cp, seg=seg, scale=0.5, every=every, K=K, slots=slots)
     assert torch.equal(o1, o2), f"outputs differ: max {float((o1.float() - o2.float()).abs().max()):.3e}"
     assert torch.equal(S1, S2), f"final states differ: max {float((S1 - S2).abs().max()):.3e}"
     if every:
         assert torch.equal(c1, c2), "checkpoints differ"
 
 
-def test_pieces_match_oracle(kda, oracle, monkeypatch):
+def test_pieces_match_oracle(kda, oracle):
     """Many pieces (3 slots each at H = 4): every unit of the three crosses
     piece boundaries; outputs and final states within the oracle bars."""
-    monkeypatch.setenv("KDA_PREP_BUDGET_MB", "1")
     lens = [700, 64, 0, 1300]
     x = _inputs(lens, 4, seed=5)
-    o, Sf, _ = _run(kda, x, prep=True, scale=0.75)
+    o, Sf, _ = _run(kda, x, prep=True, scale=0.75, slots=3)
     o_ref, S_ref = oracle.prefill(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
                                   x["cu"].cpu().numpy(), S0=to64(x["S0"]), scale=0.75)
     assert normwise_err(to64(o), o_ref, head_axis=1) <= OUT_TOL
@@ -107,13 +121,12 @@ def test_two_kernel_form_reports_bad_seqlens(kda):
     assert torch.all(o[100:] == 7.0)
 
 
-def test_kernel_timing_counts_the_launches(kda, monkeypatch):
+def test_kernel_timing_counts_the_launches(kda):
     """Launch timing around one two-kernel call: one slot list, and one
     chunk-local launch and one walk per piece (5 pieces here)."""
-    monkeypatch.setenv("KDA_PREP_BUDGET_MB", "1")
-    x = _inputs([500, 300], 4, seed=3)  # 14 slots; 3 slots of 4 heads per MiB -> pieces of 3 (5 pieces)
+    x = _inputs([500, 300], 4, seed=3)  # 14 slots in pieces of 3 (5 pieces)
     kda.kernel_timing_start()
-    _run(kda, x, prep=True)
+    _run(kda, x, prep=True, slots=3)
     kern = kda.kernel_timing_stop()
     n_pieces = -(-(800 // 64 + 2) // 3)
     assert kern["kda_chunk_list_kernel"]["launches"] == 1

@@ -4,9 +4,14 @@ It serves callers that may not call cudaMalloc or hand over a workspace (a
 host that forbids device allocation after start-up, a plugin whose host owns
 every buffer): its scratch is a fixed device array inside the library.  This
 test calls it through the C ABI, twice in a row on different inputs, and
-checks each result against kda_chunk_fwd with a caller workspace, within the
-parity bars the other tests use.  It sits in a file of its own, collected
-last, and works alone in a fresh process as well as after the other tests.
+checks each result against kda_chunk_fwd with a caller workspace bit for bit
+(the forms the fixed scratch selects run the same operations in the same
+order as the workspace call's), and one result against the oracle within the
+parity bars the other tests use.  The sizes cover the three forms the fixed
+scratch leads to: everything in one piece, the two-kernel form in several
+pieces, and the one-kernel form when the carried states do not fit beside
+the context-parallel scratch.  It sits in a file of its own, collected last,
+and works alone in a fresh process as well as after the other tests.
 """
 import ctypes
 
@@ -66,14 +71,41 @@ def _with_workspace(x, seg):
                          cp_mode=kda.CP_ON, segment_len=seg)
 
 
-def test_noalloc_matches_workspace_entry_point_twice(lib):
-    cases = [(_inputs([3000, 1500], 3, seed=1), 1024), (_inputs([700, 0, 2600], 2, seed=2), 512)]
-    for x, seg in cases:  # two calls in a row share the fixed scratch
+def _layout(lib, x, seg):
+    """(pieces, two-kernel form?) that 64 MiB of scratch leads to, from the
+    library's own workspace arithmetic."""
+    import kda_gated_delta_02_gb300 as kda
+    T, H, _ = x["k"].shape
+    N = x["cu"].shape[0] - 1
+    cp = kda.chunk_fwd_workspace_size(N, T, H, 128, 128, kda.CP_ON, seg)
+    units = T // kda.chunk_fwd_plan(N, T, H, 128, 128, kda.CP_ON, seg) + N
+    a = lambda n: (n + 255) // 256 * 256
+    room = (64 << 20) - a(cp) - a((T // 64 + units) * 8) - a(2 * 2 * H * 128 * 128 * 4)
+    per_slot = H * 66048
+    if room < per_slot:
+        return 0, False
+    nslots = T // 64 + units
+    return -(-nslots // min(nslots, room // per_slot)), True
+
+
+def test_noalloc_matches_workspace_entry_point_twice(lib, oracle):
+    cases = [(_inputs([3000, 1500], 3, seed=1), 1024, (1, True)),   # one piece
+             (_inputs([8192], 8, seed=2), 1024, (2, True)),          # the slots in two pieces
+             (_inputs([2048], 96, seed=4), 1024, (0, False))]        # one-kernel form
+    for x, seg, form in cases:  # calls in a row share the fixed scratch
+        assert _layout(lib, x, seg) == form
         o, Sf = _noalloc(lib, x, seg)
         o_ref, Sf_ref = _with_workspace(x, seg)
         torch.cuda.synchronize()
-        assert normwise_err(to64(o), to64(o_ref), 1) <= OUT_TOL
-        assert normwise_err(to64(Sf), to64(Sf_ref), 1) <= STATE_TOL
+        assert torch.equal(o, o_ref), f"outputs differ: max {float((o.float() - o_ref.float()).abs().max()):.3e}"
+        assert torch.equal(Sf, Sf_ref), f"states differ: max {float((Sf - Sf_ref).abs().max()):.3e}"
+    x, seg, _ = cases[0]
+    o, Sf = _noalloc(lib, x, seg)
+    torch.cuda.synchronize()
+    o_or, S_or = oracle.prefill(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
+                                x["cu"].cpu().numpy(), S0=to64(x["S0"]))
+    assert normwise_err(to64(o), o_or, 1) <= OUT_TOL
+    assert normwise_err(to64(Sf), S_or, 1) <= STATE_TOL
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib):
