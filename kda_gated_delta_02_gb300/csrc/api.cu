@@ -130,75 +130,126 @@ void drop_timed() {
 }
 
 // Two-kernel tcgen05 prefill (dk = dv = 128): workspace after the CP scratch =
-// slot list | two carry states [2 tiles][H][128][128] f32 | operand blobs of
-// one piece of slots.  The piece is as large as the workspace the caller gives
-// allows (pieces of equal size); kda_chunk_fwd_prep_workspace_size asks for
-// all slots in one piece, up to a cap of 16 GiB of blobs.
+// slot list | one item counter per piece | two carry states [2 tiles][H][128][128]
+// f32 | operand blobs of one or two pieces of slots.
+//
+// With two blob buffers the pieces are pipelined: the chunk-local kernel of
+// piece p + 1 runs while the walk of piece p holds its SMs, and fills every SM
+// once the walk is done; piece p + 2 reuses piece p's buffer (run_split).
+// Calls with few slots run as one piece, and so do calls whose walks alone
+// have a CTA for every SM (units x heads >= SMs: nothing is left idle to
+// overlap); a context-parallel call keeps all slots in one piece when the
+// workspace allows (the transition pass's blobs then serve the replay).  kda_chunk_fwd_prep_workspace_size asks for the
+// layout the call prefers, the blobs capped at 16 GiB; smaller workspaces get
+// smaller pieces.
 struct SplitLayout {
-    int nslots = 0, piece = 0;
-    size_t off_list = 0, off_carry = 0, carry_stride = 0, off_blob = 0, total = 0;
+    int nslots = 0, piece = 0, nbuf = 1, pieces = 0;
+    size_t off_list = 0, off_claim = 0, off_carry = 0, carry_stride = 0, off_blob = 0, buf_bytes = 0, total = 0;
 };
 
 constexpr size_t kSplitBlobCap = (size_t)16384 << 20;
+constexpr int kPipePieces = 4;     // pieces of a pipelined call
+constexpr int kPipeMinSlots = 64;  // fewer slots than this run as one piece
 
-// Layout for `units` units with `blob_bytes` of room for blobs; piece = 0 when
-// not even one slot fits.
-SplitLayout split_layout(int units, int T, int H, size_t blob_bytes) {
+// whether a call of `units` units over H heads prefers pipelined pieces
+bool pipe_wanted(int units, int T, int H, bool one_piece) {
+    return !one_piece && T / kChunk + units >= kPipeMinSlots && (long)units * H < sm_count();
+}
+
+inline size_t blob_per_slot(int H) { return (size_t)H * kda::kChunkBlobBytes; }
+
+// Layout with room for the blobs of `room` slots.  one_piece: all slots in one
+// piece when they fit; nbuf_max: 1 for a caller that runs the pieces in order
+// on one stream.
+SplitLayout split_layout_slots(int units, int T, int H, long room, bool one_piece, int nbuf_max) {
     SplitLayout S;
     S.nslots = T / kChunk + units;
-    const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
-    long piece = (long)(blob_bytes / per_slot);
-    if (piece > S.nslots) piece = S.nslots;
+    const long n = S.nslots;
+    const long want = pipe_wanted(units, T, H, one_piece) ? (n + kPipePieces - 1) / kPipePieces : n;
+    long piece = 0;
+    if (nbuf_max <= 1) {
+        piece = room < n ? room : n;
+    } else if (room >= n && want >= n) {
+        piece = n;
+    } else if (room >= 2) {
+        piece = want < room / 2 ? want : room / 2;
+        S.nbuf = 2;
+    } else if (room >= 1) {
+        piece = 1;
+    }
     if (piece >= 1) {
-        const long pieces = (S.nslots + piece - 1) / piece;
-        S.piece = (int)((S.nslots + pieces - 1) / pieces);
+        const long pieces = (n + piece - 1) / piece;
+        S.piece = (int)((n + pieces - 1) / pieces);
+        S.pieces = (int)pieces;
+        if (S.pieces == 1) S.nbuf = 1;
+    } else {
+        S.nbuf = 0;
     }
     size_t o = 0;
     S.off_list = o;
-    o = align256(o + (size_t)S.nslots * 8);
+    o = align256(o + (size_t)n * 8);
+    S.off_claim = o;
+    o = align256(o + (size_t)n * 4);
     S.off_carry = o;
     S.carry_stride = (size_t)2 * H * 128 * 128;  // floats per carry state
     o = align256(o + 2 * S.carry_stride * 4);
     S.off_blob = o;
-    o = align256(o + (size_t)S.piece * per_slot);
+    S.buf_bytes = (size_t)S.piece * blob_per_slot(H);
+    o = align256(o + (size_t)S.nbuf * S.buf_bytes);
     S.total = o;
     return S;
 }
 
 // The layout kda_chunk_fwd_prep_workspace_size asks for.
-SplitLayout split_layout_wanted(int units, int T, int H) {
-    const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
-    const size_t all = (size_t)(T / kChunk + units) * per_slot, cap = kSplitBlobCap;
-    return split_layout(units, T, H, all < cap ? all : (cap < per_slot ? per_slot : cap));
+SplitLayout split_layout_wanted(int units, int T, int H, bool one_piece) {
+    const long n = T / kChunk + units;
+    const long cap = (long)(kSplitBlobCap / blob_per_slot(H));
+    const long want = pipe_wanted(units, T, H, one_piece) ? 2 * ((n + kPipePieces - 1) / kPipePieces) : n;
+    return split_layout_slots(units, T, H, want < cap ? want : (cap < 1 ? 1 : cap), one_piece, 2);
 }
 
 // The layout that fits `bytes` of workspace (piece = 0: none fits).
-SplitLayout split_layout_fit(int units, int T, int H, size_t bytes) {
-    const SplitLayout fixed = split_layout(units, T, H, 0);  // list and carries only
+SplitLayout split_layout_fit(int units, int T, int H, size_t bytes, bool one_piece) {
+    const SplitLayout fixed = split_layout_slots(units, T, H, 0, one_piece, 2);  // list, counters, carries
     if (bytes < fixed.total) return fixed;
-    return split_layout(units, T, H, bytes - fixed.total);
+    return split_layout_slots(units, T, H, (long)((bytes - fixed.total) / blob_per_slot(H)), one_piece, 2);
 }
 
 // One pass of the two-kernel prefill over `units` units: the chunk list, then
-// per piece the chunk-local kernel and the walk.  With skip_prep the blobs of
-// a single piece are already in place (written by an earlier pass with
-// need_q set).
+// per piece the chunk-local kernel and the walk, all on `st`.  With two blob
+// buffers the chunk-local kernel of piece p + 1 is a programmatic dependent
+// launch of the walk of piece p: the walk lets it start as soon as all of the
+// walk's CTAs are resident, so it runs on the SMs the walk leaves free and
+// fills the rest when the walk ends.  It reads nothing the walk writes and
+// writes the other buffer, whose last reader (the walk of piece p - 1)
+// completed before the walk of piece p started; every walk is an ordinary
+// launch, so it starts only after all earlier work on the stream.  With
+// skip_prep the blobs of a single piece are already in place (written by an
+// earlier pass with need_q set).
 cudaError_t run_split(const kda::ChunkArgs &a, int units, unsigned char *ws, const SplitLayout &S, bool need_q,
                       bool skip_prep, cudaStream_t st) {
     int2 *list = reinterpret_cast<int2 *>(ws + S.off_list);
+    int *claim = reinterpret_cast<int *>(ws + S.off_claim);
     float *carry = reinterpret_cast<float *>(ws + S.off_carry);
     unsigned char *blob = ws + S.off_blob;
+    const int P = S.pieces;
+    const bool overlap = S.nbuf == 2;
     cudaError_t e = cudaSuccess;
-    if (!skip_prep)
-        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(a, units, S.nslots, list, st); });
-    for (int s0 = 0, pc = 0; e == cudaSuccess && s0 < S.nslots; s0 += S.piece, ++pc) {
-        const int s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
+    if (!skip_prep) {
+        e = cudaMemsetAsync(claim, 0, (size_t)P * sizeof(int), st);
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(a, units, S.nslots, list, st); });
+    }
+    for (int pc = 0; e == cudaSuccess && pc < P; ++pc) {
+        const int s0 = pc * S.piece, s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
+        unsigned char *buf = blob + (size_t)(pc % (S.nbuf > 0 ? S.nbuf : 1)) * S.buf_bytes;
         if (!skip_prep)
-            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st,
-                             [&] { return kda::launch_chunk_prep(a, list, s0, s1, blob, need_q, st); });
+            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
+                return kda::launch_chunk_prep(a, list, s0, s1, buf, need_q, claim + pc, overlap && pc > 0, st);
+            });
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
-                return kda::launch_chunk_walk(a, units, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
+                return kda::launch_chunk_walk(a, units, buf, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,
                                               carry + (size_t)((pc + 1) & 1) * S.carry_stride, st);
             });
     }
@@ -246,8 +297,7 @@ HostLayout host_layout(int N, int T, int H, int dk, int dv, int in_dtype, int pi
     if (L.pipelined) {
         const int nslots = T / kChunk + N;
         const int pc = pieces < 1 ? 1 : (pieces > nslots ? nslots : pieces);
-        const size_t per_slot = (size_t)H * kda::kChunkBlobBytes;
-        L.S = split_layout(N, T, H, (size_t)((nslots + pc - 1) / pc) * per_slot);
+        L.S = split_layout_slots(N, T, H, (nslots + pc - 1) / pc, false, 1);
         o += L.S.total;
     }
     L.total = align256(o);
@@ -305,7 +355,7 @@ size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, in
     const CpLayout L = cp_layout(N, T, H, dk, dv, cp_mode, segment_len);
     if (dk != 128 || dv != 128 || N < 1 || T < 0 || H < 1) return L.total;
     const int units = L.seg_len ? L.P_max : N;
-    return align256(L.total) + split_layout_wanted(units, T, H).total;
+    return align256(L.total) + split_layout_wanted(units, T, H, L.seg_len != 0).total;
 }
 
 int kda_chunk_fwd_plan(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
@@ -351,7 +401,7 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g, 
     if (split) {
         split = workspace_bytes > split_off;
         if (split) {
-            SL = split_layout_fit(L.seg_len ? L.P_max : N, T, H, workspace_bytes - split_off);
+            SL = split_layout_fit(L.seg_len ? L.P_max : N, T, H, workspace_bytes - split_off, L.seg_len != 0);
             split = SL.piece >= 1;
         }
     }
@@ -659,6 +709,7 @@ int kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float 
     a.status = status; a.mode = kda::MODE_SEQ; a.cu_seqlens = dcu; a.S_init = ds0; a.S_final = dsf;
     unsigned char *area = ws + L.off_area;
     int2 *list = reinterpret_cast<int2 *>(area + S.off_list);
+    int *claim = reinterpret_cast<int *>(area + S.off_claim);
     float *carry = reinterpret_cast<float *>(area + S.off_carry);
     unsigned char *blob = area + S.off_blob;
     // the copy streams start after earlier work on the caller's stream
@@ -674,11 +725,12 @@ int kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float 
     for (int pc = 0; e == cudaSuccess && pc < P; ++pc) {
         const int s0 = pc * S.piece, s1 = s0 + S.piece < S.nslots ? s0 + S.piece : S.nslots;
         e = cudaStreamWaitEvent(st, ev[pc], 0);
+        if (e == cudaSuccess && pc == 0) e = cudaMemsetAsync(claim, 0, (size_t)P * sizeof(int), st);
         if (e == cudaSuccess && pc == 0)
             e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(a, N, S.nslots, list, st); });
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_CHUNK_PREP, st,
-                             [&] { return kda::launch_chunk_prep(a, list, s0, s1, blob, true, st); });
+                             [&] { return kda::launch_chunk_prep(a, list, s0, s1, blob, true, claim + pc, false, st); });
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
                 return kda::launch_chunk_walk(a, N, blob, s0, s1, carry + (size_t)(pc & 1) * S.carry_stride,

@@ -107,6 +107,7 @@ constexpr uint32_t P_BETA = 98304;   // f32 [64]
 constexpr uint32_t P_PART = 98560;   // f32 [2][4][128] half-block products
 constexpr uint32_t P_BAR = 102656;   // 2 mbarriers: A/B product, W product
 constexpr uint32_t P_TMEM = 102672;  // tensor-memory base address
+constexpr uint32_t P_CLAIM = 102676; // items claimed by thread 0 (2 ints)
 constexpr uint32_t P_SMEM = 102688 + 1024;
 constexpr int LDF = 68;
 constexpr uint32_t TM1_AB = 0, TM1_W = 160;  // 224 of 256 columns
@@ -121,6 +122,7 @@ struct PrepParams {
     const int2 *list;    // slot -> {first token, length}
     int slot0;           // first slot of this launch
     int nitems;          // (slot1 - slot0) * H items, w = (slot - slot0) * H + h
+    int *claim;          // item counter of this launch, zero at launch; CTAs claim items in order
     unsigned char *blob; // [w][kChunkBlobBytes]
     int need_q;          // 0: transitions only (no Q~, no B)
     int pf_beta;         // tb is encoded (H a multiple of 4)
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = p.H, nitems = p.nitems, G = gridDim.x;
+    const int H = p.H, nitems = p.nitems;
     float *sBeta = reinterpret_cast<float *>(sm + P_BETA);
     float *sPart = reinterpret_cast<float *>(sm + P_PART);
     const uint32_t bar_ab = sb + P_BAR, bar_w = sb + P_BAR + 8;
@@ -153,29 +155,45 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
     const int qd = warp & 3;  // TMEM lane quadrant of this warp
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
 
-    // Items w = (slot - slot0) * H + h, strided over the resident CTAs.  While
-    // item w runs, the rows of item w + G are prefetched into L2 (its chunk
+    // Items w = (slot - slot0) * H + h, claimed in increasing order from the
+    // launch's counter, so CTAs that start late (the SMs were busy with other
+    // work) take fewer items and the blobs are written roughly in slot order.
+    // Each CTA holds the item it works on and the next one it claimed: while
+    // item w runs, the rows of the next item are prefetched into L2 (its chunk
     // entry was read one item earlier), so its loads do not wait on DRAM.
+    int *sClaim = reinterpret_cast<int *>(sm + P_CLAIM);
     bool alive = true;
     uint32_t it = 0;  // items processed (mbarrier parity)
-    int w = blockIdx.x;
+    if (tid == 0) {
+        const int w0 = atomicAdd(p.claim, 1);
+        sClaim[0] = w0;
+        sClaim[1] = atomicAdd(p.claim, 1);
+    }
+    __syncthreads();
+    int w = sClaim[0], wn = sClaim[1];
     int2 cl = (w < nitems) ? p.list[p.slot0 + w / H] : make_int2(0, 0);
-    int2 ncl = (w + G < nitems) ? p.list[p.slot0 + (w + G) / H] : make_int2(0, 0);
-    for (; w < nitems; w += G) {
+    int2 ncl = (wn < nitems) ? p.list[p.slot0 + wn / H] : make_int2(0, 0);
+    __syncthreads();  // claims read before thread 0 writes the next one
+
+    while (w < nitems) {
     const int h = w % H;
     const int tc = cl.x, Lc = cl.y;
-    int2 nncl = make_int2(0, 0);
+    int wnn;
     {
-        const int wn = w + G;
-        if (wn < nitems && ncl.y > 0 && tid == 0) {
-            const int hn = wn % H;
-            if (need_q) umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
-            umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
-            umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
-            if (p.pf_beta) umma::prefetch_tile_2d(&p.tb, hn & ~3, ncl.x);
+        if (tid == 0) {
+            sClaim[0] = (wn < nitems) ? atomicAdd(p.claim, 1) : nitems;
+            if (wn < nitems && ncl.y > 0) {
+                const int hn = wn % H;
+                if (need_q) umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
+                if (p.pf_beta) umma::prefetch_tile_2d(&p.tb, hn & ~3, ncl.x);
+            }
         }
-        if (w + 2 * G < nitems) nncl = p.list[p.slot0 + (w + 2 * G) / H];
+        __syncthreads();
+        wnn = sClaim[0];
     }
+    const int2 nncl = (wnn < nitems) ? p.list[p.slot0 + wnn / H] : make_int2(0, 0);
     if (Lc > 0) {
     unsigned char *out = p.blob + ((size_t)w * kChunkBlobBytes);
 
@@ -554,11 +572,18 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
         break;
     }
     }  // Lc > 0
+    __syncthreads();  // the claim was read by every thread before thread 0 writes the next
+    w = wn;
+    wn = wnn;
     cl = ncl;
     ncl = nncl;
     }  // items
     if (!alive && tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
     if (warp == 0) umma::tmem_dealloc(tmem, 256);
+    // launched as a programmatic dependent of a walk: finish only after that
+    // walk has, so the next walk on the stream (which waits for this launch)
+    // also follows it (a no-op for an ordinary launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // ============================================================================ state walk
@@ -592,6 +617,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
     const int H = p.H, dv = p.dv;
+    // a chunk-local launch that follows on the stream as a programmatic
+    // dependent may start once every CTA of this walk is resident: it reads
+    // nothing this walk writes
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // ---------------------------------------------------------------- work unit and its chunks in this piece
     int n, t0, t1;
@@ -945,7 +974,7 @@ bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
 }  // namespace
 
 cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
-                              bool need_q, cudaStream_t st) {
+                              bool need_q, int *claim, bool after_walk, cudaStream_t st) {
     if (slot1 <= slot0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(sp::kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          sp::P_SMEM);
@@ -964,6 +993,7 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
     P.need_q = (need_q && a.q) ? 1 : 0;
     P.status = a.status;
     P.nitems = (slot1 - slot0) * a.H;
+    P.claim = claim;
     // prefetch boxes (H is a multiple of 4 for the beta box; other H prefetch nothing there)
     bool ok = encode_rows(&P.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, a.T, 128, 1) &&
               encode_rows(&P.tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, a.H, a.T, 128, 1) &&
@@ -984,8 +1014,17 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
         }
     }
     const int grid = P.nitems < 2 * sms ? P.nitems : 2 * sms;
-    sp::kda_chunk_prep_kernel<<<grid, sp::NT1, sp::P_SMEM, st>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(sp::NT1);
+    cfg.dynamicSmemBytes = sp::P_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_walk ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, sp::kda_chunk_prep_kernel, P);
 }
 
 cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char *blob, int slot0, int slot1,

@@ -48,9 +48,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st);
 constexpr unsigned kChunkBlobBytes = 66048;
 // list[slot] = {first token, length} for every chunk of units [0, units), 0 elsewhere
 cudaError_t launch_chunk_list(const ChunkArgs &a, int units, int nslots, int2 *list, cudaStream_t st);
-// blobs of slots [slot0, slot1) into blob[(slot - slot0) * H + h]
+// blobs of slots [slot0, slot1) into blob[(slot - slot0) * H + h]; claim is a
+// device int that is zero when the launch starts (its item counter).  With
+// after_walk the launch is a programmatic dependent of the walk launched just
+// before it on `st` (it may start while that walk runs; see run_split).
 cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
-                              bool need_q, cudaStream_t st);
+                              bool need_q, int *claim, bool after_walk, cudaStream_t st);
 // the chunks of every unit that fall in slots [slot0, slot1); a unit cut at
 // slot0 starts from carry_in, one cut at slot1 leaves its state in carry_out
 // ([tiles][H][128][128] fp32 each)

@@ -110,25 +110,29 @@ def _align256(x):
 
 
 @pytest.mark.parametrize("N,T,H,cp,seg", [(1, 32768, 96, 0, 0), (16, 68775, 96, 0, 0), (1, 1 << 20, 12, 1, 32768),
-                                          (3, 1771, 4, 0, 0)])
+                                          (3, 1771, 4, 0, 0), (1, 1 << 21, 96, 0, 0)])
 def test_prep_workspace_arithmetic(lib, N, T, H, cp, seg):
     """The two-kernel area after the CP scratch: slot list (8 B per slot,
-    floor(T/64) + units slots), two carry states 2 x H x 128 x 128 f32, and the
-    blobs of all slots (66,048 B per slot and head), capped at 16 GiB of blobs
-    (then pieces of equal size)."""
+    floor(T/64) + units slots), one item counter per slot, two carry states
+    2 x H x 128 x 128 f32, and the operand blobs (66,048 B per slot and head):
+    all slots in one piece for a context-parallel call or few slots, else two
+    buffers of a quarter of the slots (pipelined pieces), the blobs capped at
+    16 GiB."""
+    from parity import split_layout, split_wanted_room
     lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
     lib.kda_chunk_fwd_prep_workspace_size.restype = ctypes.c_size_t
     base = lib.kda_chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)
     got = lib.kda_chunk_fwd_prep_workspace_size(N, T, H, 128, 128, cp, seg)
     plan = lib.kda_chunk_fwd_plan(N, T, H, 128, 128, cp, seg)
     units = (T // plan + N) if plan else N
-    nslots = T // 64 + units
-    per_slot = H * 66048
-    piece = max(1, min(nslots, min(nslots * per_slot, 16384 << 20) // per_slot))
-    pieces = -(-nslots // piece)
-    piece = -(-nslots // pieces)
-    area = _align256(nslots * 8) + _align256(2 * 2 * H * 128 * 128 * 4) + _align256(piece * per_slot)
+    room = split_wanted_room(T, H, units, plan != 0)
+    piece, nbuf, pieces, area = split_layout(T, H, units, room, plan != 0)
     assert got == _align256(base) + area
+    nslots = T // 64 + units
+    if plan == 0 and nslots >= 64 and units * H < 152:
+        assert nbuf == 2 and pieces >= 4
+    else:
+        assert nbuf * piece * H * 66048 <= (16384 << 20)
     # other shapes keep the one-kernel workspace
     assert lib.kda_chunk_fwd_prep_workspace_size(N, T, H, 64, 64, cp, seg) == \
         lib.kda_chunk_fwd_workspace_size(N, T, H, 64, 64, cp, seg)

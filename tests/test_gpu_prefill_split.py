@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import OUT_TOL, STATE_TOL, normwise_err, to64
+from parity import OUT_TOL, STATE_TOL, normwise_err, split_layout, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -46,16 +46,18 @@ def _align256(n):
     return (n + 255) // 256 * 256
 
 
-def piece_workspace(kda, x, slots, cp=0, seg=0):
-    """A workspace with room for the blobs of `slots` chunk slots (all heads):
-    the context-parallel scratch, the slot list, two carry states and the
-    blobs, laid out as the library lays them out."""
+def piece_workspace(kda, x, room, cp=0, seg=0):
+    """A workspace with room for the blobs of `room` chunk slots (all heads)
+    after the context-parallel scratch, the slot list, the item counters and
+    two carry states, laid out as the library lays them out; returns it with
+    the pieces it leads to."""
     N, (T, H) = x["cu"].shape[0] - 1, x["q"].shape[:2]
     plan = kda.chunk_fwd_plan(N, T, H, 128, 128, cp, seg)
     units = (T // plan + N) if plan else N
-    nbytes = (_align256(kda.chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)) + _align256((T // 64 + units) * 8) +
-              _align256(2 * 2 * H * 128 * 128 * 4) + slots * H * 66048)
-    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    _, _, pieces, _ = split_layout(T, H, units, room, plan != 0)
+    _, _, _, fixed = split_layout(T, H, units, 0, plan != 0)
+    nbytes = _align256(kda.chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)) + fixed + room * H * 66048
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda"), pieces
 
 
 def _run(kda, x, prep, cp=0, seg=0, scale=1.0, every=0, K=0, slots=None):
@@ -63,7 +65,7 @@ def _run(kda, x, prep, cp=0, seg=0, scale=1.0, every=0, K=0, slots=None):
     if every:
         N, H = x["cu"].shape[0] - 1, x["q"].shape[1]
         ck = torch.full((N, K, H, 128, 128), 7.0, device="cuda")
-    ws = piece_workspace(kda, x, slots, cp, seg) if (prep and slots) else None
+    ws = piece_workspace(kda, x, slots, cp, seg)[0] if (prep and slots) else None
     o, Sf = kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"], scale=scale,
                           cp_mode=cp, segment_len=seg, prep=prep, ckpt_every=every, ckpt=ck, workspace=ws)
     torch.cuda.synchronize()
@@ -71,12 +73,15 @@ def _run(kda, x, prep, cp=0, seg=0, scale=1.0, every=0, K=0, slots=None):
 
 
 CASES = {
-    # name: (lengths, H, cp_mode, segment_len, slots per piece or None (one piece), checkpoint every, count)
+    # name: (lengths, H, cp_mode, segment_len, blob room in slots or None (all), checkpoint every, count)
+    # (two buffers of room // 2 slots: pipelined pieces)
     "varlen_ragged": ([3 * 64 + 17, 0, 1, 64, 700], 3, 0, 0, None, 0, 0),
-    "pieces_varlen": ([1000, 130, 0, 640, 1], 4, 0, 0, 3, 0, 0),
-    "pieces_ckpt": ([640, 1000, 1536], 4, 0, 0, 7, 256, 6),
+    "pieces_varlen": ([1000, 130, 0, 640, 1], 4, 0, 0, 6, 0, 0),
+    "pieces_ckpt": ([640, 1000, 1536], 4, 0, 0, 14, 256, 6),
+    "pieces_serial": ([1000, 130, 0, 640, 1], 4, 0, 0, 1, 0, 0),
+    "pipeline_default": ([5000, 3000], 2, 0, 0, None, 0, 0),
     "cp_one_piece": ([5000], 2, 1, 1024, None, 0, 0),
-    "cp_pieces": ([3000, 0, 1500, 64], 2, 1, 1024, 7, 0, 0),
+    "cp_pieces": ([3000, 0, 1500, 64], 2, 1, 1024, 14, 0, 0),
     "cp_ckpt": ([4096], 2, 1, 1024, None, 768, 5),
 }
 
@@ -98,11 +103,11 @@ def test_two_kernel_form_equals_one_kernel_form(kda, name):
 
 
 def test_pieces_match_oracle(kda, oracle):
-    """Many pieces (3 slots each at H = 4): every unit of the three crosses
-    piece boundaries; outputs and final states within the oracle bars."""
+    """Many pipelined pieces (3 slots each at H = 4): every unit of the three
+    crosses piece boundaries; outputs and final states within the oracle bars."""
     lens = [700, 64, 0, 1300]
     x = _inputs(lens, 4, seed=5)
-    o, Sf, _ = _run(kda, x, prep=True, scale=0.75, slots=3)
+    o, Sf, _ = _run(kda, x, prep=True, scale=0.75, slots=6)
     o_ref, S_ref = oracle.prefill(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
                                   x["cu"].cpu().numpy(), S0=to64(x["S0"]), scale=0.75)
     assert normwise_err(to64(o), o_ref, head_axis=1) <= OUT_TOL
@@ -124,13 +129,39 @@ def test_two_kernel_form_reports_bad_seqlens(kda):
 def test_kernel_timing_counts_the_launches(kda):
     """Launch timing around one two-kernel call: one slot list, and one
     chunk-local launch and one walk per piece (5 pieces here)."""
-    x = _inputs([500, 300], 4, seed=3)  # 14 slots in pieces of 3 (5 pieces)
+    x = _inputs([500, 300], 4, seed=3)  # 14 slots in two buffers of 3 (5 pieces)
+    assert piece_workspace(kda, x, 6)[1] == 5
     kda.kernel_timing_start()
-    _run(kda, x, prep=True, slots=3)
+    _run(kda, x, prep=True, slots=6)
     kern = kda.kernel_timing_stop()
-    n_pieces = -(-(800 // 64 + 2) // 3)
+    n_pieces = 5
     assert kern["kda_chunk_list_kernel"]["launches"] == 1
     assert kern["kda_chunk_prep_kernel"]["launches"] == n_pieces
     assert kern["kda_chunk_walk_kernel"]["launches"] == n_pieces
     assert all(v["ms"] > 0 for v in kern.values())
     assert kda.kernel_timing_stop() == {}  # nothing recorded after stop
+
+
+def test_pipelined_pieces_on_a_side_stream_graph(kda):
+    """The pipelined form forks onto the library's two streams and joins back:
+    the caller's stream sees the whole call (a graph captured on it replays
+    the same bits as an eager call)."""
+    x = _inputs([5000, 3000], 2, seed=17)
+    ref = _run(kda, x, prep=True)
+    o = torch.empty_like(x["v"])
+    Sf = torch.empty(2, 2, 128, 128, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.chunk_fwd_prep_workspace_size(2, 8000, 2, 128, 128, 0), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"], out=o,
+                      final_state=Sf, cp_mode=0, workspace=ws)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"], out=o,
+                          final_state=Sf, cp_mode=0, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    o.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref[0]) and torch.equal(Sf, ref[1])

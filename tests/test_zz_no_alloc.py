@@ -73,24 +73,22 @@ def _with_workspace(x, seg):
 
 def _layout(lib, x, seg):
     """(pieces, two-kernel form?) that 64 MiB of scratch leads to, from the
-    library's own workspace arithmetic."""
+    library's workspace arithmetic."""
     import kda_gated_delta_02_gb300 as kda
+    from parity import split_layout
     T, H, _ = x["k"].shape
     N = x["cu"].shape[0] - 1
     cp = kda.chunk_fwd_workspace_size(N, T, H, 128, 128, kda.CP_ON, seg)
     units = T // kda.chunk_fwd_plan(N, T, H, 128, 128, kda.CP_ON, seg) + N
-    a = lambda n: (n + 255) // 256 * 256
-    room = (64 << 20) - a(cp) - a((T // 64 + units) * 8) - a(2 * 2 * H * 128 * 128 * 4)
-    per_slot = H * 66048
-    if room < per_slot:
-        return 0, False
-    nslots = T // 64 + units
-    return -(-nslots // min(nslots, room // per_slot)), True
+    fixed = split_layout(T, H, units, 0, True)[3]
+    room = ((64 << 20) - (cp + 255) // 256 * 256 - fixed) // (H * 66048)
+    pieces = split_layout(T, H, units, max(room, 0), True)[2]
+    return pieces, pieces > 0
 
 
 def test_noalloc_matches_workspace_entry_point_twice(lib, oracle):
     cases = [(_inputs([3000, 1500], 3, seed=1), 1024, (1, True)),   # one piece
-             (_inputs([8192], 8, seed=2), 1024, (2, True)),          # the slots in two pieces
+             (_inputs([8192], 8, seed=2), 1024, (3, True)),          # pipelined pieces
              (_inputs([2048], 96, seed=4), 1024, (0, False))]        # one-kernel form
     for x, seg, form in cases:  # calls in a row share the fixed scratch
         assert _layout(lib, x, seg) == form
