@@ -77,6 +77,44 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     return LIB
 
 
+def build_variant(tag: str, defines, force: bool = False) -> str:
+    """A second library, libkda_<tag>.so, from the same sources with extra
+    preprocessor defines (test builds: e.g. KDA_TEST_SHORT_FIRST_WAIT).  Only
+    the translation units that test the define are recompiled; the others
+    reuse the library's objects.  Returns its path."""
+    lib = build()
+    out = os.path.join(PKG, f"libkda_{tag}.so")
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(lib):
+        return out
+    vdir = os.path.join(BUILD, tag)
+    os.makedirs(vdir, exist_ok=True)
+    nvcc = nvcc_path()
+    dflags = [f"-D{d}" for d in defines]
+
+    def uses_define(src):
+        with open(src) as f:
+            text = f.read()
+        return any(d.split("=")[0] in text for d in defines)
+
+    def obj_for(src):
+        if not uses_define(src):
+            return os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(vdir, os.path.basename(src) + ".o")
+        r = subprocess.run([nvcc] + ARCH + NVCC_FLAGS + dflags + ["-c", src, "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(obj_for, sources()))
+    tmp = out + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose=True,
           extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None)

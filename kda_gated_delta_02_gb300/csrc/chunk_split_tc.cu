@@ -40,6 +40,15 @@ namespace sp {
 constexpr int D = 128;
 constexpr int CH = 64;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
+// The bound of the walk's first wait (on its first chunk's copy).  A test
+// build (KDA_TEST_SHORT_FIRST_WAIT) gives up on it at once, to exercise the
+// timeout path: status reported, the copy still in flight drained (full
+// bound), memory released.  The library itself uses the full bound.
+#ifdef KDA_TEST_SHORT_FIRST_WAIT
+constexpr uint32_t FIRST_WAIT_LIMIT = 0;
+#else
+constexpr uint32_t FIRST_WAIT_LIMIT = WAIT_LIMIT;
+#endif
 
 // operand blob of one (chunk, head): byte offsets, every tile 1024-aligned
 constexpr uint32_t BL_W = 0;        // W, MN-major (128 key rows i x 64 tokens t)     bf16
@@ -719,7 +728,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pm = (uint32_t)it & 1u;
         const int tc = t0 + CH * j, Lc = min(CH, t1 - tc);
         const uint32_t bb = W_BUF + (uint32_t)b * W_BUFSTRIDE;
-        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, WAIT_LIMIT);
+        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, j == jb ? FIRST_WAIT_LIMIT : WAIT_LIMIT);
         timed_out |= !landed;
         pend_b = landed ? -1 : b;  // a copy that has not landed is still in flight
         pend_ph = ph;

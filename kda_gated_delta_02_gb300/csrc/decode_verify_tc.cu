@@ -74,6 +74,15 @@ constexpr uint32_t TM_AB = 64;  // X KR^T, lanes 0-63 (32 columns)
 constexpr uint32_t TM_S = 0;    // K~^T U (128 columns, batch 3, after all of the above are read)
 constexpr uint32_t TMEM_COLS = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
+// The bound of thread 0's wait for the first batch of products.  A test build
+// (KDA_TEST_SHORT_FIRST_WAIT) gives up on it at once, to exercise the timeout
+// path: status reported, the copies and the products still in flight drained
+// (full bound), tensor memory freed.  The library itself uses the full bound.
+#ifdef KDA_TEST_SHORT_FIRST_WAIT
+constexpr uint32_t FIRST_WAIT_LIMIT = 0;
+#else
+constexpr uint32_t FIRST_WAIT_LIMIT = WAIT_LIMIT;
+#endif
 
 struct VtcParams {
     VerifyArgs a;
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     // thread 0 polls the MMA barrier (both commits); a CTA barrier releases
     // the rest, so `ok` is uniform across the CTA (the TMEM loads are
     // warp-collective)
-    if (tid == 0) ok = ok && umma::mbar_wait(bar0 + 8, 0, WAIT_LIMIT);
+    if (tid == 0) ok = ok && umma::mbar_wait(bar0 + 8, 0, FIRST_WAIT_LIMIT);
     ok = __syncthreads_and(ok) != 0;
     umma::fence_after();
 
