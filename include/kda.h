@@ -160,16 +160,22 @@ size_t kda_chunk_fwd_workspace_size(int N, int T, int H, int dk, int dv, int cp_
                                     int segment_len);
 
 /* Workspace bytes that select kda_chunk_fwd's two-kernel form (bf16 inputs,
- * dk = dv = 128) with all chunk slots in one piece: the CP scratch above, then
- * a slot list (8 bytes per 64-token chunk slot; floor(T / 64) + units slots,
- * units = sequences or segments), two carry states (2 x 2 x H x 128 x 128 f32)
- * and the operand blobs (66,048 bytes per slot and head), the blobs capped at
- * 16 GiB.  kda_chunk_fwd uses whatever
- * workspace it is given: room for fewer slots runs the slots in equal pieces
- * (one chunk-local launch and one walk per piece); room for none runs the
- * one-kernel form.  Equals kda_chunk_fwd_workspace_size for other shapes.
- * Pure host arithmetic; this form has no counterpart on the pages beyond the
- * chunk algebra it reorders. */
+ * dk = dv = 128) in the layout the call prefers: the CP scratch above, then a
+ * slot list (8 bytes per 64-token chunk slot; floor(T / 64) + units slots,
+ * units = sequences or segments), one 4-byte item counter per slot, two carry
+ * states (2 x 2 x H x 128 x 128 f32) and the operand blobs (66,048 bytes per
+ * slot and head).  A call whose walks leave SMs idle (units x H below the SM
+ * count) with at least 64 slots asks for two blob buffers of a quarter of the
+ * slots each: its four pieces are pipelined, the chunk-local kernel of piece
+ * p + 1 running as a programmatic dependent launch beside the walk of piece
+ * p.  Other calls, and context-parallel ones (whose transition blobs then
+ * serve the replay), ask for all slots in one piece.  Blobs are capped at 16
+ * GiB.  kda_chunk_fwd uses whatever workspace it is given: room for fewer
+ * slots runs smaller pieces (pipelined while two slots fit, else one at a
+ * time); room for none runs the one-kernel form.  Equals
+ * kda_chunk_fwd_workspace_size for other shapes.  Pure host arithmetic (it
+ * reads the SM count of the current device); this form has no counterpart
+ * on the pages beyond the chunk algebra it reorders and overlaps. */
 size_t kda_chunk_fwd_prep_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,
                                          int segment_len);
 
