@@ -238,10 +238,16 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
         e[r].z = __expf(fmaxf(e[r].z, g_min));
         e[r].w = __expf(fmaxf(e[r].w, g_min));
     }
+    // four products as two packed f32x2 multiplies (each lane rounds like a scalar multiply)
+    auto mul4 = [](float4 a, float4 b) {
+        const float2 lo = __fmul2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y));
+        const float2 hi = __fmul2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    };
     {
         float4 ph = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < 8; ++r) {  // (scalar: packed here costs registers)
             ph.x *= e[r].x;
             ph.y *= e[r].y;
             ph.z *= e[r].z;
@@ -250,7 +256,6 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
         *reinterpret_cast<float4 *>(sPart + (hf * 4 + i) * 128 + ch) = ph;
     }
     __syncthreads();
-    auto mul4 = [](float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); };
     float4 dl[4], pz;  // block decays; the other half's product for this thread's half
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -375,12 +380,15 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
             }
             if (!is_q) {
                 if (cg <= qd) {
-                    const float bt = sBeta[t];
+                    const float2 bt2 = make_float2(sBeta[t], sBeta[t]);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
+                    for (int j = 0; j < 16; j += 4) {
+                        const float2 a01 = __fmul2_rn(bt2, make_float2(v[j], v[j + 1]));
+                        const float2 a23 = __fmul2_rn(bt2, make_float2(v[j + 2], v[j + 3]));
                         *reinterpret_cast<float4 *>(sAf + t * LDF + s0 + j) =
-                            make_float4((s0 + j < t) ? bt * v[j] : 0.f, (s0 + j + 1 < t) ? bt * v[j + 1] : 0.f,
-                                        (s0 + j + 2 < t) ? bt * v[j + 2] : 0.f, (s0 + j + 3 < t) ? bt * v[j + 3] : 0.f);
+                            make_float4((s0 + j < t) ? a01.x : 0.f, (s0 + j + 1 < t) ? a01.y : 0.f,
+                                        (s0 + j + 2 < t) ? a23.x : 0.f, (s0 + j + 3 < t) ? a23.y : 0.f);
+                    }
                 }
             } else if (need_q) {
                 uint32_t bp[8];
@@ -433,10 +441,18 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
         {
             const int hb = (tid >> 6) & 1, r = (tid >> 2) & 15, c0 = 4 * (tid & 3);
             const int bi = 2 * hb + 1, bj = 2 * hb;
+            // packed f32x2 fused multiply-adds and adds (each lane rounds like the scalar op)
             auto fma4 = [](float a, float4 b, float4 acc) {
-                return make_float4(fmaf(a, b.x, acc.x), fmaf(a, b.y, acc.y), fmaf(a, b.z, acc.z), fmaf(a, b.w, acc.w));
+                const float2 a2 = make_float2(a, a);
+                const float2 lo = __ffma2_rn(a2, make_float2(b.x, b.y), make_float2(acc.x, acc.y));
+                const float2 hi = __ffma2_rn(a2, make_float2(b.z, b.w), make_float2(acc.z, acc.w));
+                return make_float4(lo.x, lo.y, hi.x, hi.y);
             };
-            auto add4 = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+            auto add4 = [](float4 a, float4 b) {
+                const float2 lo = __fadd2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y));
+                const float2 hi = __fadd2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w));
+                return make_float4(lo.x, lo.y, hi.x, hi.y);
+            };
             if (tid < 128) {
                 const float *Ar = sAf + (16 * bi + r) * LDF + 16 * bj;
                 const float *Tc = sTf + (16 * bj) * LDF + 16 * bj + c0;
@@ -522,8 +538,11 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
             const float4 tb4 = *reinterpret_cast<const float4 *>(sTf + t * LDF + s0 + 4);
             const float4 ba = *reinterpret_cast<const float4 *>(sBeta + s0);
             const float4 bb = *reinterpret_cast<const float4 *>(sBeta + s0 + 4);
-            const float v[8] = {ta.x * ba.x, ta.y * ba.y, ta.z * ba.z, ta.w * ba.w,
-                                tb4.x * bb.x, tb4.y * bb.y, tb4.z * bb.z, tb4.w * bb.w};
+            const float2 v01 = __fmul2_rn(make_float2(ta.x, ta.y), make_float2(ba.x, ba.y));
+            const float2 v23 = __fmul2_rn(make_float2(ta.z, ta.w), make_float2(ba.z, ba.w));
+            const float2 v45 = __fmul2_rn(make_float2(tb4.x, tb4.y), make_float2(bb.x, bb.y));
+            const float2 v67 = __fmul2_rn(make_float2(tb4.z, tb4.w), make_float2(bb.z, bb.w));
+            const float v[8] = {v01.x, v01.y, v23.x, v23.y, v45.x, v45.y, v67.x, v67.y};
             uint32_t pk[4];
 #pragma unroll
             for (int j = 0; j < 8; j += 2)
@@ -763,10 +782,12 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
                 const float4 gm = *reinterpret_cast<const float4 *>(gam + 32 * cg + c);
-                Sreg[c + 0] *= gm.x;
-                Sreg[c + 1] *= gm.y;
-                Sreg[c + 2] *= gm.z;
-                Sreg[c + 3] *= gm.w;
+                const float2 lo = __fmul2_rn(make_float2(Sreg[c], Sreg[c + 1]), make_float2(gm.x, gm.y));
+                const float2 hi = __fmul2_rn(make_float2(Sreg[c + 2], Sreg[c + 3]), make_float2(gm.z, gm.w));
+                Sreg[c + 0] = lo.x;
+                Sreg[c + 1] = lo.y;
+                Sreg[c + 2] = hi.x;
+                Sreg[c + 3] = hi.y;
             }
             umma::st32(tq + TM_ST + 32 * cg, Sreg);
         }
