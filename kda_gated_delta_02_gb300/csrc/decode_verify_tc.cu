@@ -258,15 +258,17 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     float yq[HT], yk[HT], yv[HT];
 #pragma unroll
     for (int j = 0; j < HT; ++j) {
-        float sq = 0.f, sk = 0.f, sv = 0.f;
+        // q and k taps as packed f32x2 fused multiply-adds (each lane rounds like fmaf)
+        float2 sqk = make_float2(0.f, 0.f);
+        float sv = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (i < W) {
-                sq = fmaf(wq[i], bf2f(rq[j + i]), sq);
-                sk = fmaf(wk[i], bf2f(rk[j + i]), sk);
+                sqk = __ffma2_rn(make_float2(wq[i], wk[i]), make_float2(bf2f(rq[j + i]), bf2f(rk[j + i])), sqk);
                 sv = fmaf(wv[i], bf2f(rv[j + i]), sv);
             }
         }
+        float sq = sqk.x, sk = sqk.y;
         if (silu) {  // y / (1 + e^{-y}); the fast quotient is 0 where e^{-y} overflows, the limit
             sq = __fdividef(sq, 1.f + __expf(-sq));
             sk = __fdividef(sk, 1.f + __expf(-sk));
@@ -305,8 +307,9 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         float v[16];
 #pragma unroll
         for (int j = 0; j < HT; ++j) {
-            v[j] = yq[j] * yq[j];
-            v[HT + j] = yk[j] * yk[j];
+            const float2 sq2 = __fmul2_rn(make_float2(yq[j], yk[j]), make_float2(yq[j], yk[j]));
+            v[j] = sq2.x;
+            v[HT + j] = sq2.y;
         }
         const float s = warp_transpose_sum<16>(v, lane);
         if ((lane & 1) == 0) sPart[warp * 16 + (lane >> 1)] = s;
@@ -504,7 +507,11 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         }
         float s2[HT];
 #pragma unroll
-        for (int j = 0; j < HT; ++j) s2[j] = o[j] * o[j];
+        for (int j = 0; j < HT; j += 2) {
+            const float2 o2 = __fmul2_rn(make_float2(o[j], o[j + 1]), make_float2(o[j], o[j + 1]));
+            s2[j] = o2.x;
+            s2[j + 1] = o2.y;
+        }
         const float tot = warp_transpose_sum<8>(s2, lane);
         if ((lane & 3) == 0) sPart2[warp * 8 + (lane >> 2)] = tot;
     }
@@ -530,8 +537,9 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
                 uint32_t out[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack_bf16(w[e]);
-                    out[e] = pack_bf16(fmaf(xa, f.x, acc[8 * j + 2 * e]), fmaf(xa, f.y, acc[8 * j + 2 * e + 1]));
+                    const float2 r2 = __ffma2_rn(make_float2(xa, xa), unpack_bf16(w[e]),
+                                                 make_float2(acc[8 * j + 2 * e], acc[8 * j + 2 * e + 1]));
+                    out[e] = pack_bf16(r2.x, r2.y);
                 }
                 sts128(ad, out[0], out[1], out[2], out[3]);
             }
