@@ -74,8 +74,10 @@ extern "C" {
 #define KDA_KERNEL_SEGMENT_COMPOSE 5 /* CP composition */
 #define KDA_KERNEL_SEGMENT_TABLE 6   /* CP segment table */
 #define KDA_KERNEL_VERIFY 7          /* kda_decode_verify_replay (verify or single-token decode) */
-#define KDA_KERNEL_CHUNK_BWD 8       /* kda_chunk_bwd */
-#define KDA_KERNEL_KINDS 9
+#define KDA_KERNEL_CHUNK_BWD 8       /* kda_chunk_bwd on the CUDA cores (d = 64 or f32 inputs) */
+#define KDA_KERNEL_BWD_WALK 9        /* kda_chunk_bwd, tensor cores: reverse state walk */
+#define KDA_KERNEL_BWD_CHUNK 10      /* kda_chunk_bwd, tensor cores: chunk gradients */
+#define KDA_KERNEL_KINDS 11
 
 /* Human-readable name of a return status. Never NULL. */
 const char *kda_status_string(int status);

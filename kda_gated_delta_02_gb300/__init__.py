@@ -276,7 +276,8 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
 # kernel families of kda_kernel_timing_stop, in KDA_KERNEL_* order
 KERNEL_FAMILIES = ("kda_chunk_list_kernel", "kda_chunk_prep_kernel", "kda_chunk_walk_kernel",
                    "kda_chunk_tc_kernel", "kda_chunk_kernel", "kda_compose_kernel", "kda_segment_table_kernel",
-                   "kda_decode_verify_replay", "kda_chunk_bwd_kernel")
+                   "kda_decode_verify_replay", "kda_chunk_bwd_kernel", "kda_bwd_walk_kernel",
+                   "kda_bwd_chunk_kernel")
 
 
 def chunk_fwd_host(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,

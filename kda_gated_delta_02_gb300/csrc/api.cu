@@ -560,13 +560,50 @@ int kda_decode_verify_replay_ragged(void *state, void *conv_tail, const float *c
     return cuda_status(timed_launch(KDA_KERNEL_VERIFY, st, [&] { return kda::launch_verify(a, st); }));
 }
 
+namespace {
+// Workspace of the tensor-core backward (d = 128, bf16): per (slot, head) the
+// forward pass's operand blob, T and M^T (f32), the walk's S^T and U^T tiles
+// and the reverse walk's dS'^T and dU'^T tiles; the slot list and the item
+// counters in front.
+struct BwdTcLayout {
+    size_t nslots, off_list, off_claim, off_blob, off_aux, off_s, off_u, off_ds, off_du, total;
+};
+BwdTcLayout bwd_tc_layout(int N, int T, int H) {
+    BwdTcLayout L;
+    L.nslots = (size_t)T / kChunk + N;
+    const size_t sh = L.nslots * H;
+    size_t off = 0;
+    L.off_list = off;
+    off += align256(L.nslots * sizeof(int2));
+    L.off_claim = off;
+    off += 256;
+    L.off_blob = off;
+    off += align256(sh * kda::kChunkBlobBytes);
+    L.off_aux = off;
+    off += align256(sh * 32768);
+    L.off_s = off;
+    off += align256(sh * 32768);
+    L.off_u = off;
+    off += align256(sh * 16384);
+    L.off_ds = off;
+    off += align256(sh * 32768);
+    L.off_du = off;
+    off += align256(sh * 16384);
+    L.total = off;
+    return L;
+}
+}  // namespace
+
 size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
     if (N < 1 || T < 0 || H < 1 || dk != dv || !dim_ok(dk)) return 0;
     const size_t DD = (size_t)dk * dv * 4;
     const size_t units = (size_t)N * H, slots = units < (size_t)kda::kBwdMaxCtas ? units : (size_t)kda::kBwdMaxCtas;
     const size_t parts = slots * (size_t)(dk / 32) * 2 * kda::chunk_bwd_partial_floats(dk) * 4;
-    return align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD) + align256(parts) +
-           align256((size_t)T * H * dk * 4);
+    const size_t cores = align256((size_t)(T / kChunk + N) * H * DD) + align256(slots * kChunk * DD) +
+                         align256(parts) + align256((size_t)T * H * dk * 4);
+    if (dk != 128) return cores;
+    const size_t tc = bwd_tc_layout(N, T, H).total;  // bf16 inputs take the tensor-core form
+    return tc > cores ? tc : cores;
 }
 
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -587,6 +624,43 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     const size_t DD = (size_t)dk * dv * 4;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dk == 128 && in_dtype == KDA_DTYPE_BF16) {
+        // the chunk (WY) form on the tensor cores: forward pass keeping its
+        // operands, reverse state walk, chunk gradients
+        const BwdTcLayout L = bwd_tc_layout(N, T, H);
+        const int nslots = (int)L.nslots;
+        int2 *list = reinterpret_cast<int2 *>(ws + L.off_list);
+        int *claim = reinterpret_cast<int *>(ws + L.off_claim);
+        unsigned char *blob = ws + L.off_blob;
+        float *aux = reinterpret_cast<float *>(ws + L.off_aux);
+        kda::ChunkArgs fa = {};
+        fa.q = q; fa.k = k; fa.v = v; fa.g = g; fa.beta = beta; fa.o = nullptr;
+        fa.T = T; fa.H = H; fa.dk = dk; fa.dv = dv; fa.scale = scale; fa.g_min = g_min;
+        fa.mode = kda::MODE_SEQ; fa.cu_seqlens = cu_seqlens; fa.S_init = initial_state; fa.status = status;
+        kda::BwdTcArgs b = {};
+        b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.cu_seqlens = cu_seqlens;
+        b.N = N; b.T = T; b.H = H; b.scale = scale; b.g_min = g_min; b.dS_final = dS_final;
+        b.dq = dq; b.dk = dk_; b.dv = dv_; b.dg = dg; b.dbeta = dbeta; b.dS0 = dS0;
+        b.list = list; b.claim = claim + 1; b.blob = blob; b.aux = aux;
+        b.save_s = ws + L.off_s; b.save_u = ws + L.off_u; b.save_ds = ws + L.off_ds; b.save_du = ws + L.off_du;
+        b.status = status;
+        cudaError_t e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st);
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(fa, N, nslots, list, st); });
+        if (e == cudaSuccess && T > 0)
+            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
+                return kda::launch_chunk_prep(fa, list, 0, nslots, blob, true, claim, false, st, aux);
+            });
+        if (e == cudaSuccess && T > 0)
+            e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+                return kda::launch_chunk_walk(fa, N, blob, 0, nslots, nullptr, nullptr, st, ws + L.off_s, ws + L.off_u);
+            });
+        if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] { return kda::launch_bwd_walk(b, st); });
+        if (e == cudaSuccess && T > 0)
+            e = timed_launch(KDA_KERNEL_BWD_CHUNK, st, [&] { return kda::launch_bwd_chunk(b, nslots, st); });
+        return cuda_status(e);
+    }
     kda::BwdArgs a = {};
     a.q = q; a.k = k; a.v = v; a.dout = dout; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
     a.S0 = initial_state; a.dS_final = dS_final;
@@ -600,7 +674,6 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     a.wbuf = reinterpret_cast<float *>(
         ws + off_par + align256(slots * (size_t)(dk / 32) * 2 * kda::chunk_bwd_partial_floats(dk) * 4));
     a.N = N; a.T = T; a.H = H; a.scale = scale; a.g_min = g_min; a.status = status;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,
                                     [&] { return kda::launch_chunk_bwd(a, dk, in_dtype == KDA_DTYPE_BF16, st); }));
 }

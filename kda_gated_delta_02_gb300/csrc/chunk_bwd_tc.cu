@@ -1,0 +1,988 @@
+// chunk_bwd_tc.cu -- backward of the tensor-core prefill (dk = dv = 128, bf16
+// inputs) in the chunk (WY) form: the chunk kernel's training use ("Noyaux KDA
+// et FlashKDA", section "FlashKDA : le noyau par blocs").
+//
+// For a 64-token chunk entered with state S (gamma the running sum of the
+// floored log-decays per key channel, Gam = e^gamma, Gam_C its last value,
+// K~ = K Gam, Q~ = Q Gam, K^ = K Gam_C / Gam, M = strict_lower(K~ (K / Gam)^T),
+// A = diag(b) M, T = (I + A)^{-1}, TB = T diag(b), W = TB K~):
+//     Vres = V - K~ S,  U = TB Vres,  O = scale (Q~ S + B U),
+//     S_C = diag(Gam_C) S + K^^T U.
+// Only the state gradient dS_C (arriving at the chunk end) is serial; it is
+// the adjoint of the forward walk on the same operand blobs:
+//     dU = scale B^T dO + K^ dS_C,  dS = scale Q~^T dO + diag(Gam_C) dS_C - W^T dU.
+// Given the chunk-start state S and dS_C, every chunk's token gradients are
+// local (the reverse of each forward step):
+//     dVres = TB^T dU (= dv),  dTB = dU Vres^T,  dT = dTB diag(b),
+//     dbeta_s = sum_t dTB[t][s] T[t][s] + sum_s' dA[s][s'] M[s][s'],
+//     dA = strict_lower(-T^T dT T^T),  dM = diag(b) dA,  dB = scale lower(dO U^T),
+//     dQ~ = scale dO S^T + (dB through the causal tiles),
+//     dK~ = -dVres S^T + (dM through the causal tiles),  dK^ = U dS_C^T,
+//     dgamma_C += Gam_C . rowsum(dS_C . S)
+// and the log-decay gradient is the reverse cumulative sum of the gradient of
+// gamma.  The causal tiles M and B carry the forward's 16-token block
+// anchoring: row t (block i) is L_t = k_t x_t (x_t = e^{gamma_t - gamma_a},
+// a = the token before block i), column s of row block i is
+// R_i[s] = k_s e^{gamma_a - gamma_s}; so with A' holding dM and dB in the
+// segment columns of each row's block, dL = A' R_seg (rows) and
+// dR_seg = A'^T L (columns), both single tensor-core products, and
+// dk_t += x_t dL_t, dk_s += sum_i f_i(s) dR_i[s] (f_i(s) = e^{gamma_a_i - gamma_s}),
+// dgamma = k . dk-terms with the signs of their exponents.
+//
+// Three launches after the forward pass (which keeps every blob, the fp32 T
+// and M of every chunk, and the walk's bf16 operand tiles S^T and U^T):
+//   kda_bwd_walk_kernel   one CTA per (sequence, head), chunks in reverse: dS'
+//                         = dS / scale resident in tensor memory, the four
+//                         products of a chunk on the tensor cores; keeps the
+//                         bf16 tiles dS'^T and dU'^T of every chunk;
+//   kda_bwd_chunk_kernel  persistent over (chunk, head) items: nine products
+//                         per item on the tensor cores (operands in shared
+//                         memory, accumulators in tensor memory), the rest on
+//                         the CUDA cores in fp32.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace bt {
+
+constexpr int D = 128;
+constexpr int CH = 64;
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+constexpr uint32_t TILE_S = 32768;  // bf16 S^T / dS'^T tile (K-major 128 x 128)
+constexpr uint32_t TILE_U = 16384;  // bf16 U^T / dU'^T tile (K-major 128 x 64)
+constexpr uint32_t AUX_FLOATS = 8192;
+
+// first row of segment i of the anchored column operand: 8 i (i + 1)
+__host__ __device__ constexpr int segoff(int i) { return 8 * i * (i + 1); }
+
+__device__ __forceinline__ float bf16_at(const void *base, size_t idx) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// ============================================================================ reverse walk
+constexpr int NR = 512;
+constexpr uint32_t R_BUF = 0;          // two operand blobs (double buffer)
+constexpr uint32_t R_BUFSTRIDE = 66560;
+constexpr uint32_t R_DO = 133120;      // two dO tiles (value halves of [64 t][128 B], 8 KB apart)
+constexpr uint32_t R_ST = 165888;      // dS'^T bf16, K-major 128 x 128
+constexpr uint32_t R_UT = 198656;      // dU'^T bf16, K-major 128 x 64
+constexpr uint32_t R_BAR = 215040;     // 4 mbarriers: buffer 0, buffer 1, dU product, dS products
+constexpr uint32_t R_TMEM = 215072;
+constexpr uint32_t R_SMEM = 215088 + 1024;
+constexpr uint32_t TM_S = 0, TM_U = 128;  // 256 columns
+
+struct RwalkParams {
+    const int32_t *cu;             // [N + 1]
+    int N, T, H;
+    CUtensorMap tdo;               // dout [T][H][128] bf16, box 64 x 1 x 64, 128-byte swizzle
+    const unsigned char *blob;     // [slot][H][kChunkBlobBytes]
+    const float *dS_final;         // [N][H][128][128] or null (zero)
+    float *dS0;                    // [N][H][128][128] or null
+    float wscale;                  // the state gradient walks as dS / wscale
+    int zero_do;                   // scale == 0: dO enters no product
+    unsigned char *save_ds, *save_du;  // [slot][H] tiles dS'^T (32 KB), dU'^T (16 KB)
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_constant__ RwalkParams P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t sb4 = sb >> 4;
+    const uint32_t bar0 = sb + R_BAR, bar_u = bar0 + 16, bar_o = bar0 + 24;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x, h = blockIdx.y, H = P.H;
+    const int t0 = P.cu[n], t1 = P.cu[n + 1];
+    const size_t uoff = ((size_t)n * H + h) * D * D;
+    if (t0 < 0 || t1 < t0 || t1 > P.T) {
+        if (tid == 0 && h == 0) report_status(P.status, KDA_STATUS_BAD_SEQLENS);
+        return;
+    }
+    const int nch = (t1 - t0 + CH - 1) / CH, sbase = t0 / CH + n;
+    if (nch == 0) {  // an empty sequence passes its final-state gradient through
+        if (P.dS0)
+            for (int e = tid; e < D * D; e += NR) P.dS0[uoff + e] = P.dS_final ? P.dS_final[uoff + e] : 0.f;
+        return;
+    }
+    const float wscale = P.wscale, inv = 1.0f / wscale;
+
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b) umma::mbar_init(bar0 + 8 * b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 0) umma::tmem_alloc(sb + R_TMEM, 256);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<const uint32_t *>(sm + R_TMEM);
+    const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, column group
+    const int jrow = 32 * qd + lane;          // dS'^T row (value column j) owned
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+
+    {  // dS'^T = dS_final^T / wscale (lane j, columns = key channel i)
+        float r[32];
+        const float *src = P.dS_final ? P.dS_final + uoff : nullptr;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) r[c] = src ? src[(size_t)(32 * cg + c) * D + jrow] * inv : 0.f;
+        umma::st32(tq + TM_S + 32 * cg, r);
+    }
+
+    // one thread issues the copies of a chunk: the blob (one bulk copy) and dO
+    // (two swizzled value halves; rows past the tensor end are zero-filled,
+    // rows past the sequence end are zeroed after arrival)
+    auto issue = [&](int j, int b) {
+        if (tid == 0) {
+            umma::fence_proxy_async();
+            const uint32_t bar = bar0 + 8 * b;
+            umma::mbar_expect_tx(bar, kChunkBlobBytes + 16384u);
+            umma::bulk_load(sb + R_BUF + b * R_BUFSTRIDE, P.blob + ((size_t)(sbase + j) * H + h) * kChunkBlobBytes,
+                            kChunkBlobBytes, bar);
+            umma::tma_load_3d(sb + R_DO + b * 16384, &P.tdo, 0, h, t0 + CH * j, bar);
+            umma::tma_load_3d(sb + R_DO + b * 16384 + 8192, &P.tdo, 64, h, t0 + CH * j, bar);
+        }
+    };
+
+    bool timed_out = false;
+    int pend_b = 0;  // buffer with a copy in flight (the next chunk's, or one whose wait gave up)
+    uint32_t pend_ph = 0;
+    int pend_m = -1;  // products whose completion wait gave up (0: dU, 1: dS)
+    uint32_t pend_mph = 0;
+    const bool save = P.save_ds != nullptr;
+    issue(nch - 1, 0);
+
+    for (int j = nch - 1; j >= 0; --j) {
+        const int it = nch - 1 - j, b = it & 1;
+        const uint32_t ph = (uint32_t)(it >> 1) & 1u, pm = (uint32_t)it & 1u;
+        const int tc = t0 + CH * j, Lc = min(CH, t1 - tc);
+        const uint32_t bb = R_BUF + (uint32_t)b * R_BUFSTRIDE;
+        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, WAIT_LIMIT);
+        timed_out |= !landed;
+        pend_b = landed ? -1 : b;
+        pend_ph = ph;
+        if (j > 0 && !timed_out) {
+            issue(j - 1, b ^ 1);
+            pend_b = b ^ 1;
+            pend_ph = (uint32_t)((it + 1) >> 1) & 1u;
+        }
+        const int z0 = P.zero_do ? 0 : Lc;  // dO rows (tokens) past the sequence end are not ours
+        for (int idx = tid; idx < (CH - z0) * 16; idx += NR) {
+            const int r = z0 + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4 *>(sm + R_DO + b * 16384 + (c >> 3) * 8192 + umma::mnmaj(8 * (c & 7), r, 1)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the previous chunk's saved tiles have been read before they are overwritten
+        if (save && it > 0) {
+            if (tid == 0) umma::bulk_wait_read();
+            __syncthreads();
+        }
+        // dS'^T (this thread's lane, columns 32 cg ..) as the bf16 operand, and
+        // the resident gradient decayed in place, dS'^T diag(Gam_C), onto
+        // which the dO^T Q~ and -dU'^T W products accumulate
+        {
+            const float *gam = reinterpret_cast<const float *>(sm + bb + kBlobGam);
+            float r[32];
+            umma::ld32(tq + TM_S + 32 * cg, r);
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(r[c + 0], r[c + 1]);
+                pk.y = pack_bf16(r[c + 2], r[c + 3]);
+                pk.z = pack_bf16(r[c + 4], r[c + 5]);
+                pk.w = pack_bf16(r[c + 6], r[c + 7]);
+                *reinterpret_cast<uint4 *>(sm + R_ST + umma::kmaj(jrow, 32 * cg + c, 128)) = pk;
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 gm = *reinterpret_cast<const float4 *>(gam + 32 * cg + c);
+                const float2 lo = __fmul2_rn(make_float2(r[c], r[c + 1]), make_float2(gm.x, gm.y));
+                const float2 hi = __fmul2_rn(make_float2(r[c + 2], r[c + 3]), make_float2(gm.z, gm.w));
+                r[c + 0] = lo.x;
+                r[c + 1] = lo.y;
+                r[c + 2] = hi.x;
+                r[c + 3] = hi.y;
+            }
+            umma::st32(tq + TM_S + 32 * cg, r);
+        }
+        umma::fence_proxy_async();
+        umma::fence_before();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
+
+        // ------------------------------------------------------------ dU'^T = dO^T B + dS'^T K^^T; dS'^T += dO^T Q~
+        if (tid == 0) {
+            umma::fence_after();
+            // A = dO^T (MN-major: value halves 8 KB apart, 8-token groups 1 KB);
+            // B = the blob's B read as MN-major (n = key token s, k = query token t)
+            constexpr uint32_t id_a = umma::idesc_bf16(128, 64, 1, 1, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma::mma(tmem + TM_U, umma::sdesc4(sb4 + ((R_DO + b * 16384 + ks * 2048) >> 4), 8192, 1024),
+                          umma::sdesc4(sb4 + ((bb + kBlobBM + ks * 2048) >> 4), 1024, 1024), id_a, ks > 0 ? 1u : 0u);
+            // A = dS'^T (K-major); B = K^ read as K-major (n = t, k = i: 8-token groups 2 KB apart)
+            constexpr uint32_t id_b = umma::idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                umma::mma(tmem + TM_U, umma::sdesc4(sb4 + ((R_ST + kb * 16384 + kin) >> 4), 16, 1024),
+                          umma::sdesc4(sb4 + ((bb + kBlobKT + kb * 1024 + kin) >> 4), 16, 2048), id_b, 1u);
+            }
+            umma::commit(bar_u);
+            // B = Q~ read as MN-major (n = i: 64-channel blocks 8 KB apart, k = t)
+            constexpr uint32_t id_c = umma::idesc_bf16(128, 128, 1, 1, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma::mma(tmem + TM_S, umma::sdesc4(sb4 + ((R_DO + b * 16384 + ks * 2048) >> 4), 8192, 1024),
+                          umma::sdesc4(sb4 + ((bb + kBlobQT + ks * 2048) >> 4), 8192, 1024), id_c, 1u);
+            if (save) {
+                umma::bulk_store(P.save_ds + ((size_t)(sbase + j) * H + h) * TILE_S, sb + R_ST, TILE_S);
+                umma::bulk_commit();
+            }
+        }
+        if (!umma::mbar_wait(bar_u, pm, WAIT_LIMIT)) {
+            timed_out = true;
+            pend_m = 0;
+            pend_mph = pm;
+        }
+        umma::fence_after();
+
+        // ------------------------------------------------------------ dU'^T (bf16) operand
+        {
+            float v[16];
+            umma::ld16(tq + TM_U + 16 * cg, v);
+#pragma unroll
+            for (int c = 0; c < 16; c += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(v[c + 0], v[c + 1]);
+                pk.y = pack_bf16(v[c + 2], v[c + 3]);
+                pk.z = pack_bf16(v[c + 4], v[c + 5]);
+                pk.w = pack_bf16(v[c + 6], v[c + 7]);
+                *reinterpret_cast<uint4 *>(sm + R_UT + umma::kmaj(jrow, 16 * cg + c, 128)) = pk;
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before();
+        if (__syncthreads_or(timed_out)) {
+            timed_out = true;
+            break;
+        }
+
+        // ------------------------------------------------------------ dS'^T -= dU'^T W
+        if (tid == 0) {
+            umma::fence_after();
+            // B = W read as K-major (n = key channel i, k = t), negated
+            constexpr uint32_t id_d = umma::idesc_bf16(128, 128, 0, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma::mma(tmem + TM_S, umma::sdesc4(sb4 + ((R_UT + ks * 32) >> 4), 16, 1024),
+                          umma::sdesc4(sb4 + ((bb + kBlobW + ks * 32) >> 4), 16, 1024), id_d, 1u);
+            umma::commit(bar_o);
+            if (save) {
+                umma::bulk_store(P.save_du + ((size_t)(sbase + j) * H + h) * TILE_U, sb + R_UT, TILE_U);
+                umma::bulk_commit();
+            }
+        }
+        if (!umma::mbar_wait(bar_o, pm, WAIT_LIMIT)) {
+            timed_out = true;
+            pend_m = 1;
+            pend_mph = pm;
+        }
+        umma::fence_after();
+    }
+
+    if (timed_out) {
+        if (tid == 0) report_status(P.status, KDA_STATUS_TIMEOUT);
+        // let a copy still in flight land and products still running finish
+        // before the shared and tensor memory are released
+        if (pend_b >= 0) umma::mbar_wait(bar0 + 8 * pend_b, pend_ph, WAIT_LIMIT);
+        if (pend_m >= 0) umma::mbar_wait(pend_m ? bar_o : bar_u, pend_mph, WAIT_LIMIT);
+    } else if (P.dS0) {
+        float r[32];
+        umma::ld32(tq + TM_S + 32 * cg, r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) P.dS0[uoff + (size_t)(32 * cg + c) * D + jrow] = r[c] * wscale;
+    }
+    if (save && tid == 0) umma::bulk_wait_all();
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================ chunk gradients
+constexpr int NB = 256;
+// shared memory, 1024-aligned regions.  Phases A and B (the first three
+// product batches):
+constexpr uint32_t B_SB = 0;        // S^T bf16 [j][i] (K-major 128 x 128)
+constexpr uint32_t B_DS = 32768;    // dS'^T bf16 [j][i]
+constexpr uint32_t B_DO = 65536;    // [dO ; -dVres] K-major 128 rows x 128 (rows 0-63 by TMA)
+constexpr uint32_t B_VR = 98304;    // Vres^T bf16 [j][s]
+constexpr uint32_t B_UB = 114688;   // U^T bf16 [j][t]   (B_VR + 16 KB: second M block of [Vres; U])
+constexpr uint32_t B_DU = 131072;   // dU'^T bf16 [j][t]
+constexpr uint32_t B_DOT = 147456;  // dO^T bf16 [j][t]  (B_DU + 16 KB: second N block of [dU'; dO])
+constexpr uint32_t B_TBL = 147456;  //   before that: the low bf16 part of T diag(b)
+constexpr uint32_t B_KT = 163840;   // K~, MN-major (n = t, k = i)
+constexpr uint32_t B_TB = 180224;   // T diag(b), MN-major (n = s, k = t)
+constexpr uint32_t B_TF = 188416;   // T f32 [64][64]
+constexpr uint32_t B_MT = 204800;   // M^T f32 [64][64]
+// phases C and D, over the phase A / B regions once the second batch is done
+// (A' in two bf16 parts, high and low: the anchored products cancel between
+// their row and column sides in the log-decay gradient, so A' keeps about 16
+// mantissa bits):
+constexpr uint32_t B_AP = 0;        // A' high part, K-major 128 rows x 192 (three K blocks of 16 KB)
+constexpr uint32_t B_APL = 49152;   // A' low part
+constexpr uint32_t B_T16 = 98304;   // T bf16 K-major 64 x 64
+constexpr uint32_t B_DT = 106496;   // dT, MN-major (m = t, k = s)
+constexpr uint32_t B_ZT = 114688;   // -Z, MN-major (n = b, k = t)
+constexpr uint32_t B_RS = 122880;   // R_seg^T K-major 128 channels x 192 (three K blocks)
+constexpr uint32_t B_LT = 188416;   // L^T K-major 128 channels x 128 (two K blocks), over T and M^T
+                                    // once the beta gradient has read them
+constexpr uint32_t B_MISC = 221184;
+constexpr uint32_t B_BETA = B_MISC;           // f32 [64]
+constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
+constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [2][128] halves of rowsum(dS' . S)
+constexpr uint32_t B_DBP = B_DGC + 1024;      // f32 [4][64] beta gradient parts
+constexpr uint32_t B_CUM = B_DBP + 1024;      // f32 [3][128] decay-gradient sums of the halves
+constexpr uint32_t B_BAR = B_CUM + 1536;      // 6 mbarriers: loads, five product batches
+constexpr uint32_t B_TMEM = B_BAR + 48;
+constexpr uint32_t B_CLAIM = B_TMEM + 8;
+constexpr uint32_t B_SMEM = B_CLAIM + 8 + 1024;
+static_assert(B_RS + 49152 <= B_TF, "phase C regions overlap the kept T and M");
+static_assert(B_LT + 32768 <= B_MISC, "L^T");
+static_assert(B_SMEM <= 232448, "shared memory");
+// tensor-memory columns of the products
+constexpr uint32_t T1 = 0, T2 = 64, T3 = 0, T4 = 320, T5 = 448, T6 = 128, T7 = 192, T8 = 0, T9 = 128;
+
+struct BchunkParams {
+    const void *k, *q, *v;           // bf16 [T][H][128]
+    const float *g, *beta;           // [T][H][128], [T][H]
+    int H;
+    float scale, wscale, g_min;
+    int zero_do;
+    const int2 *list;                // slot -> {first token, length}
+    int nitems;                      // slots x H; item w = slot * H + h
+    int *claim;                      // item counter, zero at launch
+    const unsigned char *save_s, *save_u, *save_ds, *save_du;  // [slot][H] tiles
+    const float *aux;                // [slot][H][2][64][64]: T, M^T
+    CUtensorMap tdo;                 // dout box 64 x 1 x 64, 128-byte swizzle
+    float *dq, *dk, *dv, *dg, *dbeta;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_constant__ BchunkParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t sb4 = sb >> 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, hf = warp >> 2;
+    const int l = 32 * qd + lane;  // TMEM lane: channel / value column / row owned
+    const int H = p.H;
+    float *sBeta = reinterpret_cast<float *>(sm + B_BETA);
+    float *sPart = reinterpret_cast<float *>(sm + B_PART);
+    float *sDgc = reinterpret_cast<float *>(sm + B_DGC);
+    float *sDbp = reinterpret_cast<float *>(sm + B_DBP);
+    float *sCum = reinterpret_cast<float *>(sm + B_CUM);
+    const float *sTF = reinterpret_cast<const float *>(sm + B_TF);
+    const float *sMT = reinterpret_cast<const float *>(sm + B_MT);
+    int *sClaim = reinterpret_cast<int *>(sm + B_CLAIM);
+    const uint32_t bar = sb + B_BAR;  // bar + 8 k: k = 0 loads, 1..5 product batches
+    const float scale = p.scale, wscale = p.wscale, g_min = p.g_min;
+
+    if (tid == 0) {
+        for (int b = 0; b < 6; ++b) umma::mbar_init(bar + 8 * b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        sClaim[0] = atomicAdd(p.claim, 1);
+    }
+    if (warp == 0) umma::tmem_alloc(sb + B_TMEM, 512);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<const uint32_t *>(sm + B_TMEM);
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
+    int w = sClaim[0];
+    uint32_t it = 0;
+    bool alive = true;
+
+    while (w < p.nitems) {
+    const int slot = w / H, h = w % H;
+    const int2 cl = p.list[slot];
+    const int tc = cl.x, Lc = cl.y;
+    const uint32_t par = it & 1u;
+    if (Lc > 0) {
+    uint32_t pend = 0;  // barriers whose wait gave up
+    // ---------------------------------------------------------------- loads
+    if (tid == 0) {
+        umma::fence_proxy_async();
+        umma::mbar_expect_tx(bar, 2 * TILE_S + 2 * TILE_U + 4 * AUX_FLOATS + 16384u);
+        umma::bulk_load(sb + B_SB, p.save_s + (size_t)w * TILE_S, TILE_S, bar);
+        umma::bulk_load(sb + B_DS, p.save_ds + (size_t)w * TILE_S, TILE_S, bar);
+        umma::bulk_load(sb + B_UB, p.save_u + (size_t)w * TILE_U, TILE_U, bar);
+        umma::bulk_load(sb + B_DU, p.save_du + (size_t)w * TILE_U, TILE_U, bar);
+        umma::bulk_load(sb + B_TF, p.aux + (size_t)w * AUX_FLOATS, 4 * AUX_FLOATS, bar);
+        umma::tma_load_3d(sb + B_DO, &p.tdo, 0, h, tc, bar);
+        umma::tma_load_3d(sb + B_DO + 16384, &p.tdo, 64, h, tc, bar);
+    }
+    // thread (channel ch = l, half hf): tokens 32 hf .. 32 hf + 31.  x, y:
+    // running products of e^{g} from the start of the token's 16-token block
+    // (inclusive) and to its end (exclusive); k and q of each token as a bf16 pair
+    const int ch = l;
+    float x[32], y[32];
+    uint32_t kq[32];
+    uint32_t below = 0;  // bit u: g < g_min (no gradient)
+    {
+        float e[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = 32 * hf + u;
+            const bool ok = t < Lc;
+            const size_t row = ((size_t)(tc + t) * H + h) * D + ch;
+            const float gv = ok ? p.g[row] : 0.f;
+            below |= (ok && gv < g_min) ? (1u << u) : 0u;
+            e[u] = __expf(fmaxf(gv, g_min));
+            const uint32_t kb = ok ? (uint32_t)reinterpret_cast<const uint16_t *>(p.k)[row] : 0u;
+            const uint32_t qb = ok ? (uint32_t)reinterpret_cast<const uint16_t *>(p.q)[row] : 0u;
+            kq[u] = kb | (qb << 16);
+        }
+#pragma unroll
+        for (int bl = 0; bl < 2; ++bl) {
+            x[16 * bl] = e[16 * bl];
+#pragma unroll
+            for (int u = 16 * bl + 1; u < 16 * bl + 16; ++u) x[u] = x[u - 1] * e[u];
+            y[16 * bl + 15] = 1.f;
+#pragma unroll
+            for (int u = 16 * bl + 14; u >= 16 * bl; --u) y[u] = y[u + 1] * e[u + 1];
+        }
+    }
+    sPart[(2 * hf) * 128 + ch] = x[15];
+    sPart[(2 * hf + 1) * 128 + ch] = x[31];
+    if (tid < CH) sBeta[tid] = (tid < Lc) ? p.beta[(size_t)(tc + tid) * H + h] : 0.f;
+    __syncthreads();
+    float dl[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) dl[m] = sPart[m * 128 + ch];
+    // products of the block decays before / after each of this thread's blocks
+    const float pre0 = hf ? dl[0] * dl[1] : 1.f, pre1 = hf ? pre0 * dl[2] : dl[0];
+    const float post1 = hf ? 1.f : dl[2] * dl[3], post0 = hf ? dl[3] : dl[1] * post1;
+    auto kf = [&](int u) { return __uint_as_float(kq[u] << 16); };
+    auto qf = [&](int u) { return __uint_as_float(kq[u] & 0xFFFF0000u); };
+    // K~ = K Gam as the MN-major B operand of (K~ S)^T (n = t, k = i = ch)
+#pragma unroll
+    for (int u = 0; u < 32; u += 8) {
+        float v8[8];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) v8[e2] = kf(u + e2) * ((u + e2) < 16 ? pre0 : pre1) * x[u + e2];
+        sts128(sb + B_KT + umma::mnmaj(32 * hf + u, ch, 1), pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
+               pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+    }
+    pend |= umma::mbar_wait(bar, par, WAIT_LIMIT) ? 0u : 1u;
+    {  // dO rows past the chunk end (every row when dO enters no product) are zero
+        const int z0 = p.zero_do ? 0 : Lc;
+        for (int idx = tid; idx < (CH - z0) * 16; idx += NB) {
+            const int r = z0 + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4 *>(sm + B_DO + (c >> 3) * 16384 + r * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    {  // T diag(b) as the MN-major B operand of dVres^T (n = s, k = t), high and low bf16 parts
+        const int t = tid >> 2, s0 = 16 * (tid & 3);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int s = s0 + 8 * hh;
+            float tb[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) tb[e2] = sTF[t * 64 + s + e2] * sBeta[s + e2];
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; e2 += 2) {
+                hi[e2 >> 1] = pack_bf16(tb[e2], tb[e2 + 1]);
+                const float2 h2 = unpack_bf16(hi[e2 >> 1]);
+                lo[e2 >> 1] = pack_bf16(tb[e2] - h2.x, tb[e2 + 1] - h2.y);
+            }
+            sts128(sb + B_TB + umma::mnmaj(s, t, 1), hi[0], hi[1], hi[2], hi[3]);
+            sts128(sb + B_TBL + umma::mnmaj(s, t, 1), lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 1: (K~ S)^T, dVres^T / wscale
+    if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t id1 = umma::idesc_bf16(128, 64, 0, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T1, umma::sdesc4(sb4 + ((B_SB + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((B_KT + ks * 2048) >> 4), 1024, 1024), id1, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T2, umma::sdesc4(sb4 + ((B_DU + (ks & 3) * 32) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + (((ks < 4 ? B_TB : B_TBL) + (ks & 3) * 2048) >> 4), 1024, 1024), id1,
+                      ks > 0 ? 1u : 0u);
+        umma::commit(bar + 8);
+    }
+    pend |= umma::mbar_wait(bar + 8, par, WAIT_LIMIT) ? 0u : 2u;
+    umma::fence_after();
+    {  // thread (value column j = l, half hf)
+        const int j = l;
+        float a[32];
+        umma::ld32(tq + T1 + 32 * hf, a);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = 32 * hf + u;
+            const float vv = (t < Lc) ? bf16_at(p.v, ((size_t)(tc + t) * H + h) * D + j) : 0.f;
+            a[u] = vv - a[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 32; u += 8)
+            sts128(sb + B_VR + umma::kmaj(j, 32 * hf + u, 128), pack_bf16(a[u], a[u + 1]), pack_bf16(a[u + 2], a[u + 3]),
+                   pack_bf16(a[u + 4], a[u + 5]), pack_bf16(a[u + 6], a[u + 7]));
+        umma::ld32(tq + T2 + 32 * hf, a);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int s = 32 * hf + u;
+            const float dvr = a[u] * wscale;
+            if (s < Lc) p.dv[((size_t)(tc + s) * H + h) * D + j] = dvr;
+            sts16(sb + B_DO + umma::kmaj(64 + s, j, 128), bf16_bits(-dvr));
+        }
+        // dO^T row j from column j of the dO tile
+#pragma unroll
+        for (int u = 0; u < 32; u += 8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; e2 += 2) {
+                const uint32_t lo = lds16(sb + B_DO + umma::kmaj(32 * hf + u + e2, j, 128));
+                const uint32_t hi = lds16(sb + B_DO + umma::kmaj(32 * hf + u + e2 + 1, j, 128));
+                pk[e2 >> 1] = lo | (hi << 16);
+            }
+            sts128(sb + B_DOT + umma::kmaj(j, 32 * hf + u, 128), pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 2: [Vres; U][dU'; dO]^T, S [dO; -dVres]^T, dS' U^T
+    if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t id3 = umma::idesc_bf16(128, 128, 1, 1, 0);
+        constexpr uint32_t id4 = umma::idesc_bf16(128, 128, 1, 0, 0);
+        constexpr uint32_t id5 = umma::idesc_bf16(128, 64, 1, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T3, umma::sdesc4(sb4 + ((B_VR + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 16384, 1024), id3, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T4, umma::sdesc4(sb4 + ((B_SB + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_DO + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4), 16, 1024), id4,
+                      ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T5, umma::sdesc4(sb4 + ((B_DS + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id5, ks > 0 ? 1u : 0u);
+        umma::commit(bar + 16);
+    }
+    {  // rowsum(dS' . S) for key channel ch over this half's value columns
+        float acc = 0.f;
+#pragma unroll 8
+        for (int jj = 0; jj < 64; ++jj) {
+            const int j = 64 * hf + jj;
+            const float a = __uint_as_float((uint32_t)lds16(sb + B_DS + umma::kmaj(j, ch, 128)) << 16);
+            const float b = __uint_as_float((uint32_t)lds16(sb + B_SB + umma::kmaj(j, ch, 128)) << 16);
+            acc = fmaf(a, b, acc);
+        }
+        sDgc[hf * 128 + ch] = acc;
+    }
+    pend |= umma::mbar_wait(bar + 16, par, WAIT_LIMIT) ? 0u : 4u;
+    umma::fence_after();
+    __syncthreads();  // every thread is done with the S and dS' tiles
+    // the phase A / B regions are free: zero A', and T in bf16
+    for (int idx = tid; idx < 2 * 49152 / 16; idx += NB)
+        *reinterpret_cast<uint4 *>(sm + B_AP + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
+    {
+        const int t = tid >> 2, s0 = 16 * (tid & 3);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int s = s0 + 8 * hh;
+            const float4 a0 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s + 4);
+            sts128(sb + B_T16 + umma::kmaj(t, s, 64), pack_bf16(a0.x, a0.y), pack_bf16(a0.z, a0.w),
+                   pack_bf16(a1.x, a1.y), pack_bf16(a1.z, a1.w));
+        }
+    }
+    __syncthreads();
+    if (qd < 2) {  // lanes 0-63: s = l; columns t: dTB[t][s] / wscale
+        const int s = l;
+        float a[32];
+        umma::ld32(tq + T3 + 32 * hf, a);
+        const float bs = sBeta[s];
+        float dbp = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = 32 * hf + u;
+            const float dtb = a[u] * wscale;
+            dbp = fmaf(dtb, sTF[t * 64 + s], dbp);
+            a[u] = dtb * bs;
+        }
+        sDbp[hf * 64 + s] = dbp;
+#pragma unroll
+        for (int u = 0; u < 32; u += 8)
+            sts128(sb + B_DT + umma::kmaj(s, 32 * hf + u, 64), pack_bf16(a[u], a[u + 1]), pack_bf16(a[u + 2], a[u + 3]),
+                   pack_bf16(a[u + 4], a[u + 5]), pack_bf16(a[u + 6], a[u + 7]));
+    } else {  // lanes 64-127: s = l - 64; columns 64 + t: (dO U^T)[t][s]
+        const int s = l - 64;
+        float a[32];
+        umma::ld32(tq + T3 + 64 + 32 * hf, a);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = 32 * hf + u;
+            if (t >= s) {
+                const uint32_t o = umma::kmaj(64 + t, segoff(t >> 4) + s, 128);
+                const float x = scale * a[u];
+                const uint16_t hb = bf16_bits(x);
+                sts16(sb + B_AP + o, hb);
+                sts16(sb + B_APL + o, bf16_bits(x - __uint_as_float((uint32_t)hb << 16)));
+            }
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 3: Z = dT T^T
+    if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t id6 = umma::idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            umma::mma(tmem + T6, umma::sdesc4(sb4 + ((B_DT + ks * 2048) >> 4), 8192, 1024),
+                      umma::sdesc4(sb4 + ((B_T16 + ks * 32) >> 4), 16, 1024), id6, ks > 0 ? 1u : 0u);
+        umma::commit(bar + 24);
+    }
+    {  // meanwhile the anchored column operand R_seg^T
+        // column factor of segment i for a token of block bk: 1 / delta_bk when
+        // i = bk, else the decays of the blocks strictly between
+#pragma unroll
+        for (int bl = 0; bl < 2; ++bl) {
+            const int bk = 2 * hf + bl;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < bk) continue;
+                float c = 1.f;
+                if (i == bk) {
+                    c = __frcp_rn(dl[bk]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m > bk && m < i) c *= dl[m];
+                }
+#pragma unroll
+                for (int u8 = 0; u8 < 16; u8 += 8) {
+                    float a[8];
+#pragma unroll
+                    for (int e2 = 0; e2 < 8; ++e2) {
+                        const int u = 16 * bl + u8 + e2;
+                        a[e2] = kf(u) * (y[u] * c);
+                    }
+                    sts128(sb + B_RS + umma::kmaj(ch, segoff(i) + 16 * bk + u8, 128), pack_bf16(a[0], a[1]),
+                           pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+                }
+            }
+        }
+    }
+    pend |= umma::mbar_wait(bar + 24, par, WAIT_LIMIT) ? 0u : 8u;
+    umma::fence_after();
+    if (qd < 2) {  // -Z as the MN-major B operand (n = b, k = t): row t = l
+        float a[32];
+        umma::ld32(tq + T6 + 32 * hf, a);
+#pragma unroll
+        for (int u = 0; u < 32; u += 8)
+            sts128(sb + B_ZT + umma::kmaj(l, 32 * hf + u, 64), pack_bf16(-a[u], -a[u + 1]), pack_bf16(-a[u + 2], -a[u + 3]),
+                   pack_bf16(-a[u + 4], -a[u + 5]), pack_bf16(-a[u + 6], -a[u + 7]));
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 4: dA = T^T (-Z)
+    if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t id7 = umma::idesc_bf16(128, 64, 1, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            umma::mma(tmem + T7, umma::sdesc4(sb4 + ((B_T16 + ks * 2048) >> 4), 8192, 1024),
+                      umma::sdesc4(sb4 + ((B_ZT + ks * 2048) >> 4), 1024, 1024), id7, ks > 0 ? 1u : 0u);
+        umma::commit(bar + 32);
+    }
+    pend |= umma::mbar_wait(bar + 32, par, WAIT_LIMIT) ? 0u : 16u;
+    umma::fence_after();
+    if (qd < 2) {  // row a = l of dA (strictly lower): beta gradient, dM into A'
+        const int a = l;
+        float v[32];
+        umma::ld32(tq + T7 + 32 * hf, v);
+        const float ba = sBeta[a];
+        float dbp = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int b = 32 * hf + u;
+            if (b < a) {
+                dbp = fmaf(v[u], sMT[b * 64 + a], dbp);
+                const uint32_t o = umma::kmaj(a, segoff(a >> 4) + b, 128);
+                const float x = ba * v[u];
+                const uint16_t hb = bf16_bits(x);
+                sts16(sb + B_AP + o, hb);
+                sts16(sb + B_APL + o, bf16_bits(x - __uint_as_float((uint32_t)hb << 16)));
+            }
+        }
+        sDbp[128 + hf * 64 + a] = dbp;
+    }
+    __syncthreads();  // T and M^T read: L^T goes over them
+    // the anchored row operand L^T (row ch: k x, then q x)
+#pragma unroll
+    for (int u = 0; u < 32; u += 8) {
+        float a[8], b[8];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) {
+            a[e2] = kf(u + e2) * x[u + e2];
+            b[e2] = qf(u + e2) * x[u + e2];
+        }
+        sts128(sb + B_LT + umma::kmaj(ch, 32 * hf + u, 128), pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]),
+               pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+        sts128(sb + B_LT + umma::kmaj(ch, 64 + 32 * hf + u, 128), pack_bf16(b[0], b[1]), pack_bf16(b[2], b[3]),
+               pack_bf16(b[4], b[5]), pack_bf16(b[6], b[7]));
+    }
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+
+    // ---------------------------------------------------------------- batch 5: dL = A' R_seg, dR_seg = A'^T L
+    if (tid == 0) {
+        umma::fence_after();
+        constexpr uint32_t id8 = umma::idesc_bf16(128, 128, 0, 0, 0);
+        constexpr uint32_t id9 = umma::idesc_bf16(128, 160, 0, 1, 0);
+#pragma unroll
+        for (int pt = 0; pt < 2; ++pt) {  // A' high part, then low part
+            const uint32_t ap = pt ? B_APL : B_AP;
+#pragma unroll
+            for (int ks = 0; ks < 10; ++ks) {
+                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                umma::mma(tmem + T8, umma::sdesc4(sb4 + ((B_RS + kb * 16384 + kin) >> 4), 16, 1024),
+                          umma::sdesc4(sb4 + ((ap + kb * 16384 + kin) >> 4), 16, 1024), id8, (pt || ks > 0) ? 1u : 0u);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+                umma::mma(tmem + T9, umma::sdesc4(sb4 + ((B_LT + kb * 16384 + kin) >> 4), 16, 1024),
+                          umma::sdesc4(sb4 + ((ap + ks * 2048) >> 4), 16384, 1024), id9, (pt || ks > 0) ? 1u : 0u);
+            }
+        }
+        umma::commit(bar + 40);
+    }
+    if (tid < CH && tid < Lc)
+        p.dbeta[(size_t)(tc + tid) * H + h] = (sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]);
+    pend |= umma::mbar_wait(bar + 40, par, WAIT_LIMIT) ? 0u : 32u;
+    umma::fence_after();
+
+    // ---------------------------------------------------------------- token gradients of channel ch
+    {
+        const float gamC = dl[0] * dl[1] * dl[2] * dl[3];
+        const float dgc = gamC * wscale * (sDgc[ch] + sDgc[128 + ch]);
+        float dgam[32];
+        float sh = 0.f;  // sum over this half of dK^ . K^
+#pragma unroll
+        for (int u0 = 0; u0 < 32; u0 += 8) {
+            const int bl = u0 >> 4, bk = 2 * hf + bl;
+            const int t0 = 32 * hf + u0;
+            float a4[8], a5[8], a6[8], a7[8], a8[8];
+            umma::ld8(tq + T4 + t0, a4);       // S dO^T
+            umma::ld8(tq + T4 + 64 + t0, a5);  // -S dVres^T
+            umma::ld8(tq + T5 + t0, a6);       // dS' U^T
+            umma::ld8(tq + T8 + t0, a7);       // dL (k rows)
+            umma::ld8(tq + T8 + 64 + t0, a8);  // dL (q rows)
+            float kc[8], rr[8];  // sum_i f_i dR_i, and sum_i R_i dR_i with R_i as the product read it (bf16)
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) kc[e2] = rr[e2] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < bk) continue;
+                float c = 1.f;
+                if (i == bk) {
+                    c = __frcp_rn(dl[bk]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m > bk && m < i) c *= dl[m];
+                }
+                float r8[8];
+                umma::ld8(tq + T9 + segoff(i) + t0, r8);
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2) {
+                    const float f = y[u0 + e2] * c;
+                    kc[e2] = fmaf(f, r8[e2], kc[e2]);
+                    rr[e2] = fmaf(bf16_round(kf(u0 + e2) * f), r8[e2], rr[e2]);
+                }
+            }
+            const float pre = bl ? pre1 : pre0, post = bl ? post1 : post0;
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) {
+                const int u = u0 + e2, t = t0 + e2;
+                const float xx = x[u], gam = pre * xx, suf = y[u] * post;
+                const float kk = kf(u), qq = qf(u);
+                const float dqs = scale * a4[e2];
+                const float dq = fmaf(dqs, gam, xx * a8[e2]);
+                const float kh = wscale * a6[e2] * suf;
+                const float dk = fmaf(a5[e2], gam, xx * a7[e2]) + kc[e2] + kh;
+                // the anchored terms with the bf16 values of L and R_seg that the
+                // products used: each (row, column) pair inside [t, 63] then
+                // cancels in the reverse cumulative sum as it does exactly
+                dgam[u] = fmaf(dqs, qq * gam, a5[e2] * (kk * gam)) - kh * kk +
+                          fmaf(bf16_round(kk * xx), a7[e2], bf16_round(qq * xx) * a8[e2]) - rr[e2];
+                sh = fmaf(kh, kk, sh);
+                if (t < Lc) {
+                    const size_t o = ((size_t)(tc + t) * H + h) * D + ch;
+                    p.dq[o] = dq;
+                    p.dk[o] = dk;
+                }
+            }
+        }
+        float tot = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) tot += dgam[u];
+        if (hf) sCum[ch] = tot;
+        sCum[128 * (1 + hf) + ch] = sh;
+        __syncthreads();
+        // gamma_C (and the K^ factors through it) collects at the chunk's last
+        // token, so it adds to the reverse cumulative sum at every token
+        float acc = dgc + sCum[128 + ch] + sCum[256 + ch] + (hf ? 0.f : sCum[ch]);
+#pragma unroll
+        for (int u = 31; u >= 0; --u) {
+            acc += dgam[u];
+            const int t = 32 * hf + u;
+            if (t < Lc) p.dg[((size_t)(tc + t) * H + h) * D + ch] = ((below >> u) & 1u) ? 0.f : acc;
+        }
+    }
+    umma::fence_before();
+    ++it;
+    if (__syncthreads_or(pend != 0)) {  // uniform: leave once the copies and products in flight are done
+        if (pend & 1u) umma::mbar_wait(bar, par, WAIT_LIMIT);
+        for (int b = 1; b < 6; ++b)
+            if (pend & (1u << b)) umma::mbar_wait(bar + 8 * b, par, WAIT_LIMIT);
+        alive = false;
+        break;
+    }
+    }  // Lc > 0
+    if (tid == 0) sClaim[0] = atomicAdd(p.claim, 1);
+    __syncthreads();
+    w = sClaim[0];
+    __syncthreads();  // the claim was read by every thread before thread 0 writes the next
+    }  // items
+    if (!alive && tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace bt
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// dout [T][H][128] bf16, box 64 x 1 head x 64 tokens, 128-byte swizzle
+bool encode_dout(CUtensorMap *m, const void *dout, int T, int H) {
+    if (T <= 0) return true;  // no chunk: the map is never used
+    EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128u, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {256u, 256u * (cuuint64_t)H};
+    cuuint32_t box[3] = {64u, 1u, 64u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(dout), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+cudaError_t launch_bwd_walk(const BwdTcArgs &a, cudaStream_t st) {
+    if (a.N <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(bt::kda_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bt::R_SMEM);
+    if (e != cudaSuccess) return e;
+    bt::RwalkParams P;
+    memset(&P, 0, sizeof(P));
+    P.cu = a.cu_seqlens;
+    P.N = a.N;
+    P.T = a.T;
+    P.H = a.H;
+    if (!encode_dout(&P.tdo, a.dout, a.T, a.H)) return cudaErrorInvalidValue;
+    P.blob = a.blob;
+    P.dS_final = a.dS_final;
+    P.dS0 = a.dS0;
+    P.zero_do = a.scale == 0.f ? 1 : 0;
+    P.wscale = a.scale == 0.f ? 1.f : a.scale;
+    P.save_ds = a.save_ds;
+    P.save_du = a.save_du;
+    P.status = a.status;
+    bt::kda_bwd_walk_kernel<<<dim3(a.N, a.H), bt::NR, bt::R_SMEM, st>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st) {
+    if (nslots <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(bt::kda_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bt::B_SMEM);
+    if (e != cudaSuccess) return e;
+    bt::BchunkParams P;
+    memset(&P, 0, sizeof(P));
+    P.k = a.k;
+    P.q = a.q;
+    P.v = a.v;
+    P.g = a.g;
+    P.beta = a.beta;
+    P.H = a.H;
+    P.scale = a.scale;
+    P.zero_do = a.scale == 0.f ? 1 : 0;
+    P.wscale = a.scale == 0.f ? 1.f : a.scale;
+    P.g_min = a.g_min;
+    P.list = a.list;
+    P.nitems = nslots * a.H;
+    P.claim = a.claim;
+    P.save_s = a.save_s;
+    P.save_u = a.save_u;
+    P.save_ds = a.save_ds;
+    P.save_du = a.save_du;
+    P.aux = a.aux;
+    if (!encode_dout(&P.tdo, a.dout, a.T, a.H)) return cudaErrorInvalidValue;
+    P.dq = a.dq;
+    P.dk = a.dk;
+    P.dv = a.dv;
+    P.dg = a.dg;
+    P.dbeta = a.dbeta;
+    P.status = a.status;
+    static int sms = 0;
+    if (sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            cudaGetLastError();
+            sms = 152;
+        }
+    }
+    const int grid = P.nitems < sms ? P.nitems : sms;  // persistent: one CTA per SM
+    bt::kda_bwd_chunk_kernel<<<grid, bt::NB, bt::B_SMEM, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -51,12 +51,12 @@ constexpr uint32_t FIRST_WAIT_LIMIT = WAIT_LIMIT;
 #endif
 
 // operand blob of one (chunk, head): byte offsets, every tile 1024-aligned
-constexpr uint32_t BL_W = 0;        // W, MN-major (128 key rows i x 64 tokens t)     bf16
-constexpr uint32_t BL_TB = 16384;   // T diag(b), K-major 64 x 64                     bf16
-constexpr uint32_t BL_QT = 24576;   // Q e^gamma, K-major 64 x 128                     bf16
-constexpr uint32_t BL_KT = 40960;   // K e^{gamma_63 - gamma}, MN-major (s x dk)        bf16
-constexpr uint32_t BL_BM = 57344;   // B, K-major 64 x 64 (masked, diagonal included)  bf16
-constexpr uint32_t BL_GAM = 65536;  // e^{gamma_63} per key channel                     f32 [128]
+constexpr uint32_t BL_W = kBlobW;      // W, MN-major (128 key rows i x 64 tokens t)     bf16
+constexpr uint32_t BL_TB = kBlobTB;    // T diag(b), K-major 64 x 64                     bf16
+constexpr uint32_t BL_QT = kBlobQT;    // Q e^gamma, K-major 64 x 128                     bf16
+constexpr uint32_t BL_KT = kBlobKT;    // K e^{gamma_63 - gamma}, MN-major (s x dk)        bf16
+constexpr uint32_t BL_BM = kBlobBM;    // B, K-major 64 x 64 (masked, diagonal included)  bf16
+constexpr uint32_t BL_GAM = kBlobGam;  // e^{gamma_63} per key channel                     f32 [128]
 static_assert(BL_GAM + 512 == kChunkBlobBytes, "blob layout");
 
 // rows of R_i start at row 8 i (i+1): 0, 16, 48, 96 (16 (i+1) rows each)
@@ -133,12 +133,18 @@ struct PrepParams {
     int nitems;          // (slot1 - slot0) * H items, w = (slot - slot0) * H + h
     int *claim;          // item counter of this launch, zero at launch; CTAs claim items in order
     unsigned char *blob; // [w][kChunkBlobBytes]
+    float *aux;          // backward's forward pass only: [w][2][64][64] T (row t) and M^T (row s)
     int need_q;          // 0: transitions only (no Q~, no B)
     int pf_beta;         // tb is encoded (H a multiple of 4)
     uint32_t *status;
 };
 
-__global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_constant__ PrepParams p) {
+// The body of the chunk-local kernel.  AUX (the forward pass that a backward
+// runs) also keeps, per item, the fp32 dependency inverse T and the strictly
+// lower tile M = (K x)(K / x)^T before the beta scaling, which the backward's
+// chunk kernel needs and the blob does not hold.
+template <bool AUX>
+__device__ __forceinline__ void prep_body(const PrepParams &p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -379,6 +385,11 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;
             }
             if (!is_q) {
+                if constexpr (AUX) {  // M^T [s][t], strictly lower M, zero elsewhere
+                    float *mt = p.aux + (size_t)w * 8192 + 4096;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) mt[(s0 + j) * 64 + t] = (s0 + j < t) ? v[j] : 0.f;
+                }
                 if (cg <= qd) {
                     const float2 bt2 = make_float2(sBeta[t], sBeta[t]);
 #pragma unroll
@@ -519,6 +530,11 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
             __syncthreads();
             product(sTf + 32 * LDF + 32, X64, acc);  // T_22 X
             const int t = 32 + 16 * mt + gq, s0 = 8 * nt + 2 * q4;
+            if constexpr (AUX) {  // T_21 = -T_22 X in fp32
+                float *ta = p.aux + (size_t)w * 8192;
+                *reinterpret_cast<float2 *>(ta + t * 64 + s0) = make_float2(-acc[0], -acc[1]);
+                *reinterpret_cast<float2 *>(ta + (t + 8) * 64 + s0) = make_float2(-acc[2], -acc[3]);
+            }
             const float b0 = sBeta[s0], b1 = sBeta[s0 + 1];
             *reinterpret_cast<uint32_t *>(sm + P_TB + umma::kmaj(t, s0, 64)) = pack_bf16(-acc[0] * b0, -acc[1] * b1);
             *reinterpret_cast<uint32_t *>(sm + P_TB + umma::kmaj(t + 8, s0, 64)) = pack_bf16(-acc[2] * b0, -acc[3] * b1);
@@ -548,6 +564,14 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
             for (int j = 0; j < 8; j += 2)
                 pk[j >> 1] = pack_bf16((s0 + j <= t) ? v[j] : 0.f, (s0 + j + 1 <= t) ? v[j + 1] : 0.f);
             *reinterpret_cast<uint4 *>(sm + P_TB + umma::kmaj(t, s0, 64)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if constexpr (AUX) {  // the same blocks of T in fp32, zero above the diagonal
+                float *dst = p.aux + (size_t)w * 8192 + t * 64 + s0;
+                *reinterpret_cast<float4 *>(dst) = make_float4((s0 <= t) ? ta.x : 0.f, (s0 + 1 <= t) ? ta.y : 0.f,
+                                                              (s0 + 2 <= t) ? ta.z : 0.f, (s0 + 3 <= t) ? ta.w : 0.f);
+                *reinterpret_cast<float4 *>(dst + 4) =
+                    make_float4((s0 + 4 <= t) ? tb4.x : 0.f, (s0 + 5 <= t) ? tb4.y : 0.f, (s0 + 6 <= t) ? tb4.z : 0.f,
+                                (s0 + 7 <= t) ? tb4.w : 0.f);
+            }
         }
     }
     umma::fence_proxy_async();
@@ -614,6 +638,13 @@ __global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_con
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+__global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_kernel(const __grid_constant__ PrepParams p) {
+    prep_body<false>(p);
+}
+__global__ void __launch_bounds__(NT1, 2) kda_chunk_prep_aux_kernel(const __grid_constant__ PrepParams p) {
+    prep_body<true>(p);
+}
+
 // ============================================================================ state walk
 constexpr int NT2 = 512;
 constexpr uint32_t W_BUF = 0;           // two operand blobs (double buffer)
@@ -633,6 +664,10 @@ struct WalkParams {
     int slot0, slot1;
     const float *carry_in;       // [tiles][H][128][128]: state of the unit cut at slot0
     float *carry_out;            // state of the unit cut at slot1
+    // backward's forward pass: per (slot, head) the bf16 operand tiles the walk
+    // builds, S^T at the chunk start (K-major 128 x 128, 32 KB) and U^T
+    // (K-major 128 x 64, 16 KB), indexed by absolute slot; null for none
+    unsigned char *save_s, *save_u;
 };
 
 __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_constant__ WalkParams P) {
@@ -672,7 +707,8 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
     const bool transition = p.mode == MODE_TRANSITION;
     const bool m_part = transition && tile == 0;  // augmented columns [0, dk): M
     const bool has_v = !m_part;
-    const bool need_q = !transition;
+    const bool need_q = !transition && p.o != nullptr;  // outputs wanted
+    const bool save = P.save_s != nullptr;
     const int vcol0 = transition ? 0 : tile * D;
 
     // ---------------------------------------------------------------- setup
@@ -763,6 +799,12 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                     make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        // the previous chunk's saved tiles have been read out of shared memory
+        // before they are overwritten
+        if (save && it > 0) {
+            if (tid == 0) umma::bulk_wait_read();
+            __syncthreads();
+        }
         // S^T (this thread's TMEM lane, columns 32 cg ..) as the bf16 operand of
         // the products, and the resident state decayed to the chunk end in place,
         // Diag-cols(e^{gamma_63}) S^T, onto which the U^T K~ product accumulates
@@ -817,6 +859,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                           (has_v || ks > 0) ? 1u : 0u);
             }
             umma::commit(bar_u);
+            if (save) {
+                umma::bulk_store(P.save_s + ((size_t)(sbase + j) * H + h) * 32768u, sb + W_ST, 32768u);
+                umma::bulk_commit();
+            }
             if (need_q) {
                 constexpr uint32_t idq = umma::idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
@@ -869,6 +915,10 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                 umma::mma(tmem + TM_ST, a, umma::sdesc4(sb4 + ((bb + BL_KT + ks * 4096) >> 4), 1024, 2048), ids, 1u);
             }
             umma::commit(bar_o);
+            if (save && P.save_u) {
+                umma::bulk_store(P.save_u + ((size_t)(sbase + j) * H + h) * 16384u, sb + W_UT, 16384u);
+                umma::bulk_commit();
+            }
         }
         if (!umma::mbar_wait(bar_o, pm, WAIT_LIMIT)) {
             timed_out = true;
@@ -897,6 +947,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         // ------------------------------------------------------------ outputs
         // staged as a row-major [64][128] bf16 tile over U^T (read by the
         // products that just completed), then written with 16-byte stores
+        // (no outputs in a pass that saves the tiles)
         unsigned char *ostage = sm + W_UT;
         if (need_q) {  // staged whatever the wait returned; the barrier below decides
             float v[16];
@@ -956,6 +1007,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
             for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * ld_dst + col0 + jrow] = Sreg[c];
         }
     }
+    if (save && tid == 0) umma::bulk_wait_all();  // saved tiles written before the shared memory goes
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tmem, 256);
@@ -1004,10 +1056,10 @@ bool encode_rows(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
 }  // namespace
 
 cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
-                              bool need_q, int *claim, bool after_walk, cudaStream_t st) {
+                              bool need_q, int *claim, bool after_walk, cudaStream_t st, float *aux) {
     if (slot1 <= slot0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(sp::kda_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         sp::P_SMEM);
+    auto kern = aux ? sp::kda_chunk_prep_aux_kernel : sp::kda_chunk_prep_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sp::P_SMEM);
     if (e != cudaSuccess) return e;
     sp::PrepParams P;
     memset(&P, 0, sizeof(P));
@@ -1024,6 +1076,7 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
     P.status = a.status;
     P.nitems = (slot1 - slot0) * a.H;
     P.claim = claim;
+    P.aux = aux;
     // prefetch boxes (H is a multiple of 4 for the beta box; other H prefetch nothing there)
     bool ok = encode_rows(&P.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, a.H, a.T, 128, 1) &&
               encode_rows(&P.tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, a.H, a.T, 128, 1) &&
@@ -1054,13 +1107,15 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_walk ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, sp::kda_chunk_prep_kernel, P);
+    return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char *blob, int slot0, int slot1,
-                              const float *carry_in, float *carry_out, cudaStream_t st) {
+                              const float *carry_in, float *carry_out, cudaStream_t st, unsigned char *save_s,
+                              unsigned char *save_u) {
     const int ntiles = (a.mode == MODE_TRANSITION) ? 2 : 1;
     if (units <= 0) return cudaSuccess;
+    if (save_s && (a.o || a.mode != MODE_SEQ)) return cudaErrorInvalidValue;  // the saving pass has no outputs
     cudaError_t e = cudaFuncSetAttribute(sp::kda_chunk_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          sp::W_SMEM);
     if (e != cudaSuccess) return e;
@@ -1072,6 +1127,8 @@ cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char
     P.slot1 = slot1;
     P.carry_in = carry_in;
     P.carry_out = carry_out;
+    P.save_s = save_s;
+    P.save_u = save_u;
     EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
     if (!fn) return cudaErrorInvalidValue;
     const int T = a.T;

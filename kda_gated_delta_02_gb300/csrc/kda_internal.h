@@ -46,19 +46,33 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int units, cudaStream_t st);
 // kChunkBlobBytes per (chunk, head), then the state walk over the blobs.
 // Chunk j of unit u (tokens [t0, t1)) is slot floor(t0 / 64) + u + j.
 constexpr unsigned kChunkBlobBytes = 66048;
+// Byte offsets inside a blob; every tile 1024-aligned, bf16 tiles in the
+// 128-byte swizzled layouts of the tensor-core operands.
+constexpr unsigned kBlobW = 0;        // W = T diag(b) K e^gamma: rows = key channel i (128 B of t each)
+constexpr unsigned kBlobTB = 16384;   // T diag(b): rows t (128 B of s each)
+constexpr unsigned kBlobQT = 24576;   // Q e^gamma: [i / 64][t][64 i]
+constexpr unsigned kBlobKT = 40960;   // K e^{gamma_63 - gamma}: [t / 8][i / 64][t % 8][64 i]
+constexpr unsigned kBlobBM = 57344;   // B (lower, diagonal included): rows t (128 B of s each)
+constexpr unsigned kBlobGam = 65536;  // e^{gamma_63} per key channel, f32 [128]
 // list[slot] = {first token, length} for every chunk of units [0, units), 0 elsewhere
 cudaError_t launch_chunk_list(const ChunkArgs &a, int units, int nslots, int2 *list, cudaStream_t st);
 // blobs of slots [slot0, slot1) into blob[(slot - slot0) * H + h]; claim is a
 // device int that is zero when the launch starts (its item counter).  With
 // after_walk the launch is a programmatic dependent of the walk launched just
-// before it on `st` (it may start while that walk runs; see run_split).
+// before it on `st` (it may start while that walk runs; see run_split).  With
+// aux (a backward's forward pass) every item also leaves its fp32 T and M^T in
+// aux[(slot - slot0) * H + h] ([2][64][64] f32).
 cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, int slot1, unsigned char *blob,
-                              bool need_q, int *claim, bool after_walk, cudaStream_t st);
+                              bool need_q, int *claim, bool after_walk, cudaStream_t st, float *aux = nullptr);
 // the chunks of every unit that fall in slots [slot0, slot1); a unit cut at
 // slot0 starts from carry_in, one cut at slot1 leaves its state in carry_out
 // ([tiles][H][128][128] fp32 each)
+// With save_s / save_u (a backward's forward pass, outputs o not needed: null)
+// the walk also stores, per (slot, head), its bf16 operand tiles S^T at the
+// chunk start (32 KB) and U^T (16 KB), indexed by absolute slot.
 cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char *blob, int slot0, int slot1,
-                              const float *carry_in, float *carry_out, cudaStream_t st);
+                              const float *carry_in, float *carry_out, cudaStream_t st,
+                              unsigned char *save_s = nullptr, unsigned char *save_u = nullptr);
 // The driver's tensor-map encoder (cuTensorMapEncodeTiled), reached through
 // the runtime's entry-point query; null when the driver does not provide it.
 void *tensor_map_encoder();
@@ -102,6 +116,30 @@ constexpr int kBwdMaxCtas = 160;
 // floats of one chunk's column partials of one split-form CTA
 size_t chunk_bwd_partial_floats(int d);
 cudaError_t launch_chunk_bwd(const BwdArgs &a, int d, bool bf16, cudaStream_t st);
+
+// Backward on the tensor cores (chunk_bwd_tc.cu): dk = dv = 128, bf16 q, k,
+// v, dout.  The forward pass (chunk-local kernel with aux, walk saving its
+// tiles) fills blob, aux, save_s and save_u for every slot; the reverse walk
+// fills save_ds and save_du and writes dS0; the chunk kernel writes dq, dk,
+// dv, dg, dbeta.  Per (slot, head): blob kChunkBlobBytes, aux 32 KB, save_s
+// and save_ds 32 KB, save_u and save_du 16 KB.
+struct BwdTcArgs {
+    const void *q, *k, *v, *dout;
+    const float *g, *beta;
+    const int32_t *cu_seqlens;
+    int N, T, H;
+    float scale, g_min;
+    const float *dS_final;
+    float *dq, *dk, *dv, *dg, *dbeta, *dS0;
+    const int2 *list;
+    int *claim;                      // item counter of the chunk kernel, zero at launch
+    const unsigned char *blob;
+    const float *aux;
+    unsigned char *save_s, *save_u, *save_ds, *save_du;
+    uint32_t *status;
+};
+cudaError_t launch_bwd_walk(const BwdTcArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st);
 
 struct VerifyArgs {
     void *state, *tail;

@@ -188,7 +188,16 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, i
                  "r"(c0), "r"(c1), "r"(c2), "r"(src_saddr)
                  : "memory");
 }
+// Plain (1-D) bulk copy shared -> global of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), tracked as a bulk group of the issuing thread.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src_saddr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src_saddr),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until this thread's bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 // Wait until the source shared memory of this thread's bulk groups has been read.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 

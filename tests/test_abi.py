@@ -149,11 +149,24 @@ def test_kernel_timing_without_launches(lib):
     assert lib.kda_kernel_timing_stop(None, None, 2) != 0  # outputs required
 
 
+def _bwd_tc_bytes(N, T, H):
+    """The tensor-core backward's workspace (d = 128, bf16): the slot list and
+    item counters, then per (slot, head) the operand blob (66,048 B), T and M^T
+    (f32, 32 KB), the walk's S^T and U^T tiles (32 + 16 KB) and the reverse
+    walk's dS'^T and dU'^T tiles (32 + 16 KB), each part 256-byte aligned."""
+    slots = T // 64 + N
+    sh = slots * H
+    return (_align256(slots * 8) + 256 + _align256(sh * 66048) + _align256(sh * 32768) + _align256(sh * 32768) +
+            _align256(sh * 16384) + _align256(sh * 32768) + _align256(sh * 16384))
+
+
 def test_backward_workspace_arithmetic(lib):
-    """Chunk checkpoints (floor(T/64) + N slots) and 64 states per (sequence,
-    head) in flight, d x d fp32 each, two buffers of 64 x (3d + 1) fp32 column
-    partials per CTA (d/32 CTAs per unit), then w = v - p of every token (T x H
-    x d fp32); 0 for unsupported shapes."""
+    """CUDA-core form: chunk checkpoints (floor(T/64) + N slots) and 64 states
+    per (sequence, head) in flight, d x d fp32 each, two buffers of 64 x (3d +
+    1) fp32 column partials per CTA (d/32 CTAs per unit), then w = v - p of
+    every token (T x H x d fp32).  At d = 128 the size is the larger of that
+    and the tensor-core form's (bf16 inputs take that form); 0 for
+    unsupported shapes."""
     lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
     N, T, H = 3, 1000, 4
     for d in (128, 64):
@@ -161,11 +174,15 @@ def test_backward_workspace_arithmetic(lib):
         parts = lambda units: units * (d // 32) * 2 * 64 * (3 * d + 1) * 4
         wb = lambda h: _align256(T * h * d * 4)  # w = v - p of every token
         want = _align256((T // 64 + N) * H * dd) + _align256(N * H * 64 * dd) + _align256(parts(N * H)) + wb(H)
+        if d == 128:
+            want = max(want, _bwd_tc_bytes(N, T, H))
         assert lib.kda_chunk_bwd_workspace_size(N, T, H, d, d) == want
         # many units: scratch and partials stop growing at 160 units in flight
         N2, H2 = 100, 96
         want2 = (_align256((T // 64 + N2) * H2 * dd) + _align256(160 * 64 * dd) + _align256(parts(160)) +
                  wb(H2))
+        if d == 128:
+            want2 = max(want2, _bwd_tc_bytes(N2, T, H2))
         assert lib.kda_chunk_bwd_workspace_size(N2, T, H2, d, d) == want2
     d = 128
     assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 64) == 0

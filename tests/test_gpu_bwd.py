@@ -2,10 +2,16 @@
 oracle, on the same seeded inputs (the GPU's bf16 inputs rounded once, given
 to both).
 
-Bar: every gradient (dq, dk, dv, dg, dbeta, dS0) within 1e-3 normwise
-relative error per head (max |gpu - oracle| / max |oracle|): the kernel is
-fp32 throughout, so the gap is fp32 accumulation over the sequence.  dg is
-exactly zero where the floor holds.
+Two forms, chosen by shape and input type:
+- bf16 inputs at d = 128: the chunk (WY) form on the tensor cores (forward
+  pass keeping its operands, reverse state walk, chunk gradients).  Its
+  products take bf16 operands with fp32 accumulation, so the bar is 1e-2
+  normwise per head: the error budget of exactly that rounding is pinned on
+  the CPU (tests/test_oracle_chunk_reverse.py::test_bf16_operand_error_budget).
+- d = 64, or fp32 inputs: the token-level reverse mode in fp32 on the CUDA
+  cores; bar 1e-3 (fp32 accumulation over the sequence).
+Every gradient (dq, dk, dv, dg, dbeta, dS0) is compared as max |gpu - oracle|
+/ max |oracle| per head; dg is exactly zero where g is under the floor.
 """
 import numpy as np
 import pytest
@@ -15,6 +21,11 @@ from parity import normwise_err, to64
 
 pytestmark = pytest.mark.gpu
 BWD_TOL = 1e-3
+TC_TOL = 1e-2
+
+
+def _tol(d, dtype):
+    return TC_TOL if (d == 128 and dtype == torch.bfloat16) else BWD_TOL
 
 
 @pytest.fixture(scope="module")
@@ -47,22 +58,23 @@ def _case(lens, H, d, dtype, seed, floor_frac=0.1):
     return dict(q=c(q), k=c(k), v=c(v), g=c(g), beta=c(beta), cu=c(cu), S0=c(S0), do=c(do), dSf=c(dSf))
 
 
-def _compare(kda, oracle, x, scale):
+def _compare(kda, oracle, x, scale, tol, heads=None):
     got = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"],
                         dS_final=x["dSf"], scale=scale)
     torch.cuda.synchronize()
-    ref = oracle.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
-                          x["cu"].cpu().numpy(), to64(x["do"]), S0=to64(x["S0"]), dS_final=to64(x["dSf"]),
-                          scale=scale)
+    sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
+    ref = oracle.backward(to64(sel(x["q"])), to64(sel(x["k"])), to64(sel(x["v"])), to64(sel(x["g"])),
+                          to64(sel(x["beta"])), x["cu"].cpu().numpy(), to64(sel(x["do"])), S0=to64(sel(x["S0"])),
+                          dS_final=to64(sel(x["dSf"])), scale=scale)
     names = ("dq", "dk", "dv", "dg", "dbeta", "dS0")
     for name, a, b in zip(names, got, ref):
-        a64 = to64(a)
+        a64 = to64(sel(a))
         assert np.all(np.isfinite(a64)), f"{name}: non-finite"
         if name == "dbeta":
             e = np.max(np.abs(a64 - b)) / max(np.max(np.abs(b)), 1e-30)
         else:
             e = normwise_err(a64, b, head_axis=1)
-        assert e <= BWD_TOL, f"{name}: error {e:.3e}"
+        assert e <= tol, f"{name}: error {e:.3e}"
     g = x["g"].cpu()
     assert torch.all(got[3].cpu()[g < -5.0] == 0.0), "gradient through the floor"
     return got
@@ -70,10 +82,11 @@ def _compare(kda, oracle, x, scale):
 
 @pytest.mark.parametrize("d,dtype,lens", [(128, torch.bfloat16, [200, 0, 65, 1]),
                                           (64, torch.float32, [150, 64]),
-                                          (128, torch.float32, [64, 129])])
+                                          (128, torch.float32, [64, 129]),
+                                          (64, torch.bfloat16, [100, 37])])
 def test_backward_matches_oracle(kda, oracle, d, dtype, lens):
     x = _case(lens, 2, d, dtype, seed=d + len(lens))
-    got = _compare(kda, oracle, x, scale=0.7)
+    got = _compare(kda, oracle, x, scale=0.7, tol=_tol(d, dtype))
     # the empty sequence passes its final-state gradient straight to dS0
     for n, L in enumerate(lens):
         if L == 0:
@@ -81,9 +94,9 @@ def test_backward_matches_oracle(kda, oracle, d, dtype, lens):
 
 
 def test_backward_many_chunks(kda, oracle):
-    """2,048 tokens (32 chunks) x 4 heads, bf16."""
+    """2,048 tokens (32 chunks) x 4 heads, bf16 (tensor-core form)."""
     x = _case([2048], 4, 128, torch.bfloat16, seed=7)
-    _compare(kda, oracle, x, scale=1.0)
+    _compare(kda, oracle, x, scale=1.0, tol=TC_TOL)
 
 
 def test_backward_bad_seqlens_and_workspace(kda):
@@ -111,11 +124,49 @@ def test_backward_bad_seqlens_and_workspace(kda):
 
 def test_backward_more_units_than_ctas(kda, oracle):
     """30 sequences x 8 heads = 240 (sequence, head) units over at most 160
-    persistent CTAs: units share a CTA's scratch in turn."""
+    persistent CTAs (CUDA-core form, d = 64): units share a CTA's scratch in turn."""
     rng = np.random.default_rng(13)
     lens = rng.integers(0, 140, size=30).tolist()
     x = _case(lens, 8, 64, torch.bfloat16, seed=13)
-    _compare(kda, oracle, x, scale=1.0)
+    _compare(kda, oracle, x, scale=1.0, tol=BWD_TOL)
+
+
+def test_tensor_core_backward_many_short_sequences(kda, oracle):
+    """40 ragged sequences (0 to 150 tokens) x 6 heads in the tensor-core form:
+    many more (chunk, head) items than persistent CTAs, partial chunks,
+    empty sequences."""
+    rng = np.random.default_rng(17)
+    lens = rng.integers(0, 150, size=40).tolist()
+    lens[3] = 0
+    x = _case(lens, 6, 128, torch.bfloat16, seed=17)
+    got = _compare(kda, oracle, x, scale=0.5, tol=TC_TOL)
+    assert torch.equal(got[5][3], x["dSf"][3])
+
+
+def test_tensor_core_backward_scale_zero(kda, oracle):
+    """scale = 0: the outputs are zero, so do enters no gradient; the state
+    gradient still flows from dS_final."""
+    x = _case([300, 70], 2, 128, torch.bfloat16, seed=19)
+    _compare(kda, oracle, x, scale=0.0, tol=TC_TOL)
+
+
+def test_tensor_core_backward_full_length_sampled_heads(kda, oracle):
+    """The bench's workload, 32,768 tokens x 96 heads in one launch; heads 0
+    and 95 against the oracle at every token (the heads are independent)."""
+    x = _case([32768], 96, 128, torch.bfloat16, seed=23, floor_frac=0.02)
+    _compare(kda, oracle, x, scale=128 ** -0.5, tol=TC_TOL, heads=[0, 95])
+
+
+def test_tensor_core_backward_launches(kda):
+    """One slot list, one chunk-local launch (keeping T and M), one forward
+    walk (keeping its tiles), one reverse walk and one chunk-gradient launch."""
+    x = _case([500, 300], 2, 128, torch.bfloat16, seed=29)
+    kda.kernel_timing_start()
+    kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"])
+    kern = kda.kernel_timing_stop()
+    assert {k: v["launches"] for k, v in kern.items()} == {
+        "kda_chunk_list_kernel": 1, "kda_chunk_prep_kernel": 1, "kda_chunk_walk_kernel": 1,
+        "kda_bwd_walk_kernel": 1, "kda_bwd_chunk_kernel": 1}
 
 
 def _grads(kda, x, scale):
@@ -125,9 +176,20 @@ def _grads(kda, x, scale):
     return got
 
 
-def test_absent_states_and_no_dS0(kda, oracle):
+def test_tensor_core_backward_is_deterministic(kda):
+    """Items are claimed dynamically, but every result is written by one
+    thread in a fixed order: two calls give the same bits."""
+    x = _case([1000, 333], 3, 128, torch.bfloat16, seed=31)
+    a = _grads(kda, x, 0.8)
+    b = _grads(kda, x, 0.8)
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_absent_states_and_no_dS0(kda, oracle, d, dtype):
     """initial_state and dS_final absent (zero), dS0 not asked for."""
-    x = _case([130, 64], 2, 128, torch.bfloat16, seed=41)
+    x = _case([130, 64], 2, d, dtype, seed=41)
     got = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], scale=0.8, want_dS0=False)
     torch.cuda.synchronize()
     assert got[5] is None
@@ -135,17 +197,18 @@ def test_absent_states_and_no_dS0(kda, oracle):
                           x["cu"].cpu().numpy(), to64(x["do"]), scale=0.8)
     for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got[:5], ref[:5]):
         e = normwise_err(to64(a), b, head_axis=1)
-        assert e <= BWD_TOL, f"{name}: error {e:.3e}"
+        assert e <= _tol(d, dtype), f"{name}: error {e:.3e}"
 
 
 def test_floor_held_on_whole_chunks(kda, oracle):
     """g at the floor exactly (-5) on whole chunks passes its gradient; g below
-    it on other chunks passes none."""
+    it on other chunks passes none (tensor-core form: e^{-5 x 64} inside a
+    chunk is carried by the 16-token block anchoring)."""
     x = _case([256], 2, 128, torch.bfloat16, seed=43, floor_frac=0.0)
     g = x["g"].clone()
     g[0:64] = -5.0
     g[128:192] = -6.0
     x["g"] = g
-    got = _compare(kda, oracle, x, scale=1.0)
+    got = _compare(kda, oracle, x, scale=1.0, tol=TC_TOL)
     assert torch.all(got[3][128:192] == 0.0)
     assert torch.count_nonzero(got[3][0:64]) > 0
