@@ -480,27 +480,37 @@ def main(argv=None):
                           workspace=bws)
 
         bwd_step()
-        Kb = max(2, K // 10)
-        bms, kb = timed_launches(kda, bwd_step, Kb, stream)
-        bms = reduce_max(bms, ws)
-        # per token-head: fp32 flops of the forward pass (3 d^2 FMA), the recompute
-        # from the stored w = v - p (2 d^2) and the backward step (8 d^2 FMA); bytes
-        # of the recomputed state written and read back (2 x d^2 x 4) and of w
-        # (2 x d x 4) plus the inputs and gradients
-        d2 = w.dk * w.dv
-        flops = T * H * 2.0 * (3 * d2 + 2 * d2 + 8 * d2)
+        tc_form = w.dk == 128 and inp["q"].dtype == torch.bfloat16
+        Kb = max(3, K // 4) if tc_form else max(2, K // 10)
+        bms = reduce_max(cuda_time(bwd_step, Kb, stream), ws)
+        _, kb = timed_launches(kda, bwd_step, Kb, stream)  # kernel table (launch events add gaps)
+        kb_total = sum(v["ms"] for v in kb.values())
+        bkern = {name: {"launches_per_step": v["launches"] / Kb, "ms_per_launch": v["ms"] / max(v["launches"], 1),
+                        "share_of_step": v["ms"] / max(kb_total, 1e-9)} for name, v in kb.items()}
         # algorithmic I/O per token-head: q, k, v, do bf16 + g, beta in; dq, dk, dv, dg, dbeta fp32 out
         io = T * H * (4 * 128 * 2 + 128 * 4 + 4 + 3 * 128 * 4 + 128 * 4 + 4)
-        scratch = T * H * 2.0 * (d2 + w.dv) * 4  # the kernel's own recomputed states and w, written and read
-        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 flop x max SM clock, TFLOP/s
-        out["backward"] = {"workload": w.name + " backward (dq, dk, dv, dg, dbeta)", "ms": bms,
-                           "tok_s": ws * T / (bms * 1e-3), "fp32_tflops": flops / (bms * 1e-3) / 1e12,
-                           "fp32_peak_tflops": fp32_peak, "frac_alu": flops / (bms * 1e-3) / 1e12 / fp32_peak,
-                           "algorithmic_bytes_per_step": io,
-                           "frac_hbm": io / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "kernel_own_bytes_gbs": (io + scratch) / (bms * 1e-3) / 1e9,
-                           "kernel_own_frac_hbm": (io + scratch) / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "ratio_to_forward": bms / ms}
+        entry = {"workload": w.name + " backward (dq, dk, dv, dg, dbeta)", "ms": bms,
+                 "tok_s": ws * T / (bms * 1e-3), "algorithmic_bytes_per_step": io,
+                 "frac_hbm": io / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"], "ratio_to_forward": bms / ms,
+                 "kernels": bkern}
+        if tc_form:
+            # tensor-core products issued per (chunk, head), padding included:
+            # forward pass (A/B tiles 128x160x128, W 128x64x64, walk U 128x64x(64+128),
+            # state 128x128x64), reverse walk (dU 128x64x(64+128), dS 2 x 128x128x64)
+            # and the chunk kernel (batches of 128x64x128, 2 x 128x64x64, 2 x 128x128x128,
+            # 128x64x128, 2 x 128x64x64, 2 x (128x128x160 + 128x160x128))
+            macs = (128 * 160 * 128 + 128 * 64 * 64 + 128 * 64 * 192 + 128 * 128 * 64 +
+                    128 * 64 * 192 + 2 * 128 * 128 * 64 +
+                    128 * 64 * 128 + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 128 + 128 * 64 * 128 +
+                    2 * 128 * 64 * 64 + 2 * (128 * 128 * 160 + 128 * 160 * 128))
+            flops = 2.0 * macs * (T // 64) * H
+            entry.update({"form": "chunk (WY) form on the tensor cores",
+                          "tensor_tflops_issued": flops / (bms * 1e-3) / 1e12,
+                          "tensor_frac": flops / (bms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                          "workspace_bytes": int(bws.numel())})
+        else:
+            entry["form"] = "token-level reverse mode on the CUDA cores"
+        out["backward"] = entry
         launches += sum(v["launches"] for v in kb.values())
         del inp, dout, bws
         torch.cuda.empty_cache()

@@ -336,6 +336,11 @@ constexpr uint32_t B_KT = 163840;   // K~, MN-major (n = t, k = i)
 constexpr uint32_t B_TB = 180224;   // T diag(b), MN-major (n = s, k = t)
 constexpr uint32_t B_TF = 188416;   // T f32 [64][64]
 constexpr uint32_t B_MT = 204800;   // M^T f32 [64][64]
+// the item's rows, staged by TMA where tiles arrive later or are built later:
+// k and q [64 t][128] bf16 over U^T and Vres^T, g [64 t][128] f32 over dS'^T
+// (those two tiles are copied once the rows are read), v in the rows 64-127
+// of the [dO; -dVres] tile (its two 8 KB value halves) until -dVres goes there
+constexpr uint32_t B_KST = B_UB, B_QST = B_VR, B_GST = B_DS;
 // phases C and D, over the phase A / B regions once the second batch is done
 // (A' in two bf16 parts, high and low: the anchored products cancel between
 // their row and column sides in the log-decay gradient, so A' keeps about 16
@@ -354,9 +359,9 @@ constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
 constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [2][128] halves of rowsum(dS' . S)
 constexpr uint32_t B_DBP = B_DGC + 1024;      // f32 [4][64] beta gradient parts
 constexpr uint32_t B_CUM = B_DBP + 1024;      // f32 [3][128] decay-gradient sums of the halves
-constexpr uint32_t B_BAR = B_CUM + 1536;      // 6 mbarriers: loads, five product batches
-constexpr uint32_t B_TMEM = B_BAR + 48;
-constexpr uint32_t B_CLAIM = B_TMEM + 8;
+constexpr uint32_t B_BAR = B_CUM + 1536;      // 7 mbarriers: loads, five product batches, late loads
+constexpr uint32_t B_TMEM = B_BAR + 56;
+constexpr uint32_t B_CLAIM = B_TMEM + 8;      // int [2]: item in hand, next item
 constexpr uint32_t B_SMEM = B_CLAIM + 8 + 1024;
 static_assert(B_RS + 49152 <= B_TF, "phase C regions overlap the kept T and M");
 static_assert(B_LT + 32768 <= B_MISC, "L^T");
@@ -375,7 +380,8 @@ struct BchunkParams {
     int *claim;                      // item counter, zero at launch
     const unsigned char *save_s, *save_u, *save_ds, *save_du;  // [slot][H] tiles
     const float *aux;                // [slot][H][2][64][64]: T, M^T
-    CUtensorMap tdo;                 // dout box 64 x 1 x 64, 128-byte swizzle
+    CUtensorMap tdo, tv;             // dout, v: box 64 x 1 x 64, 128-byte swizzle
+    CUtensorMap tk, tq, tg;          // k, q, g: box 128 x 1 x 64, no swizzle
     float *dq, *dk, *dv, *dg, *dbeta;
     uint32_t *status;
 };
@@ -397,13 +403,14 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     const float *sTF = reinterpret_cast<const float *>(sm + B_TF);
     const float *sMT = reinterpret_cast<const float *>(sm + B_MT);
     int *sClaim = reinterpret_cast<int *>(sm + B_CLAIM);
-    const uint32_t bar = sb + B_BAR;  // bar + 8 k: k = 0 loads, 1..5 product batches
+    const uint32_t bar = sb + B_BAR;  // bar + 8 k: k = 0 loads, 1..5 product batches, 6 late loads
     const float scale = p.scale, wscale = p.wscale, g_min = p.g_min;
 
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) umma::mbar_init(bar + 8 * b, 1);
+        for (int b = 0; b < 7; ++b) umma::mbar_init(bar + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         sClaim[0] = atomicAdd(p.claim, 1);
+        sClaim[1] = atomicAdd(p.claim, 1);
     }
     if (warp == 0) umma::tmem_alloc(sb + B_TMEM, 512);
     umma::fence_before();
@@ -411,9 +418,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_after();
     const uint32_t tmem = *reinterpret_cast<const uint32_t *>(sm + B_TMEM);
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
-    int w = sClaim[0];
+    int w = sClaim[0], wn = sClaim[1];
     uint32_t it = 0;
     bool alive = true;
+    __syncthreads();  // claims read before thread 0 writes the next ones
 
     while (w < p.nitems) {
     const int slot = w / H, h = w % H;
@@ -425,14 +433,36 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     // ---------------------------------------------------------------- loads
     if (tid == 0) {
         umma::fence_proxy_async();
-        umma::mbar_expect_tx(bar, 2 * TILE_S + 2 * TILE_U + 4 * AUX_FLOATS + 16384u);
+        umma::mbar_expect_tx(bar, TILE_S + TILE_U + 4 * AUX_FLOATS + 4 * 16384u + 32768u);
         umma::bulk_load(sb + B_SB, p.save_s + (size_t)w * TILE_S, TILE_S, bar);
-        umma::bulk_load(sb + B_DS, p.save_ds + (size_t)w * TILE_S, TILE_S, bar);
-        umma::bulk_load(sb + B_UB, p.save_u + (size_t)w * TILE_U, TILE_U, bar);
         umma::bulk_load(sb + B_DU, p.save_du + (size_t)w * TILE_U, TILE_U, bar);
         umma::bulk_load(sb + B_TF, p.aux + (size_t)w * AUX_FLOATS, 4 * AUX_FLOATS, bar);
         umma::tma_load_3d(sb + B_DO, &p.tdo, 0, h, tc, bar);
         umma::tma_load_3d(sb + B_DO + 16384, &p.tdo, 64, h, tc, bar);
+        umma::tma_load_3d(sb + B_DO + 8192, &p.tv, 0, h, tc, bar);
+        umma::tma_load_3d(sb + B_DO + 24576, &p.tv, 64, h, tc, bar);
+        umma::tma_load_3d(sb + B_KST, &p.tk, 0, h, tc, bar);
+        umma::tma_load_3d(sb + B_QST, &p.tq, 0, h, tc, bar);
+        umma::tma_load_3d(sb + B_GST, &p.tg, 0, h, tc, bar);
+        // the next item's tiles and rows into L2 while this one runs
+        if (wn < p.nitems) {
+            const int2 ncl = p.list[wn / H];
+            if (ncl.y > 0) {
+                const int hn = wn % H;
+                umma::prefetch_l2(p.save_s + (size_t)wn * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_ds + (size_t)wn * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_u + (size_t)wn * TILE_U, TILE_U);
+                umma::prefetch_l2(p.save_du + (size_t)wn * TILE_U, TILE_U);
+                umma::prefetch_l2(p.aux + (size_t)wn * AUX_FLOATS, 4 * AUX_FLOATS);
+                umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tv, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tv, 64, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tdo, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tdo, 64, hn, ncl.x);
+            }
+        }
     }
     // thread (channel ch = l, half hf): tokens 32 hf .. 32 hf + 31.  x, y:
     // running products of e^{g} from the start of the token's 16-token block
@@ -441,18 +471,18 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     float x[32], y[32];
     uint32_t kq[32];
     uint32_t below = 0;  // bit u: g < g_min (no gradient)
+    pend |= umma::mbar_wait(bar, par, WAIT_LIMIT) ? 0u : 1u;
     {
         float e[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = 32 * hf + u;
             const bool ok = t < Lc;
-            const size_t row = ((size_t)(tc + t) * H + h) * D + ch;
-            const float gv = ok ? p.g[row] : 0.f;
+            const float gv = ok ? *reinterpret_cast<const float *>(sm + B_GST + t * 512 + ch * 4) : 0.f;
             below |= (ok && gv < g_min) ? (1u << u) : 0u;
             e[u] = __expf(fmaxf(gv, g_min));
-            const uint32_t kb = ok ? (uint32_t)reinterpret_cast<const uint16_t *>(p.k)[row] : 0u;
-            const uint32_t qb = ok ? (uint32_t)reinterpret_cast<const uint16_t *>(p.q)[row] : 0u;
+            const uint32_t kb = ok ? (uint32_t)lds16(sb + B_KST + t * 256 + ch * 2) : 0u;
+            const uint32_t qb = ok ? (uint32_t)lds16(sb + B_QST + t * 256 + ch * 2) : 0u;
             kq[u] = kb | (qb << 16);
         }
 #pragma unroll
@@ -486,7 +516,6 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         sts128(sb + B_KT + umma::mnmaj(32 * hf + u, ch, 1), pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
                pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
     }
-    pend |= umma::mbar_wait(bar, par, WAIT_LIMIT) ? 0u : 1u;
     {  // dO rows past the chunk end (every row when dO enters no product) are zero
         const int z0 = p.zero_do ? 0 : Lc;
         for (int idx = tid; idx < (CH - z0) * 16; idx += NB) {
@@ -520,6 +549,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     // ---------------------------------------------------------------- batch 1: (K~ S)^T, dVres^T / wscale
     if (tid == 0) {
         umma::fence_after();
+        // the rows are read: the tiles that go over their staging
+        umma::fence_proxy_async();
+        umma::mbar_expect_tx(bar + 48, TILE_S + TILE_U);
+        umma::bulk_load(sb + B_DS, p.save_ds + (size_t)w * TILE_S, TILE_S, bar + 48);
+        umma::bulk_load(sb + B_UB, p.save_u + (size_t)w * TILE_U, TILE_U, bar + 48);
         constexpr uint32_t id1 = umma::idesc_bf16(128, 64, 0, 1, 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -541,13 +575,15 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = 32 * hf + u;
-            const float vv = (t < Lc) ? bf16_at(p.v, ((size_t)(tc + t) * H + h) * D + j) : 0.f;
+            const float vv =
+                (t < Lc) ? __uint_as_float((uint32_t)lds16(sb + B_DO + umma::kmaj(64 + t, j, 128)) << 16) : 0.f;
             a[u] = vv - a[u];
         }
 #pragma unroll
         for (int u = 0; u < 32; u += 8)
             sts128(sb + B_VR + umma::kmaj(j, 32 * hf + u, 128), pack_bf16(a[u], a[u + 1]), pack_bf16(a[u + 2], a[u + 3]),
                    pack_bf16(a[u + 4], a[u + 5]), pack_bf16(a[u + 6], a[u + 7]));
+        __syncthreads();  // v read: -dVres goes over it
         umma::ld32(tq + T2 + 32 * hf, a);
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
@@ -569,6 +605,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             sts128(sb + B_DOT + umma::kmaj(j, 32 * hf + u, 128), pk[0], pk[1], pk[2], pk[3]);
         }
     }
+    pend |= umma::mbar_wait(bar + 48, par, WAIT_LIMIT) ? 0u : 64u;
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
@@ -805,12 +842,25 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         for (int u0 = 0; u0 < 32; u0 += 8) {
             const int bl = u0 >> 4, bk = 2 * hf + bl;
             const int t0 = 32 * hf + u0;
-            float a4[8], a5[8], a6[8], a7[8], a8[8];
-            umma::ld8(tq + T4 + t0, a4);       // S dO^T
-            umma::ld8(tq + T4 + 64 + t0, a5);  // -S dVres^T
-            umma::ld8(tq + T5 + t0, a6);       // dS' U^T
-            umma::ld8(tq + T8 + t0, a7);       // dL (k rows)
-            umma::ld8(tq + T8 + 64 + t0, a8);  // dL (q rows)
+            // every column group of these 8 tokens in one round of loads
+            uint32_t a4[8], a5[8], a6[8], a7[8], a8[8], r9[4][8];
+            umma::ld8_async(tq + T4 + t0, a4);       // S dO^T
+            umma::ld8_async(tq + T4 + 64 + t0, a5);  // -S dVres^T
+            umma::ld8_async(tq + T5 + t0, a6);       // dS' U^T
+            umma::ld8_async(tq + T8 + t0, a7);       // dL (k rows)
+            umma::ld8_async(tq + T8 + 64 + t0, a8);  // dL (q rows)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i >= bk) umma::ld8_async(tq + T9 + segoff(i) + t0, r9[i]);  // dR_seg
+            umma::wait_ld();
+            umma::hold(a4);
+            umma::hold(a5);
+            umma::hold(a6);
+            umma::hold(a7);
+            umma::hold(a8);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i >= bk) umma::hold(r9[i]);
             float kc[8], rr[8];  // sum_i f_i dR_i, and sum_i R_i dR_i with R_i as the product read it (bf16)
 #pragma unroll
             for (int e2 = 0; e2 < 8; ++e2) kc[e2] = rr[e2] = 0.f;
@@ -825,13 +875,12 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                     for (int m = 0; m < 4; ++m)
                         if (m > bk && m < i) c *= dl[m];
                 }
-                float r8[8];
-                umma::ld8(tq + T9 + segoff(i) + t0, r8);
 #pragma unroll
                 for (int e2 = 0; e2 < 8; ++e2) {
                     const float f = y[u0 + e2] * c;
-                    kc[e2] = fmaf(f, r8[e2], kc[e2]);
-                    rr[e2] = fmaf(bf16_round(kf(u0 + e2) * f), r8[e2], rr[e2]);
+                    const float r = __uint_as_float(r9[i][e2]);
+                    kc[e2] = fmaf(f, r, kc[e2]);
+                    rr[e2] = fmaf(bf16_round(kf(u0 + e2) * f), r, rr[e2]);
                 }
             }
             const float pre = bl ? pre1 : pre0, post = bl ? post1 : post0;
@@ -840,15 +889,17 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                 const int u = u0 + e2, t = t0 + e2;
                 const float xx = x[u], gam = pre * xx, suf = y[u] * post;
                 const float kk = kf(u), qq = qf(u);
-                const float dqs = scale * a4[e2];
-                const float dq = fmaf(dqs, gam, xx * a8[e2]);
-                const float kh = wscale * a6[e2] * suf;
-                const float dk = fmaf(a5[e2], gam, xx * a7[e2]) + kc[e2] + kh;
+                const float v4 = __uint_as_float(a4[e2]), v5 = __uint_as_float(a5[e2]), v6 = __uint_as_float(a6[e2]);
+                const float v7 = __uint_as_float(a7[e2]), v8 = __uint_as_float(a8[e2]);
+                const float dqs = scale * v4;
+                const float dq = fmaf(dqs, gam, xx * v8);
+                const float kh = wscale * v6 * suf;
+                const float dk = fmaf(v5, gam, xx * v7) + kc[e2] + kh;
                 // the anchored terms with the bf16 values of L and R_seg that the
                 // products used: each (row, column) pair inside [t, 63] then
                 // cancels in the reverse cumulative sum as it does exactly
-                dgam[u] = fmaf(dqs, qq * gam, a5[e2] * (kk * gam)) - kh * kk +
-                          fmaf(bf16_round(kk * xx), a7[e2], bf16_round(qq * xx) * a8[e2]) - rr[e2];
+                dgam[u] = fmaf(dqs, qq * gam, v5 * (kk * gam)) - kh * kk +
+                          fmaf(bf16_round(kk * xx), v7, bf16_round(qq * xx) * v8) - rr[e2];
                 sh = fmaf(kh, kk, sh);
                 if (t < Lc) {
                     const size_t o = ((size_t)(tc + t) * H + h) * D + ch;
@@ -877,15 +928,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     ++it;
     if (__syncthreads_or(pend != 0)) {  // uniform: leave once the copies and products in flight are done
         if (pend & 1u) umma::mbar_wait(bar, par, WAIT_LIMIT);
-        for (int b = 1; b < 6; ++b)
+        for (int b = 1; b < 7; ++b)
             if (pend & (1u << b)) umma::mbar_wait(bar + 8 * b, par, WAIT_LIMIT);
         alive = false;
         break;
     }
     }  // Lc > 0
-    if (tid == 0) sClaim[0] = atomicAdd(p.claim, 1);
+    if (tid == 0) sClaim[0] = (wn < p.nitems) ? atomicAdd(p.claim, 1) : p.nitems;
     __syncthreads();
-    w = sClaim[0];
+    w = wn;
+    wn = sClaim[0];
     __syncthreads();  // the claim was read by every thread before thread 0 writes the next
     }  // items
     if (!alive && tid == 0) report_status(p.status, KDA_STATUS_TIMEOUT);
@@ -900,7 +952,7 @@ namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-// dout [T][H][128] bf16, box 64 x 1 head x 64 tokens, 128-byte swizzle
+// dout (or v) [T][H][128] bf16, box 64 x 1 head x 64 tokens, 128-byte swizzle
 bool encode_dout(CUtensorMap *m, const void *dout, int T, int H) {
     if (T <= 0) return true;  // no chunk: the map is never used
     EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
@@ -911,6 +963,19 @@ bool encode_dout(CUtensorMap *m, const void *dout, int T, int H) {
     cuuint32_t estr[3] = {1u, 1u, 1u};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(dout), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// [T][H][128] rows, box 128 x 1 head x 64 tokens, no swizzle
+bool encode_plain(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int T, int H) {
+    if (T <= 0) return true;
+    EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128u, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128u * (cuuint64_t)esize, 128u * (cuuint64_t)esize * H};
+    cuuint32_t box[3] = {128u, 1u, 64u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
@@ -964,7 +1029,11 @@ cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st) {
     P.save_ds = a.save_ds;
     P.save_du = a.save_du;
     P.aux = a.aux;
-    if (!encode_dout(&P.tdo, a.dout, a.T, a.H)) return cudaErrorInvalidValue;
+    if (!encode_dout(&P.tdo, a.dout, a.T, a.H) || !encode_dout(&P.tv, a.v, a.T, a.H) ||
+        !encode_plain(&P.tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        !encode_plain(&P.tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H) ||
+        !encode_plain(&P.tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H))
+        return cudaErrorInvalidValue;
     P.dq = a.dq;
     P.dk = a.dk;
     P.dv = a.dv;

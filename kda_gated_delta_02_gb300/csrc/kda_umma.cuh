@@ -137,6 +137,23 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane, without the wait:
+// several loads go out together, then wait_ld() and hold() on every array
+// loaded (hold ties its registers to a point after the wait, so no use is
+// scheduled before the values are there).
+__device__ __forceinline__ void ld8_async(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void hold(uint32_t (&r)[8]) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
 // Bulk tensor copy (TMA) of a 3-D box into shared memory; completion is
 // counted in bytes on the mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_saddr, const void *tmap, int c0, int c1, int c2,
