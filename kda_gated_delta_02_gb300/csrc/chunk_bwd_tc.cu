@@ -321,8 +321,12 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
 }
 
 // ============================================================================ chunk gradients
-constexpr int NB = 256;
-// shared memory, 1024-aligned regions.  Phases A and B (the first three
+// 512 threads: thread (lane l = 32 (warp % 4) + lane, group cg = warp / 4)
+// owns TMEM lane l (a key channel, value column or row of the products) and
+// the columns of token block cg (tokens 16 cg .. 16 cg + 15), so every per-token
+// loop is 16 long and the block anchoring of a channel is thread-local.
+constexpr int NB = 512;
+// shared memory, 1024-aligned regions.  Phases A and B (the first two
 // product batches):
 constexpr uint32_t B_SB = 0;        // S^T bf16 [j][i] (K-major 128 x 128)
 constexpr uint32_t B_DS = 32768;    // dS'^T bf16 [j][i]
@@ -353,13 +357,13 @@ constexpr uint32_t B_ZT = 114688;   // -Z, MN-major (n = b, k = t)
 constexpr uint32_t B_RS = 122880;   // R_seg^T K-major 128 channels x 192 (three K blocks)
 constexpr uint32_t B_LT = 188416;   // L^T K-major 128 channels x 128 (two K blocks), over T and M^T
                                     // once the beta gradient has read them
+constexpr uint32_t B_CUM = 0;       // the combine's block sums f32 [8][128], over A' once read
 constexpr uint32_t B_MISC = 221184;
 constexpr uint32_t B_BETA = B_MISC;           // f32 [64]
 constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
-constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [2][128] halves of rowsum(dS' . S)
-constexpr uint32_t B_DBP = B_DGC + 1024;      // f32 [4][64] beta gradient parts
-constexpr uint32_t B_CUM = B_DBP + 1024;      // f32 [3][128] decay-gradient sums of the halves
-constexpr uint32_t B_BAR = B_CUM + 1536;      // 7 mbarriers: loads, five product batches, late loads
+constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [4][128] quarters of rowsum(dS' . S)
+constexpr uint32_t B_DBP = B_DGC + 2048;      // f32 [8][64] beta gradient parts
+constexpr uint32_t B_BAR = B_DBP + 2048;      // 7 mbarriers: loads, five product batches, late loads
 constexpr uint32_t B_TMEM = B_BAR + 56;
 constexpr uint32_t B_CLAIM = B_TMEM + 8;      // int [2]: item in hand, next item
 constexpr uint32_t B_SMEM = B_CLAIM + 8 + 1024;
@@ -386,14 +390,24 @@ struct BchunkParams {
     uint32_t *status;
 };
 
+__device__ __forceinline__ void sts_bf16x8(uint32_t addr, const float (&v)[8], int o) {
+    sts128(addr, pack_bf16(v[o], v[o + 1]), pack_bf16(v[o + 2], v[o + 3]), pack_bf16(v[o + 4], v[o + 5]),
+           pack_bf16(v[o + 6], v[o + 7]));
+}
+__device__ __forceinline__ void sts_bf16x8(uint32_t addr, const float (&v)[16], int o) {
+    sts128(addr, pack_bf16(v[o], v[o + 1]), pack_bf16(v[o + 2], v[o + 3]), pack_bf16(v[o + 4], v[o + 5]),
+           pack_bf16(v[o + 6], v[o + 7]));
+}
+
 __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_constant__ BchunkParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const uint32_t sb4 = sb >> 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, hf = warp >> 2;
+    const int qd = warp & 3, cg = warp >> 2;
     const int l = 32 * qd + lane;  // TMEM lane: channel / value column / row owned
+    const int c0 = 16 * cg;        // first token (column) of this thread's block
     const int H = p.H;
     float *sBeta = reinterpret_cast<float *>(sm + B_BETA);
     float *sPart = reinterpret_cast<float *>(sm + B_PART);
@@ -464,82 +478,82 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             }
         }
     }
-    // thread (channel ch = l, half hf): tokens 32 hf .. 32 hf + 31.  x, y:
-    // running products of e^{g} from the start of the token's 16-token block
-    // (inclusive) and to its end (exclusive); k and q of each token as a bf16 pair
+    // thread (channel ch = l, block cg): e^{g} of the block's tokens and their
+    // (k, q) as a bf16 pair; x (running product from the block start,
+    // inclusive) and y (to the block end, exclusive) are formed where needed
     const int ch = l;
-    float x[32], y[32];
-    uint32_t kq[32];
+    float e[16];
+    uint32_t kq[16];
     uint32_t below = 0;  // bit u: g < g_min (no gradient)
     pend |= umma::mbar_wait(bar, par, WAIT_LIMIT) ? 0u : 1u;
-    {
-        float e[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = 32 * hf + u;
-            const bool ok = t < Lc;
-            const float gv = ok ? *reinterpret_cast<const float *>(sm + B_GST + t * 512 + ch * 4) : 0.f;
-            below |= (ok && gv < g_min) ? (1u << u) : 0u;
-            e[u] = __expf(fmaxf(gv, g_min));
-            const uint32_t kb = ok ? (uint32_t)lds16(sb + B_KST + t * 256 + ch * 2) : 0u;
-            const uint32_t qb = ok ? (uint32_t)lds16(sb + B_QST + t * 256 + ch * 2) : 0u;
-            kq[u] = kb | (qb << 16);
-        }
-#pragma unroll
-        for (int bl = 0; bl < 2; ++bl) {
-            x[16 * bl] = e[16 * bl];
-#pragma unroll
-            for (int u = 16 * bl + 1; u < 16 * bl + 16; ++u) x[u] = x[u - 1] * e[u];
-            y[16 * bl + 15] = 1.f;
-#pragma unroll
-            for (int u = 16 * bl + 14; u >= 16 * bl; --u) y[u] = y[u + 1] * e[u + 1];
-        }
+    for (int u = 0; u < 16; ++u) {
+        const int t = c0 + u;
+        const bool ok = t < Lc;
+        const float gv = ok ? *reinterpret_cast<const float *>(sm + B_GST + t * 512 + ch * 4) : 0.f;
+        below |= (ok && gv < g_min) ? (1u << u) : 0u;
+        e[u] = __expf(fmaxf(gv, g_min));
+        const uint32_t kb = ok ? (uint32_t)lds16(sb + B_KST + t * 256 + ch * 2) : 0u;
+        const uint32_t qb = ok ? (uint32_t)lds16(sb + B_QST + t * 256 + ch * 2) : 0u;
+        kq[u] = kb | (qb << 16);
     }
-    sPart[(2 * hf) * 128 + ch] = x[15];
-    sPart[(2 * hf + 1) * 128 + ch] = x[31];
+    auto prefix = [&](float (&x)[16]) {
+        x[0] = e[0];
+#pragma unroll
+        for (int u = 1; u < 16; ++u) x[u] = x[u - 1] * e[u];
+    };
+    auto suffix = [&](float (&y)[16]) {
+        y[15] = 1.f;
+#pragma unroll
+        for (int u = 14; u >= 0; --u) y[u] = y[u + 1] * e[u + 1];
+    };
+    auto kf = [&](int u) { return __uint_as_float(kq[u] << 16); };
+    auto qf = [&](int u) { return __uint_as_float(kq[u] & 0xFFFF0000u); };
+    {
+        float x[16];
+        prefix(x);
+        sPart[cg * 128 + ch] = x[15];
+    }
     if (tid < CH) sBeta[tid] = (tid < Lc) ? p.beta[(size_t)(tc + tid) * H + h] : 0.f;
     __syncthreads();
     float dl[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) dl[m] = sPart[m * 128 + ch];
-    // products of the block decays before / after each of this thread's blocks
-    const float pre0 = hf ? dl[0] * dl[1] : 1.f, pre1 = hf ? pre0 * dl[2] : dl[0];
-    const float post1 = hf ? 1.f : dl[2] * dl[3], post0 = hf ? dl[3] : dl[1] * post1;
-    auto kf = [&](int u) { return __uint_as_float(kq[u] << 16); };
-    auto qf = [&](int u) { return __uint_as_float(kq[u] & 0xFFFF0000u); };
-    // K~ = K Gam as the MN-major B operand of (K~ S)^T (n = t, k = i = ch)
+    // products of the block decays before / after this thread's block
+    float pre = 1.f, post = 1.f;
 #pragma unroll
-    for (int u = 0; u < 32; u += 8) {
-        float v8[8];
+    for (int m = 0; m < 4; ++m) {
+        if (m < cg) pre *= dl[m];
+        if (m > cg) post *= dl[m];
+    }
+    {  // K~ = K Gam as the MN-major B operand of (K~ S)^T (n = t, k = i = ch)
+        float x[16], v[16];
+        prefix(x);
 #pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) v8[e2] = kf(u + e2) * ((u + e2) < 16 ? pre0 : pre1) * x[u + e2];
-        sts128(sb + B_KT + umma::mnmaj(32 * hf + u, ch, 1), pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
-               pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+        for (int u = 0; u < 16; ++u) v[u] = kf(u) * (pre * x[u]);
+        sts_bf16x8(sb + B_KT + umma::mnmaj(c0, ch, 1), v, 0);
+        sts_bf16x8(sb + B_KT + umma::mnmaj(c0 + 8, ch, 1), v, 8);
+    }
+    {  // T diag(b) as the MN-major B operand of dVres^T (n = s, k = t), high and low bf16 parts
+        const int t = tid >> 3, s = 8 * (tid & 7);
+        float tb[8];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) tb[e2] = sTF[t * 64 + s + e2] * sBeta[s + e2];
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; e2 += 2) {
+            hi[e2 >> 1] = pack_bf16(tb[e2], tb[e2 + 1]);
+            const float2 h2 = unpack_bf16(hi[e2 >> 1]);
+            lo[e2 >> 1] = pack_bf16(tb[e2] - h2.x, tb[e2 + 1] - h2.y);
+        }
+        sts128(sb + B_TB + umma::mnmaj(s, t, 1), hi[0], hi[1], hi[2], hi[3]);
+        sts128(sb + B_TBL + umma::mnmaj(s, t, 1), lo[0], lo[1], lo[2], lo[3]);
     }
     {  // dO rows past the chunk end (every row when dO enters no product) are zero
         const int z0 = p.zero_do ? 0 : Lc;
         for (int idx = tid; idx < (CH - z0) * 16; idx += NB) {
             const int r = z0 + (idx >> 4), c = idx & 15;
             *reinterpret_cast<uint4 *>(sm + B_DO + (c >> 3) * 16384 + r * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-    {  // T diag(b) as the MN-major B operand of dVres^T (n = s, k = t), high and low bf16 parts
-        const int t = tid >> 2, s0 = 16 * (tid & 3);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int s = s0 + 8 * hh;
-            float tb[8];
-#pragma unroll
-            for (int e2 = 0; e2 < 8; ++e2) tb[e2] = sTF[t * 64 + s + e2] * sBeta[s + e2];
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 8; e2 += 2) {
-                hi[e2 >> 1] = pack_bf16(tb[e2], tb[e2 + 1]);
-                const float2 h2 = unpack_bf16(hi[e2 >> 1]);
-                lo[e2 >> 1] = pack_bf16(tb[e2] - h2.x, tb[e2 + 1] - h2.y);
-            }
-            sts128(sb + B_TB + umma::mnmaj(s, t, 1), hi[0], hi[1], hi[2], hi[3]);
-            sts128(sb + B_TBL + umma::mnmaj(s, t, 1), lo[0], lo[1], lo[2], lo[3]);
         }
     }
     umma::fence_proxy_async();
@@ -568,41 +582,39 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     }
     pend |= umma::mbar_wait(bar + 8, par, WAIT_LIMIT) ? 0u : 2u;
     umma::fence_after();
-    {  // thread (value column j = l, half hf)
+    {  // thread (value column j = l, block cg)
         const int j = l;
-        float a[32];
-        umma::ld32(tq + T1 + 32 * hf, a);
+        float a[16];
+        umma::ld16(tq + T1 + c0, a);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = 32 * hf + u;
+        for (int u = 0; u < 16; ++u) {
+            const int t = c0 + u;
             const float vv =
                 (t < Lc) ? __uint_as_float((uint32_t)lds16(sb + B_DO + umma::kmaj(64 + t, j, 128)) << 16) : 0.f;
             a[u] = vv - a[u];
         }
-#pragma unroll
-        for (int u = 0; u < 32; u += 8)
-            sts128(sb + B_VR + umma::kmaj(j, 32 * hf + u, 128), pack_bf16(a[u], a[u + 1]), pack_bf16(a[u + 2], a[u + 3]),
-                   pack_bf16(a[u + 4], a[u + 5]), pack_bf16(a[u + 6], a[u + 7]));
+        sts_bf16x8(sb + B_VR + umma::kmaj(j, c0, 128), a, 0);
+        sts_bf16x8(sb + B_VR + umma::kmaj(j, c0 + 8, 128), a, 8);
         __syncthreads();  // v read: -dVres goes over it
-        umma::ld32(tq + T2 + 32 * hf, a);
+        umma::ld16(tq + T2 + c0, a);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int s = 32 * hf + u;
+        for (int u = 0; u < 16; ++u) {
+            const int s = c0 + u;
             const float dvr = a[u] * wscale;
             if (s < Lc) p.dv[((size_t)(tc + s) * H + h) * D + j] = dvr;
             sts16(sb + B_DO + umma::kmaj(64 + s, j, 128), bf16_bits(-dvr));
         }
         // dO^T row j from column j of the dO tile
 #pragma unroll
-        for (int u = 0; u < 32; u += 8) {
+        for (int u = 0; u < 16; u += 8) {
             uint32_t pk[4];
 #pragma unroll
             for (int e2 = 0; e2 < 8; e2 += 2) {
-                const uint32_t lo = lds16(sb + B_DO + umma::kmaj(32 * hf + u + e2, j, 128));
-                const uint32_t hi = lds16(sb + B_DO + umma::kmaj(32 * hf + u + e2 + 1, j, 128));
+                const uint32_t lo = lds16(sb + B_DO + umma::kmaj(c0 + u + e2, j, 128));
+                const uint32_t hi = lds16(sb + B_DO + umma::kmaj(c0 + u + e2 + 1, j, 128));
                 pk[e2 >> 1] = lo | (hi << 16);
             }
-            sts128(sb + B_DOT + umma::kmaj(j, 32 * hf + u, 128), pk[0], pk[1], pk[2], pk[3]);
+            sts128(sb + B_DOT + umma::kmaj(j, c0 + u, 128), pk[0], pk[1], pk[2], pk[3]);
         }
     }
     pend |= umma::mbar_wait(bar + 48, par, WAIT_LIMIT) ? 0u : 64u;
@@ -631,16 +643,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                       umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id5, ks > 0 ? 1u : 0u);
         umma::commit(bar + 16);
     }
-    {  // rowsum(dS' . S) for key channel ch over this half's value columns
+    {  // rowsum(dS' . S) for key channel ch over value columns 32 cg .. 32 cg + 31
         float acc = 0.f;
 #pragma unroll 8
-        for (int jj = 0; jj < 64; ++jj) {
-            const int j = 64 * hf + jj;
+        for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * cg + jj;
             const float a = __uint_as_float((uint32_t)lds16(sb + B_DS + umma::kmaj(j, ch, 128)) << 16);
             const float b = __uint_as_float((uint32_t)lds16(sb + B_SB + umma::kmaj(j, ch, 128)) << 16);
             acc = fmaf(a, b, acc);
         }
-        sDgc[hf * 128 + ch] = acc;
+        sDgc[cg * 128 + ch] = acc;
     }
     pend |= umma::mbar_wait(bar + 16, par, WAIT_LIMIT) ? 0u : 4u;
     umma::fence_after();
@@ -649,44 +661,37 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     for (int idx = tid; idx < 2 * 49152 / 16; idx += NB)
         *reinterpret_cast<uint4 *>(sm + B_AP + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
     {
-        const int t = tid >> 2, s0 = 16 * (tid & 3);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int s = s0 + 8 * hh;
-            const float4 a0 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s);
-            const float4 a1 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s + 4);
-            sts128(sb + B_T16 + umma::kmaj(t, s, 64), pack_bf16(a0.x, a0.y), pack_bf16(a0.z, a0.w),
-                   pack_bf16(a1.x, a1.y), pack_bf16(a1.z, a1.w));
-        }
+        const int t = tid >> 3, s = 8 * (tid & 7);
+        const float4 a0 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s);
+        const float4 a1 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s + 4);
+        sts128(sb + B_T16 + umma::kmaj(t, s, 64), pack_bf16(a0.x, a0.y), pack_bf16(a0.z, a0.w), pack_bf16(a1.x, a1.y),
+               pack_bf16(a1.z, a1.w));
     }
     __syncthreads();
     if (qd < 2) {  // lanes 0-63: s = l; columns t: dTB[t][s] / wscale
         const int s = l;
-        float a[32];
-        umma::ld32(tq + T3 + 32 * hf, a);
+        float a[16];
+        umma::ld16(tq + T3 + c0, a);
         const float bs = sBeta[s];
         float dbp = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = 32 * hf + u;
+        for (int u = 0; u < 16; ++u) {
             const float dtb = a[u] * wscale;
-            dbp = fmaf(dtb, sTF[t * 64 + s], dbp);
+            dbp = fmaf(dtb, sTF[(c0 + u) * 64 + s], dbp);
             a[u] = dtb * bs;
         }
-        sDbp[hf * 64 + s] = dbp;
-#pragma unroll
-        for (int u = 0; u < 32; u += 8)
-            sts128(sb + B_DT + umma::kmaj(s, 32 * hf + u, 64), pack_bf16(a[u], a[u + 1]), pack_bf16(a[u + 2], a[u + 3]),
-                   pack_bf16(a[u + 4], a[u + 5]), pack_bf16(a[u + 6], a[u + 7]));
+        sDbp[cg * 64 + s] = dbp;
+        sts_bf16x8(sb + B_DT + umma::kmaj(s, c0, 64), a, 0);
+        sts_bf16x8(sb + B_DT + umma::kmaj(s, c0 + 8, 64), a, 8);
     } else {  // lanes 64-127: s = l - 64; columns 64 + t: (dO U^T)[t][s]
         const int s = l - 64;
-        float a[32];
-        umma::ld32(tq + T3 + 64 + 32 * hf, a);
+        float a[16];
+        umma::ld16(tq + T3 + 64 + c0, a);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = 32 * hf + u;
+        for (int u = 0; u < 16; ++u) {
+            const int t = c0 + u;
             if (t >= s) {
-                const uint32_t o = umma::kmaj(64 + t, segoff(t >> 4) + s, 128);
+                const uint32_t o = umma::kmaj(64 + t, segoff(cg) + s, 128);
                 const float x = scale * a[u];
                 const uint16_t hb = bf16_bits(x);
                 sts16(sb + B_AP + o, hb);
@@ -708,46 +713,38 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                       umma::sdesc4(sb4 + ((B_T16 + ks * 32) >> 4), 16, 1024), id6, ks > 0 ? 1u : 0u);
         umma::commit(bar + 24);
     }
-    {  // meanwhile the anchored column operand R_seg^T
-        // column factor of segment i for a token of block bk: 1 / delta_bk when
-        // i = bk, else the decays of the blocks strictly between
+    {  // meanwhile the anchored column operand R_seg^T: for segment i >= cg,
+       // R_i[s] = k_s y_s c_i with c_i = 1 / delta_cg (i = cg), else the decays
+       // of the blocks strictly between
+        float y[16];
+        suffix(y);
 #pragma unroll
-        for (int bl = 0; bl < 2; ++bl) {
-            const int bk = 2 * hf + bl;
+        for (int i = 0; i < 4; ++i) {
+            if (i < cg) continue;
+            float c = 1.f;
+            if (i == cg) {
+                c = __frcp_rn(dl[cg]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i < bk) continue;
-                float c = 1.f;
-                if (i == bk) {
-                    c = __frcp_rn(dl[bk]);
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        if (m > bk && m < i) c *= dl[m];
-                }
-#pragma unroll
-                for (int u8 = 0; u8 < 16; u8 += 8) {
-                    float a[8];
-#pragma unroll
-                    for (int e2 = 0; e2 < 8; ++e2) {
-                        const int u = 16 * bl + u8 + e2;
-                        a[e2] = kf(u) * (y[u] * c);
-                    }
-                    sts128(sb + B_RS + umma::kmaj(ch, segoff(i) + 16 * bk + u8, 128), pack_bf16(a[0], a[1]),
-                           pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
-                }
+                for (int m = 0; m < 4; ++m)
+                    if (m > cg && m < i) c *= dl[m];
             }
+            float a[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) a[u] = kf(u) * (y[u] * c);
+            sts_bf16x8(sb + B_RS + umma::kmaj(ch, segoff(i) + c0, 128), a, 0);
+            sts_bf16x8(sb + B_RS + umma::kmaj(ch, segoff(i) + c0 + 8, 128), a, 8);
         }
     }
     pend |= umma::mbar_wait(bar + 24, par, WAIT_LIMIT) ? 0u : 8u;
     umma::fence_after();
     if (qd < 2) {  // -Z as the MN-major B operand (n = b, k = t): row t = l
-        float a[32];
-        umma::ld32(tq + T6 + 32 * hf, a);
+        float a[16];
+        umma::ld16(tq + T6 + c0, a);
 #pragma unroll
-        for (int u = 0; u < 32; u += 8)
-            sts128(sb + B_ZT + umma::kmaj(l, 32 * hf + u, 64), pack_bf16(-a[u], -a[u + 1]), pack_bf16(-a[u + 2], -a[u + 3]),
-                   pack_bf16(-a[u + 4], -a[u + 5]), pack_bf16(-a[u + 6], -a[u + 7]));
+        for (int u = 0; u < 16; ++u) a[u] = -a[u];
+        sts_bf16x8(sb + B_ZT + umma::kmaj(l, c0, 64), a, 0);
+        sts_bf16x8(sb + B_ZT + umma::kmaj(l, c0 + 8, 64), a, 8);
     }
     umma::fence_proxy_async();
     umma::fence_before();
@@ -767,13 +764,13 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_after();
     if (qd < 2) {  // row a = l of dA (strictly lower): beta gradient, dM into A'
         const int a = l;
-        float v[32];
-        umma::ld32(tq + T7 + 32 * hf, v);
+        float v[16];
+        umma::ld16(tq + T7 + c0, v);
         const float ba = sBeta[a];
         float dbp = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int b = 32 * hf + u;
+        for (int u = 0; u < 16; ++u) {
+            const int b = c0 + u;
             if (b < a) {
                 dbp = fmaf(v[u], sMT[b * 64 + a], dbp);
                 const uint32_t o = umma::kmaj(a, segoff(a >> 4) + b, 128);
@@ -783,22 +780,21 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                 sts16(sb + B_APL + o, bf16_bits(x - __uint_as_float((uint32_t)hb << 16)));
             }
         }
-        sDbp[128 + hf * 64 + a] = dbp;
+        sDbp[256 + cg * 64 + a] = dbp;
     }
     __syncthreads();  // T and M^T read: L^T goes over them
-    // the anchored row operand L^T (row ch: k x, then q x)
+    {  // the anchored row operand L^T (row ch: k x, then q x)
+        float x[16], a[16], b[16];
+        prefix(x);
 #pragma unroll
-    for (int u = 0; u < 32; u += 8) {
-        float a[8], b[8];
-#pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) {
-            a[e2] = kf(u + e2) * x[u + e2];
-            b[e2] = qf(u + e2) * x[u + e2];
+        for (int u = 0; u < 16; ++u) {
+            a[u] = kf(u) * x[u];
+            b[u] = qf(u) * x[u];
         }
-        sts128(sb + B_LT + umma::kmaj(ch, 32 * hf + u, 128), pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]),
-               pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
-        sts128(sb + B_LT + umma::kmaj(ch, 64 + 32 * hf + u, 128), pack_bf16(b[0], b[1]), pack_bf16(b[2], b[3]),
-               pack_bf16(b[4], b[5]), pack_bf16(b[6], b[7]));
+        sts_bf16x8(sb + B_LT + umma::kmaj(ch, c0, 128), a, 0);
+        sts_bf16x8(sb + B_LT + umma::kmaj(ch, c0 + 8, 128), a, 8);
+        sts_bf16x8(sb + B_LT + umma::kmaj(ch, 64 + c0, 128), b, 0);
+        sts_bf16x8(sb + B_LT + umma::kmaj(ch, 64 + c0 + 8, 128), b, 8);
     }
     umma::fence_proxy_async();
     umma::fence_before();
@@ -827,31 +823,50 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         }
         umma::commit(bar + 40);
     }
-    if (tid < CH && tid < Lc)
-        p.dbeta[(size_t)(tc + tid) * H + h] = (sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]);
+    if (tid < CH && tid < Lc) {
+        float db = 0.f;
+#pragma unroll
+        for (int pq = 0; pq < 8; ++pq) db += sDbp[pq * 64 + tid];
+        p.dbeta[(size_t)(tc + tid) * H + h] = db;
+    }
     pend |= umma::mbar_wait(bar + 40, par, WAIT_LIMIT) ? 0u : 32u;
     umma::fence_after();
 
-    // ---------------------------------------------------------------- token gradients of channel ch
+    // ---------------------------------------------------------------- token gradients of channel ch, block cg
     {
         const float gamC = dl[0] * dl[1] * dl[2] * dl[3];
-        const float dgc = gamC * wscale * (sDgc[ch] + sDgc[128 + ch]);
-        float dgam[32];
-        float sh = 0.f;  // sum over this half of dK^ . K^
+        const float dgc = gamC * wscale * ((sDgc[ch] + sDgc[128 + ch]) + (sDgc[256 + ch] + sDgc[384 + ch]));
+        float dgam[16];
+        float sh = 0.f;  // sum over this block of dK^ . K^
+        // column factors of the segments i >= cg (see R_seg^T)
+        float cs[4];
 #pragma unroll
-        for (int u0 = 0; u0 < 32; u0 += 8) {
-            const int bl = u0 >> 4, bk = 2 * hf + bl;
-            const int t0 = 32 * hf + u0;
-            // every column group of these 8 tokens in one round of loads
-            uint32_t a4[8], a5[8], a6[8], a7[8], a8[8], r9[4][8];
-            umma::ld8_async(tq + T4 + t0, a4);       // S dO^T
-            umma::ld8_async(tq + T4 + 64 + t0, a5);  // -S dVres^T
-            umma::ld8_async(tq + T5 + t0, a6);       // dS' U^T
-            umma::ld8_async(tq + T8 + t0, a7);       // dL (k rows)
-            umma::ld8_async(tq + T8 + 64 + t0, a8);  // dL (q rows)
+        for (int i = 0; i < 4; ++i) {
+            float c = 1.f;
+            if (i == cg) {
+                c = __frcp_rn(dl[cg]);
+            } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (m > cg && m < i) c *= dl[m];
+            }
+            cs[i] = c;
+        }
+        float xr = 1.f, y[16];
+        suffix(y);
+#pragma unroll
+        for (int u0 = 0; u0 < 16; u0 += 4) {
+            const int t0 = c0 + u0;
+            // every column group of these 4 tokens in one round of loads
+            uint32_t a4[4], a5[4], a6[4], a7[4], a8[4], r9[4][4];
+            umma::ld4_async(tq + T4 + t0, a4);       // S dO^T
+            umma::ld4_async(tq + T4 + 64 + t0, a5);  // -S dVres^T
+            umma::ld4_async(tq + T5 + t0, a6);       // dS' U^T
+            umma::ld4_async(tq + T8 + t0, a7);       // dL (k rows)
+            umma::ld4_async(tq + T8 + 64 + t0, a8);  // dL (q rows)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (i >= bk) umma::ld8_async(tq + T9 + segoff(i) + t0, r9[i]);  // dR_seg
+                if (i >= cg) umma::ld4_async(tq + T9 + segoff(i) + t0, r9[i]);  // dR_seg
             umma::wait_ld();
             umma::hold(a4);
             umma::hold(a5);
@@ -860,46 +875,33 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             umma::hold(a8);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (i >= bk) umma::hold(r9[i]);
-            float kc[8], rr[8];  // sum_i f_i dR_i, and sum_i R_i dR_i with R_i as the product read it (bf16)
+                if (i >= cg) umma::hold(r9[i]);
 #pragma unroll
-            for (int e2 = 0; e2 < 8; ++e2) kc[e2] = rr[e2] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i < bk) continue;
-                float c = 1.f;
-                if (i == bk) {
-                    c = __frcp_rn(dl[bk]);
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        if (m > bk && m < i) c *= dl[m];
-                }
-#pragma unroll
-                for (int e2 = 0; e2 < 8; ++e2) {
-                    const float f = y[u0 + e2] * c;
-                    const float r = __uint_as_float(r9[i][e2]);
-                    kc[e2] = fmaf(f, r, kc[e2]);
-                    rr[e2] = fmaf(bf16_round(kf(u0 + e2) * f), r, rr[e2]);
-                }
-            }
-            const float pre = bl ? pre1 : pre0, post = bl ? post1 : post0;
-#pragma unroll
-            for (int e2 = 0; e2 < 8; ++e2) {
+            for (int e2 = 0; e2 < 4; ++e2) {
                 const int u = u0 + e2, t = t0 + e2;
-                const float xx = x[u], gam = pre * xx, suf = y[u] * post;
+                xr *= e[u];  // x of token u
+                float kc = 0.f, rr = 0.f;  // sum_i f_i dR_i, and sum_i R_i dR_i with R_i as the product read it
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < cg) continue;
+                    const float f = y[u] * cs[i];
+                    const float r = __uint_as_float(r9[i][e2]);
+                    kc = fmaf(f, r, kc);
+                    rr = fmaf(bf16_round(kf(u) * f), r, rr);
+                }
+                const float xx = xr, gam = pre * xx, suf = y[u] * post;
                 const float kk = kf(u), qq = qf(u);
                 const float v4 = __uint_as_float(a4[e2]), v5 = __uint_as_float(a5[e2]), v6 = __uint_as_float(a6[e2]);
                 const float v7 = __uint_as_float(a7[e2]), v8 = __uint_as_float(a8[e2]);
                 const float dqs = scale * v4;
                 const float dq = fmaf(dqs, gam, xx * v8);
                 const float kh = wscale * v6 * suf;
-                const float dk = fmaf(v5, gam, xx * v7) + kc[e2] + kh;
+                const float dk = fmaf(v5, gam, xx * v7) + kc + kh;
                 // the anchored terms with the bf16 values of L and R_seg that the
                 // products used: each (row, column) pair inside [t, 63] then
                 // cancels in the reverse cumulative sum as it does exactly
                 dgam[u] = fmaf(dqs, qq * gam, v5 * (kk * gam)) - kh * kk +
-                          fmaf(bf16_round(kk * xx), v7, bf16_round(qq * xx) * v8) - rr[e2];
+                          fmaf(bf16_round(kk * xx), v7, bf16_round(qq * xx) * v8) - rr;
                 sh = fmaf(kh, kk, sh);
                 if (t < Lc) {
                     const size_t o = ((size_t)(tc + t) * H + h) * D + ch;
@@ -910,17 +912,20 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         }
         float tot = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) tot += dgam[u];
-        if (hf) sCum[ch] = tot;
-        sCum[128 * (1 + hf) + ch] = sh;
+        for (int u = 0; u < 16; ++u) tot += dgam[u];
+        sCum[cg * 128 + ch] = tot;
+        sCum[(4 + cg) * 128 + ch] = sh;
         __syncthreads();
         // gamma_C (and the K^ factors through it) collects at the chunk's last
         // token, so it adds to the reverse cumulative sum at every token
-        float acc = dgc + sCum[128 + ch] + sCum[256 + ch] + (hf ? 0.f : sCum[ch]);
+        float acc = dgc + ((sCum[512 + ch] + sCum[640 + ch]) + (sCum[768 + ch] + sCum[896 + ch]));
 #pragma unroll
-        for (int u = 31; u >= 0; --u) {
+        for (int c = 3; c > 0; --c)
+            if (c > cg) acc += sCum[c * 128 + ch];
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
             acc += dgam[u];
-            const int t = 32 * hf + u;
+            const int t = c0 + u;
             if (t < Lc) p.dg[((size_t)(tc + t) * H + h) * D + ch] = ((below >> u) & 1u) ? 0.f : acc;
         }
     }
