@@ -566,7 +566,8 @@ namespace {
 // and the reverse walk's dS'^T and dU'^T tiles; the slot list and the item
 // counters in front.
 struct BwdTcLayout {
-    size_t nslots, off_list, off_claim, off_blob, off_aux, off_s, off_u, off_ds, off_du, total;
+    size_t nslots, off_list, off_claim, off_carry, carry_stride, off_blob, off_aux, off_s, off_u, off_ds, off_du,
+        total;
 };
 BwdTcLayout bwd_tc_layout(int N, int T, int H) {
     BwdTcLayout L;
@@ -575,8 +576,11 @@ BwdTcLayout bwd_tc_layout(int N, int T, int H) {
     size_t off = 0;
     L.off_list = off;
     off += align256(L.nslots * sizeof(int2));
-    L.off_claim = off;
+    L.off_claim = off;  // one item counter per piece of the forward pass, one for the chunk kernel
     off += 256;
+    L.off_carry = off;  // two states per head for a sequence cut between pieces
+    L.carry_stride = (size_t)H * 128 * 128;
+    off += align256(2 * L.carry_stride * 4);
     L.off_blob = off;
     off += align256(sh * kda::kChunkBlobBytes);
     L.off_aux = off;
@@ -642,20 +646,35 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
         b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.cu_seqlens = cu_seqlens;
         b.N = N; b.T = T; b.H = H; b.scale = scale; b.g_min = g_min; b.dS_final = dS_final;
         b.dq = dq; b.dk = dk_; b.dv = dv_; b.dg = dg; b.dbeta = dbeta; b.dS0 = dS0;
-        b.list = list; b.claim = claim + 1; b.blob = blob; b.aux = aux;
+        b.list = list; b.blob = blob; b.aux = aux;
         b.save_s = ws + L.off_s; b.save_u = ws + L.off_u; b.save_ds = ws + L.off_ds; b.save_du = ws + L.off_du;
         b.status = status;
-        cudaError_t e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st);
+        // the forward pass in pieces as the prefill runs them: the chunk-local
+        // launch of piece p + 1 a programmatic dependent of the walk of piece
+        // p (it reads nothing the walk writes, and every piece keeps its own
+        // blobs, T and M for the reverse walk and the chunk kernel)
+        const int P = pipe_wanted(N, T, H, false) ? kPipePieces : 1;
+        const int piece = (nslots + P - 1) / P;
+        float *carry = reinterpret_cast<float *>(ws + L.off_carry);
+        b.claim = claim + P;
+        cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)(P + 1) * sizeof(int), st);
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(fa, N, nslots, list, st); });
-        if (e == cudaSuccess && T > 0)
+        for (int pc = 0; e == cudaSuccess && T > 0 && pc < P; ++pc) {
+            const int s0 = pc * piece, s1 = s0 + piece < nslots ? s0 + piece : nslots;
+            if (s0 >= s1) break;
+            unsigned char *pb = blob + (size_t)s0 * H * kda::kChunkBlobBytes;
             e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
-                return kda::launch_chunk_prep(fa, list, 0, nslots, blob, true, claim, false, st, aux);
+                return kda::launch_chunk_prep(fa, list, s0, s1, pb, true, claim + pc, pc > 0, st,
+                                              aux + (size_t)s0 * H * 8192);
             });
-        if (e == cudaSuccess && T > 0)
-            e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
-                return kda::launch_chunk_walk(fa, N, blob, 0, nslots, nullptr, nullptr, st, ws + L.off_s, ws + L.off_u);
-            });
+            if (e == cudaSuccess)
+                e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+                    return kda::launch_chunk_walk(fa, N, pb, s0, s1, carry + (size_t)(pc & 1) * L.carry_stride,
+                                                  carry + (size_t)((pc + 1) & 1) * L.carry_stride, st, ws + L.off_s,
+                                                  ws + L.off_u);
+                });
+        }
         if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] { return kda::launch_bwd_walk(b, st); });
         if (e == cudaSuccess && T > 0)
             e = timed_launch(KDA_KERNEL_BWD_CHUNK, st, [&] { return kda::launch_bwd_chunk(b, nslots, st); });

@@ -345,19 +345,16 @@ constexpr uint32_t B_MT = 204800;   // M^T f32 [64][64]
 // (those two tiles are copied once the rows are read), v in the rows 64-127
 // of the [dO; -dVres] tile (its two 8 KB value halves) until -dVres goes there
 constexpr uint32_t B_KST = B_UB, B_QST = B_VR, B_GST = B_DS;
-// phases C and D, over the phase A / B regions once the second batch is done
-// (A' in two bf16 parts, high and low: the anchored products cancel between
-// their row and column sides in the log-decay gradient, so A' keeps about 16
-// mantissa bits):
-constexpr uint32_t B_AP = 0;        // A' high part, K-major 128 rows x 192 (three K blocks of 16 KB)
-constexpr uint32_t B_APL = 49152;   // A' low part
+// phases C and D, over the phase A / B regions once the second batch is done:
+constexpr uint32_t B_AP = 0;        // A' K-major 128 rows x 192 (three K blocks of 16 KB)
 constexpr uint32_t B_T16 = 98304;   // T bf16 K-major 64 x 64
 constexpr uint32_t B_DT = 106496;   // dT, MN-major (m = t, k = s)
 constexpr uint32_t B_ZT = 114688;   // -Z, MN-major (n = b, k = t)
 constexpr uint32_t B_RS = 122880;   // R_seg^T K-major 128 channels x 192 (three K blocks)
 constexpr uint32_t B_LT = 188416;   // L^T K-major 128 channels x 128 (two K blocks), over T and M^T
                                     // once the beta gradient has read them
-constexpr uint32_t B_CUM = 0;       // the combine's block sums f32 [8][128], over A' once read
+constexpr uint32_t B_CUM = B_KT;    // the combine's block sums f32 [8][128] (K~ is built after the
+                                    // next item's copies, which go out during the combine, have landed)
 constexpr uint32_t B_MISC = 221184;
 constexpr uint32_t B_BETA = B_MISC;           // f32 [64]
 constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
@@ -436,6 +433,26 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     uint32_t it = 0;
     bool alive = true;
     __syncthreads();  // claims read before thread 0 writes the next ones
+    // thread 0 issues an item's copies, all on the loads barrier: the tiles
+    // S^T, dU'^T, T | M^T, and the rows (dO and v by swizzled boxes, k, q, g
+    // plain).  An item's copies go out during the previous item's combine
+    // (every region they fill is free by then) unless that item was skipped.
+    auto issue_loads = [&](int wi, int hi, int ti) {
+        umma::fence_proxy_async();
+        umma::mbar_expect_tx(bar, TILE_S + TILE_U + 4 * AUX_FLOATS + 4 * 16384u + 32768u);
+        umma::bulk_load(sb + B_SB, p.save_s + (size_t)wi * TILE_S, TILE_S, bar);
+        umma::bulk_load(sb + B_DU, p.save_du + (size_t)wi * TILE_U, TILE_U, bar);
+        umma::bulk_load(sb + B_TF, p.aux + (size_t)wi * AUX_FLOATS, 4 * AUX_FLOATS, bar);
+        umma::tma_load_3d(sb + B_DO, &p.tdo, 0, hi, ti, bar);
+        umma::tma_load_3d(sb + B_DO + 16384, &p.tdo, 64, hi, ti, bar);
+        umma::tma_load_3d(sb + B_DO + 8192, &p.tv, 0, hi, ti, bar);
+        umma::tma_load_3d(sb + B_DO + 24576, &p.tv, 64, hi, ti, bar);
+        umma::tma_load_3d(sb + B_KST, &p.tk, 0, hi, ti, bar);
+        umma::tma_load_3d(sb + B_QST, &p.tq, 0, hi, ti, bar);
+        umma::tma_load_3d(sb + B_GST, &p.tg, 0, hi, ti, bar);
+    };
+    bool preloaded = false;  // thread 0: the item in hand's copies went out during the previous one
+    int2 ncl = make_int2(0, 0);  // thread 0: chunk entry of the next item
 
     while (w < p.nitems) {
     const int slot = w / H, h = w % H;
@@ -446,21 +463,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     uint32_t pend = 0;  // barriers whose wait gave up
     // ---------------------------------------------------------------- loads
     if (tid == 0) {
-        umma::fence_proxy_async();
-        umma::mbar_expect_tx(bar, TILE_S + TILE_U + 4 * AUX_FLOATS + 4 * 16384u + 32768u);
-        umma::bulk_load(sb + B_SB, p.save_s + (size_t)w * TILE_S, TILE_S, bar);
-        umma::bulk_load(sb + B_DU, p.save_du + (size_t)w * TILE_U, TILE_U, bar);
-        umma::bulk_load(sb + B_TF, p.aux + (size_t)w * AUX_FLOATS, 4 * AUX_FLOATS, bar);
-        umma::tma_load_3d(sb + B_DO, &p.tdo, 0, h, tc, bar);
-        umma::tma_load_3d(sb + B_DO + 16384, &p.tdo, 64, h, tc, bar);
-        umma::tma_load_3d(sb + B_DO + 8192, &p.tv, 0, h, tc, bar);
-        umma::tma_load_3d(sb + B_DO + 24576, &p.tv, 64, h, tc, bar);
-        umma::tma_load_3d(sb + B_KST, &p.tk, 0, h, tc, bar);
-        umma::tma_load_3d(sb + B_QST, &p.tq, 0, h, tc, bar);
-        umma::tma_load_3d(sb + B_GST, &p.tg, 0, h, tc, bar);
+        if (!preloaded) issue_loads(w, h, tc);
         // the next item's tiles and rows into L2 while this one runs
+        ncl = (wn < p.nitems) ? p.list[wn / H] : make_int2(0, 0);
         if (wn < p.nitems) {
-            const int2 ncl = p.list[wn / H];
             if (ncl.y > 0) {
                 const int hn = wn % H;
                 umma::prefetch_l2(p.save_s + (size_t)wn * TILE_S, TILE_S);
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_after();
     __syncthreads();  // every thread is done with the S and dS' tiles
     // the phase A / B regions are free: zero A', and T in bf16
-    for (int idx = tid; idx < 2 * 49152 / 16; idx += NB)
+    for (int idx = tid; idx < 49152 / 16; idx += NB)
         *reinterpret_cast<uint4 *>(sm + B_AP + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
     {
         const int t = tid >> 3, s = 8 * (tid & 7);
@@ -690,13 +696,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int t = c0 + u;
-            if (t >= s) {
-                const uint32_t o = umma::kmaj(64 + t, segoff(cg) + s, 128);
-                const float x = scale * a[u];
-                const uint16_t hb = bf16_bits(x);
-                sts16(sb + B_AP + o, hb);
-                sts16(sb + B_APL + o, bf16_bits(x - __uint_as_float((uint32_t)hb << 16)));
-            }
+            if (t >= s) sts16(sb + B_AP + umma::kmaj(64 + t, segoff(cg) + s, 128), bf16_bits(scale * a[u]));
         }
     }
     umma::fence_proxy_async();
@@ -773,11 +773,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             const int b = c0 + u;
             if (b < a) {
                 dbp = fmaf(v[u], sMT[b * 64 + a], dbp);
-                const uint32_t o = umma::kmaj(a, segoff(a >> 4) + b, 128);
-                const float x = ba * v[u];
-                const uint16_t hb = bf16_bits(x);
-                sts16(sb + B_AP + o, hb);
-                sts16(sb + B_APL + o, bf16_bits(x - __uint_as_float((uint32_t)hb << 16)));
+                sts16(sb + B_AP + umma::kmaj(a, segoff(a >> 4) + b, 128), bf16_bits(ba * v[u]));
             }
         }
         sDbp[256 + cg * 64 + a] = dbp;
@@ -806,20 +802,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         constexpr uint32_t id8 = umma::idesc_bf16(128, 128, 0, 0, 0);
         constexpr uint32_t id9 = umma::idesc_bf16(128, 160, 0, 1, 0);
 #pragma unroll
-        for (int pt = 0; pt < 2; ++pt) {  // A' high part, then low part
-            const uint32_t ap = pt ? B_APL : B_AP;
+        for (int ks = 0; ks < 10; ++ks) {
+            const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+            umma::mma(tmem + T8, umma::sdesc4(sb4 + ((B_RS + kb * 16384 + kin) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((B_AP + kb * 16384 + kin) >> 4), 16, 1024), id8, ks > 0 ? 1u : 0u);
+        }
 #pragma unroll
-            for (int ks = 0; ks < 10; ++ks) {
-                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                umma::mma(tmem + T8, umma::sdesc4(sb4 + ((B_RS + kb * 16384 + kin) >> 4), 16, 1024),
-                          umma::sdesc4(sb4 + ((ap + kb * 16384 + kin) >> 4), 16, 1024), id8, (pt || ks > 0) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-                umma::mma(tmem + T9, umma::sdesc4(sb4 + ((B_LT + kb * 16384 + kin) >> 4), 16, 1024),
-                          umma::sdesc4(sb4 + ((ap + ks * 2048) >> 4), 16384, 1024), id9, (pt || ks > 0) ? 1u : 0u);
-            }
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
+            umma::mma(tmem + T9, umma::sdesc4(sb4 + ((B_LT + kb * 16384 + kin) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((B_AP + ks * 2048) >> 4), 16384, 1024), id9, ks > 0 ? 1u : 0u);
         }
         umma::commit(bar + 40);
     }
@@ -831,6 +823,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     }
     pend |= umma::mbar_wait(bar + 40, par, WAIT_LIMIT) ? 0u : 32u;
     umma::fence_after();
+    if (tid == 0) {  // every product has read its operands: the next item's copies, and the one after claimed
+        preloaded = wn < p.nitems && ncl.y > 0 && pend == 0;
+        if (preloaded) issue_loads(wn, wn % H, ncl.x);
+        sClaim[0] = (wn < p.nitems) ? atomicAdd(p.claim, 1) : p.nitems;
+    }
 
     // ---------------------------------------------------------------- token gradients of channel ch, block cg
     {
@@ -935,11 +932,14 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         if (pend & 1u) umma::mbar_wait(bar, par, WAIT_LIMIT);
         for (int b = 1; b < 7; ++b)
             if (pend & (1u << b)) umma::mbar_wait(bar + 8 * b, par, WAIT_LIMIT);
+        if (tid == 0 && preloaded) umma::mbar_wait(bar, par ^ 1u, WAIT_LIMIT);  // the next item's copies
         alive = false;
         break;
     }
-    }  // Lc > 0
-    if (tid == 0) sClaim[0] = (wn < p.nitems) ? atomicAdd(p.claim, 1) : p.nitems;
+    } else if (tid == 0) {  // Lc > 0: nothing to do for this item; claim the one after the next
+        preloaded = false;
+        sClaim[0] = (wn < p.nitems) ? atomicAdd(p.claim, 1) : p.nitems;
+    }
     __syncthreads();
     w = wn;
     wn = sClaim[0];

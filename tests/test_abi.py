@@ -150,14 +150,15 @@ def test_kernel_timing_without_launches(lib):
 
 
 def _bwd_tc_bytes(N, T, H):
-    """The tensor-core backward's workspace (d = 128, bf16): the slot list and
-    item counters, then per (slot, head) the operand blob (66,048 B), T and M^T
+    """The tensor-core backward's workspace (d = 128, bf16): the slot list, the
+    item counters and two carry states per head, then per (slot, head) the operand blob (66,048 B), T and M^T
     (f32, 32 KB), the walk's S^T and U^T tiles (32 + 16 KB) and the reverse
     walk's dS'^T and dU'^T tiles (32 + 16 KB), each part 256-byte aligned."""
     slots = T // 64 + N
     sh = slots * H
-    return (_align256(slots * 8) + 256 + _align256(sh * 66048) + _align256(sh * 32768) + _align256(sh * 32768) +
-            _align256(sh * 16384) + _align256(sh * 32768) + _align256(sh * 16384))
+    carry = _align256(2 * H * 128 * 128 * 4)  # two states per head for a sequence cut between pieces
+    return (_align256(slots * 8) + 256 + carry + _align256(sh * 66048) + _align256(sh * 32768) +
+            _align256(sh * 32768) + _align256(sh * 16384) + _align256(sh * 32768) + _align256(sh * 16384))
 
 
 def test_backward_workspace_arithmetic(lib):
