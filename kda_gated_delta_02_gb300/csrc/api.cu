@@ -656,8 +656,7 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
         const int P = pipe_wanted(N, T, H, false) ? kPipePieces : 1;
         const int piece = (nslots + P - 1) / P;
         float *carry = reinterpret_cast<float *>(ws + L.off_carry);
-        b.claim = claim + P;
-        cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)(P + 1) * sizeof(int), st);
+        cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)(2 * P) * sizeof(int), st);
         if (e == cudaSuccess)
             e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(fa, N, nslots, list, st); });
         for (int pc = 0; e == cudaSuccess && T > 0 && pc < P; ++pc) {
@@ -675,9 +674,37 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
                                                   ws + L.off_u);
                 });
         }
-        if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] { return kda::launch_bwd_walk(b, st); });
-        if (e == cudaSuccess && T > 0)
-            e = timed_launch(KDA_KERNEL_BWD_CHUNK, st, [&] { return kda::launch_bwd_chunk(b, nslots, st); });
+        // then the reverse pass in the same pieces, newest first: the chunk
+        // gradients of piece p (which need its reverse walk complete) run as a
+        // programmatic dependent of the reverse walk of the piece before it
+        // in slot order, on the SMs that walk leaves free
+        auto rpiece = [&](int r, int &s0, int &s1) {  // r-th piece of the reverse pass
+            const int pc = P - 1 - r;
+            s0 = pc * piece;
+            s1 = s0 + piece < nslots ? s0 + piece : nslots;
+        };
+        for (int r = 0; e == cudaSuccess && r <= P; ++r) {
+            int s0 = 0, s1 = 0;
+            if (r < P) {
+                rpiece(r, s0, s1);
+                if (T == 0) {
+                    s0 = 0;
+                    s1 = nslots;
+                }
+                e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+                    return kda::launch_bwd_walk(b, s0, s1, carry + (size_t)(r & 1) * L.carry_stride,
+                                                carry + (size_t)((r + 1) & 1) * L.carry_stride, st);
+                });
+                if (T == 0) break;
+            }
+            if (e == cudaSuccess && r > 0) {
+                int c0 = 0, c1 = 0;
+                rpiece(r - 1, c0, c1);
+                e = timed_launch(KDA_KERNEL_BWD_CHUNK, st, [&] {
+                    return kda::launch_bwd_chunk(b, c0, c1, claim + P + (r - 1), r < P, st);
+                });
+            }
+        }
         return cuda_status(e);
     }
     kda::BwdArgs a = {};

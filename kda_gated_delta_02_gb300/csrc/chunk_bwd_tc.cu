@@ -92,6 +92,13 @@ struct RwalkParams {
     float wscale;                  // the state gradient walks as dS / wscale
     int zero_do;                   // scale == 0: dO enters no product
     unsigned char *save_ds, *save_du;  // [slot][H] tiles dS'^T (32 KB), dU'^T (16 KB)
+    // this launch walks the chunks in slots [slot0, slot1) (a piece); a
+    // sequence that continues in later slots starts from carry_in, one that
+    // continues in earlier slots leaves its dS' in carry_out ([H][128][128]
+    // f32 each, lane-major as the tensor memory holds it)
+    int slot0, slot1;
+    const float *carry_in;
+    float *carry_out;
     uint32_t *status;
 };
 
@@ -103,18 +110,25 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
     const uint32_t bar0 = sb + R_BAR, bar_u = bar0 + 16, bar_o = bar0 + 24;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, h = blockIdx.y, H = P.H;
+    // a chunk-gradient launch that follows on the stream as a programmatic
+    // dependent may start once every CTA of this walk is resident: it reads
+    // only what earlier launches wrote
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int t0 = P.cu[n], t1 = P.cu[n + 1];
     const size_t uoff = ((size_t)n * H + h) * D * D;
     if (t0 < 0 || t1 < t0 || t1 > P.T) {
-        if (tid == 0 && h == 0) report_status(P.status, KDA_STATUS_BAD_SEQLENS);
+        if (tid == 0 && h == 0 && P.slot1 == P.N + P.T / CH) report_status(P.status, KDA_STATUS_BAD_SEQLENS);
         return;
     }
     const int nch = (t1 - t0 + CH - 1) / CH, sbase = t0 / CH + n;
-    if (nch == 0) {  // an empty sequence passes its final-state gradient through
-        if (P.dS0)
+    if (nch == 0) {  // an empty sequence passes its final-state gradient through (in the piece of its slot)
+        if (P.dS0 && sbase >= P.slot0 && sbase < P.slot1)
             for (int e = tid; e < D * D; e += NR) P.dS0[uoff + e] = P.dS_final ? P.dS_final[uoff + e] : 0.f;
         return;
     }
+    const int jb = max(0, P.slot0 - sbase), je = min(nch, P.slot1 - sbase);
+    if (jb >= je) return;
+    const bool cut_in = je < nch, cut_out = jb > 0;  // continues in later / earlier slots
     const float wscale = P.wscale, inv = 1.0f / wscale;
 
     if (tid == 0) {
@@ -130,11 +144,17 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
     const int jrow = 32 * qd + lane;          // dS'^T row (value column j) owned
     const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
 
-    {  // dS'^T = dS_final^T / wscale (lane j, columns = key channel i)
+    {  // dS'^T = dS_final^T / wscale (lane j, columns = key channel i), or the carried dS'^T
         float r[32];
-        const float *src = P.dS_final ? P.dS_final + uoff : nullptr;
+        if (cut_in) {
+            const float *src = P.carry_in + (size_t)h * D * D;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) r[c] = src ? src[(size_t)(32 * cg + c) * D + jrow] * inv : 0.f;
+            for (int c = 0; c < 32; ++c) r[c] = src[(size_t)(32 * cg + c) * D + jrow];
+        } else {
+            const float *src = P.dS_final ? P.dS_final + uoff : nullptr;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = src ? src[(size_t)(32 * cg + c) * D + jrow] * inv : 0.f;
+        }
         umma::st32(tq + TM_S + 32 * cg, r);
     }
 
@@ -159,10 +179,10 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
     int pend_m = -1;  // products whose completion wait gave up (0: dU, 1: dS)
     uint32_t pend_mph = 0;
     const bool save = P.save_ds != nullptr;
-    issue(nch - 1, 0);
+    issue(je - 1, 0);
 
-    for (int j = nch - 1; j >= 0; --j) {
-        const int it = nch - 1 - j, b = it & 1;
+    for (int j = je - 1; j >= jb; --j) {
+        const int it = je - 1 - j, b = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pm = (uint32_t)it & 1u;
         const int tc = t0 + CH * j, Lc = min(CH, t1 - tc);
         const uint32_t bb = R_BUF + (uint32_t)b * R_BUFSTRIDE;
@@ -170,7 +190,7 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
         timed_out |= !landed;
         pend_b = landed ? -1 : b;
         pend_ph = ph;
-        if (j > 0 && !timed_out) {
+        if (j > jb && !timed_out) {
             issue(j - 1, b ^ 1);
             pend_b = b ^ 1;
             pend_ph = (uint32_t)((it + 1) >> 1) & 1u;
@@ -308,6 +328,12 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
         // before the shared and tensor memory are released
         if (pend_b >= 0) umma::mbar_wait(bar0 + 8 * pend_b, pend_ph, WAIT_LIMIT);
         if (pend_m >= 0) umma::mbar_wait(pend_m ? bar_o : bar_u, pend_mph, WAIT_LIMIT);
+    } else if (cut_out) {
+        float r[32];
+        umma::ld32(tq + TM_S + 32 * cg, r);
+        float *dst = P.carry_out + (size_t)h * D * D;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * D + jrow] = r[c];
     } else if (P.dS0) {
         float r[32];
         umma::ld32(tq + TM_S + 32 * cg, r);
@@ -377,7 +403,8 @@ struct BchunkParams {
     float scale, wscale, g_min;
     int zero_do;
     const int2 *list;                // slot -> {first token, length}
-    int nitems;                      // slots x H; item w = slot * H + h
+    int slot0;                       // first slot of this launch (a piece)
+    int nitems;                      // slots x H of this launch; item w (slot0 H + w overall) = slot, head
     int *claim;                      // item counter, zero at launch
     const unsigned char *save_s, *save_u, *save_ds, *save_du;  // [slot][H] tiles
     const float *aux;                // [slot][H][2][64][64]: T, M^T
@@ -440,9 +467,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     auto issue_loads = [&](int wi, int hi, int ti) {
         umma::fence_proxy_async();
         umma::mbar_expect_tx(bar, TILE_S + TILE_U + 4 * AUX_FLOATS + 4 * 16384u + 32768u);
-        umma::bulk_load(sb + B_SB, p.save_s + (size_t)wi * TILE_S, TILE_S, bar);
-        umma::bulk_load(sb + B_DU, p.save_du + (size_t)wi * TILE_U, TILE_U, bar);
-        umma::bulk_load(sb + B_TF, p.aux + (size_t)wi * AUX_FLOATS, 4 * AUX_FLOATS, bar);
+        const size_t wa = (size_t)p.slot0 * p.H + wi;  // (slot, head) index over all slots
+        umma::bulk_load(sb + B_SB, p.save_s + wa * TILE_S, TILE_S, bar);
+        umma::bulk_load(sb + B_DU, p.save_du + wa * TILE_U, TILE_U, bar);
+        umma::bulk_load(sb + B_TF, p.aux + wa * AUX_FLOATS, 4 * AUX_FLOATS, bar);
         umma::tma_load_3d(sb + B_DO, &p.tdo, 0, hi, ti, bar);
         umma::tma_load_3d(sb + B_DO + 16384, &p.tdo, 64, hi, ti, bar);
         umma::tma_load_3d(sb + B_DO + 8192, &p.tv, 0, hi, ti, bar);
@@ -455,7 +483,8 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     int2 ncl = make_int2(0, 0);  // thread 0: chunk entry of the next item
 
     while (w < p.nitems) {
-    const int slot = w / H, h = w % H;
+    const int slot = p.slot0 + w / H, h = w % H;
+    const size_t wa = (size_t)p.slot0 * H + w;  // (slot, head) index over all slots
     const int2 cl = p.list[slot];
     const int tc = cl.x, Lc = cl.y;
     const uint32_t par = it & 1u;
@@ -465,15 +494,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     if (tid == 0) {
         if (!preloaded) issue_loads(w, h, tc);
         // the next item's tiles and rows into L2 while this one runs
-        ncl = (wn < p.nitems) ? p.list[wn / H] : make_int2(0, 0);
+        ncl = (wn < p.nitems) ? p.list[p.slot0 + wn / H] : make_int2(0, 0);
         if (wn < p.nitems) {
             if (ncl.y > 0) {
                 const int hn = wn % H;
-                umma::prefetch_l2(p.save_s + (size_t)wn * TILE_S, TILE_S);
-                umma::prefetch_l2(p.save_ds + (size_t)wn * TILE_S, TILE_S);
-                umma::prefetch_l2(p.save_u + (size_t)wn * TILE_U, TILE_U);
-                umma::prefetch_l2(p.save_du + (size_t)wn * TILE_U, TILE_U);
-                umma::prefetch_l2(p.aux + (size_t)wn * AUX_FLOATS, 4 * AUX_FLOATS);
+                const size_t wna = (size_t)p.slot0 * H + wn;
+                umma::prefetch_l2(p.save_s + wna * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_ds + wna * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_u + wna * TILE_U, TILE_U);
+                umma::prefetch_l2(p.save_du + wna * TILE_U, TILE_U);
+                umma::prefetch_l2(p.aux + wna * AUX_FLOATS, 4 * AUX_FLOATS);
                 umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
                 umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
                 umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
@@ -572,8 +602,8 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         // the rows are read: the tiles that go over their staging
         umma::fence_proxy_async();
         umma::mbar_expect_tx(bar + 48, TILE_S + TILE_U);
-        umma::bulk_load(sb + B_DS, p.save_ds + (size_t)w * TILE_S, TILE_S, bar + 48);
-        umma::bulk_load(sb + B_UB, p.save_u + (size_t)w * TILE_U, TILE_U, bar + 48);
+        umma::bulk_load(sb + B_DS, p.save_ds + wa * TILE_S, TILE_S, bar + 48);
+        umma::bulk_load(sb + B_UB, p.save_u + wa * TILE_U, TILE_U, bar + 48);
         constexpr uint32_t id1 = umma::idesc_bf16(128, 64, 0, 1, 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -949,6 +979,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tmem, 512);
+    // launched as a programmatic dependent of a reverse walk: finish only
+    // after that walk has, so the next launch on the stream (which waits for
+    // this one) also follows it (a no-op for an ordinary launch)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 }  // namespace bt
@@ -985,7 +1019,8 @@ bool encode_plain(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int 
 }
 }  // namespace
 
-cudaError_t launch_bwd_walk(const BwdTcArgs &a, cudaStream_t st) {
+cudaError_t launch_bwd_walk(const BwdTcArgs &a, int slot0, int slot1, const float *carry_in, float *carry_out,
+                            cudaStream_t st) {
     if (a.N <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(bt::kda_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bt::R_SMEM);
@@ -1004,12 +1039,18 @@ cudaError_t launch_bwd_walk(const BwdTcArgs &a, cudaStream_t st) {
     P.wscale = a.scale == 0.f ? 1.f : a.scale;
     P.save_ds = a.save_ds;
     P.save_du = a.save_du;
+    P.slot0 = slot0;
+    P.slot1 = slot1;
+    P.carry_in = carry_in;
+    P.carry_out = carry_out;
     P.status = a.status;
     bt::kda_bwd_walk_kernel<<<dim3(a.N, a.H), bt::NR, bt::R_SMEM, st>>>(P);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st) {
+cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int slot0, int slot1, int *claim, bool after_walk,
+                             cudaStream_t st) {
+    const int nslots = slot1 - slot0;
     if (nslots <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(bt::kda_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bt::B_SMEM);
@@ -1027,8 +1068,9 @@ cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st) {
     P.wscale = a.scale == 0.f ? 1.f : a.scale;
     P.g_min = a.g_min;
     P.list = a.list;
+    P.slot0 = slot0;
     P.nitems = nslots * a.H;
-    P.claim = a.claim;
+    P.claim = claim;
     P.save_s = a.save_s;
     P.save_u = a.save_u;
     P.save_ds = a.save_ds;
@@ -1055,8 +1097,17 @@ cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st) {
         }
     }
     const int grid = P.nitems < sms ? P.nitems : sms;  // persistent: one CTA per SM
-    bt::kda_bwd_chunk_kernel<<<grid, bt::NB, bt::B_SMEM, st>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(bt::NB);
+    cfg.dynamicSmemBytes = bt::B_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_walk ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, bt::kda_bwd_chunk_kernel, P);
 }
 
 }  // namespace kda

@@ -132,14 +132,22 @@ struct BwdTcArgs {
     const float *dS_final;
     float *dq, *dk, *dv, *dg, *dbeta, *dS0;
     const int2 *list;
-    int *claim;                      // item counter of the chunk kernel, zero at launch
     const unsigned char *blob;
     const float *aux;
     unsigned char *save_s, *save_u, *save_ds, *save_du;
     uint32_t *status;
 };
-cudaError_t launch_bwd_walk(const BwdTcArgs &a, cudaStream_t st);
-cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int nslots, cudaStream_t st);
+// The reverse walk over the chunks in slots [slot0, slot1), newest first; a
+// sequence cut at slot1 starts from carry_in, one cut at slot0 leaves its
+// state gradient in carry_out ([H][128][128] f32 each).
+cudaError_t launch_bwd_walk(const BwdTcArgs &a, int slot0, int slot1, const float *carry_in, float *carry_out,
+                            cudaStream_t st);
+// The chunk gradients of slots [slot0, slot1); claim is a device int that is
+// zero when the launch starts.  With after_walk the launch is a programmatic
+// dependent of the reverse walk launched just before it on `st` (it may start
+// while that walk runs: it reads only what earlier launches wrote).
+cudaError_t launch_bwd_chunk(const BwdTcArgs &a, int slot0, int slot1, int *claim, bool after_walk,
+                             cudaStream_t st);
 
 struct VerifyArgs {
     void *state, *tail;

@@ -143,6 +143,22 @@ def test_tensor_core_backward_many_short_sequences(kda, oracle):
     assert torch.equal(got[5][3], x["dSf"][3])
 
 
+def test_tensor_core_backward_in_pieces(kda, oracle):
+    """105 chunk slots over 2 heads run as four pipelined pieces (the forward
+    pass, then the reverse walk newest piece first with each piece's chunk
+    gradients overlapping the next piece's walk): sequences cross piece
+    boundaries in both passes (carried states and state gradients), one is
+    empty."""
+    lens = [3000, 1500, 0, 2000]
+    x = _case(lens, 2, 128, torch.bfloat16, seed=37)
+    kda.kernel_timing_start()
+    got = _compare(kda, oracle, x, scale=0.9, tol=TC_TOL)
+    kern = kda.kernel_timing_stop()
+    assert kern["kda_bwd_walk_kernel"]["launches"] == 4 and kern["kda_bwd_chunk_kernel"]["launches"] == 4
+    assert kern["kda_chunk_walk_kernel"]["launches"] == 4
+    assert torch.equal(got[5][2], x["dSf"][2])
+
+
 def test_tensor_core_backward_scale_zero(kda, oracle):
     """scale = 0: the outputs are zero, so do enters no gradient; the state
     gradient still flows from dS_final."""
