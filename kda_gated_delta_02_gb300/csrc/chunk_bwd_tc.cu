@@ -658,16 +658,22 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_before();
     __syncthreads();
 
-    // ---------------------------------------------------------------- batch 2: [Vres; U][dU'; dO]^T, S [dO; -dVres]^T, dS' U^T
+    // ---------------------------------------------------------------- batch 2: Vres dU'^T, dO U^T, S [dO; -dVres]^T, dS' U^T
     if (tid == 0) {
         umma::fence_after();
-        constexpr uint32_t id3 = umma::idesc_bf16(128, 128, 1, 1, 0);
+        constexpr uint32_t id3 = umma::idesc_bf16(128, 64, 1, 1, 0);
         constexpr uint32_t id4 = umma::idesc_bf16(128, 128, 1, 0, 0);
         constexpr uint32_t id5 = umma::idesc_bf16(128, 64, 1, 1, 0);
+        // lanes 0-63: (dU' Vres^T)^T, lane s (A = [Vres; U], rows 64-127 unused)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T3, umma::sdesc4(sb4 + ((B_VR + ks * 2048) >> 4), 16384, 1024),
-                      umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 16384, 1024), id3, ks > 0 ? 1u : 0u);
+                      umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 1024, 1024), id3, ks > 0 ? 1u : 0u);
+        // lanes 64-127: dO U^T, lane t (A = [dU'; dO], rows 0-63 unused)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T3 + 64, umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id3, ks > 0 ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T4, umma::sdesc4(sb4 + ((B_SB + ks * 2048) >> 4), 16384, 1024),
@@ -719,14 +725,15 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         sDbp[cg * 64 + s] = dbp;
         sts_bf16x8(sb + B_DT + umma::kmaj(s, c0, 64), a, 0);
         sts_bf16x8(sb + B_DT + umma::kmaj(s, c0 + 8, 64), a, 8);
-    } else {  // lanes 64-127: s = l - 64; columns 64 + t: (dO U^T)[t][s]
-        const int s = l - 64;
+    } else {  // lanes 64-127: t = l - 64; columns 64 + s: (dO U^T)[t][s] -> A' row 64 + t (s <= t)
+        const int t = l - 64, bt = t >> 4;
         float a[16];
         umma::ld16(tq + T3 + 64 + c0, a);
+        if (cg <= bt) {  // the columns of this block lie in the segment of row t
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int t = c0 + u;
-            if (t >= s) sts16(sb + B_AP + umma::kmaj(64 + t, segoff(cg) + s, 128), bf16_bits(scale * a[u]));
+            for (int u = 0; u < 16; ++u) a[u] = (c0 + u <= t) ? scale * a[u] : 0.f;
+            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0, 128), a, 0);
+            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0 + 8, 128), a, 8);
         }
     }
     umma::fence_proxy_async();
@@ -792,8 +799,8 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     }
     pend |= umma::mbar_wait(bar + 32, par, WAIT_LIMIT) ? 0u : 16u;
     umma::fence_after();
-    if (qd < 2) {  // row a = l of dA (strictly lower): beta gradient, dM into A'
-        const int a = l;
+    if (qd < 2) {  // row a = l of dA (strictly lower): beta gradient, dM into A' row a
+        const int a = l, ba_blk = a >> 4;
         float v[16];
         umma::ld16(tq + T7 + c0, v);
         const float ba = sBeta[a];
@@ -801,12 +808,15 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int b = c0 + u;
-            if (b < a) {
-                dbp = fmaf(v[u], sMT[b * 64 + a], dbp);
-                sts16(sb + B_AP + umma::kmaj(a, segoff(a >> 4) + b, 128), bf16_bits(ba * v[u]));
-            }
+            const float da = (b < a) ? v[u] : 0.f;
+            dbp = fmaf(da, sMT[b * 64 + a], dbp);
+            v[u] = ba * da;
         }
         sDbp[256 + cg * 64 + a] = dbp;
+        if (cg <= ba_blk) {
+            sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0, 128), v, 0);
+            sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0 + 8, 128), v, 8);
+        }
     }
     __syncthreads();  // T and M^T read: L^T goes over them
     {  // the anchored row operand L^T (row ch: k x, then q x)
