@@ -493,26 +493,6 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     // ---------------------------------------------------------------- loads
     if (tid == 0) {
         if (!preloaded) issue_loads(w, h, tc);
-        // the next item's tiles and rows into L2 while this one runs
-        ncl = (wn < p.nitems) ? p.list[p.slot0 + wn / H] : make_int2(0, 0);
-        if (wn < p.nitems) {
-            if (ncl.y > 0) {
-                const int hn = wn % H;
-                const size_t wna = (size_t)p.slot0 * H + wn;
-                umma::prefetch_l2(p.save_s + wna * TILE_S, TILE_S);
-                umma::prefetch_l2(p.save_ds + wna * TILE_S, TILE_S);
-                umma::prefetch_l2(p.save_u + wna * TILE_U, TILE_U);
-                umma::prefetch_l2(p.save_du + wna * TILE_U, TILE_U);
-                umma::prefetch_l2(p.aux + wna * AUX_FLOATS, 4 * AUX_FLOATS);
-                umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tv, 0, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tv, 64, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tdo, 0, hn, ncl.x);
-                umma::prefetch_tile_3d(&p.tdo, 64, hn, ncl.x);
-            }
-        }
     }
     // thread (channel ch = l, block cg): e^{g} of the block's tokens and their
     // (k, q) as a bf16 pair; x (running product from the block start,
@@ -615,6 +595,26 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
                       umma::sdesc4(sb4 + (((ks < 4 ? B_TB : B_TBL) + (ks & 3) * 2048) >> 4), 1024, 1024), id1,
                       ks > 0 ? 1u : 0u);
         umma::commit(bar + 8);
+        // the next item's tiles and rows into L2 while this one runs
+        ncl = (wn < p.nitems) ? p.list[p.slot0 + wn / H] : make_int2(0, 0);
+        if (wn < p.nitems) {
+            if (ncl.y > 0) {
+                const int hn = wn % H;
+                const size_t wna = (size_t)p.slot0 * H + wn;
+                umma::prefetch_l2(p.save_s + wna * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_ds + wna * TILE_S, TILE_S);
+                umma::prefetch_l2(p.save_u + wna * TILE_U, TILE_U);
+                umma::prefetch_l2(p.save_du + wna * TILE_U, TILE_U);
+                umma::prefetch_l2(p.aux + wna * AUX_FLOATS, 4 * AUX_FLOATS);
+                umma::prefetch_tile_3d(&p.tk, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tq, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tg, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tv, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tv, 64, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tdo, 0, hn, ncl.x);
+                umma::prefetch_tile_3d(&p.tdo, 64, hn, ncl.x);
+            }
+        }
     }
     pend |= umma::mbar_wait(bar + 8, par, WAIT_LIMIT) ? 0u : 2u;
     umma::fence_after();
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         const float gamC = dl[0] * dl[1] * dl[2] * dl[3];
         const float dgc = gamC * wscale * ((sDgc[ch] + sDgc[128 + ch]) + (sDgc[256 + ch] + sDgc[384 + ch]));
         float dgam[16];
-        float sh = 0.f;  // sum over this block of dK^ . K^
+        float2 sh2 = make_float2(0.f, 0.f);  // sum over this block of dK^ . K^ (even, odd tokens)
         // column factors of the segments i >= cg (see R_seg^T)
         float cs[4];
 #pragma unroll
@@ -913,37 +913,57 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (i >= cg) umma::hold(r9[i]);
+            // two tokens at a time as packed f32x2 operations (each lane rounds
+            // like the scalar operation)
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const int u = u0 + e2, t = t0 + e2;
-                xr *= e[u];  // x of token u
-                float kc = 0.f, rr = 0.f;  // sum_i f_i dR_i, and sum_i R_i dR_i with R_i as the product read it
+            for (int pr = 0; pr < 4; pr += 2) {
+                const int u = u0 + pr, t = t0 + pr;
+                const float x0 = xr * e[u], x1 = x0 * e[u + 1];  // x of the two tokens
+                xr = x1;
+                const float2 xx = make_float2(x0, x1), yy = make_float2(y[u], y[u + 1]);
+                const float2 kk = make_float2(kf(u), kf(u + 1)), qq = make_float2(qf(u), qf(u + 1));
+                float2 kc = make_float2(0.f, 0.f), rr = kc;  // sum_i f_i dR_i, sum_i R_i dR_i (R_i as the product read it)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i < cg) continue;
-                    const float f = y[u] * cs[i];
-                    const float r = __uint_as_float(r9[i][e2]);
-                    kc = fmaf(f, r, kc);
-                    rr = fmaf(bf16_round(kf(u) * f), r, rr);
+                    const float2 f = __fmul2_rn(yy, make_float2(cs[i], cs[i]));
+                    const float2 r = make_float2(__uint_as_float(r9[i][pr]), __uint_as_float(r9[i][pr + 1]));
+                    kc = __ffma2_rn(f, r, kc);
+                    const float2 kf2 = __fmul2_rn(kk, f);
+                    rr = __ffma2_rn(__bfloat1622float2(__floats2bfloat162_rn(kf2.x, kf2.y)), r, rr);
                 }
-                const float xx = xr, gam = pre * xx, suf = y[u] * post;
-                const float kk = kf(u), qq = qf(u);
-                const float v4 = __uint_as_float(a4[e2]), v5 = __uint_as_float(a5[e2]), v6 = __uint_as_float(a6[e2]);
-                const float v7 = __uint_as_float(a7[e2]), v8 = __uint_as_float(a8[e2]);
-                const float dqs = scale * v4;
-                const float dq = fmaf(dqs, gam, xx * v8);
-                const float kh = wscale * v6 * suf;
-                const float dk = fmaf(v5, gam, xx * v7) + kc + kh;
+                const float2 gam = __fmul2_rn(make_float2(pre, pre), xx), suf = __fmul2_rn(yy, make_float2(post, post));
+                const float2 v4 = make_float2(__uint_as_float(a4[pr]), __uint_as_float(a4[pr + 1]));
+                const float2 v5 = make_float2(__uint_as_float(a5[pr]), __uint_as_float(a5[pr + 1]));
+                const float2 v6 = make_float2(__uint_as_float(a6[pr]), __uint_as_float(a6[pr + 1]));
+                const float2 v7 = make_float2(__uint_as_float(a7[pr]), __uint_as_float(a7[pr + 1]));
+                const float2 v8 = make_float2(__uint_as_float(a8[pr]), __uint_as_float(a8[pr + 1]));
+                const float2 dqs = __fmul2_rn(make_float2(scale, scale), v4);
+                const float2 dq = __ffma2_rn(dqs, gam, __fmul2_rn(xx, v8));
+                const float2 kh = __fmul2_rn(__fmul2_rn(make_float2(wscale, wscale), v6), suf);
+                const float2 dk = __fadd2_rn(__fadd2_rn(__ffma2_rn(v5, gam, __fmul2_rn(xx, v7)), kc), kh);
                 // the anchored terms with the bf16 values of L and R_seg that the
                 // products used: each (row, column) pair inside [t, 63] then
                 // cancels in the reverse cumulative sum as it does exactly
-                dgam[u] = fmaf(dqs, qq * gam, v5 * (kk * gam)) - kh * kk +
-                          fmaf(bf16_round(kk * xx), v7, bf16_round(qq * xx) * v8) - rr;
-                sh = fmaf(kh, kk, sh);
+                const float2 lk = __fmul2_rn(kk, xx), lq = __fmul2_rn(qq, xx);
+                const float2 lkb = __bfloat1622float2(__floats2bfloat162_rn(lk.x, lk.y));
+                const float2 lqb = __bfloat1622float2(__floats2bfloat162_rn(lq.x, lq.y));
+                float2 dg = __ffma2_rn(dqs, __fmul2_rn(qq, gam), __fmul2_rn(v5, __fmul2_rn(kk, gam)));
+                dg = __ffma2_rn(make_float2(-kh.x, -kh.y), kk, dg);
+                dg = __fadd2_rn(dg, __ffma2_rn(lkb, v7, __fmul2_rn(lqb, v8)));
+                dg = __fadd2_rn(dg, make_float2(-rr.x, -rr.y));
+                dgam[u] = dg.x;
+                dgam[u + 1] = dg.y;
+                sh2 = __ffma2_rn(kh, kk, sh2);
                 if (t < Lc) {
                     const size_t o = ((size_t)(tc + t) * H + h) * D + ch;
-                    p.dq[o] = dq;
-                    p.dk[o] = dk;
+                    p.dq[o] = dq.x;
+                    p.dk[o] = dk.x;
+                }
+                if (t + 1 < Lc) {
+                    const size_t o = ((size_t)(tc + t + 1) * H + h) * D + ch;
+                    p.dq[o] = dq.y;
+                    p.dk[o] = dk.y;
                 }
             }
         }
@@ -951,7 +971,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 16; ++u) tot += dgam[u];
         sCum[cg * 128 + ch] = tot;
-        sCum[(4 + cg) * 128 + ch] = sh;
+        sCum[(4 + cg) * 128 + ch] = sh2.x + sh2.y;
         __syncthreads();
         // gamma_C (and the K^ factors through it) collects at the chunk's last
         // token, so it adds to the reverse cumulative sum at every token
