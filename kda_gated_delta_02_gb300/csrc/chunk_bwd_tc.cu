@@ -356,20 +356,20 @@ constexpr int NB = 512;
 // product batches):
 constexpr uint32_t B_SB = 0;        // S^T bf16 [j][i] (K-major 128 x 128)
 constexpr uint32_t B_DS = 32768;    // dS'^T bf16 [j][i]
-constexpr uint32_t B_DO = 65536;    // [dO ; -dVres] K-major 128 rows x 128 (rows 0-63 by TMA)
+constexpr uint32_t B_DO = 65536;    // dO K-major 64 rows x 128 (rows 0-63 of each 16 KB K block, by TMA)
 constexpr uint32_t B_VR = 98304;    // Vres^T bf16 [j][s]
 constexpr uint32_t B_UB = 114688;   // U^T bf16 [j][t]   (B_VR + 16 KB: second M block of [Vres; U])
 constexpr uint32_t B_DU = 131072;   // dU'^T bf16 [j][t]
-constexpr uint32_t B_DOT = 147456;  // dO^T bf16 [j][t]  (B_DU + 16 KB: second N block of [dU'; dO])
-constexpr uint32_t B_TBL = 147456;  //   before that: the low bf16 part of T diag(b)
-constexpr uint32_t B_KT = 163840;   // K~, MN-major (n = t, k = i)
+constexpr uint32_t B_TBL = 147456;  // the low bf16 part of T diag(b)
+constexpr uint32_t B_KT = 163840;   // K~, MN-major (n = t, k = i); then -dVres^T bf16 [j][s]
+constexpr uint32_t B_NDV = B_KT;
 constexpr uint32_t B_TB = 180224;   // T diag(b), MN-major (n = s, k = t)
 constexpr uint32_t B_TF = 188416;   // T f32 [64][64]
 constexpr uint32_t B_MT = 204800;   // M^T f32 [64][64]
 // the item's rows, staged by TMA where tiles arrive later or are built later:
 // k and q [64 t][128] bf16 over U^T and Vres^T, g [64 t][128] f32 over dS'^T
 // (those two tiles are copied once the rows are read), v in the rows 64-127
-// of the [dO; -dVres] tile (its two 8 KB value halves) until -dVres goes there
+// of the dO tile's K blocks (two 8 KB value halves)
 constexpr uint32_t B_KST = B_UB, B_QST = B_VR, B_GST = B_DS;
 // phases C and D, over the phase A / B regions once the second batch is done:
 constexpr uint32_t B_AP = 0;        // A' K-major 128 rows x 192 (three K blocks of 16 KB)
@@ -384,8 +384,8 @@ constexpr uint32_t B_CUM = B_KT;    // the combine's block sums f32 [8][128] (K~
 constexpr uint32_t B_MISC = 221184;
 constexpr uint32_t B_BETA = B_MISC;           // f32 [64]
 constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
-constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [4][128] quarters of rowsum(dS' . S)
-constexpr uint32_t B_DBP = B_DGC + 2048;      // f32 [8][64] beta gradient parts
+constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [8][128] parts of rowsum(dS' . S)
+constexpr uint32_t B_DBP = B_DGC + 4096;      // f32 [8][64] beta gradient parts
 constexpr uint32_t B_BAR = B_DBP + 2048;      // 7 mbarriers: loads, five product batches, late loads
 constexpr uint32_t B_TMEM = B_BAR + 56;
 constexpr uint32_t B_CLAIM = B_TMEM + 8;      // int [2]: item in hand, next item
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     }
     pend |= umma::mbar_wait(bar + 8, par, WAIT_LIMIT) ? 0u : 2u;
     umma::fence_after();
-    {  // thread (value column j = l, block cg)
+    {  // thread (value column j = l, block cg): Vres^T and -dVres^T rows j
         const int j = l;
         float a[16];
         umma::ld16(tq + T1 + c0, a);
@@ -631,70 +631,67 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         }
         sts_bf16x8(sb + B_VR + umma::kmaj(j, c0, 128), a, 0);
         sts_bf16x8(sb + B_VR + umma::kmaj(j, c0 + 8, 128), a, 8);
-        __syncthreads();  // v read: -dVres goes over it
         umma::ld16(tq + T2 + c0, a);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int s = c0 + u;
             const float dvr = a[u] * wscale;
             if (s < Lc) p.dv[((size_t)(tc + s) * H + h) * D + j] = dvr;
-            sts16(sb + B_DO + umma::kmaj(64 + s, j, 128), bf16_bits(-dvr));
+            a[u] = -dvr;
         }
-        // dO^T row j from column j of the dO tile
-#pragma unroll
-        for (int u = 0; u < 16; u += 8) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 8; e2 += 2) {
-                const uint32_t lo = lds16(sb + B_DO + umma::kmaj(c0 + u + e2, j, 128));
-                const uint32_t hi = lds16(sb + B_DO + umma::kmaj(c0 + u + e2 + 1, j, 128));
-                pk[e2 >> 1] = lo | (hi << 16);
-            }
-            sts128(sb + B_DOT + umma::kmaj(j, c0 + u, 128), pk[0], pk[1], pk[2], pk[3]);
-        }
+        sts_bf16x8(sb + B_NDV + umma::kmaj(j, c0, 128), a, 0);
+        sts_bf16x8(sb + B_NDV + umma::kmaj(j, c0 + 8, 128), a, 8);
     }
     pend |= umma::mbar_wait(bar + 48, par, WAIT_LIMIT) ? 0u : 64u;
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
 
-    // ---------------------------------------------------------------- batch 2: Vres dU'^T, dO U^T, S [dO; -dVres]^T, dS' U^T
+    // ---------------------------------------------------------------- batch 2: Vres dU'^T, dO U^T, S dO^T, -S dVres^T, dS' U^T
     if (tid == 0) {
         umma::fence_after();
         constexpr uint32_t id3 = umma::idesc_bf16(128, 64, 1, 1, 0);
-        constexpr uint32_t id4 = umma::idesc_bf16(128, 128, 1, 0, 0);
+        constexpr uint32_t id3b = umma::idesc_bf16(128, 64, 0, 1, 0);
+        constexpr uint32_t id4a = umma::idesc_bf16(128, 64, 1, 0, 0);
         constexpr uint32_t id5 = umma::idesc_bf16(128, 64, 1, 1, 0);
         // lanes 0-63: (dU' Vres^T)^T, lane s (A = [Vres; U], rows 64-127 unused)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T3, umma::sdesc4(sb4 + ((B_VR + ks * 2048) >> 4), 16384, 1024),
                       umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 1024, 1024), id3, ks > 0 ? 1u : 0u);
-        // lanes 64-127: dO U^T, lane t (A = [dU'; dO], rows 0-63 unused)
+        // lanes 64-127: dO U^T, lane t: A = the K-major dO tile read from 64 rows
+        // before it, so its rows 0-63 land in lanes 64-127 (rows 0-63 unused)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            umma::mma(tmem + T3 + 64, umma::sdesc4(sb4 + ((B_DU + ks * 2048) >> 4), 16384, 1024),
-                      umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id3, ks > 0 ? 1u : 0u);
+            umma::mma(tmem + T3 + 64, umma::sdesc4(sb4 + ((B_DO - 8192 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id3b, ks > 0 ? 1u : 0u);
+        // S dO^T (columns 0-63) and -S dVres^T (columns 64-127)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T4, umma::sdesc4(sb4 + ((B_SB + ks * 2048) >> 4), 16384, 1024),
-                      umma::sdesc4(sb4 + ((B_DO + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4), 16, 1024), id4,
+                      umma::sdesc4(sb4 + ((B_DO + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4), 16, 1024), id4a,
                       ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T4 + 64, umma::sdesc4(sb4 + ((B_SB + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_NDV + ks * 2048) >> 4), 1024, 1024), id5, ks > 0 ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T5, umma::sdesc4(sb4 + ((B_DS + ks * 2048) >> 4), 16384, 1024),
                       umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id5, ks > 0 ? 1u : 0u);
         umma::commit(bar + 16);
     }
-    {  // rowsum(dS' . S) for key channel ch over value columns 32 cg .. 32 cg + 31
-        float acc = 0.f;
+    {  // rowsum(dS' . S): key channels 2 cp, 2 cp + 1 over value columns 16 jg .. 16 jg + 15
+        const int cp = tid & 63, jg = tid >> 6;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll 8
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j = 32 * cg + jj;
-            const float a = __uint_as_float((uint32_t)lds16(sb + B_DS + umma::kmaj(j, ch, 128)) << 16);
-            const float b = __uint_as_float((uint32_t)lds16(sb + B_SB + umma::kmaj(j, ch, 128)) << 16);
-            acc = fmaf(a, b, acc);
+        for (int jj = 0; jj < 16; ++jj) {
+            const int j = 16 * jg + jj;
+            const float2 a = unpack_bf16(lds32(sb + B_DS + umma::kmaj(j, 2 * cp, 128)));
+            const float2 b = unpack_bf16(lds32(sb + B_SB + umma::kmaj(j, 2 * cp, 128)));
+            acc = __ffma2_rn(a, b, acc);
         }
-        sDgc[cg * 128 + ch] = acc;
+        *reinterpret_cast<float2 *>(sDgc + jg * 128 + 2 * cp) = acc;
     }
     pend |= umma::mbar_wait(bar + 16, par, WAIT_LIMIT) ? 0u : 4u;
     umma::fence_after();
@@ -872,7 +869,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     // ---------------------------------------------------------------- token gradients of channel ch, block cg
     {
         const float gamC = dl[0] * dl[1] * dl[2] * dl[3];
-        const float dgc = gamC * wscale * ((sDgc[ch] + sDgc[128 + ch]) + (sDgc[256 + ch] + sDgc[384 + ch]));
+        float dsum = 0.f;
+#pragma unroll
+        for (int jg = 0; jg < 8; ++jg) dsum += sDgc[jg * 128 + ch];
+        const float dgc = gamC * wscale * dsum;
         float dgam[16];
         float2 sh2 = make_float2(0.f, 0.f);  // sum over this block of dK^ . K^ (even, odd tokens)
         // column factors of the segments i >= cg (see R_seg^T)
