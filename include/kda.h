@@ -215,19 +215,39 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  * Backward of kda_chunk_fwd (training; "Noyaux KDA et FlashKDA", section
  * "FlashKDA : le noyau par blocs" names it as the chunk kernel's other use):
  * the gradients of a loss L with respect to every input, given dL/do and
- * dL/dS_final.  Reverse mode of the recurrence per token (S before, S' after,
- * D = Diag(e^{max(g, g_min)}), X = D S, p = X^T k, u = beta (v - p),
- * S' = X + k u^T, o = scale S'^T q; G = dL/dS'):
+ * dL/dS_final.  Two forms, chosen by shape and input type:
+ *
+ * bf16 inputs at d = 128: the chunk (WY) form on the tensor cores.  For a
+ * 64-token chunk entered with state S (gamma the running sum of the floored
+ * log-decays, K~ = K e^gamma, Q~ = Q e^gamma, K^ = K e^{gamma_63 - gamma},
+ * M = strict_lower(K~ (K e^-gamma)^T), T = (I + diag(b) M)^{-1}, TB = T diag(b),
+ * W = TB K~, B = lower(Q~ (K e^-gamma)^T)):
+ *     Vres = V - K~ S,  U = TB Vres,  O = scale (Q~ S + B U),  S_C = Diag(e^{gamma_63}) S + K^^T U.
+ * A forward pass (the two-kernel prefill's kernels, in pipelined pieces)
+ * keeps every chunk's operand blob, its fp32 T and M, and the bf16 state and
+ * U tiles; a reverse walk per (sequence, head) carries dS (arriving at each
+ * chunk end) backwards, dU = scale B^T dO + K^ dS_C and
+ * dS = scale Q~^T dO + Diag(e^{gamma_63}) dS_C - W^T dU, on the same blobs;
+ * then every chunk's token gradients are formed in parallel (the reverse of
+ * each forward step: dVres = TB^T dU = dv, dTB = dU Vres^T,
+ * dA = strict_lower(-T^T dTB diag(b) T^T), dB = scale lower(dO U^T), the causal
+ * tiles' gradients through the forward's 16-token block anchoring, and the
+ * reverse cumulative sum of the log-decay gradient).  Products take bf16
+ * operands with fp32 accumulation (T diag(b) keeps a second bf16 part);
+ * gradients are within 1e-2 of the fp64 reverse mode, normwise per head.
+ *
+ * d = 64, or fp32 inputs: the reverse mode of the token recurrence in fp32 on
+ * the CUDA cores (S before a token, S' after it, D = Diag(e^{max(g, g_min)}),
+ * X = D S, p = X^T k, u = beta (v - p), S' = X + k u^T, o = scale S'^T q;
+ * G = dL/dS'):
  *     G += scale q do^T;  dq = scale S' do;  du = G^T k;  dv = beta du;
  *     dbeta = du . (v - p);  dk = G u - beta X du;  dX = G - beta k du^T;
- *     dg_i = sum_j dX_ij X_ij, 0 where g_i < g_min;  G <- D dX;  dS0 = G at the start.
- * Computed in fp32 on the CUDA cores; each (sequence, head) is walked by a
- * cluster of d/32 CTAs, one per 32 value columns of the state (the columns
- * evolve independently), whose per-column partial sums of dq, dk, dg and
- * dbeta are added in a fixed order (results do not depend on scheduling;
- * when no such cluster fits the device, one CTA per (sequence, head) gives
- * the same bits).  States are recomputed from chunk-start checkpoints (64
- * tokens) kept in the workspace.
+ *     dg_i = sum_j dX_ij X_ij, 0 where g_i < g_min;  G <- D dX;  dS0 = G at the start,
+ * each (sequence, head) walked by a cluster of d/32 CTAs, one per 32 value
+ * columns of the state, whose per-column partial sums are added in a fixed
+ * order; states are recomputed from chunk-start checkpoints.
+ *
+ * Both forms are deterministic (the same inputs give the same bits).
  *  q, k, v, g, beta, cu_seqlens, N, T, H, initial_state, scale, g_min,
  *  in_dtype   as kda_chunk_fwd (dk = dv = 64 or 128; cp off).
  *  dout       device [T][H][dv], in_dtype: dL/do.
@@ -235,14 +255,18 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *  dq, dk, dv device f32 [T][H][d]; dg device f32 [T][H][dk] (w.r.t. the raw
  *             g); dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
  *  workspace  device scratch of at least kda_chunk_bwd_workspace_size(...)
- *             bytes: (floor(T/64) + N) x H chunk checkpoints and
- *             min(N x H, 160) x 64 states, d x d f32 each (at most 160
- *             (sequence, head) units are in flight, one scratch slot each),
- *             then min(N x H, 160) x d/32 x 2 buffers of 64 x (3d + 1) f32
- *             column partials, then T x H x d f32 (w = v - p of every token,
- *             kept by the forward pass for the recompute), each part
- *             256-byte aligned;
- *             KDA_ERR_WORKSPACE when smaller.
+ *             bytes, 256-byte aligned parts.  Tensor-core form, with
+ *             S = floor(T/64) + N chunk slots: the slot list (S x 8 B),
+ *             item counters (256 B), two carry states per head
+ *             (2 x H x 128 x 128 f32), then per (slot, head) the operand
+ *             blob (66,048 B), T and M^T (f32, 32 KB), the bf16 tiles of
+ *             the state and U (32 + 16 KB) and of the state gradient and dU
+ *             (32 + 16 KB).  CUDA-core form: S x H chunk checkpoints and
+ *             min(N x H, 160) x 64 states, d x d f32 each, then
+ *             min(N x H, 160) x d/32 x 2 buffers of 64 x (3d + 1) f32 column
+ *             partials, then T x H x d f32 (w = v - p of every token).  The
+ *             size is the larger of the two at d = 128 (independent of
+ *             in_dtype); KDA_ERR_WORKSPACE when smaller.
  * Invalid cu_seqlens set KDA_STATUS_BAD_SEQLENS; that sequence is skipped.
  */
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
