@@ -55,6 +55,16 @@ namespace bt {
 constexpr int D = 128;
 constexpr int CH = 64;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
+// The bound of the first wait of each kernel (the reverse walk's on its first
+// chunk's copies, the chunk kernel's on its first item's copies).  A test
+// build (KDA_TEST_SHORT_FIRST_WAIT) gives up on it at once, to exercise the
+// timeout path: status reported, the copies still in flight drained (full
+// bound), memory released.  The library itself uses the full bound.
+#ifdef KDA_TEST_SHORT_FIRST_WAIT
+constexpr uint32_t FIRST_WAIT_LIMIT = 0;
+#else
+constexpr uint32_t FIRST_WAIT_LIMIT = WAIT_LIMIT;
+#endif
 constexpr uint32_t TILE_S = 32768;  // bf16 S^T / dS'^T tile (K-major 128 x 128)
 constexpr uint32_t TILE_U = 16384;  // bf16 U^T / dU'^T tile (K-major 128 x 64)
 constexpr uint32_t AUX_FLOATS = 8192;
@@ -186,7 +196,7 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pm = (uint32_t)it & 1u;
         const int tc = t0 + CH * j, Lc = min(CH, t1 - tc);
         const uint32_t bb = R_BUF + (uint32_t)b * R_BUFSTRIDE;
-        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, WAIT_LIMIT);
+        const bool landed = umma::mbar_wait(bar0 + 8 * b, ph, j == je - 1 ? FIRST_WAIT_LIMIT : WAIT_LIMIT);
         timed_out |= !landed;
         pend_b = landed ? -1 : b;
         pend_ph = ph;
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     float e[16];
     uint32_t kq[16];
     uint32_t below = 0;  // bit u: g < g_min (no gradient)
-    pend |= umma::mbar_wait(bar, par, WAIT_LIMIT) ? 0u : 1u;
+    pend |= umma::mbar_wait(bar, par, it == 0 ? FIRST_WAIT_LIMIT : WAIT_LIMIT) ? 0u : 1u;
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
         const int t = c0 + u;

@@ -6,9 +6,10 @@ then sets KDA_STATUS_TIMEOUT in the caller's status word, waits (bounded) for
 every copy and product it issued, frees its tensor memory and returns, so the
 context stays usable.  A test build of the library (libkda_shortwait.so,
 compiled with KDA_TEST_SHORT_FIRST_WAIT) gives up on one wait at once: the
-state walk's wait for its first chunk's operand copy (a copy in flight) and
-the verify kernel's wait for its first batch of products (products in
-flight).  These tests call that build through the C ABI, check the status
+state walk's wait for its first chunk's operand copy (a copy in flight), the
+verify kernel's wait for its first batch of products (products in flight),
+and in the backward the reverse walk's wait for its first chunk's copies and
+the chunk-gradient kernel's wait for its first item's copies.  These tests call that build through the C ABI, check the status
 word, synchronise (no fault), and then check that the library's ordinary calls
 on the same inputs still match the oracle.
 """
@@ -34,7 +35,7 @@ def libs():
     path = build.build_variant("shortwait", ["KDA_TEST_SHORT_FIRST_WAIT"])
     test_lib = ctypes.CDLL(path)
     main = kda.load_library()
-    for name in ("kda_chunk_fwd", "kda_decode_verify_replay"):
+    for name in ("kda_chunk_fwd", "kda_decode_verify_replay", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size"):
         getattr(test_lib, name).restype = getattr(main, name).restype
         getattr(test_lib, name).argtypes = getattr(main, name).argtypes
     return kda, test_lib
@@ -104,3 +105,40 @@ def test_verify_product_timeout_drains_and_reports(libs, oracle):
     assert normwise_err(to64(o2), o_r, head_axis=2) <= OUT_TOL
     assert normwise_err(to64(st2), st_r, head_axis=1) <= STATE_TOL
     assert torch.equal(tl2.cpu(), torch.from_numpy(tl_r).to(torch.bfloat16))
+
+
+def test_backward_copy_timeouts_drain_and_report(libs, oracle):
+    """The tensor-core backward (d = 128, bf16): the reverse walk and the chunk
+    kernel give up on their first copy; the call reports KDA_STATUS_TIMEOUT
+    and leaves nothing running; the ordinary library then matches the oracle."""
+    kda, test_lib = libs
+    gen = torch.Generator().manual_seed(13)
+    lens, H, d = [300, 150], 2, 128
+    T = sum(lens)
+    q = torch.nn.functional.normalize(torch.randn(T, H, d, generator=gen), dim=-1).bfloat16().cuda()
+    k = torch.nn.functional.normalize(torch.randn(T, H, d, generator=gen), dim=-1).bfloat16().cuda()
+    v = torch.randn(T, H, d, generator=gen).bfloat16().cuda()
+    g = torch.clamp_min(-torch.nn.functional.softplus(torch.randn(T, H, d, generator=gen)), -5.0).cuda()
+    beta = torch.sigmoid(torch.randn(T, H, generator=gen)).cuda()
+    do = torch.randn(T, H, d, generator=gen).bfloat16().cuda()
+    cu = torch.tensor([0, lens[0], T], dtype=torch.int32).cuda()
+    outs = [torch.zeros(T, H, d, device="cuda") for _ in range(4)] + [torch.zeros(T, H, device="cuda")]
+    dS0 = torch.zeros(2, H, d, d, device="cuda")
+    ws_bytes = int(test_lib.kda_chunk_bwd_workspace_size(2, T, H, d, d))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = test_lib.kda_chunk_bwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu), 2, T, H, d, d, None, _p(do), None,
+                                *[_p(o) for o in outs], _p(dS0), 1.0, -5.0, 0, _p(ws), ctypes.c_size_t(ws_bytes),
+                                _p(status), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()  # the kernels returned: nothing left running
+    assert int(status.item()) & STATUS_TIMEOUT
+    # the ordinary library on the same inputs
+    got = kda.chunk_bwd(q, k, v, g, beta, cu, do)
+    torch.cuda.synchronize()
+    ref = oracle.backward(to64(q), to64(k), to64(v), to64(g), to64(beta), cu.cpu().numpy(), to64(do))
+    for a, b in zip(got[:5], ref[:5]):
+        if b.ndim == 2:
+            assert np.max(np.abs(to64(a) - b)) <= 1e-2 * max(np.max(np.abs(b)), 1e-30)
+        else:
+            assert normwise_err(to64(a), b, head_axis=1) <= 1e-2
