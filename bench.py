@@ -508,6 +508,26 @@ def main(argv=None):
                           "tensor_tflops_issued": flops / (bms * 1e-3) / 1e12,
                           "tensor_frac": flops / (bms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
                           "workspace_bytes": int(bws.numel())})
+            # the training pair: the forward keeps its operands, the backward
+            # is the reverse pass alone (a training step runs each once)
+            def fwd_train():
+                kda.chunk_fwd_train(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"],
+                                    saved=bws)
+
+            def bwd_saved():
+                kda.chunk_bwd_saved(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], dout,
+                                    bws)
+
+            fwd_train()
+            bwd_saved()
+            fms = reduce_max(cuda_time(fwd_train, Kb, stream), ws)
+            sms = reduce_max(cuda_time(bwd_saved, Kb, stream), ws)
+            entry["training_pair"] = {
+                "fwd_train_ms": fms, "fwd_train_vs_forward": fms / ms,
+                "bwd_saved_ms": sms, "bwd_saved_vs_forward": sms / ms,
+                "step_ms": fms + sms,
+                "note": "kda_chunk_fwd_train (prefill outputs + the operands the backward needs) then "
+                        "kda_chunk_bwd_saved (reverse pass only); same results as kda_chunk_fwd / kda_chunk_bwd"}
         else:
             entry["form"] = "token-level reverse mode on the CUDA cores"
         out["backward"] = entry

@@ -278,6 +278,41 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
 size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv);
 
 /*
+ * The training pair of the tensor-core form (dk = dv = 128, bf16 inputs;
+ * KDA_ERR_UNSUPPORTED_SHAPE otherwise): the forward pass that kda_chunk_bwd
+ * runs first, returning the prefill's outputs as well, then the reverse pass
+ * alone.  A training step calls kda_chunk_fwd_train once and
+ * kda_chunk_bwd_saved once instead of kda_chunk_fwd and kda_chunk_bwd (which
+ * runs the forward pass again).
+ *  kda_chunk_fwd_train: arguments and results as kda_chunk_fwd (cp off), and
+ *             saved: device buffer of at least
+ *             kda_chunk_bwd_workspace_size(N, T, H, 128, 128) bytes that
+ *             receives the slot list, every chunk's operand blob, T and M^T,
+ *             and the walk's state and U tiles (the tensor-core layout of
+ *             kda_chunk_bwd's workspace).  o and final_state are those of
+ *             kda_chunk_fwd bit for bit.
+ *  kda_chunk_bwd_saved: arguments as kda_chunk_bwd without initial_state
+ *             (the state tiles are saved), and saved as written by
+ *             kda_chunk_fwd_train with the same q, k, v, g, beta,
+ *             cu_seqlens, N, T, H, scale and g_min (the library does not
+ *             check that they are the same); it also holds the reverse
+ *             pass's own tiles, so it is written.  Results are those of
+ *             kda_chunk_bwd on the same inputs bit for bit.
+ * KDA_ERR_WORKSPACE when saved is smaller than the size.
+ */
+int kda_chunk_fwd_train(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const int32_t *cu_seqlens, int N, int T, int H, int dk,
+                        int dv, const float *initial_state, float *final_state, void *o,
+                        float scale, float g_min, int in_dtype, void *saved, size_t saved_bytes,
+                        uint32_t *status, void *stream);
+int kda_chunk_bwd_saved(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const int32_t *cu_seqlens, int N, int T, int H, int dk,
+                        int dv, const void *dout, const float *dS_final, float *dq, float *dk_,
+                        float *dv_, float *dg, float *dbeta, float *dS0, float scale, float g_min,
+                        int in_dtype, void *saved, size_t saved_bytes, uint32_t *status,
+                        void *stream);
+
+/*
  * Segment transitions of one sequence ("Noyaux KDA et FlashKDA", section "Le
  * parallelisme de contexte intra-appareil": the transition of each segment is
  * evaluated independently of the incoming state).  Exported for tests and

@@ -598,6 +598,125 @@ BwdTcLayout bwd_tc_layout(int N, int T, int H) {
 }
 }  // namespace
 
+namespace {
+kda::ChunkArgs bwd_tc_fwd_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, int T, int H, const float *S0, float *S_final, void *o,
+                               float scale, float g_min, uint32_t *status) {
+    kda::ChunkArgs fa = {};
+    fa.q = q; fa.k = k; fa.v = v; fa.g = g; fa.beta = beta; fa.o = o;
+    fa.T = T; fa.H = H; fa.dk = 128; fa.dv = 128; fa.scale = scale; fa.g_min = g_min;
+    fa.mode = kda::MODE_SEQ; fa.cu_seqlens = cu_seqlens; fa.S_init = S0; fa.S_final = S_final; fa.status = status;
+    return fa;
+}
+
+kda::BwdTcArgs bwd_tc_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int N, int T, int H, const void *dout, const float *dS_final,
+                           float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0, float scale,
+                           float g_min, unsigned char *ws, uint32_t *status) {
+    const BwdTcLayout L = bwd_tc_layout(N, T, H);
+    kda::BwdTcArgs b = {};
+    b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.cu_seqlens = cu_seqlens;
+    b.N = N; b.T = T; b.H = H; b.scale = scale; b.g_min = g_min; b.dS_final = dS_final;
+    b.dq = dq; b.dk = dk; b.dv = dv; b.dg = dg; b.dbeta = dbeta; b.dS0 = dS0;
+    b.list = reinterpret_cast<const int2 *>(ws + L.off_list);
+    b.blob = ws + L.off_blob;
+    b.aux = reinterpret_cast<const float *>(ws + L.off_aux);
+    b.save_s = ws + L.off_s; b.save_u = ws + L.off_u; b.save_ds = ws + L.off_ds; b.save_du = ws + L.off_du;
+    b.status = status;
+    return b;
+}
+
+int bwd_tc_pieces(int N, int T, int H) { return pipe_wanted(N, T, H, false) ? kPipePieces : 1; }
+
+// The forward pass of the tensor-core backward, in the prefill's pieces: the
+// chunk-local launch of piece p + 1 a programmatic dependent of the walk of
+// piece p (it reads nothing the walk writes, and every piece keeps its own
+// blobs, T and M for the reverse walk and the chunk kernel); the walks keep
+// their state and U tiles, and write o and S_final when fa has them.
+cudaError_t bwd_tc_forward(const kda::ChunkArgs &fa, int N, int T, int H, unsigned char *ws, cudaStream_t st) {
+    const BwdTcLayout L = bwd_tc_layout(N, T, H);
+    const int nslots = (int)L.nslots, P = bwd_tc_pieces(N, T, H), piece = (nslots + P - 1) / P;
+    int2 *list = reinterpret_cast<int2 *>(ws + L.off_list);
+    int *claim = reinterpret_cast<int *>(ws + L.off_claim);
+    unsigned char *blob = ws + L.off_blob;
+    float *aux = reinterpret_cast<float *>(ws + L.off_aux);
+    float *carry = reinterpret_cast<float *>(ws + L.off_carry);
+    cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)P * sizeof(int), st);
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(fa, N, nslots, list, st); });
+    for (int pc = 0; e == cudaSuccess && T > 0 && pc < P; ++pc) {
+        const int s0 = pc * piece, s1 = s0 + piece < nslots ? s0 + piece : nslots;
+        if (s0 >= s1) break;
+        unsigned char *pb = blob + (size_t)s0 * H * kda::kChunkBlobBytes;
+        e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
+            return kda::launch_chunk_prep(fa, list, s0, s1, pb, true, claim + pc, pc > 0, st, aux + (size_t)s0 * H * 8192);
+        });
+        if (e == cudaSuccess)
+            e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+                return kda::launch_chunk_walk(fa, N, pb, s0, s1, carry + (size_t)(pc & 1) * L.carry_stride,
+                                              carry + (size_t)((pc + 1) & 1) * L.carry_stride, st, ws + L.off_s,
+                                              ws + L.off_u);
+            });
+    }
+    if (e == cudaSuccess && T == 0 && fa.S_final && N > 0) {  // no chunk: the final states are the initial ones
+        const size_t bytes = (size_t)N * H * 128 * 128 * 4;
+        e = fa.S_init ? cudaMemcpyAsync(fa.S_final, fa.S_init, bytes, cudaMemcpyDeviceToDevice, st)
+                      : cudaMemsetAsync(fa.S_final, 0, bytes, st);
+    }
+    return e;
+}
+
+// The reverse pass over what bwd_tc_forward kept, in the same pieces, newest
+// first: the chunk gradients of piece p (which need its reverse walk
+// complete) run as a programmatic dependent of the reverse walk of the piece
+// before it in slot order, on the SMs that walk leaves free.
+cudaError_t bwd_tc_reverse(const kda::BwdTcArgs &b, int N, int T, int H, unsigned char *ws, cudaStream_t st) {
+    const BwdTcLayout L = bwd_tc_layout(N, T, H);
+    const int nslots = (int)L.nslots, P = bwd_tc_pieces(N, T, H), piece = (nslots + P - 1) / P;
+    int *claim = reinterpret_cast<int *>(ws + L.off_claim) + P;
+    float *carry = reinterpret_cast<float *>(ws + L.off_carry);
+    cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)P * sizeof(int), st);
+    auto rpiece = [&](int r, int &s0, int &s1) {  // r-th piece of the reverse pass
+        const int pc = P - 1 - r;
+        s0 = pc * piece;
+        s1 = s0 + piece < nslots ? s0 + piece : nslots;
+    };
+    for (int r = 0; e == cudaSuccess && r <= P; ++r) {
+        int s0 = 0, s1 = 0;
+        if (r < P) {
+            rpiece(r, s0, s1);
+            if (T == 0) {
+                s0 = 0;
+                s1 = nslots;
+            }
+            e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+                return kda::launch_bwd_walk(b, s0, s1, carry + (size_t)(r & 1) * L.carry_stride,
+                                            carry + (size_t)((r + 1) & 1) * L.carry_stride, st);
+            });
+            if (T == 0) break;
+        }
+        if (e == cudaSuccess && r > 0) {
+            int c0 = 0, c1 = 0;
+            rpiece(r - 1, c0, c1);
+            e = timed_launch(KDA_KERNEL_BWD_CHUNK, st,
+                             [&] { return kda::launch_bwd_chunk(b, c0, c1, claim + (r - 1), r < P, st); });
+        }
+    }
+    return e;
+}
+
+// Shape, pointer and workspace checks of the tensor-core training pair.
+int train_pair_check(int N, int T, int H, int dk, int dv, int in_dtype, const int32_t *cu_seqlens, void *saved,
+                     size_t saved_bytes) {
+    if (N < 1 || T < 0 || H < 1 || !cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (dk != 128 || dv != 128 || in_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if ((size_t)T * H * dk >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(saved)) return KDA_ERR_ALIGNMENT;
+    if (!saved || saved_bytes < bwd_tc_layout(N, T, H).total) return KDA_ERR_WORKSPACE;
+    return KDA_OK;
+}
+}  // namespace
+
 size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv) {
     if (N < 1 || T < 0 || H < 1 || dk != dv || !dim_ok(dk)) return 0;
     const size_t DD = (size_t)dk * dv * 4;
@@ -632,79 +751,13 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     if (dk == 128 && in_dtype == KDA_DTYPE_BF16) {
         // the chunk (WY) form on the tensor cores: forward pass keeping its
         // operands, reverse state walk, chunk gradients
-        const BwdTcLayout L = bwd_tc_layout(N, T, H);
-        const int nslots = (int)L.nslots;
-        int2 *list = reinterpret_cast<int2 *>(ws + L.off_list);
-        int *claim = reinterpret_cast<int *>(ws + L.off_claim);
-        unsigned char *blob = ws + L.off_blob;
-        float *aux = reinterpret_cast<float *>(ws + L.off_aux);
-        kda::ChunkArgs fa = {};
-        fa.q = q; fa.k = k; fa.v = v; fa.g = g; fa.beta = beta; fa.o = nullptr;
-        fa.T = T; fa.H = H; fa.dk = dk; fa.dv = dv; fa.scale = scale; fa.g_min = g_min;
-        fa.mode = kda::MODE_SEQ; fa.cu_seqlens = cu_seqlens; fa.S_init = initial_state; fa.status = status;
-        kda::BwdTcArgs b = {};
-        b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.cu_seqlens = cu_seqlens;
-        b.N = N; b.T = T; b.H = H; b.scale = scale; b.g_min = g_min; b.dS_final = dS_final;
-        b.dq = dq; b.dk = dk_; b.dv = dv_; b.dg = dg; b.dbeta = dbeta; b.dS0 = dS0;
-        b.list = list; b.blob = blob; b.aux = aux;
-        b.save_s = ws + L.off_s; b.save_u = ws + L.off_u; b.save_ds = ws + L.off_ds; b.save_du = ws + L.off_du;
-        b.status = status;
-        // the forward pass in pieces as the prefill runs them: the chunk-local
-        // launch of piece p + 1 a programmatic dependent of the walk of piece
-        // p (it reads nothing the walk writes, and every piece keeps its own
-        // blobs, T and M for the reverse walk and the chunk kernel)
-        const int P = pipe_wanted(N, T, H, false) ? kPipePieces : 1;
-        const int piece = (nslots + P - 1) / P;
-        float *carry = reinterpret_cast<float *>(ws + L.off_carry);
-        cudaError_t e = cudaMemsetAsync(claim, 0, (size_t)(2 * P) * sizeof(int), st);
+        kda::ChunkArgs fa = bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state, nullptr, nullptr, scale,
+                                            g_min, status);
+        cudaError_t e = bwd_tc_forward(fa, N, T, H, ws, st);
         if (e == cudaSuccess)
-            e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(fa, N, nslots, list, st); });
-        for (int pc = 0; e == cudaSuccess && T > 0 && pc < P; ++pc) {
-            const int s0 = pc * piece, s1 = s0 + piece < nslots ? s0 + piece : nslots;
-            if (s0 >= s1) break;
-            unsigned char *pb = blob + (size_t)s0 * H * kda::kChunkBlobBytes;
-            e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
-                return kda::launch_chunk_prep(fa, list, s0, s1, pb, true, claim + pc, pc > 0, st,
-                                              aux + (size_t)s0 * H * 8192);
-            });
-            if (e == cudaSuccess)
-                e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
-                    return kda::launch_chunk_walk(fa, N, pb, s0, s1, carry + (size_t)(pc & 1) * L.carry_stride,
-                                                  carry + (size_t)((pc + 1) & 1) * L.carry_stride, st, ws + L.off_s,
-                                                  ws + L.off_u);
-                });
-        }
-        // then the reverse pass in the same pieces, newest first: the chunk
-        // gradients of piece p (which need its reverse walk complete) run as a
-        // programmatic dependent of the reverse walk of the piece before it
-        // in slot order, on the SMs that walk leaves free
-        auto rpiece = [&](int r, int &s0, int &s1) {  // r-th piece of the reverse pass
-            const int pc = P - 1 - r;
-            s0 = pc * piece;
-            s1 = s0 + piece < nslots ? s0 + piece : nslots;
-        };
-        for (int r = 0; e == cudaSuccess && r <= P; ++r) {
-            int s0 = 0, s1 = 0;
-            if (r < P) {
-                rpiece(r, s0, s1);
-                if (T == 0) {
-                    s0 = 0;
-                    s1 = nslots;
-                }
-                e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
-                    return kda::launch_bwd_walk(b, s0, s1, carry + (size_t)(r & 1) * L.carry_stride,
-                                                carry + (size_t)((r + 1) & 1) * L.carry_stride, st);
-                });
-                if (T == 0) break;
-            }
-            if (e == cudaSuccess && r > 0) {
-                int c0 = 0, c1 = 0;
-                rpiece(r - 1, c0, c1);
-                e = timed_launch(KDA_KERNEL_BWD_CHUNK, st, [&] {
-                    return kda::launch_bwd_chunk(b, c0, c1, claim + P + (r - 1), r < P, st);
-                });
-            }
-        }
+            e = bwd_tc_reverse(bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_, dg,
+                                           dbeta, dS0, scale, g_min, ws, status),
+                               N, T, H, ws, st);
         return cuda_status(e);
     }
     kda::BwdArgs a = {};
@@ -722,6 +775,42 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
     a.N = N; a.T = T; a.H = H; a.scale = scale; a.g_min = g_min; a.status = status;
     return cuda_status(timed_launch(KDA_KERNEL_CHUNK_BWD, st,
                                     [&] { return kda::launch_chunk_bwd(a, dk, in_dtype == KDA_DTYPE_BF16, st); }));
+}
+
+int kda_chunk_fwd_train(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                        const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const float *initial_state,
+                        float *final_state, void *o, float scale, float g_min, int in_dtype, void *saved,
+                        size_t saved_bytes, uint32_t *status, void *stream) {
+    int rc = train_pair_check(N, T, H, dk, dv, in_dtype, cu_seqlens, saved, saved_bytes);
+    if (rc != KDA_OK) return rc;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
+        !aligned16(initial_state) || !aligned16(final_state))
+        return KDA_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(saved);
+    return cuda_status(bwd_tc_forward(bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state, final_state,
+                                                      o, scale, g_min, status),
+                                      N, T, H, ws, st));
+}
+
+int kda_chunk_bwd_saved(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                        const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const void *dout,
+                        const float *dS_final, float *dq, float *dk_, float *dv_, float *dg, float *dbeta,
+                        float *dS0, float scale, float g_min, int in_dtype, void *saved, size_t saved_bytes,
+                        uint32_t *status, void *stream) {
+    int rc = train_pair_check(N, T, H, dk, dv, in_dtype, cu_seqlens, saved, saved_bytes);
+    if (rc != KDA_OK) return rc;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dout) ||
+        !aligned16(dS_final) || !aligned16(dS0))
+        return KDA_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(saved);
+    return cuda_status(bwd_tc_reverse(bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_,
+                                                  dg, dbeta, dS0, scale, g_min, ws, status),
+                                      N, T, H, ws, st));
 }
 
 size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, int in_dtype, int pieces) {

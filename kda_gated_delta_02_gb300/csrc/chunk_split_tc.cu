@@ -946,8 +946,12 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
 
         // ------------------------------------------------------------ outputs
         // staged as a row-major [64][128] bf16 tile over U^T (read by the
-        // products that just completed), then written with 16-byte stores
-        // (no outputs in a pass that saves the tiles)
+        // products that just completed, and in a pass that saves the tiles by
+        // the copy of U^T, waited for here), then written with 16-byte stores
+        if (save && need_q) {
+            if (tid == 0) umma::bulk_wait_read();
+            __syncthreads();
+        }
         unsigned char *ostage = sm + W_UT;
         if (need_q) {  // staged whatever the wait returned; the barrier below decides
             float v[16];
@@ -1115,7 +1119,7 @@ cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char
                               unsigned char *save_u) {
     const int ntiles = (a.mode == MODE_TRANSITION) ? 2 : 1;
     if (units <= 0) return cudaSuccess;
-    if (save_s && (a.o || a.mode != MODE_SEQ)) return cudaErrorInvalidValue;  // the saving pass has no outputs
+    if (save_s && a.mode != MODE_SEQ) return cudaErrorInvalidValue;  // tiles are kept by sequence slots
     cudaError_t e = cudaFuncSetAttribute(sp::kda_chunk_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          sp::W_SMEM);
     if (e != cudaSuccess) return e;

@@ -67,9 +67,9 @@ cudaError_t launch_chunk_prep(const ChunkArgs &a, const int2 *list, int slot0, i
 // the chunks of every unit that fall in slots [slot0, slot1); a unit cut at
 // slot0 starts from carry_in, one cut at slot1 leaves its state in carry_out
 // ([tiles][H][128][128] fp32 each)
-// With save_s / save_u (a backward's forward pass, outputs o not needed: null)
-// the walk also stores, per (slot, head), its bf16 operand tiles S^T at the
-// chunk start (32 KB) and U^T (16 KB), indexed by absolute slot.
+// With save_s / save_u (the forward pass a backward uses; o may be null) the
+// walk also stores, per (slot, head), its bf16 operand tiles S^T at the chunk
+// start (32 KB) and U^T (16 KB), indexed by absolute slot (sequence mode).
 cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char *blob, int slot0, int slot1,
                               const float *carry_in, float *carry_out, cudaStream_t st,
                               unsigned char *save_s = nullptr, unsigned char *save_u = nullptr);

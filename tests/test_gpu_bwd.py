@@ -228,3 +228,36 @@ def test_floor_held_on_whole_chunks(kda, oracle):
     got = _compare(kda, oracle, x, scale=1.0, tol=TC_TOL)
     assert torch.all(got[3][128:192] == 0.0)
     assert torch.count_nonzero(got[3][0:64]) > 0
+
+
+def test_training_pair_equals_forward_and_backward(kda, oracle):
+    """chunk_fwd_train returns chunk_fwd's outputs bit for bit and keeps what
+    chunk_bwd_saved needs; chunk_bwd_saved returns chunk_bwd's gradients bit
+    for bit (same kernels on the same operands), in four pieces with a cut
+    sequence, an empty one, and dS_final."""
+    lens = [3000, 0, 1500, 2000]
+    x = _case(lens, 2, 128, torch.bfloat16, seed=47)
+    o_ref, S_ref = kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"],
+                                 scale=0.6)
+    o, Sf, saved = kda.chunk_fwd_train(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], initial_state=x["S0"],
+                                       scale=0.6)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(Sf, S_ref)
+    ref = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"],
+                        dS_final=x["dSf"], scale=0.6)
+    got = kda.chunk_bwd_saved(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], saved,
+                              dS_final=x["dSf"], scale=0.6)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    # and the pair's backward against the oracle
+    r = oracle.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
+                        x["cu"].cpu().numpy(), to64(x["do"]), S0=to64(x["S0"]), dS_final=to64(x["dSf"]), scale=0.6)
+    assert normwise_err(to64(got[0]), r[0], head_axis=1) <= TC_TOL
+    assert normwise_err(to64(got[3]), r[3], head_axis=1) <= TC_TOL
+
+
+def test_training_pair_rejects_other_shapes(kda):
+    x = _case([100], 1, 64, torch.bfloat16, seed=53)
+    with pytest.raises(kda.KDAError):
+        kda.chunk_fwd_train(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"])
