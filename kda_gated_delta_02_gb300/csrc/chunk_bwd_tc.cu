@@ -211,11 +211,6 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
             *reinterpret_cast<uint4 *>(sm + R_DO + b * 16384 + (c >> 3) * 8192 + umma::mnmaj(8 * (c & 7), r, 1)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
-        // the previous chunk's saved tiles have been read before they are overwritten
-        if (save && it > 0) {
-            if (tid == 0) umma::bulk_wait_read();
-            __syncthreads();
-        }
         // dS'^T (this thread's lane, columns 32 cg ..) as the bf16 operand, and
         // the resident gradient decayed in place, dS'^T diag(Gam_C), onto
         // which the dO^T Q~ and -dU'^T W products accumulate
@@ -318,11 +313,14 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
             for (int ks = 0; ks < 4; ++ks)
                 umma::mma(tmem + TM_S, umma::sdesc4(sb4 + ((R_UT + ks * 32) >> 4), 16, 1024),
                           umma::sdesc4(sb4 + ((bb + kBlobW + ks * 32) >> 4), 16, 1024), id_d, 1u);
-            umma::commit(bar_o);
             if (save) {
+                // the copies of this chunk's tiles have read them before the
+                // products complete, so the next chunk may overwrite them
                 umma::bulk_store(P.save_du + ((size_t)(sbase + j) * H + h) * TILE_U, sb + R_UT, TILE_U);
                 umma::bulk_commit();
+                umma::bulk_wait_read();
             }
+            umma::commit(bar_o);
         }
         if (!umma::mbar_wait(bar_o, pm, WAIT_LIMIT)) {
             timed_out = true;

@@ -799,12 +799,6 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                     make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        // the previous chunk's saved tiles have been read out of shared memory
-        // before they are overwritten
-        if (save && it > 0) {
-            if (tid == 0) umma::bulk_wait_read();
-            __syncthreads();
-        }
         // S^T (this thread's TMEM lane, columns 32 cg ..) as the bf16 operand of
         // the products, and the resident state decayed to the chunk end in place,
         // Diag-cols(e^{gamma_63}) S^T, onto which the U^T K~ product accumulates
@@ -914,11 +908,17 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
                     umma::mma(tmem + TM_O, a, umma::sdesc4(sb4 + ((bb + BL_BM + ks * 32) >> 4), 16, 1024), ido, 1u);
                 umma::mma(tmem + TM_ST, a, umma::sdesc4(sb4 + ((bb + BL_KT + ks * 4096) >> 4), 1024, 2048), ids, 1u);
             }
-            umma::commit(bar_o);
-            if (save && P.save_u) {
-                umma::bulk_store(P.save_u + ((size_t)(sbase + j) * H + h) * 16384u, sb + W_UT, 16384u);
-                umma::bulk_commit();
+            if (save) {
+                // the copies of this chunk's tiles have read them before the
+                // products complete (they run meanwhile), so whoever passes the
+                // barrier may overwrite S^T and U^T (next chunk, output stage)
+                if (P.save_u) {
+                    umma::bulk_store(P.save_u + ((size_t)(sbase + j) * H + h) * 16384u, sb + W_UT, 16384u);
+                    umma::bulk_commit();
+                }
+                umma::bulk_wait_read();
             }
+            umma::commit(bar_o);
         }
         if (!umma::mbar_wait(bar_o, pm, WAIT_LIMIT)) {
             timed_out = true;
@@ -947,11 +947,7 @@ __global__ void __launch_bounds__(NT2, 1) kda_chunk_walk_kernel(const __grid_con
         // ------------------------------------------------------------ outputs
         // staged as a row-major [64][128] bf16 tile over U^T (read by the
         // products that just completed, and in a pass that saves the tiles by
-        // the copy of U^T, waited for here), then written with 16-byte stores
-        if (save && need_q) {
-            if (tid == 0) umma::bulk_wait_read();
-            __syncthreads();
-        }
+        // its copy), then written with 16-byte stores
         unsigned char *ostage = sm + W_UT;
         if (need_q) {  // staged whatever the wait returned; the barrier below decides
             float v[16];
