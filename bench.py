@@ -640,7 +640,34 @@ def main(argv=None):
                      "ms_cp_off": cms_off, "speedup_vs_off": cms_off / cms,
                      "frac_hbm_min_bytes": (minimal / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"]}
         launches += sum(v["launches"] for v in kcp.values())
-        del ci, oc, wbuf
+        del oc, wbuf
+        torch.cuda.empty_cache()
+        if "backward" in only and cw.dk == 128 and ci["q"].dtype == torch.bfloat16:
+            # the backward of the same call over context-parallel segments
+            dco = torch.randn(ci["v"].shape, dtype=torch.float32, device="cuda").to(ci["v"].dtype)
+            lib = kda.load_library()
+            bneed = lib.kda_chunk_bwd_cp_workspace_size(1, Tc, Hc, cw.dk, cw.dv, kda.CP_AUTO, 0)
+            bwb = torch.empty(max(bneed, 1), dtype=torch.uint8, device="cuda")
+
+            def cpb_step(mode=kda.CP_AUTO):
+                kda.chunk_bwd_cp(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], ci["cu_seqlens"], dco,
+                                 cp_mode=mode, workspace=bwb, want_dS0=False)
+
+            cpb_step()
+            Kcb = max(3, K // 8)
+            cbms = reduce_max(cuda_time(cpb_step, Kcb, stream), ws)
+            _, kcb = timed_launches(kda, cpb_step, Kcb, stream)  # kernel table (launch events add gaps)
+            cbms_off = reduce_max(cuda_time(lambda: cpb_step(kda.CP_OFF), 1, stream), ws)
+            kcb_total = sum(v["ms"] for v in kcb.values())
+            out["cp"]["backward"] = {
+                "ms": cbms, "tok_s": ws * Tc / (cbms * 1e-3), "ratio_to_forward": cbms / cms,
+                "ms_cp_off": cbms_off, "speedup_vs_off": cbms_off / cbms, "workspace_bytes": int(bwb.numel()),
+                "segments": "automatic: about one (segment, head) unit per SM for the reverse walks",
+                "kernels": {name: {"launches_per_step": v["launches"] / Kcb,
+                                   "share_of_step": v["ms"] / max(kcb_total, 1e-9)} for name, v in kcb.items()}}
+            launches += sum(v["launches"] for v in kcb.values())
+            del dco, bwb
+        del ci
         torch.cuda.empty_cache()
 
     cpu = None

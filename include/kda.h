@@ -77,7 +77,8 @@ extern "C" {
 #define KDA_KERNEL_CHUNK_BWD 8       /* kda_chunk_bwd on the CUDA cores (d = 64 or f32 inputs) */
 #define KDA_KERNEL_BWD_WALK 9        /* kda_chunk_bwd, tensor cores: reverse state walk */
 #define KDA_KERNEL_BWD_CHUNK 10      /* kda_chunk_bwd, tensor cores: chunk gradients */
-#define KDA_KERNEL_KINDS 11
+#define KDA_KERNEL_BWD_COMPOSE 11    /* kda_chunk_bwd_cp: state gradient over the segments */
+#define KDA_KERNEL_KINDS 12
 
 /* Human-readable name of a return status. Never NULL. */
 const char *kda_status_string(int status);
@@ -276,6 +277,40 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *g, c
                   float g_min, int in_dtype, void *workspace, size_t workspace_bytes,
                   uint32_t *status, void *stream);
 size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv);
+
+/*
+ * kda_chunk_bwd with the prefill's context-parallel schedule for long
+ * sequences ("Noyaux KDA et FlashKDA", section "Le parallelisme de contexte
+ * intra-appareil", in reverse): cp_mode and segment_len as kda_chunk_fwd.
+ * When the call is cut into segments (bf16, d = 128), the forward pass runs
+ * as the CP prefill does (every segment's transition S_end = M S_start + N,
+ * the ordered composition, the replay keeping its tiles); the state gradient
+ * is affine over a segment too, dS_start = M^T dS_end + r with r the
+ * gradient a segment reaches from zero at its end, so every segment's r is
+ * walked in parallel, a short scan composes them last to first per
+ * (sequence, head), and every segment is walked again from its exact end
+ * gradient; then the chunk gradients as in kda_chunk_bwd.  Otherwise (CP off
+ * or declined, other shapes) it is kda_chunk_bwd.  Results agree with
+ * kda_chunk_bwd within the tensor-core form's rounding (1e-2 of the fp64
+ * reverse mode).
+ *  cp_mode    KDA_CP_AUTO cuts the call when kda_chunk_fwd's automatic mode
+ *             would; segment_len 0 then picks segments of at least 1,024
+ *             tokens, about one (segment, head) unit per SM (the reverse
+ *             walks hold one block per SM).  KDA_CP_ON with segment_len 0
+ *             picks the same length.
+ *  workspace  at least kda_chunk_bwd_cp_workspace_size(...) bytes: the CP
+ *             prefill's area, the tensor-core layout over S = floor(T/64) +
+ *             P_max slots, and 2 x P_max x H x 128 x 128 f32 (r and the
+ *             segment-end gradients); KDA_ERR_WORKSPACE when smaller.
+ */
+int kda_chunk_bwd_cp(const void *q, const void *k, const void *v, const float *g,
+                     const float *beta, const int32_t *cu_seqlens, int N, int T, int H, int dk,
+                     int dv, const float *initial_state, const void *dout, const float *dS_final,
+                     float *dq, float *dk_, float *dv_, float *dg, float *dbeta, float *dS0,
+                     float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
+                     void *workspace, size_t workspace_bytes, uint32_t *status, void *stream);
+size_t kda_chunk_bwd_cp_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode,
+                                       int segment_len);
 
 /*
  * The training pair of the tensor-core form (dk = dv = 128, bf16 inputs;

@@ -78,6 +78,11 @@ def load_library():
         lib.kda_chunk_fwd_host_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.kda_chunk_bwd.restype = I
         lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, F, F, I, P, S, P, P]
+        lib.kda_chunk_bwd_cp.restype = I
+        lib.kda_chunk_bwd_cp.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, F, F, I, I, I, P, S,
+                                         P, P]
+        lib.kda_chunk_bwd_cp_workspace_size.restype = S
+        lib.kda_chunk_bwd_cp_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.kda_chunk_fwd_train.restype = I
         lib.kda_chunk_fwd_train.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, P, S, P, P]
         lib.kda_chunk_bwd_saved.restype = I
@@ -282,7 +287,7 @@ def segment_compose(M, Nm, S0=None, want_segment_states=True, stream=None):
 KERNEL_FAMILIES = ("kda_chunk_list_kernel", "kda_chunk_prep_kernel", "kda_chunk_walk_kernel",
                    "kda_chunk_tc_kernel", "kda_chunk_kernel", "kda_compose_kernel", "kda_segment_table_kernel",
                    "kda_decode_verify_replay", "kda_chunk_bwd_kernel", "kda_bwd_walk_kernel",
-                   "kda_bwd_chunk_kernel")
+                   "kda_bwd_chunk_kernel", "kda_bwd_compose_kernel")
 
 
 def chunk_fwd_host(q, k, v, g, beta, cu_seqlens, initial_state=None, output_final_state=True, scale=1.0,
@@ -341,6 +346,37 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=Non
                                ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(status),
                                _stream(stream))
         _check(rc, "kda_chunk_bwd")
+        return dq, dkk, dvv, dg, db, dS0
+
+
+def chunk_bwd_cp(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=None, scale=1.0, g_min=-5.0,
+                 cp_mode=None, segment_len=0, workspace=None, status=None, stream=None, want_dS0=True):
+    """chunk_bwd with the prefill's context-parallel schedule for long
+    sequences (cp_mode and segment_len as chunk_fwd; default: automatic)."""
+    T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
+    _expect(do, "do", q.dtype, (T, H, dv))
+    _expect(dS_final, "dS_final", torch.float32, (N, H, dk, dv))
+    cp = CP_AUTO if cp_mode is None else int(cp_mode)
+    with _on(stream):
+        lib = load_library()
+        dev = q.device
+        f32 = torch.float32
+        dq = torch.empty((T, H, dk), dtype=f32, device=dev)
+        dkk = torch.empty((T, H, dk), dtype=f32, device=dev)
+        dvv = torch.empty((T, H, dv), dtype=f32, device=dev)
+        dg = torch.empty((T, H, dk), dtype=f32, device=dev)
+        db = torch.empty((T, H), dtype=f32, device=dev)
+        dS0 = torch.empty((N, H, dk, dv), dtype=f32, device=dev) if want_dS0 else None
+        need = int(lib.kda_chunk_bwd_cp_workspace_size(N, T, H, dk, dv, cp, int(segment_len)))
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        rc = lib.kda_chunk_bwd_cp(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                                  _ptr(initial_state), _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv),
+                                  _ptr(dg), _ptr(db), _ptr(dS0), float(scale), float(g_min), _in_dtype(q), cp,
+                                  int(segment_len), _ptr(workspace),
+                                  ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(status),
+                                  _stream(stream))
+        _check(rc, "kda_chunk_bwd_cp")
         return dq, dkk, dvv, dg, db, dS0
 
 

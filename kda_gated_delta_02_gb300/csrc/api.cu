@@ -569,7 +569,7 @@ struct BwdTcLayout {
     size_t nslots, off_list, off_claim, off_carry, carry_stride, off_blob, off_aux, off_s, off_u, off_ds, off_du,
         total;
 };
-BwdTcLayout bwd_tc_layout(int N, int T, int H) {
+BwdTcLayout bwd_tc_layout(int N, int T, int H) {  // N units: sequences, or segments
     BwdTcLayout L;
     L.nslots = (size_t)T / kChunk + N;
     const size_t sh = L.nslots * H;
@@ -612,8 +612,9 @@ kda::ChunkArgs bwd_tc_fwd_args(const void *q, const void *k, const void *v, cons
 kda::BwdTcArgs bwd_tc_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
                            const int32_t *cu_seqlens, int N, int T, int H, const void *dout, const float *dS_final,
                            float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0, float scale,
-                           float g_min, unsigned char *ws, uint32_t *status) {
-    const BwdTcLayout L = bwd_tc_layout(N, T, H);
+                           float g_min, unsigned char *ws, uint32_t *status, int layout_units = -1) {
+    // the workspace is laid out for N sequences, or for layout_units segments
+    const BwdTcLayout L = bwd_tc_layout(layout_units < 0 ? N : layout_units, T, H);
     kda::BwdTcArgs b = {};
     b.q = q; b.k = k; b.v = v; b.dout = dout; b.g = g; b.beta = beta; b.cu_seqlens = cu_seqlens;
     b.N = N; b.T = T; b.H = H; b.scale = scale; b.g_min = g_min; b.dS_final = dS_final;
@@ -811,6 +812,151 @@ int kda_chunk_bwd_saved(const void *q, const void *k, const void *v, const float
     return cuda_status(bwd_tc_reverse(bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_,
                                                   dg, dbeta, dS0, scale, g_min, ws, status),
                                       N, T, H, ws, st));
+}
+
+namespace {
+// Workspace of the context-parallel backward: the forward's CP area (segment
+// table, transitions, segment states), the tensor-core layout over the
+// segments' slots, then r and dS_end per (segment, head).
+struct BwdCpLayout {
+    CpLayout cp;
+    size_t off_tc = 0, off_r = 0, off_end = 0, total = 0;
+};
+BwdCpLayout bwd_cp_layout(int N, int T, int H, int cp_mode, int segment_len) {
+    BwdCpLayout B;
+    if (segment_len <= 0 && N > 0 && H > 0) {
+        // the reverse walks hold one CTA per SM: about one wave of
+        // (segment, head) units, segments of at least 16 chunks
+        const long per_seq = sm_count() / ((long)N * H);
+        const long segs = per_seq < 1 ? 1 : per_seq;
+        const long per = (T / N + segs - 1) / segs;
+        long seg = ((per + kChunk - 1) / kChunk) * kChunk;
+        if (seg < 16 * kChunk) seg = 16 * kChunk;
+        segment_len = seg > (1L << 30) ? (1 << 30) : (int)seg;
+    }
+    B.cp = cp_layout(N, T, H, 128, 128, cp_mode, segment_len);
+    if (B.cp.seg_len == 0) return B;
+    size_t o = align256(B.cp.total);
+    B.off_tc = o;
+    o += align256(bwd_tc_layout(B.cp.P_max, T, H).total);
+    const size_t st = (size_t)B.cp.P_max * H * 128 * 128 * 4;
+    B.off_r = o;
+    o += align256(st);
+    B.off_end = o;
+    o += align256(st);
+    B.total = o;
+    return B;
+}
+}  // namespace
+
+size_t kda_chunk_bwd_cp_workspace_size(int N, int T, int H, int dk, int dv, int cp_mode, int segment_len) {
+    const size_t base = kda_chunk_bwd_workspace_size(N, T, H, dk, dv);
+    if (base == 0 || dk != 128 || cp_mode == KDA_CP_OFF) return base;
+    if (cp_mode != KDA_CP_ON && cp_mode != KDA_CP_AUTO) return 0;
+    const BwdCpLayout B = bwd_cp_layout(N, T, H, cp_mode, segment_len);
+    return B.total > base ? B.total : base;
+}
+
+int kda_chunk_bwd_cp(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                     const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const float *initial_state,
+                     const void *dout, const float *dS_final, float *dq, float *dk_, float *dv_, float *dg,
+                     float *dbeta, float *dS0, float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
+                     void *workspace, size_t workspace_bytes, uint32_t *status, void *stream) {
+    if (cp_mode != KDA_CP_OFF && cp_mode != KDA_CP_ON && cp_mode != KDA_CP_AUTO) return KDA_ERR_INVALID_ARG;
+    if (segment_len < 0 || segment_len % kChunk != 0) return KDA_ERR_INVALID_ARG;
+    const BwdCpLayout B = (dk == 128 && dv == 128 && in_dtype == KDA_DTYPE_BF16 && N >= 1 && H >= 1 && T > 0)
+                              ? bwd_cp_layout(N, T, H, cp_mode, segment_len)
+                              : BwdCpLayout();
+    if (B.cp.seg_len == 0)  // no segments for this call: the sequence form
+        return kda_chunk_bwd(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, dout, dS_final, dq, dk_,
+                             dv_, dg, dbeta, dS0, scale, g_min, in_dtype, workspace, workspace_bytes, status, stream);
+    if (!cu_seqlens || !q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dout) ||
+        !aligned16(initial_state) || !aligned16(dS_final) || !aligned16(dS0) || !aligned16(workspace))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)T * H * dk >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!workspace || workspace_bytes < B.total) return KDA_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const CpLayout &C = B.cp;
+    const int Pm = C.P_max;
+    int32_t *count = reinterpret_cast<int32_t *>(ws + C.off_count);
+    int32_t *table = reinterpret_cast<int32_t *>(ws + C.off_table);
+    int32_t *first = reinterpret_cast<int32_t *>(ws + C.off_first);
+    float *M = reinterpret_cast<float *>(ws + C.off_M);
+    float *Nm = reinterpret_cast<float *>(ws + C.off_N);
+    float *Sin = reinterpret_cast<float *>(ws + C.off_Sin);
+    unsigned char *tw = ws + B.off_tc;
+    const BwdTcLayout L = bwd_tc_layout(Pm, T, H);
+    const int nslots = (int)L.nslots;
+    int2 *list = reinterpret_cast<int2 *>(tw + L.off_list);
+    int *claim = reinterpret_cast<int *>(tw + L.off_claim);
+    unsigned char *blob = tw + L.off_blob;
+    float *aux = reinterpret_cast<float *>(tw + L.off_aux);
+    float *r = reinterpret_cast<float *>(ws + B.off_r);
+    float *dend = reinterpret_cast<float *>(ws + B.off_end);
+
+    // forward pass, as the CP prefill runs it: segment table, every chunk's
+    // blob (with T and M kept), transitions, the segment states, and the
+    // replay keeping its state and U tiles
+    kda::ChunkArgs a = bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state, nullptr, nullptr, scale,
+                                       g_min, status);
+    a.seg_len = C.seg_len;
+    a.seg_table = table;
+    a.seg_count = count;
+    cudaError_t e = timed_launch(KDA_KERNEL_SEGMENT_TABLE, st, [&] {
+        return kda::launch_segment_table(cu_seqlens, N, T, C.seg_len, Pm, table, first, count, status, st);
+    });
+    if (e == cudaSuccess) e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st);
+    kda::ChunkArgs ar = a;
+    ar.mode = kda::MODE_REPLAY;
+    ar.S_in = Sin;
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(ar, Pm, nslots, list, st); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
+            return kda::launch_chunk_prep(ar, list, 0, nslots, blob, true, claim, false, st, aux);
+        });
+    kda::ChunkArgs at = a;
+    at.mode = kda::MODE_TRANSITION;
+    at.M_out = M;
+    at.N_out = Nm;
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+            return kda::launch_chunk_walk(at, Pm, blob, 0, nslots, nullptr, nullptr, st);
+        });
+    kda::ComposeArgs c = {};
+    c.M = M; c.Nm = Nm; c.S0 = initial_state; c.S_in = Sin; c.S_final = nullptr;
+    c.first = first; c.P = 0; c.chains = N; c.H = H; c.dk = 128; c.dv = 128;
+    if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_SEGMENT_COMPOSE, st, [&] { return kda::launch_compose(c, st); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+            return kda::launch_chunk_walk(ar, Pm, blob, 0, nslots, nullptr, nullptr, st, tw + L.off_s, tw + L.off_u);
+        });
+    // reverse pass: every segment from zero (r_p), the scan of the state
+    // gradient over the segments last to first, every segment again from its
+    // exact end gradient keeping its tiles, then the chunk gradients
+    kda::BwdTcArgs b = bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_, dg, dbeta,
+                                   dS0, scale, g_min, tw, status, Pm);
+    kda::BwdSegments sg = {table, count, Pm, nullptr, r, false};
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+            return kda::launch_bwd_walk(b, 0, nslots, nullptr, nullptr, st, &sg);
+        });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_COMPOSE, st, [&] {
+            return kda::launch_bwd_compose(M, r, first, cu_seqlens, dS_final, dend, dS0, N, H, scale, st);
+        });
+    kda::BwdSegments sg2 = {table, count, Pm, dend, nullptr, true};
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+            return kda::launch_bwd_walk(b, 0, nslots, nullptr, nullptr, st, &sg2);
+        });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_CHUNK, st,
+                         [&] { return kda::launch_bwd_chunk(b, 0, nslots, claim + 1, false, st); });
+    return cuda_status(e);
 }
 
 size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, int in_dtype, int pieces) {

@@ -109,6 +109,14 @@ struct RwalkParams {
     int slot0, slot1;
     const float *carry_in;
     float *carry_out;
+    // context-parallel segments (seg_table non-null): unit = segment, its
+    // token range from the table ({sequence, t0, t1, last} per segment);
+    // the walk starts from dS_in[unit][h] (raw dS', [dk][dv]) or from zero
+    // when dS_in is null, and leaves the raw dS' at the segment start in
+    // r_out[unit][h] when r_out is non-null
+    const int32_t *seg_table, *seg_count;
+    const float *dS_in;
+    float *r_out;
     uint32_t *status;
 };
 
@@ -124,16 +132,32 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
     // dependent may start once every CTA of this walk is resident: it reads
     // only what earlier launches wrote
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    const int t0 = P.cu[n], t1 = P.cu[n + 1];
-    const size_t uoff = ((size_t)n * H + h) * D * D;
+    const bool segs = P.seg_table != nullptr;
+    int t0, t1;
+    if (segs) {
+        if (n >= *P.seg_count) return;
+        const int4 se = reinterpret_cast<const int4 *>(P.seg_table)[n];
+        t0 = se.y;
+        t1 = se.z;
+    } else {
+        t0 = P.cu[n];
+        t1 = P.cu[n + 1];
+    }
+    const size_t uoff = ((size_t)n * H + h) * D * D;  // [unit][h] (sequence or segment)
     if (t0 < 0 || t1 < t0 || t1 > P.T) {
         if (tid == 0 && h == 0 && P.slot1 == P.N + P.T / CH) report_status(P.status, KDA_STATUS_BAD_SEQLENS);
         return;
     }
     const int nch = (t1 - t0 + CH - 1) / CH, sbase = t0 / CH + n;
-    if (nch == 0) {  // an empty sequence passes its final-state gradient through (in the piece of its slot)
-        if (P.dS0 && sbase >= P.slot0 && sbase < P.slot1)
-            for (int e = tid; e < D * D; e += NR) P.dS0[uoff + e] = P.dS_final ? P.dS_final[uoff + e] : 0.f;
+    if (nch == 0) {  // an empty unit passes its gradient through (in the piece of its slot)
+        if (sbase >= P.slot0 && sbase < P.slot1) {
+            if (segs) {
+                if (P.r_out)
+                    for (int e = tid; e < D * D; e += NR) P.r_out[uoff + e] = P.dS_in ? P.dS_in[uoff + e] : 0.f;
+            } else if (P.dS0) {
+                for (int e = tid; e < D * D; e += NR) P.dS0[uoff + e] = P.dS_final ? P.dS_final[uoff + e] : 0.f;
+            }
+        }
         return;
     }
     const int jb = max(0, P.slot0 - sbase), je = min(nch, P.slot1 - sbase);
@@ -156,10 +180,10 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
 
     {  // dS'^T = dS_final^T / wscale (lane j, columns = key channel i), or the carried dS'^T
         float r[32];
-        if (cut_in) {
-            const float *src = P.carry_in + (size_t)h * D * D;
+        if (cut_in || segs) {  // raw dS' carried from a later piece, given for a segment, or zero
+            const float *src = cut_in ? P.carry_in + (size_t)h * D * D : (P.dS_in ? P.dS_in + uoff : nullptr);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = src[(size_t)(32 * cg + c) * D + jrow];
+            for (int c = 0; c < 32; ++c) r[c] = src ? src[(size_t)(32 * cg + c) * D + jrow] : 0.f;
         } else {
             const float *src = P.dS_final ? P.dS_final + uoff : nullptr;
 #pragma unroll
@@ -336,13 +360,13 @@ __global__ void __launch_bounds__(NR, 1) kda_bwd_walk_kernel(const __grid_consta
         // before the shared and tensor memory are released
         if (pend_b >= 0) umma::mbar_wait(bar0 + 8 * pend_b, pend_ph, WAIT_LIMIT);
         if (pend_m >= 0) umma::mbar_wait(pend_m ? bar_o : bar_u, pend_mph, WAIT_LIMIT);
-    } else if (cut_out) {
+    } else if (cut_out || (segs && P.r_out)) {  // raw dS' to the next piece, or the segment's
         float r[32];
         umma::ld32(tq + TM_S + 32 * cg, r);
-        float *dst = P.carry_out + (size_t)h * D * D;
+        float *dst = cut_out ? P.carry_out + (size_t)h * D * D : P.r_out + uoff;
 #pragma unroll
         for (int c = 0; c < 32; ++c) dst[(size_t)(32 * cg + c) * D + jrow] = r[c];
-    } else if (P.dS0) {
+    } else if (P.dS0 && !segs) {
         float r[32];
         umma::ld32(tq + TM_S + 32 * cg, r);
 #pragma unroll
@@ -1023,6 +1047,74 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+// ============================================================================ reverse composition
+// The state gradient over context-parallel segments: with the forward
+// transition of segment p, S_end = M_p S_start + N_p, and r_p the raw
+// gradient a segment's reverse walk reaches at its start from zero at its
+// end, dS'_start = M_p^T dS'_end + r_p (all linear in dS' = dS / scale).  One
+// CTA per (sequence, head, 16 value columns) runs a sequence's segments last
+// to first in fp32, leaving dS' at every segment's end (the start of each
+// segment's second reverse walk) and scale dS' at the sequence start (dS0).
+constexpr int NC = 256;
+struct BcomposeParams {
+    const float *M;        // [P][H][dk][dk] forward transitions
+    const float *r;        // [P][H][dk][dv] raw dS' at each segment start, from zero
+    const int32_t *first;  // [N + 1] first segment of each sequence
+    const int32_t *cu;     // [N + 1] sequence bounds (an empty sequence passes dS_final through)
+    const float *dS_final; // [N][H][dk][dv] or null (zero)
+    float *dS_end;         // [P][H][dk][dv] raw dS' at each segment end
+    float *dS0;            // [N][H][dk][dv] or null
+    int H;
+    float wscale;
+};
+
+__global__ void __launch_bounds__(NC) kda_bwd_compose_kernel(const __grid_constant__ BcomposeParams P) {
+    __shared__ float cur[D][17];  // raw dS' of this CTA's 16 value columns
+    const int n = blockIdx.x, h = blockIdx.y, c0 = 16 * blockIdx.z, tid = threadIdx.x;
+    const int H = P.H, pf = P.first[n], pl = P.first[n + 1];
+    const float inv = 1.0f / P.wscale;
+    if (P.cu[n] == P.cu[n + 1]) {
+        if (P.dS0)
+            for (int e = tid; e < D * 16; e += NC) {
+                const size_t o = (((size_t)n * H + h) * D + (e >> 4)) * D + c0 + (e & 15);
+                P.dS0[o] = P.dS_final ? P.dS_final[o] : 0.f;
+            }
+        return;
+    }
+    for (int e = tid; e < D * 16; e += NC) {
+        const int i = e >> 4, c = e & 15;
+        cur[i][c] = P.dS_final ? P.dS_final[(((size_t)n * H + h) * D + i) * D + c0 + c] * inv : 0.f;
+    }
+    __syncthreads();
+    // thread (key row i, 8 columns): out[i][c] = sum_k M_p[k][i] cur[k][c] + r_p[i][c]
+    const int i = tid & (D - 1), cq = 8 * (tid >> 7);
+    for (int pp = pl - 1; pp >= pf; --pp) {
+        const size_t so = ((size_t)pp * H + h) * D * D;
+        float acc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            P.dS_end[so + (size_t)i * D + c0 + cq + c] = cur[i][cq + c];
+            acc[c] = P.r[so + (size_t)i * D + c0 + cq + c];
+        }
+        const float *Mp = P.M + so;
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float m = Mp[(size_t)k * D + i];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = fmaf(m, cur[k][cq + c], acc[c]);
+        }
+        __syncthreads();  // every thread has read cur
+#pragma unroll
+        for (int c = 0; c < 8; ++c) cur[i][cq + c] = acc[c];
+        __syncthreads();
+    }
+    if (P.dS0) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            P.dS0[(((size_t)n * H + h) * D + i) * D + c0 + cq + c] = cur[i][cq + c] * P.wscale;
+    }
+}
+
 }  // namespace bt
 
 namespace {
@@ -1058,7 +1150,7 @@ bool encode_plain(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int 
 }  // namespace
 
 cudaError_t launch_bwd_walk(const BwdTcArgs &a, int slot0, int slot1, const float *carry_in, float *carry_out,
-                            cudaStream_t st) {
+                            cudaStream_t st, const BwdSegments *sg) {
     if (a.N <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(bt::kda_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bt::R_SMEM);
@@ -1082,7 +1174,35 @@ cudaError_t launch_bwd_walk(const BwdTcArgs &a, int slot0, int slot1, const floa
     P.carry_in = carry_in;
     P.carry_out = carry_out;
     P.status = a.status;
-    bt::kda_bwd_walk_kernel<<<dim3(a.N, a.H), bt::NR, bt::R_SMEM, st>>>(P);
+    int units = a.N;
+    if (sg) {  // segments: no pieces, no tiles in the first pass
+        P.seg_table = sg->table;
+        P.seg_count = sg->count;
+        P.dS_in = sg->dS_in;
+        P.r_out = sg->r_out;
+        P.dS0 = nullptr;
+        if (!sg->save) P.save_ds = P.save_du = nullptr;
+        units = sg->P_max;
+    }
+    bt::kda_bwd_walk_kernel<<<dim3(units, a.H), bt::NR, bt::R_SMEM, st>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_compose(const float *M, const float *r, const int32_t *first, const int32_t *cu,
+                               const float *dS_final, float *dS_end, float *dS0, int N, int H, float scale,
+                               cudaStream_t st) {
+    if (N <= 0) return cudaSuccess;
+    bt::BcomposeParams P;
+    P.M = M;
+    P.r = r;
+    P.first = first;
+    P.cu = cu;
+    P.dS_final = dS_final;
+    P.dS_end = dS_end;
+    P.dS0 = dS0;
+    P.H = H;
+    P.wscale = scale == 0.f ? 1.f : scale;
+    bt::kda_bwd_compose_kernel<<<dim3(N, H, bt::D / 16), bt::NC, 0, st>>>(P);
     return cudaGetLastError();
 }
 

@@ -702,7 +702,7 @@ __global__ void kda_segment_table_kernel(const int32_t *cu_seqlens, int N, int T
         for (int s = 0; s < ns; ++s) {
             if (P >= P_max) {
                 report_status(status, KDA_STATUS_SEGMENT_OVERFLOW);
-                seq_first[N] = P;
+                for (int m = n + 1; m <= N; ++m) seq_first[m] = P;  // later sequences: no segment
                 *seg_count = P;
                 return;
             }

@@ -1115,7 +1115,7 @@ cudaError_t launch_chunk_walk(const ChunkArgs &a, int units, const unsigned char
                               unsigned char *save_u) {
     const int ntiles = (a.mode == MODE_TRANSITION) ? 2 : 1;
     if (units <= 0) return cudaSuccess;
-    if (save_s && a.mode != MODE_SEQ) return cudaErrorInvalidValue;  // tiles are kept by sequence slots
+    if (save_s && a.mode == MODE_TRANSITION) return cudaErrorInvalidValue;  // tiles are kept by state slots
     cudaError_t e = cudaFuncSetAttribute(sp::kda_chunk_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          sp::W_SMEM);
     if (e != cudaSuccess) return e;

@@ -140,8 +140,26 @@ struct BwdTcArgs {
 // The reverse walk over the chunks in slots [slot0, slot1), newest first; a
 // sequence cut at slot1 starts from carry_in, one cut at slot0 leaves its
 // state gradient in carry_out ([H][128][128] f32 each).
+// Context-parallel segments for the reverse walk (one piece): the segment
+// table of the forward's schedule; the first pass starts every segment from
+// zero (dS_in null) and leaves r_out, the second starts from dS_in and keeps
+// the tiles (save).
+struct BwdSegments {
+    const int32_t *table, *count;
+    int P_max;
+    const float *dS_in;
+    float *r_out;
+    bool save;
+};
 cudaError_t launch_bwd_walk(const BwdTcArgs &a, int slot0, int slot1, const float *carry_in, float *carry_out,
-                            cudaStream_t st);
+                            cudaStream_t st, const BwdSegments *sg = nullptr);
+// dS' over a sequence's segments, last to first: dS'_start = M_p^T dS'_end + r_p
+// (M [P][H][dk][dk] the forward transitions, first [N+1] each sequence's
+// first segment); dS_end [P][H][dk][dv] raw dS' at each segment end, dS0 =
+// scale dS' at the sequence start (or null).
+cudaError_t launch_bwd_compose(const float *M, const float *r, const int32_t *first, const int32_t *cu,
+                               const float *dS_final, float *dS_end, float *dS0, int N, int H, float scale,
+                               cudaStream_t st);
 // The chunk gradients of slots [slot0, slot1); claim is a device int that is
 // zero when the launch starts.  With after_walk the launch is a programmatic
 // dependent of the reverse walk launched just before it on `st` (it may start

@@ -58,9 +58,13 @@ def _case(lens, H, d, dtype, seed, floor_frac=0.1):
     return dict(q=c(q), k=c(k), v=c(v), g=c(g), beta=c(beta), cu=c(cu), S0=c(S0), do=c(do), dSf=c(dSf))
 
 
-def _compare(kda, oracle, x, scale, tol, heads=None):
-    got = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"],
-                        dS_final=x["dSf"], scale=scale)
+def _compare(kda, oracle, x, scale, tol, heads=None, segment_len=None):
+    if segment_len is None:
+        got = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"],
+                            dS_final=x["dSf"], scale=scale)
+    else:
+        got = kda.chunk_bwd_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], initial_state=x["S0"],
+                               dS_final=x["dSf"], scale=scale, cp_mode=kda.CP_ON, segment_len=segment_len)
     torch.cuda.synchronize()
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
     ref = oracle.backward(to64(sel(x["q"])), to64(sel(x["k"])), to64(sel(x["v"])), to64(sel(x["g"])),
@@ -261,3 +265,62 @@ def test_training_pair_rejects_other_shapes(kda):
     x = _case([100], 1, 64, torch.bfloat16, seed=53)
     with pytest.raises(kda.KDAError):
         kda.chunk_fwd_train(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"])
+
+
+@pytest.mark.parametrize("lens,seg", [([5000], 1024), ([3000, 0, 1500, 2000], 1024), ([1100, 64, 1], 512),
+                                      ([700], 64)])
+def test_context_parallel_backward_matches_oracle(kda, oracle, lens, seg):
+    """The backward over context-parallel segments: the forward pass as the CP
+    prefill runs it (transitions, their ordered composition, the replay
+    keeping its tiles), every segment walked back from zero, the state
+    gradient scanned over the segments last to first, every segment walked
+    back again from its exact end gradient, then the chunk gradients.
+    Sequences span several segments, end mid-segment and mid-chunk, are
+    shorter than one segment or empty; segments of one chunk each."""
+    x = _case(lens, 2, 128, torch.bfloat16, seed=59 + seg)
+    kda.kernel_timing_start()
+    got = _compare(kda, oracle, x, scale=0.7, tol=TC_TOL, segment_len=seg)
+    kern = kda.kernel_timing_stop()
+    assert kern["kda_bwd_walk_kernel"]["launches"] == 2 and kern["kda_bwd_chunk_kernel"]["launches"] == 1
+    assert kern["kda_bwd_compose_kernel"]["launches"] == 1 and kern["kda_compose_kernel"]["launches"] == 1
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(got[5][n], x["dSf"][n])
+
+
+def test_context_parallel_backward_long_sampled_heads(kda, oracle):
+    """Two long sequences (24,576 and 8,000 tokens) over 16 heads cut into
+    2,048-token segments; heads 0 and 15 against the oracle."""
+    x = _case([24576, 8000], 16, 128, torch.bfloat16, seed=61, floor_frac=0.02)
+    _compare(kda, oracle, x, scale=128 ** -0.5, tol=TC_TOL, heads=[0, 15], segment_len=2048)
+
+
+def test_context_parallel_backward_arguments(kda):
+    """A segment length that is not a multiple of the chunk, an unknown mode
+    and a workspace below the size are refused; cp off (or no segment for the
+    call) is the sequence form bit for bit."""
+    x = _case([300, 200], 1, 128, torch.bfloat16, seed=67)
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"])
+    with pytest.raises(kda.KDAError):
+        kda.chunk_bwd_cp(*args, cp_mode=kda.CP_ON, segment_len=100)
+    with pytest.raises(kda.KDAError):
+        kda.chunk_bwd_cp(*args, cp_mode=7, segment_len=128)
+    lib = kda.load_library()
+    need = lib.kda_chunk_bwd_cp_workspace_size(2, 500, 1, 128, 128, kda.CP_ON, 128)
+    assert need >= lib.kda_chunk_bwd_workspace_size(2, 500, 1, 128, 128)
+    import ctypes
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    outs = [torch.empty(500, 1, 128, device="cuda") for _ in range(4)] + [torch.empty(500, 1, device="cuda")]
+    small = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    rc = lib.kda_chunk_bwd_cp(P(x["q"]), P(x["k"]), P(x["v"]), P(x["g"]), P(x["beta"]), P(x["cu"]), 2, 500, 1,
+                              128, 128, None, P(x["do"]), None, *[P(o) for o in outs], None, 1.0, -5.0, 0,
+                              kda.CP_ON, 128, P(small), ctypes.c_size_t(4096), None, None)
+    with pytest.raises(kda.KDAError):
+        kda._check(rc, "kda_chunk_bwd_cp")
+    ref = _grads(kda, x, 0.9)
+    for mode, seg in ((kda.CP_OFF, 0), (kda.CP_AUTO, 0)):
+        got = kda.chunk_bwd_cp(*args, initial_state=x["S0"], dS_final=x["dSf"], scale=0.9, cp_mode=mode,
+                               segment_len=seg)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
