@@ -112,7 +112,10 @@ int kda_version(void);
  *               exact initial states (4 launches).
  *               KDA_CP_AUTO: CP when (sequence, head) units are too few to
  *               fill the GPU and sequences are long.
- *  segment_len  CP segment length in tokens (multiple of 64), or 0 = automatic.
+ *  segment_len  CP segment length in tokens (multiple of 64), or 0 = automatic:
+ *               segments of at least 1,024 tokens, about one (segment, head)
+ *               unit per SM at dk = dv = 128 (the state walk holds one block
+ *               per SM), two per SM otherwise.
  *  workspace    device scratch of at least kda_chunk_fwd_workspace_size(...)
  *               bytes (may be NULL when that size is 0).  Contents on entry
  *               are ignored; on exit they are unspecified.  With bf16 inputs
@@ -294,10 +297,8 @@ size_t kda_chunk_bwd_workspace_size(int N, int T, int H, int dk, int dv);
  * kda_chunk_bwd within the tensor-core form's rounding (1e-2 of the fp64
  * reverse mode).
  *  cp_mode    KDA_CP_AUTO cuts the call when kda_chunk_fwd's automatic mode
- *             would; segment_len 0 then picks segments of at least 1,024
- *             tokens, about one (segment, head) unit per SM (the reverse
- *             walks hold one block per SM).  KDA_CP_ON with segment_len 0
- *             picks the same length.
+ *             would, and segment_len 0 picks kda_chunk_fwd's length (about
+ *             one (segment, head) unit per SM).
  *  workspace  at least kda_chunk_bwd_cp_workspace_size(...) bytes: the CP
  *             prefill's area, the tensor-core layout over S = floor(T/64) +
  *             P_max slots, and 2 x P_max x H x 128 x 128 f32 (r and the

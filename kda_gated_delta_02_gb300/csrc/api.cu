@@ -66,7 +66,10 @@ CpLayout cp_layout(int N, int T, int H, int dk, int dv, int cp_mode, int segment
     int seg = segment_len;
     if (seg <= 0) {
         const int sms = sm_count();
-        long target = (2L * sms + (long)N * H - 1) / ((long)N * H);  // segments per sequence
+        // segments per sequence: at d = 128 the walks hold one block per SM,
+        // so about one wave of (segment, head) units; else two per SM
+        long target = (dk == 128 && dv == 128) ? (long)sms / ((long)N * H)
+                                               : (2L * sms + (long)N * H - 1) / ((long)N * H);
         if (target < 1) target = 1;
         long per = (T / (N > 0 ? N : 1) + target - 1) / target;
         seg = (int)(((per + kChunk - 1) / kChunk) * kChunk);
@@ -824,16 +827,6 @@ struct BwdCpLayout {
 };
 BwdCpLayout bwd_cp_layout(int N, int T, int H, int cp_mode, int segment_len) {
     BwdCpLayout B;
-    if (segment_len <= 0 && N > 0 && H > 0) {
-        // the reverse walks hold one CTA per SM: about one wave of
-        // (segment, head) units, segments of at least 16 chunks
-        const long per_seq = sm_count() / ((long)N * H);
-        const long segs = per_seq < 1 ? 1 : per_seq;
-        const long per = (T / N + segs - 1) / segs;
-        long seg = ((per + kChunk - 1) / kChunk) * kChunk;
-        if (seg < 16 * kChunk) seg = 16 * kChunk;
-        segment_len = seg > (1L << 30) ? (1 << 30) : (int)seg;
-    }
     B.cp = cp_layout(N, T, H, 128, 128, cp_mode, segment_len);
     if (B.cp.seg_len == 0) return B;
     size_t o = align256(B.cp.total);
