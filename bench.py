@@ -636,9 +636,14 @@ def main(argv=None):
         cms = reduce_max(cms, ws)
         cms_off = reduce_max(cuda_time(lambda: cp_step(kda.CP_OFF), 1, stream), ws)
         minimal = Tc * Hc * BYTES_PER_TOKHEAD
+        # the CP schedule's own bytes: the minimum plus its transition pass's
+        # second read of k, v, g and beta (768 - 256 + 512 + 4 B per token-head)
+        cp_bytes = Tc * Hc * (BYTES_PER_TOKHEAD + 1028)
         out["cp"] = {"workload": cw.name, "segment_len": seg, "ms": cms, "tok_s": ws * Tc / (cms * 1e-3),
                      "ms_cp_off": cms_off, "speedup_vs_off": cms_off / cms,
-                     "frac_hbm_min_bytes": (minimal / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"]}
+                     "frac_hbm_min_bytes": (minimal / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+                     "frac_hbm_cp_bytes": (cp_bytes / (cms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+                     "cp_bytes_per_tokhead": BYTES_PER_TOKHEAD + 1028}
         launches += sum(v["launches"] for v in kcp.values())
         del oc, wbuf
         torch.cuda.empty_cache()
