@@ -671,6 +671,24 @@ def main(argv=None):
                 "kernels": {name: {"launches_per_step": v["launches"] / Kcb,
                                    "share_of_step": v["ms"] / max(kcb_total, 1e-9)} for name, v in kcb.items()}}
             launches += sum(v["launches"] for v in kcb.values())
+
+            def cp_fwd_train():
+                kda.chunk_fwd_train(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], ci["cu_seqlens"], saved=bwb,
+                                    cp_mode=kda.CP_AUTO)
+
+            def cp_bwd_saved():
+                kda.chunk_bwd_saved(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], ci["cu_seqlens"], dco, bwb,
+                                    cp_mode=kda.CP_AUTO, want_dS0=False)
+
+            cp_fwd_train()
+            cp_bwd_saved()
+            tfms = reduce_max(cuda_time(cp_fwd_train, Kcb, stream), ws)
+            tbms = reduce_max(cuda_time(cp_bwd_saved, Kcb, stream), ws)
+            out["cp"]["backward"]["training_pair"] = {
+                "fwd_train_ms": tfms, "fwd_train_vs_forward": tfms / cms,
+                "bwd_saved_ms": tbms, "bwd_saved_vs_forward": tbms / cms, "step_ms": tfms + tbms,
+                "note": "kda_chunk_fwd_train_cp then kda_chunk_bwd_saved_cp (reverse pass only); same results as "
+                        "kda_chunk_fwd / kda_chunk_bwd_cp"}
             del dco, bwb
         del ci
         torch.cuda.empty_cache()

@@ -349,6 +349,35 @@ int kda_chunk_bwd_saved(const void *q, const void *k, const void *v, const float
                         void *stream);
 
 /*
+ * The training pair with kda_chunk_bwd_cp's context-parallel schedule: the
+ * forward pass kda_chunk_bwd_cp runs first (segment table, operand blobs with
+ * T and M^T, transitions, their composition, the replay keeping its tiles),
+ * returning the prefill's outputs as well, then its reverse pass alone.
+ * Arguments as kda_chunk_fwd_train / kda_chunk_bwd_saved plus cp_mode and
+ * segment_len (as kda_chunk_bwd_cp; both calls must get the same values, and
+ * the same inputs, which the library does not check).
+ *  saved   device buffer of at least kda_chunk_bwd_cp_workspace_size(N, T,
+ *          H, 128, 128, cp_mode, segment_len) bytes; kda_chunk_fwd_train_cp
+ *          writes it, kda_chunk_bwd_saved_cp reads it and writes its own
+ *          parts (segment gradients, state-gradient tiles).
+ * When the call is not cut into segments they are kda_chunk_fwd_train and
+ * kda_chunk_bwd_saved.  Results are kda_chunk_fwd's (cp_mode, segment_len)
+ * outputs and kda_chunk_bwd_cp's gradients bit for bit (same kernels on the
+ * same operands).  KDA_ERR_WORKSPACE when saved is smaller than the size.
+ */
+int kda_chunk_fwd_train_cp(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const int32_t *cu_seqlens, int N, int T, int H,
+                           int dk, int dv, const float *initial_state, float *final_state, void *o,
+                           float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
+                           void *saved, size_t saved_bytes, uint32_t *status, void *stream);
+int kda_chunk_bwd_saved_cp(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const int32_t *cu_seqlens, int N, int T, int H,
+                           int dk, int dv, const void *dout, const float *dS_final, float *dq,
+                           float *dk_, float *dv_, float *dg, float *dbeta, float *dS0, float scale,
+                           float g_min, int in_dtype, int cp_mode, int segment_len, void *saved,
+                           size_t saved_bytes, uint32_t *status, void *stream);
+
+/*
  * Segment transitions of one sequence ("Noyaux KDA et FlashKDA", section "Le
  * parallelisme de contexte intra-appareil": the transition of each segment is
  * evaluated independently of the incoming state).  Exported for tests and

@@ -88,6 +88,11 @@ def load_library():
         lib.kda_chunk_bwd_saved.restype = I
         lib.kda_chunk_bwd_saved.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, F, F, I, P, S, P,
                                             P]
+        lib.kda_chunk_fwd_train_cp.restype = I
+        lib.kda_chunk_fwd_train_cp.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, F, F, I, I, I, P, S, P, P]
+        lib.kda_chunk_bwd_saved_cp.restype = I
+        lib.kda_chunk_bwd_saved_cp.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, F, F, I, I, I,
+                                               P, S, P, P]
         lib.kda_chunk_bwd_workspace_size.restype = S
         lib.kda_chunk_bwd_workspace_size.argtypes = [I, I, I, I, I]
         lib.kda_kernel_timing_start.restype = I
@@ -381,31 +386,41 @@ def chunk_bwd_cp(q, k, v, g, beta, cu_seqlens, do, initial_state=None, dS_final=
 
 
 def chunk_fwd_train(q, k, v, g, beta, cu_seqlens, initial_state=None, scale=1.0, g_min=-5.0, saved=None,
-                    status=None, stream=None):
+                    status=None, stream=None, cp_mode=None, segment_len=0):
     """The forward of the training pair (d = 128, bf16): returns (o,
     final_state, saved); `saved` (uint8, device) holds what chunk_bwd_saved
-    needs.  o and final_state equal chunk_fwd's bit for bit."""
+    needs.  o and final_state equal chunk_fwd's bit for bit.  With cp_mode
+    (and segment_len) given, the pair of chunk_bwd_cp's schedule: pass the
+    same values to chunk_bwd_saved."""
     T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, initial_state)
     with _on(stream):
         lib = load_library()
         o = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
         Sf = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-        need = int(lib.kda_chunk_bwd_workspace_size(N, T, H, dk, dv))
+        if cp_mode is None:
+            need = int(lib.kda_chunk_bwd_workspace_size(N, T, H, dk, dv))
+        else:
+            need = int(lib.kda_chunk_bwd_cp_workspace_size(N, T, H, dk, dv, int(cp_mode), int(segment_len)))
         if saved is None or saved.numel() * saved.element_size() < need:
             saved = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-        rc = lib.kda_chunk_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk,
-                                     dv, _ptr(initial_state), _ptr(Sf), _ptr(o), float(scale), float(g_min),
-                                     _in_dtype(q), _ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()),
-                                     _ptr(status), _stream(stream))
-        _check(rc, "kda_chunk_fwd_train")
+        head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
+                _ptr(initial_state), _ptr(Sf), _ptr(o), float(scale), float(g_min), _in_dtype(q))
+        tail = (_ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()), _ptr(status), _stream(stream))
+        if cp_mode is None:
+            rc = lib.kda_chunk_fwd_train(*head, *tail)
+            _check(rc, "kda_chunk_fwd_train")
+        else:
+            rc = lib.kda_chunk_fwd_train_cp(*head, int(cp_mode), int(segment_len), *tail)
+            _check(rc, "kda_chunk_fwd_train_cp")
         return o, Sf, saved
 
 
 def chunk_bwd_saved(q, k, v, g, beta, cu_seqlens, do, saved, dS_final=None, scale=1.0, g_min=-5.0, status=None,
-                    stream=None, want_dS0=True):
+                    stream=None, want_dS0=True, cp_mode=None, segment_len=0):
     """The backward of the training pair: the reverse pass over `saved` from
-    chunk_fwd_train (same inputs, scale and g_min).  Returns (dq, dk, dv, dg,
-    dbeta, dS0) as chunk_bwd does, bit for bit."""
+    chunk_fwd_train (same inputs, scale, g_min, cp_mode and segment_len).
+    Returns (dq, dk, dv, dg, dbeta, dS0) as chunk_bwd (chunk_bwd_cp with
+    cp_mode) does, bit for bit."""
     T, H, dk, dv, N = _check_prefill(q, k, v, g, beta, cu_seqlens, None)
     _expect(do, "do", q.dtype, (T, H, dv))
     _expect(dS_final, "dS_final", torch.float32, (N, H, dk, dv))
@@ -419,12 +434,16 @@ def chunk_bwd_saved(q, k, v, g, beta, cu_seqlens, do, saved, dS_final=None, scal
         dg = torch.empty((T, H, dk), dtype=f32, device=dev)
         db = torch.empty((T, H), dtype=f32, device=dev)
         dS0 = torch.empty((N, H, dk, dv), dtype=f32, device=dev) if want_dS0 else None
-        rc = lib.kda_chunk_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv,
-                                     _ptr(do), _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(db),
-                                     _ptr(dS0), float(scale), float(g_min), _in_dtype(q), _ptr(saved),
-                                     ctypes.c_size_t(saved.numel() * saved.element_size()), _ptr(status),
-                                     _stream(stream))
-        _check(rc, "kda_chunk_bwd_saved")
+        head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(do),
+                _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(db), _ptr(dS0), float(scale),
+                float(g_min), _in_dtype(q))
+        tail = (_ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()), _ptr(status), _stream(stream))
+        if cp_mode is None:
+            rc = lib.kda_chunk_bwd_saved(*head, *tail)
+            _check(rc, "kda_chunk_bwd_saved")
+        else:
+            rc = lib.kda_chunk_bwd_saved_cp(*head, int(cp_mode), int(segment_len), *tail)
+            _check(rc, "kda_chunk_bwd_saved_cp")
         return dq, dkk, dvv, dg, db, dS0
 
 

@@ -850,16 +850,138 @@ size_t kda_chunk_bwd_cp_workspace_size(int N, int T, int H, int dk, int dv, int 
     return B.total > base ? B.total : base;
 }
 
+namespace {
+// Pointers into the context-parallel backward's workspace.
+struct BwdCpPtrs {
+    int32_t *count, *table, *first;
+    float *M, *Nm, *Sin, *r, *dend;
+    unsigned char *tw;  // the tensor-core layout over the segments' slots
+    int Pm, nslots;
+};
+BwdCpPtrs bwd_cp_ptrs(const BwdCpLayout &B, int T, int H, unsigned char *ws) {
+    const CpLayout &C = B.cp;
+    BwdCpPtrs p;
+    p.count = reinterpret_cast<int32_t *>(ws + C.off_count);
+    p.table = reinterpret_cast<int32_t *>(ws + C.off_table);
+    p.first = reinterpret_cast<int32_t *>(ws + C.off_first);
+    p.M = reinterpret_cast<float *>(ws + C.off_M);
+    p.Nm = reinterpret_cast<float *>(ws + C.off_N);
+    p.Sin = reinterpret_cast<float *>(ws + C.off_Sin);
+    p.r = reinterpret_cast<float *>(ws + B.off_r);
+    p.dend = reinterpret_cast<float *>(ws + B.off_end);
+    p.tw = ws + B.off_tc;
+    p.Pm = C.P_max;
+    p.nslots = (int)bwd_tc_layout(C.P_max, T, H).nslots;
+    return p;
+}
+
+// The forward pass as the CP prefill runs it, keeping what the reverse pass
+// needs: segment table, every chunk's blob (with T and M^T), the transitions
+// of every segment, their ordered composition, and the replay from each
+// segment's exact start keeping its state and U tiles (and writing o and the
+// final states when a has them).
+cudaError_t bwd_cp_forward(kda::ChunkArgs a, int N, int T, int H, const BwdCpLayout &B, unsigned char *ws,
+                           cudaStream_t st) {
+    const BwdCpPtrs w = bwd_cp_ptrs(B, T, H, ws);
+    const BwdTcLayout L = bwd_tc_layout(w.Pm, T, H);
+    int2 *list = reinterpret_cast<int2 *>(w.tw + L.off_list);
+    int *claim = reinterpret_cast<int *>(w.tw + L.off_claim);
+    unsigned char *blob = w.tw + L.off_blob;
+    float *aux = reinterpret_cast<float *>(w.tw + L.off_aux);
+    a.seg_len = B.cp.seg_len;
+    a.seg_table = w.table;
+    a.seg_count = w.count;
+    cudaError_t e = timed_launch(KDA_KERNEL_SEGMENT_TABLE, st, [&] {
+        return kda::launch_segment_table(a.cu_seqlens, N, T, B.cp.seg_len, w.Pm, w.table, w.first, w.count,
+                                         a.status, st);
+    });
+    if (e == cudaSuccess) e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st);
+    kda::ChunkArgs ar = a;
+    ar.mode = kda::MODE_REPLAY;
+    ar.S_in = w.Sin;
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st,
+                         [&] { return kda::launch_chunk_list(ar, w.Pm, w.nslots, list, st); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
+            return kda::launch_chunk_prep(ar, list, 0, w.nslots, blob, true, claim, false, st, aux);
+        });
+    kda::ChunkArgs at = a;
+    at.mode = kda::MODE_TRANSITION;
+    at.o = nullptr;
+    at.S_final = nullptr;
+    at.M_out = w.M;
+    at.N_out = w.Nm;
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+            return kda::launch_chunk_walk(at, w.Pm, blob, 0, w.nslots, nullptr, nullptr, st);
+        });
+    kda::ComposeArgs c = {};
+    c.M = w.M; c.Nm = w.Nm; c.S0 = a.S_init; c.S_in = w.Sin; c.S_final = nullptr;
+    c.first = w.first; c.P = 0; c.chains = N; c.H = H; c.dk = 128; c.dv = 128;
+    if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_SEGMENT_COMPOSE, st, [&] { return kda::launch_compose(c, st); });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
+            return kda::launch_chunk_walk(ar, w.Pm, blob, 0, w.nslots, nullptr, nullptr, st, w.tw + L.off_s,
+                                          w.tw + L.off_u);
+        });
+    return e;
+}
+
+// The reverse pass over what bwd_cp_forward kept: every segment walked back
+// from zero (r), the state gradient scanned over the segments last to first,
+// every segment walked back again from its exact end gradient keeping its
+// tiles, then the chunk gradients.
+cudaError_t bwd_cp_reverse(kda::BwdTcArgs b, int N, int T, int H, const BwdCpLayout &B, unsigned char *ws,
+                           float scale, cudaStream_t st) {
+    const BwdCpPtrs w = bwd_cp_ptrs(B, T, H, ws);
+    const BwdTcLayout L = bwd_tc_layout(w.Pm, T, H);
+    int *claim = reinterpret_cast<int *>(w.tw + L.off_claim);
+    cudaError_t e = cudaMemsetAsync(claim + 1, 0, sizeof(int), st);
+    kda::BwdSegments sg = {w.table, w.count, w.Pm, nullptr, w.r, false};
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+            return kda::launch_bwd_walk(b, 0, w.nslots, nullptr, nullptr, st, &sg);
+        });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_COMPOSE, st, [&] {
+            return kda::launch_bwd_compose(w.M, w.r, w.first, b.cu_seqlens, b.dS_final, w.dend, b.dS0, N, H, scale,
+                                           st);
+        });
+    kda::BwdSegments sg2 = {w.table, w.count, w.Pm, w.dend, nullptr, true};
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
+            return kda::launch_bwd_walk(b, 0, w.nslots, nullptr, nullptr, st, &sg2);
+        });
+    if (e == cudaSuccess)
+        e = timed_launch(KDA_KERNEL_BWD_CHUNK, st,
+                         [&] { return kda::launch_bwd_chunk(b, 0, w.nslots, claim + 1, false, st); });
+    return e;
+}
+
+// The CP backward's layout when the call is cut into segments (bf16,
+// d = 128, T > 0), else an empty layout (seg_len 0).
+BwdCpLayout bwd_cp_plan(int N, int T, int H, int dk, int dv, int in_dtype, int cp_mode, int segment_len) {
+    if (dk == 128 && dv == 128 && in_dtype == KDA_DTYPE_BF16 && N >= 1 && H >= 1 && T > 0)
+        return bwd_cp_layout(N, T, H, cp_mode, segment_len);
+    return BwdCpLayout();
+}
+
+int bwd_cp_check_args(int cp_mode, int segment_len) {
+    if (cp_mode != KDA_CP_OFF && cp_mode != KDA_CP_ON && cp_mode != KDA_CP_AUTO) return KDA_ERR_INVALID_ARG;
+    if (segment_len < 0 || segment_len % kChunk != 0) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+}  // namespace
+
 int kda_chunk_bwd_cp(const void *q, const void *k, const void *v, const float *g, const float *beta,
                      const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const float *initial_state,
                      const void *dout, const float *dS_final, float *dq, float *dk_, float *dv_, float *dg,
                      float *dbeta, float *dS0, float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
                      void *workspace, size_t workspace_bytes, uint32_t *status, void *stream) {
-    if (cp_mode != KDA_CP_OFF && cp_mode != KDA_CP_ON && cp_mode != KDA_CP_AUTO) return KDA_ERR_INVALID_ARG;
-    if (segment_len < 0 || segment_len % kChunk != 0) return KDA_ERR_INVALID_ARG;
-    const BwdCpLayout B = (dk == 128 && dv == 128 && in_dtype == KDA_DTYPE_BF16 && N >= 1 && H >= 1 && T > 0)
-                              ? bwd_cp_layout(N, T, H, cp_mode, segment_len)
-                              : BwdCpLayout();
+    int rc = bwd_cp_check_args(cp_mode, segment_len);
+    if (rc != KDA_OK) return rc;
+    const BwdCpLayout B = bwd_cp_plan(N, T, H, dk, dv, in_dtype, cp_mode, segment_len);
     if (B.cp.seg_len == 0)  // no segments for this call: the sequence form
         return kda_chunk_bwd(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, dout, dS_final, dq, dk_,
                              dv_, dg, dbeta, dS0, scale, g_min, in_dtype, workspace, workspace_bytes, status, stream);
@@ -872,84 +994,62 @@ int kda_chunk_bwd_cp(const void *q, const void *k, const void *v, const float *g
     if (!workspace || workspace_bytes < B.total) return KDA_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const CpLayout &C = B.cp;
-    const int Pm = C.P_max;
-    int32_t *count = reinterpret_cast<int32_t *>(ws + C.off_count);
-    int32_t *table = reinterpret_cast<int32_t *>(ws + C.off_table);
-    int32_t *first = reinterpret_cast<int32_t *>(ws + C.off_first);
-    float *M = reinterpret_cast<float *>(ws + C.off_M);
-    float *Nm = reinterpret_cast<float *>(ws + C.off_N);
-    float *Sin = reinterpret_cast<float *>(ws + C.off_Sin);
-    unsigned char *tw = ws + B.off_tc;
-    const BwdTcLayout L = bwd_tc_layout(Pm, T, H);
-    const int nslots = (int)L.nslots;
-    int2 *list = reinterpret_cast<int2 *>(tw + L.off_list);
-    int *claim = reinterpret_cast<int *>(tw + L.off_claim);
-    unsigned char *blob = tw + L.off_blob;
-    float *aux = reinterpret_cast<float *>(tw + L.off_aux);
-    float *r = reinterpret_cast<float *>(ws + B.off_r);
-    float *dend = reinterpret_cast<float *>(ws + B.off_end);
-
-    // forward pass, as the CP prefill runs it: segment table, every chunk's
-    // blob (with T and M kept), transitions, the segment states, and the
-    // replay keeping its state and U tiles
-    kda::ChunkArgs a = bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state, nullptr, nullptr, scale,
-                                       g_min, status);
-    a.seg_len = C.seg_len;
-    a.seg_table = table;
-    a.seg_count = count;
-    cudaError_t e = timed_launch(KDA_KERNEL_SEGMENT_TABLE, st, [&] {
-        return kda::launch_segment_table(cu_seqlens, N, T, C.seg_len, Pm, table, first, count, status, st);
-    });
-    if (e == cudaSuccess) e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st);
-    kda::ChunkArgs ar = a;
-    ar.mode = kda::MODE_REPLAY;
-    ar.S_in = Sin;
+    cudaError_t e = bwd_cp_forward(bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state, nullptr,
+                                                   nullptr, scale, g_min, status),
+                                   N, T, H, B, ws, st);
     if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_CHUNK_LIST, st, [&] { return kda::launch_chunk_list(ar, Pm, nslots, list, st); });
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_CHUNK_PREP, st, [&] {
-            return kda::launch_chunk_prep(ar, list, 0, nslots, blob, true, claim, false, st, aux);
-        });
-    kda::ChunkArgs at = a;
-    at.mode = kda::MODE_TRANSITION;
-    at.M_out = M;
-    at.N_out = Nm;
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
-            return kda::launch_chunk_walk(at, Pm, blob, 0, nslots, nullptr, nullptr, st);
-        });
-    kda::ComposeArgs c = {};
-    c.M = M; c.Nm = Nm; c.S0 = initial_state; c.S_in = Sin; c.S_final = nullptr;
-    c.first = first; c.P = 0; c.chains = N; c.H = H; c.dk = 128; c.dv = 128;
-    if (e == cudaSuccess) e = timed_launch(KDA_KERNEL_SEGMENT_COMPOSE, st, [&] { return kda::launch_compose(c, st); });
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_CHUNK_WALK, st, [&] {
-            return kda::launch_chunk_walk(ar, Pm, blob, 0, nslots, nullptr, nullptr, st, tw + L.off_s, tw + L.off_u);
-        });
-    // reverse pass: every segment from zero (r_p), the scan of the state
-    // gradient over the segments last to first, every segment again from its
-    // exact end gradient keeping its tiles, then the chunk gradients
-    kda::BwdTcArgs b = bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_, dg, dbeta,
-                                   dS0, scale, g_min, tw, status, Pm);
-    kda::BwdSegments sg = {table, count, Pm, nullptr, r, false};
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
-            return kda::launch_bwd_walk(b, 0, nslots, nullptr, nullptr, st, &sg);
-        });
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_BWD_COMPOSE, st, [&] {
-            return kda::launch_bwd_compose(M, r, first, cu_seqlens, dS_final, dend, dS0, N, H, scale, st);
-        });
-    kda::BwdSegments sg2 = {table, count, Pm, dend, nullptr, true};
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_BWD_WALK, st, [&] {
-            return kda::launch_bwd_walk(b, 0, nslots, nullptr, nullptr, st, &sg2);
-        });
-    if (e == cudaSuccess)
-        e = timed_launch(KDA_KERNEL_BWD_CHUNK, st,
-                         [&] { return kda::launch_bwd_chunk(b, 0, nslots, claim + 1, false, st); });
+        e = bwd_cp_reverse(bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_, dv_, dg,
+                                       dbeta, dS0, scale, g_min, ws + B.off_tc, status, B.cp.P_max),
+                           N, T, H, B, ws, scale, st);
     return cuda_status(e);
+}
+
+int kda_chunk_fwd_train_cp(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv,
+                           const float *initial_state, float *final_state, void *o, float scale, float g_min,
+                           int in_dtype, int cp_mode, int segment_len, void *saved, size_t saved_bytes,
+                           uint32_t *status, void *stream) {
+    int rc = bwd_cp_check_args(cp_mode, segment_len);
+    if (rc != KDA_OK) return rc;
+    const BwdCpLayout B = bwd_cp_plan(N, T, H, dk, dv, in_dtype, cp_mode, segment_len);
+    if (B.cp.seg_len == 0)
+        return kda_chunk_fwd_train(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, initial_state, final_state, o,
+                                   scale, g_min, in_dtype, saved, saved_bytes, status, stream);
+    if (!cu_seqlens || !q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
+        !aligned16(initial_state) || !aligned16(final_state) || !aligned16(saved))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)T * H * dk >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!saved || saved_bytes < B.total) return KDA_ERR_WORKSPACE;
+    return cuda_status(bwd_cp_forward(bwd_tc_fwd_args(q, k, v, g, beta, cu_seqlens, T, H, initial_state,
+                                                      final_state, o, scale, g_min, status),
+                                      N, T, H, B, static_cast<unsigned char *>(saved),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int kda_chunk_bwd_saved_cp(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int N, int T, int H, int dk, int dv, const void *dout,
+                           const float *dS_final, float *dq, float *dk_, float *dv_, float *dg, float *dbeta,
+                           float *dS0, float scale, float g_min, int in_dtype, int cp_mode, int segment_len,
+                           void *saved, size_t saved_bytes, uint32_t *status, void *stream) {
+    int rc = bwd_cp_check_args(cp_mode, segment_len);
+    if (rc != KDA_OK) return rc;
+    const BwdCpLayout B = bwd_cp_plan(N, T, H, dk, dv, in_dtype, cp_mode, segment_len);
+    if (B.cp.seg_len == 0)
+        return kda_chunk_bwd_saved(q, k, v, g, beta, cu_seqlens, N, T, H, dk, dv, dout, dS_final, dq, dk_, dv_, dg,
+                                   dbeta, dS0, scale, g_min, in_dtype, saved, saved_bytes, status, stream);
+    if (!cu_seqlens || !q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dout) ||
+        !aligned16(dS_final) || !aligned16(dS0) || !aligned16(saved))
+        return KDA_ERR_ALIGNMENT;
+    if ((size_t)T * H * dk >= ((size_t)1 << 40)) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!saved || saved_bytes < B.total) return KDA_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(saved);
+    return cuda_status(bwd_cp_reverse(bwd_tc_args(q, k, v, g, beta, cu_seqlens, N, T, H, dout, dS_final, dq, dk_,
+                                                  dv_, dg, dbeta, dS0, scale, g_min, ws + B.off_tc, status,
+                                                  B.cp.P_max),
+                                      N, T, H, B, ws, scale, static_cast<cudaStream_t>(stream)));
 }
 
 size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, int in_dtype, int pieces) {

@@ -324,3 +324,34 @@ def test_context_parallel_backward_arguments(kda):
         torch.cuda.synchronize()
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+
+
+def test_context_parallel_training_pair(kda, oracle):
+    """The training pair on the context-parallel schedule: chunk_fwd_train
+    returns chunk_fwd's CP outputs bit for bit and keeps the segments'
+    operands; chunk_bwd_saved returns chunk_bwd_cp's gradients bit for bit;
+    sequences over several segments, an empty one, dS_final."""
+    lens = [3000, 0, 1500, 2000]
+    x = _case(lens, 2, 128, torch.bfloat16, seed=71)
+    cp = dict(cp_mode=kda.CP_ON, segment_len=1024)
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"])
+    o_ref, S_ref = kda.chunk_fwd(*args, initial_state=x["S0"], scale=0.6, **cp)
+    kda.kernel_timing_start()
+    o, Sf, saved = kda.chunk_fwd_train(*args, initial_state=x["S0"], scale=0.6, **cp)
+    kern = kda.kernel_timing_stop()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(Sf, S_ref)
+    assert torch.equal(Sf[1], x["S0"][1])
+    assert kern["kda_chunk_walk_kernel"]["launches"] == 2 and "kda_bwd_walk_kernel" not in kern
+    ref = kda.chunk_bwd_cp(*args, x["do"], initial_state=x["S0"], dS_final=x["dSf"], scale=0.6, **cp)
+    kda.kernel_timing_start()
+    got = kda.chunk_bwd_saved(*args, x["do"], saved, dS_final=x["dSf"], scale=0.6, **cp)
+    kern = kda.kernel_timing_stop()
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    assert "kda_chunk_walk_kernel" not in kern and kern["kda_bwd_walk_kernel"]["launches"] == 2
+    r = oracle.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
+                        x["cu"].cpu().numpy(), to64(x["do"]), S0=to64(x["S0"]), dS_final=to64(x["dSf"]), scale=0.6)
+    for i in (0, 1, 2, 3, 5):
+        assert normwise_err(to64(got[i]), r[i], head_axis=1) <= TC_TOL
