@@ -15,7 +15,8 @@
 // local (the reverse of each forward step):
 //     dVres = TB^T dU (= dv),  dTB = dU Vres^T,  dT = dTB diag(b),
 //     dbeta_s = sum_t dTB[t][s] T[t][s] + sum_s' dA[s][s'] M[s][s'],
-//     dA = strict_lower(-T^T dT T^T),  dM = diag(b) dA,  dB = scale lower(dO U^T),
+//     dA = strict_lower(-T^T dT T^T) = strict_lower(-(T^T dU) U^T)  (U = T diag(b) Vres),
+//     dM = diag(b) dA,  dB = scale lower(dO U^T),
 //     dQ~ = scale dO S^T + (dB through the causal tiles),
 //     dK~ = -dVres S^T + (dM through the causal tiles),  dK^ = U dS_C^T,
 //     dgamma_C += Gam_C . rowsum(dS_C . S)
@@ -35,10 +36,10 @@
 //                         = dS / scale resident in tensor memory, the four
 //                         products of a chunk on the tensor cores; keeps the
 //                         bf16 tiles dS'^T and dU'^T of every chunk;
-//   kda_bwd_chunk_kernel  persistent over (chunk, head) items: nine products
-//                         per item on the tensor cores (operands in shared
-//                         memory, accumulators in tensor memory), the rest on
-//                         the CUDA cores in fp32.
+//   kda_bwd_chunk_kernel  persistent over (chunk, head) items: three batches
+//                         of products per item on the tensor cores (operands in
+//                         shared memory, accumulators in tensor memory), the
+//                         rest on the CUDA cores in fp32.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -393,6 +394,8 @@ constexpr uint32_t B_VR = 98304;    // Vres^T bf16 [j][s]
 constexpr uint32_t B_UB = 114688;   // U^T bf16 [j][t]   (B_VR + 16 KB: second M block of [Vres; U])
 constexpr uint32_t B_DU = 131072;   // dU'^T bf16 [j][t]
 constexpr uint32_t B_TBL = 147456;  // the low bf16 part of T diag(b)
+constexpr uint32_t B_TN = 155648;   // T bf16, MN-major (n = b, k = t)
+constexpr uint32_t B_PT = B_TBL;    // after the first batch: P^T = (T^T dU')^T bf16 [j][a] (16 KB)
 constexpr uint32_t B_KT = 163840;   // K~, MN-major (n = t, k = i); then -dVres^T bf16 [j][s]
 constexpr uint32_t B_NDV = B_KT;
 constexpr uint32_t B_TB = 180224;   // T diag(b), MN-major (n = s, k = t)
@@ -405,12 +408,9 @@ constexpr uint32_t B_MT = 204800;   // M^T f32 [64][64]
 constexpr uint32_t B_KST = B_UB, B_QST = B_VR, B_GST = B_DS;
 // phases C and D, over the phase A / B regions once the second batch is done:
 constexpr uint32_t B_AP = 0;        // A' K-major 128 rows x 192 (three K blocks of 16 KB)
-constexpr uint32_t B_T16 = 98304;   // T bf16 K-major 64 x 64
-constexpr uint32_t B_DT = 106496;   // dT, MN-major (m = t, k = s)
-constexpr uint32_t B_ZT = 114688;   // -Z, MN-major (n = b, k = t)
+constexpr uint32_t B_LT0 = 98304;   // L^T K-major 128 channels x 128: K block 0 (k x)
 constexpr uint32_t B_RS = 122880;   // R_seg^T K-major 128 channels x 192 (three K blocks)
-constexpr uint32_t B_LT = 188416;   // L^T K-major 128 channels x 128 (two K blocks), over T and M^T
-                                    // once the beta gradient has read them
+constexpr uint32_t B_LT1 = 172032;  //   and K block 1 (q x)
 constexpr uint32_t B_CUM = B_KT;    // the combine's block sums f32 [8][128] (K~ is built after the
                                     // next item's copies, which go out during the combine, have landed)
 constexpr uint32_t B_MISC = 221184;
@@ -418,15 +418,16 @@ constexpr uint32_t B_BETA = B_MISC;           // f32 [64]
 constexpr uint32_t B_PART = B_MISC + 256;     // f32 [4][128] block decays
 constexpr uint32_t B_DGC = B_PART + 2048;     // f32 [8][128] parts of rowsum(dS' . S)
 constexpr uint32_t B_DBP = B_DGC + 4096;      // f32 [8][64] beta gradient parts
-constexpr uint32_t B_BAR = B_DBP + 2048;      // 7 mbarriers: loads, five product batches, late loads
+constexpr uint32_t B_BAR = B_DBP + 2048;      // 5 mbarriers: loads, three product batches, late loads
 constexpr uint32_t B_TMEM = B_BAR + 56;
 constexpr uint32_t B_CLAIM = B_TMEM + 8;      // int [2]: item in hand, next item
 constexpr uint32_t B_SMEM = B_CLAIM + 8 + 1024;
-static_assert(B_RS + 49152 <= B_TF, "phase C regions overlap the kept T and M");
-static_assert(B_LT + 32768 <= B_MISC, "L^T");
+static_assert(B_LT0 + 16384 <= B_RS && B_RS + 49152 <= B_LT1 && B_LT1 + 16384 <= B_TF,
+              "phase C regions overlap one another or the kept T and M");
+static_assert(B_TN + 8192 <= B_KT, "T tile");
 static_assert(B_SMEM <= 232448, "shared memory");
 // tensor-memory columns of the products
-constexpr uint32_t T1 = 0, T2 = 64, T3 = 0, T4 = 320, T5 = 448, T6 = 128, T7 = 192, T8 = 0, T9 = 128;
+constexpr uint32_t T1 = 0, T2 = 64, TP = 128, T3 = 0, T4 = 320, T5 = 448, T7 = 192, T8 = 0, T9 = 128;
 
 struct BchunkParams {
     const void *k, *q, *v;           // bf16 [T][H][128]
@@ -473,11 +474,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     const float *sTF = reinterpret_cast<const float *>(sm + B_TF);
     const float *sMT = reinterpret_cast<const float *>(sm + B_MT);
     int *sClaim = reinterpret_cast<int *>(sm + B_CLAIM);
-    const uint32_t bar = sb + B_BAR;  // bar + 8 k: k = 0 loads, 1..5 product batches, 6 late loads
+    const uint32_t bar = sb + B_BAR;  // bar + 8 k: k = 0 loads, 1..3 product batches, 4 late loads
     const float scale = p.scale, wscale = p.wscale, g_min = p.g_min;
 
     if (tid == 0) {
-        for (int b = 0; b < 7; ++b) umma::mbar_init(bar + 8 * b, 1);
+        for (int b = 0; b < 5; ++b) umma::mbar_init(bar + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         sClaim[0] = atomicAdd(p.claim, 1);
         sClaim[1] = atomicAdd(p.claim, 1);
@@ -596,6 +597,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         }
         sts128(sb + B_TB + umma::mnmaj(s, t, 1), hi[0], hi[1], hi[2], hi[3]);
         sts128(sb + B_TBL + umma::mnmaj(s, t, 1), lo[0], lo[1], lo[2], lo[3]);
+        // and T itself, the B operand of P^T = dU'^T T
+        const float4 a0 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s);
+        const float4 a1 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s + 4);
+        sts128(sb + B_TN + umma::mnmaj(s, t, 1), pack_bf16(a0.x, a0.y), pack_bf16(a0.z, a0.w), pack_bf16(a1.x, a1.y),
+               pack_bf16(a1.z, a1.w));
     }
     {  // dO rows past the chunk end (every row when dO enters no product) are zero
         const int z0 = p.zero_do ? 0 : Lc;
@@ -608,14 +614,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     umma::fence_before();
     __syncthreads();
 
-    // ---------------------------------------------------------------- batch 1: (K~ S)^T, dVres^T / wscale
+    // ---------------------------------------------------------------- batch 1: (K~ S)^T, dVres^T / wscale, P^T
+    // (dA = -T^T dT T^T with dT = dU Vres^T diag(b) and U = T diag(b) Vres is
+    // -(T^T dU) U^T: P = T^T dU' here, P U^T with the second batch)
     if (tid == 0) {
         umma::fence_after();
         // the rows are read: the tiles that go over their staging
         umma::fence_proxy_async();
-        umma::mbar_expect_tx(bar + 48, TILE_S + TILE_U);
-        umma::bulk_load(sb + B_DS, p.save_ds + wa * TILE_S, TILE_S, bar + 48);
-        umma::bulk_load(sb + B_UB, p.save_u + wa * TILE_U, TILE_U, bar + 48);
+        umma::mbar_expect_tx(bar + 32, TILE_S + TILE_U);
+        umma::bulk_load(sb + B_DS, p.save_ds + wa * TILE_S, TILE_S, bar + 32);
+        umma::bulk_load(sb + B_UB, p.save_u + wa * TILE_U, TILE_U, bar + 32);
         constexpr uint32_t id1 = umma::idesc_bf16(128, 64, 0, 1, 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -626,6 +634,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             umma::mma(tmem + T2, umma::sdesc4(sb4 + ((B_DU + (ks & 3) * 32) >> 4), 16, 1024),
                       umma::sdesc4(sb4 + (((ks < 4 ? B_TB : B_TBL) + (ks & 3) * 2048) >> 4), 1024, 1024), id1,
                       ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            umma::mma(tmem + TP, umma::sdesc4(sb4 + ((B_DU + ks * 32) >> 4), 16, 1024),
+                      umma::sdesc4(sb4 + ((B_TN + ks * 2048) >> 4), 1024, 1024), id1, ks > 0 ? 1u : 0u);
         umma::commit(bar + 8);
         // the next item's tiles and rows into L2 while this one runs
         ncl = (wn < p.nitems) ? p.list[p.slot0 + wn / H] : make_int2(0, 0);
@@ -673,13 +685,16 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         }
         sts_bf16x8(sb + B_NDV + umma::kmaj(j, c0, 128), a, 0);
         sts_bf16x8(sb + B_NDV + umma::kmaj(j, c0 + 8, 128), a, 8);
+        umma::ld16(tq + TP + c0, a);  // P^T row j, columns a = c0 ..
+        sts_bf16x8(sb + B_PT + umma::kmaj(j, c0, 128), a, 0);
+        sts_bf16x8(sb + B_PT + umma::kmaj(j, c0 + 8, 128), a, 8);
     }
-    pend |= umma::mbar_wait(bar + 48, par, WAIT_LIMIT) ? 0u : 64u;
+    pend |= umma::mbar_wait(bar + 32, par, WAIT_LIMIT) ? 0u : 16u;
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
 
-    // ---------------------------------------------------------------- batch 2: Vres dU'^T, dO U^T, S dO^T, -S dVres^T, dS' U^T
+    // ---------------------------------------------------------------- batch 2: Vres dU'^T, dO U^T, S dO^T, -S dVres^T, dS' U^T, P U^T
     if (tid == 0) {
         umma::fence_after();
         constexpr uint32_t id3 = umma::idesc_bf16(128, 64, 1, 1, 0);
@@ -711,6 +726,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         for (int ks = 0; ks < 8; ++ks)
             umma::mma(tmem + T5, umma::sdesc4(sb4 + ((B_DS + ks * 2048) >> 4), 16384, 1024),
                       umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id5, ks > 0 ? 1u : 0u);
+        // lanes 0-63: P U^T, lane a (A = P^T read MN-major, rows 64-127 unused)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            umma::mma(tmem + T7, umma::sdesc4(sb4 + ((B_PT + ks * 2048) >> 4), 16384, 1024),
+                      umma::sdesc4(sb4 + ((B_UB + ks * 2048) >> 4), 1024, 1024), id3, ks > 0 ? 1u : 0u);
         umma::commit(bar + 16);
     }
     {  // rowsum(dS' . S): key channels 2 cp, 2 cp + 1 over value columns 16 jg .. 16 jg + 15
@@ -728,58 +748,11 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     pend |= umma::mbar_wait(bar + 16, par, WAIT_LIMIT) ? 0u : 4u;
     umma::fence_after();
     __syncthreads();  // every thread is done with the S and dS' tiles
-    // the phase A / B regions are free: zero A', and T in bf16
+    // the phase A / B regions are free: zero A'; meanwhile the anchored
+    // operands of the last batch, which no readout below touches
     for (int idx = tid; idx < 49152 / 16; idx += NB)
         *reinterpret_cast<uint4 *>(sm + B_AP + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
-    {
-        const int t = tid >> 3, s = 8 * (tid & 7);
-        const float4 a0 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s);
-        const float4 a1 = *reinterpret_cast<const float4 *>(sTF + t * 64 + s + 4);
-        sts128(sb + B_T16 + umma::kmaj(t, s, 64), pack_bf16(a0.x, a0.y), pack_bf16(a0.z, a0.w), pack_bf16(a1.x, a1.y),
-               pack_bf16(a1.z, a1.w));
-    }
-    __syncthreads();
-    if (qd < 2) {  // lanes 0-63: s = l; columns t: dTB[t][s] / wscale
-        const int s = l;
-        float a[16];
-        umma::ld16(tq + T3 + c0, a);
-        const float bs = sBeta[s];
-        float dbp = 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const float dtb = a[u] * wscale;
-            dbp = fmaf(dtb, sTF[(c0 + u) * 64 + s], dbp);
-            a[u] = dtb * bs;
-        }
-        sDbp[cg * 64 + s] = dbp;
-        sts_bf16x8(sb + B_DT + umma::kmaj(s, c0, 64), a, 0);
-        sts_bf16x8(sb + B_DT + umma::kmaj(s, c0 + 8, 64), a, 8);
-    } else {  // lanes 64-127: t = l - 64; columns 64 + s: (dO U^T)[t][s] -> A' row 64 + t (s <= t)
-        const int t = l - 64, bt = t >> 4;
-        float a[16];
-        umma::ld16(tq + T3 + 64 + c0, a);
-        if (cg <= bt) {  // the columns of this block lie in the segment of row t
-#pragma unroll
-            for (int u = 0; u < 16; ++u) a[u] = (c0 + u <= t) ? scale * a[u] : 0.f;
-            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0, 128), a, 0);
-            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0 + 8, 128), a, 8);
-        }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-
-    // ---------------------------------------------------------------- batch 3: Z = dT T^T
-    if (tid == 0) {
-        umma::fence_after();
-        constexpr uint32_t id6 = umma::idesc_bf16(128, 64, 1, 0, 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            umma::mma(tmem + T6, umma::sdesc4(sb4 + ((B_DT + ks * 2048) >> 4), 8192, 1024),
-                      umma::sdesc4(sb4 + ((B_T16 + ks * 32) >> 4), 16, 1024), id6, ks > 0 ? 1u : 0u);
-        umma::commit(bar + 24);
-    }
-    {  // meanwhile the anchored column operand R_seg^T: for segment i >= cg,
+    {  // the anchored column operand R_seg^T: for segment i >= cg,
        // R_i[s] = k_s y_s c_i with c_i = 1 / delta_cg (i = cg), else the decays
        // of the blocks strictly between
         float y[16];
@@ -802,53 +775,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             sts_bf16x8(sb + B_RS + umma::kmaj(ch, segoff(i) + c0 + 8, 128), a, 8);
         }
     }
-    pend |= umma::mbar_wait(bar + 24, par, WAIT_LIMIT) ? 0u : 8u;
-    umma::fence_after();
-    if (qd < 2) {  // -Z as the MN-major B operand (n = b, k = t): row t = l
-        float a[16];
-        umma::ld16(tq + T6 + c0, a);
-#pragma unroll
-        for (int u = 0; u < 16; ++u) a[u] = -a[u];
-        sts_bf16x8(sb + B_ZT + umma::kmaj(l, c0, 64), a, 0);
-        sts_bf16x8(sb + B_ZT + umma::kmaj(l, c0 + 8, 64), a, 8);
-    }
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-
-    // ---------------------------------------------------------------- batch 4: dA = T^T (-Z)
-    if (tid == 0) {
-        umma::fence_after();
-        constexpr uint32_t id7 = umma::idesc_bf16(128, 64, 1, 1, 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            umma::mma(tmem + T7, umma::sdesc4(sb4 + ((B_T16 + ks * 2048) >> 4), 8192, 1024),
-                      umma::sdesc4(sb4 + ((B_ZT + ks * 2048) >> 4), 1024, 1024), id7, ks > 0 ? 1u : 0u);
-        umma::commit(bar + 32);
-    }
-    pend |= umma::mbar_wait(bar + 32, par, WAIT_LIMIT) ? 0u : 16u;
-    umma::fence_after();
-    if (qd < 2) {  // row a = l of dA (strictly lower): beta gradient, dM into A' row a
-        const int a = l, ba_blk = a >> 4;
-        float v[16];
-        umma::ld16(tq + T7 + c0, v);
-        const float ba = sBeta[a];
-        float dbp = 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int b = c0 + u;
-            const float da = (b < a) ? v[u] : 0.f;
-            dbp = fmaf(da, sMT[b * 64 + a], dbp);
-            v[u] = ba * da;
-        }
-        sDbp[256 + cg * 64 + a] = dbp;
-        if (cg <= ba_blk) {
-            sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0, 128), v, 0);
-            sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0 + 8, 128), v, 8);
-        }
-    }
-    __syncthreads();  // T and M^T read: L^T goes over them
-    {  // the anchored row operand L^T (row ch: k x, then q x)
+    {  // the anchored row operand L^T (row ch: k x in K block 0, q x in K block 1)
         float x[16], a[16], b[16];
         prefix(x);
 #pragma unroll
@@ -856,16 +783,57 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
             a[u] = kf(u) * x[u];
             b[u] = qf(u) * x[u];
         }
-        sts_bf16x8(sb + B_LT + umma::kmaj(ch, c0, 128), a, 0);
-        sts_bf16x8(sb + B_LT + umma::kmaj(ch, c0 + 8, 128), a, 8);
-        sts_bf16x8(sb + B_LT + umma::kmaj(ch, 64 + c0, 128), b, 0);
-        sts_bf16x8(sb + B_LT + umma::kmaj(ch, 64 + c0 + 8, 128), b, 8);
+        sts_bf16x8(sb + B_LT0 + umma::kmaj(ch, c0, 128), a, 0);
+        sts_bf16x8(sb + B_LT0 + umma::kmaj(ch, c0 + 8, 128), a, 8);
+        sts_bf16x8(sb + B_LT1 + umma::kmaj(ch, c0, 128), b, 0);
+        sts_bf16x8(sb + B_LT1 + umma::kmaj(ch, c0 + 8, 128), b, 8);
+    }
+    __syncthreads();  // A' zeroed before its rows are written
+    if (qd < 2) {
+        {  // lanes 0-63: s = l; columns t: dTB[t][s] / wscale -> beta gradient
+            const int s = l;
+            float a[16];
+            umma::ld16(tq + T3 + c0, a);
+            float dbp = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) dbp = fmaf(a[u] * wscale, sTF[(c0 + u) * 64 + s], dbp);
+            sDbp[cg * 64 + s] = dbp;
+        }
+        {  // row a = l of dA = -wscale P U^T (strictly lower): beta gradient, dM into A' row a
+            const int a = l, ba_blk = a >> 4;
+            float v[16];
+            umma::ld16(tq + T7 + c0, v);
+            const float ba = sBeta[a];
+            float dbp = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int b = c0 + u;
+                const float da = (b < a) ? -wscale * v[u] : 0.f;
+                dbp = fmaf(da, sMT[b * 64 + a], dbp);
+                v[u] = ba * da;
+            }
+            sDbp[256 + cg * 64 + a] = dbp;
+            if (cg <= ba_blk) {
+                sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0, 128), v, 0);
+                sts_bf16x8(sb + B_AP + umma::kmaj(a, segoff(ba_blk) + c0 + 8, 128), v, 8);
+            }
+        }
+    } else {  // lanes 64-127: t = l - 64; columns 64 + s: (dO U^T)[t][s] -> A' row 64 + t (s <= t)
+        const int t = l - 64, bt = t >> 4;
+        float a[16];
+        umma::ld16(tq + T3 + 64 + c0, a);
+        if (cg <= bt) {  // the columns of this block lie in the segment of row t
+#pragma unroll
+            for (int u = 0; u < 16; ++u) a[u] = (c0 + u <= t) ? scale * a[u] : 0.f;
+            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0, 128), a, 0);
+            sts_bf16x8(sb + B_AP + umma::kmaj(64 + t, segoff(bt) + c0 + 8, 128), a, 8);
+        }
     }
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
 
-    // ---------------------------------------------------------------- batch 5: dL = A' R_seg, dR_seg = A'^T L
+    // ---------------------------------------------------------------- batch 3: dL = A' R_seg, dR_seg = A'^T L
     if (tid == 0) {
         umma::fence_after();
         constexpr uint32_t id8 = umma::idesc_bf16(128, 128, 0, 0, 0);
@@ -879,10 +847,10 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t kb = ks >> 2, kin = (ks & 3) * 32;
-            umma::mma(tmem + T9, umma::sdesc4(sb4 + ((B_LT + kb * 16384 + kin) >> 4), 16, 1024),
+            umma::mma(tmem + T9, umma::sdesc4(sb4 + (((kb ? B_LT1 : B_LT0) + kin) >> 4), 16, 1024),
                       umma::sdesc4(sb4 + ((B_AP + ks * 2048) >> 4), 16384, 1024), id9, ks > 0 ? 1u : 0u);
         }
-        umma::commit(bar + 40);
+        umma::commit(bar + 24);
     }
     if (tid < CH && tid < Lc) {
         float db = 0.f;
@@ -890,7 +858,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
         for (int pq = 0; pq < 8; ++pq) db += sDbp[pq * 64 + tid];
         p.dbeta[(size_t)(tc + tid) * H + h] = db;
     }
-    pend |= umma::mbar_wait(bar + 40, par, WAIT_LIMIT) ? 0u : 32u;
+    pend |= umma::mbar_wait(bar + 24, par, WAIT_LIMIT) ? 0u : 8u;
     umma::fence_after();
     if (tid == 0) {  // every product has read its operands: the next item's copies, and the one after claimed
         preloaded = wn < p.nitems && ncl.y > 0 && pend == 0;
@@ -1022,7 +990,7 @@ __global__ void __launch_bounds__(NB, 1) kda_bwd_chunk_kernel(const __grid_const
     ++it;
     if (__syncthreads_or(pend != 0)) {  // uniform: leave once the copies and products in flight are done
         if (pend & 1u) umma::mbar_wait(bar, par, WAIT_LIMIT);
-        for (int b = 1; b < 7; ++b)
+        for (int b = 1; b < 5; ++b)
             if (pend & (1u << b)) umma::mbar_wait(bar + 8 * b, par, WAIT_LIMIT);
         if (tid == 0 && preloaded) umma::mbar_wait(bar, par ^ 1u, WAIT_LIMIT);  // the next item's copies
         alive = false;
