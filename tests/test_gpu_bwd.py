@@ -355,3 +355,33 @@ def test_context_parallel_training_pair(kda, oracle):
                         x["cu"].cpu().numpy(), to64(x["do"]), S0=to64(x["S0"]), dS_final=to64(x["dSf"]), scale=0.6)
     for i in (0, 1, 2, 3, 5):
         assert normwise_err(to64(got[i]), r[i], head_axis=1) <= TC_TOL
+
+
+@pytest.mark.parametrize("scale,floor", [(0.0, False), (0.8, True)])
+def test_context_parallel_backward_edges(kda, oracle, scale, floor):
+    """Context-parallel segments with absent initial state and end gradient
+    (zero), dS0 not asked for; scale 0 (the state gradient is zero, dO enters
+    no product), or chunks held at and below the floor."""
+    x = _case([2500, 700], 2, 128, torch.bfloat16, seed=73 + int(floor), floor_frac=0.0)
+    if floor:
+        g = x["g"].clone()
+        g[0:64] = -5.0
+        g[1024:1100] = -6.0
+        g[2600:2700] = -5.5
+        x["g"] = g
+    got = kda.chunk_bwd_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], x["do"], scale=scale,
+                           cp_mode=kda.CP_ON, segment_len=1024, want_dS0=False)
+    torch.cuda.synchronize()
+    assert got[5] is None
+    ref = oracle.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["g"]), to64(x["beta"]),
+                          x["cu"].cpu().numpy(), to64(x["do"]), scale=scale)
+    for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), got[:5], ref[:5]):
+        a64 = to64(a)
+        assert np.all(np.isfinite(a64)), name
+        if np.max(np.abs(b)) == 0.0:
+            assert np.all(a64 == 0.0), name
+            continue
+        e = normwise_err(a64, b, head_axis=1) if name != "dbeta" else np.max(np.abs(a64 - b)) / np.max(np.abs(b))
+        assert e <= TC_TOL, f"{name}: error {e:.3e}"
+    g = x["g"].cpu()
+    assert torch.all(got[3].cpu()[g < -5.0] == 0.0)
