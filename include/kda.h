@@ -93,7 +93,8 @@ int kda_version(void);
  * "Le role de la decroissance bornee").
  *
  *  q, k, v      device, [T][H][dk] / [T][H][dv], dtype in_dtype (bf16 | f32).
- *  g            device, f32 [T][H][dk], raw log-decay; floored at g_min on load.
+ *  g            device, f32 [T][H][dk], raw log-decay; floored at g_min on load
+ *               (a NaN takes the floor, as an IEEE maximum does).
  *  beta         device, f32 [T][H].
  *  cu_seqlens   device, int32 [N+1], N sequences packed along T
  *               (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T).
@@ -257,7 +258,8 @@ size_t kda_chunk_fwd_host_workspace_size(int N, int T, int H, int dk, int dv, in
  *  dout       device [T][H][dv], in_dtype: dL/do.
  *  dS_final   device f32 [N][H][dk][dv] or NULL (zero): dL/dS_final.
  *  dq, dk, dv device f32 [T][H][d]; dg device f32 [T][H][dk] (w.r.t. the raw
- *             g); dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
+ *             g: zero where g < g_min; a NaN g gets the gradient of g = g_min);
+ *             dbeta device f32 [T][H]; dS0 device f32 [N][H][dk][dv] or NULL.
  *  workspace  device scratch of at least kda_chunk_bwd_workspace_size(...)
  *             bytes, 256-byte aligned parts.  Tensor-core form, with
  *             S = floor(T/64) + N chunk slots: the slot list (S x 8 B),
@@ -435,6 +437,7 @@ int kda_segment_compose(const float *M, const float *Nmat, const float *S0, floa
  *               KDA_STATUS_BAD_ACCEPTED_LEN is set.
  *  new_qkv      device bf16 [R][Wd+1][Cq];  new_g bf16 [R][Wd+1][H*dk];
  *  new_beta     bf16 [R][Wd+1][H]  -- row 0 bonus, rows 1..Wd drafts.
+ *               A NaN raw gate g takes the floor g_min (as an IEEE maximum).
  *  out_norm_w   device f32 [dv].
  *  o            device bf16 [R][Wd+1][H][dv]: rows for bonus + drafts.
  *  Limits: W in [1, 4] and Wd in [0, 7], so that the a + 1 + Wd <= 2*Wd + 1

@@ -36,10 +36,12 @@ Given dO and dS_C the reverse pass is, step by step in the opposite order:
     dK  = dKt Gam + dKb / Gam + dKh GamC / Gam          dQ = dQt Gam
     dgamma_t = dKt Kt - dKb Kb - dKh Kh + dQt Qt   (+ sum_t dKh Kh and
                the dgamma_C term on the chunk's last token)
-    dg'_r = sum_{t >= r} dgamma_t;   dg = dg' where g >= g_min, else 0
+    dg'_r = sum_{t >= r} dgamma_t;   dg = 0 where g < g_min, else dg'
 
 and dS0 of a chunk is dS_C of the chunk before it.  In fp64 the factors
-1/Gam stay finite (gamma >= 64 g_min = -320 within a chunk of 64).
+1/Gam stay finite (gamma >= 64 g_min = -320 within a chunk of 64).  A NaN g
+takes the floor, as an IEEE maximum does, and gets the gradient of g = g_min
+(the pages say nothing of NaN).
 """
 from __future__ import annotations
 
@@ -113,7 +115,7 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
     T, dk = k.shape
     dv = v.shape[1]
     S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
-    gp = np.maximum(g, g_min)
+    gp = np.fmax(g, g_min)
     bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
     starts, fwd = [], []
     o = np.zeros((T, dv))
@@ -130,7 +132,7 @@ def chunk_form_backward_head(q, k, v, g, beta, do, S0=None, dS_final=None, C=64,
     for (c0, c1), S_in, f in reversed(list(zip(bounds, starts, fwd))):
         dQ, dK, dV, dG, dB, dS = _chunk_reverse(f, S_in, beta[c0:c1], do[c0:c1], dS, scale, mm)
         dq[c0:c1], dkk[c0:c1], dvv[c0:c1], dgp[c0:c1], db[c0:c1] = dQ, dK, dV, dG, dB
-    dg = np.where(g >= g_min, dgp, 0.0)
+    dg = np.where(g < g_min, 0.0, dgp)
     return o, S_final, dq, dkk, dvv, dg, db, dS
 
 
@@ -151,7 +153,7 @@ def state_gradient_chain(q, k, v, g, beta, do, S0=None, dS_final=None, C=64, sca
     T, dk = k.shape
     dv = v.shape[1]
     S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
-    gp = np.maximum(g, g_min)
+    gp = np.fmax(g, g_min)
     bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
     S_in, fwd = [], []
     for c0, c1 in bounds:
@@ -175,10 +177,10 @@ def chunk_token_gradients(q, k, v, g, beta, do, S_in, dS_C, scale=1.0, g_min=-5.
     """One chunk's token gradients (dq, dk, dv, dg, dbeta) and its dS0 from the
     chunk's rows, its start state S_in and the state gradient dS_C at its end."""
     q, k, v, g, beta, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, do))
-    f = _chunk_forward(q, k, v, np.maximum(g, g_min), beta, S_in, scale)
+    f = _chunk_forward(q, k, v, np.fmax(g, g_min), beta, S_in, scale)
     dQ, dK, dV, dgp, dB, dS0 = _chunk_reverse(f, S_in, beta, do, dS_C, scale)
     # dg' of the chunk's tokens is local: gamma restarts at every chunk
-    return dQ, dK, dV, np.where(g >= g_min, dgp, 0.0), dB, dS0
+    return dQ, dK, dV, np.where(g < g_min, 0.0, dgp), dB, dS0
 
 
 def chunk_form_backward(q, k, v, g, beta, cu_seqlens, do, S0=None, dS_final=None, C=64, scale=1.0,
@@ -259,7 +261,7 @@ def chunk_form_backward_head_f32(q, k, v, g, beta, do, S0=None, dS_final=None, C
     dv = v.shape[1]
     scale = np.float32(scale)
     S = np.zeros((dk, dv), np.float32) if S0 is None else _f32(S0).copy()
-    gp = np.maximum(g, np.float32(g_min))
+    gp = np.fmax(g, np.float32(g_min))
     bounds = [(c0, min(c0 + C, T)) for c0 in range(0, T, C)]
     starts, fwd = [], []
     o = np.zeros((T, dv), np.float32)
@@ -318,6 +320,6 @@ def chunk_form_backward_head_f32(q, k, v, g, beta, do, S0=None, dS_final=None, C
         dgp[c0:c1] = np.cumsum(dgam[::-1], axis=0, dtype=np.float32)[::-1]
         db[c0:c1] = dbeta
         dS = dS0
-    dg = np.where(g >= np.float32(g_min), dgp, np.float32(0))
+    dg = np.where(g < np.float32(g_min), np.float32(0), dgp)
     out = (o, S_final, dq, dkk, dvv, dg, db, dS)
     return tuple(np.asarray(x, dtype=np.float64) for x in out)

@@ -62,12 +62,16 @@
 /*               that reduce the rule to decayed / plain linear attention)    */
 /* tmp must hold dv doubles.                                                 */
 /* ------------------------------------------------------------------------- */
+/* The floor max(g, g_min).  A NaN log-decay takes the floor (the pages say  */
+/* nothing of NaN; IEEE maximum returns the non-NaN operand).                */
+static double floor_g(double g, double g_min) { return g >= g_min ? g : g_min; }
+
 static void kda_token(int dk, int dv, double *S, const double *k, const double *v,
                       const double *g, double beta, double g_min, int erase,
                       double *tmp)
 {
     for (int i = 0; i < dk; ++i) {
-        double gi = g[i] < g_min ? g_min : g[i];
+        double gi = floor_g(g[i], g_min);
         double d = exp(gi);
         for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] *= d;
     }
@@ -216,7 +220,7 @@ int oracle_kda_backward(int N, int T, int H, int dk, int dv, const int32_t *cu_s
                 dq[th * dk + i] = scale * acc;
             }
             for (int i = 0; i < dk; ++i) {
-                double gi = gt[i] < g_min ? g_min : gt[i];
+                double gi = floor_g(gt[i], g_min);
                 double d = exp(gi);
                 for (int j = 0; j < dv; ++j) X[(size_t)i * dv + j] = d * Sp[(size_t)i * dv + j];
             }
@@ -243,7 +247,7 @@ int oracle_kda_backward(int N, int T, int H, int dk, int dv, const int32_t *cu_s
                 dk_[th * dk + i] = acc;
             }
             for (int i = 0; i < dk; ++i) {
-                double gi = gt[i] < g_min ? g_min : gt[i];
+                double gi = floor_g(gt[i], g_min);
                 double d = exp(gi), acc = 0.0;
                 for (int j = 0; j < dv; ++j) {
                     double dx = G[(size_t)i * dv + j] - bt * kt[i] * du[j];
@@ -377,7 +381,7 @@ int oracle_chunk_form_head(int T, int dk, int dv, int C, const double *q, const 
             double acc = 0.0;
             for (int t = 0; t < L; ++t) {
                 double gi = g[(size_t)(c0 + t) * dk + i];
-                acc += (gi < g_min ? g_min : gi);
+                acc += floor_g(gi, g_min);
                 gam[(size_t)t * dk + i] = acc;
             }
         }
@@ -534,7 +538,7 @@ static void verify_unit(const struct verify_args *A, int r, int h, int a, int n_
         }
         for (int i = 0; i < dk; ++i) {
             double gg = -softplus(graw[i]);
-            gv[i] = gg < A->g_min ? A->g_min : gg;
+            gv[i] = floor_g(gg, A->g_min);
         }
         double beta = sigmoid(*braw);
         kda_token(dk, dv, S, kv, vv, gv, beta, A->g_min, 1, tmp);

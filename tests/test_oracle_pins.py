@@ -607,3 +607,44 @@ def test_backward_without_final_state_gradient_and_beta_zero(oracle):
         np.testing.assert_allclose(dq[t, 0], St @ do[t, 0], rtol=1e-12, atol=1e-12)
     want = sum(np.outer(decay[t] * q[t, 0], do[t, 0]) for t in range(T))
     np.testing.assert_allclose(dS0[0, 0], want, rtol=1e-12, atol=1e-12)
+
+
+def test_nan_log_decay_takes_the_floor(oracle):
+    """A NaN log-decay acts exactly as g = g_min (the floor takes the non-NaN
+    operand, as an IEEE maximum does): prefill, segment transitions, the
+    backward (dg included) and the chunk-form reverse pass give identical
+    results; in verify a NaN raw gate acts as +inf (whose decay 1 / (1 + e^g)
+    is 0, floored to e^{g_min})."""
+    from oracle import chunk_reverse
+    rng = np.random.default_rng(97)
+    T, H, dk, dv = 40, 2, 6, 5
+    q, k, v, g, beta = rand_inputs(rng, T, H, dk, dv)
+    nan = rng.random(g.shape) < 0.2
+    g_nan, g_flr = g.copy(), g.copy()
+    g_nan[nan] = np.nan
+    g_flr[nan] = G_MIN
+    cu = np.array([0, 25, T], dtype=np.int32)
+    S0 = 0.1 * rng.standard_normal((2, H, dk, dv))
+    for a, b in zip(oracle.prefill(q, k, v, g_nan, beta, cu, S0=S0), oracle.prefill(q, k, v, g_flr, beta, cu, S0=S0)):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(oracle.segment_transition(k[:, :1], v[:, :1], g_nan[:, :1], beta[:, :1]),
+                    oracle.segment_transition(k[:, :1], v[:, :1], g_flr[:, :1], beta[:, :1])):
+        np.testing.assert_array_equal(a, b)
+    do = rng.standard_normal((T, H, dv))
+    bn = oracle.backward(q, k, v, g_nan, beta, cu, do, S0=S0)
+    bf = oracle.backward(q, k, v, g_flr, beta, cu, do, S0=S0)
+    for a, b in zip(bn, bf):
+        np.testing.assert_array_equal(a, b)
+    assert np.all(np.isfinite(bn[3]))
+    rn = chunk_reverse.chunk_form_backward_head(q[:, 0], k[:, 0], v[:, 0], g_nan[:, 0], beta[:, 0], do[:, 0], C=16)
+    rf = chunk_reverse.chunk_form_backward_head(q[:, 0], k[:, 0], v[:, 0], g_flr[:, 0], beta[:, 0], do[:, 0], C=16)
+    for a, b in zip(rn, rf):
+        np.testing.assert_array_equal(a, b)
+    inp = decode_inputs(rng, 4, 2, 4, 3)
+    i_nan, i_inf = dict(inp), dict(inp)
+    for key in ("cached_g", "new_g"):
+        m = rng.random(inp[key].shape) < 0.3
+        i_nan[key] = np.where(m, np.nan, inp[key])
+        i_inf[key] = np.where(m, np.inf, inp[key])
+    for a, b in zip(oracle.decode_verify(**i_nan), oracle.decode_verify(**i_inf)):
+        np.testing.assert_array_equal(a, b)
