@@ -563,6 +563,40 @@ def main(argv=None):
         del d, st, tl, ov, dl
         torch.cuda.empty_cache()
 
+        # latency of one small call, the shape the pages measure their verify
+        # kernel on (one sequence, 96 / 8 = 12 heads per tensor-parallel rank,
+        # 4 verify positions), replayed from a CUDA graph of 20 calls
+        sw = synth.DecodeWorkload("verify-replay latency R=1 H=12 d=128 W=4, 4 positions (bonus + 3 drafts)",
+                                  1, 12, 128, 128, Wd=3, seed=6)
+        d = synth.make_decode(sw, device="cuda")
+        st, tl = d["state"].clone(), d["tail"].clone()
+        ov = torch.empty((sw.R, sw.Wd + 1, sw.H, sw.dv), dtype=torch.bfloat16, device="cuda")
+
+        def small_step():
+            kda.decode_verify_replay(st, tl, d["conv_w"], d["cached_qkv"], d["cached_g"], d["cached_b"],
+                                     d["accepted"], d["new_qkv"], d["new_g"], d["new_b"], d["out_w"], out=ov)
+
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            small_step()
+            gs.synchronize()
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(20):
+                    small_step()
+        torch.cuda.synchronize()
+        for _ in range(Wm):
+            graph.replay()
+        lus = reduce_max(cuda_time(graph.replay, K, stream), ws) * 1e3 / 20
+        out["verify_latency"] = {"workload": sw.name, "us_per_call": lus, "calls_per_graph": 20,
+                                 "pages_number": {"us_per_layer": 5.61, "hardware": "AMD MI355X",
+                                                  "note": "the pages' optimised verify kernel, other hardware: "
+                                                          "context, not a target"}}
+        launches += 20 * K
+        del d, st, tl, ov, graph
+        torch.cuda.empty_cache()
+
     # ------------------------------------------------------------ single-token decode (window 0)
     if "decode" in only:
         dw = decode_workload(synth)
