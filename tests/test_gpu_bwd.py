@@ -385,3 +385,27 @@ def test_context_parallel_backward_edges(kda, oracle, scale, floor):
         assert e <= TC_TOL, f"{name}: error {e:.3e}"
     g = x["g"].cpu()
     assert torch.all(got[3].cpu()[g < -5.0] == 0.0)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_context_parallel_backward_random_cuts(kda, oracle, seed):
+    """Random sequence counts and lengths (empty and sub-chunk ones
+    included) and random segment lengths (multiples of 64 from one chunk to
+    sixteen) against the oracle; the training pair on the same cut gives the
+    same bits."""
+    rng = np.random.default_rng(200 + seed)
+    n = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.integers(0, 1500, size=n)]
+    lens[int(rng.integers(0, n))] = int(rng.integers(1, 64)) if n > 1 else lens[0]
+    seg = 64 * int(rng.integers(1, 17))
+    x = _case(lens, 2, 128, torch.bfloat16, seed=300 + seed)
+    if sum(lens) == 0:
+        pytest.skip("no tokens drawn")
+    got = _compare(kda, oracle, x, scale=0.75, tol=TC_TOL, segment_len=seg)
+    cp = dict(cp_mode=kda.CP_ON, segment_len=seg)
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"])
+    _, _, saved = kda.chunk_fwd_train(*args, initial_state=x["S0"], scale=0.75, **cp)
+    pair = kda.chunk_bwd_saved(*args, x["do"], saved, dS_final=x["dSf"], scale=0.75, **cp)
+    torch.cuda.synchronize()
+    for a, b in zip(pair, got):
+        assert torch.equal(a, b)
