@@ -409,3 +409,14 @@ def test_context_parallel_backward_random_cuts(kda, oracle, seed):
     torch.cuda.synchronize()
     for a, b in zip(pair, got):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_backward_beta_zero(kda, oracle, d, dtype):
+    """beta = 0 (the state only decays): dv is exactly zero, the rest against
+    the oracle, dbeta included (its gradient does not vanish)."""
+    x = _case([400, 130], 2, d, dtype, seed=131 + d)
+    x["beta"] = torch.zeros_like(x["beta"])
+    got = _compare(kda, oracle, x, scale=0.8, tol=_tol(d, dtype))
+    assert torch.count_nonzero(got[2]) == 0
+    assert torch.count_nonzero(got[4]) > 0

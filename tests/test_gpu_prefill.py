@@ -107,6 +107,26 @@ def test_no_decay_no_floor_activity(kda, oracle):
     run_and_compare(kda, oracle, inp)
 
 
+@pytest.mark.parametrize("cp", [0, 1])
+def test_beta_zero_is_pure_decay(kda, oracle, cp):
+    """beta = 0 writes nothing: the state only decays, S_T = Diag(Gam_T) S0
+    per channel, and o_t = scale (Diag(Gam_t) S0)^T q_t; checked against that
+    closed form (fp64) as well as the oracle, cp off and over segments."""
+    inp = make_inputs([700, 300], 2, 128, 128, s0=True, seed=14)
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    o, Sf, _, _ = run_and_compare(kda, oracle, inp, scale=0.9, cp_mode=cp, segment_len=256 if cp else 0)
+    g = np.maximum(to64(inp["g"]), -5.0)
+    q, S0 = to64(inp["q"]), to64(inp["S0"])
+    cu = inp["cu_seqlens"].cpu().numpy()
+    for n in range(2):
+        a, b = cu[n], cu[n + 1]
+        gam = np.exp(np.cumsum(g[a:b], axis=0))  # [t][h][i]
+        o_cf = 0.9 * np.einsum("thi,thi,hij->thj", q[a:b], gam, S0[n])
+        S_cf = gam[-1][:, :, None] * S0[n]
+        assert normwise_err(to64(o)[a:b], o_cf, head_axis=1) <= OUT_TOL
+        assert normwise_err(to64(Sf)[n], S_cf, head_axis=0) <= STATE_TOL
+
+
 def test_dependency_inverse_example_through_kernel(kda, oracle):
     """Three tokens whose intra-chunk corrections are those of the worked
     example (A21 = A32 = 1/4, A31 = 1/8 with b = 1/2, g = 0): the chunk kernel
