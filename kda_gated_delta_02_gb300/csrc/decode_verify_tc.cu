@@ -47,9 +47,9 @@ constexpr int D = 128, VT = 16, NT = 256, HT = 8, NR = HT + 3;
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_S0 = 0;       // state bf16 [dk][dv]: two 64-wide swizzled halves [128][128 B]
-constexpr uint32_t OFF_X = 32768;    // QX hi, QX lo, KX hi, KX lo: K-major 64 rows x dk
-constexpr uint32_t OFF_KR = 49152;   // KR hi, KR lo: K-major 32 rows x dk; also the rows 64..127 that
-                                     // the M = 128 product over X reads past X (discarded)
+constexpr uint32_t OFF_X = 32768;    // [QX hi | QX lo | KX hi | KX lo]: MN-major, row = key channel, 64 columns
+constexpr uint32_t OFF_KR = 49152;   // KR hi, KR lo: K-major 32 rows x dk; from here on 16 KB are also
+                                     // the rows 64..127 that the M = 128 product over X reads (discarded)
 constexpr uint32_t OFF_RAW = OFF_X;  // before the operands: pre-conv rows [<= 18][q|k|v][128] bf16
 constexpr uint32_t OFF_GR = OFF_X + 18 * 768;  //   and g rows [<= 15][128] bf16, up to 50432
 constexpr uint32_t OFF_PF = OFF_X;           // after batch 1: P = V - KX S0, fp32 [16][128]
@@ -335,26 +335,49 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     // ---------------------------------------------------------------- operands
     float kt[HT];
     {
-        const uint32_t xcol = sb + OFF_X + (uint32_t)(c >> 6) * 8192u + ((uint32_t)(c & 7) << 1);
+        // X, MN-major: row c (key channel) holds the 64 columns QX hi (token t
+        // at column t), QX lo (16 + t), KX hi (32 + t) and KX lo (48 + t), so
+        // this thread's 8 tokens of each part are one 16-byte chunk of its row
+        // (chunk 2 part + hf, swizzled by c & 7); KR stays K-major (row = token)
+        const uint32_t xrow = sb + OFF_X + (uint32_t)c * 128u, cs = (uint32_t)(c & 7);
         const uint32_t rcol = sb + OFF_KR + (uint32_t)(c >> 6) * 4096u + ((uint32_t)(c & 7) << 1);
         const int ch = (c & 63) >> 3;
+        const uint32_t h2 = (uint32_t)hf;
+        {  // QX hi and lo
+            uint32_t xh[4], xl[4];
 #pragma unroll
-        for (int j = 0; j < HT; ++j) {
-            const int t = t0 + j;
-            const float qh = yq[j] * sRN[t], kh = yk[j] * sRN[VT + t];
-            const float rx = __frcp_rn(xd[j]);
-            const uint32_t sw = (uint32_t)((ch ^ (j & 7)) << 4);  // row t = t0 + j has t & 7 == j
-            uint16_t hi, lo;
-            split2(qh * xd[j], hi, lo);
-            sts16(xcol + (uint32_t)t * 128u + sw, hi);
-            sts16(xcol + (uint32_t)(16 + t) * 128u + sw, lo);
-            split2(kh * xd[j], hi, lo);
-            sts16(xcol + (uint32_t)(32 + t) * 128u + sw, hi);
-            sts16(xcol + (uint32_t)(48 + t) * 128u + sw, lo);
-            split2(kh * rx, hi, lo);
-            sts16(rcol + (uint32_t)t * 128u + sw, hi);
-            sts16(rcol + (uint32_t)(16 + t) * 128u + sw, lo);
-            kt[j] = (t <= a) ? kh * (xa * rx) : 0.f;
+            for (int j = 0; j < HT; ++j) {
+                uint16_t hi, lo;
+                split2(yq[j] * sRN[t0 + j] * xd[j], hi, lo);
+                const uint32_t sh = (j & 1) ? 16u : 0u;
+                xh[j >> 1] = (j & 1) ? (xh[j >> 1] | ((uint32_t)hi << sh)) : (uint32_t)hi;
+                xl[j >> 1] = (j & 1) ? (xl[j >> 1] | ((uint32_t)lo << sh)) : (uint32_t)lo;
+            }
+            sts128(xrow + (((0u + h2) ^ cs) << 4), xh[0], xh[1], xh[2], xh[3]);
+            sts128(xrow + (((2u + h2) ^ cs) << 4), xl[0], xl[1], xl[2], xl[3]);
+        }
+        {  // KX hi and lo; KR by token rows
+            uint32_t xh[4], xl[4];
+#pragma unroll
+            for (int j = 0; j < HT; ++j) {
+                const int t = t0 + j;
+                const float kh = yk[j] * sRN[VT + t];
+                // 1 / x_t: x_t lies in [e^{16 g_min}, 1], normal in fp32, where
+                // the fast quotient is within 2 ulp (the hi/lo split keeps 16 bits)
+                const float rx = __fdividef(1.f, xd[j]);
+                const uint32_t sw = (uint32_t)((ch ^ (j & 7)) << 4);  // row t = t0 + j has t & 7 == j
+                uint16_t hi, lo;
+                split2(kh * xd[j], hi, lo);
+                const uint32_t sh = (j & 1) ? 16u : 0u;
+                xh[j >> 1] = (j & 1) ? (xh[j >> 1] | ((uint32_t)hi << sh)) : (uint32_t)hi;
+                xl[j >> 1] = (j & 1) ? (xl[j >> 1] | ((uint32_t)lo << sh)) : (uint32_t)lo;
+                split2(kh * rx, hi, lo);
+                sts16(rcol + (uint32_t)t * 128u + sw, hi);
+                sts16(rcol + (uint32_t)(16 + t) * 128u + sw, lo);
+                kt[j] = (t <= a) ? kh * (xa * rx) : 0.f;
+            }
+            sts128(xrow + (((4u + h2) ^ cs) << 4), xh[0], xh[1], xh[2], xh[3]);
+            sts128(xrow + (((6u + h2) ^ cs) << 4), xl[0], xl[1], xl[2], xl[3]);
         }
     }
     umma::fence_proxy_async();
@@ -369,23 +392,21 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         ok = umma::mbar_wait(bar0, 0, WAIT_LIMIT) && ok;
         if (ok) {
             umma::fence_after();
-            constexpr uint32_t idqk = umma::idesc_bf16(128, 64, 1, 0, 0);
+            constexpr uint32_t idqk = umma::idesc_bf16(128, 64, 1, 1, 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t kin = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
                 umma::mma(tmem + TM_Q, umma::sdesc4(sb4 + ((OFF_S0 + kk * 2048) >> 4), 16384, 1024),
-                          umma::sdesc4(sb4 + ((OFF_X + kin) >> 4), 16, 1024), idqk, kk > 0 ? 1u : 0u);
+                          umma::sdesc4(sb4 + ((OFF_X + kk * 2048) >> 4), 1024, 1024), idqk, kk > 0 ? 1u : 0u);
             }
             umma::commit(bar0 + 8);
         }
     } else if (tid == 32 && ok) {
         umma::fence_after();
-        constexpr uint32_t idab = umma::idesc_bf16(128, 32, 0, 0, 0);
+        constexpr uint32_t idab = umma::idesc_bf16(128, 32, 1, 0, 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t kin = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
             const uint32_t rin = (uint32_t)(kk >> 2) * 4096u + (uint32_t)(kk & 3) * 32u;
-            umma::mma(tmem + TM_AB, umma::sdesc4(sb4 + ((OFF_X + kin) >> 4), 16, 1024),
+            umma::mma(tmem + TM_AB, umma::sdesc4(sb4 + ((OFF_X + kk * 2048) >> 4), 16384, 1024),
                       umma::sdesc4(sb4 + ((OFF_KR + rin) >> 4), 16, 1024), idab, kk > 0 ? 1u : 0u);
         }
         umma::commit(bar0 + 8);
