@@ -92,21 +92,17 @@ struct VtcParams {
 };
 
 __device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
-__device__ __forceinline__ void split2(float x, uint16_t &hi, uint16_t &lo) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+// hi / lo parts of two values, each pair packed as bf16x2 (a in the low
+// half): the roundings of two scalar splits, by packed conversions
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16(a, b);
+    const float2 h = unpack_bf16(hi);
+    lo = pack_bf16(a - h.x, b - h.y);
 }
 // hi / lo parts of 8 consecutive values packed as 4 x bf16x2 each
 __device__ __forceinline__ void split8(const float *x, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint16_t h0, l0, h1, l1;
-        split2(x[2 * i], h0, l0);
-        split2(x[2 * i + 1], h1, l1);
-        hi[i] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        lo[i] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-    }
+    for (int i = 0; i < 4; ++i) split_pair(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
 }
 // One row of a K-major 128-byte swizzled tile: 16-byte chunk j (elements
 // 8j .. 8j+7 of the row's first 64) sits at chunk j ^ (row & 7).
@@ -346,35 +342,32 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         {  // QX hi and lo
             uint32_t xh[4], xl[4];
 #pragma unroll
-            for (int j = 0; j < HT; ++j) {
-                uint16_t hi, lo;
-                split2(yq[j] * sRN[t0 + j] * xd[j], hi, lo);
-                const uint32_t sh = (j & 1) ? 16u : 0u;
-                xh[j >> 1] = (j & 1) ? (xh[j >> 1] | ((uint32_t)hi << sh)) : (uint32_t)hi;
-                xl[j >> 1] = (j & 1) ? (xl[j >> 1] | ((uint32_t)lo << sh)) : (uint32_t)lo;
-            }
+            for (int j = 0; j < HT; j += 2)
+                split_pair(yq[j] * sRN[t0 + j] * xd[j], yq[j + 1] * sRN[t0 + j + 1] * xd[j + 1], xh[j >> 1],
+                           xl[j >> 1]);
             sts128(xrow + (((0u + h2) ^ cs) << 4), xh[0], xh[1], xh[2], xh[3]);
             sts128(xrow + (((2u + h2) ^ cs) << 4), xl[0], xl[1], xl[2], xl[3]);
         }
         {  // KX hi and lo; KR by token rows
             uint32_t xh[4], xl[4];
 #pragma unroll
-            for (int j = 0; j < HT; ++j) {
+            for (int j = 0; j < HT; j += 2) {
                 const int t = t0 + j;
-                const float kh = yk[j] * sRN[VT + t];
+                const float kh0 = yk[j] * sRN[VT + t], kh1 = yk[j + 1] * sRN[VT + t + 1];
                 // 1 / x_t: x_t lies in [e^{16 g_min}, 1], normal in fp32, where
                 // the fast quotient is within 2 ulp (the hi/lo split keeps 16 bits)
-                const float rx = __fdividef(1.f, xd[j]);
-                const uint32_t sw = (uint32_t)((ch ^ (j & 7)) << 4);  // row t = t0 + j has t & 7 == j
-                uint16_t hi, lo;
-                split2(kh * xd[j], hi, lo);
-                const uint32_t sh = (j & 1) ? 16u : 0u;
-                xh[j >> 1] = (j & 1) ? (xh[j >> 1] | ((uint32_t)hi << sh)) : (uint32_t)hi;
-                xl[j >> 1] = (j & 1) ? (xl[j >> 1] | ((uint32_t)lo << sh)) : (uint32_t)lo;
-                split2(kh * rx, hi, lo);
-                sts16(rcol + (uint32_t)t * 128u + sw, hi);
-                sts16(rcol + (uint32_t)(16 + t) * 128u + sw, lo);
-                kt[j] = (t <= a) ? kh * (xa * rx) : 0.f;
+                const float rx0 = __fdividef(1.f, xd[j]), rx1 = __fdividef(1.f, xd[j + 1]);
+                // rows t and t + 1 have (row & 7) == j and j + 1
+                const uint32_t sw0 = (uint32_t)((ch ^ (j & 7)) << 4), sw1 = (uint32_t)((ch ^ ((j + 1) & 7)) << 4);
+                split_pair(kh0 * xd[j], kh1 * xd[j + 1], xh[j >> 1], xl[j >> 1]);
+                uint32_t rh, rl;
+                split_pair(kh0 * rx0, kh1 * rx1, rh, rl);
+                sts16(rcol + (uint32_t)t * 128u + sw0, (uint16_t)rh);
+                sts16(rcol + (uint32_t)(16 + t) * 128u + sw0, (uint16_t)rl);
+                sts16(rcol + (uint32_t)(t + 1) * 128u + sw1, (uint16_t)(rh >> 16));
+                sts16(rcol + (uint32_t)(17 + t) * 128u + sw1, (uint16_t)(rl >> 16));
+                kt[j] = (t <= a) ? kh0 * (xa * rx0) : 0.f;
+                kt[j + 1] = (t + 1 <= a) ? kh1 * (xa * rx1) : 0.f;
             }
             sts128(xrow + (((4u + h2) ^ cs) << 4), xh[0], xh[1], xh[2], xh[3]);
             sts128(xrow + (((6u + h2) ^ cs) << 4), xl[0], xl[1], xl[2], xl[3]);
