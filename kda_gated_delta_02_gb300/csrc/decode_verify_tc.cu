@@ -253,27 +253,32 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     const bool silu = p.conv_act == KDA_CONV_SILU;
     float yq[HT], yk[HT], yv[HT];
 #pragma unroll
-    for (int j = 0; j < HT; ++j) {
-        // q and k taps as packed f32x2 fused multiply-adds (each lane rounds like fmaf)
-        float2 sqk = make_float2(0.f, 0.f);
-        float sv = 0.f;
+    for (int j = 0; j < HT; j += 2) {
+        // the taps as packed f32x2 fused multiply-adds (each lane rounds like
+        // fmaf): q and k of one token, v of two
+        float2 sqk0 = make_float2(0.f, 0.f), sqk1 = sqk0, sv2 = sqk0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (i < W) {
-                sqk = __ffma2_rn(make_float2(wq[i], wk[i]), make_float2(bf2f(rq[j + i]), bf2f(rk[j + i])), sqk);
-                sv = fmaf(wv[i], bf2f(rv[j + i]), sv);
+                sqk0 = __ffma2_rn(make_float2(wq[i], wk[i]), make_float2(bf2f(rq[j + i]), bf2f(rk[j + i])), sqk0);
+                sqk1 = __ffma2_rn(make_float2(wq[i], wk[i]), make_float2(bf2f(rq[j + 1 + i]), bf2f(rk[j + 1 + i])),
+                                  sqk1);
+                sv2 = __ffma2_rn(make_float2(wv[i], wv[i]), make_float2(bf2f(rv[j + i]), bf2f(rv[j + 1 + i])), sv2);
             }
         }
-        float sq = sqk.x, sk = sqk.y;
-        if (silu) {  // y / (1 + e^{-y}); the fast quotient is 0 where e^{-y} overflows, the limit
-            sq = __fdividef(sq, 1.f + __expf(-sq));
-            sk = __fdividef(sk, 1.f + __expf(-sk));
-            sv = __fdividef(sv, 1.f + __expf(-sv));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            float sq = u ? sqk1.x : sqk0.x, sk = u ? sqk1.y : sqk0.y, sv = u ? sv2.y : sv2.x;
+            if (silu) {  // y / (1 + e^{-y}); the fast quotient is 0 where e^{-y} overflows, the limit
+                sq = __fdividef(sq, 1.f + __expf(-sq));
+                sk = __fdividef(sk, 1.f + __expf(-sk));
+                sv = __fdividef(sv, 1.f + __expf(-sv));
+            }
+            const bool live = t0 + j + u < ntok;
+            yq[j + u] = live ? sq : 0.f;
+            yk[j + u] = live ? sk : 0.f;
+            yv[j + u] = live ? sv : 0.f;
         }
-        const bool live = t0 + j < ntok;
-        yq[j] = live ? sq : 0.f;
-        yk[j] = live ? sk : 0.f;
-        yv[j] = live ? sv : 0.f;
     }
     // decay x_t = prod_{r<=t} e^{max(-softplus(g_r), g_min)}; e^{-softplus(g)}
     // is 1 / (1 + e^g), and the floor commutes with the exponential.  The
@@ -418,12 +423,21 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
         umma::ld8(tq + TM_Q + t0, v0);
         umma::ld8(tq + TM_Q + 16 + t0, v1);
 #pragma unroll
-        for (int j = 0; j < HT; ++j) qs[j] = v0[j] + v1[j];
+        for (int j = 0; j < HT; j += 2) {
+            const float2 q2 = __fadd2_rn(make_float2(v0[j], v0[j + 1]), make_float2(v1[j], v1[j + 1]));
+            qs[j] = q2.x;
+            qs[j + 1] = q2.y;
+        }
         // P = V - KX S0 for value column c, tokens t0 .. t0 + 7 (fp32, for the solve)
         umma::ld8(tq + TM_K + t0, v0);
         umma::ld8(tq + TM_K + 16 + t0, v1);
 #pragma unroll
-        for (int j = 0; j < HT; ++j) sPf[(t0 + j) * D + c] = yv[j] - (v0[j] + v1[j]);
+        for (int j = 0; j < HT; j += 2) {
+            const float2 k2 = __fadd2_rn(make_float2(v0[j], v0[j + 1]), make_float2(v1[j], v1[j + 1]));
+            const float2 p2 = __fadd2_rn(make_float2(yv[j], yv[j + 1]), make_float2(-k2.x, -k2.y));
+            sPf[(t0 + j) * D + c] = p2.x;
+            sPf[(t0 + j + 1) * D + c] = p2.y;
+        }
         // K~^T operand (k = s: hi 0-15, lo 16-31), this half's tokens
         store_split8(sb + OFF_P + (uint32_t)c * 128u, c, hf, kt);
     }
@@ -505,19 +519,24 @@ __global__ void __launch_bounds__(NT, 3) kda_verify_tc_kernel(const __grid_const
     // outputs while the state product runs: O = scale (QX S0 + B U) in fp32
     float o[HT];
     if (ok) {
+        // two tokens at a time as packed f32x2 fused multiply-adds (each lane
+        // rounds like fmaf, in the same order of s)
 #pragma unroll
-        for (int j = 0; j < HT; ++j) {
-            const float *brow = sBf + (t0 + j) * 16;
-            float acc = qs[j];
+        for (int j = 0; j < HT; j += 2) {
+            const float *b0 = sBf + (t0 + j) * 16, *b1 = b0 + 16;
+            float2 acc = make_float2(qs[j], qs[j + 1]);
 #pragma unroll
             for (int s = 0; s < VT; s += 4) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(brow + s);
-                acc = fmaf(b4.x, uu[s], acc);
-                acc = fmaf(b4.y, uu[s + 1], acc);
-                acc = fmaf(b4.z, uu[s + 2], acc);
-                acc = fmaf(b4.w, uu[s + 3], acc);
+                const float4 x4 = *reinterpret_cast<const float4 *>(b0 + s);
+                const float4 y4 = *reinterpret_cast<const float4 *>(b1 + s);
+                acc = __ffma2_rn(make_float2(x4.x, y4.x), make_float2(uu[s], uu[s]), acc);
+                acc = __ffma2_rn(make_float2(x4.y, y4.y), make_float2(uu[s + 1], uu[s + 1]), acc);
+                acc = __ffma2_rn(make_float2(x4.z, y4.z), make_float2(uu[s + 2], uu[s + 2]), acc);
+                acc = __ffma2_rn(make_float2(x4.w, y4.w), make_float2(uu[s + 3], uu[s + 3]), acc);
             }
-            o[j] = p.scale * acc;
+            const float2 os = __fmul2_rn(make_float2(p.scale, p.scale), acc);
+            o[j] = os.x;
+            o[j + 1] = os.y;
         }
         float s2[HT];
 #pragma unroll
