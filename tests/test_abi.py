@@ -188,3 +188,29 @@ def test_backward_workspace_arithmetic(lib):
     d = 128
     assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 64) == 0
     assert lib.kda_chunk_bwd_workspace_size(0, T, H, d, d) == 0
+
+
+@pytest.mark.parametrize("N,T,H,cp,seg", [(1, 1 << 20, 12, -1, 0), (1, 1 << 20, 12, 1, 32768), (3, 5000, 2, 1, 1024),
+                                          (1, 32768, 96, -1, 0), (2, 3000, 4, 0, 0), (1, 70000, 2, 1, 0)])
+def test_cp_backward_workspace_arithmetic(lib, N, T, H, cp, seg):
+    """The context-parallel backward's workspace: the CP prefill's scratch,
+    the tensor-core backward's layout over the P_max = floor(T / segment) + N
+    segment slots, then r and the segment-end gradients (P_max x H x 128 x 128
+    f32 each), every part 256-byte aligned; the sequence form's size when the
+    call is not cut (cp off, or automatic and declined), and never less."""
+    lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_bwd_cp_workspace_size.restype = ctypes.c_size_t
+    base = lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 128)
+    got = lib.kda_chunk_bwd_cp_workspace_size(N, T, H, 128, 128, cp, seg)
+    plan = lib.kda_chunk_fwd_plan(N, T, H, 128, 128, cp, seg)
+    if cp == 0 or plan == 0:
+        assert got == base
+        return
+    assert plan % 64 == 0 and (seg == 0 or plan == seg)
+    pm = T // plan + N
+    cp_total = lib.kda_chunk_fwd_workspace_size(N, T, H, 128, 128, cp, seg)
+    per_seg = _align256(pm * H * 128 * 128 * 4)
+    want = _align256(cp_total) + _align256(_bwd_tc_bytes(pm, T, H)) + 2 * per_seg
+    assert got == max(base, want)
+    assert lib.kda_chunk_bwd_cp_workspace_size(N, T, H, 128, 128, 5, seg) == 0
