@@ -6,11 +6,15 @@ kda_chunk_fwd call per step (its two-kernel form: chunk slot list, chunk-local
 kernel, state walk).  Extra keys measured in the same run:
   "verify": fused verify-replay on 256 requests x 96 heads (state GB/s, % HBM)
   "verify_ragged": the same with 3..7 drafts per request (ragged entry point)
+  "verify_latency": one call at 1 request x 12 heads, 4 positions, from a
+            CUDA graph of 20 calls
   "backward": the backward of the headline prefill (dq, dk, dv, dg, dbeta)
+            and its training pair (forward keeping its operands, reverse pass)
   "ckpt":   the headline prefill also emitting the state every 4096 tokens
   "decode": the same entry point as single-token decode (window 0) on 256 x 96
   "varlen": 16 packed sequences (1K-8K tokens) continuing from stored states
-  "cp":     1M-token, 12-head prefill with the context-parallel schedule
+  "cp":     1M-token, 12-head prefill with the context-parallel schedule,
+            its backward over the same segments and that training pair
   "roofline" (the step's dominant kernel), "path_roofline", "kernels",
   "cpu_baseline", "e2e" (host buffers through kda_chunk_fwd_host), "clocks",
   "gpu_launches".
