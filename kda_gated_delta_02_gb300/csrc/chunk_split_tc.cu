@@ -24,6 +24,11 @@
 // floor(T / 64) + units.  The blob area holds a window of slots (a "piece");
 // a unit that crosses a piece boundary hands its state to the next piece
 // through a carry buffer (at most one unit crosses each boundary).
+//
+// The backward (chunk_bwd_tc.cu) runs these kernels as its forward pass:
+// kda_chunk_prep_aux_kernel also keeps every (chunk, head)'s fp32 T and M^T,
+// and the walk can save its bf16 S^T and U^T operand tiles of every chunk by
+// bulk copies (with or without the outputs).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
