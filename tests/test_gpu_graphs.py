@@ -1,6 +1,7 @@
-"""The device calls are capturable in CUDA graphs (serving loops replay a
-captured step instead of launching it): a captured verify, single-token
-decode and two-kernel prefill replay to the eager results bit for bit."""
+"""The device calls are capturable in CUDA graphs (serving loops and training
+steps replay a captured step instead of launching it): a captured verify,
+single-token decode, two-kernel prefill and backward (sequence form and over
+context-parallel segments) replay to the eager results bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -110,3 +111,47 @@ def test_ragged_verify_in_a_graph(kda):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(st_g, st_e) and torch.equal(tl_g, tl_e) and torch.equal(o_g, o_e)
+
+
+@pytest.mark.parametrize("cp", [0, 1])
+def test_backward_in_a_graph(kda, cp):
+    """The tensor-core backward (its pipelined pieces: programmatic dependent
+    launches) and the context-parallel backward replay from a CUDA graph to
+    the eager gradients bit for bit; the outputs are allocated inside the
+    capture, from the graph's pool."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(7 + cp)
+    lens = [3000, 1500, 0, 2000] if not cp else [2500, 700]
+    T, H, D = sum(lens), 2, 128
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    q = torch.nn.functional.normalize(torch.randn(T, H, D, generator=gen), dim=-1).bfloat16().cuda()
+    k = torch.nn.functional.normalize(torch.randn(T, H, D, generator=gen), dim=-1).bfloat16().cuda()
+    v = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    g = torch.clamp_min(-torch.nn.functional.softplus(torch.randn(T, H, D, generator=gen)), -5.0).cuda()
+    beta = torch.sigmoid(torch.randn(T, H, generator=gen)).cuda()
+    S0 = (0.02 * torch.randn(len(lens), H, D, D, generator=gen)).cuda()
+    do = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    lib = kda.load_library()
+    need = (lib.kda_chunk_bwd_workspace_size(len(lens), T, H, D, D) if not cp else
+            lib.kda_chunk_bwd_cp_workspace_size(len(lens), T, H, D, D, kda.CP_ON, 1024))
+    ws = torch.empty(int(need), dtype=torch.uint8, device="cuda")
+
+    def call():
+        if cp:
+            return kda.chunk_bwd_cp(q, k, v, g, beta, cu, do, initial_state=S0, scale=0.8, cp_mode=kda.CP_ON,
+                                    segment_len=1024, workspace=ws)
+        return kda.chunk_bwd(q, k, v, g, beta, cu, do, initial_state=S0, scale=0.8, workspace=ws)
+
+    eager = [x.clone() for x in call()]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up outside the capture (attributes, maps)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = call()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(out, eager):
+        assert torch.equal(a, b)
