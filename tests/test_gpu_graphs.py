@@ -155,3 +155,40 @@ def test_backward_in_a_graph(kda, cp):
     torch.cuda.synchronize()
     for a, b in zip(out, eager):
         assert torch.equal(a, b)
+
+
+def test_training_pair_in_a_graph(kda):
+    """A captured training step (the forward keeping its operands, then the
+    reverse pass from them) replays to the eager outputs and gradients bit
+    for bit."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(11)
+    lens = [1500, 700]
+    T, H, D = sum(lens), 2, 128
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    q = torch.nn.functional.normalize(torch.randn(T, H, D, generator=gen), dim=-1).bfloat16().cuda()
+    k = torch.nn.functional.normalize(torch.randn(T, H, D, generator=gen), dim=-1).bfloat16().cuda()
+    v = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    g = torch.clamp_min(-torch.nn.functional.softplus(torch.randn(T, H, D, generator=gen)), -5.0).cuda()
+    beta = torch.sigmoid(torch.randn(T, H, generator=gen)).cuda()
+    do = torch.randn(T, H, D, generator=gen).bfloat16().cuda()
+    saved = torch.empty(int(kda.load_library().kda_chunk_bwd_workspace_size(2, T, H, D, D)), dtype=torch.uint8,
+                        device="cuda")
+
+    def step():
+        o, Sf, _ = kda.chunk_fwd_train(q, k, v, g, beta, cu, scale=0.6, saved=saved)
+        return (o, Sf) + tuple(kda.chunk_bwd_saved(q, k, v, g, beta, cu, do, saved, scale=0.6))
+
+    eager = [None if x is None else x.clone() for x in step()]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = step()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(out, eager):
+        assert (a is None and b is None) or torch.equal(a, b)
